@@ -1,0 +1,257 @@
+/*
+ * dspark.h - C ABI of the DSpark draft-sampling / exact-verification library
+ * for NVIDIA GB300 (sm_103a).
+ *
+ * Three operations, each a pass over vocabulary-wide logit rows:
+ *
+ *   dspark_markov_sample  the semi-autoregressive draft's sequential head:
+ *                         low-rank Markov logit bias, sampling policy, a
+ *                         proposal per position left to right, the full
+ *                         proposal distribution q and a confidence per
+ *                         position.
+ *   dspark_verify         exact verification of a proposal block against the
+ *                         target's logits: greedy contiguous-prefix argmax
+ *                         acceptance, or accept-with-min(1, p/q), residual
+ *                         resampling and a bonus token.
+ *   dspark_accept_stats   the analytical training-side statistics: L1
+ *                         distance, acceptance rate, tau and the weighted
+ *                         CE / L1 / confidence-BCE numerators.
+ *
+ * Sources, by page title and section:
+ *   [FT] FreeToken PR #69 "[2/3] feat(dsv4): implement exact DSpark
+ *        speculative decoding": "End-to-end speculative cycle",
+ *        "Checkpoint-faithful DSpark architecture", "Exact decoding
+ *        semantics" (Greedy; Probabilistic).
+ *   [MB] NeMo Megatron-Bridge "DSpark Speculative Decoding (Draft Training)
+ *        Design": "Semi-autoregressive draft", "Training objective",
+ *        "Acceptance and confidence", "Loss return contract", "Memory
+ *        contract for the full-vocabulary terms".
+ *   [PT] pypto "DeepSeek V4 DSpark NPU Serving Dev Notes": "Speculative
+ *        decoding (K=7)" (decode tile, Acceptance).
+ *
+ * Conventions shared by every entry point
+ *   Memory     Every array argument is DEVICE memory owned by the caller.  The
+ *              library allocates nothing and keeps no state between calls;
+ *              scratch lives in the caller's workspace.
+ *   Stream     `stream` is a cudaStream_t (NULL = the legacy default stream).
+ *              Work is enqueued asynchronously; nothing synchronises the host.
+ *   Layout     Row-major.  Logit rows are contiguous, V elements each.
+ *   dtype      DSPARK_BF16 (bfloat16 bit patterns) or DSPARK_F32.
+ *   Sizes      1 <= gamma <= DSPARK_MAX_GAMMA; V a multiple of 8 with
+ *              8 <= V <= DSPARK_MAX_VOCAB; B (or N) >= 0, and 0 is a no-op.
+ *   Alignment  Logit, q and hidden-state arrays start on a 16-byte boundary.
+ *   Returns    DSPARK_OK, or a negative dspark_status for an argument error
+ *              found on the host before anything is enqueued (nothing is
+ *              launched then), or DSPARK_ECUDA if a launch failed.
+ *   Status     Problems that depend on data are reported per request in
+ *              `status` (dspark_request_status), never by a trap.
+ *   Workspace  dspark_workspace_size() gives the bytes an operation needs.
+ *              The workspace must be zero-filled once after allocation
+ *              (e.g. cudaMemsetAsync(ws, 0, bytes, stream)); every call that
+ *              completes leaves it zero-filled again, so it can be reused by
+ *              the next call on the same stream without clearing.  Calls that
+ *              share one workspace must not overlap in time.
+ *   Random     Each random decision draws u in [0,1) from Philox-4x32-10
+ *              (Salmon et al., SC'11) with key (lo32 seed, hi32 seed) and
+ *              counter (draw, lo32 pos, hi32 pos, lo32 request_id):
+ *              u = (first output word >> 8) * 2^-24.  pos is the absolute
+ *              position of the token being decided; draw 0 = proposal,
+ *              1 = accept test, 2 = residual / bonus.  Only the low 32 bits
+ *              of request_id enter the counter.
+ */
+#ifndef DSPARK_H
+#define DSPARK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DSPARK_MAX_GAMMA 16
+#define DSPARK_MAX_VOCAB (1 << 20)
+#define DSPARK_MAX_RANK 256
+#define DSPARK_MAX_BATCH 256  /* requests per dspark_markov_sample call */
+
+/* Sampling policy of one request [FT Exact decoding semantics > Probabilistic:
+ * p and q are formed after the request's temperature, top-p and top-k].
+ *   greedy != 0   one-hot at the argmax (lowest index on ties); the other
+ *                 fields are ignored.
+ *   temperature   > 0; logits are scaled by the fp32 value of 1/temperature.
+ *   top_k         0 or >= V disables; otherwise exactly top_k tokens are kept,
+ *                 taken in (logit descending, index ascending) order.
+ *   top_p         >= 1 disables; otherwise the shortest prefix of that order,
+ *                 inside the top-k set, whose share of the kept mass is
+ *                 >= top_p (at least one token).
+ * Temperature is applied first, then top-k, then top-p on the renormalised
+ * top-k distribution. */
+typedef struct {
+    float temperature;
+    int32_t top_k;
+    float top_p;
+    int32_t greedy;
+} dspark_policy;
+
+typedef enum {
+    DSPARK_OK = 0,
+    DSPARK_EINVAL = -1,   /* a size, pointer, alignment or enum is invalid   */
+    DSPARK_ENOSPC = -2,   /* workspace smaller than dspark_workspace_size() */
+    DSPARK_ECUDA = -3,    /* a CUDA launch or attribute call failed          */
+    DSPARK_ENOTSUP = -4   /* valid but unsupported on this device / build    */
+} dspark_status;
+
+enum { DSPARK_BF16 = 0, DSPARK_F32 = 1 };
+
+/* Values written to the per-request `status` arrays. */
+typedef enum {
+    DSPARK_REQ_OK = 0,
+    DSPARK_REQ_NONFINITE = 1,  /* a NaN or +inf logit in a row the request uses */
+    DSPARK_REQ_EMPTY = 2,      /* a row whose logits are all -inf               */
+    DSPARK_REQ_TIMEOUT = 3,    /* a bounded device-side wait gave up            */
+    DSPARK_REQ_BAD_POLICY = 4, /* temperature <= 0 or NaN, top_k < 0, top_p NaN */
+    DSPARK_REQ_BAD_TOKEN = 5   /* an anchor, proposal or label outside [0, V)   */
+} dspark_request_status;
+
+enum {
+    DSPARK_OP_MARKOV_SAMPLE = 0,
+    DSPARK_OP_VERIFY = 1,
+    DSPARK_OP_ACCEPT_STATS = 2
+};
+
+/* Workspace bytes `op` needs for these sizes (r and H matter only for
+ * DSPARK_OP_MARKOV_SAMPLE; pass B = N for DSPARK_OP_ACCEPT_STATS).  Returns 0
+ * for invalid sizes. */
+size_t dspark_workspace_size(int op, int B, int gamma, int V, int r, int H);
+
+/*
+ * dspark_markov_sample - the draft's sequential head over one gamma block.
+ *
+ * [FT Checkpoint-faithful DSpark architecture]: the Markov head runs left to
+ * right so proposal k conditions on proposal k-1, the first on the anchor; the
+ * full proposal distribution q and the confidences are kept.
+ * [MB Semi-autoregressive draft]: the Markov head is a low-rank
+ * token-conditioned additive logit bias; the confidence is
+ * c_k = sigmoid(w^T [h_k ; embed(x_{k-1})]).
+ *
+ * For k = 1..gamma, for every request b (x_0 = anchor[b]):
+ *   z_k[v]  = backbone[b,k-1,v] + sum_j U[x_{k-1}, j] * W[v, j]   (fp32)
+ *   q_k     = policy(z_k)
+ *   x_k     = inverse-CDF draw from q_k in token-index order (u: pos0+k,
+ *             draw 0); greedy requests take the argmax
+ *   c_k     = sigmoid(w_conf[0:H] . h[b,k-1,:] + w_conf[H:2H] . E[x_{k-1},:])
+ *
+ *   backbone  [B, gamma, V] logits of the parallel backbone, `dtype`.
+ *   anchor    int32 [B]: the last committed token of each request.
+ *   U         bf16 [V, r]: token embedding of the Markov head (row x).
+ *   W         bf16 [V, r]: the r x V output matrix stored transposed, i.e.
+ *             row v holds its column v (a Linear(r, V) weight).
+ *   r         rank: 0 (no bias; U and W unused) or a multiple of 16 up to
+ *             DSPARK_MAX_RANK.
+ *   h         [B, gamma, H] draft hidden states (h_dtype), or NULL to skip
+ *             the confidence (conf, E, w_conf then unused).
+ *   E         bf16 [V, H] draft token embedding;  w_conf  fp32 [2H].
+ *   policy    [B] per-request policies, or NULL: every request greedy.
+ *   seed, request_id  uint64 [B];  pos0  int64 [B]: position of the anchor.
+ *   proposals int32 [B, gamma] out: x_1..x_gamma (-1 after a failure).
+ *   q         fp32 [B, gamma, V] out: q_k of sampled requests (0 outside the
+ *             support); rows of greedy requests are not written.  May be NULL
+ *             only when policy is NULL.
+ *   q_at_x    fp32 [B, gamma] out: q_k(x_k); 1 for greedy requests.
+ *   conf      fp32 [B, gamma] out (when h != NULL): c_k.
+ *   status    int32 [B] out: dspark_request_status.
+ *
+ * B <= DSPARK_MAX_BATCH.  The gamma steps are sequential; each enqueues at
+ * most two kernels.
+ */
+int dspark_markov_sample(const void* backbone, int dtype, const int32_t* anchor,
+                         const uint16_t* U, const uint16_t* W, int r,
+                         const void* h, int h_dtype, const uint16_t* E,
+                         const float* w_conf, int H, const dspark_policy* policy,
+                         const uint64_t* seed, const uint64_t* request_id,
+                         const int64_t* pos0, int B, int gamma, int V,
+                         int32_t* proposals, float* q, float* q_at_x,
+                         float* conf, int32_t* status, void* workspace,
+                         size_t workspace_bytes, void* stream);
+
+/*
+ * dspark_verify - exact verification of one proposal block per request.
+ *
+ * [FT Exact decoding semantics > Greedy]: accept the contiguous prefix of
+ * proposals equal to the target argmax; at the first disagreement emit the
+ * target's own token; a later accidental match is never accepted.
+ * [FT > Probabilistic]: accept x_k with probability min(1, p(x_k)/q(x_k)); at
+ * the first rejection sample from normalised max(p - q, 0); if every
+ * proposal survives, sample a bonus token from the target's next-position
+ * distribution.  [PT Acceptance]: 1..gamma+1 tokens per request and step.
+ *
+ * Target row i (i = 0..gamma) is the target's next-token distribution after
+ * (anchor, x_1..x_i): row k-1 scores proposal x_k, row gamma gives the bonus.
+ *   target     [B, gamma+1, V] target logits, `dtype`.
+ *   proposals  int32 [B, gamma].
+ *   q, q_at_x  fp32 [B, gamma, V] and [B, gamma] from dspark_markov_sample;
+ *              read only for sampled requests (may be NULL if policy is NULL).
+ *   policy     [B], or NULL: every request greedy (the fastest path).
+ *   seed, request_id, pos0  as for dspark_markov_sample.  The accept test of
+ *              x_k draws at pos0+k (draw 1); the residual at rejection j at
+ *              pos0+j (draw 2); the bonus at pos0+gamma+1 (draw 2).
+ *   out_tokens int32 [B, gamma+1] out: the emitted tokens, -1 after them.
+ *   num_accepted int32 [B] out: accepted proposals n (emitted = n + 1), or -1
+ *              for a failed request.
+ *   status     int32 [B] out.
+ * Sampled accept test: accept iff p(x) > 0 and u < p(x)/q(x) (q(x) = 0 with
+ * p(x) > 0 accepts).  A residual with zero mass falls back to p.
+ */
+int dspark_verify(const void* target, int dtype, const int32_t* proposals,
+                  const float* q, const float* q_at_x,
+                  const dspark_policy* policy, const uint64_t* seed,
+                  const uint64_t* request_id, const int64_t* pos0, int B,
+                  int gamma, int V, int32_t* out_tokens, int32_t* num_accepted,
+                  int32_t* status, void* workspace, size_t workspace_bytes,
+                  void* stream);
+
+/*
+ * dspark_accept_stats - analytical acceptance statistics of a draft against
+ * the target, per position, and the weighted loss numerators.
+ *
+ * [MB Training objective]: weights exp(-k/gamma); L_ce (0.1) against the
+ * target's teacher-forced next tokens; L_l1 (0.9) the raw
+ * ||p_draft - p_target||_1; L_conf (1.0) BCE of the confidence against the
+ * acceptance label.  [MB Acceptance and confidence]: accept_rate =
+ * clamp(1 - 0.5 L1, 0, 1); tau = sum_k cumprod(accept_rate)_k + 1.
+ * [MB Loss return contract]: numerators and a token count, never ratios.
+ *
+ *   draft, target  [N, gamma, V] logits (`dtype`); position k = 1..gamma of
+ *                  block n; both at temperature 1 with no truncation.
+ *   labels         int32 [N, gamma]: the teacher tokens for the CE term.
+ *   conf_logits    fp32 [N, gamma]: the confidence head's logits z.
+ *   mask           uint8 [N, gamma] (nonzero = counted) or NULL (all).
+ *   l1, accept     fp32 [N, gamma] out, for every position.
+ *   tau            fp32 [N] out.
+ *   loss_num       fp64 [4] out: sum m w_k CE, sum m w_k L1, sum m w_k BCE and
+ *                  0.1 CE + 0.9 L1 + 1.0 BCE, with BCE = softplus(z) - a z.
+ *   report         fp64 [2] out: sum m accept, sum tau (report numerators;
+ *                  their denominators are num_tokens and N).
+ *   num_tokens     int64 [1] out: sum m.
+ *   status         int32 [N] out, or NULL.
+ * Sums are formed in a fixed order: repeated calls give identical bits.
+ */
+int dspark_accept_stats(const void* draft, const void* target, int dtype,
+                        const int32_t* labels, const float* conf_logits,
+                        const uint8_t* mask, int N, int gamma, int V,
+                        float* l1, float* accept, float* tau, double* loss_num,
+                        double* report, int64_t* num_tokens, int32_t* status,
+                        void* workspace, size_t workspace_bytes, void* stream);
+
+/* A short English description of a dspark_status or request-status code
+ * (negative = dspark_status, non-negative = dspark_request_status). */
+const char* dspark_status_string(int code);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int dspark_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSPARK_H */

@@ -1,0 +1,106 @@
+"""Host-side checks of the C ABI: the library builds for sm_103a, exports
+every entry point include/dspark.h declares, and rejects invalid arguments
+before touching device memory (no kernel runs here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import verify_dspark_markov_gb300 as ds
+from verify_dspark_markov_gb300 import binding, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return binding.load()
+
+
+def declared_symbols():
+    text = open(os.path.join(ROOT, "include", "dspark.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(dspark_\w+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(lib):
+    syms = declared_symbols()
+    assert len(syms) >= 6
+    for s in syms:
+        assert hasattr(lib, s), s
+    assert set(binding.EXPORTED) == set(syms)
+
+
+def test_version_and_status_strings(lib):
+    assert lib.dspark_version() >= 100
+    for code in (0, -1, -2, -3, -4, 1, 2, 3, 4, 5):
+        assert ds.status_string(code) and "unknown" not in ds.status_string(code)
+    assert "unknown" in ds.status_string(99)
+
+
+def test_workspace_sizes(lib):
+    n1 = ds.workspace_size(ds.OP_VERIFY, 64, 7, 129280)
+    n2 = ds.workspace_size(ds.OP_VERIFY, 128, 7, 129280)
+    assert 0 < n1 < n2
+    assert ds.workspace_size(ds.OP_VERIFY, 64, 0, 129280) == 0      # invalid gamma
+    assert ds.workspace_size(ds.OP_VERIFY, 64, 7, 129281) == 0      # V not a multiple of 8
+    assert ds.workspace_size(99, 64, 7, 129280) == 0
+
+
+FAKE = ctypes.c_void_p(0x7F0000000000)       # aligned, never dereferenced
+FAKE_ODD = ctypes.c_void_p(0x7F0000000004)   # misaligned by 4
+
+
+def _verify(lib, target=FAKE, dtype=0, B=4, gamma=5, V=1024, ws_bytes=1 << 20, policy=None,
+            props=FAKE):
+    return lib.dspark_verify(target, dtype, props, FAKE, FAKE, policy, FAKE, FAKE, FAKE, B, gamma, V,
+                             FAKE, FAKE, FAKE, FAKE, ws_bytes, None)
+
+
+def test_verify_rejects_invalid_arguments(lib):
+    assert _verify(lib, B=0) == binding.OK                  # empty batch: no-op
+    assert _verify(lib, gamma=0) == binding.EINVAL
+    assert _verify(lib, gamma=17) == binding.EINVAL
+    assert _verify(lib, V=1001) == binding.EINVAL
+    assert _verify(lib, V=0) == binding.EINVAL
+    assert _verify(lib, B=-1) == binding.EINVAL
+    assert _verify(lib, dtype=7) == binding.EINVAL
+    assert _verify(lib, target=None) == binding.EINVAL
+    assert _verify(lib, props=None) == binding.EINVAL
+    assert _verify(lib, target=FAKE_ODD) == binding.EINVAL
+    assert _verify(lib, ws_bytes=16) == binding.ENOSPC
+
+
+def _markov(lib, B=4, gamma=5, V=1024, r=0, U=None, W=None, policy=None, q=None, h=None, H=0,
+            ws_bytes=1 << 20):
+    return lib.dspark_markov_sample(FAKE, 0, FAKE, U, W, r, h, 0, FAKE, FAKE, H, policy, FAKE, FAKE,
+                                    FAKE, B, gamma, V, FAKE, q, FAKE, FAKE, FAKE, FAKE, ws_bytes, None)
+
+
+def test_markov_rejects_invalid_arguments(lib):
+    assert _markov(lib, B=0) == binding.OK
+    assert _markov(lib, B=257) == binding.EINVAL            # above DSPARK_MAX_BATCH
+    assert _markov(lib, r=8, U=FAKE, W=FAKE) == binding.EINVAL      # rank not a multiple of 16
+    assert _markov(lib, r=272, U=FAKE, W=FAKE) == binding.EINVAL    # rank above the maximum
+    assert _markov(lib, r=16) == binding.EINVAL             # r > 0 without U / W
+    assert _markov(lib, r=16, U=FAKE_ODD, W=FAKE) == binding.EINVAL
+    assert _markov(lib, policy=FAKE, q=None) == binding.EINVAL      # sampled requests need q
+    assert _markov(lib, h=FAKE, H=0) == binding.EINVAL
+    assert _markov(lib, ws_bytes=0) == binding.ENOSPC
+
+
+def test_accept_stats_rejects_invalid_arguments(lib):
+    f = lib.dspark_accept_stats
+    assert f(FAKE, FAKE, 0, FAKE, FAKE, None, 4, 0, 1024, *([FAKE] * 7), FAKE, 1 << 20, None) == binding.EINVAL
+    assert f(FAKE, FAKE, 3, FAKE, FAKE, None, 4, 5, 1024, *([FAKE] * 7), FAKE, 1 << 20, None) == binding.EINVAL
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    with pytest.raises((RuntimeError, OSError)):
+        binding._lib = None
+        try:
+            binding.load(str(tmp_path / "missing.so"))
+        finally:
+            binding._lib = None

@@ -1,0 +1,241 @@
+"""Thin ctypes binding of ``libdspark.so`` (the C ABI in ``include/dspark.h``).
+
+Argument marshalling only: torch tensors supply device memory and the current
+stream; every step of the computation runs in the library's CUDA kernels.
+There is no CPU fallback: if the library is missing or a CUDA device is absent,
+the calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+OK, EINVAL, ENOSPC, ECUDA, ENOTSUP = 0, -1, -2, -3, -4
+BF16, F32 = 0, 1
+OP_MARKOV_SAMPLE, OP_VERIFY, OP_ACCEPT_STATS = 0, 1, 2
+REQ_OK, REQ_NONFINITE, REQ_EMPTY, REQ_TIMEOUT, REQ_BAD_POLICY, REQ_BAD_TOKEN = range(6)
+
+EXPORTED = ("dspark_workspace_size", "dspark_markov_sample", "dspark_verify",
+            "dspark_accept_stats", "dspark_status_string", "dspark_version")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class DsparkError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what}: {status_string(code)} ({code})")
+        self.code = code
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(path: str | None = None):
+    """Load (but never build) the CUDA library; raise if it is missing."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            p = path or _build.LIB
+            if not os.path.exists(p):
+                raise RuntimeError(f"{p} is missing: build it with "
+                                   "verify_dspark_markov_gb300.build.build() first")
+            lib = ctypes.CDLL(p)
+            P, i32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+            lib.dspark_workspace_size.argtypes = [i32] * 6
+            lib.dspark_workspace_size.restype = sz
+            lib.dspark_markov_sample.argtypes = ([P, i32, P, P, P, i32, P, i32, P, P, i32]
+                                                 + [P] * 4 + [i32] * 3 + [P] * 6 + [sz, P])
+            lib.dspark_markov_sample.restype = i32
+            lib.dspark_verify.argtypes = [P, i32, P, P, P, P, P, P, P] + [i32] * 3 + [P] * 4 + [sz, P]
+            lib.dspark_verify.restype = i32
+            lib.dspark_accept_stats.argtypes = ([P, P, i32, P, P, P] + [i32] * 3 + [P] * 8
+                                                + [sz, P])
+            lib.dspark_accept_stats.restype = i32
+            lib.dspark_status_string.argtypes = [i32]
+            lib.dspark_status_string.restype = ctypes.c_char_p
+            lib.dspark_version.argtypes = []
+            lib.dspark_version.restype = i32
+            _lib = lib
+    return _lib
+
+
+def status_string(code: int) -> str:
+    return load().dspark_status_string(int(code)).decode()
+
+
+def workspace_size(op: int, B: int, gamma: int, V: int, r: int = 0, H: int = 0) -> int:
+    return int(load().dspark_workspace_size(op, B, gamma, V, r, H))
+
+
+# ------------------------------------------------------------------ helpers
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return BF16
+    if t.dtype == torch.float32:
+        return F32
+    raise TypeError(f"logits must be bfloat16 or float32, got {t.dtype}")
+
+
+def _dev(t: torch.Tensor, name: str, dtype=None):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+class Workspace:
+    """A zero-filled device buffer per (device, op); grown on demand.  The
+    library leaves it zero-filled after every completed call."""
+
+    def __init__(self):
+        self._bufs = {}
+
+    def get(self, op: int, nbytes: int, device) -> torch.Tensor | None:
+        if nbytes == 0:
+            return None
+        key = (torch.device(device).index, op)
+        buf = self._bufs.get(key)
+        if buf is None or buf.numel() < nbytes:
+            buf = torch.zeros(nbytes, dtype=torch.uint8, device=device)
+            self._bufs[key] = buf
+        return buf
+
+
+_default_ws = Workspace()
+
+
+def _check(code: int, what: str):
+    if code != OK:
+        raise DsparkError(code, what)
+
+
+def _policy_ptr(policy):
+    """policy: None (all greedy) or an int32 [B, 4] CUDA tensor of packed
+    dspark_policy records (float temperature, int top_k, float top_p, int greedy)."""
+    if policy is None:
+        return None
+    _dev(policy, "policy", torch.int32)
+    if policy.dim() != 2 or policy.shape[1] != 4:
+        raise ValueError("policy must be an int32 [B, 4] tensor of packed records")
+    return _ptr(policy)
+
+
+# ------------------------------------------------------------------ entry points
+def verify(target, proposals, q=None, q_at_x=None, policy=None, seed=None, request_id=None,
+           pos0=None, out=None, workspace: Workspace | None = None, stream=None):
+    """Exact verify of [B, gamma+1, V] target logits against [B, gamma]
+    proposals.  Returns (out_tokens [B, gamma+1], num_accepted [B], status [B])."""
+    _dev(target, "target")
+    B, rows, V = target.shape
+    gamma = rows - 1
+    _dev(proposals, "proposals", torch.int32)
+    dev = target.device
+    if out is None:
+        out = (torch.empty((B, rows), dtype=torch.int32, device=dev),
+               torch.empty((B,), dtype=torch.int32, device=dev),
+               torch.empty((B,), dtype=torch.int32, device=dev))
+    ws_n = workspace_size(OP_VERIFY, B, gamma, V)
+    ws = (workspace or _default_ws).get(OP_VERIFY, ws_n, dev)
+    code = load().dspark_verify(
+        _ptr(target), _dtype_code(target), _ptr(proposals), _ptr(_dev(q, "q", torch.float32)),
+        _ptr(_dev(q_at_x, "q_at_x", torch.float32)), _policy_ptr(policy),
+        _ptr(_dev(seed, "seed", torch.int64)), _ptr(_dev(request_id, "request_id", torch.int64)),
+        _ptr(_dev(pos0, "pos0", torch.int64)), B, gamma, V,
+        _ptr(out[0]), _ptr(out[1]), _ptr(out[2]), _ptr(ws), ws_n, _stream(stream))
+    _check(code, "dspark_verify")
+    return out
+
+
+def markov_sample(backbone, anchor, U=None, W=None, h=None, E=None, w_conf=None, policy=None,
+                  seed=None, request_id=None, pos0=None, workspace: Workspace | None = None,
+                  stream=None, out=None):
+    """The draft's sequential head over [B, gamma, V] backbone logits.
+    Returns dict(proposals, q, q_at_x, conf, status)."""
+    _dev(backbone, "backbone")
+    B, gamma, V = backbone.shape
+    dev = backbone.device
+    _dev(anchor, "anchor", torch.int32)
+    r = 0 if U is None else U.shape[1]
+    if r:
+        _dev(U, "U", torch.bfloat16)
+        _dev(W, "W", torch.bfloat16)
+    H = 0
+    h_code = F32
+    if h is not None:
+        _dev(h, "h")
+        h_code = _dtype_code(h)
+        H = h.shape[2]
+        _dev(E, "E", torch.bfloat16)
+        _dev(w_conf, "w_conf", torch.float32)
+    if out is None:
+        out = dict(proposals=torch.empty((B, gamma), dtype=torch.int32, device=dev),
+                   q=(torch.empty((B, gamma, V), dtype=torch.float32, device=dev)
+                      if policy is not None else None),
+                   q_at_x=torch.empty((B, gamma), dtype=torch.float32, device=dev),
+                   conf=(torch.empty((B, gamma), dtype=torch.float32, device=dev)
+                         if h is not None else None),
+                   status=torch.empty((B,), dtype=torch.int32, device=dev))
+    ws_n = workspace_size(OP_MARKOV_SAMPLE, B, gamma, V, r, H)
+    ws = (workspace or _default_ws).get(OP_MARKOV_SAMPLE, ws_n, dev)
+    code = load().dspark_markov_sample(
+        _ptr(backbone), _dtype_code(backbone), _ptr(anchor), _ptr(U), _ptr(W), r, _ptr(h), h_code,
+        _ptr(E), _ptr(w_conf), H, _policy_ptr(policy),
+        _ptr(_dev(seed, "seed", torch.int64)), _ptr(_dev(request_id, "request_id", torch.int64)),
+        _ptr(_dev(pos0, "pos0", torch.int64)), B, gamma, V,
+        _ptr(out["proposals"]), _ptr(out["q"]), _ptr(out["q_at_x"]), _ptr(out["conf"]),
+        _ptr(out["status"]), _ptr(ws), ws_n, _stream(stream))
+    _check(code, "dspark_markov_sample")
+    return out
+
+
+def accept_stats(draft, target, labels, conf_logits, mask=None, workspace: Workspace | None = None,
+                 stream=None, out=None):
+    """Acceptance statistics of [N, gamma, V] draft logits against the
+    target.  Returns dict(l1, accept, tau, loss_num, report, num_tokens, status)."""
+    _dev(draft, "draft")
+    _dev(target, "target")
+    if draft.shape != target.shape or draft.dtype != target.dtype:
+        raise ValueError("draft and target must match in shape and dtype")
+    N, gamma, V = draft.shape
+    dev = draft.device
+    _dev(labels, "labels", torch.int32)
+    _dev(conf_logits, "conf_logits", torch.float32)
+    _dev(mask, "mask", torch.uint8)
+    if out is None:
+        out = dict(l1=torch.empty((N, gamma), dtype=torch.float32, device=dev),
+                   accept=torch.empty((N, gamma), dtype=torch.float32, device=dev),
+                   tau=torch.empty((N,), dtype=torch.float32, device=dev),
+                   loss_num=torch.empty((4,), dtype=torch.float64, device=dev),
+                   report=torch.empty((2,), dtype=torch.float64, device=dev),
+                   num_tokens=torch.empty((1,), dtype=torch.int64, device=dev),
+                   status=torch.empty((N,), dtype=torch.int32, device=dev))
+    ws_n = workspace_size(OP_ACCEPT_STATS, N, gamma, V)
+    ws = (workspace or _default_ws).get(OP_ACCEPT_STATS, ws_n, dev)
+    code = load().dspark_accept_stats(
+        _ptr(draft), _ptr(target), _dtype_code(draft), _ptr(labels), _ptr(conf_logits), _ptr(mask),
+        N, gamma, V, _ptr(out["l1"]), _ptr(out["accept"]), _ptr(out["tau"]), _ptr(out["loss_num"]),
+        _ptr(out["report"]), _ptr(out["num_tokens"]), _ptr(out["status"]), _ptr(ws), ws_n,
+        _stream(stream))
+    _check(code, "dspark_accept_stats")
+    return out

@@ -1,0 +1,219 @@
+// C ABI of the DSpark library: argument validation, workspace layout and
+// kernel dispatch.  Everything here runs on the host; every step of the
+// computation runs in the kernels it launches on the caller's stream.
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <algorithm>
+
+#include "dspark.h"
+#include "kernels.h"
+
+namespace dspark {
+namespace {
+
+constexpr size_t kAlign = 256;
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool valid_common(int B, int gamma, int V, int dtype) {
+    return B >= 0 && gamma >= 1 && gamma <= DSPARK_MAX_GAMMA && V >= 8 && V <= DSPARK_MAX_VOCAB &&
+           V % 8 == 0 && (dtype == DSPARK_BF16 || dtype == DSPARK_F32);
+}
+
+// Workspace carve-up.  Regions that must be zero between calls come first.
+struct ArgmaxScratch {
+    size_t rowkey, rowbad, ticket, end;
+};
+ArgmaxScratch argmax_scratch(size_t offset, int groups, int rows_per_group) {
+    ArgmaxScratch s;
+    const size_t rows = static_cast<size_t>(groups) * rows_per_group;
+    s.rowkey = offset;
+    s.rowbad = align_up(s.rowkey + rows * sizeof(unsigned long long));
+    s.ticket = align_up(s.rowbad + rows * sizeof(unsigned int));
+    s.end = align_up(s.ticket + static_cast<size_t>(groups) * sizeof(unsigned int));
+    return s;
+}
+
+struct VerifyLayout {
+    ArgmaxScratch greedy;
+    size_t total;
+};
+VerifyLayout verify_layout(int B, int gamma) {
+    VerifyLayout l;
+    l.greedy = argmax_scratch(0, B, gamma + 1);
+    l.total = l.greedy.end;
+    return l;
+}
+
+struct MarkovLayout {
+    ArgmaxScratch greedy;
+    size_t total;
+};
+MarkovLayout markov_layout(int B, int gamma) {
+    MarkovLayout l;
+    l.greedy = argmax_scratch(0, B, gamma);
+    l.total = l.greedy.end;
+    return l;
+}
+
+template <typename T>
+T* at(void* ws, size_t off) {
+    return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
+}
+
+int device_sms() {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return sms;
+}
+
+// Fill `p.total`, `p.chunk` and return the grid of the flat-split argmax:
+// one wave of resident CTAs, each an equal contiguous range of the rows.
+int plan_argmax(ArgmaxParams& p, int64_t rows) {
+    const int sms = device_sms();
+    const int occ = argmax_rows_occupancy(p.dtype);
+    if (sms <= 0 || occ <= 0) return 0;
+    p.total = rows * static_cast<int64_t>(p.V);
+    const int64_t slots = static_cast<int64_t>(sms) * occ;
+    int64_t chunk = std::max<int64_t>(8192, (p.total + slots - 1) / slots);
+    chunk = (chunk + 7) / 8 * 8;
+    p.chunk = chunk;
+    return static_cast<int>((p.total + chunk - 1) / chunk);
+}
+
+}  // namespace
+}  // namespace dspark
+
+using namespace dspark;
+
+extern "C" {
+
+int dspark_version(void) { return 100; }
+
+const char* dspark_status_string(int code) {
+    switch (code) {
+        case DSPARK_OK: return "ok";
+        case DSPARK_EINVAL: return "invalid argument";
+        case DSPARK_ENOSPC: return "workspace too small";
+        case DSPARK_ECUDA: return "CUDA launch failed";
+        case DSPARK_ENOTSUP: return "not supported";
+        case DSPARK_REQ_NONFINITE: return "request: non-finite logit";
+        case DSPARK_REQ_EMPTY: return "request: all logits -inf";
+        case DSPARK_REQ_TIMEOUT: return "request: device wait timed out";
+        case DSPARK_REQ_BAD_POLICY: return "request: invalid sampling policy";
+        case DSPARK_REQ_BAD_TOKEN: return "request: token id outside [0, V)";
+        default: return "unknown status";
+    }
+}
+
+size_t dspark_workspace_size(int op, int B, int gamma, int V, int r, int H) {
+    if (!valid_common(B, gamma, V, DSPARK_BF16) || r < 0 || H < 0) return 0;
+    switch (op) {
+        case DSPARK_OP_MARKOV_SAMPLE: return markov_layout(B, gamma).total;
+        case DSPARK_OP_VERIFY: return verify_layout(B, gamma).total;
+        case DSPARK_OP_ACCEPT_STATS: return 0;
+        default: return 0;
+    }
+}
+
+int dspark_verify(const void* target, int dtype, const int32_t* proposals, const float* q,
+                  const float* q_at_x, const dspark_policy* policy, const uint64_t* seed,
+                  const uint64_t* request_id, const int64_t* pos0, int B, int gamma, int V,
+                  int32_t* out_tokens, int32_t* num_accepted, int32_t* status, void* workspace,
+                  size_t workspace_bytes, void* stream) {
+    if (!valid_common(B, gamma, V, dtype)) return DSPARK_EINVAL;
+    if (B == 0) return DSPARK_OK;
+    if (!target || !proposals || !out_tokens || !num_accepted || !status) return DSPARK_EINVAL;
+    if (!aligned16(target)) return DSPARK_EINVAL;
+    if (policy && (!q || !q_at_x || !seed || !request_id || !pos0 || !aligned16(q)))
+        return DSPARK_EINVAL;
+    const VerifyLayout lay = verify_layout(B, gamma);
+    if (workspace_bytes < lay.total || (lay.total && !workspace)) return DSPARK_ENOSPC;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+    if (policy) return DSPARK_ENOTSUP;
+
+    ArgmaxParams p{};
+    p.logits = target;
+    p.dtype = dtype;
+    p.V = V;
+    p.rows_per_group = gamma + 1;
+    p.gamma = gamma;
+    p.mode = kArgmaxVerify;
+    p.rowkey = at<unsigned long long>(workspace, lay.greedy.rowkey);
+    p.rowbad = at<unsigned int>(workspace, lay.greedy.rowbad);
+    p.ticket = at<unsigned int>(workspace, lay.greedy.ticket);
+    p.proposals = proposals;
+    p.out_tokens = out_tokens;
+    p.num_accepted = num_accepted;
+    p.status = status;
+    const int grid = plan_argmax(p, static_cast<int64_t>(B) * (gamma + 1));
+    if (grid <= 0) return DSPARK_ECUDA;
+    return launch_argmax_rows(p, grid, s) == cudaSuccess ? DSPARK_OK : DSPARK_ECUDA;
+}
+
+int dspark_markov_sample(const void* backbone, int dtype, const int32_t* anchor, const uint16_t* U,
+                         const uint16_t* W, int r, const void* h, int h_dtype, const uint16_t* E,
+                         const float* w_conf, int H, const dspark_policy* policy,
+                         const uint64_t* seed, const uint64_t* request_id, const int64_t* pos0,
+                         int B, int gamma, int V, int32_t* proposals, float* q, float* q_at_x,
+                         float* conf, int32_t* status, void* workspace, size_t workspace_bytes,
+                         void* stream) {
+    if (!valid_common(B, gamma, V, dtype)) return DSPARK_EINVAL;
+    if (B > DSPARK_MAX_BATCH) return DSPARK_EINVAL;
+    if (r < 0 || r > DSPARK_MAX_RANK || r % 16 != 0) return DSPARK_EINVAL;
+    if (B == 0) return DSPARK_OK;
+    if (!backbone || !anchor || !proposals || !q_at_x || !status) return DSPARK_EINVAL;
+    if (!aligned16(backbone)) return DSPARK_EINVAL;
+    if (r > 0 && (!U || !W || !aligned16(U) || !aligned16(W))) return DSPARK_EINVAL;
+    if (h && (H <= 0 || !E || !w_conf || !conf || (h_dtype != DSPARK_BF16 && h_dtype != DSPARK_F32)))
+        return DSPARK_EINVAL;
+    if (policy && (!q || !seed || !request_id || !pos0 || !aligned16(q))) return DSPARK_EINVAL;
+    const MarkovLayout lay = markov_layout(B, gamma);
+    if (workspace_bytes < lay.total || (lay.total && !workspace)) return DSPARK_ENOSPC;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+    if (policy || r > 0) return DSPARK_ENOTSUP;
+
+    // Greedy drafting without a Markov bias: x_k = argmax of backbone row k.
+    ArgmaxParams p{};
+    p.logits = backbone;
+    p.dtype = dtype;
+    p.V = V;
+    p.rows_per_group = gamma;
+    p.gamma = gamma;
+    p.mode = kArgmaxDraft;
+    p.rowkey = at<unsigned long long>(workspace, lay.greedy.rowkey);
+    p.rowbad = at<unsigned int>(workspace, lay.greedy.rowbad);
+    p.ticket = at<unsigned int>(workspace, lay.greedy.ticket);
+    p.anchor = anchor;
+    p.props_out = proposals;
+    p.q_at_x = q_at_x;
+    p.status = status;
+    const int grid = plan_argmax(p, static_cast<int64_t>(B) * gamma);
+    if (grid <= 0) return DSPARK_ECUDA;
+    if (launch_argmax_rows(p, grid, s) != cudaSuccess) return DSPARK_ECUDA;
+    if (h) {
+        ConfParams c{h, h_dtype, E, w_conf, H, B, gamma, V, anchor, proposals, 1, gamma, conf};
+        if (launch_confidence(c, s) != cudaSuccess) return DSPARK_ECUDA;
+    }
+    return DSPARK_OK;
+}
+
+int dspark_accept_stats(const void* draft, const void* target, int dtype, const int32_t* labels,
+                        const float* conf_logits, const uint8_t* mask, int N, int gamma, int V,
+                        float* l1, float* accept, float* tau, double* loss_num, double* report,
+                        int64_t* num_tokens, int32_t* status, void* workspace,
+                        size_t workspace_bytes, void* stream) {
+    (void)draft; (void)target; (void)labels; (void)conf_logits; (void)mask; (void)l1;
+    (void)accept; (void)tau; (void)loss_num; (void)report; (void)num_tokens; (void)status;
+    (void)workspace; (void)workspace_bytes; (void)stream;
+    if (!valid_common(N, gamma, V, dtype)) return DSPARK_EINVAL;
+    return DSPARK_ENOTSUP;
+}
+
+}  // extern "C"

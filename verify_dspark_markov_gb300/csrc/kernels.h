@@ -1,0 +1,58 @@
+// Internal launch interface between the C ABI (abi.cu) and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "dspark.h"
+
+namespace dspark {
+
+enum { kArgmaxVerify = 0, kArgmaxDraft = 1 };
+
+// Flat-split row argmax (argmax.cu).
+struct ArgmaxParams {
+    const void* logits;
+    int dtype;
+    int64_t total;            // rows * V elements
+    int64_t chunk;            // elements per CTA, a multiple of 8
+    int V;
+    int rows_per_group;       // rows of one request: gamma+1 (verify) or gamma (draft)
+    int gamma;
+    int mode;                 // kArgmaxVerify / kArgmaxDraft
+    unsigned long long* rowkey;  // [groups * rows_per_group], zero on entry and exit
+    unsigned int* rowbad;        // [groups * rows_per_group], zero on entry and exit
+    unsigned int* ticket;        // [groups], zero on entry and exit
+    // verify
+    const int32_t* proposals;
+    int32_t* out_tokens;
+    int32_t* num_accepted;
+    // draft
+    const int32_t* anchor;
+    int32_t* props_out;
+    float* q_at_x;
+    int32_t* status;
+};
+
+cudaError_t launch_argmax_rows(const ArgmaxParams& p, int grid, cudaStream_t stream);
+int argmax_rows_threads();
+int argmax_rows_occupancy(int dtype);
+
+// Confidence head c_k = sigmoid(w[:H] . h_k + w[H:] . E[x_{k-1}]) (confidence.cu).
+struct ConfParams {
+    const void* h;
+    int h_dtype;
+    const uint16_t* E;
+    const float* w;
+    int H;
+    int B;
+    int gamma;
+    int V;
+    const int32_t* anchor;
+    const int32_t* proposals;  // [B, gamma]; x_{k-1} = proposals[k-2] for k >= 2
+    int k_first, k_last;       // 1-based positions to compute, inclusive
+    float* conf;
+};
+cudaError_t launch_confidence(const ConfParams& p, cudaStream_t stream);
+
+}  // namespace dspark
