@@ -243,6 +243,34 @@ int dspark_accept_stats(const void* draft, const void* target, int dtype,
                         double* report, int64_t* num_tokens, int32_t* status,
                         void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * dspark_verify_greedy_noalloc - the greedy verify of dspark_verify (policy
+ * NULL), for callers that cannot allocate device memory.  None of the pages
+ * has a counterpart; it exists for callers such as a plugin inside a runtime
+ * that owns all device memory and offers no allocator, or a latency-critical
+ * path that must not call cudaMalloc (which may synchronize the device).
+ *
+ * Arguments and outputs are those of dspark_verify with every request greedy;
+ * the caller still provides target, proposals and the three output arrays.
+ * There is no workspace argument: the scratch is a static device array of the
+ * library, reserved on every GPU that loads it until the process exits.  It
+ * holds at most DSPARK_NOALLOC_MAX_REQUESTS requests, i.e. at most
+ * DSPARK_NOALLOC_MAX_ROWS target rows (B * (gamma + 1) with gamma <= 16);
+ * larger calls return DSPARK_ENOSPC and launch nothing.  The function
+ * allocates nothing.
+ *
+ * The first call on a device looks up the array's device address (a one-time
+ * set-up per device); make that first call before any stream capture.  All
+ * calls on a device share the array: each call clears the part it uses before
+ * its kernel runs, and calls whose work overlaps on the GPU (e.g. on two
+ * streams) race on it, so serialize them.
+ */
+#define DSPARK_NOALLOC_MAX_REQUESTS 256
+#define DSPARK_NOALLOC_MAX_ROWS 4352
+int dspark_verify_greedy_noalloc(const void* target, int dtype, const int32_t* proposals, int B,
+                                 int gamma, int V, int32_t* out_tokens, int32_t* num_accepted,
+                                 int32_t* status, void* stream);
+
 /* A short English description of a dspark_status or request-status code
  * (negative = dspark_status, non-negative = dspark_request_status). */
 const char* dspark_status_string(int code);

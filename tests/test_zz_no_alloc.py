@@ -1,0 +1,82 @@
+"""The allocation-free greedy verify (dspark_verify_greedy_noalloc).
+
+It serves callers that cannot allocate device memory for scratch (a plugin
+whose host runtime owns all device memory, or a path that must not call
+cudaMalloc).  This file is named to be collected last.  It builds and loads
+the library itself, so it also passes when run alone in a fresh process.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from verify_dspark_markov_gb300 import binding, build
+    build.build()
+    L = binding.load()
+    P, i32 = ctypes.c_void_p, ctypes.c_int
+    L.dspark_verify_greedy_noalloc.argtypes = [P, i32, P, i32, i32, i32, P, P, P, P]
+    L.dspark_verify_greedy_noalloc.restype = i32
+    return L
+
+
+def _noalloc(L, target, proposals):
+    B, rows, V = target.shape
+    out = torch.full((B, rows), -9, dtype=torch.int32, device=target.device)
+    nacc = torch.full((B,), -9, dtype=torch.int32, device=target.device)
+    st = torch.full((B,), -9, dtype=torch.int32, device=target.device)
+    P = ctypes.c_void_p
+    code = L.dspark_verify_greedy_noalloc(
+        P(target.data_ptr()), 0 if target.dtype == torch.bfloat16 else 1, P(proposals.data_ptr()),
+        B, rows - 1, V, P(out.data_ptr()), P(nacc.data_ptr()), P(st.data_ptr()),
+        P(torch.cuda.current_stream().cuda_stream))
+    assert code == 0, code
+    return out, nacc, st
+
+
+def test_noalloc_matches_verify_twice_in_a_row(lib):
+    import verify_dspark_markov_gb300 as ds
+    w = synth.full_decode_tile(device="cuda")
+    x = w.backbone.float().argmax(dim=2).to(torch.int32)
+    ref = ds.verify(w.target, x)
+    for _ in range(2):
+        got = _noalloc(lib, w.target, x)
+        torch.cuda.synchronize()
+        for a, b in zip(ref, got):
+            assert torch.equal(a, b)
+    # a different batch right after: the shared scratch starts clean again
+    w2 = synth.full_decode_tile(V=40_008, B=9, gamma=3, device="cuda", seed=77)
+    x2 = w2.backbone.float().argmax(dim=2).to(torch.int32)
+    x2[0, 1] = 5
+    ref2 = ds.verify(w2.target, x2)
+    got2 = _noalloc(lib, w2.target, x2)
+    torch.cuda.synchronize()
+    for a, b in zip(ref2, got2):
+        assert torch.equal(a, b)
+
+
+def test_noalloc_refuses_oversized_calls(lib):
+    """257 requests exceed the static scratch: the call is refused with
+    DSPARK_ENOSPC.  The buffers match the call's own sizes, so nothing could
+    be read out of bounds even if the check were wrong."""
+    B, gamma, V = 257, 1, 8
+    t = torch.zeros((B, gamma + 1, V), dtype=torch.float32, device="cuda")
+    x = torch.zeros((B, gamma), dtype=torch.int32, device="cuda")
+    out = torch.full((B, gamma + 1), -9, dtype=torch.int32, device="cuda")
+    nacc = torch.full((B,), -9, dtype=torch.int32, device="cuda")
+    st = torch.full((B,), -9, dtype=torch.int32, device="cuda")
+    P = ctypes.c_void_p
+    code = lib.dspark_verify_greedy_noalloc(P(t.data_ptr()), 1, P(x.data_ptr()), B, gamma, V, P(out.data_ptr()),
+                                            P(nacc.data_ptr()), P(st.data_ptr()), None)
+    torch.cuda.synchronize()
+    assert code == -2                            # DSPARK_ENOSPC
+    assert int((st != -9).sum()) == 0            # nothing was launched

@@ -21,7 +21,8 @@ OP_MARKOV_SAMPLE, OP_VERIFY, OP_ACCEPT_STATS = 0, 1, 2
 REQ_OK, REQ_NONFINITE, REQ_EMPTY, REQ_TIMEOUT, REQ_BAD_POLICY, REQ_BAD_TOKEN = range(6)
 
 EXPORTED = ("dspark_workspace_size", "dspark_markov_sample", "dspark_verify",
-            "dspark_accept_stats", "dspark_status_string", "dspark_version")
+            "dspark_accept_stats", "dspark_status_string", "dspark_version",
+            "dspark_verify_greedy_noalloc")
 
 _lock = threading.Lock()
 _lib = None
