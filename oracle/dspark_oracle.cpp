@@ -437,6 +437,8 @@ extern "C" void orc_verify(const void* target, int32_t dtype,
 // tau = sum_k cumprod(accept_rate)_k + 1.
 // [MB Loss return contract]: numerators and a token count, never ratios.
 // Readings: k = 1..gamma; the teacher tokens are an explicit labels input;
+// a block's status is the largest code of its positions (a label outside
+// [0, V) outranks a non-finite logit);
 // the confidence enters as a logit z and BCE = softplus(z) - accept * z in
 // its stable form; the label is the clamped accept_rate; num_tokens counts
 // mask = 1 positions; l1 / accept / tau are reported for every position.
@@ -466,7 +468,7 @@ extern "C" void orc_accept_stats(const void* draft, const void* target,
             for (int v = 0; v < V; ++v) {
                 d[v] = load_value(draft, dtype, idx * V + v);
                 t[v] = load_value(target, dtype, idx * V + v);
-                if (is_bad_logit(d[v]) || is_bad_logit(t[v])) st = ORC_NONFINITE;
+                if (is_bad_logit(d[v]) || is_bad_logit(t[v])) st = std::max(st, static_cast<int>(ORC_NONFINITE));
                 dmax = std::max(dmax, d[v]);
                 tmax = std::max(tmax, t[v]);
             }
