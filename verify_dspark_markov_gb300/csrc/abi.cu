@@ -59,6 +59,10 @@ MarkovLayout markov_layout(int B, int gamma) {
     return l;
 }
 
+size_t stats_workspace(int N, int gamma) {
+    return align_up(static_cast<size_t>(N) * gamma * sizeof(StatsRecord));
+}
+
 template <typename T>
 T* at(void* ws, size_t off) {
     return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
@@ -115,7 +119,7 @@ size_t dspark_workspace_size(int op, int B, int gamma, int V, int r, int H) {
     switch (op) {
         case DSPARK_OP_MARKOV_SAMPLE: return markov_layout(B, gamma).total;
         case DSPARK_OP_VERIFY: return verify_layout(B, gamma).total;
-        case DSPARK_OP_ACCEPT_STATS: return 0;
+        case DSPARK_OP_ACCEPT_STATS: return stats_workspace(B, gamma);
         default: return 0;
     }
 }
@@ -209,11 +213,42 @@ int dspark_accept_stats(const void* draft, const void* target, int dtype, const 
                         float* l1, float* accept, float* tau, double* loss_num, double* report,
                         int64_t* num_tokens, int32_t* status, void* workspace,
                         size_t workspace_bytes, void* stream) {
-    (void)draft; (void)target; (void)labels; (void)conf_logits; (void)mask; (void)l1;
-    (void)accept; (void)tau; (void)loss_num; (void)report; (void)num_tokens; (void)status;
-    (void)workspace; (void)workspace_bytes; (void)stream;
     if (!valid_common(N, gamma, V, dtype)) return DSPARK_EINVAL;
-    return DSPARK_ENOTSUP;
+    if (static_cast<int64_t>(N) * gamma * stats_cluster_size() > 0x7FFFFFFFll) return DSPARK_EINVAL;
+    if (!loss_num || !report || !num_tokens) return DSPARK_EINVAL;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (N == 0) {  // empty batch: the numerators and the count are zero
+        if (cudaMemsetAsync(loss_num, 0, 4 * sizeof(double), s) != cudaSuccess ||
+            cudaMemsetAsync(report, 0, 2 * sizeof(double), s) != cudaSuccess ||
+            cudaMemsetAsync(num_tokens, 0, sizeof(int64_t), s) != cudaSuccess)
+            return DSPARK_ECUDA;
+        return DSPARK_OK;
+    }
+    if (!draft || !target || !labels || !conf_logits || !l1 || !accept || !tau) return DSPARK_EINVAL;
+    if (!aligned16(draft) || !aligned16(target)) return DSPARK_EINVAL;
+    const size_t need = stats_workspace(N, gamma);
+    if (workspace_bytes < need || !workspace) return DSPARK_ENOSPC;
+    StatsParams p{};
+    p.draft = draft;
+    p.target = target;
+    p.dtype = dtype;
+    p.labels = labels;
+    p.conf_logits = conf_logits;
+    p.mask = mask;
+    p.N = N;
+    p.gamma = gamma;
+    p.V = V;
+    const int C = stats_cluster_size();
+    p.slice = ((V + C - 1) / C + 7) / 8 * 8;
+    p.l1 = l1;
+    p.accept = accept;
+    p.rec = at<StatsRecord>(workspace, 0);
+    p.tau = tau;
+    p.loss_num = loss_num;
+    p.report = report;
+    p.num_tokens = num_tokens;
+    p.status = status;
+    return launch_accept_stats(p, s) == cudaSuccess ? DSPARK_OK : DSPARK_ECUDA;
 }
 
 }  // extern "C"

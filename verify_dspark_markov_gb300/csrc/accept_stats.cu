@@ -1,0 +1,287 @@
+// Analytical acceptance statistics [MB Training objective; Acceptance and
+// confidence; Loss return contract].  Per position (n, k):
+//   p_d = softmax(draft row), p_t = softmax(target row)   (T = 1, full vocab)
+//   L1  = ||p_d - p_t||_1,  accept = clamp(1 - L1/2, 0, 1)
+//   CE  = -log p_d[label],  BCE = softplus(z) - accept * z   (z: confidence logit)
+// and per block n: tau = 1 + sum_k prod_{j<=k} accept_j; over the batch the
+// exp(-k/gamma)-weighted numerators and the token count, never ratios.
+//
+// Kernel 1 (one cluster of kC CTAs per row pair): each CTA streams a 1/kC
+// slice of both rows once from HBM, keeping an online (max, sum of exp) per
+// thread; the cluster combines the slices' statistics through distributed
+// shared memory; each CTA then re-reads its slice (a ~129 KB working set per
+// CTA, so the re-read is served by L2) to form the L1 terms.  NaN / +inf poison
+// the running sums, which is how non-finite rows are detected at no cost.
+// Kernel 2 (one CTA): tau, statuses and the weighted sums in a fixed order,
+// so repeated calls give identical bits.
+
+#include <cooperative_groups.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace cg = cooperative_groups;
+
+namespace dspark {
+
+namespace {
+
+constexpr int kC = 8;          // CTAs per row pair (cluster size)
+constexpr int kThreads = 256;
+constexpr int kBatch = 4;      // 16-byte vectors per row per thread in flight
+constexpr float kLog2e = 1.4426950408889634f;
+
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Online softmax statistics: m = running max (starts at -FLT_MAX so that -inf
+// logits contribute exp(-inf) = 0), s = sum of exp(x - m).
+struct Online {
+    float m, s;
+    __device__ __forceinline__ void init() { m = -3.402823466e38f; s = 0.0f; }
+    template <int kN>
+    __device__ __forceinline__ void add(const float (&x)[kN]) {
+        float mx = x[0];
+#pragma unroll
+        for (int i = 1; i < kN; ++i) mx = fmaxf(mx, x[i]);
+        if (mx > m) {
+            s *= ex2((m - mx) * kLog2e);
+            m = mx;
+        }
+#pragma unroll
+        for (int i = 0; i < kN; ++i) s += ex2((x[i] - m) * kLog2e);
+    }
+    __device__ __forceinline__ void merge(float m2, float s2) {
+        const float mn = fmaxf(m, m2);
+        s = s * ex2((m - mn) * kLog2e) + s2 * ex2((m2 - mn) * kLog2e);
+        m = mn;
+    }
+};
+
+template <int kDtype>
+__device__ __forceinline__ void unpack(const uint4& v, float (&x)[kDtype == kBF16 ? 8 : 4]) {
+    if constexpr (kDtype == kBF16) {
+        x[0] = bf16_lo(v.x); x[1] = bf16_hi(v.x); x[2] = bf16_lo(v.y); x[3] = bf16_hi(v.y);
+        x[4] = bf16_lo(v.z); x[5] = bf16_hi(v.z); x[6] = bf16_lo(v.w); x[7] = bf16_hi(v.w);
+    } else {
+        x[0] = __uint_as_float(v.x); x[1] = __uint_as_float(v.y);
+        x[2] = __uint_as_float(v.z); x[3] = __uint_as_float(v.w);
+    }
+}
+
+template <int kDtype>
+__global__ void __cluster_dims__(kC, 1, 1) __launch_bounds__(kThreads)
+    stats_pairs_kernel(const StatsParams p) {
+    constexpr int kPer = kDtype == kBF16 ? 8 : 4;
+    constexpr int64_t kEsize = kDtype == kBF16 ? 2 : 4;
+    __shared__ float s_warp[4][kThreads / 32];
+    __shared__ float s_stats[4];   // this CTA's (md, sd, mt, st)
+    __shared__ double s_l1;        // this CTA's L1 partial
+
+    cg::cluster_group cluster = cg::this_cluster();
+    const int rank = static_cast<int>(cluster.block_rank());
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int64_t pair = blockIdx.x / kC;
+    const int64_t lo = static_cast<int64_t>(rank) * p.slice;
+    const int64_t hi = min(lo + p.slice, static_cast<int64_t>(p.V));
+    const int nvec = hi > lo ? static_cast<int>((hi - lo) / kPer) : 0;
+    const char* drow = static_cast<const char*>(p.draft) + (pair * p.V + lo) * kEsize;
+    const char* trow = static_cast<const char*>(p.target) + (pair * p.V + lo) * kEsize;
+
+    // ---- pass 1: online max / sum of exp over the slice, both rows
+    Online od, ot;
+    od.init();
+    ot.init();
+    for (int j0 = tid; j0 < nvec; j0 += kBatch * kThreads) {
+        uint4 vd[kBatch], vt[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            const int j = j0 + u * kThreads;
+            if (j < nvec) {
+                vd[u] = ld_stream_v4(drow + static_cast<int64_t>(j) * 16);
+                vt[u] = ld_stream_v4(trow + static_cast<int64_t>(j) * 16);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            if (j0 + u * kThreads < nvec) {
+                float x[kPer];
+                unpack<kDtype>(vd[u], x);
+                od.add(x);
+                unpack<kDtype>(vt[u], x);
+                ot.add(x);
+            }
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        od.merge(__shfl_xor_sync(0xFFFFFFFFu, od.m, o), __shfl_xor_sync(0xFFFFFFFFu, od.s, o));
+        ot.merge(__shfl_xor_sync(0xFFFFFFFFu, ot.m, o), __shfl_xor_sync(0xFFFFFFFFu, ot.s, o));
+    }
+    if (lane == 0) {
+        s_warp[0][warp] = od.m; s_warp[1][warp] = od.s;
+        s_warp[2][warp] = ot.m; s_warp[3][warp] = ot.s;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        Online a, b;
+        a.init();
+        b.init();
+        for (int w = 0; w < kThreads / 32; ++w) {
+            a.merge(s_warp[0][w], s_warp[1][w]);
+            b.merge(s_warp[2][w], s_warp[3][w]);
+        }
+        s_stats[0] = a.m; s_stats[1] = a.s; s_stats[2] = b.m; s_stats[3] = b.s;
+    }
+    cluster.sync();
+    // every CTA combines the kC slices in rank order: identical results
+    Online gd, gt;
+    gd.init();
+    gt.init();
+    for (int r = 0; r < kC; ++r) {
+        const float* st = cluster.map_shared_rank(s_stats, r);
+        gd.merge(st[0], st[1]);
+        gt.merge(st[2], st[3]);
+    }
+    const float inv_sd = 1.0f / gd.s, inv_st = 1.0f / gt.s;
+
+    // ---- pass 2: sum of |p_d - p_t| over the slice (re-read, served by L2)
+    float l1 = 0.0f;
+    for (int j0 = tid; j0 < nvec; j0 += kBatch * kThreads) {
+        uint4 vd[kBatch], vt[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            const int j = j0 + u * kThreads;
+            if (j < nvec) {
+                vd[u] = ld_stream_v4(drow + static_cast<int64_t>(j) * 16);
+                vt[u] = ld_stream_v4(trow + static_cast<int64_t>(j) * 16);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            if (j0 + u * kThreads < nvec) {
+                float xd[kPer], xt[kPer];
+                unpack<kDtype>(vd[u], xd);
+                unpack<kDtype>(vt[u], xt);
+#pragma unroll
+                for (int i = 0; i < kPer; ++i)
+                    l1 += fabsf(ex2((xd[i] - gd.m) * kLog2e) * inv_sd - ex2((xt[i] - gt.m) * kLog2e) * inv_st);
+            }
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) l1 += __shfl_xor_sync(0xFFFFFFFFu, l1, o);
+    if (lane == 0) s_warp[0][warp] = l1;
+    __syncthreads();
+    if (tid == 0) {
+        double a = 0.0;
+        for (int w = 0; w < kThreads / 32; ++w) a += s_warp[0][w];
+        s_l1 = a;
+    }
+    cluster.sync();
+    if (rank == 0 && tid == 0) {
+        double dist = 0.0;
+        for (int r = 0; r < kC; ++r) dist += *cluster.map_shared_rank(&s_l1, r);
+        const float L1 = static_cast<float>(dist);
+        const float acc = fminf(1.0f, fmaxf(0.0f, 1.0f - 0.5f * L1));
+        int32_t code = (gd.s != gd.s || gt.s != gt.s) ? kReqNonfinite : kReqOk;
+        const int32_t y = p.labels[pair];
+        float ce;
+        if (y < 0 || y >= p.V) {
+            code = kReqBadToken;
+            ce = __int_as_float(0x7FC00000);
+        } else {
+            float dy;
+            if (kDtype == kBF16)
+                dy = __uint_as_float(static_cast<uint32_t>(static_cast<const uint16_t*>(p.draft)[pair * p.V + y]) << 16);
+            else
+                dy = static_cast<const float*>(p.draft)[pair * p.V + y];
+            ce = gd.m + logf(gd.s) - dy;
+        }
+        const float zc = p.conf_logits[pair];
+        const float bce = fmaxf(zc, 0.0f) - acc * zc + log1pf(expf(-fabsf(zc)));
+        p.l1[pair] = L1;
+        p.accept[pair] = acc;
+        StatsRecord rec;
+        rec.ce = ce;
+        rec.l1 = L1;
+        rec.bce = bce;
+        rec.acc = acc;
+        rec.code = code;
+        p.rec[pair] = rec;
+    }
+    cluster.sync();  // no CTA leaves while rank 0 reads its shared memory
+}
+
+constexpr int kFinalThreads = 256;
+
+__global__ void __launch_bounds__(kFinalThreads) stats_final_kernel(const StatsParams p) {
+    __shared__ double s_sum[5][kFinalThreads];
+    __shared__ long long s_cnt[kFinalThreads];
+    const int tid = threadIdx.x;
+    double ce = 0.0, l1 = 0.0, bce = 0.0, acc_sum = 0.0, tau_sum = 0.0;
+    long long cnt = 0;
+    for (int n = tid; n < p.N; n += kFinalThreads) {
+        double tau = 1.0, survive = 1.0;
+        int32_t code = kReqOk;
+        for (int k = 1; k <= p.gamma; ++k) {
+            const int64_t i = static_cast<int64_t>(n) * p.gamma + (k - 1);
+            const StatsRecord r = p.rec[i];
+            survive *= r.acc;
+            tau += survive;
+            code = max(code, r.code);
+            if (!p.mask || p.mask[i]) {
+                const double w = exp(-static_cast<double>(k) / p.gamma);
+                ce += w * r.ce;
+                l1 += w * r.l1;
+                bce += w * r.bce;
+                acc_sum += r.acc;
+                ++cnt;
+            }
+        }
+        p.tau[n] = static_cast<float>(tau);
+        if (p.status) p.status[n] = code;
+        tau_sum += tau;
+    }
+    s_sum[0][tid] = ce; s_sum[1][tid] = l1; s_sum[2][tid] = bce;
+    s_sum[3][tid] = acc_sum; s_sum[4][tid] = tau_sum;
+    s_cnt[tid] = cnt;
+    __syncthreads();
+    if (tid == 0) {  // fixed order: identical bits on every call
+        double t[5] = {0, 0, 0, 0, 0};
+        long long c = 0;
+        for (int i = 0; i < kFinalThreads; ++i) {
+            for (int j = 0; j < 5; ++j) t[j] += s_sum[j][i];
+            c += s_cnt[i];
+        }
+        p.loss_num[0] = t[0];
+        p.loss_num[1] = t[1];
+        p.loss_num[2] = t[2];
+        p.loss_num[3] = 0.1 * t[0] + 0.9 * t[1] + 1.0 * t[2];
+        p.report[0] = t[3];
+        p.report[1] = t[4];
+        *p.num_tokens = c;
+    }
+}
+
+}  // namespace
+
+int stats_cluster_size() { return kC; }
+
+cudaError_t launch_accept_stats(const StatsParams& p, cudaStream_t stream) {
+    const int64_t pairs = static_cast<int64_t>(p.N) * p.gamma;
+    const dim3 grid(static_cast<unsigned>(pairs * kC));
+    if (p.dtype == kBF16)
+        stats_pairs_kernel<kBF16><<<grid, kThreads, 0, stream>>>(p);
+    else
+        stats_pairs_kernel<kF32><<<grid, kThreads, 0, stream>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    stats_final_kernel<<<1, kFinalThreads, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace dspark

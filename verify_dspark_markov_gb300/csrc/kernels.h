@@ -55,4 +55,31 @@ struct ConfParams {
 };
 cudaError_t launch_confidence(const ConfParams& p, cudaStream_t stream);
 
+// Acceptance statistics (accept_stats.cu).
+struct StatsRecord {  // one position's terms, consumed by the fixed-order finaliser
+    float ce, l1, bce, acc;
+    int32_t code;
+    int32_t pad[3];
+};
+struct StatsParams {
+    const void* draft;
+    const void* target;
+    int dtype;
+    const int32_t* labels;
+    const float* conf_logits;
+    const uint8_t* mask;
+    int N, gamma, V;
+    int slice;                // elements per CTA slice, a multiple of 8
+    float* l1;
+    float* accept;
+    StatsRecord* rec;         // [N * gamma] workspace
+    float* tau;
+    double* loss_num;
+    double* report;
+    int64_t* num_tokens;
+    int32_t* status;
+};
+int stats_cluster_size();
+cudaError_t launch_accept_stats(const StatsParams& p, cudaStream_t stream);
+
 }  // namespace dspark
