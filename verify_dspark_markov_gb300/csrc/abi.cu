@@ -39,14 +39,19 @@ ArgmaxScratch argmax_scratch(size_t offset, int groups, int rows_per_group) {
 
 struct VerifyLayout {
     ArgmaxScratch greedy;
-    size_t total;
+    size_t ticket, records, total;
 };
 VerifyLayout verify_layout(int B, int gamma) {
     VerifyLayout l;
     l.greedy = argmax_scratch(0, B, gamma + 1);
-    l.total = l.greedy.end;
+    l.ticket = l.greedy.end;  // sampled path: one ticket per request (zero between calls)
+    l.records = align_up(l.ticket + static_cast<size_t>(B) * sizeof(unsigned int));
+    l.total = align_up(l.records + static_cast<size_t>(B) * (gamma + 1) * sizeof(RowRecord));
     return l;
 }
+
+// Largest vocabulary the row engine holds in one cluster's shared memory.
+bool policy_vocab_ok(int V) { return policy_slice(V) * sizeof(float) <= 200 * 1024; }
 
 struct MarkovLayout {
     ArgmaxScratch greedy;
@@ -139,7 +144,29 @@ int dspark_verify(const void* target, int dtype, const int32_t* proposals, const
     if (workspace_bytes < lay.total || (lay.total && !workspace)) return DSPARK_ENOSPC;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
-    if (policy) return DSPARK_ENOTSUP;
+    if (policy) {  // per-request policies: the row engine
+        if (!policy_vocab_ok(V)) return DSPARK_ENOTSUP;
+        VerifyProbParams vp{};
+        vp.target = target;
+        vp.dtype = dtype;
+        vp.proposals = proposals;
+        vp.q = q;
+        vp.q_at_x = q_at_x;
+        vp.policy = policy;
+        vp.seed = seed;
+        vp.request_id = request_id;
+        vp.pos0 = pos0;
+        vp.B = B;
+        vp.gamma = gamma;
+        vp.V = V;
+        vp.slice = policy_slice(V);
+        vp.out_tokens = out_tokens;
+        vp.num_accepted = num_accepted;
+        vp.status = status;
+        vp.records = at<RowRecord>(workspace, lay.records);
+        vp.ticket = at<unsigned int>(workspace, lay.ticket);
+        return launch_verify_prob(vp, s) == cudaSuccess ? DSPARK_OK : DSPARK_ECUDA;
+    }
 
     ArgmaxParams p{};
     p.logits = target;
@@ -181,7 +208,36 @@ int dspark_markov_sample(const void* backbone, int dtype, const int32_t* anchor,
     if (workspace_bytes < lay.total || (lay.total && !workspace)) return DSPARK_ENOSPC;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
-    if (policy || r > 0) return DSPARK_ENOTSUP;
+    if (r > 0) return DSPARK_ENOTSUP;
+    if (policy) {  // per-request policies: one row-engine launch per step
+        if (!policy_vocab_ok(V)) return DSPARK_ENOTSUP;
+        MarkovStepParams mp{};
+        mp.backbone = backbone;
+        mp.dtype = dtype;
+        mp.zbuf = nullptr;
+        mp.anchor = anchor;
+        mp.proposals = proposals;
+        mp.q = q;
+        mp.q_at_x = q_at_x;
+        mp.status = status;
+        mp.policy = policy;
+        mp.seed = seed;
+        mp.request_id = request_id;
+        mp.pos0 = pos0;
+        mp.B = B;
+        mp.gamma = gamma;
+        mp.V = V;
+        mp.slice = policy_slice(V);
+        for (int k = 1; k <= gamma; ++k) {
+            mp.k = k;
+            if (launch_markov_step(mp, s) != cudaSuccess) return DSPARK_ECUDA;
+        }
+        if (h) {
+            ConfParams c{h, h_dtype, E, w_conf, H, B, gamma, V, anchor, proposals, 1, gamma, conf};
+            if (launch_confidence(c, s) != cudaSuccess) return DSPARK_ECUDA;
+        }
+        return DSPARK_OK;
+    }
 
     // Greedy drafting without a Markov bias: x_k = argmax of backbone row k.
     ArgmaxParams p{};

@@ -55,6 +55,58 @@ struct ConfParams {
 };
 cudaError_t launch_confidence(const ConfParams& p, cudaStream_t stream);
 
+// Sampled paths on the row engine (policy_kernels.cu).
+struct RowRecord {  // the policy of one target row, for the request's decision
+    float zmax;
+    float inv_t;
+    uint32_t tau;     // support = {key > tau} + {key == tau, index <= cut}
+    int32_t cut;
+    uint64_t mass;    // fixed-point (2^-40) mass of the support
+    float p_x;        // p of the proposal this row scores
+    int32_t status;
+    int32_t argmax;
+    int32_t pad;
+};
+struct VerifyProbParams {
+    const void* target;
+    int dtype;
+    const int32_t* proposals;
+    const float* q;
+    const float* q_at_x;
+    const dspark_policy* policy;
+    const uint64_t* seed;
+    const uint64_t* request_id;
+    const int64_t* pos0;
+    int B, gamma, V;
+    int slice;                 // elements per CTA of a row's cluster
+    int32_t* out_tokens;
+    int32_t* num_accepted;
+    int32_t* status;
+    RowRecord* records;        // [B * (gamma + 1)] workspace
+    unsigned int* ticket;      // [B] workspace, zero on entry and exit
+};
+struct MarkovStepParams {
+    const void* backbone;      // [B, gamma, V] (dtype), read when zbuf is null
+    int dtype;
+    const float* zbuf;         // [B, V] fp32 logits with the Markov bias, or null
+    const int32_t* anchor;
+    int32_t* proposals;
+    float* q;
+    float* q_at_x;
+    int32_t* status;
+    const dspark_policy* policy;   // null: every request greedy
+    const uint64_t* seed;
+    const uint64_t* request_id;
+    const int64_t* pos0;
+    int B, gamma, V;
+    int slice;
+    int k;                     // 1-based step
+};
+int policy_cluster_size();
+int policy_slice(int V);
+cudaError_t launch_verify_prob(const VerifyProbParams& p, cudaStream_t stream);
+cudaError_t launch_markov_step(const MarkovStepParams& p, cudaStream_t stream);
+
 // Acceptance statistics (accept_stats.cu).
 struct StatsRecord {  // one position's terms, consumed by the fixed-order finaliser
     float ce, l1, bce, acc;

@@ -1,0 +1,547 @@
+// Row engine: the sampling policy of one vocabulary row, computed by a
+// cluster of kC CTAs that each hold a contiguous slice of the row in shared
+// memory (as fp32), plus the exact inverse-CDF draw over the policy's weights.
+//
+// The policy [FT Exact decoding semantics > Probabilistic] as this library
+// reads it: greedy = one-hot at the lowest-index argmax; otherwise temperature,
+// then top-k keeping exactly k tokens in (logit descending, index ascending)
+// order, then top-p keeping the shortest prefix of that order (inside the top-k
+// set) whose share of the kept mass is >= p; probabilities are the
+// renormalised exp((z - zmax) / T) on that support.
+//
+// Exactness: the support is described by a key threshold and an index cut
+// (support = {key > tau} + {key == tau, index <= cut}), found by radix selection
+// on order-preserving 32-bit keys; masses are fixed-point integers
+// w = round(2^40 exp((z - zmax)/T)), so every sum, every top-p comparison and
+// every inverse-CDF boundary is an exact, order-independent integer decision.
+// To keep the radix passes off the bulk of the row, the selection starts from
+// a window [zmax - D, zmax] chosen by a single counting (or mass) pass over 8
+// candidate widths, and the first digit starts after the common prefix of the
+// window's end keys.
+#pragma once
+
+#include <cooperative_groups.h>
+
+#include "common.cuh"
+
+namespace dspark {
+namespace rp {
+
+namespace cg = cooperative_groups;
+
+constexpr int kC = 8;           // CTAs per row
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kBins = 256;      // 8-bit radix digits
+constexpr int kWin = 8;         // candidate window widths
+constexpr double kFix = 1099511627776.0;  // 2^40: fixed-point scale of the weights
+constexpr float kLog2e = 1.4426950408889634f;
+
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Unnormalised policy weight exp((z - zmax) * invT) and its fixed-point form.
+__device__ __forceinline__ float weight_f(float z, float zmax, float inv_t) {
+    return ex2(((z - zmax) * inv_t) * kLog2e);
+}
+__device__ __forceinline__ uint64_t to_fixed(float w) {
+    return __float2ull_rn(w * static_cast<float>(kFix));
+}
+
+struct Policy {
+    float inv_t;
+    int32_t top_k;   // 0 = off (already normalised: 0 < top_k < V, else 0)
+    float top_p;     // >= 1 = off
+    int32_t greedy;
+};
+
+// Results of the policy of one row, identical in every CTA of the cluster.
+struct RowResult {
+    float zmax;
+    int32_t argmax;
+    int32_t status;
+    uint32_t tau;       // support = {key > tau} + {key == tau, index <= cut}
+    int32_t cut;
+    uint64_t mass;      // sum of fixed-point weights over the support
+};
+
+// Shared state of one CTA of the engine (static shared memory).
+struct Smem {
+    // cluster exchange slots, double-buffered so that one cluster barrier per
+    // exchange suffices (a slot is rewritten only two exchanges later)
+    unsigned long long xu[2][kWin + 2];
+    uint32_t hcnt[2][kBins];
+    unsigned long long hmass[2][kBins];
+    unsigned long long wu[kWarps][kWin + 2];  // per-warp partials
+    unsigned long long scan_u[kWarps];
+    int32_t pick[4];
+    int parity;      // which exchange buffer is next
+    int hparity;     // which histogram buffer is next
+};
+
+__device__ __forceinline__ bool in_set(uint32_t key, int32_t idx, uint32_t tau, int32_t cut) {
+    return key > tau || (key == tau && idx <= cut);
+}
+
+// Block-sum of up to kWin+2 uint64 values per thread, then a cluster-sum; every
+// thread of every CTA returns the same totals in out[].
+template <int kN>
+__device__ __forceinline__ void cluster_sum_u64(Smem& sm, cg::cluster_group& cl, unsigned long long (&v)[kN],
+                                                unsigned long long (&out)[kN]) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int i = 0; i < kN; ++i) {
+        unsigned long long x = v[i];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xFFFFFFFFu, x, o);
+        if (lane == 0) sm.wu[warp][i] = x;
+    }
+    __syncthreads();
+    const int buf = sm.parity;
+    if (threadIdx.x < kN) {
+        unsigned long long t = 0;
+        for (int w = 0; w < kWarps; ++w) t += sm.wu[w][threadIdx.x];
+        sm.xu[buf][threadIdx.x] = t;
+    }
+    cl.sync();
+#pragma unroll
+    for (int i = 0; i < kN; ++i) {
+        unsigned long long t = 0;
+        for (int r = 0; r < kC; ++r) t += cl.map_shared_rank(&sm.xu[buf][0], r)[i];
+        out[i] = t;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) sm.parity ^= 1;
+    __syncthreads();
+}
+
+// Block-max then cluster-max of one uint64 (and OR of a flag word).
+__device__ __forceinline__ void cluster_max_u64(Smem& sm, cg::cluster_group& cl, unsigned long long v,
+                                                unsigned long long flags, unsigned long long& out_max,
+                                                unsigned long long& out_flags) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const unsigned long long w = __shfl_xor_sync(0xFFFFFFFFu, v, o);
+        v = w > v ? w : v;
+        flags |= __shfl_xor_sync(0xFFFFFFFFu, flags, o);
+    }
+    if (lane == 0) {
+        sm.wu[warp][0] = v;
+        sm.wu[warp][1] = flags;
+    }
+    __syncthreads();
+    const int buf = sm.parity;
+    if (threadIdx.x == 0) {
+        unsigned long long m = 0, f = 0;
+        for (int w = 0; w < kWarps; ++w) {
+            m = sm.wu[w][0] > m ? sm.wu[w][0] : m;
+            f |= sm.wu[w][1];
+        }
+        sm.xu[buf][0] = m;
+        sm.xu[buf][1] = f;
+    }
+    cl.sync();
+    unsigned long long m = 0, f = 0;
+    for (int r = 0; r < kC; ++r) {
+        const unsigned long long* x = cl.map_shared_rank(&sm.xu[buf][0], r);
+        m = x[0] > m ? x[0] : m;
+        f |= x[1];
+    }
+    out_max = m;
+    out_flags = f;
+    __syncthreads();
+    if (threadIdx.x == 0) sm.parity ^= 1;
+    __syncthreads();
+}
+
+// Exclusive prefix over the CTAs of the cluster of one uint64 per CTA (value
+// given by thread 0); returns (prefix of this CTA's rank for every rank via
+// totals[]).  totals[r] = value of rank r.
+__device__ __forceinline__ void cluster_gather_u64(Smem& sm, cg::cluster_group& cl, unsigned long long mine,
+                                                   unsigned long long (&totals)[kC]) {
+    const int buf = sm.parity;
+    if (threadIdx.x == 0) sm.xu[buf][0] = mine;
+    cl.sync();
+#pragma unroll
+    for (int r = 0; r < kC; ++r) totals[r] = cl.map_shared_rank(&sm.xu[buf][0], r)[0];
+    __syncthreads();
+    if (threadIdx.x == 0) sm.parity ^= 1;
+    __syncthreads();
+}
+
+// Inclusive block scan of one uint64 per thread.
+__device__ __forceinline__ unsigned long long block_scan_u64(Smem& sm, unsigned long long x) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const unsigned long long y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) sm.scan_u[warp] = x;
+    __syncthreads();
+    unsigned long long base = 0;
+    for (int w = 0; w < warp; ++w) base += sm.scan_u[w];
+    __syncthreads();
+    return x + base;
+}
+
+// The slice [lo, lo + n) of the row held by this CTA, as fp32 in shared memory.
+struct Slice {
+    const float* z;
+    int lo, n;
+    int per;  // contiguous elements per thread for ordered scans
+};
+
+// Radix selection on keys: among elements matching `pred` with key in the
+// range sharing the common prefix of [klo, khi], find the key tau at which the
+// descending cumulative measure (count, or fixed-point mass when kMass)
+// reaches `target`.  Returns tau, the measure strictly above tau and the
+// count / mass of elements equal to tau (all within pred).
+template <bool kMass, typename Pred>
+__device__ bool radix_select(Smem& sm, cg::cluster_group& cl, const Slice& sl, uint32_t klo, uint32_t khi,
+                             unsigned long long target, float zmax, float inv_t, Pred pred, uint32_t& tau,
+                             unsigned long long& above, unsigned long long& eq_cnt,
+                             unsigned long long& eq_mass) {
+    const int tid = threadIdx.x;
+    int hi_bit = klo == khi ? 0 : 32 - __clz(static_cast<int>(klo ^ khi));  // bits still open
+    uint32_t prefix = hi_bit >= 32 ? 0u : (khi >> hi_bit);
+    above = 0;
+    eq_cnt = 0;
+    eq_mass = 0;
+    if (hi_bit == 0) {  // a single key in the window: count it
+        unsigned long long v[2] = {0, 0};
+        for (int i = tid; i < sl.n; i += kThreads) {
+            const float z = sl.z[i];
+            const uint32_t key = ordered_key(z);
+            if (key == khi && pred(key, sl.lo + i)) {
+                v[0] += 1;
+                if (kMass) v[1] += to_fixed(weight_f(z, zmax, inv_t));
+            }
+        }
+        unsigned long long o[2];
+        cluster_sum_u64<2>(sm, cl, v, o);
+        tau = khi;
+        eq_cnt = o[0];
+        eq_mass = o[1];
+        return (kMass ? o[1] : o[0]) >= target;
+    }
+    bool found = true;
+    while (hi_bit > 0) {
+        const int nb = hi_bit >= 8 ? 8 : hi_bit;
+        const int lo_bit = hi_bit - nb;
+        const int buf = sm.hparity;
+        for (int b = tid; b < kBins; b += kThreads) {
+            sm.hcnt[buf][b] = 0;
+            if (kMass) sm.hmass[buf][b] = 0;
+        }
+        __syncthreads();
+        for (int i = tid; i < sl.n; i += kThreads) {
+            const float z = sl.z[i];
+            const uint32_t key = ordered_key(z);
+            const bool match = (hi_bit >= 32 ? true : (key >> hi_bit) == prefix) && pred(key, sl.lo + i);
+            if (match) {
+                const uint32_t d = (key >> lo_bit) & ((1u << nb) - 1u);
+                atomicAdd(&sm.hcnt[buf][d], 1u);
+                if (kMass) atomicAdd(&sm.hmass[buf][d], static_cast<unsigned long long>(to_fixed(weight_f(z, zmax, inv_t))));
+            }
+        }
+        cl.sync();
+        // thread t takes bin (nbins - 1 - t): descending key order
+        const int nbins = 1 << nb;
+        const int b = nbins - 1 - tid;
+        unsigned long long c = 0, m = 0;
+        if (b >= 0) {
+            for (int r = 0; r < kC; ++r) {
+                c += cl.map_shared_rank(&sm.hcnt[buf][0], r)[b];
+                if (kMass) m += cl.map_shared_rank(&sm.hmass[buf][0], r)[b];
+            }
+        }
+        const unsigned long long mine = kMass ? m : c;
+        if (tid == 0) sm.pick[1] = 0;
+        const unsigned long long incl = block_scan_u64(sm, mine);
+        if (b >= 0 && above + incl >= target && above + incl - mine < target) {
+            sm.pick[0] = b;
+            sm.pick[1] = 1;
+            reinterpret_cast<unsigned long long*>(&sm.scan_u[0])[0] = incl - mine;  // measure above b
+            reinterpret_cast<unsigned long long*>(&sm.wu[0][0])[0] = c;
+            reinterpret_cast<unsigned long long*>(&sm.wu[0][1])[0] = m;
+        }
+        __syncthreads();
+        if (!sm.pick[1]) found = false;
+        const int pb = sm.pick[1] ? sm.pick[0] : 0;
+        above += sm.pick[1] ? sm.scan_u[0] : 0ull;
+        eq_cnt = sm.wu[0][0];
+        eq_mass = sm.wu[0][1];
+        prefix = (prefix << nb) | static_cast<uint32_t>(pb);
+        hi_bit = lo_bit;
+        __syncthreads();
+        if (tid == 0) sm.hparity ^= 1;
+        __syncthreads();
+    }
+    tau = prefix;
+    return found;
+}
+
+// Global index of the t-th (1-based) element in index order with key == tau
+// and pred; every CTA returns it.
+template <typename Pred>
+__device__ int32_t tie_index(Smem& sm, cg::cluster_group& cl, const Slice& sl, uint32_t tau,
+                             unsigned long long t, Pred pred) {
+    const int tid = threadIdx.x;
+    const int rank = static_cast<int>(cl.block_rank());
+    // ordered ownership: thread i owns [i*per, (i+1)*per) of the slice
+    const int a = min(tid * sl.per, sl.n), e = min(a + sl.per, sl.n);
+    unsigned long long mine = 0;
+    for (int i = a; i < e; ++i) {
+        const uint32_t key = ordered_key(sl.z[i]);
+        if (key == tau && pred(key, sl.lo + i)) ++mine;
+    }
+    const unsigned long long incl = block_scan_u64(sm, mine);
+    __shared__ unsigned long long s_total;
+    if (tid == kThreads - 1) s_total = incl;
+    __syncthreads();
+    unsigned long long totals[kC];
+    cluster_gather_u64(sm, cl, s_total, totals);
+    unsigned long long before = 0;
+    int owner = kC - 1;
+    for (int r = 0; r < kC; ++r) {
+        if (before + totals[r] >= t) { owner = r; break; }
+        before += totals[r];
+    }
+    const int buf = sm.parity;
+    if (rank == owner && tid == 0) sm.xu[buf][0] = static_cast<unsigned long long>(sl.lo + max(sl.n - 1, 0));
+    __syncthreads();
+    if (rank == owner) {
+        const unsigned long long want = t - before;
+        if (incl >= want && incl - mine < want) {
+            unsigned long long k = incl - mine;
+            for (int i = a; i < e; ++i) {
+                const uint32_t key = ordered_key(sl.z[i]);
+                if (key == tau && pred(key, sl.lo + i) && ++k == want) {
+                    sm.xu[buf][0] = static_cast<unsigned long long>(sl.lo + i);
+                    break;
+                }
+            }
+        }
+    }
+    cl.sync();
+    const int32_t idx = static_cast<int32_t>(cl.map_shared_rank(&sm.xu[buf][0], owner)[0]);
+    __syncthreads();
+    if (tid == 0) sm.parity ^= 1;
+    __syncthreads();
+    return idx;
+}
+
+// The policy of the row held by the cluster.  z slice already loaded; max key,
+// argmax and the bad flag already reduced.
+__device__ void row_policy(Smem& sm, cg::cluster_group& cl, const Slice& sl, int V, const Policy& pol,
+                           RowResult& res) {
+    const float zmax = res.zmax;
+    const uint32_t kmax = ordered_key(zmax);
+    // greedy: the argmax alone
+    res.tau = kmax;
+    res.cut = res.argmax;
+    res.mass = static_cast<unsigned long long>(kFix);
+    if (pol.greedy) return;
+    const float inv_t = pol.inv_t;
+    const int tid = threadIdx.x;
+
+    // ---- top-k: exactly k tokens
+    uint32_t tau_k = 0;      // key > 0 holds for every non-NaN value: "all"
+    int32_t cut_k = -1;
+    const bool use_k = pol.top_k > 0;
+    if (use_k) {
+        unsigned long long v[kWin + 1], cnt[kWin + 1];
+#pragma unroll
+        for (int i = 0; i <= kWin; ++i) v[i] = 0;
+        for (int i = tid; i < sl.n; i += kThreads) {
+            const float d = zmax - sl.z[i];
+#pragma unroll
+            for (int w = 0; w < kWin; ++w) v[w] += d <= static_cast<float>(1 << w) ? 1ull : 0ull;
+        }
+        cluster_sum_u64<kWin + 1>(sm, cl, v, cnt);
+        // the narrowest width holding k elements, doubled against rounding at its edge
+        float zlo = -__int_as_float(0x7F800000);
+        for (int w = kWin - 1; w >= 0; --w)
+            if (cnt[w] >= static_cast<unsigned long long>(pol.top_k)) zlo = zmax - static_cast<float>(2 << w);
+        const uint32_t klo = zlo == -__int_as_float(0x7F800000) ? 0u : ordered_key(zlo);
+        unsigned long long above, eqc, eqm;
+        auto all = [](uint32_t, int32_t) { return true; };
+        if (!radix_select<false>(sm, cl, sl, klo, kmax, static_cast<unsigned long long>(pol.top_k), zmax, inv_t,
+                                 all, tau_k, above, eqc, eqm))
+            radix_select<false>(sm, cl, sl, 0u, kmax, static_cast<unsigned long long>(pol.top_k), zmax, inv_t,
+                                all, tau_k, above, eqc, eqm);
+        const unsigned long long need = static_cast<unsigned long long>(pol.top_k) - above;
+        cut_k = tie_index(sm, cl, sl, tau_k, need, [](uint32_t, int32_t) { return true; });
+    }
+    auto in_k = [tau_k, cut_k](uint32_t key, int32_t idx) { return in_set(key, idx, tau_k, cut_k); };
+
+    // ---- kept mass, and the mass inside each candidate window (for top-p)
+    const bool use_p = pol.top_p < 1.0f;
+    unsigned long long v[kWin + 1], ms[kWin + 1];
+#pragma unroll
+    for (int i = 0; i <= kWin; ++i) v[i] = 0;
+    for (int i = tid; i < sl.n; i += kThreads) {
+        const float z = sl.z[i];
+        const float d = (zmax - z) * inv_t;
+        if (d > 41.0f * 0.6931472f + 1.0f) continue;  // weight rounds to 0 in 2^-40 units
+        const uint32_t key = ordered_key(z);
+        if (!in_k(key, sl.lo + i)) continue;
+        const unsigned long long w = to_fixed(weight_f(z, zmax, inv_t));
+        v[kWin] += w;
+#pragma unroll
+        for (int wi = 0; wi < kWin; ++wi) v[wi] += d <= static_cast<float>(2 << wi) ? w : 0ull;
+    }
+    cluster_sum_u64<kWin + 1>(sm, cl, v, ms);
+    const unsigned long long kept = ms[kWin];
+    res.tau = tau_k;
+    res.cut = cut_k;
+    res.mass = kept;
+    if (!use_p) return;
+
+    // ---- top-p: shortest prefix of the order with mass >= p * kept
+    double th = ceil(static_cast<double>(pol.top_p) * static_cast<double>(kept));
+    unsigned long long theta = th < 1.0 ? 1ull : static_cast<unsigned long long>(th);
+    if (theta > kept) theta = kept;
+    float zlo = -__int_as_float(0x7F800000);
+    for (int w = kWin - 1; w >= 0; --w)
+        if (ms[w] >= theta) zlo = zmax - static_cast<float>(4 << w) / inv_t;  // doubled width
+    uint32_t klo = zlo == -__int_as_float(0x7F800000) ? 0u : ordered_key(zlo);
+    if (use_k && klo < tau_k) klo = tau_k;  // the cut lies inside the top-k set
+    uint32_t tau_p;
+    unsigned long long above, eqc, eqm;
+    if (!radix_select<true>(sm, cl, sl, klo, kmax, theta, zmax, inv_t, in_k, tau_p, above, eqc, eqm))
+        radix_select<true>(sm, cl, sl, 0u, kmax, theta, zmax, inv_t, in_k, tau_p, above, eqc, eqm);
+    // tied elements share one weight; take just enough of them in index order
+    const unsigned long long wt = eqc ? eqm / eqc : 0ull;
+    unsigned long long t = wt ? (theta - above + wt - 1) / wt : eqc;
+    if (t < 1) t = 1;
+    if (t > eqc) t = eqc;
+    const int32_t cut_p = tie_index(sm, cl, sl, tau_p, t, in_k);
+    res.tau = tau_p;
+    res.cut = cut_p;
+    res.mass = above + t * wt;
+}
+
+// Inverse-CDF draw in token-index order over fixed-point weights w(i) (a
+// functor of the slice-local index): the smallest index whose inclusive
+// prefix exceeds floor(m * total / 2^24), m the 24-bit uniform.  Every CTA
+// returns the index.
+template <typename Wf>
+__device__ int32_t sample_fixed(Smem& sm, cg::cluster_group& cl, const Slice& sl, uint32_t m24, Wf wf,
+                                unsigned long long& total_out) {
+    const int tid = threadIdx.x;
+    const int rank = static_cast<int>(cl.block_rank());
+    const int a = min(tid * sl.per, sl.n), e = min(a + sl.per, sl.n);
+    unsigned long long mine = 0;
+    for (int i = a; i < e; ++i) mine += wf(i);
+    const unsigned long long incl = block_scan_u64(sm, mine);
+    __shared__ unsigned long long s_total;
+    if (tid == kThreads - 1) s_total = incl;
+    __syncthreads();
+    unsigned long long totals[kC];
+    cluster_gather_u64(sm, cl, s_total, totals);
+    unsigned long long total = 0;
+    for (int r = 0; r < kC; ++r) total += totals[r];
+    total_out = total;
+    if (total == 0) return -1;
+    const unsigned long long target =
+        static_cast<unsigned long long>((static_cast<unsigned __int128>(m24) * total) >> 24);
+    unsigned long long before = 0;
+    int owner = kC - 1;
+    for (int r = 0; r < kC; ++r) {
+        if (before + totals[r] > target) { owner = r; break; }
+        before += totals[r];
+    }
+    const int buf = sm.parity;
+    if (rank == owner && tid == 0) sm.xu[buf][0] = static_cast<unsigned long long>(sl.lo + max(sl.n - 1, 0));
+    __syncthreads();
+    if (rank == owner) {
+        const unsigned long long tl = target - before;  // within this CTA: first prefix > tl
+        if (incl > tl && incl - mine <= tl) {
+            unsigned long long c = incl - mine;
+            for (int i = a; i < e; ++i) {
+                c += wf(i);
+                if (c > tl) {
+                    sm.xu[buf][0] = static_cast<unsigned long long>(sl.lo + i);
+                    break;
+                }
+            }
+        }
+    }
+    cl.sync();
+    const int32_t idx = static_cast<int32_t>(cl.map_shared_rank(&sm.xu[buf][0], owner)[0]);
+    __syncthreads();
+    if (tid == 0) sm.parity ^= 1;
+    __syncthreads();
+    return idx;
+}
+
+// Load this CTA's slice of a row into shared memory (fp32) and reduce the
+// row's max key / lowest argmax / non-finite flag over the cluster.
+template <int kDtype>
+__device__ void load_slice_and_max(Smem& sm, cg::cluster_group& cl, const void* row, int lo, int n, float* zs,
+                                   RowResult& res, bool& bad) {
+    constexpr int kPer = kDtype == kBF16 ? 8 : 4;
+    constexpr int kEsize = kDtype == kBF16 ? 2 : 4;
+    const char* src = static_cast<const char*>(row) + static_cast<int64_t>(lo) * kEsize;
+    unsigned long long best = 0;
+    float nanacc = -__int_as_float(0x7F800000);
+    const int nvec = n / kPer;
+    for (int j = threadIdx.x; j < nvec; j += kThreads) {
+        const uint4 v = ld_stream_v4(src + static_cast<int64_t>(j) * 16);
+        float x[kPer];
+        if constexpr (kDtype == kBF16) {
+            x[0] = bf16_lo(v.x); x[1] = bf16_hi(v.x); x[2] = bf16_lo(v.y); x[3] = bf16_hi(v.y);
+            x[4] = bf16_lo(v.z); x[5] = bf16_hi(v.z); x[6] = bf16_lo(v.w); x[7] = bf16_hi(v.w);
+            *reinterpret_cast<float4*>(zs + j * 8) = make_float4(x[0], x[1], x[2], x[3]);
+            *reinterpret_cast<float4*>(zs + j * 8 + 4) = make_float4(x[4], x[5], x[6], x[7]);
+        } else {
+            x[0] = __uint_as_float(v.x); x[1] = __uint_as_float(v.y);
+            x[2] = __uint_as_float(v.z); x[3] = __uint_as_float(v.w);
+            *reinterpret_cast<float4*>(zs + j * 4) = make_float4(x[0], x[1], x[2], x[3]);
+        }
+#pragma unroll
+        for (int l = 0; l < kPer; ++l) {
+            nanacc = fmax_nan(nanacc, x[l]);
+            if (x[l] > -__int_as_float(0x7F800000)) {
+                const unsigned long long k =
+                    (static_cast<unsigned long long>(ordered_key(x[l])) << 32) |
+                    (0xFFFFFFFFull - static_cast<uint32_t>(lo + j * kPer + l));
+                best = k > best ? k : best;
+            }
+        }
+    }
+    unsigned long long mk, fl;
+    cluster_max_u64(sm, cl, best, bad_logit(nanacc) ? 1ull : 0ull, mk, fl);
+    bad = fl != 0;
+    if (mk == 0) {
+        res.zmax = -__int_as_float(0x7F800000);
+        res.argmax = -1;
+    } else {
+        res.zmax = key_to_float(static_cast<uint32_t>(mk >> 32));
+        res.argmax = static_cast<int32_t>(0xFFFFFFFFu - static_cast<uint32_t>(mk));
+    }
+}
+
+// Normalise a request's policy record; returns false for an invalid one.
+__device__ __forceinline__ bool make_policy(const dspark_policy& in, int V, Policy& out) {
+    out.greedy = in.greedy != 0;
+    out.inv_t = 1.0f;
+    out.top_k = 0;
+    out.top_p = 1.0f;
+    if (out.greedy) return true;
+    const float T = in.temperature;
+    if (!(T > 0.0f) || isinf(T) || in.top_k < 0 || isnan(in.top_p)) return false;
+    out.inv_t = 1.0f / T;
+    out.top_k = (in.top_k > 0 && in.top_k < V) ? in.top_k : 0;
+    out.top_p = in.top_p;
+    return true;
+}
+
+}  // namespace rp
+}  // namespace dspark
