@@ -55,12 +55,15 @@ bool policy_vocab_ok(int V) { return policy_slice(V) * sizeof(float) <= 200 * 10
 
 struct MarkovLayout {
     ArgmaxScratch greedy;
-    size_t total;
+    size_t error_flag, zbuf, total;
 };
-MarkovLayout markov_layout(int B, int gamma) {
+MarkovLayout markov_layout(int B, int gamma, int V, int r) {
     MarkovLayout l;
     l.greedy = argmax_scratch(0, B, gamma);
-    l.total = l.greedy.end;
+    l.error_flag = l.greedy.end;  // zero between calls; set only after a device wait gave up
+    l.zbuf = align_up(l.error_flag + sizeof(int));
+    const size_t zbytes = r > 0 ? static_cast<size_t>(B) * V * sizeof(float) : 0;
+    l.total = align_up(l.zbuf + zbytes);
     return l;
 }
 
@@ -122,7 +125,7 @@ const char* dspark_status_string(int code) {
 size_t dspark_workspace_size(int op, int B, int gamma, int V, int r, int H) {
     if (!valid_common(B, gamma, V, DSPARK_BF16) || r < 0 || H < 0) return 0;
     switch (op) {
-        case DSPARK_OP_MARKOV_SAMPLE: return markov_layout(B, gamma).total;
+        case DSPARK_OP_MARKOV_SAMPLE: return markov_layout(B, gamma, V, r).total;
         case DSPARK_OP_VERIFY: return verify_layout(B, gamma).total;
         case DSPARK_OP_ACCEPT_STATS: return stats_workspace(B, gamma);
         default: return 0;
@@ -204,17 +207,41 @@ int dspark_markov_sample(const void* backbone, int dtype, const int32_t* anchor,
     if (h && (H <= 0 || !E || !w_conf || !conf || (h_dtype != DSPARK_BF16 && h_dtype != DSPARK_F32)))
         return DSPARK_EINVAL;
     if (policy && (!q || !seed || !request_id || !pos0 || !aligned16(q))) return DSPARK_EINVAL;
-    const MarkovLayout lay = markov_layout(B, gamma);
+    const MarkovLayout lay = markov_layout(B, gamma, V, r);
     if (workspace_bytes < lay.total || (lay.total && !workspace)) return DSPARK_ENOSPC;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
-    if (r > 0) return DSPARK_ENOTSUP;
-    if (policy) {  // per-request policies: one row-engine launch per step
+    if (policy || r > 0) {  // the row engine, one launch per step (after the bias GEMM when r > 0)
         if (!policy_vocab_ok(V)) return DSPARK_ENOTSUP;
+        int* error_flag = at<int>(workspace, lay.error_flag);
+        float* zbuf = r > 0 ? at<float>(workspace, lay.zbuf) : nullptr;
+        MarkovGemmParams gp{};
+        int ggrid = 0;
+        if (r > 0) {
+            gp.backbone = backbone;
+            gp.dtype = dtype;
+            gp.U = U;
+            gp.W = W;
+            gp.anchor = anchor;
+            gp.proposals = proposals;
+            gp.B = B;
+            gp.gamma = gamma;
+            gp.V = V;
+            gp.r = r;
+            gp.N = (B + 15) / 16 * 16;
+            gp.tmem_cols = 32;
+            while (gp.tmem_cols < gp.N) gp.tmem_cols *= 2;
+            gp.zbuf = zbuf;
+            gp.error_flag = error_flag;
+            const int sms = device_sms();
+            const int ntiles = (V + 127) / 128;
+            ggrid = std::min(sms > 0 ? sms : 1, ntiles);
+            if (markov_gemm_smem(r, gp.N) > 220 * 1024) return DSPARK_ENOTSUP;
+        }
         MarkovStepParams mp{};
         mp.backbone = backbone;
         mp.dtype = dtype;
-        mp.zbuf = nullptr;
+        mp.zbuf = zbuf;
         mp.anchor = anchor;
         mp.proposals = proposals;
         mp.q = q;
@@ -228,7 +255,12 @@ int dspark_markov_sample(const void* backbone, int dtype, const int32_t* anchor,
         mp.gamma = gamma;
         mp.V = V;
         mp.slice = policy_slice(V);
+        mp.error_flag = r > 0 ? error_flag : nullptr;
         for (int k = 1; k <= gamma; ++k) {
+            if (r > 0) {
+                gp.k = k;
+                if (launch_markov_bias(gp, ggrid, s) != cudaSuccess) return DSPARK_ECUDA;
+            }
             mp.k = k;
             if (launch_markov_step(mp, s) != cudaSuccess) return DSPARK_ECUDA;
         }

@@ -101,7 +101,26 @@ struct MarkovStepParams {
     int B, gamma, V;
     int slice;
     int k;                     // 1-based step
+    const int* error_flag;     // set by the bias kernel when a device wait gave up
 };
+
+// Markov bias on the tensor cores (markov_gemm.cu).
+struct MarkovGemmParams {
+    const void* backbone;      // [B, gamma, V] (dtype)
+    int dtype;
+    const uint16_t* U;         // bf16 [V, r]
+    const uint16_t* W;         // bf16 [V, r]
+    const int32_t* anchor;
+    const int32_t* proposals;  // [B, gamma]: x_{k-1} = proposals[b, k-2] for k >= 2
+    int B, gamma, V, r;
+    int N;                     // batch padded to a multiple of 16 (MMA N)
+    int tmem_cols;             // power of two >= max(32, N)
+    int k;                     // 1-based step
+    float* zbuf;               // [B, V] fp32 out
+    int* error_flag;
+};
+int markov_gemm_smem(int r, int N);
+cudaError_t launch_markov_bias(const MarkovGemmParams& p, int grid, cudaStream_t stream);
 int policy_cluster_size();
 int policy_slice(int V);
 cudaError_t launch_verify_prob(const VerifyProbParams& p, cudaStream_t stream);

@@ -232,6 +232,14 @@ __global__ void __cluster_dims__(rp::kC, 1, 1) __launch_bounds__(rp::kThreads)
         }
         return;  // uniform over the cluster: no cluster barrier follows
     }
+    if (p.error_flag && *p.error_flag) {  // the bias of this step is not trustworthy
+        if (rank == 0 && tid == 0) {
+            p.proposals[pidx] = -1;
+            p.q_at_x[pidx] = 0.0f;
+            p.status[b] = kReqTimeout;
+        }
+        return;
+    }
     const int lo = rank * p.slice;
     const int n = max(0, min(p.slice, p.V - lo));
     rp::Slice sl{zs, lo, n, (n + kThreads - 1) / kThreads};
