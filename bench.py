@@ -1,18 +1,27 @@
 #!/usr/bin/env python
 """Benchmark of the DSpark draft-sampling / exact-verify hot path on GB300.
 
-Default workload (the one the headline metric is quoted on): the full decode
-tile, 64 requests x (1 anchor + gamma = 7 proposals) = 512 target rows over a
-129,280-token vocabulary, bf16 logits, greedy requests, no Markov bias (r = 0).
-One step = the whole path on one batch: the draft proposals (argmax of the 448
-draft backbone rows) followed by the exact greedy verify of the 512 target
-rows.  Inputs are resident in HBM when the timed region starts.  The step's
-inputs (248 MB) exceed L2 (135.5 MB on GB300); in addition a 2 x L2-sized read
-of another buffer before every timed step, outside the step's events, evicts
-them (a read, so no dirty lines are left to be written back inside the step).
+One step = the whole path over one batch of synthetic input, inputs resident
+in HBM when the timed region starts.  Workloads (``--workload``):
 
-Prints one JSON line.  `--impl reference` times the CPU oracle on the same
-workload instead (the reference arm), on a bounded sample of requests.
+  full_decode_tile   (default; the headline metric's workload) 64 requests x
+                     (1 anchor + gamma = 7) = 512 target rows, V = 129,280,
+                     bf16, greedy, no Markov bias: the draft proposals (argmax
+                     of the 448 draft rows) then the exact greedy verify.
+  decode_verify_tile 64 requests, gamma = 5, bf16, T = 0.7 / top-k 50 /
+                     top-p 0.95, Markov rank 256, draft hidden 4096: Markov
+                     sampling (bias GEMM + policy + draw per position,
+                     confidences) then the sampled verify.
+  mixed_serving      256 requests, gamma = 5, per-request policies, 25 %
+                     greedy, 10 % adversarial drafts, rank 256.
+  training_stats     4096 blocks x gamma = 7 fp32 row pairs: L1, accept rate,
+                     tau and the weighted loss numerators.
+
+The step's inputs exceed L2 (135.5 MB on GB300) in every workload; in addition
+a 2 x L2-sized read of another buffer before every timed step, outside the
+step's events, evicts them (a read, so no dirty lines are left to be written
+back inside the step).  Prints one JSON line.  ``--impl reference`` times the
+CPU oracle on a bounded sample of the same workload instead.
 """
 from __future__ import annotations
 
@@ -35,6 +44,7 @@ METRIC = ("verified positions/s and achieved HBM GB/s (% of GB300 roofline) at "
           "512×(γ+1)×129,280")
 UNIT = "positions/s"
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 
 
 def peaks():
@@ -42,8 +52,8 @@ def peaks():
     if os.path.exists(path):
         with open(path) as f:
             d = json.load(f)
-        return float(d["hbm_gbs"]), "measured"
-    return FALLBACK_HBM_GBS, "fallback"
+        return float(d["hbm_gbs"]), float(d.get("bf16_tflops", FALLBACK_BF16_TFLOPS)), "measured"
+    return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
 
 
 def dist_env():
@@ -112,21 +122,224 @@ class Clocks:
                 "samples": len(sm), "reasons": sorted(reasons)}
 
 
-# ----------------------------------------------------------------- workload
-def make_workload(device):
-    w = synth.full_decode_tile(device=device)
-    return w
+# ------------------------------------------------------------------ workloads
+class Serving:
+    """Draft sampling then exact verify of one batch."""
+
+    def __init__(self, name, w, esize):
+        self.name, self.w, self.esize = name, w, esize
+        self.positions = w.B * (w.gamma + 1)
+        self.greedy_only = bool(w.policy.greedy.all()) and w.weights.r == 0
+
+    def config(self):
+        w = self.w
+        return {"workload": self.name, "requests": w.B, "gamma": w.gamma, "vocab": w.V,
+                "target_rows": w.B * (w.gamma + 1), "draft_rows": w.B * w.gamma,
+                "policy": "greedy" if self.greedy_only else "per-request temperature / top-k / top-p",
+                "markov_rank": w.weights.r, "draft_hidden": w.weights.H}
+
+    def setup(self, ds, dev):
+        w = self.w
+        B, g, V = w.B, w.gamma, w.V
+        self.ds = ds
+        self.ws = ds.Workspace()
+        self.pol = None if self.greedy_only else w.policy.packed().to(dev)
+        self.keys = dict(seed=w.keys.seed.to(dev), request_id=w.keys.request_id.to(dev), pos0=w.keys.pos0.to(dev))
+        self.wts = dict(U=w.weights.U, W=w.weights.W, E=w.weights.E, w_conf=w.weights.w_conf)
+        self.draft_out = dict(proposals=torch.empty((B, g), dtype=torch.int32, device=dev),
+                              q=None if self.pol is None else torch.empty((B, g, V), dtype=torch.float32, device=dev),
+                              q_at_x=torch.empty((B, g), dtype=torch.float32, device=dev),
+                              conf=torch.empty((B, g), dtype=torch.float32, device=dev) if w.h is not None else None,
+                              status=torch.empty((B,), dtype=torch.int32, device=dev))
+        self.ver_out = (torch.empty((B, g + 1), dtype=torch.int32, device=dev),
+                        torch.empty((B,), dtype=torch.int32, device=dev),
+                        torch.empty((B,), dtype=torch.int32, device=dev))
+        self.inputs = [w.backbone, w.target, w.anchor] + ([w.h] if w.h is not None else [])
+
+    def draft(self, stream, backbone=None, anchor=None, h=None):
+        w = self.w
+        d = self.draft_out
+        self.ds.markov_sample(backbone if backbone is not None else w.backbone,
+                              anchor if anchor is not None else w.anchor,
+                              h=h if h is not None else w.h, policy=self.pol, workspace=self.ws, out=d,
+                              stream=stream, **self.wts, **(self.keys if self.pol is not None else {}))
+
+    def verify(self, stream, target=None):
+        d = self.draft_out
+        self.ds.verify(target if target is not None else self.w.target, d["proposals"], q=d["q"],
+                       q_at_x=d["q_at_x"] if self.pol is not None else None, policy=self.pol,
+                       workspace=self.ws, out=self.ver_out, stream=stream,
+                       **(self.keys if self.pol is not None else {}))
+
+    def parts(self):
+        return [("draft", self.draft), ("verify", self.verify)]
+
+    def bytes(self):
+        """Bytes the method must move once, per part."""
+        w, e = self.w, self.esize
+        B, g, V, r, H = w.B, w.gamma, w.V, w.weights.r, w.weights.H
+        sampled = int((self.w.policy.greedy == 0).sum()) if self.pol is not None else 0
+        draft = (B * g * V * e                      # backbone rows
+                 + g * (V * r * 2 + B * r * 2)      # the rank-r matrix per step, gathered U rows
+                 + sampled * g * V * 4              # q rows of sampled requests
+                 + B * g * (H * 2 * 2 if w.h is not None else 0)  # h and E rows for c_k
+                 + B * 4 + B * g * 12)              # anchors, proposals, q(x), c_k
+        rejecting = 0
+        if self.pol is not None:
+            nacc = self.ver_out[1].cpu()
+            greedy = self.w.policy.greedy.cpu() != 0
+            rejecting = int(((nacc < g) & (nacc >= 0) & ~greedy).sum())
+        verify = (B * (g + 1) * V * e + rejecting * V * 4 + B * g * 8 + B * (g + 1) * 4 + B * 8)
+        return {"draft": draft, "verify": verify}
+
+    def flops(self):
+        w = self.w
+        return {"draft": 2 * w.B * w.weights.r * w.V * w.gamma}
+
+    def e2e_step(self, stream, dev_inputs, host_inputs, host_outputs):
+        for d, h in zip(dev_inputs, host_inputs):
+            d.copy_(h, non_blocking=True)
+        backbone, target, anchor = dev_inputs[:3]
+        h = dev_inputs[3] if len(dev_inputs) > 3 else None
+        self.draft(stream, backbone=backbone, anchor=anchor, h=h)
+        self.verify(stream, target=target)
+        for h, d in zip(host_outputs, self.ver_out):
+            h.copy_(d, non_blocking=True)
+
+    def outputs(self):
+        return list(self.ver_out)
+
+    def check(self):
+        st = self.ver_out[2]
+        assert int((st != 0).sum()) == 0, "unexpected request failures in the benchmark workload"
+
+    def cpu_sample(self, budget_s, max_requests=None):
+        """The oracle on whole requests of the workload (draft + verify), one
+        request at a time, single-threaded."""
+        import oracle
+        oracle.build()
+        w = self.w
+        bb, tg = synth.host(w.backbone), synth.host(w.target)
+        anchor = w.anchor.cpu().numpy()
+        keys = w.keys.numpy()
+        pol = (synth.uniform_policy(w.B, greedy=True) if self.pol is None else w.policy).numpy()
+        U = synth.host(w.weights.U) if w.weights.r else None
+        Wm = synth.host(w.weights.W) if w.weights.r else None
+        hh = synth.host(w.h) if w.h is not None else None
+        E = synth.host(w.weights.E) if w.h is not None else None
+        wc = w.weights.w_conf.cpu().numpy() if w.h is not None else None
+        done, b, t0 = 0, 0, time.perf_counter()
+        while True:
+            sl = slice(b, b + 1)
+            k = {n: v[sl] for n, v in keys.items()}
+            p = {n: v[sl] for n, v in pol.items()}
+            d = oracle.markov_sample(bb[sl], anchor[sl], U, Wm, None if hh is None else hh[sl], E, wc, p, **k)
+            oracle.verify(tg[sl], d["proposals"], d["q"], d["q_at_x"], p, **k)
+            done += 1
+            b = (b + 1) % w.B
+            el = time.perf_counter() - t0
+            if el >= budget_s or (max_requests and done >= max_requests):
+                break
+        pos = done * (w.gamma + 1)
+        return {"value": pos / el, "unit": UNIT, "cores": 1, "kind": "oracle",
+                "sample": f"{done} whole requests of the workload (draft of {w.gamma} rows + verify of "
+                          f"{w.gamma + 1} rows each; {pos} verified positions) in {el:.1f} s, "
+                          f"single-threaded C++ oracle"}
 
 
-def algorithmic_bytes(w):
-    """Bytes the method must move once: draft rows read (argmax), target rows
-    read, proposals / decisions written and read."""
-    esize = 2
-    draft = w.B * w.gamma * w.V * esize + w.B * 4 + w.B * w.gamma * (4 + 4)   # rows + anchor + props, q_at_x
-    verify = w.B * (w.gamma + 1) * w.V * esize + w.B * w.gamma * 4 + w.B * (w.gamma + 1) * 4 + w.B * 8
-    return draft, verify
+class Stats:
+    """Acceptance statistics of one batch of row pairs."""
+
+    def __init__(self, w, blocks=None):
+        self.w = w
+        self.name = "training_stats"
+        self.positions = w.N * w.gamma
+        self.blocks = blocks or w.N  # blocks of the workload (the CPU arm generates a subset)
+
+    def config(self):
+        w = self.w
+        return {"workload": self.name, "blocks": self.blocks, "gamma": w.gamma, "vocab": w.V,
+                "row_pairs": self.blocks * w.gamma, "dtype": "fp32"}
+
+    def setup(self, ds, dev):
+        w = self.w
+        self.ds = ds
+        self.ws = ds.Workspace()
+        N, g = w.N, w.gamma
+        self.out = dict(l1=torch.empty((N, g), dtype=torch.float32, device=dev),
+                        accept=torch.empty((N, g), dtype=torch.float32, device=dev),
+                        tau=torch.empty((N,), dtype=torch.float32, device=dev),
+                        loss_num=torch.empty((4,), dtype=torch.float64, device=dev),
+                        report=torch.empty((2,), dtype=torch.float64, device=dev),
+                        num_tokens=torch.empty((1,), dtype=torch.int64, device=dev),
+                        status=torch.empty((N,), dtype=torch.int32, device=dev))
+        self.inputs = [w.draft, w.target, w.labels, w.conf_logits]
+
+    def stats(self, stream, draft=None, target=None, labels=None, conf=None):
+        w = self.w
+        self.ds.accept_stats(draft if draft is not None else w.draft, target if target is not None else w.target,
+                             labels if labels is not None else w.labels, conf if conf is not None else w.conf_logits,
+                             workspace=self.ws, out=self.out, stream=stream)
+
+    def parts(self):
+        return [("stats", self.stats)]
+
+    def bytes(self):
+        w = self.w
+        return {"stats": 2 * w.N * w.gamma * w.V * 4 + w.N * w.gamma * 16 + w.N * 8 + 64}
+
+    def flops(self):
+        return {}
+
+    def e2e_step(self, stream, dev_inputs, host_inputs, host_outputs):
+        for d, h in zip(dev_inputs, host_inputs):
+            d.copy_(h, non_blocking=True)
+        self.stats(stream, *dev_inputs)
+        for h, d in zip(host_outputs, self.outputs()):
+            h.copy_(d, non_blocking=True)
+
+    def outputs(self):
+        return [self.out["loss_num"], self.out["report"], self.out["num_tokens"], self.out["tau"]]
+
+    def check(self):
+        assert int((self.out["status"] != 0).sum()) == 0
+
+    def cpu_sample(self, budget_s, max_requests=None):
+        import oracle
+        oracle.build()
+        w = self.w
+        done, n, t0 = 0, 0, time.perf_counter()
+        while True:
+            sl = slice(n, n + 1)
+            oracle.accept_stats(synth.host(w.draft[sl]), synth.host(w.target[sl]), w.labels[sl].cpu().numpy(),
+                                w.conf_logits[sl].cpu().numpy())
+            done += 1
+            n = (n + 1) % w.N
+            el = time.perf_counter() - t0
+            if el >= budget_s or (max_requests and done >= max_requests):
+                break
+        pos = done * w.gamma
+        return {"value": pos / el, "unit": UNIT, "cores": 1, "kind": "oracle",
+                "sample": f"{done} whole blocks ({pos} row pairs) of a {w.N}-block draw of the workload's "
+                          f"recipe in {el:.1f} s, single-threaded C++ oracle"}
 
 
+def make_workload(name, device):
+    if name == "full_decode_tile":
+        return Serving(name, synth.full_decode_tile(device=device), 2)
+    if name == "decode_verify_tile":
+        return Serving(name, synth.decode_verify_tile(device=device), 2)
+    if name == "mixed_serving":
+        return Serving(name, synth.mixed_serving(device=device), 2)
+    if name == "training_stats":
+        return Stats(synth.training_stats(device=device))
+    raise ValueError(name)
+
+
+WORKLOADS = ("full_decode_tile", "decode_verify_tile", "mixed_serving", "training_stats")
+
+
+# ------------------------------------------------------------------ GPU arm
 def run_gpu(args):
     import verify_dspark_markov_gb300 as ds
     from verify_dspark_markov_gb300 import build
@@ -142,21 +355,10 @@ def run_gpu(args):
         torch.distributed.barrier()
     ds.load()
 
-    w = make_workload(dev)
-    B, gamma, V = w.B, w.gamma, w.V
-    positions = B * (gamma + 1)
-    ws = ds.Workspace()
-    draft_out = dict(proposals=torch.empty((B, gamma), dtype=torch.int32, device=dev), q=None,
-                     q_at_x=torch.empty((B, gamma), dtype=torch.float32, device=dev), conf=None,
-                     status=torch.empty((B,), dtype=torch.int32, device=dev))
-    ver_out = (torch.empty((B, gamma + 1), dtype=torch.int32, device=dev),
-               torch.empty((B,), dtype=torch.int32, device=dev),
-               torch.empty((B,), dtype=torch.int32, device=dev))
+    wl = make_workload(args.workload, dev)
+    wl.setup(ds, dev)
     stream = torch.cuda.current_stream(dev)
-
-    def step():
-        ds.markov_sample(w.backbone, w.anchor, workspace=ws, out=draft_out, stream=stream)
-        ds.verify(w.target, draft_out["proposals"], workspace=ws, out=ver_out, stream=stream)
+    parts = wl.parts()
 
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush_r = torch.ones(max(2 * l2, 256 << 20) // 8, dtype=torch.int64, device=dev)
@@ -167,179 +369,160 @@ def run_gpu(args):
 
     for _ in range(args.warmup):
         flush_l2()
-        step()
+        for _, fn in parts:
+            fn(stream)
     torch.cuda.synchronize()
+    wl.check()
 
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    steps = args.steps
+    if args.max_seconds:  # keep the timed region near a minute for the big workloads
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _, fn in parts:
+            fn(stream)
+        b.record(stream)
+        b.synchronize()
+        steps = max(3, min(steps, int(args.max_seconds / max(a.elapsed_time(b) * 1e-3, 1e-6))))
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(parts) + 1)] for _ in range(steps)]
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     with Clocks(local) as clk:
-        time.sleep(0.3)                           # let the sampler start
+        time.sleep(0.3)  # let the sampler start
         t0 = time.perf_counter()
         w0 = time.time()
-        for i in range(args.steps):
+        for i in range(steps):
             flush_l2()
-            e = ev[i]
-            e[0].record(stream)
-            ds.markov_sample(w.backbone, w.anchor, workspace=ws, out=draft_out, stream=stream)
-            e[1].record(stream)
-            ds.verify(w.target, draft_out["proposals"], workspace=ws, out=ver_out, stream=stream)
-            e[2].record(stream)
+            ev[i][0].record(stream)
+            for j, (_, fn) in enumerate(parts):
+                fn(stream)
+                ev[i][j + 1].record(stream)
         torch.cuda.synchronize()
         wall = time.perf_counter() - t0
         w1 = time.time()
         time.sleep(0.1)
-    step_ms = [ev[i][0].elapsed_time(ev[i][2]) for i in range(args.steps)]
-    draft_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(args.steps)]
-    verify_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(args.steps)]
+    step_ms = [ev[i][0].elapsed_time(ev[i][-1]) for i in range(steps)]
+    part_ms = {name: float(np.mean([ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(steps)]))
+               for j, (name, _) in enumerate(parts)}
     ms = float(np.mean(step_ms))
     if world > 1:
         t = torch.tensor([ms], device=dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         ms = float(t.item())
 
-    # ---- end to end through the public API, host buffers, copies included
-    h_backbone = w.backbone.cpu().pin_memory()
-    h_target = w.target.cpu().pin_memory()
-    h_anchor = w.anchor.cpu().pin_memory()
-    d_backbone = torch.empty_like(w.backbone)
-    d_target = torch.empty_like(w.target)
-    d_anchor = torch.empty_like(w.anchor)
-    h_out = torch.empty((B, gamma + 1), dtype=torch.int32).pin_memory()
-    h_nacc = torch.empty((B,), dtype=torch.int32).pin_memory()
-    h_status = torch.empty((B,), dtype=torch.int32).pin_memory()
-
-    def e2e_step():
-        d_backbone.copy_(h_backbone, non_blocking=True)
-        d_anchor.copy_(h_anchor, non_blocking=True)
-        d_target.copy_(h_target, non_blocking=True)
-        ds.markov_sample(d_backbone, d_anchor, workspace=ws, out=draft_out, stream=stream)
-        ds.verify(d_target, draft_out["proposals"], workspace=ws, out=ver_out, stream=stream)
-        h_out.copy_(ver_out[0], non_blocking=True)
-        h_nacc.copy_(ver_out[1], non_blocking=True)
-        h_status.copy_(ver_out[2], non_blocking=True)
-
+    # ---- end to end through the public API: host inputs, copies included
+    host_in = [t.cpu().pin_memory() for t in wl.inputs]
+    dev_in = [torch.empty_like(t) for t in wl.inputs]
+    host_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in wl.outputs()]
     for _ in range(2):
-        e2e_step()
+        wl.e2e_step(stream, dev_in, host_in, host_out)
     torch.cuda.synchronize()
     e2e_ms = []
-    for _ in range(max(3, args.steps // 4)):
+    for _ in range(max(3, min(20, steps // 10))):
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        e2e_step()
+        wl.e2e_step(stream, dev_in, host_in, host_out)
         b.record(stream)
         b.synchronize()
         e2e_ms.append(a.elapsed_time(b))
-    h2d = h_backbone.numel() * 2 + h_target.numel() * 2 + h_anchor.numel() * 4
-    d2h = h_out.numel() * 4 + h_nacc.numel() * 4 + h_status.numel() * 4
-    assert int((ver_out[2] != 0).sum()) == 0, "unexpected request failures in the benchmark workload"
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
 
-    peak, peak_kind = peaks()
-    draft_b, verify_b = algorithmic_bytes(w)
-    vms = float(np.mean(verify_ms))
-    dms = float(np.mean(draft_ms))
-    achieved = (draft_b + verify_b) / ((vms + dms) * 1e-3) / 1e9
+    hbm, tflops_peak, peak_kind = peaks()
+    nbytes = wl.bytes()
+    flops = wl.flops()
+    dom = max(part_ms, key=part_ms.get)
+    achieved = nbytes[dom] / (part_ms[dom] * 1e-3) / 1e9
+    kernel = {"full_decode_tile": "argmax_rows_kernel<bf16> (draft + verify launches)",
+              "training_stats": "stats_pairs_kernel<f32> + stats_final_kernel"}.get(
+                  wl.name, {"draft": "markov_sample (markov_bias_kernel + markov_step_kernel per position)",
+                            "verify": "verify_rows_kernel<bf16>"}.get(dom, dom))
+    if wl.name == "full_decode_tile":  # the same kernel serves both parts: average over both launches
+        achieved = sum(nbytes.values()) / (sum(part_ms.values()) * 1e-3) / 1e9
     result = {
         "metric": METRIC,
-        "value": positions * world / (ms * 1e-3),
+        "value": wl.positions * world / (ms * 1e-3),
         "unit": UNIT,
         "n_gpus": world,
-        "steps": args.steps,
+        "steps": steps,
         "warmup": args.warmup,
         "ms_per_step": ms,
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16",
+        "dtype": "bf16" if wl.name != "training_stats" else "f32",
         "data": "synthetic",
-        "config": {"workload": "full_decode_tile", "requests": B, "gamma": gamma, "vocab": V,
-                   "target_rows": positions, "draft_rows": B * gamma, "policy": "greedy",
-                   "markov_rank": 0, "l2": "inputs larger than L2 (248 MB per step vs 135.5 MB), plus a 2 x L2 read of another buffer before every step",
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
-        "roofline": {"bound": "hbm", "kernel": "argmax_rows_kernel<bf16>",
-                     "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "peak_kind": peak_kind, "traffic": None,
-                     "bytes_per_step": draft_b + verify_b},
-        "parts_ms": {"draft_argmax": dms, "verify": vms,
-                     "verify_GBps": verify_b / (vms * 1e-3) / 1e9,
-                     "draft_GBps": draft_b / (dms * 1e-3) / 1e9},
-        "e2e": {"value": positions * world / (float(np.mean(e2e_ms)) * 1e-3), "unit": UNIT,
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": float(np.mean(e2e_ms))},
-        "gpu_launches": 2 * args.steps,
+        "config": dict(wl.config(), l2="inputs larger than L2, plus a 2 x L2 read of another buffer "
+                                       "before every step",
+                       parallelism=f"replicas x{world}" if world > 1 else "single GPU"),
+        "roofline": {"bound": "hbm", "kernel": kernel, "part": dom, "achieved": achieved, "peak": hbm,
+                     "unit": "GB/s", "frac": achieved / hbm, "peak_kind": peak_kind, "traffic": None,
+                     "bytes_per_step": sum(nbytes.values())},
+        "parts_ms": part_ms,
+        "parts_GBps": {k: nbytes[k] / (part_ms[k] * 1e-3) / 1e9 for k in part_ms},
+        "e2e": {"value": wl.positions * world / (float(np.mean(e2e_ms)) * 1e-3), "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": float(np.mean(e2e_ms))},
         "clocks": clk.summary(w0, w1),
         "wall_s_timed_region": wall,
     }
+    if flops.get("draft"):
+        t = flops["draft"] / (part_ms["draft"] * 1e-3) / 1e12
+        result["tensor"] = {"part": "draft (markov_bias_kernel, tcgen05)", "achieved": t,
+                            "peak": tflops_peak, "unit": "TFLOP/s", "frac": t / tflops_peak,
+                            "note": "FLOPs of the bias GEMM over the whole draft part's time"}
+    if isinstance(wl, Serving):
+        g = wl.w.gamma
+        if wl.name == "full_decode_tile":
+            launches = 2
+        else:
+            launches = (2 * g if wl.w.weights.r else g) + (1 if wl.w.h is not None else 0) + 1
+    else:
+        launches = 2
+    result["gpu_launches"] = launches * steps
     traffic = os.path.join(ROOT, "profiles", "traffic.json")
     if os.path.exists(traffic):
         with open(traffic) as f:
-            t = json.load(f).get("argmax_rows_kernel<bf16>:full_decode_tile")
-        if t:
-            result["roofline"]["traffic"] = t
+            tr = json.load(f).get(wl.name)
+        if tr:
+            result["roofline"]["traffic"] = tr
     if rank == 0 and not args.no_cpu_baseline:
-        result["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_seconds)
+        result["cpu_baseline"] = wl.cpu_sample(args.cpu_seconds)
     if world > 1:
         torch.distributed.barrier()
         torch.distributed.destroy_process_group()
     return result if rank == 0 else None
 
 
-# ------------------------------------------------------------ CPU (oracle)
-def cpu_baseline(w, budget_s=12.0, max_requests=None):
-    """The oracle, as it stands, on a bounded sample of the same workload:
-    whole requests (draft argmax of gamma rows + greedy verify of gamma+1
-    rows), single-threaded."""
-    import oracle
-    oracle.build()
-    B = w.B
-    bb = synth.host(w.backbone)
-    tg = synth.host(w.target)
-    anchor = w.anchor.cpu().numpy()
-    keys = w.keys.numpy()
-    pol = synth.uniform_policy(B, greedy=True).numpy()
-    done = 0
-    t0 = time.perf_counter()
-    b = 0
-    while True:
-        sl = slice(b, b + 1)
-        k = {n: v[sl] for n, v in keys.items()}
-        p = {n: v[sl] for n, v in pol.items()}
-        d = oracle.markov_sample(bb[sl], anchor[sl], None, None, None, None, None, p, **k)
-        oracle.verify(tg[sl], d["proposals"], None, None, p, **k)
-        done += 1
-        b = (b + 1) % B
-        el = time.perf_counter() - t0
-        if el >= budget_s or (max_requests and done >= max_requests):
-            break
-    positions = done * (w.gamma + 1)
-    return {"value": positions / el, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{done} whole requests of the workload ({positions} verified positions, "
-                      f"{done * w.gamma} draft rows) in {el:.1f} s, single-threaded C++ oracle"}
+# ------------------------------------------------------------ reference arm
+def make_workload_small(name):
+    """The workload generated on the CPU for the oracle-only reference arm
+    (the training statistics for 64 of its 4096 blocks)."""
+    if name == "training_stats":
+        return Stats(synth.training_stats(device="cpu", N=64), blocks=4096)
+    return make_workload(name, "cpu")
 
 
 def run_reference(args):
+    """The CPU oracle, as it stands, on bounded samples of the workload."""
     rank, world, local = dist_env()
     if rank != 0:
         return None
-    w = make_workload("cpu")
-    per_step = []
+    wl = make_workload_small(args.workload)
     for _ in range(args.warmup):
-        cpu_baseline(w, budget_s=0.0, max_requests=1)
+        wl.cpu_sample(0.0, max_requests=1)
+    per, t_steps = [], []
     for _ in range(args.steps):
-        r = cpu_baseline(w, budget_s=min(10.0, args.cpu_seconds), max_requests=4)
-        per_step.append(r)
-    value = float(np.mean([r["value"] for r in per_step]))
-    cores = 1
+        t0 = time.perf_counter()
+        per.append(wl.cpu_sample(min(10.0, args.cpu_seconds), max_requests=4))
+        t_steps.append(time.perf_counter() - t0)
+    value = float(np.mean([r["value"] for r in per]))
     return {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": (w.gamma + 1) * 4 / value * 1e3,
+            "warmup": args.warmup, "ms_per_step": float(np.mean(t_steps)) * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "impl": "reference",
-            "config": {"workload": "full_decode_tile", "requests": w.B, "gamma": w.gamma,
-                       "vocab": w.V, "target_rows": w.B * (w.gamma + 1), "policy": "greedy",
-                       "markov_rank": 0, "parallelism": "single CPU thread"},
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
-                             "sample": "4 whole requests per step (draft argmax + greedy verify)"},
+            "config": dict(wl.config(), parallelism="single CPU thread"),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": per[-1]["sample"] + " per step"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
@@ -349,6 +532,9 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--workload", default="full_decode_tile", choices=WORKLOADS)
+    ap.add_argument("--max-seconds", type=float, default=30.0,
+                    help="cap on the timed region's GPU time (fewer steps for slow workloads)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

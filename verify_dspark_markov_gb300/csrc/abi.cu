@@ -51,7 +51,7 @@ VerifyLayout verify_layout(int B, int gamma) {
 }
 
 // Largest vocabulary the row engine holds in one cluster's shared memory.
-bool policy_vocab_ok(int V) { return policy_slice(V) * sizeof(float) <= 200 * 1024; }
+bool policy_vocab_ok(int V) { return policy_smem_bytes(V, 0) <= 200 * 1024; }
 
 struct MarkovLayout {
     ArgmaxScratch greedy;

@@ -65,7 +65,7 @@ struct RowRecord {  // the policy of one target row, for the request's decision
     float p_x;        // p of the proposal this row scores
     int32_t status;
     int32_t argmax;
-    int32_t pad;
+    int32_t count;    // support size
 };
 struct VerifyProbParams {
     const void* target;
@@ -123,6 +123,7 @@ int markov_gemm_smem(int r, int N);
 cudaError_t launch_markov_bias(const MarkovGemmParams& p, int grid, cudaStream_t stream);
 int policy_cluster_size();
 int policy_slice(int V);
+int policy_smem_bytes(int V, int store_bf16);
 cudaError_t launch_verify_prob(const VerifyProbParams& p, cudaStream_t stream);
 cudaError_t launch_markov_step(const MarkovStepParams& p, cudaStream_t stream);
 

@@ -24,7 +24,7 @@ namespace dspark {
 
 namespace {
 
-constexpr int kThreads = 128;
+constexpr int kThreads = 256;  // 8 warps: all stage operands; two per TMEM lane quadrant read back
 constexpr int kTileM = 128;
 
 __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
@@ -83,6 +83,15 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// 16-byte asynchronous copy global -> shared (no register staging), so that
+// a thread keeps many copies in flight while staging an operand tile.
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)), "l"(gsrc) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
 // Byte offset of element (row, k) in the canonical no-swizzle K-major layout
 // with K columns: 8-row x 8-element core matrices, K-adjacent ones 128 B
 // apart, row-group-adjacent ones 16 * K bytes apart.
@@ -137,10 +146,12 @@ __global__ void __launch_bounds__(kThreads, 1) markov_bias_kernel(const MarkovGe
         // A operand: W rows v0 .. v0+127, zero past the vocabulary
         for (int c = tid; c < kTileM * kchunks; c += kThreads) {
             const int m = c / kchunks, kc = c % kchunks;
-            uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            if (v0 + m < p.V) v = ld_stream_v4(p.W + static_cast<int64_t>(v0 + m) * r + kc * 8);
-            *reinterpret_cast<uint4*>(sA + canon_off(m, kc, r)) = v;
+            if (v0 + m < p.V)
+                cp_async16(sA + canon_off(m, kc, r), p.W + static_cast<int64_t>(v0 + m) * r + kc * 8);
+            else
+                *reinterpret_cast<uint4*>(sA + canon_off(m, kc, r)) = make_uint4(0u, 0u, 0u, 0u);
         }
+        cp_async_wait_all();
         fence_proxy_async_smem();
         __syncthreads();
         if (tid == 0) {
@@ -157,11 +168,13 @@ __global__ void __launch_bounds__(kThreads, 1) markov_bias_kernel(const MarkovGe
         phase ^= 1u;
         if (!ok) s_timeout = 1;
         tc_fence_after();
-        // epilogue: lane = vocabulary entry v0 + 32w + lane, columns = requests
-        const int v = v0 + warp * 32 + lane;
-        for (int c0 = 0; c0 < N; c0 += 16) {
+        // epilogue: warp w reads TMEM lane quadrant w % 4 (vocabulary entries
+        // v0 + 32 (w % 4) + lane) and every other 16-column group from w / 4
+        const int quad = warp & 3;
+        const int v = v0 + quad * 32 + lane;
+        for (int c0 = (warp >> 2) * 16; c0 < N; c0 += 32) {
             float acc[16];
-            tmem_ld16(tmem + (static_cast<uint32_t>(warp * 32) << 16) + static_cast<uint32_t>(c0), acc);
+            tmem_ld16(tmem + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(c0), acc);
             if (v < p.V) {
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {

@@ -30,22 +30,34 @@ __device__ __forceinline__ float inv_mass(uint64_t mass) {
     return static_cast<float>(rp::kFix / static_cast<double>(mass));
 }
 
+// Dynamic shared memory: the row slice (bf16 or fp32), then the candidate
+// buffer (used in rank 0).
+__host__ __device__ constexpr int slice_bytes(int slice, int store_bf16) {
+    return ((slice * (store_bf16 ? 2 : 4)) + 15) / 16 * 16;
+}
+
 template <int kDtype>
 __global__ void __cluster_dims__(rp::kC, 1, 1) __launch_bounds__(rp::kThreads)
     verify_rows_kernel(const VerifyProbParams p) {
-    extern __shared__ __align__(16) float zs[];
+    extern __shared__ __align__(16) unsigned char dyn[];
     __shared__ rp::Smem sm;
     __shared__ float s_px;          // p(x) of this row's proposal, in its owner CTA
     __shared__ int32_t s_last;      // rank 0: this cluster decides the request
-    __shared__ int32_t s_plan[4];   // rank 0: (row to sample, residual?, token, status)
+    __shared__ int32_t s_plan[4];   // rank 0: (row to draw from, rejected position, token, -)
+    __shared__ int32_t s_bcast[4];
     cg::cluster_group cl = cg::this_cluster();
     const int rank = static_cast<int>(cl.block_rank());
     const int tid = threadIdx.x;
+    constexpr int kStoreBf16 = kDtype == kBF16;
+    void* zs = dyn;
+    unsigned long long* cbuf = reinterpret_cast<unsigned long long*>(dyn + slice_bytes(p.slice, kStoreBf16));
     if (tid == 0) {
         sm.parity = 0;
         sm.hparity = 0;
         s_px = 0.0f;
         s_last = 0;
+        s_plan[0] = -1;
+        s_plan[1] = 0;
     }
     __syncthreads();
 
@@ -54,7 +66,7 @@ __global__ void __cluster_dims__(rp::kC, 1, 1) __launch_bounds__(rp::kThreads)
     const int b = static_cast<int>(row / rows), i = static_cast<int>(row % rows);
     const int lo = rank * p.slice;
     const int n = max(0, min(p.slice, p.V - lo));
-    rp::Slice sl{zs, lo, n, (n + kThreads - 1) / kThreads};
+    rp::Slice sl{zs, lo, n, (n + kThreads - 1) / kThreads, kStoreBf16};
     const int esize = kDtype == kBF16 ? 2 : 4;
     const char* tgt = static_cast<const char*>(p.target);
 
@@ -64,7 +76,9 @@ __global__ void __cluster_dims__(rp::kC, 1, 1) __launch_bounds__(rp::kThreads)
     bool bad;
     rp::load_slice_and_max<kDtype>(sm, cl, tgt + row * p.V * esize, lo, n, zs, res, bad);
     res.status = bad ? kReqNonfinite : (res.argmax < 0 ? kReqEmpty : (pol_ok ? kReqOk : kReqBadPolicy));
-    if (res.status == kReqOk) rp::row_policy(sm, cl, sl, p.V, pol, res);
+    res.count = 1;
+    res.in_buf = 0;
+    if (res.status == kReqOk) rp::row_policy(sm, cl, sl, p.V, pol, res, cbuf);
 
     // p(x) of the proposal scored by this row (rows 0..gamma-1), in its owner CTA
     int32_t x = -1;
@@ -72,7 +86,7 @@ __global__ void __cluster_dims__(rp::kC, 1, 1) __launch_bounds__(rp::kThreads)
     const bool x_ok = x >= 0 && x < p.V;
     const int owner = x_ok ? x / p.slice : 0;
     if (res.status == kReqOk && !pol.greedy && x_ok && rank == owner && tid == 0) {
-        const float z = zs[x - lo];
+        const float z = sl.val(x - lo);
         s_px = rp::in_set(ordered_key(z), x, res.tau, res.cut)
                    ? rp::weight_f(z, res.zmax, pol.inv_t) * inv_mass(res.mass)
                    : 0.0f;
@@ -88,13 +102,15 @@ __global__ void __cluster_dims__(rp::kC, 1, 1) __launch_bounds__(rp::kThreads)
         rec.p_x = (x_ok && !pol.greedy) ? *cl.map_shared_rank(&s_px, owner) : 0.0f;
         rec.status = res.status;
         rec.argmax = res.argmax;
+        rec.count = res.count;
         p.records[row] = rec;
         const unsigned old = atom_add_acq_rel(p.ticket + b, 1u);
         s_last = old == static_cast<unsigned>(rows - 1);
     }
     cl.sync();
-    const bool last = *cl.map_shared_rank(&s_last, 0) != 0;
-    if (!last) {
+    if (tid == 0) s_bcast[0] = *cl.map_shared_rank(&s_last, 0);
+    __syncthreads();
+    if (s_bcast[0] == 0) {
         cl.sync();  // keep this CTA's shared memory alive for the cluster's readers
         return;
     }
@@ -112,8 +128,6 @@ __global__ void __cluster_dims__(rp::kC, 1, 1) __launch_bounds__(rp::kThreads)
         if (status == kReqOk)
             for (int r = 0; r < rows; ++r)
                 if (rec[r].status != kReqOk) { status = rec[r].status; break; }
-        s_plan[0] = -1;
-        s_plan[3] = status;
         if (status != kReqOk) {
             for (int r = 0; r < rows; ++r) out[r] = -1;
             p.num_accepted[b] = -1;
@@ -140,8 +154,9 @@ __global__ void __cluster_dims__(rp::kC, 1, 1) __launch_bounds__(rp::kThreads)
         }
     }
     cl.sync();
-    const int32_t* plan = cl.map_shared_rank(s_plan, 0);
-    const int R = plan[0], j = plan[1];
+    if (tid < 2) s_bcast[1 + tid] = cl.map_shared_rank(s_plan, 0)[tid];
+    __syncthreads();
+    const int R = s_bcast[1], j = s_bcast[2];
     if (R >= 0) {
         // draw the residual / bonus token from target row R of request b
         const RowRecord rr = p.records[static_cast<int64_t>(b) * rows + R];
@@ -150,49 +165,58 @@ __global__ void __cluster_dims__(rp::kC, 1, 1) __launch_bounds__(rp::kThreads)
         bool unused_bad;
         rp::load_slice_and_max<kDtype>(sm, cl, tgt + trow * p.V * esize, lo, n, zs, unused, unused_bad);
         const float invS = inv_mass(rr.mass);
-        auto p_of = [&](int li) {
-            const float z = zs[li];
-            return rp::in_set(ordered_key(z), lo + li, rr.tau, rr.cut) ? rp::weight_f(z, rr.zmax, rr.inv_t) * invS
-                                                                       : 0.0f;
-        };
+        const float* qrow = j ? p.q + (static_cast<int64_t>(b) * p.gamma + (j - 1)) * p.V : nullptr;
         const int64_t pos = p.pos0[b] + (j ? j : p.gamma + 1);
         const uint32_t m24 = uniform_bits24(p.seed[b], p.request_id[b], pos, 2);
+        // p of a support element, its fixed-point weight and residual weight
+        auto pw = [&](uint32_t key) { return rp::to_fixed(rp::weight_f(key_to_float(key), rr.zmax, rr.inv_t)); };
+        auto resid = [&](uint32_t key, int32_t idx) {
+            const float pv = rp::weight_f(key_to_float(key), rr.zmax, rr.inv_t) * invS;
+            return rp::to_fixed(fmaxf(pv - qrow[idx], 0.0f));
+        };
         int32_t token = -1;
-        unsigned long long total = 0;
-        if (j) {
-            // residual weights max(p - q_j, 0), formed in a coalesced pass over the
-            // slice and kept in place of the logits
-            const float* qrow = p.q + (static_cast<int64_t>(b) * p.gamma + (j - 1)) * p.V + lo;
-            __syncthreads();
-            for (int li = tid; li < n; li += kThreads) {
-                const float pv = p_of(li);
-                const float qv = qrow[li];
-                zs[li] = fmaxf(pv - qv, 0.0f);  // overwrites only this thread's own element
-            }
-            __syncthreads();
-            token = rp::sample_fixed(sm, cl, sl, m24, [&](int li) { return rp::to_fixed(zs[li]); }, total);
-            if (total == 0) {  // no residual mass left (round-off): draw from p itself
-                rp::load_slice_and_max<kDtype>(sm, cl, tgt + trow * p.V * esize, lo, n, zs, unused, unused_bad);
-                token = rp::sample_fixed(
-                    sm, cl, sl, m24,
-                    [&](int li) {
-                        const float z = zs[li];
-                        return rp::in_set(ordered_key(z), lo + li, rr.tau, rr.cut)
-                                   ? rp::to_fixed(rp::weight_f(z, rr.zmax, rr.inv_t))
-                                   : 0ull;
-                    },
-                    total);
+        if (rr.count <= rp::kCap) {
+            // small support: gathered in rank 0, drawn in token order
+            const int cnt = rp::compact_to_rank0(sm, cl, sl, cbuf, [&](uint32_t key, int32_t idx) {
+                return rp::in_set(key, idx, rr.tau, rr.cut);
+            });
+            if (rank == 0) {
+                unsigned long long total = 0;
+                if (j) {
+                    token = rp::draw_small_support(sm, cbuf, cnt, m24, resid, total);
+                    if (total == 0) {  // no residual mass left (round-off): draw from p itself
+                        for (int e = tid; e < cnt; e += kThreads) {  // back to value-order keys
+                            const unsigned long long c = cbuf[e];
+                            cbuf[e] = rp::value_order(rp::io_key(c), rp::io_idx(c));
+                        }
+                        __syncthreads();
+                        token = rp::draw_small_support(sm, cbuf, cnt, m24,
+                                                       [&](uint32_t key, int32_t) { return pw(key); }, total);
+                    }
+                } else {
+                    token = rp::draw_small_support(sm, cbuf, cnt, m24, [&](uint32_t key, int32_t) { return pw(key); },
+                                                   total);
+                }
             }
         } else {
-            token = rp::sample_fixed(
-                sm, cl, sl, m24,
-                [&](int li) {
-                    const float z = zs[li];
-                    return rp::in_set(ordered_key(z), lo + li, rr.tau, rr.cut)
-                               ? rp::to_fixed(rp::weight_f(z, rr.zmax, rr.inv_t))
-                               : 0ull;
-                },
-                total);
+            // the whole vocabulary: a draw over every CTA's slice
+            unsigned long long total = 0;
+            auto in_sup = [&](int li, float z) { return rp::in_set(ordered_key(z), lo + li, rr.tau, rr.cut); };
+            if (j) {
+                token = rp::sample_fixed(sm, cl, sl, m24,
+                                         [&](int li) {
+                                             const float z = sl.val(li);
+                                             return in_sup(li, z) ? resid(ordered_key(z), lo + li) : 0ull;
+                                         },
+                                         total);
+            }
+            if (!j || total == 0)
+                token = rp::sample_fixed(sm, cl, sl, m24,
+                                         [&](int li) {
+                                             const float z = sl.val(li);
+                                             return in_sup(li, z) ? pw(ordered_key(z)) : 0ull;
+                                         },
+                                         total);
         }
         if (rank == 0 && tid == 0) {
             out[R] = token;
@@ -206,9 +230,10 @@ __global__ void __cluster_dims__(rp::kC, 1, 1) __launch_bounds__(rp::kThreads)
 template <int kDtype>
 __global__ void __cluster_dims__(rp::kC, 1, 1) __launch_bounds__(rp::kThreads)
     markov_step_kernel(const MarkovStepParams p) {
-    extern __shared__ __align__(16) float zs[];
+    extern __shared__ __align__(16) unsigned char dyn[];
     __shared__ rp::Smem sm;
     __shared__ float s_qx;
+    __shared__ int32_t s_x;
     cg::cluster_group cl = cg::this_cluster();
     const int rank = static_cast<int>(cl.block_rank());
     const int tid = threadIdx.x;
@@ -216,6 +241,7 @@ __global__ void __cluster_dims__(rp::kC, 1, 1) __launch_bounds__(rp::kThreads)
         sm.parity = 0;
         sm.hparity = 0;
         s_qx = 0.0f;
+        s_x = -1;
     }
     __syncthreads();
 
@@ -240,27 +266,23 @@ __global__ void __cluster_dims__(rp::kC, 1, 1) __launch_bounds__(rp::kThreads)
         }
         return;
     }
+    const bool z_bf16 = !p.zbuf && kDtype == kBF16;
     const int lo = rank * p.slice;
     const int n = max(0, min(p.slice, p.V - lo));
-    rp::Slice sl{zs, lo, n, (n + kThreads - 1) / kThreads};
+    void* zs = dyn;
+    unsigned long long* cbuf = reinterpret_cast<unsigned long long*>(dyn + slice_bytes(p.slice, z_bf16));
+    rp::Slice sl{zs, lo, n, (n + kThreads - 1) / kThreads, z_bf16 ? 1 : 0};
     rp::Policy pol;
     const bool pol_ok = p.policy ? rp::make_policy(p.policy[b], p.V, pol)
                                  : (pol = rp::Policy{1.0f, 0, 1.0f, 1}, true);
-    const void* zrow;
-    int zdtype;
-    if (p.zbuf) {  // logits with the Markov bias, fp32 [B, V]
-        zrow = p.zbuf + static_cast<int64_t>(b) * p.V;
-        zdtype = kF32;
-    } else {
-        zrow = static_cast<const char*>(p.backbone) + pidx * p.V * (kDtype == kBF16 ? 2 : 4);
-        zdtype = kDtype;
-    }
     rp::RowResult res;
     bool bad;
-    if (zdtype == kF32)
-        rp::load_slice_and_max<kF32>(sm, cl, zrow, lo, n, zs, res, bad);
+    if (p.zbuf)  // logits with the Markov bias, fp32 [B, V]
+        rp::load_slice_and_max<kF32>(sm, cl, p.zbuf + static_cast<int64_t>(b) * p.V, lo, n, zs, res, bad);
     else
-        rp::load_slice_and_max<kBF16>(sm, cl, zrow, lo, n, zs, res, bad);
+        rp::load_slice_and_max<kDtype>(
+            sm, cl, static_cast<const char*>(p.backbone) + pidx * p.V * (kDtype == kBF16 ? 2 : 4), lo, n, zs, res,
+            bad);
     res.status = bad ? kReqNonfinite : (res.argmax < 0 ? kReqEmpty : (pol_ok ? kReqOk : kReqBadPolicy));
     if (res.status != kReqOk) {
         if (rank == 0 && tid == 0) {
@@ -271,38 +293,76 @@ __global__ void __cluster_dims__(rp::kC, 1, 1) __launch_bounds__(rp::kThreads)
         cl.sync();
         return;
     }
-    rp::row_policy(sm, cl, sl, p.V, pol, res);
-    int32_t xk;
+    res.count = 1;
+    res.in_buf = 0;
+    rp::row_policy(sm, cl, sl, p.V, pol, res, cbuf);
     if (pol.greedy) {
-        xk = res.argmax;
-        if (rank == 0 && tid == 0) s_qx = 1.0f;
+        if (rank == 0 && tid == 0) {
+            s_x = res.argmax;
+            s_qx = 1.0f;
+        }
     } else {
         const float invS = inv_mass(res.mass);
         float* qrow = p.q + pidx * p.V + lo;
         for (int li = tid; li < n; li += kThreads) {
-            const float z = zs[li];
+            const float z = sl.val(li);
             qrow[li] = rp::in_set(ordered_key(z), lo + li, res.tau, res.cut) ? rp::weight_f(z, res.zmax, pol.inv_t) * invS
                                                                                : 0.0f;
         }
         const uint32_t m24 = uniform_bits24(p.seed[b], p.request_id[b], p.pos0[b] + k, 0);
-        unsigned long long total = 0;
-        xk = rp::sample_fixed(
-            sm, cl, sl, m24,
-            [&](int li) {
-                const float z = zs[li];
-                return rp::in_set(ordered_key(z), lo + li, res.tau, res.cut)
-                           ? rp::to_fixed(rp::weight_f(z, res.zmax, pol.inv_t))
-                           : 0ull;
-            },
-            total);
-        if (xk >= lo && xk < lo + n && tid == 0)
-            s_qx = rp::weight_f(zs[xk - lo], res.zmax, pol.inv_t) * invS;
+        if (res.in_buf) {
+            // the support is rank 0's first res.count candidates
+            if (rank == 0) {
+                unsigned long long total = 0;
+                const int32_t xk = rp::draw_small_support(
+                    sm, cbuf, res.count, m24,
+                    [&](uint32_t key, int32_t) {
+                        return rp::to_fixed(rp::weight_f(key_to_float(key), res.zmax, pol.inv_t));
+                    },
+                    total);
+                if (tid == 0) {
+                    s_x = xk;
+                    s_qx = 0.0f;
+                }
+                __syncthreads();
+                if (tid == 0) {
+                    // q(x): the weight of x over the support mass
+                    for (int e = 0; e < res.count; ++e)
+                        if (rp::io_idx(cbuf[e]) == xk) {
+                            s_qx = rp::weight_f(key_to_float(rp::io_key(cbuf[e])), res.zmax, pol.inv_t) * invS;
+                            break;
+                        }
+                }
+            }
+        } else {
+            unsigned long long total = 0;
+            const int32_t xk = rp::sample_fixed(
+                sm, cl, sl, m24,
+                [&](int li) {
+                    const float z = sl.val(li);
+                    return rp::in_set(ordered_key(z), lo + li, res.tau, res.cut)
+                               ? rp::to_fixed(rp::weight_f(z, res.zmax, pol.inv_t))
+                               : 0ull;
+                },
+                total);
+            if (xk >= lo && xk < lo + n && tid == 0) {
+                s_x = xk;
+                s_qx = rp::weight_f(sl.val(xk - lo), res.zmax, pol.inv_t) * invS;
+            }
+        }
     }
     cl.sync();
     if (rank == 0 && tid == 0) {
-        const int owner = pol.greedy ? 0 : xk / p.slice;
+        // the rank holding the draw's results: 0 for greedy / small supports,
+        // the owner of x for a draw over every slice
+        int src = 0;
+        if (!pol.greedy && !res.in_buf) {
+            for (int r = 0; r < kC; ++r)
+                if (*cl.map_shared_rank(&s_x, r) >= 0) { src = r; break; }
+        }
+        const int32_t xk = *cl.map_shared_rank(&s_x, src);
         p.proposals[pidx] = xk;
-        p.q_at_x[pidx] = *cl.map_shared_rank(&s_qx, owner);
+        p.q_at_x[pidx] = *cl.map_shared_rank(&s_qx, src);
         if (k == 1) p.status[b] = kReqOk;
     }
     cl.sync();
@@ -319,8 +379,12 @@ int policy_cluster_size() { return kC; }
 
 int policy_slice(int V) { return ((V + kC - 1) / kC + 7) / 8 * 8; }
 
+int policy_smem_bytes(int V, int store_bf16) {
+    return slice_bytes(policy_slice(V), store_bf16) + rp::kCap * static_cast<int>(sizeof(unsigned long long));
+}
+
 cudaError_t launch_verify_prob(const VerifyProbParams& p, cudaStream_t stream) {
-    const int smem = p.slice * static_cast<int>(sizeof(float));
+    const int smem = policy_smem_bytes(p.V, p.dtype == kBF16);
     const dim3 grid(static_cast<unsigned>(static_cast<int64_t>(p.B) * (p.gamma + 1) * kC));
     cudaError_t e;
     if (p.dtype == kBF16) {
@@ -334,7 +398,7 @@ cudaError_t launch_verify_prob(const VerifyProbParams& p, cudaStream_t stream) {
 }
 
 cudaError_t launch_markov_step(const MarkovStepParams& p, cudaStream_t stream) {
-    const int smem = p.slice * static_cast<int>(sizeof(float));
+    const int smem = policy_smem_bytes(p.V, !p.zbuf && p.dtype == kBF16);
     const dim3 grid(static_cast<unsigned>(p.B * kC));
     cudaError_t e;
     if (p.dtype == kBF16) {

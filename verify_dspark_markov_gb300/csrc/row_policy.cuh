@@ -34,6 +34,8 @@ constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kBins = 256;      // 8-bit radix digits
 constexpr int kWin = 8;         // candidate window widths
+constexpr int kCap = 2048;      // candidate buffer of rank 0 (composite keys)
+constexpr int kSample = 8;      // 1 in kSample elements feeds the window estimate
 constexpr double kFix = 1099511627776.0;  // 2^40: fixed-point scale of the weights
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -66,6 +68,9 @@ struct RowResult {
     uint32_t tau;       // support = {key > tau} + {key == tau, index <= cut}
     int32_t cut;
     uint64_t mass;      // sum of fixed-point weights over the support
+    int32_t count;      // support size
+    int32_t in_buf;     // 1: the support's composite keys are the first `count` of
+                        // rank 0's candidate buffer, sorted by (key desc, index asc)
 };
 
 // Shared state of one CTA of the engine (static shared memory).
@@ -76,6 +81,8 @@ struct Smem {
     uint32_t hcnt[2][kBins];
     unsigned long long hmass[2][kBins];
     unsigned long long wu[kWarps][kWin + 2];  // per-warp partials
+    unsigned long long gat[kC][kWin + 2];     // slots gathered from the cluster's ranks
+    unsigned long long tot[kWin + 2];         // their combination, for every thread
     unsigned long long scan_u[kWarps];
     int32_t pick[4];
     int parity;      // which exchange buffer is next
@@ -107,12 +114,20 @@ __device__ __forceinline__ void cluster_sum_u64(Smem& sm, cg::cluster_group& cl,
         sm.xu[buf][threadIdx.x] = t;
     }
     cl.sync();
-#pragma unroll
-    for (int i = 0; i < kN; ++i) {
-        unsigned long long t = 0;
-        for (int r = 0; r < kC; ++r) t += cl.map_shared_rank(&sm.xu[buf][0], r)[i];
-        out[i] = t;
+    // one remote load per (rank, value) pair, then one combination per value
+    if (threadIdx.x < kC * kN) {
+        const int r = threadIdx.x / kN, i = threadIdx.x % kN;
+        sm.gat[r][i] = cl.map_shared_rank(&sm.xu[buf][0], r)[i];
     }
+    __syncthreads();
+    if (threadIdx.x < kN) {
+        unsigned long long t = 0;
+        for (int r = 0; r < kC; ++r) t += sm.gat[r][threadIdx.x];
+        sm.tot[threadIdx.x] = t;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < kN; ++i) out[i] = sm.tot[i];
     __syncthreads();
     if (threadIdx.x == 0) sm.parity ^= 1;
     __syncthreads();
@@ -145,14 +160,23 @@ __device__ __forceinline__ void cluster_max_u64(Smem& sm, cg::cluster_group& cl,
         sm.xu[buf][1] = f;
     }
     cl.sync();
-    unsigned long long m = 0, f = 0;
-    for (int r = 0; r < kC; ++r) {
-        const unsigned long long* x = cl.map_shared_rank(&sm.xu[buf][0], r);
-        m = x[0] > m ? x[0] : m;
-        f |= x[1];
+    if (threadIdx.x < 2 * kC) {
+        const int r = threadIdx.x >> 1, i = threadIdx.x & 1;
+        sm.gat[r][i] = cl.map_shared_rank(&sm.xu[buf][0], r)[i];
     }
-    out_max = m;
-    out_flags = f;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        unsigned long long m = 0, f = 0;
+        for (int r = 0; r < kC; ++r) {
+            m = sm.gat[r][0] > m ? sm.gat[r][0] : m;
+            f |= sm.gat[r][1];
+        }
+        sm.tot[0] = m;
+        sm.tot[1] = f;
+    }
+    __syncthreads();
+    out_max = sm.tot[0];
+    out_flags = sm.tot[1];
     __syncthreads();
     if (threadIdx.x == 0) sm.parity ^= 1;
     __syncthreads();
@@ -166,8 +190,10 @@ __device__ __forceinline__ void cluster_gather_u64(Smem& sm, cg::cluster_group& 
     const int buf = sm.parity;
     if (threadIdx.x == 0) sm.xu[buf][0] = mine;
     cl.sync();
+    if (threadIdx.x < kC) sm.gat[threadIdx.x][0] = cl.map_shared_rank(&sm.xu[buf][0], threadIdx.x)[0];
+    __syncthreads();
 #pragma unroll
-    for (int r = 0; r < kC; ++r) totals[r] = cl.map_shared_rank(&sm.xu[buf][0], r)[0];
+    for (int r = 0; r < kC; ++r) totals[r] = sm.gat[r][0];
     __syncthreads();
     if (threadIdx.x == 0) sm.parity ^= 1;
     __syncthreads();
@@ -189,11 +215,17 @@ __device__ __forceinline__ unsigned long long block_scan_u64(Smem& sm, unsigned 
     return x + base;
 }
 
-// The slice [lo, lo + n) of the row held by this CTA, as fp32 in shared memory.
+// The slice [lo, lo + n) of the row held by this CTA in shared memory, stored
+// as bf16 (for bf16 inputs: half the footprint, more rows in flight) or fp32.
 struct Slice {
-    const float* z;
+    const void* z;
     int lo, n;
-    int per;  // contiguous elements per thread for ordered scans
+    int per;   // contiguous elements per thread for ordered scans
+    int bf16;  // storage format
+    __device__ __forceinline__ float val(int i) const {
+        return bf16 ? __uint_as_float(static_cast<uint32_t>(static_cast<const uint16_t*>(z)[i]) << 16)
+                    : static_cast<const float*>(z)[i];
+    }
 };
 
 // Radix selection on keys: among elements matching `pred` with key in the
@@ -215,7 +247,7 @@ __device__ bool radix_select(Smem& sm, cg::cluster_group& cl, const Slice& sl, u
     if (hi_bit == 0) {  // a single key in the window: count it
         unsigned long long v[2] = {0, 0};
         for (int i = tid; i < sl.n; i += kThreads) {
-            const float z = sl.z[i];
+            const float z = sl.val(i);
             const uint32_t key = ordered_key(z);
             if (key == khi && pred(key, sl.lo + i)) {
                 v[0] += 1;
@@ -240,7 +272,7 @@ __device__ bool radix_select(Smem& sm, cg::cluster_group& cl, const Slice& sl, u
         }
         __syncthreads();
         for (int i = tid; i < sl.n; i += kThreads) {
-            const float z = sl.z[i];
+            const float z = sl.val(i);
             const uint32_t key = ordered_key(z);
             const bool match = (hi_bit >= 32 ? true : (key >> hi_bit) == prefix) && pred(key, sl.lo + i);
             if (match) {
@@ -297,7 +329,7 @@ __device__ int32_t tie_index(Smem& sm, cg::cluster_group& cl, const Slice& sl, u
     const int a = min(tid * sl.per, sl.n), e = min(a + sl.per, sl.n);
     unsigned long long mine = 0;
     for (int i = a; i < e; ++i) {
-        const uint32_t key = ordered_key(sl.z[i]);
+        const uint32_t key = ordered_key(sl.val(i));
         if (key == tau && pred(key, sl.lo + i)) ++mine;
     }
     const unsigned long long incl = block_scan_u64(sm, mine);
@@ -320,7 +352,7 @@ __device__ int32_t tie_index(Smem& sm, cg::cluster_group& cl, const Slice& sl, u
         if (incl >= want && incl - mine < want) {
             unsigned long long k = incl - mine;
             for (int i = a; i < e; ++i) {
-                const uint32_t key = ordered_key(sl.z[i]);
+                const uint32_t key = ordered_key(sl.val(i));
                 if (key == tau && pred(key, sl.lo + i) && ++k == want) {
                     sm.xu[buf][0] = static_cast<unsigned long long>(sl.lo + i);
                     break;
@@ -329,17 +361,20 @@ __device__ int32_t tie_index(Smem& sm, cg::cluster_group& cl, const Slice& sl, u
         }
     }
     cl.sync();
-    const int32_t idx = static_cast<int32_t>(cl.map_shared_rank(&sm.xu[buf][0], owner)[0]);
+    if (tid == 0) sm.tot[0] = cl.map_shared_rank(&sm.xu[buf][0], owner)[0];
+    __syncthreads();
+    const int32_t idx = static_cast<int32_t>(sm.tot[0]);
     __syncthreads();
     if (tid == 0) sm.parity ^= 1;
     __syncthreads();
     return idx;
 }
 
-// The policy of the row held by the cluster.  z slice already loaded; max key,
-// argmax and the bad flag already reduced.
-__device__ void row_policy(Smem& sm, cg::cluster_group& cl, const Slice& sl, int V, const Policy& pol,
-                           RowResult& res) {
+// The policy by radix selection over the whole slice (the fallback when the
+// candidate set of row_policy would not fit).  z slice already loaded; max
+// key, argmax and the bad flag already reduced.
+__device__ void row_policy_radix(Smem& sm, cg::cluster_group& cl, const Slice& sl, int V, const Policy& pol,
+                                 RowResult& res) {
     const float zmax = res.zmax;
     const uint32_t kmax = ordered_key(zmax);
     // greedy: the argmax alone
@@ -359,7 +394,7 @@ __device__ void row_policy(Smem& sm, cg::cluster_group& cl, const Slice& sl, int
 #pragma unroll
         for (int i = 0; i <= kWin; ++i) v[i] = 0;
         for (int i = tid; i < sl.n; i += kThreads) {
-            const float d = zmax - sl.z[i];
+            const float d = zmax - sl.val(i);
 #pragma unroll
             for (int w = 0; w < kWin; ++w) v[w] += d <= static_cast<float>(1 << w) ? 1ull : 0ull;
         }
@@ -386,7 +421,7 @@ __device__ void row_policy(Smem& sm, cg::cluster_group& cl, const Slice& sl, int
 #pragma unroll
     for (int i = 0; i <= kWin; ++i) v[i] = 0;
     for (int i = tid; i < sl.n; i += kThreads) {
-        const float z = sl.z[i];
+        const float z = sl.val(i);
         const float d = (zmax - z) * inv_t;
         if (d > 41.0f * 0.6931472f + 1.0f) continue;  // weight rounds to 0 in 2^-40 units
         const uint32_t key = ordered_key(z);
@@ -474,7 +509,9 @@ __device__ int32_t sample_fixed(Smem& sm, cg::cluster_group& cl, const Slice& sl
         }
     }
     cl.sync();
-    const int32_t idx = static_cast<int32_t>(cl.map_shared_rank(&sm.xu[buf][0], owner)[0]);
+    if (tid == 0) sm.tot[0] = cl.map_shared_rank(&sm.xu[buf][0], owner)[0];
+    __syncthreads();
+    const int32_t idx = static_cast<int32_t>(sm.tot[0]);
     __syncthreads();
     if (tid == 0) sm.parity ^= 1;
     __syncthreads();
@@ -484,7 +521,7 @@ __device__ int32_t sample_fixed(Smem& sm, cg::cluster_group& cl, const Slice& sl
 // Load this CTA's slice of a row into shared memory (fp32) and reduce the
 // row's max key / lowest argmax / non-finite flag over the cluster.
 template <int kDtype>
-__device__ void load_slice_and_max(Smem& sm, cg::cluster_group& cl, const void* row, int lo, int n, float* zs,
+__device__ void load_slice_and_max(Smem& sm, cg::cluster_group& cl, const void* row, int lo, int n, void* zs,
                                    RowResult& res, bool& bad) {
     constexpr int kPer = kDtype == kBF16 ? 8 : 4;
     constexpr int kEsize = kDtype == kBF16 ? 2 : 4;
@@ -495,15 +532,14 @@ __device__ void load_slice_and_max(Smem& sm, cg::cluster_group& cl, const void* 
     for (int j = threadIdx.x; j < nvec; j += kThreads) {
         const uint4 v = ld_stream_v4(src + static_cast<int64_t>(j) * 16);
         float x[kPer];
-        if constexpr (kDtype == kBF16) {
+        if constexpr (kDtype == kBF16) {  // kept as bf16
             x[0] = bf16_lo(v.x); x[1] = bf16_hi(v.x); x[2] = bf16_lo(v.y); x[3] = bf16_hi(v.y);
             x[4] = bf16_lo(v.z); x[5] = bf16_hi(v.z); x[6] = bf16_lo(v.w); x[7] = bf16_hi(v.w);
-            *reinterpret_cast<float4*>(zs + j * 8) = make_float4(x[0], x[1], x[2], x[3]);
-            *reinterpret_cast<float4*>(zs + j * 8 + 4) = make_float4(x[4], x[5], x[6], x[7]);
+            reinterpret_cast<uint4*>(zs)[j] = v;
         } else {
             x[0] = __uint_as_float(v.x); x[1] = __uint_as_float(v.y);
             x[2] = __uint_as_float(v.z); x[3] = __uint_as_float(v.w);
-            *reinterpret_cast<float4*>(zs + j * 4) = make_float4(x[0], x[1], x[2], x[3]);
+            reinterpret_cast<uint4*>(zs)[j] = v;
         }
 #pragma unroll
         for (int l = 0; l < kPer; ++l) {
@@ -526,6 +562,327 @@ __device__ void load_slice_and_max(Smem& sm, cg::cluster_group& cl, const void* 
         res.zmax = key_to_float(static_cast<uint32_t>(mk >> 32));
         res.argmax = static_cast<int32_t>(0xFFFFFFFFu - static_cast<uint32_t>(mk));
     }
+}
+
+// ---------------------------------------------------------------- candidates
+// Composite sort key of a logit: larger value first, then lower index.
+__device__ __forceinline__ unsigned long long value_order(uint32_t key, int32_t idx) {
+    return (static_cast<unsigned long long>(key) << 32) | (0xFFFFFFFFull - static_cast<uint32_t>(idx));
+}
+// ... and of a token index: lower index first (the key kept in the low word).
+__device__ __forceinline__ unsigned long long index_order(uint32_t key, int32_t idx) {
+    return (static_cast<unsigned long long>(0xFFFFFFFFu - static_cast<uint32_t>(idx)) << 32) | key;
+}
+__device__ __forceinline__ uint32_t vo_key(unsigned long long c) { return static_cast<uint32_t>(c >> 32); }
+__device__ __forceinline__ int32_t vo_idx(unsigned long long c) {
+    return static_cast<int32_t>(0xFFFFFFFFu - static_cast<uint32_t>(c));
+}
+__device__ __forceinline__ uint32_t io_key(unsigned long long c) { return static_cast<uint32_t>(c); }
+__device__ __forceinline__ int32_t io_idx(unsigned long long c) {
+    return static_cast<int32_t>(0xFFFFFFFFu - static_cast<uint32_t>(c >> 32));
+}
+
+// Bitonic sort of buf[0, n) in descending order (n <= kCap), padding with 0
+// (below every real composite key) up to a power of two.  All threads of the CTA.
+__device__ void sort_desc(unsigned long long* buf, int n) {
+    int P = 1;
+    while (P < n) P <<= 1;
+    for (int i = n + threadIdx.x; i < P; i += kThreads) buf[i] = 0ull;
+    __syncthreads();
+    for (int k = 2; k <= P; k <<= 1) {
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            for (int i = threadIdx.x; i < P; i += kThreads) {
+                const int ixj = i ^ j;
+                if (ixj > i) {
+                    const unsigned long long a = buf[i], b = buf[ixj];
+                    const bool down = (i & k) == 0;
+                    if (down ? (a < b) : (a > b)) {
+                        buf[i] = b;
+                        buf[ixj] = a;
+                    }
+                }
+            }
+            __syncthreads();
+        }
+    }
+}
+
+// First position i in [0, n) whose inclusive prefix of w(i) satisfies
+// prefix >= th (strict = false) or prefix > th (strict = true); n if none.
+// Also returns the total.  All threads of one CTA; w is evaluated in
+// contiguous per-thread ranges.
+template <typename Wf>
+__device__ int find_crossing(Smem& sm, int n, unsigned long long th, bool strict, Wf w,
+                             unsigned long long& total) {
+    const int per = (n + kThreads - 1) / kThreads;
+    const int a = min(static_cast<int>(threadIdx.x) * per, n), e = min(a + per, n);
+    unsigned long long mine = 0;
+    for (int i = a; i < e; ++i) mine += w(i);
+    const unsigned long long incl = block_scan_u64(sm, mine);
+    __shared__ unsigned long long s_tot;
+    __shared__ int s_pos;
+    if (threadIdx.x == kThreads - 1) s_tot = incl;
+    if (threadIdx.x == 0) s_pos = n;
+    __syncthreads();
+    const unsigned long long before = incl - mine;
+    const bool here = strict ? (incl > th && before <= th) : (incl >= th && before < th);
+    if (here && mine > 0) {
+        unsigned long long c = before;
+        for (int i = a; i < e; ++i) {
+            c += w(i);
+            if (strict ? c > th : c >= th) {
+                s_pos = i;
+                break;
+            }
+        }
+    }
+    __syncthreads();
+    total = s_tot;
+    const int pos = s_pos;
+    __syncthreads();
+    return pos;
+}
+
+// Window widths: top-k in logit units, top-p in units of (zmax - z) / T.
+__device__ __forceinline__ float k_width(int w) { return 0.25f * static_cast<float>(1 << w); }
+__device__ __forceinline__ float p_width(int w) { return 0.5f * static_cast<float>(1 << w); }
+
+// The policy of the row held by the cluster.  The elements that can belong
+// to a truncated support (the top-k set, or the top of the row holding the
+// top-p mass) are compacted into rank 0's candidate buffer, sorted by
+// (logit descending, index ascending), and the cuts are taken there by
+// exact fixed-point prefix sums.  cbuf = this CTA's candidate buffer (only
+// rank 0's is used).  Falls back to row_policy_radix if the candidates would
+// not fit.
+__device__ void row_policy(Smem& sm, cg::cluster_group& cl, const Slice& sl, int V, const Policy& pol,
+                           RowResult& res, unsigned long long* cbuf) {
+    const float zmax = res.zmax;
+    const uint32_t kmax = ordered_key(zmax);
+    const int tid = threadIdx.x;
+    const int rank = static_cast<int>(cl.block_rank());
+    res.tau = kmax;
+    res.cut = res.argmax;
+    res.mass = static_cast<unsigned long long>(kFix);
+    res.count = 1;
+    res.in_buf = 0;
+    if (pol.greedy) return;
+    const float inv_t = pol.inv_t;
+    const bool use_k = pol.top_k > 0;
+    const bool use_p = pol.top_p < 1.0f;
+    constexpr float kZeroWeight = 41.0f * 0.6931472f + 1.0f;  // beyond: the weight rounds to 0
+
+    // ---- total mass when top-k is off (the kept set is the whole row)
+    unsigned long long total_mass = 0;
+    if (!use_k) {
+        unsigned long long v[1] = {0}, o[1];
+        for (int i = tid; i < sl.n; i += kThreads) {
+            const float z = sl.val(i);
+            if ((zmax - z) * inv_t <= kZeroWeight) v[0] += to_fixed(weight_f(z, zmax, inv_t));
+        }
+        cluster_sum_u64<1>(sm, cl, v, o);
+        total_mass = o[0];
+        if (!use_p) {  // no truncation: the whole vocabulary
+            res.tau = 0u;
+            res.cut = -1;
+            res.mass = total_mass;
+            res.count = V;
+            return;
+        }
+    }
+    unsigned long long theta = 0;
+    if (!use_k) {
+        const double th = ceil(static_cast<double>(pol.top_p) * static_cast<double>(total_mass));
+        theta = th < 1.0 ? 1ull : static_cast<unsigned long long>(th);
+        if (theta > total_mass) theta = total_mass;
+    }
+
+    // ---- window estimate from one element in kSample
+    unsigned long long est[kWin], eo[kWin];
+#pragma unroll
+    for (int w = 0; w < kWin; ++w) est[w] = 0;
+    for (int i = tid * kSample; i < sl.n; i += kThreads * kSample) {
+        const float z = sl.val(i);
+        if (use_k) {
+            const float d = zmax - z;
+#pragma unroll
+            for (int w = 0; w < kWin; ++w) est[w] += d <= k_width(w) ? 1ull : 0ull;
+        } else {
+            const float d = (zmax - z) * inv_t;
+            if (d <= kZeroWeight) {
+                const unsigned long long wt = to_fixed(weight_f(z, zmax, inv_t));
+#pragma unroll
+                for (int w = 0; w < kWin; ++w) est[w] += d <= p_width(w) ? wt : 0ull;
+            }
+        }
+    }
+    cluster_sum_u64<kWin>(sm, cl, est, eo);
+    const unsigned long long need = use_k ? static_cast<unsigned long long>(pol.top_k) : theta;
+    int w = kWin;  // kWin = the whole row
+    for (int i = kWin - 1; i >= 0; --i)
+        if (eo[i] * kSample >= need + need / 4 + (use_k ? 32ull : 0ull)) w = i;
+
+    // ---- exact candidate count (and mass), widening until it suffices
+    int count = 0;
+    bool fits = false;
+    float zthr = 0.0f;
+    for (;;) {
+        zthr = w >= kWin ? -__int_as_float(0x7F800000)
+                         : (use_k ? zmax - k_width(w) : zmax - p_width(w) / inv_t);
+        unsigned long long v[2] = {0, 0}, o[2];
+        for (int i = tid; i < sl.n; i += kThreads) {
+            const float z = sl.val(i);
+            if (z >= zthr) {
+                v[0] += 1;
+                if (!use_k && (zmax - z) * inv_t <= kZeroWeight) v[1] += to_fixed(weight_f(z, zmax, inv_t));
+            }
+        }
+        cluster_sum_u64<2>(sm, cl, v, o);
+        const bool enough = use_k ? o[0] >= need : o[1] >= need;
+        if (enough || w >= kWin) {
+            count = static_cast<int>(min(o[0], static_cast<unsigned long long>(0x7FFFFFFF)));
+            fits = o[0] <= static_cast<unsigned long long>(kCap);
+            break;
+        }
+        ++w;
+    }
+    if (!fits) {  // too many candidates: radix selection over the slices
+        row_policy_radix(sm, cl, sl, V, pol, res);
+        res.count = 0x7FFFFFFF;
+        return;
+    }
+
+    // ---- compact the candidates into rank 0's buffer
+    __shared__ unsigned int s_n;
+    if (tid == 0) s_n = 0;
+    __syncthreads();
+    unsigned int mine = 0;
+    for (int i = tid; i < sl.n; i += kThreads) mine += sl.val(i) >= zthr ? 1u : 0u;
+    unsigned long long gathered[kC];
+    {
+        // this CTA's candidate count, then the prefix over ranks
+        const unsigned long long incl = block_scan_u64(sm, mine);
+        __shared__ unsigned long long s_cnt;
+        if (tid == kThreads - 1) s_cnt = incl;
+        __syncthreads();
+        cluster_gather_u64(sm, cl, s_cnt, gathered);
+    }
+    unsigned long long base = 0;
+    for (int r = 0; r < rank; ++r) base += gathered[r];
+    unsigned long long* dst = cl.map_shared_rank(cbuf, 0);
+    for (int i = tid; i < sl.n; i += kThreads) {
+        const float z = sl.val(i);
+        if (z >= zthr) {
+            const unsigned int pos = atomicAdd(&s_n, 1u);
+            dst[base + pos] = value_order(ordered_key(z), sl.lo + i);
+        }
+    }
+    cl.sync();
+
+    // ---- rank 0: sort, take the cuts
+    const int buf = sm.parity;
+    if (rank == 0) {
+        sort_desc(cbuf, count);
+        const int K = use_k ? min(pol.top_k, count) : count;
+        auto wt = [&](int i) -> unsigned long long {
+            return i < K ? to_fixed(weight_f(key_to_float(vo_key(cbuf[i])), zmax, inv_t)) : 0ull;
+        };
+        unsigned long long kept = 0;
+        int m = K;
+        if (use_k) {
+            find_crossing(sm, K, 0ull, true, wt, kept);  // the kept mass
+        } else {
+            kept = total_mass;
+        }
+        unsigned long long mass = kept;
+        if (use_p) {
+            if (use_k) {
+                const double th = ceil(static_cast<double>(pol.top_p) * static_cast<double>(kept));
+                theta = th < 1.0 ? 1ull : static_cast<unsigned long long>(th);
+                if (theta > kept) theta = kept;
+            }
+            unsigned long long tot;
+            const int pos = find_crossing(sm, K, theta, false, wt, tot);
+            m = min(pos + 1, K);
+            unsigned long long pm;
+            find_crossing(sm, m, 0ull, true, wt, pm);  // mass of the first m
+            mass = pm;
+        }
+        if (tid == 0) {
+            const unsigned long long last = cbuf[m - 1];
+            sm.xu[buf][0] = vo_key(last);
+            sm.xu[buf][1] = static_cast<unsigned long long>(static_cast<uint32_t>(vo_idx(last)));
+            sm.xu[buf][2] = mass;
+            sm.xu[buf][3] = static_cast<unsigned long long>(m);
+        }
+    }
+    cl.sync();
+    if (tid < 4) sm.tot[tid] = cl.map_shared_rank(&sm.xu[buf][0], 0)[tid];
+    __syncthreads();
+    res.tau = static_cast<uint32_t>(sm.tot[0]);
+    res.cut = static_cast<int32_t>(static_cast<uint32_t>(sm.tot[1]));
+    res.mass = sm.tot[2];
+    res.count = static_cast<int32_t>(sm.tot[3]);
+    res.in_buf = 1;
+    __syncthreads();
+    if (tid == 0) sm.parity ^= 1;
+    __syncthreads();
+}
+
+// Inverse-CDF draw over a support held in rank 0's candidate buffer (its
+// first n composite keys, in value order): re-keyed by token index, sorted,
+// and drawn by exact prefix sums of w(key, index).  Returns the token in
+// rank 0 (other ranks: -1).  Rank 0's threads only.
+template <typename Wf>
+__device__ int32_t draw_small_support(Smem& sm, unsigned long long* cbuf, int n, uint32_t m24, Wf w,
+                                      unsigned long long& total) {
+    for (int i = threadIdx.x; i < n; i += kThreads) {
+        const unsigned long long c = cbuf[i];
+        cbuf[i] = index_order(vo_key(c), vo_idx(c));
+    }
+    __syncthreads();
+    sort_desc(cbuf, n);
+    auto wi = [&](int i) -> unsigned long long { return w(io_key(cbuf[i]), io_idx(cbuf[i])); };
+    unsigned long long tot;
+    find_crossing(sm, n, 0ull, true, wi, tot);
+    total = tot;
+    if (tot == 0) return -1;
+    const unsigned long long target =
+        static_cast<unsigned long long>((static_cast<unsigned __int128>(m24) * tot) >> 24);
+    unsigned long long t2;
+    const int pos = find_crossing(sm, n, target, true, wi, t2);
+    return pos < n ? io_idx(cbuf[pos]) : io_idx(cbuf[n - 1]);
+}
+
+// Compact the elements of the slice satisfying pred(key, index) into rank 0's
+// candidate buffer in value order (as value_order keys); returns their total
+// (every CTA).  The caller guarantees the total fits kCap.
+template <typename Pred>
+__device__ int compact_to_rank0(Smem& sm, cg::cluster_group& cl, const Slice& sl, unsigned long long* cbuf,
+                                Pred pred) {
+    const int tid = threadIdx.x;
+    const int rank = static_cast<int>(cl.block_rank());
+    __shared__ unsigned int s_n2;
+    __shared__ unsigned long long s_cnt2;
+    if (tid == 0) s_n2 = 0;
+    unsigned int mine = 0;
+    for (int i = tid; i < sl.n; i += kThreads) mine += pred(ordered_key(sl.val(i)), sl.lo + i) ? 1u : 0u;
+    const unsigned long long incl = block_scan_u64(sm, mine);
+    if (tid == kThreads - 1) s_cnt2 = incl;
+    __syncthreads();
+    unsigned long long counts[kC];
+    cluster_gather_u64(sm, cl, s_cnt2, counts);
+    unsigned long long base = 0, total = 0;
+    for (int r = 0; r < kC; ++r) {
+        if (r < rank) base += counts[r];
+        total += counts[r];
+    }
+    unsigned long long* dst = cl.map_shared_rank(cbuf, 0);
+    for (int i = tid; i < sl.n; i += kThreads) {
+        const uint32_t key = ordered_key(sl.val(i));
+        if (pred(key, sl.lo + i)) dst[base + atomicAdd(&s_n2, 1u)] = value_order(key, sl.lo + i);
+    }
+    cl.sync();
+    return static_cast<int>(total);
 }
 
 // Normalise a request's policy record; returns false for an invalid one.
