@@ -180,3 +180,35 @@ def test_draft_sampled_policies(ds, oracle, maker, kw):
                            **_keys_dev(w.keys))
     torch.cuda.synchronize()
     _check_draft(ref, got, w.V)
+
+
+def test_workspace_reuse_across_sizes(ds, oracle):
+    """One workspace shared by calls of different sizes and paths, in turn
+    (sampled verify, greedy verify, Markov drafting with and without the
+    bias): every call must find its counters at zero and match the oracle."""
+    wsp = ds.Workspace()
+    for (V, B, r) in ((2048, 24, 0), (1024, 5, 64), (4096, 40, 0), (2048, 3, 16)):
+        w = synth.decode_verify_tile(V=V, B=B, r=r, H=0)
+        draft = _draft_oracle(oracle, w) if r == 0 else None
+        if draft is not None:
+            ref = oracle.verify(synth.host(w.target), draft["proposals"], draft["q"], draft["q_at_x"],
+                                w.policy.numpy(), **w.keys.numpy())
+            got = ds.verify(w.target.cuda(), torch.from_numpy(draft["proposals"]).cuda(),
+                            q=torch.from_numpy(draft["q"]).cuda(), q_at_x=torch.from_numpy(draft["q_at_x"]).cuda(),
+                            policy=w.policy.packed().cuda(), workspace=wsp, **_keys_dev(w.keys))
+            torch.cuda.synchronize()
+            _check_verify(ref, tuple(t.cpu().numpy() for t in got))
+            x = torch.from_numpy(draft["proposals"]).cuda()
+            gref = oracle.verify(synth.host(w.target), draft["proposals"], None, None,
+                                 synth.uniform_policy(B, greedy=True).numpy(), **w.keys.numpy())
+            ggot = ds.verify(w.target.cuda(), x, workspace=wsp)
+            torch.cuda.synchronize()
+            np.testing.assert_array_equal(ggot[0].cpu().numpy(), gref["out_tokens"])
+        kw = {} if r == 0 else dict(U=w.weights.U.cuda(), W=w.weights.W.cuda())
+        mref = oracle.markov_sample(synth.host(w.backbone), w.anchor.numpy(),
+                                    synth.host(w.weights.U) if r else None, synth.host(w.weights.W) if r else None,
+                                    None, None, None, w.policy.numpy(), **w.keys.numpy())
+        mgot = ds.markov_sample(w.backbone.cuda(), w.anchor.cuda(), policy=w.policy.packed().cuda(),
+                                workspace=wsp, **kw, **_keys_dev(w.keys))
+        torch.cuda.synchronize()
+        _check_draft(mref, mgot, V)

@@ -57,9 +57,13 @@ struct MarkovLayout {
     ArgmaxScratch greedy;
     size_t error_flag, zbuf, total;
 };
+// The regions that must be zero between calls come first and are sized for
+// the largest batch and block (DSPARK_MAX_BATCH x DSPARK_MAX_GAMMA), so that
+// the z buffer of one call never overlaps them in a later call of other sizes.
 MarkovLayout markov_layout(int B, int gamma, int V, int r) {
     MarkovLayout l;
-    l.greedy = argmax_scratch(0, B, gamma);
+    (void)gamma;
+    l.greedy = argmax_scratch(0, DSPARK_MAX_BATCH, DSPARK_MAX_GAMMA);
     l.error_flag = l.greedy.end;  // zero between calls; set only after a device wait gave up
     l.zbuf = align_up(l.error_flag + sizeof(int));
     const size_t zbytes = r > 0 ? static_cast<size_t>(B) * V * sizeof(float) : 0;

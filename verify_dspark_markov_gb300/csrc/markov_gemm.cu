@@ -164,29 +164,48 @@ __global__ void __launch_bounds__(kThreads, 1) markov_bias_kernel(const MarkovGe
             }
             mma_commit(&mbar);
         }
+        // backbone values of this thread's entries, read while the MMAs run (all
+        // loads issued before any store, so none waits on a store to z)
+        const int quad = warp & 3;
+        const int v = v0 + quad * 32 + lane;
+        const int c_first = (warp >> 2) * 16;
+        constexpr int kMaxBatches = 8;  // N <= 256 columns, 16 per batch, two warps per quadrant
+        float base[kMaxBatches][16];
+#pragma unroll
+        for (int bi = 0; bi < kMaxBatches; ++bi) {
+            const int c0 = c_first + bi * 32;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const int b = c0 + i;
+                float x = 0.0f;
+                if (c0 < N && b < p.B && v < p.V) {
+                    if constexpr (kDtype == kBF16)
+                        x = __uint_as_float(static_cast<uint32_t>(__ldg(reinterpret_cast<const unsigned short*>(
+                                                bb + b * bb_stride * 2) + v))
+                                            << 16);
+                    else
+                        x = __ldg(reinterpret_cast<const float*>(bb + b * bb_stride * 4) + v);
+                }
+                base[bi][i] = x;
+            }
+        }
         const bool ok = mbar_wait(&mbar, phase, kWaitLimitNs);
         phase ^= 1u;
         if (!ok) s_timeout = 1;
         tc_fence_after();
         // epilogue: warp w reads TMEM lane quadrant w % 4 (vocabulary entries
         // v0 + 32 (w % 4) + lane) and every other 16-column group from w / 4
-        const int quad = warp & 3;
-        const int v = v0 + quad * 32 + lane;
-        for (int c0 = (warp >> 2) * 16; c0 < N; c0 += 32) {
+#pragma unroll
+        for (int bi = 0; bi < kMaxBatches; ++bi) {
+            const int c0 = c_first + bi * 32;
+            if (c0 >= N) break;
             float acc[16];
             tmem_ld16(tmem + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(c0), acc);
             if (v < p.V) {
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
                     const int b = c0 + i;
-                    if (b < p.B) {
-                        float base;
-                        if constexpr (kDtype == kBF16)
-                            base = __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const uint16_t*>(bb + b * bb_stride * 2)[v]) << 16);
-                        else
-                            base = reinterpret_cast<const float*>(bb + b * bb_stride * 4)[v];
-                        p.zbuf[static_cast<int64_t>(b) * p.V + v] = base + acc[i];
-                    }
+                    if (b < p.B) p.zbuf[static_cast<int64_t>(b) * p.V + v] = base[bi][i] + acc[i];
                 }
             }
         }

@@ -224,6 +224,12 @@ __global__ void __cluster_dims__(rp::kC, 1, 1) __launch_bounds__(rp::kThreads)
             p.status[b] = kReqOk;
         }
     }
+    // leave the workspace zero-filled: this request's row records are consumed
+    cl.sync();
+    if (rank == 0) {
+        uint32_t* recw = reinterpret_cast<uint32_t*>(p.records + static_cast<int64_t>(b) * rows);
+        for (int e = tid; e < rows * static_cast<int>(sizeof(RowRecord) / 4); e += kThreads) recw[e] = 0u;
+    }
     cl.sync();  // keep shared memory alive until every CTA is done reading
 }
 

@@ -772,8 +772,8 @@ __device__ void row_policy(Smem& sm, cg::cluster_group& cl, const Slice& sl, int
     for (int i = tid; i < sl.n; i += kThreads) {
         const float z = sl.val(i);
         if (z >= zthr) {
-            const unsigned int pos = atomicAdd(&s_n, 1u);
-            dst[base + pos] = value_order(ordered_key(z), sl.lo + i);
+            const unsigned long long at = base + atomicAdd(&s_n, 1u);
+            if (at < static_cast<unsigned long long>(kCap)) dst[at] = value_order(ordered_key(z), sl.lo + i);
         }
     }
     cl.sync();
@@ -877,9 +877,13 @@ __device__ int compact_to_rank0(Smem& sm, cg::cluster_group& cl, const Slice& sl
         total += counts[r];
     }
     unsigned long long* dst = cl.map_shared_rank(cbuf, 0);
+    total = min(total, static_cast<unsigned long long>(kCap));
     for (int i = tid; i < sl.n; i += kThreads) {
         const uint32_t key = ordered_key(sl.val(i));
-        if (pred(key, sl.lo + i)) dst[base + atomicAdd(&s_n2, 1u)] = value_order(key, sl.lo + i);
+        if (pred(key, sl.lo + i)) {
+            const unsigned long long at = base + atomicAdd(&s_n2, 1u);
+            if (at < static_cast<unsigned long long>(kCap)) dst[at] = value_order(key, sl.lo + i);
+        }
     }
     cl.sync();
     return static_cast<int>(total);
