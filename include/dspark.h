@@ -49,8 +49,13 @@
  *              The workspace must be zero-filled once after allocation
  *              (e.g. cudaMemsetAsync(ws, 0, bytes, stream)); every call that
  *              completes leaves it zero-filled again, so it can be reused by
- *              the next call on the same stream without clearing.  Calls that
- *              share one workspace must not overlap in time.
+ *              the next call of the same operation on the same stream without
+ *              clearing.  Calls that share one workspace must not overlap in
+ *              time, and a workspace serves one operation (clear it before
+ *              handing it to another).  The greedy paths keep all their state
+ *              on chip and ignore the workspace (it may be NULL): dspark_verify
+ *              with policy NULL, and dspark_markov_sample with policy NULL and
+ *              r = 0.
  *   Random     Each random decision draws u in [0,1) from Philox-4x32-10
  *              (Salmon et al., SC'11) with key (lo32 seed, hi32 seed) and
  *              counter (draw, lo32 pos, hi32 pos, lo32 request_id):
@@ -245,28 +250,19 @@ int dspark_accept_stats(const void* draft, const void* target, int dtype,
 
 /*
  * dspark_verify_greedy_noalloc - the greedy verify of dspark_verify (policy
- * NULL), for callers that cannot allocate device memory.  None of the pages
- * has a counterpart; it exists for callers such as a plugin inside a runtime
- * that owns all device memory and offers no allocator, or a latency-critical
- * path that must not call cudaMalloc (which may synchronize the device).
+ * NULL) without workspace arguments, for callers that cannot allocate device
+ * memory.  None of the pages has a counterpart; it exists for callers such as
+ * a plugin inside a runtime that owns all device memory and offers no
+ * allocator, or a latency-critical path that must not call cudaMalloc (which
+ * may synchronize the device).
  *
  * Arguments and outputs are those of dspark_verify with every request greedy;
- * the caller still provides target, proposals and the three output arrays.
- * There is no workspace argument: the scratch is a static device array of the
- * library, reserved on every GPU that loads it until the process exits.  It
- * holds at most DSPARK_NOALLOC_MAX_REQUESTS requests, i.e. at most
- * DSPARK_NOALLOC_MAX_ROWS target rows (B * (gamma + 1) with gamma <= 16);
- * larger calls return DSPARK_ENOSPC and launch nothing.  The function
- * allocates nothing.
- *
- * The first call on a device looks up the array's device address (a one-time
- * set-up per device); make that first call before any stream capture.  All
- * calls on a device share the array: each call clears the part it uses before
- * its kernel runs, and calls whose work overlaps on the GPU (e.g. on two
- * streams) race on it, so serialize them.
+ * the caller provides target, proposals and the three output arrays.  The
+ * greedy kernel keeps every intermediate in shared memory (each request's
+ * rows are reduced by one thread-block cluster), so the call needs no scratch
+ * at all: the library allocates nothing and reserves no device memory for it.
+ * Calls on different streams may overlap freely.
  */
-#define DSPARK_NOALLOC_MAX_REQUESTS 256
-#define DSPARK_NOALLOC_MAX_ROWS 4352
 int dspark_verify_greedy_noalloc(const void* target, int dtype, const int32_t* proposals, int B,
                                  int gamma, int V, int32_t* out_tokens, int32_t* num_accepted,
                                  int32_t* status, void* stream);

@@ -70,7 +70,7 @@ def test_verify_rejects_invalid_arguments(lib):
     assert _verify(lib, target=None) == binding.EINVAL
     assert _verify(lib, props=None) == binding.EINVAL
     assert _verify(lib, target=FAKE_ODD) == binding.EINVAL
-    assert _verify(lib, ws_bytes=16) == binding.ENOSPC
+    assert _verify(lib, ws_bytes=16, policy=FAKE) == binding.ENOSPC   # sampled path needs workspace
 
 
 def _markov(lib, B=4, gamma=5, V=1024, r=0, U=None, W=None, policy=None, q=None, h=None, H=0,
@@ -88,7 +88,8 @@ def test_markov_rejects_invalid_arguments(lib):
     assert _markov(lib, r=16, U=FAKE_ODD, W=FAKE) == binding.EINVAL
     assert _markov(lib, policy=FAKE, q=None) == binding.EINVAL      # sampled requests need q
     assert _markov(lib, h=FAKE, H=0) == binding.EINVAL
-    assert _markov(lib, ws_bytes=0) == binding.ENOSPC
+    assert _markov(lib, ws_bytes=0, policy=FAKE, q=FAKE) == binding.ENOSPC
+    assert _markov(lib, ws_bytes=0, r=16, U=FAKE, W=FAKE) == binding.ENOSPC
 
 
 def test_accept_stats_rejects_invalid_arguments(lib):

@@ -103,7 +103,9 @@ def test_verify_greedy_special_values(ds, oracle):
     assert res["status"].tolist() == [1, 1, 2, 0, 0, 5]
 
 
-def test_verify_greedy_leaves_workspace_zero_and_repeats(ds, oracle):
+def test_verify_greedy_needs_no_workspace_and_repeats(ds, oracle):
+    """The greedy verify keeps its state on chip: repeated calls give the same
+    result and the binding never allocates a workspace for them."""
     w = synth.full_decode_tile(V=8192, B=16, device="cuda")
     x = _draft_argmax(oracle, w).cuda()
     wsp = ds.Workspace()
@@ -113,8 +115,7 @@ def test_verify_greedy_leaves_workspace_zero_and_repeats(ds, oracle):
         for a, b in zip(first, again):
             assert torch.equal(a, b)
     torch.cuda.synchronize()
-    buf = wsp.get(ds.OP_VERIFY, 1, "cuda")
-    assert int(buf.count_nonzero()) == 0
+    assert wsp._bufs == {}
 
 
 def test_draft_greedy_r0_with_confidence(ds, oracle):

@@ -156,7 +156,8 @@ def verify(target, proposals, q=None, q_at_x=None, policy=None, seed=None, reque
         out = (torch.empty((B, rows), dtype=torch.int32, device=dev),
                torch.empty((B,), dtype=torch.int32, device=dev),
                torch.empty((B,), dtype=torch.int32, device=dev))
-    ws_n = workspace_size(OP_VERIFY, B, gamma, V)
+    # greedy calls (policy None) keep their state on chip and take no workspace
+    ws_n = workspace_size(OP_VERIFY, B, gamma, V) if policy is not None else 0
     ws = (workspace or _default_ws).get(OP_VERIFY, ws_n, dev)
     code = load().dspark_verify(
         _ptr(target), _dtype_code(target), _ptr(proposals), _ptr(_dev(q, "q", torch.float32)),
@@ -197,7 +198,7 @@ def markov_sample(backbone, anchor, U=None, W=None, h=None, E=None, w_conf=None,
                    conf=(torch.empty((B, gamma), dtype=torch.float32, device=dev)
                          if h is not None else None),
                    status=torch.empty((B,), dtype=torch.int32, device=dev))
-    ws_n = workspace_size(OP_MARKOV_SAMPLE, B, gamma, V, r, H)
+    ws_n = workspace_size(OP_MARKOV_SAMPLE, B, gamma, V, r, H) if (policy is not None or r) else 0
     ws = (workspace or _default_ws).get(OP_MARKOV_SAMPLE, ws_n, dev)
     code = load().dspark_markov_sample(
         _ptr(backbone), _dtype_code(backbone), _ptr(anchor), _ptr(U), _ptr(W), r, _ptr(h), h_code,

@@ -24,28 +24,14 @@ bool valid_common(int B, int gamma, int V, int dtype) {
 }
 
 // Workspace carve-up.  Regions that must be zero between calls come first.
-struct ArgmaxScratch {
-    size_t rowkey, rowbad, ticket, end;
-};
-ArgmaxScratch argmax_scratch(size_t offset, int groups, int rows_per_group) {
-    ArgmaxScratch s;
-    const size_t rows = static_cast<size_t>(groups) * rows_per_group;
-    s.rowkey = offset;
-    s.rowbad = align_up(s.rowkey + rows * sizeof(unsigned long long));
-    s.ticket = align_up(s.rowbad + rows * sizeof(unsigned int));
-    s.end = align_up(s.ticket + static_cast<size_t>(groups) * sizeof(unsigned int));
-    return s;
-}
-
+// The greedy paths keep all their state on chip and use no workspace.
 struct VerifyLayout {
-    ArgmaxScratch greedy;
     size_t ticket, records, total;
 };
 VerifyLayout verify_layout(int B, int gamma) {
     VerifyLayout l;
-    l.greedy = argmax_scratch(0, B, gamma + 1);
-    l.ticket = l.greedy.end;  // sampled path: one ticket per request (zero between calls)
-    l.records = align_up(l.ticket + static_cast<size_t>(B) * sizeof(unsigned int));
+    l.ticket = 0;  // sampled path: one ticket per request (zero between calls)
+    l.records = align_up(static_cast<size_t>(B) * sizeof(unsigned int));
     l.total = align_up(l.records + static_cast<size_t>(B) * (gamma + 1) * sizeof(RowRecord));
     return l;
 }
@@ -54,18 +40,15 @@ VerifyLayout verify_layout(int B, int gamma) {
 bool policy_vocab_ok(int V) { return policy_smem_bytes(V, 0) <= 200 * 1024; }
 
 struct MarkovLayout {
-    ArgmaxScratch greedy;
     size_t error_flag, zbuf, total;
 };
-// The regions that must be zero between calls come first and are sized for
-// the largest batch and block (DSPARK_MAX_BATCH x DSPARK_MAX_GAMMA), so that
-// the z buffer of one call never overlaps them in a later call of other sizes.
+// The word that must be zero between calls sits at a fixed offset, so the z
+// buffer of one call never overlaps it in a later call of other sizes.
 MarkovLayout markov_layout(int B, int gamma, int V, int r) {
     MarkovLayout l;
     (void)gamma;
-    l.greedy = argmax_scratch(0, DSPARK_MAX_BATCH, DSPARK_MAX_GAMMA);
-    l.error_flag = l.greedy.end;  // zero between calls; set only after a device wait gave up
-    l.zbuf = align_up(l.error_flag + sizeof(int));
+    l.error_flag = 0;  // zero between calls; set only after a device wait gave up
+    l.zbuf = align_up(sizeof(int));
     const size_t zbytes = r > 0 ? static_cast<size_t>(B) * V * sizeof(float) : 0;
     l.total = align_up(l.zbuf + zbytes);
     return l;
@@ -85,20 +68,6 @@ int device_sms() {
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
     return sms;
-}
-
-// Fill `p.total`, `p.chunk` and return the grid of the flat-split argmax:
-// one wave of resident CTAs, each an equal contiguous range of the rows.
-int plan_argmax(ArgmaxParams& p, int64_t rows) {
-    const int sms = device_sms();
-    const int occ = argmax_rows_occupancy(p.dtype);
-    if (sms <= 0 || occ <= 0) return 0;
-    p.total = rows * static_cast<int64_t>(p.V);
-    const int64_t slots = static_cast<int64_t>(sms) * occ;
-    int64_t chunk = std::max<int64_t>(8192, (p.total + slots - 1) / slots);
-    chunk = (chunk + 7) / 8 * 8;
-    p.chunk = chunk;
-    return static_cast<int>((p.total + chunk - 1) / chunk);
 }
 
 }  // namespace
@@ -147,11 +116,11 @@ int dspark_verify(const void* target, int dtype, const int32_t* proposals, const
     if (!aligned16(target)) return DSPARK_EINVAL;
     if (policy && (!q || !q_at_x || !seed || !request_id || !pos0 || !aligned16(q)))
         return DSPARK_EINVAL;
-    const VerifyLayout lay = verify_layout(B, gamma);
-    if (workspace_bytes < lay.total || (lay.total && !workspace)) return DSPARK_ENOSPC;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
     if (policy) {  // per-request policies: the row engine
+        const VerifyLayout lay = verify_layout(B, gamma);
+        if (workspace_bytes < lay.total || !workspace) return DSPARK_ENOSPC;
         if (!policy_vocab_ok(V)) return DSPARK_ENOTSUP;
         VerifyProbParams vp{};
         vp.target = target;
@@ -182,16 +151,11 @@ int dspark_verify(const void* target, int dtype, const int32_t* proposals, const
     p.rows_per_group = gamma + 1;
     p.gamma = gamma;
     p.mode = kArgmaxVerify;
-    p.rowkey = at<unsigned long long>(workspace, lay.greedy.rowkey);
-    p.rowbad = at<unsigned int>(workspace, lay.greedy.rowbad);
-    p.ticket = at<unsigned int>(workspace, lay.greedy.ticket);
     p.proposals = proposals;
     p.out_tokens = out_tokens;
     p.num_accepted = num_accepted;
     p.status = status;
-    const int grid = plan_argmax(p, static_cast<int64_t>(B) * (gamma + 1));
-    if (grid <= 0) return DSPARK_ECUDA;
-    return launch_argmax_rows(p, grid, s) == cudaSuccess ? DSPARK_OK : DSPARK_ECUDA;
+    return launch_argmax_rows(p, B, s) == cudaSuccess ? DSPARK_OK : DSPARK_ECUDA;
 }
 
 int dspark_markov_sample(const void* backbone, int dtype, const int32_t* anchor, const uint16_t* U,
@@ -211,11 +175,11 @@ int dspark_markov_sample(const void* backbone, int dtype, const int32_t* anchor,
     if (h && (H <= 0 || !E || !w_conf || !conf || (h_dtype != DSPARK_BF16 && h_dtype != DSPARK_F32)))
         return DSPARK_EINVAL;
     if (policy && (!q || !seed || !request_id || !pos0 || !aligned16(q))) return DSPARK_EINVAL;
-    const MarkovLayout lay = markov_layout(B, gamma, V, r);
-    if (workspace_bytes < lay.total || (lay.total && !workspace)) return DSPARK_ENOSPC;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
     if (policy || r > 0) {  // the row engine, one launch per step (after the bias GEMM when r > 0)
+        const MarkovLayout lay = markov_layout(B, gamma, V, r);
+        if (workspace_bytes < lay.total || !workspace) return DSPARK_ENOSPC;
         if (!policy_vocab_ok(V)) return DSPARK_ENOTSUP;
         int* error_flag = at<int>(workspace, lay.error_flag);
         float* zbuf = r > 0 ? at<float>(workspace, lay.zbuf) : nullptr;
@@ -283,16 +247,11 @@ int dspark_markov_sample(const void* backbone, int dtype, const int32_t* anchor,
     p.rows_per_group = gamma;
     p.gamma = gamma;
     p.mode = kArgmaxDraft;
-    p.rowkey = at<unsigned long long>(workspace, lay.greedy.rowkey);
-    p.rowbad = at<unsigned int>(workspace, lay.greedy.rowbad);
-    p.ticket = at<unsigned int>(workspace, lay.greedy.ticket);
     p.anchor = anchor;
     p.props_out = proposals;
     p.q_at_x = q_at_x;
     p.status = status;
-    const int grid = plan_argmax(p, static_cast<int64_t>(B) * gamma);
-    if (grid <= 0) return DSPARK_ECUDA;
-    if (launch_argmax_rows(p, grid, s) != cudaSuccess) return DSPARK_ECUDA;
+    if (launch_argmax_rows(p, B, s) != cudaSuccess) return DSPARK_ECUDA;
     if (h) {
         ConfParams c{h, h_dtype, E, w_conf, H, B, gamma, V, anchor, proposals, 1, gamma, conf};
         if (launch_confidence(c, s) != cudaSuccess) return DSPARK_ECUDA;

@@ -10,19 +10,15 @@ namespace dspark {
 
 enum { kArgmaxVerify = 0, kArgmaxDraft = 1 };
 
-// Flat-split row argmax (argmax.cu).
+// Row arg-max and greedy decisions, one cluster per request (argmax.cu).
 struct ArgmaxParams {
-    const void* logits;
+    const void* logits;       // [groups, rows_per_group, V]
     int dtype;
-    int64_t total;            // rows * V elements
-    int64_t chunk;            // elements per CTA, a multiple of 8
     int V;
     int rows_per_group;       // rows of one request: gamma+1 (verify) or gamma (draft)
     int gamma;
     int mode;                 // kArgmaxVerify / kArgmaxDraft
-    unsigned long long* rowkey;  // [groups * rows_per_group], zero on entry and exit
-    unsigned int* rowbad;        // [groups * rows_per_group], zero on entry and exit
-    unsigned int* ticket;        // [groups], zero on entry and exit
+    int64_t per;              // elements per CTA of a request (set by the launcher)
     // verify
     const int32_t* proposals;
     int32_t* out_tokens;
@@ -33,10 +29,8 @@ struct ArgmaxParams {
     float* q_at_x;
     int32_t* status;
 };
-
-cudaError_t launch_argmax_rows(const ArgmaxParams& p, int grid, cudaStream_t stream);
-int argmax_rows_threads();
-int argmax_rows_occupancy(int dtype);
+cudaError_t launch_argmax_rows(ArgmaxParams p, int groups, cudaStream_t stream);
+int argmax_cluster_size(int dtype, int groups);
 
 // Confidence head c_k = sigmoid(w[:H] . h_k + w[H:] . E[x_{k-1}]) (confidence.cu).
 struct ConfParams {
