@@ -74,10 +74,13 @@ def test_markov_tiny_rank16(ds, oracle, greedy):
     _check(ref, got)
 
 
-@pytest.mark.parametrize("B,V,r", [(5, 4096, 256), (16, 4096, 64), (33, 2056, 128)])
+@pytest.mark.parametrize("B,V,r", [(5, 4096, 256), (16, 4096, 64), (33, 2056, 128), (160, 2056, 256),
+                                   (200, 1032, 48), (129, 1000, 16)])
 def test_markov_ragged_batches(ds, oracle, B, V, r):
-    """Batches that are not a multiple of the MMA N step (padding rows), a
-    vocabulary that is not a multiple of the 128-row tile."""
+    """Batches that do not fill the 128-request M tile (padding rows) or need
+    two of them (B > 128), vocabularies that are not a multiple of the
+    vocabulary tile, and ranks that are not a multiple of 64 (the W tiles then
+    arrive without swizzle)."""
     w = synth.decode_verify_tile(V=V, B=B, r=r, H=32)
     ref, got = _both(ds, oracle, w)
     _check(ref, got)

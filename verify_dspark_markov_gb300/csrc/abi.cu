@@ -184,7 +184,7 @@ int dspark_markov_sample(const void* backbone, int dtype, const int32_t* anchor,
         int* error_flag = at<int>(workspace, lay.error_flag);
         float* zbuf = r > 0 ? at<float>(workspace, lay.zbuf) : nullptr;
         MarkovGemmParams gp{};
-        int ggrid = 0;
+        MarkovGemmPlan plan{};
         if (r > 0) {
             gp.backbone = backbone;
             gp.dtype = dtype;
@@ -196,15 +196,9 @@ int dspark_markov_sample(const void* backbone, int dtype, const int32_t* anchor,
             gp.gamma = gamma;
             gp.V = V;
             gp.r = r;
-            gp.N = (B + 15) / 16 * 16;
-            gp.tmem_cols = 32;
-            while (gp.tmem_cols < gp.N) gp.tmem_cols *= 2;
             gp.zbuf = zbuf;
             gp.error_flag = error_flag;
-            const int sms = device_sms();
-            const int ntiles = (V + 127) / 128;
-            ggrid = std::min(sms > 0 ? sms : 1, ntiles);
-            if (markov_gemm_smem(r, gp.N) > 220 * 1024) return DSPARK_ENOTSUP;
+            if (!prepare_markov_bias(gp, plan)) return DSPARK_ENOTSUP;
         }
         MarkovStepParams mp{};
         mp.backbone = backbone;
@@ -227,7 +221,7 @@ int dspark_markov_sample(const void* backbone, int dtype, const int32_t* anchor,
         for (int k = 1; k <= gamma; ++k) {
             if (r > 0) {
                 gp.k = k;
-                if (launch_markov_bias(gp, ggrid, s) != cudaSuccess) return DSPARK_ECUDA;
+                if (launch_markov_bias(gp, plan, s) != cudaSuccess) return DSPARK_ECUDA;
             }
             mp.k = k;
             if (launch_markov_step(mp, s) != cudaSuccess) return DSPARK_ECUDA;

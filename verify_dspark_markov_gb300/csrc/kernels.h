@@ -107,14 +107,24 @@ struct MarkovGemmParams {
     const int32_t* anchor;
     const int32_t* proposals;  // [B, gamma]: x_{k-1} = proposals[b, k-2] for k >= 2
     int B, gamma, V, r;
-    int N;                     // batch padded to a multiple of 16 (MMA N)
-    int tmem_cols;             // power of two >= max(32, N)
     int k;                     // 1-based step
     float* zbuf;               // [B, V] fp32 out
     int* error_flag;
+    // set by prepare_markov_bias
+    int mtiles;                // 128-request M tiles (1 or 2)
+    int nt;                    // vocabulary rows per tile (MMA N)
+    int stages;                // W tiles in flight per CTA
+    int grid;
 };
-int markov_gemm_smem(int r, int N);
-cudaError_t launch_markov_bias(const MarkovGemmParams& p, int grid, cudaStream_t stream);
+// Opaque per-call state of the bias GEMM (the W tensor map).
+struct MarkovGemmPlan {
+    alignas(64) unsigned char tmap[128];
+    bool sw128;
+};
+// Fill the launch shape of `p` and the tensor map of W; false if B or r are
+// outside what the kernel supports.
+bool prepare_markov_bias(MarkovGemmParams& p, MarkovGemmPlan& plan);
+cudaError_t launch_markov_bias(const MarkovGemmParams& p, const MarkovGemmPlan& plan, cudaStream_t stream);
 int policy_cluster_size();
 int policy_slice(int V);
 int policy_smem_bytes(int V, int store_bf16);

@@ -7,15 +7,25 @@
 // times the r x V matrix, the one dense contraction on the path.  With W
 // stored as [V, r] (row v = column v of Wm) both operands are K-major.
 //
-// tcgen05 (5th-generation tensor cores), swap-AB so that the long vocabulary
-// dimension is M:  D[128 v, N b] = W_tile[128 v, r] x U_x^T[r, N b], bf16
-// operands in shared memory (canonical no-swizzle K-major layout: 8-row x
-// 16-byte core matrices, K-adjacent core matrices 128 bytes apart), fp32
-// accumulator in tensor memory.  One thread issues the MMAs and commits them
-// to an mbarrier; four warps read the accumulator back with tcgen05.ld (warp w
-// owns TMEM lanes 32w..32w+31 = vocabulary entries), add the backbone and
-// write z with coalesced stores.  Persistent CTAs (one per SM) walk the
-// vocabulary tiles; the gathered U rows are loaded once per CTA.
+// tcgen05 (5th-generation tensor cores) with the requests on M:
+//   D[128 b, NT v] = U_x[128 b, r] x W_tile[NT v, r]^T
+// The gathered rows U_x (one or two 128-request M tiles) are written to shared
+// memory once per CTA; W streams through a ring of shared-memory stages by TMA
+// (128-byte swizzle when r is a multiple of 64, else a no-swizzle 3-D box that
+// lands directly in the canonical core-matrix layout).  Warp roles: warp 0
+// issues the TMA loads, warp 1 allocates tensor memory and issues the MMAs
+// (one thread), warps 2..9 drain the accumulators.  Accumulators are
+// double-buffered in tensor memory so that the epilogue of one vocabulary
+// tile overlaps the MMAs of the next.  In the epilogue each thread owns one
+// request row (its TMEM lane) and a half of the tile's columns, so the
+// backbone loads and z stores are contiguous 16-byte accesses.  Persistent
+// CTAs, one per SM, walk the vocabulary tiles.
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <mutex>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -24,22 +34,34 @@ namespace dspark {
 
 namespace {
 
-constexpr int kThreads = 256;  // 8 warps: all stage operands; two per TMEM lane quadrant read back
-constexpr int kTileM = 128;
+constexpr int kThreads = 320;  // producer warp, MMA warp, 8 epilogue warps
+constexpr int kEpiWarps = 8;
+constexpr int kMaxStages = 4;
+constexpr uint32_t kTmemCols = 256;  // two accumulator buffers of mtiles * nt = 128 columns
+constexpr int kSmemBudget = 200 * 1024;
 
-__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
-    // start address >> 4, leading byte offset >> 4 (K direction), stride byte
-    // offset >> 4 (M/N direction), descriptor version 1, no swizzle
+struct GemmSmem {
+    uint64_t full[kMaxStages];   // W stage landed (TMA transaction bytes)
+    uint64_t empty[kMaxStages];  // W stage consumed (MMA commit)
+    uint64_t acc_full[2];        // accumulator ready (MMA commit)
+    uint64_t acc_empty[2];       // accumulator drained (one arrival per epilogue warp)
+    uint32_t tmem_base;
+    int timeout;
+};
+
+// ---------------------------------------------------------------- tcgen05
+// Shared-memory matrix descriptor: start >> 4, leading byte offset >> 4,
+// stride byte offset >> 4, descriptor version 1, layout type (0 = no
+// swizzle, 2 = 128-byte swizzle).
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo, uint32_t layout) {
     return static_cast<uint64_t>((addr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>(lbo >> 4) << 16) |
-           (static_cast<uint64_t>(sbo >> 4) << 32) | (1ull << 46);
+           (static_cast<uint64_t>(sbo >> 4) << 32) | (1ull << 46) | (static_cast<uint64_t>(layout) << 61);
 }
-
 // Instruction descriptor of kind::f16: bf16 A and B, fp32 D, both K-major.
 __host__ __device__ constexpr uint32_t instr_desc(int M, int N) {
     return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
            (static_cast<uint32_t>(M >> 4) << 24);
 }
-
 __device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
                  "r"(ncols)
@@ -49,12 +71,8 @@ __device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
 __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
 }
-__device__ __forceinline__ void tc_fence_after() {
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_before() {
-    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                          uint32_t accumulate) {
     asm volatile(
@@ -69,183 +87,323 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
                      smem_u32(bar))
                  : "memory");
 }
-// 16 consecutive fp32 columns of this thread's TMEM lane.
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
-    uint32_t r[16];
+// 32 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
     asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]),
+          "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
+          "=r"(r[30]), "=r"(r[31])
         : "r"(taddr)
         : "memory");
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// ------------------------------------------------------------------ TMA
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
+            "r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int x, int y, int z, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+        "[%5];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+        : "memory");
 }
 
-// 16-byte asynchronous copy global -> shared (no register staging), so that
-// a thread keeps many copies in flight while staging an operand tile.
-__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)), "l"(gsrc) : "memory");
+// --------------------------------------------------------------- layouts
+// Byte offset of the 16-byte chunk (row m, k-chunk kc) of a K-major operand
+// tile of `rows` rows and r columns, in the layout the descriptors below
+// describe.  kSw128: r/64 boxes of rows x 128 B, 16-byte chunks XOR-swizzled
+// by (m mod 8) within each 128-byte row.  Otherwise: the canonical no-swizzle
+// layout with k-chunk-major order (chunk kc of row m at (kc * rows + m) * 16).
+template <bool kSw128>
+__device__ __forceinline__ uint32_t chunk_off(int m, int kc, int rows) {
+    if constexpr (kSw128)
+        return static_cast<uint32_t>((kc >> 3) * rows * 128 + m * 128 + (((kc & 7) ^ (m & 7)) << 4));
+    else
+        return static_cast<uint32_t>((kc * rows + m) * 16);
 }
-__device__ __forceinline__ void cp_async_wait_all() {
-    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+// Descriptor of K step ks (16 elements) of an operand tile at `base` with
+// `rows` rows.
+template <bool kSw128>
+__device__ __forceinline__ uint64_t op_desc(uint32_t base, int ks, int rows) {
+    if constexpr (kSw128)  // 4 K steps per 128-byte swizzle atom, 8-row groups 1024 B apart
+        return smem_desc(base + (ks >> 2) * rows * 128 + (ks & 3) * 32, 16, 1024, 2);
+    else  // K-adjacent core matrices rows * 16 B apart, 8-row groups 128 B apart
+        return smem_desc(base + ks * 2 * rows * 16, rows * 16, 128, 0);
 }
 
-// Byte offset of element (row, k) in the canonical no-swizzle K-major layout
-// with K columns: 8-row x 8-element core matrices, K-adjacent ones 128 B
-// apart, row-group-adjacent ones 16 * K bytes apart.
-__device__ __forceinline__ uint32_t canon_off(int row, int kc, int K) {
-    return static_cast<uint32_t>((row >> 3) * (16 * K) + kc * 128 + (row & 7) * 16);
+__device__ __forceinline__ void set_timeout(GemmSmem& sm, const MarkovGemmParams& p) {
+    atomicExch(&sm.timeout, 1);
+    *p.error_flag = 1;
+}
+__device__ __forceinline__ bool timed_out(const GemmSmem& sm) {
+    return *reinterpret_cast<const volatile int*>(&sm.timeout) != 0;
 }
 
-template <int kDtype>
-__global__ void __launch_bounds__(kThreads, 1) markov_bias_kernel(const MarkovGemmParams p) {
-    extern __shared__ __align__(1024) uint8_t smem[];
-    __shared__ uint64_t mbar;
-    __shared__ uint32_t tmem_base;
-    __shared__ int s_timeout;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int r = p.r, N = p.N;
-    const int kchunks = r / 8;  // 16-byte chunks per operand row
+template <int kDtype, bool kSw128>
+__global__ void __launch_bounds__(kThreads, 1)
+    markov_bias_kernel(const __grid_constant__ CUtensorMap wmap, const MarkovGemmParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ GemmSmem sm;
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int r = p.r, mt = p.mtiles, NT = p.nt, S = p.stages;
+    const int a_rows = 128;
+    const uint32_t a_bytes = static_cast<uint32_t>(a_rows * r * 2);  // one M tile
+    const uint32_t w_bytes = static_cast<uint32_t>(NT * r * 2);      // one W stage
     uint8_t* sA = smem;
-    uint8_t* sB = smem + kTileM * r * 2;
+    uint8_t* sW = smem + mt * a_bytes;
+    const int ntiles = (p.V + NT - 1) / NT;
 
-    if (warp == 0) tmem_alloc(&tmem_base, p.tmem_cols);
-    if (tid == 0) {
-        mbar_init(&mbar, 1);
+    if (warp == 1) tmem_alloc(&sm.tmem_base, kTmemCols);
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kMaxStages; ++s) {
+            mbar_init(&sm.full[s], 1);
+            mbar_init(&sm.empty[s], 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&sm.acc_full[a], 1);
+            mbar_init(&sm.acc_empty[a], kEpiWarps);
+        }
+        sm.timeout = 0;
         fence_mbar_init();
-        s_timeout = 0;
+    }
+    // A operand: the gathered rows U[x_{k-1}(b)], zero rows past the batch
+    // and for failed requests (their rows are ignored downstream).
+    const int kchunks = r / 8;
+    for (int c = threadIdx.x; c < mt * a_rows * kchunks; c += kThreads) {
+        const int b = c / kchunks, kc = c % kchunks;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (b < p.B) {
+            const int32_t x = p.k == 1 ? p.anchor[b] : p.proposals[b * p.gamma + (p.k - 2)];
+            if (x >= 0 && x < p.V) v = *reinterpret_cast<const uint4*>(p.U + static_cast<int64_t>(x) * r + kc * 8);
+        }
+        *reinterpret_cast<uint4*>(sA + (b >> 7) * a_bytes + chunk_off<kSw128>(b & 127, kc, a_rows)) = v;
+    }
+    fence_proxy_async_smem();  // generic stores -> visible to the tensor cores
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sm.tmem_base;
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer
+        if (lane == 0) {
+            int issued = 0;
+            for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++issued) {
+                const int s = issued % S;
+                if (issued >= S && !mbar_wait(&sm.empty[s], ((issued / S) - 1) & 1, kWaitLimitNs)) {
+                    set_timeout(sm, p);
+                    break;
+                }
+                if (timed_out(sm)) break;
+                mbar_arrive_expect_tx(&sm.full[s], w_bytes);
+                uint8_t* dst = sW + s * w_bytes;
+                if constexpr (kSw128) {
+                    for (int kb = 0; kb < r / 64; ++kb)
+                        tma_load_2d(dst + kb * NT * 128, &wmap, kb * 64, t * NT, &sm.full[s]);
+                } else {
+                    tma_load_3d(dst, &wmap, 0, t * NT, 0, &sm.full[s]);
+                }
+            }
+            // no copy may still be landing when the CTA exits
+            for (int i = max(0, issued - S); i < issued; ++i)
+                if (!mbar_wait(&sm.full[i % S], (i / S) & 1, kWaitLimitNs)) set_timeout(sm, p);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t idesc = instr_desc(128, NT);
+            const uint32_t abase = smem_u32(sA), wbase = smem_u32(sW);
+            int i = 0;
+            for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++i) {
+                const int s = i % S, a = i & 1;
+                if (!mbar_wait(&sm.full[s], (i / S) & 1, kWaitLimitNs) ||
+                    (i >= 2 && !mbar_wait(&sm.acc_empty[a], ((i >> 1) - 1) & 1, kWaitLimitNs))) {
+                    set_timeout(sm, p);
+                    break;
+                }
+                if (timed_out(sm)) break;
+                tc_fence_after();
+                for (int m = 0; m < mt; ++m) {
+                    const uint32_t d = tmem + static_cast<uint32_t>(a * mt * NT + m * NT);
+                    for (int ks = 0; ks < r / 16; ++ks)
+                        mma_bf16(d, op_desc<kSw128>(abase + m * a_bytes, ks, a_rows),
+                                 op_desc<kSw128>(wbase + s * w_bytes, ks, NT), idesc, ks > 0 ? 1u : 0u);
+                }
+                mma_commit(&sm.empty[s]);
+                mma_commit(&sm.acc_full[a]);
+            }
+            // the tensor memory is released only after the last MMAs landed
+            if (i > 0 && !mbar_wait(&sm.acc_full[(i - 1) & 1], ((i - 1) >> 1) & 1, kWaitLimitNs)) set_timeout(sm, p);
+        }
+    } else {
+        // ------------------------------------------------ epilogue
+        const int e = warp - 2;
+        const int quad = warp & 3;  // TMEM lanes 32 quad .. 32 quad + 31
+        const int half = e >> 2;    // which half of the tile's columns
+        const int ncol = NT / 2;    // 64 or 32 columns per thread and M tile
+        const int row = quad * 32 + lane;
+        const size_t esz = kDtype == kBF16 ? 2 : 4;
+        const char* bb = static_cast<const char*>(p.backbone) + static_cast<size_t>(p.k - 1) * p.V * esz;
+        const size_t bb_stride = static_cast<size_t>(p.gamma) * p.V * esz;  // one request
+        constexpr int kVec = kDtype == kBF16 ? 8 : 4;                     // elements per 16-byte vector
+        int i = 0;
+        for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++i) {
+            const int a = i & 1;
+            const int v0 = t * NT + half * ncol;
+            // Backbone of this thread's 64 (row, column) entries of the tile
+            // (mtiles * ncol = 64: flat entry f is M tile f / ncol, column
+            // f % ncol), read before the accumulator is ready.
+            constexpr int kNV = 64 / kVec;
+            uint4 base[kNV];
+#pragma unroll
+            for (int n = 0; n < kNV; ++n) {
+                const int f = n * kVec, m = f / ncol, c = f % ncol;
+                const int b = m * 128 + row;
+                base[n] = make_uint4(0u, 0u, 0u, 0u);
+                if (b < p.B && v0 + c < p.V)
+                    base[n] = ld_stream_v4(bb + b * bb_stride + static_cast<size_t>(v0 + c) * esz);
+            }
+            if (!mbar_wait(&sm.acc_full[a], (i >> 1) & 1, kWaitLimitNs)) {
+                set_timeout(sm, p);
+                break;
+            }
+            if (timed_out(sm)) break;
+            tc_fence_after();
+#pragma unroll
+            for (int g = 0; g < 2; ++g) {  // two groups of 32 flat entries
+                const int m = (32 * g) / ncol, c0 = (32 * g) % ncol;
+                const int b = m * 128 + row;
+                uint32_t acc[32];
+                tmem_ld32(tmem + (static_cast<uint32_t>(quad * 32) << 16) +
+                              static_cast<uint32_t>(a * mt * NT + m * NT + half * ncol + c0),
+                          acc);
+                tmem_wait_ld();
+                if (b < p.B) {
+                    float* z = p.zbuf + static_cast<size_t>(b) * p.V + v0 + c0;
+#pragma unroll
+                    for (int j = 0; j < 32; j += 4) {
+                        if (v0 + c0 + j >= p.V) break;
+                        const uint4 w = base[(32 * g + j) / kVec];
+                        float x[4];
+                        if constexpr (kDtype == kBF16) {
+                            const int q = (j % kVec) / 2;  // word holding elements j, j+1
+                            const uint32_t w0 = q == 0 ? w.x : q == 1 ? w.y : q == 2 ? w.z : w.w;
+                            const uint32_t w1 = q == 0 ? w.y : q == 1 ? w.z : w.w;
+                            x[0] = bf16_lo(w0);
+                            x[1] = bf16_hi(w0);
+                            x[2] = bf16_lo(w1);
+                            x[3] = bf16_hi(w1);
+                        } else {
+                            x[0] = __uint_as_float(w.x);
+                            x[1] = __uint_as_float(w.y);
+                            x[2] = __uint_as_float(w.z);
+                            x[3] = __uint_as_float(w.w);
+                        }
+                        float4 o;
+                        o.x = x[0] + __uint_as_float(acc[j]);
+                        o.y = x[1] + __uint_as_float(acc[j + 1]);
+                        o.z = x[2] + __uint_as_float(acc[j + 2]);
+                        o.w = x[3] + __uint_as_float(acc[j + 3]);
+                        *reinterpret_cast<float4*>(z + j) = o;
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.acc_empty[a]);
+        }
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = tmem_base;
+    if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+}
 
-    // B operand: the gathered rows U[x_{k-1}(b)], zero rows past the batch
-    for (int c = tid; c < N * kchunks; c += kThreads) {
-        const int b = c / kchunks, kc = c % kchunks;
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (b < p.B) {
-            int32_t x = p.k == 1 ? p.anchor[b] : p.proposals[b * p.gamma + (p.k - 2)];
-            if (x < 0 || x >= p.V) x = 0;  // a failed request: its row is ignored downstream
-            v = *reinterpret_cast<const uint4*>(p.U + static_cast<int64_t>(x) * r + kc * 8);
-        }
-        *reinterpret_cast<uint4*>(sB + canon_off(b, kc, r)) = v;
-    }
+// ------------------------------------------------------------------ host
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
 
-    const uint32_t idesc = instr_desc(kTileM, N);
-    const uint32_t aaddr = smem_u32(sA), baddr = smem_u32(sB);
-    const int ntiles = (p.V + kTileM - 1) / kTileM;
-    uint32_t phase = 0;
-    const int64_t bb_stride = static_cast<int64_t>(p.gamma) * p.V;  // backbone [B, gamma, V]
-    const char* bb = static_cast<const char*>(p.backbone) + static_cast<int64_t>(p.k - 1) * p.V * (kDtype == kBF16 ? 2 : 4);
+int smem_bytes(const MarkovGemmParams& p) {
+    return p.mtiles * 128 * p.r * 2 + p.stages * p.nt * p.r * 2 + 1024;  // + alignment slack
+}
 
-    for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
-        const int v0 = t * kTileM;
-        // A operand: W rows v0 .. v0+127, zero past the vocabulary
-        for (int c = tid; c < kTileM * kchunks; c += kThreads) {
-            const int m = c / kchunks, kc = c % kchunks;
-            if (v0 + m < p.V)
-                cp_async16(sA + canon_off(m, kc, r), p.W + static_cast<int64_t>(v0 + m) * r + kc * 8);
-            else
-                *reinterpret_cast<uint4*>(sA + canon_off(m, kc, r)) = make_uint4(0u, 0u, 0u, 0u);
-        }
-        cp_async_wait_all();
-        fence_proxy_async_smem();
-        __syncthreads();
-        if (tid == 0) {
-            tc_fence_after();
-            for (int ks = 0; ks < r / 16; ++ks) {
-                // one K step = two K-adjacent core matrices = 256 bytes further
-                const uint64_t ad = smem_desc(aaddr + ks * 256, 128, 16 * r);
-                const uint64_t bd = smem_desc(baddr + ks * 256, 128, 16 * r);
-                mma_bf16(tmem, ad, bd, idesc, ks > 0 ? 1u : 0u);
-            }
-            mma_commit(&mbar);
-        }
-        // backbone values of this thread's entries, read while the MMAs run (all
-        // loads issued before any store, so none waits on a store to z)
-        const int quad = warp & 3;
-        const int v = v0 + quad * 32 + lane;
-        const int c_first = (warp >> 2) * 16;
-        constexpr int kMaxBatches = 8;  // N <= 256 columns, 16 per batch, two warps per quadrant
-        float base[kMaxBatches][16];
-#pragma unroll
-        for (int bi = 0; bi < kMaxBatches; ++bi) {
-            const int c0 = c_first + bi * 32;
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const int b = c0 + i;
-                float x = 0.0f;
-                if (c0 < N && b < p.B && v < p.V) {
-                    if constexpr (kDtype == kBF16)
-                        x = __uint_as_float(static_cast<uint32_t>(__ldg(reinterpret_cast<const unsigned short*>(
-                                                bb + b * bb_stride * 2) + v))
-                                            << 16);
-                    else
-                        x = __ldg(reinterpret_cast<const float*>(bb + b * bb_stride * 4) + v);
-                }
-                base[bi][i] = x;
-            }
-        }
-        const bool ok = mbar_wait(&mbar, phase, kWaitLimitNs);
-        phase ^= 1u;
-        if (!ok) s_timeout = 1;
-        tc_fence_after();
-        // epilogue: warp w reads TMEM lane quadrant w % 4 (vocabulary entries
-        // v0 + 32 (w % 4) + lane) and every other 16-column group from w / 4
-#pragma unroll
-        for (int bi = 0; bi < kMaxBatches; ++bi) {
-            const int c0 = c_first + bi * 32;
-            if (c0 >= N) break;
-            float acc[16];
-            tmem_ld16(tmem + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(c0), acc);
-            if (v < p.V) {
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int b = c0 + i;
-                    if (b < p.B) p.zbuf[static_cast<int64_t>(b) * p.V + v] = base[bi][i] + acc[i];
-                }
-            }
-        }
-        tc_fence_before();
-        __syncthreads();  // TMEM and the A tile are free for the next tile
-        if (s_timeout) break;
-    }
-    if (s_timeout) {
-        // report, then give MMAs still in flight a bounded chance to land
-        // before the tensor memory is released
-        if (tid == 0) {
-            *p.error_flag = 1;
-            mbar_wait(&mbar, phase ^ 1u, kWaitLimitNs);
-        }
-        tc_fence_before();
-    }
-    __syncthreads();
-    tc_fence_after();
-    if (warp == 0) tmem_dealloc(tmem, p.tmem_cols);
+template <int kDtype, bool kSw128>
+cudaError_t launch_one(const MarkovGemmParams& p, const CUtensorMap& map, cudaStream_t stream) {
+    const int smem = smem_bytes(p);
+    const cudaError_t e =
+        cudaFuncSetAttribute(markov_bias_kernel<kDtype, kSw128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    markov_bias_kernel<kDtype, kSw128><<<p.grid, kThreads, smem, stream>>>(map, p);
+    return cudaGetLastError();
 }
 
 }  // namespace
 
-int markov_gemm_smem(int r, int N) { return (kTileM + N) * r * 2; }
+bool prepare_markov_bias(MarkovGemmParams& p, MarkovGemmPlan& plan) {
+    if (p.B < 1 || p.B > 256 || p.r < 16 || p.r > 256 || p.r % 16 != 0) return false;
+    p.mtiles = (p.B + 127) / 128;
+    p.nt = 128 / p.mtiles;
+    const int a = p.mtiles * 128 * p.r * 2, w = p.nt * p.r * 2;
+    p.stages = std::min(kMaxStages, (kSmemBudget - a) / w);
+    if (p.stages < 2) return false;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+        return false;
+    const int ntiles = (p.V + p.nt - 1) / p.nt;
+    p.grid = std::min(sms, ntiles);
 
-cudaError_t launch_markov_bias(const MarkovGemmParams& p, int grid, cudaStream_t stream) {
-    const int smem = markov_gemm_smem(p.r, p.N);
-    cudaError_t e;
-    if (p.dtype == kBF16) {
-        if ((e = cudaFuncSetAttribute(markov_bias_kernel<kBF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      smem)) != cudaSuccess)
-            return e;
-        markov_bias_kernel<kBF16><<<grid, kThreads, smem, stream>>>(p);
-    } else {
-        if ((e = cudaFuncSetAttribute(markov_bias_kernel<kF32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      smem)) != cudaSuccess)
-            return e;
-        markov_bias_kernel<kF32><<<grid, kThreads, smem, stream>>>(p);
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+    if (!enc) return false;
+    CUtensorMap* map = reinterpret_cast<CUtensorMap*>(plan.tmap);
+    plan.sw128 = p.r % 64 == 0;
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult res;
+    if (plan.sw128) {  // [V, r] as 2-D: boxes of 64 columns (128 B) x nt rows, 128-byte swizzle
+        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(p.r), static_cast<cuuint64_t>(p.V)};
+        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(p.r) * 2};
+        const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(p.nt)};
+        res = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(p.W), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    } else {  // (8 elements, V rows, r/8 chunks): one box = nt rows in k-chunk-major core-matrix order
+        const cuuint64_t dims[3] = {8, static_cast<cuuint64_t>(p.V), static_cast<cuuint64_t>(p.r / 8)};
+        const cuuint64_t strides[2] = {static_cast<cuuint64_t>(p.r) * 2, 16};
+        const cuuint32_t box[3] = {8, static_cast<cuuint32_t>(p.nt), static_cast<cuuint32_t>(p.r / 8)};
+        res = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t*>(p.W), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     }
-    return cudaGetLastError();
+    return res == CUDA_SUCCESS;
+}
+
+cudaError_t launch_markov_bias(const MarkovGemmParams& p, const MarkovGemmPlan& plan, cudaStream_t stream) {
+    const CUtensorMap& map = *reinterpret_cast<const CUtensorMap*>(plan.tmap);
+    if (p.dtype == kBF16)
+        return plan.sw128 ? launch_one<kBF16, true>(p, map, stream) : launch_one<kBF16, false>(p, map, stream);
+    return plan.sw128 ? launch_one<kF32, true>(p, map, stream) : launch_one<kF32, false>(p, map, stream);
 }
 
 }  // namespace dspark
