@@ -51,9 +51,8 @@ __global__ void __cluster_dims__(rp::kC, 1, 1) __launch_bounds__(rp::kThreads)
     constexpr int kStoreBf16 = kDtype == kBF16;
     void* zs = dyn;
     unsigned long long* cbuf = reinterpret_cast<unsigned long long*>(dyn + slice_bytes(p.slice, kStoreBf16));
+    rp::init_smem(sm);
     if (tid == 0) {
-        sm.parity = 0;
-        sm.hparity = 0;
         s_px = 0.0f;
         s_last = 0;
         s_plan[0] = -1;
@@ -73,9 +72,10 @@ __global__ void __cluster_dims__(rp::kC, 1, 1) __launch_bounds__(rp::kThreads)
     rp::Policy pol;
     const bool pol_ok = rp::make_policy(p.policy[b], p.V, pol);
     rp::RowResult res;
-    bool bad;
-    rp::load_slice_and_max<kDtype>(sm, cl, tgt + row * p.V * esize, lo, n, zs, res, bad);
-    res.status = bad ? kReqNonfinite : (res.argmax < 0 ? kReqEmpty : (pol_ok ? kReqOk : kReqBadPolicy));
+    bool bad, late;
+    rp::load_slice_and_max<kDtype>(sm, cl, tgt + row * p.V * esize, lo, n, zs, res, bad, late);
+    res.status = late ? kReqTimeout
+                      : bad ? kReqNonfinite : (res.argmax < 0 ? kReqEmpty : (pol_ok ? kReqOk : kReqBadPolicy));
     res.count = 1;
     res.in_buf = 0;
     if (res.status == kReqOk) rp::row_policy(sm, cl, sl, p.V, pol, res, cbuf);
@@ -162,8 +162,9 @@ __global__ void __cluster_dims__(rp::kC, 1, 1) __launch_bounds__(rp::kThreads)
         const RowRecord rr = p.records[static_cast<int64_t>(b) * rows + R];
         const int64_t trow = static_cast<int64_t>(b) * rows + R;
         rp::RowResult unused;
-        bool unused_bad;
-        rp::load_slice_and_max<kDtype>(sm, cl, tgt + trow * p.V * esize, lo, n, zs, unused, unused_bad);
+        bool unused_bad, late;
+        if (rank == 0 && tid == 0) sm.ccount = 0;  // published by the load's cluster barrier
+        rp::load_slice_and_max<kDtype>(sm, cl, tgt + trow * p.V * esize, lo, n, zs, unused, unused_bad, late);
         const float invS = inv_mass(rr.mass);
         const float* qrow = j ? p.q + (static_cast<int64_t>(b) * p.gamma + (j - 1)) * p.V : nullptr;
         const int64_t pos = p.pos0[b] + (j ? j : p.gamma + 1);
@@ -185,11 +186,6 @@ __global__ void __cluster_dims__(rp::kC, 1, 1) __launch_bounds__(rp::kThreads)
                 if (j) {
                     token = rp::draw_small_support(sm, cbuf, cnt, m24, resid, total);
                     if (total == 0) {  // no residual mass left (round-off): draw from p itself
-                        for (int e = tid; e < cnt; e += kThreads) {  // back to value-order keys
-                            const unsigned long long c = cbuf[e];
-                            cbuf[e] = rp::value_order(rp::io_key(c), rp::io_idx(c));
-                        }
-                        __syncthreads();
                         token = rp::draw_small_support(sm, cbuf, cnt, m24,
                                                        [&](uint32_t key, int32_t) { return pw(key); }, total);
                     }
@@ -219,9 +215,15 @@ __global__ void __cluster_dims__(rp::kC, 1, 1) __launch_bounds__(rp::kThreads)
                                          total);
         }
         if (rank == 0 && tid == 0) {
-            out[R] = token;
-            p.num_accepted[b] = R;
-            p.status[b] = kReqOk;
+            if (late) {
+                for (int r = 0; r < rows; ++r) out[r] = -1;
+                p.num_accepted[b] = -1;
+                p.status[b] = kReqTimeout;
+            } else {
+                out[R] = token;
+                p.num_accepted[b] = R;
+                p.status[b] = kReqOk;
+            }
         }
     }
     // leave the workspace zero-filled: this request's row records are consumed
@@ -243,9 +245,8 @@ __global__ void __cluster_dims__(rp::kC, 1, 1) __launch_bounds__(rp::kThreads)
     cg::cluster_group cl = cg::this_cluster();
     const int rank = static_cast<int>(cl.block_rank());
     const int tid = threadIdx.x;
+    rp::init_smem(sm);
     if (tid == 0) {
-        sm.parity = 0;
-        sm.hparity = 0;
         s_qx = 0.0f;
         s_x = -1;
     }
@@ -282,14 +283,15 @@ __global__ void __cluster_dims__(rp::kC, 1, 1) __launch_bounds__(rp::kThreads)
     const bool pol_ok = p.policy ? rp::make_policy(p.policy[b], p.V, pol)
                                  : (pol = rp::Policy{1.0f, 0, 1.0f, 1}, true);
     rp::RowResult res;
-    bool bad;
+    bool bad, late;
     if (p.zbuf)  // logits with the Markov bias, fp32 [B, V]
-        rp::load_slice_and_max<kF32>(sm, cl, p.zbuf + static_cast<int64_t>(b) * p.V, lo, n, zs, res, bad);
+        rp::load_slice_and_max<kF32>(sm, cl, p.zbuf + static_cast<int64_t>(b) * p.V, lo, n, zs, res, bad, late);
     else
         rp::load_slice_and_max<kDtype>(
             sm, cl, static_cast<const char*>(p.backbone) + pidx * p.V * (kDtype == kBF16 ? 2 : 4), lo, n, zs, res,
-            bad);
-    res.status = bad ? kReqNonfinite : (res.argmax < 0 ? kReqEmpty : (pol_ok ? kReqOk : kReqBadPolicy));
+            bad, late);
+    res.status = late ? kReqTimeout
+                      : bad ? kReqNonfinite : (res.argmax < 0 ? kReqEmpty : (pol_ok ? kReqOk : kReqBadPolicy));
     if (res.status != kReqOk) {
         if (rank == 0 && tid == 0) {
             p.proposals[pidx] = -1;
@@ -331,14 +333,10 @@ __global__ void __cluster_dims__(rp::kC, 1, 1) __launch_bounds__(rp::kThreads)
                     s_qx = 0.0f;
                 }
                 __syncthreads();
-                if (tid == 0) {
-                    // q(x): the weight of x over the support mass
-                    for (int e = 0; e < res.count; ++e)
-                        if (rp::io_idx(cbuf[e]) == xk) {
-                            s_qx = rp::weight_f(key_to_float(rp::io_key(cbuf[e])), res.zmax, pol.inv_t) * invS;
-                            break;
-                        }
-                }
+                // q(x): the weight of x over the support mass (the buffer is in value order)
+                for (int e = tid; e < res.count; e += kThreads)
+                    if (rp::vo_idx(cbuf[e]) == xk)
+                        s_qx = rp::weight_f(key_to_float(rp::vo_key(cbuf[e])), res.zmax, pol.inv_t) * invS;
             }
         } else {
             unsigned long long total = 0;

@@ -10,14 +10,17 @@
 // renormalised exp((z - zmax) / T) on that support.
 //
 // Exactness: the support is described by a key threshold and an index cut
-// (support = {key > tau} + {key == tau, index <= cut}), found by radix selection
-// on order-preserving 32-bit keys; masses are fixed-point integers
-// w = round(2^40 exp((z - zmax)/T)), so every sum, every top-p comparison and
-// every inverse-CDF boundary is an exact, order-independent integer decision.
-// To keep the radix passes off the bulk of the row, the selection starts from
-// a window [zmax - D, zmax] chosen by a single counting (or mass) pass over 8
-// candidate widths, and the first digit starts after the common prefix of the
-// window's end keys.
+// (support = {key > tau} + {key == tau, index <= cut}); masses are fixed-point
+// integers w = round(2^40 exp((z - zmax)/T)), so every sum, every top-p
+// comparison and every inverse-CDF boundary is an exact, order-independent
+// integer decision.  To find the cut, one pass builds a histogram of
+// s = (zmax - z)/T in bins of 1/8 (counts, and fixed-point masses when top-p
+// applies to the whole row), reduced once over the cluster; the bin where the
+// cumulative count reaches k (or the mass reaches p of the total) bounds a
+// small candidate set, which is compacted into rank 0, sorted by (logit
+// descending, index ascending) and cut there by exact prefix sums.  Rows whose
+// candidates would not fit (very flat rows) fall back to radix selection on
+// order-preserving 32-bit keys over the slices.
 #pragma once
 
 #include <cooperative_groups.h>
@@ -87,7 +90,28 @@ struct Smem {
     int32_t pick[4];
     int parity;      // which exchange buffer is next
     int hparity;     // which histogram buffer is next
+    uint64_t lbar[4];        // slice load: one mbarrier per bulk-copy piece
+    uint32_t lphase;         // parity of the next slice load
+    unsigned int ccount;     // rank 0: candidate slots claimed by the cluster
 };
+constexpr int kLoadChunks = 4;
+
+// Called by every thread at kernel start, followed by a __syncthreads.
+__device__ __forceinline__ void init_smem(Smem& sm) {
+    if (threadIdx.x == 0) {
+        sm.parity = 0;
+        sm.hparity = 0;
+        sm.lphase = 0;
+        sm.ccount = 0;
+        for (int c = 0; c < kLoadChunks; ++c) mbar_init(&sm.lbar[c], 1);
+        fence_mbar_init();
+    }
+    // the candidate histogram (buffer 1 of the radix histograms) starts empty
+    for (int b = threadIdx.x; b < kBins; b += kThreads) {
+        sm.hcnt[1][b] = 0;
+        sm.hmass[1][b] = 0;
+    }
+}
 
 __device__ __forceinline__ bool in_set(uint32_t key, int32_t idx, uint32_t tau, int32_t cut) {
     return key > tau || (key == tau && idx <= cut);
@@ -518,43 +542,68 @@ __device__ int32_t sample_fixed(Smem& sm, cg::cluster_group& cl, const Slice& sl
     return idx;
 }
 
-// Load this CTA's slice of a row into shared memory (fp32) and reduce the
-// row's max key / lowest argmax / non-finite flag over the cluster.
+// Load this CTA's slice [lo, lo + n) of a row (n a multiple of 8, the start
+// 16-byte aligned) into shared memory with 1-D bulk copies in kLoadChunks
+// pieces, and reduce the row's max key / lowest argmax / non-finite flag over
+// the cluster as the pieces land.  timeout: a copy did not land in time (the
+// row's results are then not to be used).
 template <int kDtype>
 __device__ void load_slice_and_max(Smem& sm, cg::cluster_group& cl, const void* row, int lo, int n, void* zs,
-                                   RowResult& res, bool& bad) {
-    constexpr int kPer = kDtype == kBF16 ? 8 : 4;
+                                   RowResult& res, bool& bad, bool& timeout) {
     constexpr int kEsize = kDtype == kBF16 ? 2 : 4;
+    constexpr int kPer = 16 / kEsize;
     const char* src = static_cast<const char*>(row) + static_cast<int64_t>(lo) * kEsize;
+    char* dst = static_cast<char*>(zs);
+    const int per = ((n + kLoadChunks - 1) / kLoadChunks + 7) / 8 * 8;  // elements per piece
+    const uint32_t ph = sm.lphase;
+    __syncthreads();  // every thread is done with the previous contents of zs
+    if (threadIdx.x == 0) {
+        fence_proxy_async_smem();
+        for (int c = 0; c < kLoadChunks; ++c) {
+            const int a = min(c * per, n), e = min(a + per, n);
+            if (e > a) {
+                mbar_arrive_expect_tx(&sm.lbar[c], static_cast<uint32_t>((e - a) * kEsize));
+                bulk_g2s(dst + a * kEsize, src + a * kEsize, static_cast<uint32_t>((e - a) * kEsize), &sm.lbar[c]);
+            }
+        }
+        sm.lphase = ph ^ 1u;
+    }
     unsigned long long best = 0;
     float nanacc = -__int_as_float(0x7F800000);
-    const int nvec = n / kPer;
-    for (int j = threadIdx.x; j < nvec; j += kThreads) {
-        const uint4 v = ld_stream_v4(src + static_cast<int64_t>(j) * 16);
-        float x[kPer];
-        if constexpr (kDtype == kBF16) {  // kept as bf16
-            x[0] = bf16_lo(v.x); x[1] = bf16_hi(v.x); x[2] = bf16_lo(v.y); x[3] = bf16_hi(v.y);
-            x[4] = bf16_lo(v.z); x[5] = bf16_hi(v.z); x[6] = bf16_lo(v.w); x[7] = bf16_hi(v.w);
-            reinterpret_cast<uint4*>(zs)[j] = v;
-        } else {
-            x[0] = __uint_as_float(v.x); x[1] = __uint_as_float(v.y);
-            x[2] = __uint_as_float(v.z); x[3] = __uint_as_float(v.w);
-            reinterpret_cast<uint4*>(zs)[j] = v;
+    bool late = false;
+    for (int c = 0; c < kLoadChunks; ++c) {
+        const int a = min(c * per, n), e = min(a + per, n);
+        if (e <= a) continue;  // empty in every load of this kernel: its barrier never flips
+        if (!mbar_wait(&sm.lbar[c], ph, kWaitLimitNs)) {
+            late = true;  // give the copy a second bounded chance to land before moving on
+            mbar_wait(&sm.lbar[c], ph, kWaitLimitNs);
         }
+        for (int j = a / kPer + threadIdx.x; j < e / kPer; j += kThreads) {
+            const uint4 v = ld_shared_v4(dst + j * 16);
+            float x[kPer];
+            if constexpr (kDtype == kBF16) {
+                x[0] = bf16_lo(v.x); x[1] = bf16_hi(v.x); x[2] = bf16_lo(v.y); x[3] = bf16_hi(v.y);
+                x[4] = bf16_lo(v.z); x[5] = bf16_hi(v.z); x[6] = bf16_lo(v.w); x[7] = bf16_hi(v.w);
+            } else {
+                x[0] = __uint_as_float(v.x); x[1] = __uint_as_float(v.y);
+                x[2] = __uint_as_float(v.z); x[3] = __uint_as_float(v.w);
+            }
 #pragma unroll
-        for (int l = 0; l < kPer; ++l) {
-            nanacc = fmax_nan(nanacc, x[l]);
-            if (x[l] > -__int_as_float(0x7F800000)) {
-                const unsigned long long k =
-                    (static_cast<unsigned long long>(ordered_key(x[l])) << 32) |
-                    (0xFFFFFFFFull - static_cast<uint32_t>(lo + j * kPer + l));
-                best = k > best ? k : best;
+            for (int l = 0; l < kPer; ++l) {
+                nanacc = fmax_nan(nanacc, x[l]);
+                if (x[l] > -__int_as_float(0x7F800000)) {
+                    const unsigned long long k =
+                        (static_cast<unsigned long long>(ordered_key(x[l])) << 32) |
+                        (0xFFFFFFFFull - static_cast<uint32_t>(lo + j * kPer + l));
+                    best = k > best ? k : best;
+                }
             }
         }
     }
     unsigned long long mk, fl;
-    cluster_max_u64(sm, cl, best, bad_logit(nanacc) ? 1ull : 0ull, mk, fl);
-    bad = fl != 0;
+    cluster_max_u64(sm, cl, best, (bad_logit(nanacc) ? 1ull : 0ull) | (late ? 2ull : 0ull), mk, fl);
+    bad = (fl & 1ull) != 0;
+    timeout = (fl & 2ull) != 0;
     if (mk == 0) {
         res.zmax = -__int_as_float(0x7F800000);
         res.argmax = -1;
@@ -607,6 +656,63 @@ __device__ void sort_desc(unsigned long long* buf, int n) {
     }
 }
 
+// Sort buf[0, n) descending.  Up to kThreads distinct keys: each thread
+// places one key at its rank (the number of larger keys), one pass over the
+// keys in shared memory; larger sets: the bitonic network.  All threads of
+// the CTA.
+__device__ void sort_candidates(unsigned long long* buf, int n) {
+    if (n > kThreads) {
+        sort_desc(buf, n);
+        return;
+    }
+    const int t = threadIdx.x;
+    unsigned long long c = 0;
+    int r = 0;
+    if (t < n) {
+        c = buf[t];
+        for (int j = 0; j < n; ++j) r += buf[j] > c ? 1 : 0;
+    }
+    __syncthreads();
+    if (t < n) buf[r] = c;
+    __syncthreads();
+}
+
+// Compact the elements of the slice for which pick(z, index) holds into rank
+// 0's candidate buffer as value-order composite keys: each warp claims its
+// slots with one atomic on rank 0's counter (slot order is arbitrary; the
+// buffer is sorted afterwards).  Writes past kCap are dropped.  Rank 0's
+// counter must be zero and visible to the cluster (a cluster barrier after
+// its reset) before the call; ends with a cluster barrier.
+template <typename Pick>
+__device__ void compact_candidates(Smem& sm, cg::cluster_group& cl, const Slice& sl, unsigned long long* cbuf,
+                                   Pick pick) {
+    const int lane = threadIdx.x & 31;
+    unsigned int* rcount = cl.map_shared_rank(&sm.ccount, 0);
+    unsigned long long* dst = cl.map_shared_rank(cbuf, 0);
+    for (int i0 = 0; i0 < sl.n; i0 += kThreads) {  // the same trip count for every thread
+        const int i = i0 + static_cast<int>(threadIdx.x);
+        bool take = false;
+        uint32_t key = 0;
+        if (i < sl.n) {
+            const float z = sl.val(i);
+            take = pick(z, sl.lo + i);
+            key = ordered_key(z);
+        }
+        const unsigned mask = __ballot_sync(0xFFFFFFFFu, take);
+        if (mask) {
+            const int leader = __ffs(mask) - 1;
+            unsigned base = 0;
+            if (lane == leader) base = atomicAdd(rcount, static_cast<unsigned>(__popc(mask)));
+            base = __shfl_sync(0xFFFFFFFFu, base, leader);
+            if (take) {
+                const unsigned at = base + static_cast<unsigned>(__popc(mask & ((1u << lane) - 1u)));
+                if (at < static_cast<unsigned>(kCap)) dst[at] = value_order(key, sl.lo + i);
+            }
+        }
+    }
+    cl.sync();
+}
+
 // First position i in [0, n) whose inclusive prefix of w(i) satisfies
 // prefix >= th (strict = false) or prefix > th (strict = true); n if none.
 // Also returns the total.  All threads of one CTA; w is evaluated in
@@ -647,13 +753,16 @@ __device__ int find_crossing(Smem& sm, int n, unsigned long long th, bool strict
 __device__ __forceinline__ float k_width(int w) { return 0.25f * static_cast<float>(1 << w); }
 __device__ __forceinline__ float p_width(int w) { return 0.5f * static_cast<float>(1 << w); }
 
-// The policy of the row held by the cluster.  The elements that can belong
-// to a truncated support (the top-k set, or the top of the row holding the
-// top-p mass) are compacted into rank 0's candidate buffer, sorted by
-// (logit descending, index ascending), and the cuts are taken there by
-// exact fixed-point prefix sums.  cbuf = this CTA's candidate buffer (only
-// rank 0's is used).  Falls back to row_policy_radix if the candidates would
-// not fit.
+// The policy of the row held by the cluster.  One pass builds the histogram
+// of s = (zmax - z)/T in bins of 1/8 below s = 32 (beyond, the weight is 0 in
+// fixed point): counts, plus fixed-point masses when top-k is off.  Its
+// cluster sum gives the bin where the cumulative count reaches k (top-k) or
+// the cumulative mass reaches p of the total (top-p alone); every element of
+// the support lies at or below that bin.  Those candidates are compacted into
+// rank 0's buffer, sorted by (logit descending, index ascending), and the
+// cuts are taken there by exact fixed-point prefix sums.  cbuf = this CTA's
+// candidate buffer (only rank 0's is used).  Falls back to row_policy_radix
+// when the candidates would not fit kCap.
 __device__ void row_policy(Smem& sm, cg::cluster_group& cl, const Slice& sl, int V, const Policy& pol,
                            RowResult& res, unsigned long long* cbuf) {
     const float zmax = res.zmax;
@@ -669,25 +778,41 @@ __device__ void row_policy(Smem& sm, cg::cluster_group& cl, const Slice& sl, int
     const float inv_t = pol.inv_t;
     const bool use_k = pol.top_k > 0;
     const bool use_p = pol.top_p < 1.0f;
-    constexpr float kZeroWeight = 41.0f * 0.6931472f + 1.0f;  // beyond: the weight rounds to 0
+    const bool with_mass = !use_k;  // the kept set is the whole row: its mass, and the top-p crossing
 
-    // ---- total mass when top-k is off (the kept set is the whole row)
-    unsigned long long total_mass = 0;
-    if (!use_k) {
-        unsigned long long v[1] = {0}, o[1];
-        for (int i = tid; i < sl.n; i += kThreads) {
-            const float z = sl.val(i);
-            if ((zmax - z) * inv_t <= kZeroWeight) v[0] += to_fixed(weight_f(z, zmax, inv_t));
+    // ---- histogram (buffer 1 of the radix histograms, zeroed at kernel start)
+    uint32_t* hc = sm.hcnt[1];
+    unsigned long long* hm = sm.hmass[1];
+    for (int i = tid; i < sl.n; i += kThreads) {
+        const float z = sl.val(i);
+        const float sc = (zmax - z) * inv_t;
+        if (sc < 32.0f) {
+            const int bin = min(kBins - 1, static_cast<int>(sc * 8.0f));
+            atomicAdd(&hc[bin], 1u);
+            if (with_mass) atomicAdd(&hm[bin], static_cast<unsigned long long>(to_fixed(weight_f(z, zmax, inv_t))));
         }
-        cluster_sum_u64<1>(sm, cl, v, o);
-        total_mass = o[0];
-        if (!use_p) {  // no truncation: the whole vocabulary
-            res.tau = 0u;
-            res.cut = -1;
-            res.mass = total_mass;
-            res.count = V;
-            return;
-        }
+    }
+    cl.sync();
+    unsigned long long c = 0, m = 0;  // bin tid of the cluster's histogram
+#pragma unroll
+    for (int r = 0; r < kC; ++r) {
+        c += cl.map_shared_rank(hc, r)[tid];
+        if (with_mass) m += cl.map_shared_rank(hm, r)[tid];
+    }
+    const unsigned long long cc = block_scan_u64(sm, c);
+    const unsigned long long cm = with_mass ? block_scan_u64(sm, m) : 0ull;
+    __shared__ unsigned long long s_total_mass, s_count;
+    __shared__ int s_bin;
+    if (tid == kThreads - 1) s_total_mass = cm;
+    if (tid == 0) s_bin = -1;
+    __syncthreads();
+    const unsigned long long total_mass = s_total_mass;
+    if (!use_k && !use_p) {  // no truncation: the whole vocabulary
+        res.tau = 0u;
+        res.cut = -1;
+        res.mass = total_mass;
+        res.count = V;
+        return;
     }
     unsigned long long theta = 0;
     if (!use_k) {
@@ -695,99 +820,39 @@ __device__ void row_policy(Smem& sm, cg::cluster_group& cl, const Slice& sl, int
         theta = th < 1.0 ? 1ull : static_cast<unsigned long long>(th);
         if (theta > total_mass) theta = total_mass;
     }
-
-    // ---- window estimate from one element in kSample
-    unsigned long long est[kWin], eo[kWin];
-#pragma unroll
-    for (int w = 0; w < kWin; ++w) est[w] = 0;
-    for (int i = tid * kSample; i < sl.n; i += kThreads * kSample) {
-        const float z = sl.val(i);
-        if (use_k) {
-            const float d = zmax - z;
-#pragma unroll
-            for (int w = 0; w < kWin; ++w) est[w] += d <= k_width(w) ? 1ull : 0ull;
-        } else {
-            const float d = (zmax - z) * inv_t;
-            if (d <= kZeroWeight) {
-                const unsigned long long wt = to_fixed(weight_f(z, zmax, inv_t));
-#pragma unroll
-                for (int w = 0; w < kWin; ++w) est[w] += d <= p_width(w) ? wt : 0ull;
-            }
-        }
-    }
-    cluster_sum_u64<kWin>(sm, cl, est, eo);
     const unsigned long long need = use_k ? static_cast<unsigned long long>(pol.top_k) : theta;
-    int w = kWin;  // kWin = the whole row
-    for (int i = kWin - 1; i >= 0; --i)
-        if (eo[i] * kSample >= need + need / 4 + (use_k ? 32ull : 0ull)) w = i;
-
-    // ---- exact candidate count (and mass), widening until it suffices
-    int count = 0;
-    bool fits = false;
-    float zthr = 0.0f;
-    for (;;) {
-        zthr = w >= kWin ? -__int_as_float(0x7F800000)
-                         : (use_k ? zmax - k_width(w) : zmax - p_width(w) / inv_t);
-        unsigned long long v[2] = {0, 0}, o[2];
-        for (int i = tid; i < sl.n; i += kThreads) {
-            const float z = sl.val(i);
-            if (z >= zthr) {
-                v[0] += 1;
-                if (!use_k && (zmax - z) * inv_t <= kZeroWeight) v[1] += to_fixed(weight_f(z, zmax, inv_t));
-            }
-        }
-        cluster_sum_u64<2>(sm, cl, v, o);
-        const bool enough = use_k ? o[0] >= need : o[1] >= need;
-        if (enough || w >= kWin) {
-            count = static_cast<int>(min(o[0], static_cast<unsigned long long>(0x7FFFFFFF)));
-            fits = o[0] <= static_cast<unsigned long long>(kCap);
-            break;
-        }
-        ++w;
+    const unsigned long long incl = use_k ? cc : cm, here = use_k ? c : m;
+    if (incl >= need && incl - here < need) {  // the crossing bin (unique)
+        s_bin = tid;
+        s_count = cc;
     }
-    if (!fits) {  // too many candidates: radix selection over the slices
+    __syncthreads();
+    const int bstar = s_bin;
+    const unsigned long long count = bstar >= 0 ? s_count : 0ull;
+    __syncthreads();
+    if (bstar < 0 || count > static_cast<unsigned long long>(kCap)) {  // flat row: radix selection
         row_policy_radix(sm, cl, sl, V, pol, res);
         res.count = 0x7FFFFFFF;
         return;
     }
 
-    // ---- compact the candidates into rank 0's buffer
-    __shared__ unsigned int s_n;
-    if (tid == 0) s_n = 0;
-    __syncthreads();
-    unsigned int mine = 0;
-    for (int i = tid; i < sl.n; i += kThreads) mine += sl.val(i) >= zthr ? 1u : 0u;
-    unsigned long long gathered[kC];
-    {
-        // this CTA's candidate count, then the prefix over ranks
-        const unsigned long long incl = block_scan_u64(sm, mine);
-        __shared__ unsigned long long s_cnt;
-        if (tid == kThreads - 1) s_cnt = incl;
-        __syncthreads();
-        cluster_gather_u64(sm, cl, s_cnt, gathered);
-    }
-    unsigned long long base = 0;
-    for (int r = 0; r < rank; ++r) base += gathered[r];
-    unsigned long long* dst = cl.map_shared_rank(cbuf, 0);
-    for (int i = tid; i < sl.n; i += kThreads) {
-        const float z = sl.val(i);
-        if (z >= zthr) {
-            const unsigned long long at = base + atomicAdd(&s_n, 1u);
-            if (at < static_cast<unsigned long long>(kCap)) dst[at] = value_order(ordered_key(z), sl.lo + i);
-        }
-    }
-    cl.sync();
+    // ---- compact the candidates (bins <= bstar) into rank 0's buffer
+    compact_candidates(sm, cl, sl, cbuf, [&](float z, int32_t) {
+        const float sc = (zmax - z) * inv_t;
+        return sc < 32.0f && min(kBins - 1, static_cast<int>(sc * 8.0f)) <= bstar;
+    });
 
     // ---- rank 0: sort, take the cuts
     const int buf = sm.parity;
     if (rank == 0) {
-        sort_desc(cbuf, count);
-        const int K = use_k ? min(pol.top_k, count) : count;
+        const int n = static_cast<int>(min(static_cast<unsigned long long>(sm.ccount), count));
+        sort_candidates(cbuf, n);
+        const int K = use_k ? min(pol.top_k, n) : n;
         auto wt = [&](int i) -> unsigned long long {
             return i < K ? to_fixed(weight_f(key_to_float(vo_key(cbuf[i])), zmax, inv_t)) : 0ull;
         };
         unsigned long long kept = 0;
-        int m = K;
+        int mm = K;
         if (use_k) {
             find_crossing(sm, K, 0ull, true, wt, kept);  // the kept mass
         } else {
@@ -802,17 +867,17 @@ __device__ void row_policy(Smem& sm, cg::cluster_group& cl, const Slice& sl, int
             }
             unsigned long long tot;
             const int pos = find_crossing(sm, K, theta, false, wt, tot);
-            m = min(pos + 1, K);
+            mm = min(pos + 1, K);
             unsigned long long pm;
-            find_crossing(sm, m, 0ull, true, wt, pm);  // mass of the first m
+            find_crossing(sm, mm, 0ull, true, wt, pm);  // mass of the first mm
             mass = pm;
         }
         if (tid == 0) {
-            const unsigned long long last = cbuf[m - 1];
+            const unsigned long long last = cbuf[mm - 1];
             sm.xu[buf][0] = vo_key(last);
             sm.xu[buf][1] = static_cast<unsigned long long>(static_cast<uint32_t>(vo_idx(last)));
             sm.xu[buf][2] = mass;
-            sm.xu[buf][3] = static_cast<unsigned long long>(m);
+            sm.xu[buf][3] = static_cast<unsigned long long>(mm);
         }
     }
     cl.sync();
@@ -829,12 +894,48 @@ __device__ void row_policy(Smem& sm, cg::cluster_group& cl, const Slice& sl, int
 }
 
 // Inverse-CDF draw over a support held in rank 0's candidate buffer (its
-// first n composite keys, in value order): re-keyed by token index, sorted,
-// and drawn by exact prefix sums of w(key, index).  Returns the token in
-// rank 0 (other ranks: -1).  Rank 0's threads only.
+// first n composite keys, in value order), in token-index order: the element
+// whose token-order prefix of w(key, index) straddles floor(m * total / 2^24),
+// m the 24-bit uniform.  Up to kThreads elements: each thread weighs one
+// element once and sums the weights of the lower-indexed ones; larger sets
+// are re-keyed by index and sorted.  Returns the token in rank 0 (-1 if the
+// total is 0).  Rank 0's threads only; the buffer's upper half is scratch.
 template <typename Wf>
 __device__ int32_t draw_small_support(Smem& sm, unsigned long long* cbuf, int n, uint32_t m24, Wf w,
                                       unsigned long long& total) {
+    if (n <= kThreads) {
+        unsigned long long* wbuf = cbuf + kCap / 2;
+        int32_t* ibuf = reinterpret_cast<int32_t*>(cbuf + kCap / 2 + kThreads);
+        const int t = threadIdx.x;
+        unsigned long long wt = 0;
+        int32_t idx = 0x7FFFFFFF;
+        if (t < n) {
+            const unsigned long long c = cbuf[t];
+            idx = vo_idx(c);
+            wt = w(vo_key(c), idx);
+            wbuf[t] = wt;
+            ibuf[t] = idx;
+        }
+        const unsigned long long incl = block_scan_u64(sm, wt);  // also orders the scratch writes
+        __shared__ unsigned long long s_tot;
+        __shared__ int32_t s_pick;
+        if (t == kThreads - 1) s_tot = incl;
+        if (t == 0) s_pick = -1;
+        __syncthreads();
+        total = s_tot;
+        if (total == 0) return -1;
+        const unsigned long long target =
+            static_cast<unsigned long long>((static_cast<unsigned __int128>(m24) * total) >> 24);
+        if (t < n && wt > 0) {
+            unsigned long long before = 0;
+            for (int j = 0; j < n; ++j) before += ibuf[j] < idx ? wbuf[j] : 0ull;
+            if (before <= target && target < before + wt) s_pick = idx;
+        }
+        __syncthreads();
+        const int32_t pick = s_pick;
+        __syncthreads();
+        return pick;
+    }
     for (int i = threadIdx.x; i < n; i += kThreads) {
         const unsigned long long c = cbuf[i];
         cbuf[i] = index_order(vo_key(c), vo_idx(c));
@@ -850,43 +951,25 @@ __device__ int32_t draw_small_support(Smem& sm, unsigned long long* cbuf, int n,
         static_cast<unsigned long long>((static_cast<unsigned __int128>(m24) * tot) >> 24);
     unsigned long long t2;
     const int pos = find_crossing(sm, n, target, true, wi, t2);
-    return pos < n ? io_idx(cbuf[pos]) : io_idx(cbuf[n - 1]);
+    const int32_t pick = pos < n ? io_idx(cbuf[pos]) : io_idx(cbuf[n - 1]);
+    __syncthreads();
+    for (int i = threadIdx.x; i < n; i += kThreads) {  // back to value order keys
+        const unsigned long long c = cbuf[i];
+        cbuf[i] = value_order(io_key(c), io_idx(c));
+    }
+    __syncthreads();
+    return pick;
 }
 
 // Compact the elements of the slice satisfying pred(key, index) into rank 0's
-// candidate buffer in value order (as value_order keys); returns their total
-// (every CTA).  The caller guarantees the total fits kCap.
+// candidate buffer in value order (as value_order keys); returns their count
+// in rank 0 (capped at kCap).  Rank 0's counter must have been reset before a
+// preceding cluster barrier.
 template <typename Pred>
 __device__ int compact_to_rank0(Smem& sm, cg::cluster_group& cl, const Slice& sl, unsigned long long* cbuf,
                                 Pred pred) {
-    const int tid = threadIdx.x;
-    const int rank = static_cast<int>(cl.block_rank());
-    __shared__ unsigned int s_n2;
-    __shared__ unsigned long long s_cnt2;
-    if (tid == 0) s_n2 = 0;
-    unsigned int mine = 0;
-    for (int i = tid; i < sl.n; i += kThreads) mine += pred(ordered_key(sl.val(i)), sl.lo + i) ? 1u : 0u;
-    const unsigned long long incl = block_scan_u64(sm, mine);
-    if (tid == kThreads - 1) s_cnt2 = incl;
-    __syncthreads();
-    unsigned long long counts[kC];
-    cluster_gather_u64(sm, cl, s_cnt2, counts);
-    unsigned long long base = 0, total = 0;
-    for (int r = 0; r < kC; ++r) {
-        if (r < rank) base += counts[r];
-        total += counts[r];
-    }
-    unsigned long long* dst = cl.map_shared_rank(cbuf, 0);
-    total = min(total, static_cast<unsigned long long>(kCap));
-    for (int i = tid; i < sl.n; i += kThreads) {
-        const uint32_t key = ordered_key(sl.val(i));
-        if (pred(key, sl.lo + i)) {
-            const unsigned long long at = base + atomicAdd(&s_n2, 1u);
-            if (at < static_cast<unsigned long long>(kCap)) dst[at] = value_order(key, sl.lo + i);
-        }
-    }
-    cl.sync();
-    return static_cast<int>(total);
+    compact_candidates(sm, cl, sl, cbuf, [&](float z, int32_t idx) { return pred(ordered_key(z), idx); });
+    return static_cast<int>(min(sm.ccount, static_cast<unsigned int>(kCap)));
 }
 
 // Normalise a request's policy record; returns false for an invalid one.
