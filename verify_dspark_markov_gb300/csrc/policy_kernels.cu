@@ -176,9 +176,9 @@ __global__ void __cluster_dims__(rp::kC, 1, 1) __launch_bounds__(rp::kThreads)
             return rp::to_fixed(fmaxf(pv - qrow[idx], 0.0f));
         };
         int32_t token = -1;
-        if (rr.count <= rp::kCap) {
+        if (rr.count <= rp::kThreads) {
             // small support: gathered in rank 0, drawn in token order
-            const int cnt = rp::compact_to_rank0(sm, cl, sl, cbuf, [&](uint32_t key, int32_t idx) {
+            const int cnt = rp::compact_to_rank0(sm, cl, sl, cbuf, rp::support_floor(rr.tau), [&](uint32_t key, int32_t idx) {
                 return rp::in_set(key, idx, rr.tau, rr.cut);
             });
             if (rank == 0) {
@@ -312,13 +312,32 @@ __global__ void __cluster_dims__(rp::kC, 1, 1) __launch_bounds__(rp::kThreads)
     } else {
         const float invS = inv_mass(res.mass);
         float* qrow = p.q + pidx * p.V + lo;
-        for (int li = tid; li < n; li += kThreads) {
-            const float z = sl.val(li);
-            qrow[li] = rp::in_set(ordered_key(z), lo + li, res.tau, res.cut) ? rp::weight_f(z, res.zmax, pol.inv_t) * invS
-                                                                               : 0.0f;
+        {
+            // q over the slice, 16-byte vectors at a time; only support
+            // elements (key >= tau) need their weight
+            const float zt = rp::support_floor(res.tau);
+            const int vp = sl.vper(), nv = sl.nvec();
+            for (int j = tid; j < nv; j += kThreads) {
+                const uint4 v = sl.vec(j);
+                float q8[8];
+#pragma unroll
+                for (int l = 0; l < 8; ++l) q8[l] = 0.0f;
+                if (rp::vec_max(v, sl.bf16) >= zt) {
+#pragma unroll
+                    for (int l = 0; l < 8; ++l) {
+                        if (l >= vp) break;
+                        const float z = rp::vec_elem(v, l, sl.bf16);
+                        if (rp::in_set(ordered_key(z), lo + j * vp + l, res.tau, res.cut))
+                            q8[l] = rp::weight_f(z, res.zmax, pol.inv_t) * invS;
+                    }
+                }
+                float4* d = reinterpret_cast<float4*>(qrow + j * vp);
+                d[0] = make_float4(q8[0], q8[1], q8[2], q8[3]);
+                if (vp == 8) d[1] = make_float4(q8[4], q8[5], q8[6], q8[7]);
+            }
         }
         const uint32_t m24 = uniform_bits24(p.seed[b], p.request_id[b], p.pos0[b] + k, 0);
-        if (res.in_buf) {
+        if (res.in_buf && res.count <= rp::kThreads) {
             // the support is rank 0's first res.count candidates
             if (rank == 0) {
                 unsigned long long total = 0;
@@ -360,7 +379,7 @@ __global__ void __cluster_dims__(rp::kC, 1, 1) __launch_bounds__(rp::kThreads)
         // the rank holding the draw's results: 0 for greedy / small supports,
         // the owner of x for a draw over every slice
         int src = 0;
-        if (!pol.greedy && !res.in_buf) {
+        if (!pol.greedy && !(res.in_buf && res.count <= rp::kThreads)) {
             for (int r = 0; r < kC; ++r)
                 if (*cl.map_shared_rank(&s_x, r) >= 0) { src = r; break; }
         }

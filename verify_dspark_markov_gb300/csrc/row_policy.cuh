@@ -116,6 +116,12 @@ __device__ __forceinline__ void init_smem(Smem& sm) {
 __device__ __forceinline__ bool in_set(uint32_t key, int32_t idx, uint32_t tau, int32_t cut) {
     return key > tau || (key == tau && idx <= cut);
 }
+// A value below which no element of the support {key > tau} + {key == tau,
+// ...} lies: the value of key tau, or -inf when tau is below the key of -inf
+// (tau = 0: the whole row).
+__device__ __forceinline__ float support_floor(uint32_t tau) {
+    return tau <= ordered_key(-__int_as_float(0x7F800000)) ? -__int_as_float(0x7F800000) : key_to_float(tau);
+}
 
 // Block-sum of up to kWin+2 uint64 values per thread, then a cluster-sum; every
 // thread of every CTA returns the same totals in out[].
@@ -250,7 +256,49 @@ struct Slice {
         return bf16 ? __uint_as_float(static_cast<uint32_t>(static_cast<const uint16_t*>(z)[i]) << 16)
                     : static_cast<const float*>(z)[i];
     }
+    // 16-byte vectors: 8 (bf16) or 4 (fp32) elements each; n is a multiple of 8
+    __device__ __forceinline__ int vper() const { return bf16 ? 8 : 4; }
+    __device__ __forceinline__ int nvec() const { return n / vper(); }
+    __device__ __forceinline__ uint4 vec(int j) const { return ld_shared_v4(static_cast<const char*>(z) + j * 16); }
 };
+
+__device__ __forceinline__ uint32_t bf16x2_max(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+// NaN-propagating maximum of one 16-byte vector of the slice's format.
+__device__ __forceinline__ float vec_max(const uint4& v, int bf16) {
+    if (bf16) {
+        const uint32_t m = bf16x2_max(bf16x2_max(v.x, v.y), bf16x2_max(v.z, v.w));
+        return fmax_nan(bf16_lo(m), bf16_hi(m));
+    }
+    return fmax_nan(fmax_nan(__uint_as_float(v.x), __uint_as_float(v.y)),
+                    fmax_nan(__uint_as_float(v.z), __uint_as_float(v.w)));
+}
+// Element l of a vector of the slice's format.
+__device__ __forceinline__ float vec_elem(const uint4& v, int l, int bf16) {
+    if (bf16) {
+        const uint32_t w = l < 2 ? v.x : l < 4 ? v.y : l < 6 ? v.z : v.w;
+        return (l & 1) ? bf16_hi(w) : bf16_lo(w);
+    }
+    return __uint_as_float(l == 0 ? v.x : l == 1 ? v.y : l == 2 ? v.z : v.w);
+}
+
+// The smallest value t (as an ordered key) with pred(t) true, for a predicate
+// that is monotone in the value (false below some point, true from there up
+// to kmax, and true at kmax): bisection over the ordered keys [1, kmax].
+// Every thread computes the same result without communication.
+template <typename P>
+__device__ __forceinline__ uint32_t lowest_true_key(uint32_t kmax, P pred) {
+    uint32_t lo = 1, hi = kmax;  // pred(key_to_float(hi)) holds
+    while (lo < hi) {
+        const uint32_t mid = lo + (hi - lo) / 2;
+        if (pred(key_to_float(mid))) hi = mid;
+        else lo = mid + 1;
+    }
+    return hi;
+}
 
 // Radix selection on keys: among elements matching `pred` with key in the
 // range sharing the common prefix of [klo, khi], find the key tau at which the
@@ -570,6 +618,8 @@ __device__ void load_slice_and_max(Smem& sm, cg::cluster_group& cl, const void* 
     }
     unsigned long long best = 0;
     float nanacc = -__int_as_float(0x7F800000);
+    float bval = -__int_as_float(0x7F800000);  // this thread's maximum (vectors in index order)
+    int32_t bidx = -1;
     bool late = false;
     for (int c = 0; c < kLoadChunks; ++c) {
         const int a = min(c * per, n), e = min(a + per, n);
@@ -580,26 +630,20 @@ __device__ void load_slice_and_max(Smem& sm, cg::cluster_group& cl, const void* 
         }
         for (int j = a / kPer + threadIdx.x; j < e / kPer; j += kThreads) {
             const uint4 v = ld_shared_v4(dst + j * 16);
-            float x[kPer];
-            if constexpr (kDtype == kBF16) {
-                x[0] = bf16_lo(v.x); x[1] = bf16_hi(v.x); x[2] = bf16_lo(v.y); x[3] = bf16_hi(v.y);
-                x[4] = bf16_lo(v.z); x[5] = bf16_hi(v.z); x[6] = bf16_lo(v.w); x[7] = bf16_hi(v.w);
-            } else {
-                x[0] = __uint_as_float(v.x); x[1] = __uint_as_float(v.y);
-                x[2] = __uint_as_float(v.z); x[3] = __uint_as_float(v.w);
-            }
+            const float vm = vec_max(v, kDtype == kBF16);
+            nanacc = fmax_nan(nanacc, vm);
+            if (vm > bval) {  // rare: a new maximum of this thread; its first occurrence
+                int l0 = kPer - 1;
 #pragma unroll
-            for (int l = 0; l < kPer; ++l) {
-                nanacc = fmax_nan(nanacc, x[l]);
-                if (x[l] > -__int_as_float(0x7F800000)) {
-                    const unsigned long long k =
-                        (static_cast<unsigned long long>(ordered_key(x[l])) << 32) |
-                        (0xFFFFFFFFull - static_cast<uint32_t>(lo + j * kPer + l));
-                    best = k > best ? k : best;
-                }
+                for (int l = kPer - 1; l >= 0; --l)
+                    if (vec_elem(v, l, kDtype == kBF16) == vm) l0 = l;
+                bval = vm;
+                bidx = lo + j * kPer + l0;
             }
         }
     }
+    if (bidx >= 0 && !bad_logit(bval))
+        best = (static_cast<unsigned long long>(ordered_key(bval)) << 32) | (0xFFFFFFFFull - static_cast<uint32_t>(bidx));
     unsigned long long mk, fl;
     cluster_max_u64(sm, cl, best, (bad_logit(nanacc) ? 1ull : 0ull) | (late ? 2ull : 0ull), mk, fl);
     bad = (fl & 1ull) != 0;
@@ -632,23 +676,23 @@ __device__ __forceinline__ int32_t io_idx(unsigned long long c) {
 }
 
 // Bitonic sort of buf[0, n) in descending order (n <= kCap), padding with 0
-// (below every real composite key) up to a power of two.  All threads of the CTA.
+// (below every real composite key) up to a power of two.  Each iteration
+// handles one compare-exchange pair.  All threads of the CTA.
 __device__ void sort_desc(unsigned long long* buf, int n) {
     int P = 1;
     while (P < n) P <<= 1;
     for (int i = n + threadIdx.x; i < P; i += kThreads) buf[i] = 0ull;
     __syncthreads();
+    const int half = P >> 1;
     for (int k = 2; k <= P; k <<= 1) {
         for (int j = k >> 1; j > 0; j >>= 1) {
-            for (int i = threadIdx.x; i < P; i += kThreads) {
-                const int ixj = i ^ j;
-                if (ixj > i) {
-                    const unsigned long long a = buf[i], b = buf[ixj];
-                    const bool down = (i & k) == 0;
-                    if (down ? (a < b) : (a > b)) {
-                        buf[i] = b;
-                        buf[ixj] = a;
-                    }
+            for (int q = threadIdx.x; q < half; q += kThreads) {
+                const int i = ((q & ~(j - 1)) << 1) | (q & (j - 1));
+                const int ixj = i + j;
+                const unsigned long long a = buf[i], b = buf[ixj];
+                if ((i & k) == 0 ? (a < b) : (a > b)) {
+                    buf[i] = b;
+                    buf[ixj] = a;
                 }
             }
             __syncthreads();
@@ -678,35 +722,48 @@ __device__ void sort_candidates(unsigned long long* buf, int n) {
 }
 
 // Compact the elements of the slice for which pick(z, index) holds into rank
-// 0's candidate buffer as value-order composite keys: each warp claims its
-// slots with one atomic on rank 0's counter (slot order is arbitrary; the
-// buffer is sorted afterwards).  Writes past kCap are dropped.  Rank 0's
-// counter must be zero and visible to the cluster (a cluster barrier after
-// its reset) before the call; ends with a cluster barrier.
+// 0's candidate buffer as value-order composite keys.  Every picked element
+// is >= floor, so whole 16-byte vectors below it are skipped.  Each warp
+// claims its slots with one atomic on rank 0's counter (slot order is
+// arbitrary; the buffer is sorted afterwards); writes past kCap are dropped.
+// Rank 0's counter must be zero and visible to the cluster (a cluster barrier
+// after its reset) before the call; ends with a cluster barrier.
 template <typename Pick>
 __device__ void compact_candidates(Smem& sm, cg::cluster_group& cl, const Slice& sl, unsigned long long* cbuf,
-                                   Pick pick) {
+                                   float floor, Pick pick) {
     const int lane = threadIdx.x & 31;
     unsigned int* rcount = cl.map_shared_rank(&sm.ccount, 0);
     unsigned long long* dst = cl.map_shared_rank(cbuf, 0);
-    for (int i0 = 0; i0 < sl.n; i0 += kThreads) {  // the same trip count for every thread
-        const int i = i0 + static_cast<int>(threadIdx.x);
-        bool take = false;
-        uint32_t key = 0;
-        if (i < sl.n) {
-            const float z = sl.val(i);
-            take = pick(z, sl.lo + i);
-            key = ordered_key(z);
+    const int vp = sl.vper(), nv = sl.nvec();
+    for (int j0 = 0; j0 < nv; j0 += kThreads) {  // the same trip count for every thread
+        const int j = j0 + static_cast<int>(threadIdx.x);
+        unsigned mine = 0;  // bit l: element l of vector j is picked
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (j < nv) {
+            v = sl.vec(j);
+            if (vec_max(v, sl.bf16) >= floor) {
+#pragma unroll
+                for (int l = 0; l < 8; ++l)
+                    if (l < vp && pick(vec_elem(v, l, sl.bf16), sl.lo + j * vp + l)) mine |= 1u << l;
+            }
         }
-        const unsigned mask = __ballot_sync(0xFFFFFFFFu, take);
-        if (mask) {
-            const int leader = __ffs(mask) - 1;
-            unsigned base = 0;
-            if (lane == leader) base = atomicAdd(rcount, static_cast<unsigned>(__popc(mask)));
-            base = __shfl_sync(0xFFFFFFFFu, base, leader);
-            if (take) {
-                const unsigned at = base + static_cast<unsigned>(__popc(mask & ((1u << lane) - 1u)));
-                if (at < static_cast<unsigned>(kCap)) dst[at] = value_order(key, sl.lo + i);
+        if (!__any_sync(0xFFFFFFFFu, mine != 0u)) continue;
+        const unsigned cnt = static_cast<unsigned>(__popc(mine));
+        unsigned incl = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const unsigned y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        unsigned base = 0;
+        if (lane == 31) base = atomicAdd(rcount, incl);
+        base = __shfl_sync(0xFFFFFFFFu, base, 31) + incl - cnt;
+#pragma unroll
+        for (int l = 0; l < 8; ++l) {
+            if ((mine >> l) & 1u) {
+                if (base < static_cast<unsigned>(kCap))
+                    dst[base] = value_order(ordered_key(vec_elem(v, l, sl.bf16)), sl.lo + j * vp + l);
+                ++base;
             }
         }
     }
@@ -780,33 +837,73 @@ __device__ void row_policy(Smem& sm, cg::cluster_group& cl, const Slice& sl, int
     const bool use_p = pol.top_p < 1.0f;
     const bool with_mass = !use_k;  // the kept set is the whole row: its mass, and the top-p crossing
 
-    // ---- histogram (buffer 1 of the radix histograms, zeroed at kernel start)
+    // ---- histogram (buffer 1 of the radix histograms, zeroed at kernel start).
+    // Count-only rows add 1 to a 32-bit bin.  When top-k is off, one 64-bit
+    // atomic adds (1 << 40) + floor(w * 2^16) per element: the count in the
+    // high bits and a lower bound of the fixed-point mass (floor(w 2^16) 2^24
+    // <= round(w 2^40)) in the low 40 bits (at most 16160 * 2^16 < 2^40: no
+    // carry).  The exact total mass is summed in registers.
     uint32_t* hc = sm.hcnt[1];
-    unsigned long long* hm = sm.hmass[1];
-    for (int i = tid; i < sl.n; i += kThreads) {
-        const float z = sl.val(i);
-        const float sc = (zmax - z) * inv_t;
-        if (sc < 32.0f) {
-            const int bin = min(kBins - 1, static_cast<int>(sc * 8.0f));
-            atomicAdd(&hc[bin], 1u);
-            if (with_mass) atomicAdd(&hm[bin], static_cast<unsigned long long>(to_fixed(weight_f(z, zmax, inv_t))));
+    unsigned long long* hp = sm.hmass[1];
+    unsigned long long tmass = 0;
+    const bool hist = use_k || use_p;
+    {
+        const int vp = sl.vper(), nv = sl.nvec();
+        for (int j = tid; j < nv; j += kThreads) {
+            const uint4 v = sl.vec(j);
+            if ((zmax - vec_max(v, sl.bf16)) * inv_t >= 32.0f) continue;  // the whole vector is out of range
+#pragma unroll
+            for (int l = 0; l < 8; ++l) {
+                if (l >= vp) break;
+                const float z = vec_elem(v, l, sl.bf16);
+                const float sc = (zmax - z) * inv_t;
+                if (sc < 32.0f) {
+                    const int bin = min(kBins - 1, static_cast<int>(sc * 8.0f));
+                    if (with_mass) {
+                        const float w = weight_f(z, zmax, inv_t);
+                        tmass += to_fixed(w);
+                        if (hist) atomicAdd(&hp[bin], (1ull << 40) + __float2uint_rd(w * 65536.0f));
+                    } else {
+                        atomicAdd(&hc[bin], 1u);
+                    }
+                }
+            }
+        }
+    }
+    __shared__ unsigned long long s_ctot;  // this CTA's exact mass (top-k off)
+    if (with_mass) {
+        const int lane = tid & 31, warp = tid >> 5;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) tmass += __shfl_xor_sync(0xFFFFFFFFu, tmass, o);
+        if (lane == 0) sm.wu[warp][0] = tmass;
+        __syncthreads();
+        if (tid == 0) {
+            unsigned long long t = 0;
+            for (int w = 0; w < kWarps; ++w) t += sm.wu[w][0];
+            s_ctot = t;
         }
     }
     cl.sync();
-    unsigned long long c = 0, m = 0;  // bin tid of the cluster's histogram
+    unsigned long long c = 0, m = 0, total_mass = 0;  // bin tid of the cluster's histogram
+    if (with_mass) {
 #pragma unroll
-    for (int r = 0; r < kC; ++r) {
-        c += cl.map_shared_rank(hc, r)[tid];
-        if (with_mass) m += cl.map_shared_rank(hm, r)[tid];
+        for (int r = 0; r < kC; ++r) {
+            const unsigned long long pk = cl.map_shared_rank(hp, r)[tid];
+            c += pk >> 40;
+            m += pk & ((1ull << 40) - 1ull);
+            total_mass += *cl.map_shared_rank(&s_ctot, r);
+        }
+        m <<= 24;  // lower bound of the bin's fixed-point mass
+    } else {
+#pragma unroll
+        for (int r = 0; r < kC; ++r) c += cl.map_shared_rank(hc, r)[tid];
     }
     const unsigned long long cc = block_scan_u64(sm, c);
     const unsigned long long cm = with_mass ? block_scan_u64(sm, m) : 0ull;
-    __shared__ unsigned long long s_total_mass, s_count;
+    __shared__ unsigned long long s_count;
     __shared__ int s_bin;
-    if (tid == kThreads - 1) s_total_mass = cm;
     if (tid == 0) s_bin = -1;
     __syncthreads();
-    const unsigned long long total_mass = s_total_mass;
     if (!use_k && !use_p) {  // no truncation: the whole vocabulary
         res.tau = 0u;
         res.cut = -1;
@@ -820,6 +917,9 @@ __device__ void row_policy(Smem& sm, cg::cluster_group& cl, const Slice& sl, int
         theta = th < 1.0 ? 1ull : static_cast<unsigned long long>(th);
         if (theta > total_mass) theta = total_mass;
     }
+    // Top-p alone: the first bin whose cumulative lower-bound mass reaches
+    // theta; the exact cumulative mass there is at least as large, so the
+    // support lies at or below it.
     const unsigned long long need = use_k ? static_cast<unsigned long long>(pol.top_k) : theta;
     const unsigned long long incl = use_k ? cc : cm, here = use_k ? c : m;
     if (incl >= need && incl - here < need) {  // the crossing bin (unique)
@@ -837,10 +937,12 @@ __device__ void row_policy(Smem& sm, cg::cluster_group& cl, const Slice& sl, int
     }
 
     // ---- compact the candidates (bins <= bstar) into rank 0's buffer
-    compact_candidates(sm, cl, sl, cbuf, [&](float z, int32_t) {
+    // the candidate test is monotone in z: one threshold value, found by bisection
+    const float zb = key_to_float(lowest_true_key(kmax, [&](float z) {
         const float sc = (zmax - z) * inv_t;
         return sc < 32.0f && min(kBins - 1, static_cast<int>(sc * 8.0f)) <= bstar;
-    });
+    }));
+    compact_candidates(sm, cl, sl, cbuf, zb, [zb](float z, int32_t) { return z >= zb; });
 
     // ---- rank 0: sort, take the cuts
     const int buf = sm.parity;
@@ -963,12 +1065,12 @@ __device__ int32_t draw_small_support(Smem& sm, unsigned long long* cbuf, int n,
 
 // Compact the elements of the slice satisfying pred(key, index) into rank 0's
 // candidate buffer in value order (as value_order keys); returns their count
-// in rank 0 (capped at kCap).  Rank 0's counter must have been reset before a
-// preceding cluster barrier.
+// in rank 0 (capped at kCap).  Every element satisfying pred is >= floor.
+// Rank 0's counter must have been reset before a preceding cluster barrier.
 template <typename Pred>
 __device__ int compact_to_rank0(Smem& sm, cg::cluster_group& cl, const Slice& sl, unsigned long long* cbuf,
-                                Pred pred) {
-    compact_candidates(sm, cl, sl, cbuf, [&](float z, int32_t idx) { return pred(ordered_key(z), idx); });
+                                float floor, Pred pred) {
+    compact_candidates(sm, cl, sl, cbuf, floor, [&](float z, int32_t idx) { return pred(ordered_key(z), idx); });
     return static_cast<int>(min(sm.ccount, static_cast<unsigned int>(kCap)));
 }
 
