@@ -114,6 +114,7 @@ struct MarkovGemmParams {
     int mtiles;                // 128-request M tiles (1 or 2)
     int nt;                    // vocabulary rows per tile (MMA N)
     int stages;                // W tiles in flight per CTA
+    int rpq;                   // requests per 32-row TMEM lane quadrant of an M tile
     int grid;
 };
 // Opaque per-call state of the bias GEMM (the W tensor map).

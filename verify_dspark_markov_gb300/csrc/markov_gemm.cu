@@ -12,14 +12,17 @@
 // The gathered rows U_x (one or two 128-request M tiles) are written to shared
 // memory once per CTA; W streams through a ring of shared-memory stages by TMA
 // (128-byte swizzle when r is a multiple of 64, else a no-swizzle 3-D box that
-// lands directly in the canonical core-matrix layout).  Warp roles: warp 0
-// issues the TMA loads, warp 1 allocates tensor memory and issues the MMAs
-// (one thread), warps 2..9 drain the accumulators.  Accumulators are
-// double-buffered in tensor memory so that the epilogue of one vocabulary
-// tile overlaps the MMAs of the next.  In the epilogue each thread owns one
-// request row (its TMEM lane) and a half of the tile's columns, so the
-// backbone loads and z stores are contiguous 16-byte accesses.  Persistent
-// CTAs, one per SM, walk the vocabulary tiles.
+// lands directly in the canonical core-matrix layout), 4 to 6 tiles ahead.
+// Warp roles: one thread of warp 0 issues the TMA loads and the MMAs (after
+// the MMAs of tile i it refills the stage of tile i - 1), warps 1..8 drain
+// the accumulators, one 32 x 32 block of each tile per warp.  Accumulators
+// are double-buffered in tensor memory so that the epilogue of one
+// vocabulary tile overlaps the MMAs of the next.  The W stream starts before the gather,
+// which runs as asynchronous 16-byte copies.  Requests are spread over the
+// four 32-lane TMEM quadrants so that every epilogue warp has rows; each warp
+// transposes its 32 x 32 accumulator blocks through a swizzled shared-memory
+// tile, so the backbone loads and z stores run along rows (coalesced).
+// Persistent CTAs, one per SM, walk the vocabulary tiles.
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -34,11 +37,18 @@ namespace dspark {
 
 namespace {
 
-constexpr int kThreads = 320;  // producer warp, MMA warp, 8 epilogue warps
+constexpr int kThreads = 288;  // a control warp (TMA + MMA issue) and 8 epilogue warps
 constexpr int kEpiWarps = 8;
-constexpr int kMaxStages = 4;
-constexpr uint32_t kTmemCols = 256;  // two accumulator buffers of mtiles * nt = 128 columns
-constexpr int kSmemBudget = 200 * 1024;
+constexpr int kMaxStages = 8;
+constexpr uint32_t kTmemCols = 128;  // two accumulator buffers of mtiles * nt = 64 columns
+// Per epilogue warp, for its rpq requests (<= 32): an rpq x 32 fp32 transpose
+// tile, element (row, col) at row * 32 + (col ^ row) (conflict-free both ways
+// without padding), and the backbone of its block of the next tile (rpq x 32,
+// copied asynchronously).
+__host__ __device__ constexpr int epi_warp_bytes(int esz, int rpq) { return rpq * 32 * (4 + esz); }
+__host__ __device__ constexpr int epi_bytes(int esz, int rpq) { return kEpiWarps * epi_warp_bytes(esz, rpq); }
+// Shared memory per CTA (227 KB opt-in) less an allowance for the static part.
+constexpr int kSmemMax = 232448 - 1280;
 
 struct GemmSmem {
     uint64_t full[kMaxStages];   // W stage landed (TMA transaction bytes)
@@ -47,6 +57,7 @@ struct GemmSmem {
     uint64_t acc_empty[2];       // accumulator drained (one arrival per epilogue warp)
     uint32_t tmem_base;
     int timeout;
+    int32_t x[256];  // x_{k-1} of every request (-1: none)
 };
 
 // ---------------------------------------------------------------- tcgen05
@@ -118,6 +129,14 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, i
         : "memory");
 }
 
+// 16-byte asynchronous copy global -> shared (no register staging).
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)), "l"(gsrc) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
 // --------------------------------------------------------------- layouts
 // Byte offset of the 16-byte chunk (row m, k-chunk kc) of a K-major operand
 // tile of `rows` rows and r columns, in the layout the descriptors below
@@ -164,7 +183,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* sW = smem + mt * a_bytes;
     const int ntiles = (p.V + NT - 1) / NT;
 
-    if (warp == 1) tmem_alloc(&sm.tmem_base, kTmemCols);
+    constexpr int kEsz = kDtype == kBF16 ? 2 : 4;
+    uint8_t* stage_epi = sW + S * w_bytes;  // epilogue: per warp a transpose tile, then a backbone buffer
+    auto issue_w = [&](int t, int s) {
+        mbar_arrive_expect_tx(&sm.full[s], w_bytes);
+        uint8_t* dst = sW + s * w_bytes;
+        if constexpr (kSw128) {
+            for (int kb = 0; kb < r / 64; ++kb) tma_load_2d(dst + kb * NT * 128, &wmap, kb * 64, t * NT, &sm.full[s]);
+        } else {
+            tma_load_3d(dst, &wmap, 0, t * NT, 0, &sm.full[s]);
+        }
+    };
+    int pre = 0;  // W tiles issued before the gather (they do not depend on it)
+    if (warp == 0) tmem_alloc(&sm.tmem_base, kTmemCols);
     if (threadIdx.x == 0) {
         for (int s = 0; s < kMaxStages; ++s) {
             mbar_init(&sm.full[s], 1);
@@ -176,55 +207,46 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         sm.timeout = 0;
         fence_mbar_init();
+        for (int t = blockIdx.x; t < ntiles && pre < S; t += gridDim.x, ++pre) issue_w(t, pre);
     }
-    // A operand: the gathered rows U[x_{k-1}(b)], zero rows past the batch
-    // and for failed requests (their rows are ignored downstream).
-    const int kchunks = r / 8;
-    for (int c = threadIdx.x; c < mt * a_rows * kchunks; c += kThreads) {
-        const int b = c / kchunks, kc = c % kchunks;
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    // A operand: the gathered rows U[x_{k-1}(b)]; row i of lane quadrant q of
+    // M tile m holds request m * 128 + q * rpq + i (i < rpq).  Zero rows past
+    // the batch and for failed requests (their rows are ignored downstream).
+    const int rpq = p.rpq;
+    for (int b = threadIdx.x; b < 256; b += kThreads) {
+        int32_t x = -1;
         if (b < p.B) {
-            const int32_t x = p.k == 1 ? p.anchor[b] : p.proposals[b * p.gamma + (p.k - 2)];
-            if (x >= 0 && x < p.V) v = *reinterpret_cast<const uint4*>(p.U + static_cast<int64_t>(x) * r + kc * 8);
+            x = p.k == 1 ? p.anchor[b] : p.proposals[b * p.gamma + (p.k - 2)];
+            if (x < 0 || x >= p.V) x = -1;
         }
-        *reinterpret_cast<uint4*>(sA + (b >> 7) * a_bytes + chunk_off<kSw128>(b & 127, kc, a_rows)) = v;
+        sm.x[b] = x;
     }
-    fence_proxy_async_smem();  // generic stores -> visible to the tensor cores
+    __syncthreads();
+    const int kchunks = r / 8;
+    for (int c = threadIdx.x; c < mt * 128 * kchunks; c += kThreads) {
+        const int row = c / kchunks, kc = c % kchunks;
+        const int m = row >> 7, mr = row & 127, i = mr & 31;
+        const int b = m * 128 + (mr >> 5) * rpq + i;
+        const int32_t x = (i < rpq && b < p.B) ? sm.x[b] : -1;
+        uint8_t* d = sA + m * a_bytes + chunk_off<kSw128>(mr, kc, 128);
+        if (x >= 0)
+            cp_async16(d, p.U + static_cast<int64_t>(x) * r + kc * 8);
+        else
+            *reinterpret_cast<uint4*>(d) = make_uint4(0u, 0u, 0u, 0u);
+    }
+    cp_async_wait_all();
+    fence_proxy_async_smem();  // generic and async-copy stores -> visible to the tensor cores
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = sm.tmem_base;
 
     if (warp == 0) {
-        // ------------------------------------------------ TMA producer
-        if (lane == 0) {
-            int issued = 0;
-            for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++issued) {
-                const int s = issued % S;
-                if (issued >= S && !mbar_wait(&sm.empty[s], ((issued / S) - 1) & 1, kWaitLimitNs)) {
-                    set_timeout(sm, p);
-                    break;
-                }
-                if (timed_out(sm)) break;
-                mbar_arrive_expect_tx(&sm.full[s], w_bytes);
-                uint8_t* dst = sW + s * w_bytes;
-                if constexpr (kSw128) {
-                    for (int kb = 0; kb < r / 64; ++kb)
-                        tma_load_2d(dst + kb * NT * 128, &wmap, kb * 64, t * NT, &sm.full[s]);
-                } else {
-                    tma_load_3d(dst, &wmap, 0, t * NT, 0, &sm.full[s]);
-                }
-            }
-            // no copy may still be landing when the CTA exits
-            for (int i = max(0, issued - S); i < issued; ++i)
-                if (!mbar_wait(&sm.full[i % S], (i / S) & 1, kWaitLimitNs)) set_timeout(sm, p);
-        }
-    } else if (warp == 1) {
-        // ------------------------------------------------ MMA issuer
+        // ------------------------------------------------ control: TMA + MMA issue
         if (lane == 0) {
             const uint32_t idesc = instr_desc(128, NT);
             const uint32_t abase = smem_u32(sA), wbase = smem_u32(sW);
-            int i = 0;
+            int i = 0, issued = pre;
             for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++i) {
                 const int s = i % S, a = i & 1;
                 if (!mbar_wait(&sm.full[s], (i / S) & 1, kWaitLimitNs) ||
@@ -232,7 +254,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     set_timeout(sm, p);
                     break;
                 }
-                if (timed_out(sm)) break;
                 tc_fence_after();
                 for (int m = 0; m < mt; ++m) {
                     const uint32_t d = tmem + static_cast<uint32_t>(a * mt * NT + m * NT);
@@ -242,82 +263,105 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 mma_commit(&sm.empty[s]);
                 mma_commit(&sm.acc_full[a]);
+                // refill the stage of tile i - 1 (its MMAs were issued one step ago)
+                if (i >= 1) {
+                    const int j = i - 1;
+                    const int tj = blockIdx.x + (j + S) * gridDim.x;
+                    if (tj < ntiles) {
+                        if (!mbar_wait(&sm.empty[j % S], (j / S) & 1, kWaitLimitNs)) {
+                            set_timeout(sm, p);
+                            break;
+                        }
+                        issue_w(tj, j % S);
+                        ++issued;
+                    }
+                }
             }
-            // the tensor memory is released only after the last MMAs landed
+            // Nothing may still be in flight when the tensor memory is released
+            // and the CTA exits: the last MMAs, and (after a timeout) copies.
             if (i > 0 && !mbar_wait(&sm.acc_full[(i - 1) & 1], ((i - 1) >> 1) & 1, kWaitLimitNs)) set_timeout(sm, p);
+            if (timed_out(sm))
+                for (int k = max(0, issued - S); k < issued; ++k) mbar_wait(&sm.full[k % S], (k / S) & 1, kWaitLimitNs);
         }
     } else {
         // ------------------------------------------------ epilogue
-        const int e = warp - 2;
-        const int quad = warp & 3;  // TMEM lanes 32 quad .. 32 quad + 31
-        const int half = e >> 2;    // which half of the tile's columns
-        const int ncol = NT / 2;    // 64 or 32 columns per thread and M tile
-        const int row = quad * 32 + lane;
-        const size_t esz = kDtype == kBF16 ? 2 : 4;
+        // Warp e reads TMEM lane quadrant warp % 4 (its requests): the 64
+        // flat columns of a tile (mtiles * nt = 64; flat column f is M tile
+        // f / nt, column f % nt) split into two 32-column blocks, block e / 4
+        // for this warp.  The accumulator block goes to a swizzled shared
+        // tile, then each of the block's requests is written along its row
+        // (lane = column) with the backbone added.
+        const int e = warp - 1;
+        const int quad = warp & 3;
+        const int f0 = 32 * (e >> 2);
+        const int m = f0 / NT, c0 = f0 % NT;
+        const int b0 = m * 128 + quad * rpq;             // first request of the block
+        const int nrows = max(0, min(rpq, p.B - b0));   // its valid requests
+        uint8_t* wbase_epi = stage_epi + e * epi_warp_bytes(kEsz, rpq);
+        float* T = reinterpret_cast<float*>(wbase_epi);
+        uint8_t* bbuf = wbase_epi + rpq * 32 * 4;  // [row][32 columns] of the backbone
+        const size_t esz = kEsz;
         const char* bb = static_cast<const char*>(p.backbone) + static_cast<size_t>(p.k - 1) * p.V * esz;
         const size_t bb_stride = static_cast<size_t>(p.gamma) * p.V * esz;  // one request
-        constexpr int kVec = kDtype == kBF16 ? 8 : 4;                     // elements per 16-byte vector
+        // Asynchronous copy of the block's backbone of tile t into bbuf, in
+        // 16-byte pieces (4 or 8 lanes per row).
+        auto fetch_bb = [&](int t) {
+            constexpr int kLanesPerRow = 32 * kEsz / 16;
+            constexpr int kRowsPerStep = 32 / kLanesPerRow;
+            const int piece = lane % kLanesPerRow;
+            const int col = t * NT + c0 + piece * (16 / kEsz);
+#pragma unroll
+            for (int st = 0; st < 32 / kRowsPerStep; ++st) {
+                const int rr = st * kRowsPerStep + lane / kLanesPerRow;
+                if (rr < nrows && col < p.V)
+                    cp_async16(bbuf + rr * 32 * kEsz + piece * 16,
+                               bb + static_cast<size_t>(b0 + rr) * bb_stride + static_cast<size_t>(col) * esz);
+            }
+            asm volatile("cp.async.commit_group;" ::: "memory");
+        };
         int i = 0;
+        if (nrows > 0 && blockIdx.x < ntiles) fetch_bb(blockIdx.x);
         for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++i) {
             const int a = i & 1;
-            const int v0 = t * NT + half * ncol;
-            // Backbone of this thread's 64 (row, column) entries of the tile
-            // (mtiles * ncol = 64: flat entry f is M tile f / ncol, column
-            // f % ncol), read before the accumulator is ready.
-            constexpr int kNV = 64 / kVec;
-            uint4 base[kNV];
-#pragma unroll
-            for (int n = 0; n < kNV; ++n) {
-                const int f = n * kVec, m = f / ncol, c = f % ncol;
-                const int b = m * 128 + row;
-                base[n] = make_uint4(0u, 0u, 0u, 0u);
-                if (b < p.B && v0 + c < p.V)
-                    base[n] = ld_stream_v4(bb + b * bb_stride + static_cast<size_t>(v0 + c) * esz);
-            }
             if (!mbar_wait(&sm.acc_full[a], (i >> 1) & 1, kWaitLimitNs)) {
                 set_timeout(sm, p);
+                asm volatile("cp.async.wait_group 0;" ::: "memory");
                 break;
             }
-            if (timed_out(sm)) break;
+            if (timed_out(sm)) {
+                asm volatile("cp.async.wait_group 0;" ::: "memory");
+                break;
+            }
             tc_fence_after();
-#pragma unroll
-            for (int g = 0; g < 2; ++g) {  // two groups of 32 flat entries
-                const int m = (32 * g) / ncol, c0 = (32 * g) % ncol;
-                const int b = m * 128 + row;
+            if (nrows > 0) {
                 uint32_t acc[32];
                 tmem_ld32(tmem + (static_cast<uint32_t>(quad * 32) << 16) +
-                              static_cast<uint32_t>(a * mt * NT + m * NT + half * ncol + c0),
+                              static_cast<uint32_t>(a * mt * NT + m * NT + c0),
                           acc);
                 tmem_wait_ld();
-                if (b < p.B) {
-                    float* z = p.zbuf + static_cast<size_t>(b) * p.V + v0 + c0;
+                asm volatile("cp.async.wait_group 0;" ::: "memory");  // this tile's backbone is in bbuf
+                if (lane < rpq) {  // lanes past rpq hold no request
 #pragma unroll
-                    for (int j = 0; j < 32; j += 4) {
-                        if (v0 + c0 + j >= p.V) break;
-                        const uint4 w = base[(32 * g + j) / kVec];
-                        float x[4];
-                        if constexpr (kDtype == kBF16) {
-                            const int q = (j % kVec) / 2;  // word holding elements j, j+1
-                            const uint32_t w0 = q == 0 ? w.x : q == 1 ? w.y : q == 2 ? w.z : w.w;
-                            const uint32_t w1 = q == 0 ? w.y : q == 1 ? w.z : w.w;
-                            x[0] = bf16_lo(w0);
-                            x[1] = bf16_hi(w0);
-                            x[2] = bf16_lo(w1);
-                            x[3] = bf16_hi(w1);
-                        } else {
-                            x[0] = __uint_as_float(w.x);
-                            x[1] = __uint_as_float(w.y);
-                            x[2] = __uint_as_float(w.z);
-                            x[3] = __uint_as_float(w.w);
-                        }
-                        float4 o;
-                        o.x = x[0] + __uint_as_float(acc[j]);
-                        o.y = x[1] + __uint_as_float(acc[j + 1]);
-                        o.z = x[2] + __uint_as_float(acc[j + 2]);
-                        o.w = x[3] + __uint_as_float(acc[j + 3]);
-                        *reinterpret_cast<float4*>(z + j) = o;
+                    for (int j = 0; j < 32; ++j) T[lane * 32 + (j ^ lane)] = __uint_as_float(acc[j]);
+                }
+                __syncwarp();
+                const int v = t * NT + c0 + lane;
+                float* zrow = p.zbuf + static_cast<size_t>(b0) * p.V + v;
+#pragma unroll 4
+                for (int rr = 0; rr < nrows; ++rr, zrow += p.V) {
+                    if (v < p.V) {
+                        float x;
+                        if constexpr (kDtype == kBF16)
+                            x = __uint_as_float(static_cast<uint32_t>(
+                                    reinterpret_cast<const uint16_t*>(bbuf)[rr * 32 + lane]) << 16);
+                        else
+                            x = reinterpret_cast<const float*>(bbuf)[rr * 32 + lane];
+                        *zrow = x + T[rr * 32 + (lane ^ rr)];
                     }
                 }
+                __syncwarp();
+                // the next tile's backbone streams in while its accumulator is computed
+                if (t + static_cast<int>(gridDim.x) < ntiles) fetch_bb(t + gridDim.x);
             }
             tc_fence_before();
             __syncwarp();
@@ -327,7 +371,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+    if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
 // ------------------------------------------------------------------ host
@@ -346,7 +390,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 int smem_bytes(const MarkovGemmParams& p) {
-    return p.mtiles * 128 * p.r * 2 + p.stages * p.nt * p.r * 2 + 1024;  // + alignment slack
+    return p.mtiles * 128 * p.r * 2 + p.stages * p.nt * p.r * 2 + epi_bytes(p.dtype == kBF16 ? 2 : 4, p.rpq) +
+           1024;  // + alignment slack
 }
 
 template <int kDtype, bool kSw128>
@@ -364,9 +409,11 @@ cudaError_t launch_one(const MarkovGemmParams& p, const CUtensorMap& map, cudaSt
 bool prepare_markov_bias(MarkovGemmParams& p, MarkovGemmPlan& plan) {
     if (p.B < 1 || p.B > 256 || p.r < 16 || p.r > 256 || p.r % 16 != 0) return false;
     p.mtiles = (p.B + 127) / 128;
-    p.nt = 128 / p.mtiles;
+    p.nt = 64 / p.mtiles;
     const int a = p.mtiles * 128 * p.r * 2, w = p.nt * p.r * 2;
-    p.stages = std::min(kMaxStages, (kSmemBudget - a) / w);
+    p.rpq = p.mtiles == 1 ? (p.B + 3) / 4 : 32;
+    const int budget = kSmemMax - epi_bytes(p.dtype == kBF16 ? 2 : 4, p.rpq) - 1024;  // A + W stages
+    p.stages = std::min(kMaxStages, (budget - a) / w);
     if (p.stages < 2) return false;
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
