@@ -54,8 +54,12 @@ MarkovLayout markov_layout(int B, int gamma, int V, int r) {
     return l;
 }
 
-size_t stats_workspace(int N, int gamma) {
+// Statistics: per-position records, then the per-CTA partial sums.
+size_t stats_partials_offset(int N, int gamma) {
     return align_up(static_cast<size_t>(N) * gamma * sizeof(StatsRecord));
+}
+size_t stats_workspace(int N, int gamma) {
+    return align_up(stats_partials_offset(N, gamma) + static_cast<size_t>(stats_partials(N)) * 6 * sizeof(double));
 }
 
 template <typename T>
@@ -288,6 +292,7 @@ int dspark_accept_stats(const void* draft, const void* target, int dtype, const 
     p.l1 = l1;
     p.accept = accept;
     p.rec = at<StatsRecord>(workspace, 0);
+    p.partial = at<double>(workspace, stats_partials_offset(N, gamma));
     p.tau = tau;
     p.loss_num = loss_num;
     p.report = report;

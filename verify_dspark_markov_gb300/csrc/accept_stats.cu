@@ -12,8 +12,9 @@
 // shared memory; each CTA then re-reads its slice (a ~129 KB working set per
 // CTA, so the re-read is served by L2) to form the L1 terms.  NaN / +inf poison
 // the running sums, which is how non-finite rows are detected at no cost.
-// Kernel 2 (one CTA): tau, statuses and the weighted sums in a fixed order,
-// so repeated calls give identical bits.
+// Kernels 2 and 3: tau and the status per block (one thread each) with the
+// weighted sums reduced by fixed binary trees, then the CTA partials in a
+// fixed order, so repeated calls give identical bits.
 
 #include <cooperative_groups.h>
 
@@ -28,7 +29,7 @@ namespace {
 
 constexpr int kC = 8;          // CTAs per row pair (cluster size)
 constexpr int kThreads = 256;
-constexpr int kBatch = 4;      // 16-byte vectors per row per thread in flight
+constexpr int kBatch = 6;      // 16-byte vectors per row per thread in flight
 constexpr float kLog2e = 1.4426950408889634f;
 
 __device__ __forceinline__ float ex2(float x) {
@@ -217,15 +218,22 @@ __global__ void __cluster_dims__(kC, 1, 1) __launch_bounds__(kThreads)
 }
 
 constexpr int kFinalThreads = 256;
+constexpr int kSums = 6;  // weighted CE, L1, BCE; sum of accept; sum of tau; token count
 
-__global__ void __launch_bounds__(kFinalThreads) stats_final_kernel(const StatsParams p) {
-    __shared__ double s_sum[5][kFinalThreads];
-    __shared__ long long s_cnt[kFinalThreads];
+// Kernel 2 (one thread per block n): tau_n = 1 + sum_k prod_{j<=k} accept_j,
+// the block's status, and its share of the sums; each CTA reduces its
+// threads' shares by a fixed binary tree and writes one partial per sum.
+__global__ void __launch_bounds__(kFinalThreads) stats_blocks_kernel(const StatsParams p) {
+    __shared__ double s_w[32];                         // exp(-k / gamma), k = 1..gamma
+    __shared__ double s_sum[kSums][kFinalThreads];
     const int tid = threadIdx.x;
-    double ce = 0.0, l1 = 0.0, bce = 0.0, acc_sum = 0.0, tau_sum = 0.0;
-    long long cnt = 0;
-    for (int n = tid; n < p.N; n += kFinalThreads) {
-        double tau = 1.0, survive = 1.0;
+    if (tid < p.gamma) s_w[tid] = exp(-static_cast<double>(tid + 1) / p.gamma);
+    __syncthreads();
+    const int n = blockIdx.x * kFinalThreads + tid;
+    double ce = 0.0, l1 = 0.0, bce = 0.0, acc_sum = 0.0, tau = 0.0, cnt = 0.0;
+    if (n < p.N) {
+        double survive = 1.0;
+        tau = 1.0;
         int32_t code = kReqOk;
         for (int k = 1; k <= p.gamma; ++k) {
             const int64_t i = static_cast<int64_t>(n) * p.gamma + (k - 1);
@@ -234,42 +242,62 @@ __global__ void __launch_bounds__(kFinalThreads) stats_final_kernel(const StatsP
             tau += survive;
             code = max(code, r.code);
             if (!p.mask || p.mask[i]) {
-                const double w = exp(-static_cast<double>(k) / p.gamma);
+                const double w = s_w[k - 1];
                 ce += w * r.ce;
                 l1 += w * r.l1;
                 bce += w * r.bce;
                 acc_sum += r.acc;
-                ++cnt;
+                cnt += 1.0;
             }
         }
         p.tau[n] = static_cast<float>(tau);
         if (p.status) p.status[n] = code;
-        tau_sum += tau;
     }
     s_sum[0][tid] = ce; s_sum[1][tid] = l1; s_sum[2][tid] = bce;
-    s_sum[3][tid] = acc_sum; s_sum[4][tid] = tau_sum;
-    s_cnt[tid] = cnt;
+    s_sum[3][tid] = acc_sum; s_sum[4][tid] = tau; s_sum[5][tid] = cnt;
     __syncthreads();
-    if (tid == 0) {  // fixed order: identical bits on every call
-        double t[5] = {0, 0, 0, 0, 0};
-        long long c = 0;
-        for (int i = 0; i < kFinalThreads; ++i) {
-            for (int j = 0; j < 5; ++j) t[j] += s_sum[j][i];
-            c += s_cnt[i];
-        }
-        p.loss_num[0] = t[0];
-        p.loss_num[1] = t[1];
-        p.loss_num[2] = t[2];
-        p.loss_num[3] = 0.1 * t[0] + 0.9 * t[1] + 1.0 * t[2];
-        p.report[0] = t[3];
-        p.report[1] = t[4];
-        *p.num_tokens = c;
+    for (int h = kFinalThreads / 2; h > 0; h >>= 1) {  // fixed order: identical bits on every call
+        if (tid < h)
+#pragma unroll
+            for (int j = 0; j < kSums; ++j) s_sum[j][tid] += s_sum[j][tid + h];
+        __syncthreads();
+    }
+    if (tid < kSums) p.partial[static_cast<int64_t>(blockIdx.x) * kSums + tid] = s_sum[tid][0];
+}
+
+// Kernel 3 (one CTA): the CTA partials in a fixed order.
+__global__ void __launch_bounds__(kFinalThreads) stats_total_kernel(const StatsParams p, int nparts) {
+    __shared__ double s_sum[kSums][kFinalThreads];
+    const int tid = threadIdx.x;
+    double t[kSums] = {0, 0, 0, 0, 0, 0};
+    for (int c = tid; c < nparts; c += kFinalThreads)  // each thread: a fixed subsequence
+#pragma unroll
+        for (int j = 0; j < kSums; ++j) t[j] += p.partial[static_cast<int64_t>(c) * kSums + j];
+#pragma unroll
+    for (int j = 0; j < kSums; ++j) s_sum[j][tid] = t[j];
+    __syncthreads();
+    for (int h = kFinalThreads / 2; h > 0; h >>= 1) {
+        if (tid < h)
+#pragma unroll
+            for (int j = 0; j < kSums; ++j) s_sum[j][tid] += s_sum[j][tid + h];
+        __syncthreads();
+    }
+    if (tid == 0) {
+        p.loss_num[0] = s_sum[0][0];
+        p.loss_num[1] = s_sum[1][0];
+        p.loss_num[2] = s_sum[2][0];
+        p.loss_num[3] = 0.1 * s_sum[0][0] + 0.9 * s_sum[1][0] + 1.0 * s_sum[2][0];
+        p.report[0] = s_sum[3][0];
+        p.report[1] = s_sum[4][0];
+        *p.num_tokens = static_cast<int64_t>(s_sum[5][0]);
     }
 }
 
 }  // namespace
 
 int stats_cluster_size() { return kC; }
+
+int stats_partials(int N) { return (N + kFinalThreads - 1) / kFinalThreads; }
 
 cudaError_t launch_accept_stats(const StatsParams& p, cudaStream_t stream) {
     const int64_t pairs = static_cast<int64_t>(p.N) * p.gamma;
@@ -280,7 +308,10 @@ cudaError_t launch_accept_stats(const StatsParams& p, cudaStream_t stream) {
         stats_pairs_kernel<kF32><<<grid, kThreads, 0, stream>>>(p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    stats_final_kernel<<<1, kFinalThreads, 0, stream>>>(p);
+    const int nparts = stats_partials(p.N);
+    stats_blocks_kernel<<<nparts, kFinalThreads, 0, stream>>>(p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    stats_total_kernel<<<1, kFinalThreads, 0, stream>>>(p, nparts);
     return cudaGetLastError();
 }
 

@@ -150,6 +150,7 @@ struct StatsParams {
     float* l1;
     float* accept;
     StatsRecord* rec;         // [N * gamma] workspace
+    double* partial;          // [stats_partials(N) * 6] workspace
     float* tau;
     double* loss_num;
     double* report;
@@ -157,6 +158,7 @@ struct StatsParams {
     int32_t* status;
 };
 int stats_cluster_size();
+int stats_partials(int N);
 cudaError_t launch_accept_stats(const StatsParams& p, cudaStream_t stream);
 
 }  // namespace dspark
