@@ -324,7 +324,7 @@ class Stats:
                           f"recipe in {el:.1f} s, single-threaded C++ oracle"}
 
 
-def make_workload(name, device):
+def make_workload(name, device, stats_blocks=4096):
     if name == "full_decode_tile":
         return Serving(name, synth.full_decode_tile(device=device), 2)
     if name == "decode_verify_tile":
@@ -332,7 +332,7 @@ def make_workload(name, device):
     if name == "mixed_serving":
         return Serving(name, synth.mixed_serving(device=device), 2)
     if name == "training_stats":
-        return Stats(synth.training_stats(device=device))
+        return Stats(synth.training_stats(device=device, N=stats_blocks))
     raise ValueError(name)
 
 
@@ -355,7 +355,7 @@ def run_gpu(args):
         torch.distributed.barrier()
     ds.load()
 
-    wl = make_workload(args.workload, dev)
+    wl = make_workload(args.workload, dev, args.stats_blocks)
     wl.setup(ds, dev)
     stream = torch.cuda.current_stream(dev)
     parts = wl.parts()
@@ -537,6 +537,8 @@ def main():
                     help="cap on the timed region's GPU time (fewer steps for slow workloads)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--stats-blocks", type=int, default=4096,
+                    help="training_stats only: blocks of the workload (smaller sizes for profiling captures)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     res = run_reference(args) if args.impl == "reference" else run_gpu(args)
