@@ -61,6 +61,22 @@ def dist_env():
             int(os.environ.get("LOCAL_RANK", "0")))
 
 
+def replica_step_ms(ms, world, device):
+    """The job's step time over independent replicas: the slowest rank's.
+    Every rank gets the same value (no data moves between replicas)."""
+    if world <= 1:
+        return ms
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(positions, ms, world):
+    """Whole-job positions per second: every replica processes `positions`
+    per step, the job's step takes `ms` (the slowest rank's)."""
+    return positions * world / (ms * 1e-3)
+
+
 class Clocks:
     """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
     QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -404,11 +420,7 @@ def run_gpu(args):
     step_ms = [ev[i][0].elapsed_time(ev[i][-1]) for i in range(steps)]
     part_ms = {name: float(np.mean([ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(steps)]))
                for j, (name, _) in enumerate(parts)}
-    ms = float(np.mean(step_ms))
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = replica_step_ms(float(np.mean(step_ms)), world, dev)
 
     # ---- end to end through the public API: host inputs, copies included
     host_in = [t.cpu().pin_memory() for t in wl.inputs]
@@ -434,14 +446,14 @@ def run_gpu(args):
     dom = max(part_ms, key=part_ms.get)
     achieved = nbytes[dom] / (part_ms[dom] * 1e-3) / 1e9
     kernel = {"full_decode_tile": "argmax_rows_kernel<bf16> (draft + verify launches)",
-              "training_stats": "stats_pairs_kernel<f32> + stats_final_kernel"}.get(
+              "training_stats": "stats_pairs_kernel<f32> (+ stats_blocks_kernel, stats_total_kernel)"}.get(
                   wl.name, {"draft": "markov_sample (markov_bias_kernel + markov_step_kernel per position)",
                             "verify": "verify_rows_kernel<bf16>"}.get(dom, dom))
     if wl.name == "full_decode_tile":  # the same kernel serves both parts: average over both launches
         achieved = sum(nbytes.values()) / (sum(part_ms.values()) * 1e-3) / 1e9
     result = {
         "metric": METRIC,
-        "value": wl.positions * world / (ms * 1e-3),
+        "value": replica_throughput(wl.positions, ms, world),
         "unit": UNIT,
         "n_gpus": world,
         "steps": steps,
