@@ -1,5 +1,5 @@
 // Sampled paths built on the row engine (row_policy.cuh): one cluster of
-// rp::kC CTAs per vocabulary row.
+// rp::kC CTAs per vocabulary row, reading the row in place.
 //
 //  * verify_rows_kernel - exact verify of a block under per-request policies
 //    [FT Exact decoding semantics > Probabilistic]: each cluster forms the
@@ -30,11 +30,8 @@ __device__ __forceinline__ float inv_mass(uint64_t mass) {
     return static_cast<float>(rp::kFix / static_cast<double>(mass));
 }
 
-// Dynamic shared memory: the row slice (bf16 or fp32), then the candidate
-// buffer (used in rank 0).
-__host__ __device__ constexpr int slice_bytes(int slice, int store_bf16) {
-    return ((slice * (store_bf16 ? 2 : 4)) + 15) / 16 * 16;
-}
+// Dynamic shared memory: the candidate buffer (used in rank 0).  The row
+// slices are read in place from global memory.
 
 template <int kDtype>
 __global__ void __cluster_dims__(rp::kC, 1, 1) __launch_bounds__(rp::kThreads)
@@ -49,8 +46,7 @@ __global__ void __cluster_dims__(rp::kC, 1, 1) __launch_bounds__(rp::kThreads)
     const int rank = static_cast<int>(cl.block_rank());
     const int tid = threadIdx.x;
     constexpr int kStoreBf16 = kDtype == kBF16;
-    void* zs = dyn;
-    unsigned long long* cbuf = reinterpret_cast<unsigned long long*>(dyn + slice_bytes(p.slice, kStoreBf16));
+    unsigned long long* cbuf = reinterpret_cast<unsigned long long*>(dyn);
     rp::init_smem(sm);
     if (tid == 0) {
         s_px = 0.0f;
@@ -65,17 +61,16 @@ __global__ void __cluster_dims__(rp::kC, 1, 1) __launch_bounds__(rp::kThreads)
     const int b = static_cast<int>(row / rows), i = static_cast<int>(row % rows);
     const int lo = rank * p.slice;
     const int n = max(0, min(p.slice, p.V - lo));
-    rp::Slice sl{zs, lo, n, (n + kThreads - 1) / kThreads, kStoreBf16};
     const int esize = kDtype == kBF16 ? 2 : 4;
     const char* tgt = static_cast<const char*>(p.target);
+    rp::Slice sl{tgt + (row * p.V + lo) * esize, lo, n, (n + kThreads - 1) / kThreads, kStoreBf16};
 
     rp::Policy pol;
     const bool pol_ok = rp::make_policy(p.policy[b], p.V, pol);
     rp::RowResult res;
-    bool bad, late;
-    rp::load_slice_and_max<kDtype>(sm, cl, tgt + row * p.V * esize, lo, n, zs, res, bad, late);
-    res.status = late ? kReqTimeout
-                      : bad ? kReqNonfinite : (res.argmax < 0 ? kReqEmpty : (pol_ok ? kReqOk : kReqBadPolicy));
+    bool bad;
+    rp::slice_max(sm, cl, sl, res, bad);
+    res.status = bad ? kReqNonfinite : (res.argmax < 0 ? kReqEmpty : (pol_ok ? kReqOk : kReqBadPolicy));
     res.count = 1;
     res.in_buf = 0;
     if (res.status == kReqOk) rp::row_policy(sm, cl, sl, p.V, pol, res, cbuf);
@@ -153,6 +148,7 @@ __global__ void __cluster_dims__(rp::kC, 1, 1) __launch_bounds__(rp::kThreads)
             s_plan[1] = j;                    // residual against q_j when j > 0
         }
     }
+    if (rank == 0 && tid == 0) sm.ccount = 0;  // the draw's candidate slots, published by the barrier below
     cl.sync();
     if (tid < 2) s_bcast[1 + tid] = cl.map_shared_rank(s_plan, 0)[tid];
     __syncthreads();
@@ -161,10 +157,7 @@ __global__ void __cluster_dims__(rp::kC, 1, 1) __launch_bounds__(rp::kThreads)
         // draw the residual / bonus token from target row R of request b
         const RowRecord rr = p.records[static_cast<int64_t>(b) * rows + R];
         const int64_t trow = static_cast<int64_t>(b) * rows + R;
-        rp::RowResult unused;
-        bool unused_bad, late;
-        if (rank == 0 && tid == 0) sm.ccount = 0;  // published by the load's cluster barrier
-        rp::load_slice_and_max<kDtype>(sm, cl, tgt + trow * p.V * esize, lo, n, zs, unused, unused_bad, late);
+        const rp::Slice sr{tgt + (trow * p.V + lo) * esize, lo, n, (n + kThreads - 1) / kThreads, kStoreBf16};
         const float invS = inv_mass(rr.mass);
         const float* qrow = j ? p.q + (static_cast<int64_t>(b) * p.gamma + (j - 1)) * p.V : nullptr;
         const int64_t pos = p.pos0[b] + (j ? j : p.gamma + 1);
@@ -178,7 +171,7 @@ __global__ void __cluster_dims__(rp::kC, 1, 1) __launch_bounds__(rp::kThreads)
         int32_t token = -1;
         if (rr.count <= rp::kThreads) {
             // small support: gathered in rank 0, drawn in token order
-            const int cnt = rp::compact_to_rank0(sm, cl, sl, cbuf, rp::support_floor(rr.tau), [&](uint32_t key, int32_t idx) {
+            const int cnt = rp::compact_to_rank0(sm, cl, sr, cbuf, rp::support_floor(rr.tau), [&](uint32_t key, int32_t idx) {
                 return rp::in_set(key, idx, rr.tau, rr.cut);
             });
             if (rank == 0) {
@@ -197,33 +190,26 @@ __global__ void __cluster_dims__(rp::kC, 1, 1) __launch_bounds__(rp::kThreads)
         } else {
             // the whole vocabulary: a draw over every CTA's slice
             unsigned long long total = 0;
-            auto in_sup = [&](int li, float z) { return rp::in_set(ordered_key(z), lo + li, rr.tau, rr.cut); };
             if (j) {
-                token = rp::sample_fixed(sm, cl, sl, m24,
-                                         [&](int li) {
-                                             const float z = sl.val(li);
-                                             return in_sup(li, z) ? resid(ordered_key(z), lo + li) : 0ull;
+                token = rp::sample_fixed(sm, cl, sr, m24,
+                                         [&](float z, int32_t idx) {
+                                             const uint32_t key = ordered_key(z);
+                                             return rp::in_set(key, idx, rr.tau, rr.cut) ? resid(key, idx) : 0ull;
                                          },
                                          total);
             }
             if (!j || total == 0)
-                token = rp::sample_fixed(sm, cl, sl, m24,
-                                         [&](int li) {
-                                             const float z = sl.val(li);
-                                             return in_sup(li, z) ? pw(ordered_key(z)) : 0ull;
+                token = rp::sample_fixed(sm, cl, sr, m24,
+                                         [&](float z, int32_t idx) {
+                                             const uint32_t key = ordered_key(z);
+                                             return rp::in_set(key, idx, rr.tau, rr.cut) ? pw(key) : 0ull;
                                          },
                                          total);
         }
         if (rank == 0 && tid == 0) {
-            if (late) {
-                for (int r = 0; r < rows; ++r) out[r] = -1;
-                p.num_accepted[b] = -1;
-                p.status[b] = kReqTimeout;
-            } else {
-                out[R] = token;
-                p.num_accepted[b] = R;
-                p.status[b] = kReqOk;
-            }
+            out[R] = token;
+            p.num_accepted[b] = R;
+            p.status[b] = kReqOk;
         }
     }
     // leave the workspace zero-filled: this request's row records are consumed
@@ -276,22 +262,19 @@ __global__ void __cluster_dims__(rp::kC, 1, 1) __launch_bounds__(rp::kThreads)
     const bool z_bf16 = !p.zbuf && kDtype == kBF16;
     const int lo = rank * p.slice;
     const int n = max(0, min(p.slice, p.V - lo));
-    void* zs = dyn;
-    unsigned long long* cbuf = reinterpret_cast<unsigned long long*>(dyn + slice_bytes(p.slice, z_bf16));
-    rp::Slice sl{zs, lo, n, (n + kThreads - 1) / kThreads, z_bf16 ? 1 : 0};
+    unsigned long long* cbuf = reinterpret_cast<unsigned long long*>(dyn);
+    // the logits with the Markov bias (fp32 [B, V]) or the backbone row
+    const void* zrow = p.zbuf ? static_cast<const void*>(p.zbuf + static_cast<int64_t>(b) * p.V + lo)
+                              : static_cast<const void*>(static_cast<const char*>(p.backbone) +
+                                                         (pidx * p.V + lo) * (kDtype == kBF16 ? 2 : 4));
+    rp::Slice sl{zrow, lo, n, (n + kThreads - 1) / kThreads, z_bf16 ? 1 : 0};
     rp::Policy pol;
     const bool pol_ok = p.policy ? rp::make_policy(p.policy[b], p.V, pol)
                                  : (pol = rp::Policy{1.0f, 0, 1.0f, 1}, true);
     rp::RowResult res;
-    bool bad, late;
-    if (p.zbuf)  // logits with the Markov bias, fp32 [B, V]
-        rp::load_slice_and_max<kF32>(sm, cl, p.zbuf + static_cast<int64_t>(b) * p.V, lo, n, zs, res, bad, late);
-    else
-        rp::load_slice_and_max<kDtype>(
-            sm, cl, static_cast<const char*>(p.backbone) + pidx * p.V * (kDtype == kBF16 ? 2 : 4), lo, n, zs, res,
-            bad, late);
-    res.status = late ? kReqTimeout
-                      : bad ? kReqNonfinite : (res.argmax < 0 ? kReqEmpty : (pol_ok ? kReqOk : kReqBadPolicy));
+    bool bad;
+    rp::slice_max(sm, cl, sl, res, bad);
+    res.status = bad ? kReqNonfinite : (res.argmax < 0 ? kReqEmpty : (pol_ok ? kReqOk : kReqBadPolicy));
     if (res.status != kReqOk) {
         if (rank == 0 && tid == 0) {
             p.proposals[pidx] = -1;
@@ -317,8 +300,18 @@ __global__ void __cluster_dims__(rp::kC, 1, 1) __launch_bounds__(rp::kThreads)
             // elements (key >= tau) need their weight
             const float zt = rp::support_floor(res.tau);
             const int vp = sl.vper(), nv = sl.nvec();
-            for (int j = tid; j < nv; j += kThreads) {
-                const uint4 v = sl.vec(j);
+            for (int j0 = tid; j0 < nv; j0 += kThreads * rp::kBatch) {
+              uint4 vb[rp::kBatch];
+#pragma unroll
+              for (int u = 0; u < rp::kBatch; ++u) {
+                  const int jj = j0 + u * kThreads;
+                  vb[u] = jj < nv ? sl.vec(jj) : make_uint4(0u, 0u, 0u, 0u);
+              }
+#pragma unroll
+              for (int u = 0; u < rp::kBatch; ++u) {
+                const int j = j0 + u * kThreads;
+                if (j >= nv) break;
+                const uint4 v = vb[u];
                 float q8[8];
 #pragma unroll
                 for (int l = 0; l < 8; ++l) q8[l] = 0.0f;
@@ -334,6 +327,7 @@ __global__ void __cluster_dims__(rp::kC, 1, 1) __launch_bounds__(rp::kThreads)
                 float4* d = reinterpret_cast<float4*>(qrow + j * vp);
                 d[0] = make_float4(q8[0], q8[1], q8[2], q8[3]);
                 if (vp == 8) d[1] = make_float4(q8[4], q8[5], q8[6], q8[7]);
+              }
             }
         }
         const uint32_t m24 = uniform_bits24(p.seed[b], p.request_id[b], p.pos0[b] + k, 0);
@@ -361,9 +355,8 @@ __global__ void __cluster_dims__(rp::kC, 1, 1) __launch_bounds__(rp::kThreads)
             unsigned long long total = 0;
             const int32_t xk = rp::sample_fixed(
                 sm, cl, sl, m24,
-                [&](int li) {
-                    const float z = sl.val(li);
-                    return rp::in_set(ordered_key(z), lo + li, res.tau, res.cut)
+                [&](float z, int32_t idx) {
+                    return rp::in_set(ordered_key(z), idx, res.tau, res.cut)
                                ? rp::to_fixed(rp::weight_f(z, res.zmax, pol.inv_t))
                                : 0ull;
                 },
@@ -403,7 +396,9 @@ int policy_cluster_size() { return kC; }
 int policy_slice(int V) { return ((V + kC - 1) / kC + 7) / 8 * 8; }
 
 int policy_smem_bytes(int V, int store_bf16) {
-    return slice_bytes(policy_slice(V), store_bf16) + rp::kCap * static_cast<int>(sizeof(unsigned long long));
+    (void)V;
+    (void)store_bf16;
+    return rp::kCap * static_cast<int>(sizeof(unsigned long long));
 }
 
 cudaError_t launch_verify_prob(const VerifyProbParams& p, cudaStream_t stream) {

@@ -1,6 +1,10 @@
 // Row engine: the sampling policy of one vocabulary row, computed by a
-// cluster of kC CTAs that each hold a contiguous slice of the row in shared
-// memory (as fp32), plus the exact inverse-CDF draw over the policy's weights.
+// cluster of kC CTAs that each own a contiguous slice of the row, plus the
+// exact inverse-CDF draw over the policy's weights.  The slices stay in
+// global memory: the first pass over a row streams it from HBM (or from L2
+// when the row was just written, like the Markov logits), later passes find
+// it in L2.  With no row held in shared memory a cluster needs ~24 KB, so one
+// row per SM is in flight (4 CTAs of 256 threads).
 //
 // The policy [FT Exact decoding semantics > Probabilistic] as this library
 // reads it: greedy = one-hot at the lowest-index argmax; otherwise temperature,
@@ -32,7 +36,7 @@ namespace rp {
 
 namespace cg = cooperative_groups;
 
-constexpr int kC = 8;           // CTAs per row
+constexpr int kC = 4;           // CTAs per row
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kBins = 256;      // 8-bit radix digits
@@ -40,6 +44,7 @@ constexpr int kWin = 8;         // candidate window widths
 constexpr int kCap = 2048;      // candidate buffer of rank 0 (composite keys)
 constexpr int kSample = 8;      // 1 in kSample elements feeds the window estimate
 constexpr double kFix = 1099511627776.0;  // 2^40: fixed-point scale of the weights
+static_assert(kWarps * kBins <= kCap, "the per-warp histograms live in the candidate buffer");
 constexpr float kLog2e = 1.4426950408889634f;
 
 __device__ __forceinline__ float ex2(float x) {
@@ -90,21 +95,16 @@ struct Smem {
     int32_t pick[4];
     int parity;      // which exchange buffer is next
     int hparity;     // which histogram buffer is next
-    uint64_t lbar[4];        // slice load: one mbarrier per bulk-copy piece
-    uint32_t lphase;         // parity of the next slice load
     unsigned int ccount;     // rank 0: candidate slots claimed by the cluster
 };
-constexpr int kLoadChunks = 4;
+constexpr int kBatch = 4;    // 16-byte vectors per thread in flight in a pass over a slice
 
 // Called by every thread at kernel start, followed by a __syncthreads.
 __device__ __forceinline__ void init_smem(Smem& sm) {
     if (threadIdx.x == 0) {
         sm.parity = 0;
         sm.hparity = 0;
-        sm.lphase = 0;
         sm.ccount = 0;
-        for (int c = 0; c < kLoadChunks; ++c) mbar_init(&sm.lbar[c], 1);
-        fence_mbar_init();
     }
     // the candidate histogram (buffer 1 of the radix histograms) starts empty
     for (int b = threadIdx.x; b < kBins; b += kThreads) {
@@ -245,21 +245,22 @@ __device__ __forceinline__ unsigned long long block_scan_u64(Smem& sm, unsigned 
     return x + base;
 }
 
-// The slice [lo, lo + n) of the row held by this CTA in shared memory, stored
-// as bf16 (for bf16 inputs: half the footprint, more rows in flight) or fp32.
+// The slice [lo, lo + n) of a row owned by this CTA, read in place from
+// global memory (z points at element lo; bf16 or fp32; read-only for the
+// kernel's lifetime).
 struct Slice {
     const void* z;
     int lo, n;
     int per;   // contiguous elements per thread for ordered scans
     int bf16;  // storage format
     __device__ __forceinline__ float val(int i) const {
-        return bf16 ? __uint_as_float(static_cast<uint32_t>(static_cast<const uint16_t*>(z)[i]) << 16)
-                    : static_cast<const float*>(z)[i];
+        return bf16 ? __uint_as_float(static_cast<uint32_t>(__ldg(static_cast<const unsigned short*>(z) + i)) << 16)
+                    : __ldg(static_cast<const float*>(z) + i);
     }
     // 16-byte vectors: 8 (bf16) or 4 (fp32) elements each; n is a multiple of 8
     __device__ __forceinline__ int vper() const { return bf16 ? 8 : 4; }
     __device__ __forceinline__ int nvec() const { return n / vper(); }
-    __device__ __forceinline__ uint4 vec(int j) const { return ld_shared_v4(static_cast<const char*>(z) + j * 16); }
+    __device__ __forceinline__ uint4 vec(int j) const { return __ldg(static_cast<const uint4*>(z) + j); }
 };
 
 __device__ __forceinline__ uint32_t bf16x2_max(uint32_t a, uint32_t b) {
@@ -300,6 +301,79 @@ __device__ __forceinline__ uint32_t lowest_true_key(uint32_t kmax, P pred) {
     return hi;
 }
 
+// Every element of the slice, in no particular order: fn(z, index), with
+// kBatch 16-byte vectors per thread in flight.
+template <typename F>
+__device__ __forceinline__ void for_each_elem(const Slice& sl, F fn) {
+    const int vp = sl.vper(), nv = sl.nvec();
+    for (int j0 = threadIdx.x; j0 < nv; j0 += kThreads * kBatch) {
+        uint4 vb[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            const int j = j0 + u * kThreads;
+            vb[u] = j < nv ? sl.vec(j) : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            const int j = j0 + u * kThreads;
+            if (j >= nv) break;
+#pragma unroll
+            for (int l = 0; l < 8; ++l)
+                if (l < vp) fn(vec_elem(vb[u], l, sl.bf16), sl.lo + j * vp + l);
+        }
+    }
+}
+
+// This thread's contiguous run of the slice's vectors, [a, e), for scans in
+// index order.
+__device__ __forceinline__ void thread_run(const Slice& sl, int& a, int& e) {
+    const int nv = sl.nvec();
+    const int pv = (nv + kThreads - 1) / kThreads;
+    a = min(static_cast<int>(threadIdx.x) * pv, nv);
+    e = min(a + pv, nv);
+}
+// fn(z, index) over the vectors [a, e) in index order, kBatch at a time.
+template <typename F>
+__device__ __forceinline__ void for_run(const Slice& sl, int a, int e, F fn) {
+    const int vp = sl.vper();
+    for (int j0 = a; j0 < e; j0 += kBatch) {
+        uint4 vb[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) vb[u] = j0 + u < e ? sl.vec(j0 + u) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            if (j0 + u >= e) break;
+#pragma unroll
+            for (int l = 0; l < 8; ++l)
+                if (l < vp) fn(vec_elem(vb[u], l, sl.bf16), sl.lo + (j0 + u) * vp + l);
+        }
+    }
+}
+
+// Warp-aggregated histogram update for the radix digits, where a flat row
+// sends nearly every element to one or two bins: the active lanes with the
+// same bin (bin < 0: none) add their counts and values with one atomic by
+// the group's first lane.  Values are split into two parts of 20 bits so that
+// a 32-lane sum fits 32-bit reductions.  (Where bins are spread, plain
+// atomics are cheaper than the grouping.)
+__device__ __forceinline__ void hist_add(uint32_t* cnt, unsigned long long* mass, int bin, unsigned long long w) {
+    const unsigned act = __activemask();
+    const unsigned peers = __match_any_sync(act, bin);
+    if (bin < 0) return;
+    const int lane = threadIdx.x & 31;
+    const int leader = __ffs(peers) - 1;
+    unsigned long long sum = 0;
+    if (mass) {
+        const unsigned hi = __reduce_add_sync(peers, static_cast<unsigned>(w >> 20));
+        const unsigned lo = __reduce_add_sync(peers, static_cast<unsigned>(w & 0xFFFFFull));
+        sum = (static_cast<unsigned long long>(hi) << 20) + lo;
+    }
+    if (lane == leader) {
+        if (cnt) atomicAdd(&cnt[bin], static_cast<unsigned>(__popc(peers)));
+        if (mass) atomicAdd(&mass[bin], sum);
+    }
+}
+
 // Radix selection on keys: among elements matching `pred` with key in the
 // range sharing the common prefix of [klo, khi], find the key tau at which the
 // descending cumulative measure (count, or fixed-point mass when kMass)
@@ -318,14 +392,13 @@ __device__ bool radix_select(Smem& sm, cg::cluster_group& cl, const Slice& sl, u
     eq_mass = 0;
     if (hi_bit == 0) {  // a single key in the window: count it
         unsigned long long v[2] = {0, 0};
-        for (int i = tid; i < sl.n; i += kThreads) {
-            const float z = sl.val(i);
+        for_each_elem(sl, [&](float z, int32_t idx) {
             const uint32_t key = ordered_key(z);
-            if (key == khi && pred(key, sl.lo + i)) {
+            if (key == khi && pred(key, idx)) {
                 v[0] += 1;
                 if (kMass) v[1] += to_fixed(weight_f(z, zmax, inv_t));
             }
-        }
+        });
         unsigned long long o[2];
         cluster_sum_u64<2>(sm, cl, v, o);
         tau = khi;
@@ -343,16 +416,13 @@ __device__ bool radix_select(Smem& sm, cg::cluster_group& cl, const Slice& sl, u
             if (kMass) sm.hmass[buf][b] = 0;
         }
         __syncthreads();
-        for (int i = tid; i < sl.n; i += kThreads) {
-            const float z = sl.val(i);
+        for_each_elem(sl, [&](float z, int32_t idx) {
             const uint32_t key = ordered_key(z);
-            const bool match = (hi_bit >= 32 ? true : (key >> hi_bit) == prefix) && pred(key, sl.lo + i);
-            if (match) {
-                const uint32_t d = (key >> lo_bit) & ((1u << nb) - 1u);
-                atomicAdd(&sm.hcnt[buf][d], 1u);
-                if (kMass) atomicAdd(&sm.hmass[buf][d], static_cast<unsigned long long>(to_fixed(weight_f(z, zmax, inv_t))));
-            }
-        }
+            const bool match = (hi_bit >= 32 ? true : (key >> hi_bit) == prefix) && pred(key, idx);
+            const int d = match ? static_cast<int>((key >> lo_bit) & ((1u << nb) - 1u)) : -1;
+            hist_add(sm.hcnt[buf], kMass ? sm.hmass[buf] : nullptr, d,
+                     kMass && match ? static_cast<unsigned long long>(to_fixed(weight_f(z, zmax, inv_t))) : 0ull);
+        });
         cl.sync();
         // thread t takes bin (nbins - 1 - t): descending key order
         const int nbins = 1 << nb;
@@ -397,13 +467,14 @@ __device__ int32_t tie_index(Smem& sm, cg::cluster_group& cl, const Slice& sl, u
                              unsigned long long t, Pred pred) {
     const int tid = threadIdx.x;
     const int rank = static_cast<int>(cl.block_rank());
-    // ordered ownership: thread i owns [i*per, (i+1)*per) of the slice
-    const int a = min(tid * sl.per, sl.n), e = min(a + sl.per, sl.n);
+    // ordered ownership: each thread a contiguous run of the slice's vectors
+    int a, e;
+    thread_run(sl, a, e);
     unsigned long long mine = 0;
-    for (int i = a; i < e; ++i) {
-        const uint32_t key = ordered_key(sl.val(i));
-        if (key == tau && pred(key, sl.lo + i)) ++mine;
-    }
+    for_run(sl, a, e, [&](float z, int32_t idx) {
+        const uint32_t key = ordered_key(z);
+        if (key == tau && pred(key, idx)) ++mine;
+    });
     const unsigned long long incl = block_scan_u64(sm, mine);
     __shared__ unsigned long long s_total;
     if (tid == kThreads - 1) s_total = incl;
@@ -423,13 +494,14 @@ __device__ int32_t tie_index(Smem& sm, cg::cluster_group& cl, const Slice& sl, u
         const unsigned long long want = t - before;
         if (incl >= want && incl - mine < want) {
             unsigned long long k = incl - mine;
-            for (int i = a; i < e; ++i) {
-                const uint32_t key = ordered_key(sl.val(i));
-                if (key == tau && pred(key, sl.lo + i) && ++k == want) {
-                    sm.xu[buf][0] = static_cast<unsigned long long>(sl.lo + i);
-                    break;
+            bool done = false;
+            for_run(sl, a, e, [&](float z, int32_t idx) {
+                const uint32_t key = ordered_key(z);
+                if (!done && key == tau && pred(key, idx) && ++k == want) {
+                    sm.xu[buf][0] = static_cast<unsigned long long>(idx);
+                    done = true;
                 }
-            }
+            });
         }
     }
     cl.sync();
@@ -465,11 +537,11 @@ __device__ void row_policy_radix(Smem& sm, cg::cluster_group& cl, const Slice& s
         unsigned long long v[kWin + 1], cnt[kWin + 1];
 #pragma unroll
         for (int i = 0; i <= kWin; ++i) v[i] = 0;
-        for (int i = tid; i < sl.n; i += kThreads) {
-            const float d = zmax - sl.val(i);
+        for_each_elem(sl, [&](float z, int32_t) {
+            const float d = zmax - z;
 #pragma unroll
             for (int w = 0; w < kWin; ++w) v[w] += d <= static_cast<float>(1 << w) ? 1ull : 0ull;
-        }
+        });
         cluster_sum_u64<kWin + 1>(sm, cl, v, cnt);
         // the narrowest width holding k elements, doubled against rounding at its edge
         float zlo = -__int_as_float(0x7F800000);
@@ -492,17 +564,16 @@ __device__ void row_policy_radix(Smem& sm, cg::cluster_group& cl, const Slice& s
     unsigned long long v[kWin + 1], ms[kWin + 1];
 #pragma unroll
     for (int i = 0; i <= kWin; ++i) v[i] = 0;
-    for (int i = tid; i < sl.n; i += kThreads) {
-        const float z = sl.val(i);
+    for_each_elem(sl, [&](float z, int32_t idx) {
         const float d = (zmax - z) * inv_t;
-        if (d > 41.0f * 0.6931472f + 1.0f) continue;  // weight rounds to 0 in 2^-40 units
+        if (d > 41.0f * 0.6931472f + 1.0f) return;  // weight rounds to 0 in 2^-40 units
         const uint32_t key = ordered_key(z);
-        if (!in_k(key, sl.lo + i)) continue;
+        if (!in_k(key, idx)) return;
         const unsigned long long w = to_fixed(weight_f(z, zmax, inv_t));
         v[kWin] += w;
 #pragma unroll
         for (int wi = 0; wi < kWin; ++wi) v[wi] += d <= static_cast<float>(2 << wi) ? w : 0ull;
-    }
+    });
     cluster_sum_u64<kWin + 1>(sm, cl, v, ms);
     const unsigned long long kept = ms[kWin];
     res.tau = tau_k;
@@ -534,18 +605,36 @@ __device__ void row_policy_radix(Smem& sm, cg::cluster_group& cl, const Slice& s
     res.mass = above + t * wt;
 }
 
-// Inverse-CDF draw in token-index order over fixed-point weights w(i) (a
-// functor of the slice-local index): the smallest index whose inclusive
-// prefix exceeds floor(m * total / 2^24), m the 24-bit uniform.  Every CTA
-// returns the index.
-template <typename Wf>
-__device__ int32_t sample_fixed(Smem& sm, cg::cluster_group& cl, const Slice& sl, uint32_t m24, Wf wf,
+// Inverse-CDF draw in token-index order over fixed-point weights w(z, index)
+// (index = the token): the smallest index whose inclusive prefix exceeds
+// floor(m * total / 2^24), m the 24-bit uniform.  Each thread owns a
+// contiguous run of the slice's 16-byte vectors (read kBatch at a time);
+// block scan, then the prefix over the cluster's ranks; the owning thread
+// re-reads its run to find the token.  Every CTA returns the index.
+template <typename Wz>
+__device__ int32_t sample_fixed(Smem& sm, cg::cluster_group& cl, const Slice& sl, uint32_t m24, Wz wz,
                                 unsigned long long& total_out) {
     const int tid = threadIdx.x;
     const int rank = static_cast<int>(cl.block_rank());
-    const int a = min(tid * sl.per, sl.n), e = min(a + sl.per, sl.n);
+    const int vp = sl.vper(), nv = sl.nvec();
+    const int pv = (nv + kThreads - 1) / kThreads;  // vectors per thread
+    const int a = min(tid * pv, nv), e = min(a + pv, nv);
+    auto vec_weight = [&](int j, const uint4& v) {
+        unsigned long long w = 0;
+#pragma unroll
+        for (int l = 0; l < 8; ++l)
+            if (l < vp) w += wz(vec_elem(v, l, sl.bf16), sl.lo + j * vp + l);
+        return w;
+    };
     unsigned long long mine = 0;
-    for (int i = a; i < e; ++i) mine += wf(i);
+    for (int j0 = a; j0 < e; j0 += kBatch) {
+        uint4 vb[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) vb[u] = j0 + u < e ? sl.vec(j0 + u) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u)
+            if (j0 + u < e) mine += vec_weight(j0 + u, vb[u]);
+    }
     const unsigned long long incl = block_scan_u64(sm, mine);
     __shared__ unsigned long long s_total;
     if (tid == kThreads - 1) s_total = incl;
@@ -571,11 +660,17 @@ __device__ int32_t sample_fixed(Smem& sm, cg::cluster_group& cl, const Slice& sl
         const unsigned long long tl = target - before;  // within this CTA: first prefix > tl
         if (incl > tl && incl - mine <= tl) {
             unsigned long long c = incl - mine;
-            for (int i = a; i < e; ++i) {
-                c += wf(i);
-                if (c > tl) {
-                    sm.xu[buf][0] = static_cast<unsigned long long>(sl.lo + i);
-                    break;
+            bool found = false;
+            for (int j = a; j < e && !found; ++j) {
+                const uint4 v = sl.vec(j);
+                for (int l = 0; l < vp; ++l) {
+                    const int32_t idx = sl.lo + j * vp + l;
+                    c += wz(vec_elem(v, l, sl.bf16), idx);
+                    if (c > tl) {
+                        sm.xu[buf][0] = static_cast<unsigned long long>(idx);
+                        found = true;
+                        break;
+                    }
                 }
             }
         }
@@ -590,64 +685,44 @@ __device__ int32_t sample_fixed(Smem& sm, cg::cluster_group& cl, const Slice& sl
     return idx;
 }
 
-// Load this CTA's slice [lo, lo + n) of a row (n a multiple of 8, the start
-// 16-byte aligned) into shared memory with 1-D bulk copies in kLoadChunks
-// pieces, and reduce the row's max key / lowest argmax / non-finite flag over
-// the cluster as the pieces land.  timeout: a copy did not land in time (the
-// row's results are then not to be used).
-template <int kDtype>
-__device__ void load_slice_and_max(Smem& sm, cg::cluster_group& cl, const void* row, int lo, int n, void* zs,
-                                   RowResult& res, bool& bad, bool& timeout) {
-    constexpr int kEsize = kDtype == kBF16 ? 2 : 4;
-    constexpr int kPer = 16 / kEsize;
-    const char* src = static_cast<const char*>(row) + static_cast<int64_t>(lo) * kEsize;
-    char* dst = static_cast<char*>(zs);
-    const int per = ((n + kLoadChunks - 1) / kLoadChunks + 7) / 8 * 8;  // elements per piece
-    const uint32_t ph = sm.lphase;
-    __syncthreads();  // every thread is done with the previous contents of zs
-    if (threadIdx.x == 0) {
-        fence_proxy_async_smem();
-        for (int c = 0; c < kLoadChunks; ++c) {
-            const int a = min(c * per, n), e = min(a + per, n);
-            if (e > a) {
-                mbar_arrive_expect_tx(&sm.lbar[c], static_cast<uint32_t>((e - a) * kEsize));
-                bulk_g2s(dst + a * kEsize, src + a * kEsize, static_cast<uint32_t>((e - a) * kEsize), &sm.lbar[c]);
-            }
-        }
-        sm.lphase = ph ^ 1u;
-    }
-    unsigned long long best = 0;
+// One pass over this CTA's slice (kBatch 16-byte vectors per thread in
+// flight): the row's max key / lowest argmax / non-finite flag, reduced over
+// the cluster.  Each thread keeps a packed maximum and looks for the index
+// only when a vector beats it.
+__device__ void slice_max(Smem& sm, cg::cluster_group& cl, const Slice& sl, RowResult& res, bool& bad) {
+    const int vp = sl.vper(), nv = sl.nvec();
     float nanacc = -__int_as_float(0x7F800000);
     float bval = -__int_as_float(0x7F800000);  // this thread's maximum (vectors in index order)
     int32_t bidx = -1;
-    bool late = false;
-    for (int c = 0; c < kLoadChunks; ++c) {
-        const int a = min(c * per, n), e = min(a + per, n);
-        if (e <= a) continue;  // empty in every load of this kernel: its barrier never flips
-        if (!mbar_wait(&sm.lbar[c], ph, kWaitLimitNs)) {
-            late = true;  // give the copy a second bounded chance to land before moving on
-            mbar_wait(&sm.lbar[c], ph, kWaitLimitNs);
+    for (int j0 = threadIdx.x; j0 < nv; j0 += kThreads * kBatch) {
+        uint4 v[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            const int j = j0 + u * kThreads;
+            v[u] = j < nv ? sl.vec(j) : make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u);
         }
-        for (int j = a / kPer + threadIdx.x; j < e / kPer; j += kThreads) {
-            const uint4 v = ld_shared_v4(dst + j * 16);
-            const float vm = vec_max(v, kDtype == kBF16);
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            const int j = j0 + u * kThreads;
+            if (j >= nv) break;
+            const float vm = vec_max(v[u], sl.bf16);
             nanacc = fmax_nan(nanacc, vm);
             if (vm > bval) {  // rare: a new maximum of this thread; its first occurrence
-                int l0 = kPer - 1;
+                int l0 = vp - 1;
 #pragma unroll
-                for (int l = kPer - 1; l >= 0; --l)
-                    if (vec_elem(v, l, kDtype == kBF16) == vm) l0 = l;
+                for (int l = 7; l >= 0; --l)
+                    if (l < vp && vec_elem(v[u], l, sl.bf16) == vm) l0 = l;
                 bval = vm;
-                bidx = lo + j * kPer + l0;
+                bidx = sl.lo + j * vp + l0;
             }
         }
     }
+    unsigned long long best = 0;
     if (bidx >= 0 && !bad_logit(bval))
         best = (static_cast<unsigned long long>(ordered_key(bval)) << 32) | (0xFFFFFFFFull - static_cast<uint32_t>(bidx));
     unsigned long long mk, fl;
-    cluster_max_u64(sm, cl, best, (bad_logit(nanacc) ? 1ull : 0ull) | (late ? 2ull : 0ull), mk, fl);
-    bad = (fl & 1ull) != 0;
-    timeout = (fl & 2ull) != 0;
+    cluster_max_u64(sm, cl, best, bad_logit(nanacc) ? 1ull : 0ull, mk, fl);
+    bad = fl != 0;
     if (mk == 0) {
         res.zmax = -__int_as_float(0x7F800000);
         res.argmax = -1;
@@ -735,12 +810,19 @@ __device__ void compact_candidates(Smem& sm, cg::cluster_group& cl, const Slice&
     unsigned int* rcount = cl.map_shared_rank(&sm.ccount, 0);
     unsigned long long* dst = cl.map_shared_rank(cbuf, 0);
     const int vp = sl.vper(), nv = sl.nvec();
-    for (int j0 = 0; j0 < nv; j0 += kThreads) {  // the same trip count for every thread
-        const int j = j0 + static_cast<int>(threadIdx.x);
+    for (int jb = 0; jb < nv; jb += kThreads * kBatch) {  // the same trip count for every thread
+      uint4 vb[kBatch];
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+          const int j = jb + u * kThreads + static_cast<int>(threadIdx.x);
+          vb[u] = j < nv ? sl.vec(j) : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int j = jb + u * kThreads + static_cast<int>(threadIdx.x);
         unsigned mine = 0;  // bit l: element l of vector j is picked
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        const uint4 v = vb[u];
         if (j < nv) {
-            v = sl.vec(j);
             if (vec_max(v, sl.bf16) >= floor) {
 #pragma unroll
                 for (int l = 0; l < 8; ++l)
@@ -766,6 +848,7 @@ __device__ void compact_candidates(Smem& sm, cg::cluster_group& cl, const Slice&
                 ++base;
             }
         }
+      }
     }
     cl.sync();
 }
@@ -847,10 +930,26 @@ __device__ void row_policy(Smem& sm, cg::cluster_group& cl, const Slice& sl, int
     unsigned long long* hp = sm.hmass[1];
     unsigned long long tmass = 0;
     const bool hist = use_k || use_p;
+    // Each warp counts into a private copy (in the candidate buffer, unused
+    // until the compaction): no contention between warps on busy bins.
+    const int warp_id = tid >> 5;
+    uint32_t* whc = reinterpret_cast<uint32_t*>(cbuf) + warp_id * kBins;
+    unsigned long long* whp = cbuf + warp_id * kBins;
+    for (int i = tid; i < kWarps * kBins; i += kThreads) cbuf[i] = 0ull;  // kWarps * kBins == kCap
+    __syncthreads();
     {
         const int vp = sl.vper(), nv = sl.nvec();
-        for (int j = tid; j < nv; j += kThreads) {
-            const uint4 v = sl.vec(j);
+        for (int j0 = tid; j0 < nv; j0 += kThreads * kBatch) {
+          uint4 vb[kBatch];
+#pragma unroll
+          for (int u = 0; u < kBatch; ++u) {
+              const int j = j0 + u * kThreads;
+              vb[u] = j < nv ? sl.vec(j) : make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u);
+          }
+#pragma unroll
+          for (int u = 0; u < kBatch; ++u) {
+            const uint4 v = vb[u];
+            if (j0 + u * kThreads >= nv) break;
             if ((zmax - vec_max(v, sl.bf16)) * inv_t >= 32.0f) continue;  // the whole vector is out of range
 #pragma unroll
             for (int l = 0; l < 8; ++l) {
@@ -862,12 +961,24 @@ __device__ void row_policy(Smem& sm, cg::cluster_group& cl, const Slice& sl, int
                     if (with_mass) {
                         const float w = weight_f(z, zmax, inv_t);
                         tmass += to_fixed(w);
-                        if (hist) atomicAdd(&hp[bin], (1ull << 40) + __float2uint_rd(w * 65536.0f));
+                        if (hist) atomicAdd(&whp[bin], (1ull << 40) + __float2uint_rd(w * 65536.0f));
                     } else {
-                        atomicAdd(&hc[bin], 1u);
+                        atomicAdd(&whc[bin], 1u);
                     }
                 }
             }
+          }
+        }
+    }
+    __syncthreads();
+    {  // the CTA's histogram: bin tid over the warps' copies
+        unsigned long long t = 0;
+        if (with_mass) {
+            for (int w = 0; w < kWarps; ++w) t += cbuf[w * kBins + tid];
+            hp[tid] = t;
+        } else {
+            for (int w = 0; w < kWarps; ++w) t += reinterpret_cast<const uint32_t*>(cbuf)[w * kBins + tid];
+            hc[tid] = static_cast<uint32_t>(t);
         }
     }
     __shared__ unsigned long long s_ctot;  // this CTA's exact mass (top-k off)
@@ -924,6 +1035,15 @@ __device__ void row_policy(Smem& sm, cg::cluster_group& cl, const Slice& sl, int
     const unsigned long long incl = use_k ? cc : cm, here = use_k ? c : m;
     if (incl >= need && incl - here < need) {  // the crossing bin (unique)
         s_bin = tid;
+        s_count = cc;
+    }
+    __syncthreads();
+    // No crossing: top-k reaches past s = 32 or the lower bounds of top-p's
+    // mass fall short.  Tokens past s = 32 have weight 0 in fixed point: they
+    // are never drawn and carry no mass, so every token of the support that
+    // matters is in range - take them all as candidates.
+    if (s_bin < 0 && tid == kThreads - 1) {
+        s_bin = kBins - 1;
         s_count = cc;
     }
     __syncthreads();
