@@ -282,6 +282,29 @@ def mixed_serving(V=VOCAB, B=256, gamma=5, r=256, H=4096, device="cpu", seed=100
                     extra=dict(adversarial=adv))
 
 
+FLAT_POLICIES = ((1.0, 0, 0.9), (1.0, 5000, 1.0), (1.0, 5000, 0.9), (1.3, 0, 0.5),
+                 (0.8, 0, 0.95), (1.0, 0, 1.0), (2.0, 300, 0.9), (1.0, 20000, 0.99))
+
+
+def flat_rows(V=VOCAB, B=8, gamma=3, dtype=BF16, r=0, device="cpu", seed=1006) -> Workload:
+    """Flat rows: target logits i.i.d. N(0, 0.5), so that thousands of tokens
+    share a 1/8 step of (zmax - z)/T near a top-p or top-k cut (and, in bf16,
+    ties hundreds deep); draft backbone row k = target row k + N(0, 0.3);
+    request b takes (T, top-k, top-p) = FLAT_POLICIES[b mod 8]."""
+    g = _gen(seed, device)
+    target = _normal((B, gamma + 1, V), 0.5, g, device)
+    backbone = target[:, :gamma, :] + _normal((B, gamma, V), 0.3, g, device)
+    pol = [FLAT_POLICIES[b % len(FLAT_POLICIES)] for b in range(B)]
+    policy = Policy(torch.tensor([t for t, _, _ in pol], dtype=torch.float32, device=device),
+                    torch.tensor([k for _, k, _ in pol], dtype=torch.int32, device=device),
+                    torch.tensor([p for _, _, p in pol], dtype=torch.float32, device=device),
+                    torch.zeros((B,), dtype=torch.int32, device=device))
+    td = torch.bfloat16 if dtype == BF16 else torch.float32
+    return Workload("flat_rows", B, gamma, V, dtype, target.to(td).contiguous(), backbone.to(td).contiguous(),
+                    _anchors(B, V, g, device), markov_weights(V, r, 0, g, device), None, policy,
+                    make_keys(B, 9, 100, device))
+
+
 @dataclass
 class StatsWorkload:
     name: str

@@ -104,3 +104,4 @@ def test_markov_full_vocab_rank256(ds, oracle):
     w = synth.decode_verify_tile(B=16, H=4096, device="cuda")
     ref, got = _both(ds, oracle, w)
     _check(ref, got)
+

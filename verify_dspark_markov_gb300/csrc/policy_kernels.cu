@@ -30,11 +30,12 @@ __device__ __forceinline__ float inv_mass(uint64_t mass) {
     return static_cast<float>(rp::kFix / static_cast<double>(mass));
 }
 
-// Dynamic shared memory: the candidate buffer (used in rank 0).  The row
-// slices are read in place from global memory.
+// Dynamic shared memory: the candidate buffer (used in rank 0) followed by
+// the per-warp histogram counts.  The row slices are read in place from
+// global memory.
 
 template <int kDtype>
-__global__ void __cluster_dims__(rp::kC, 1, 1) __launch_bounds__(rp::kThreads)
+__global__ void __cluster_dims__(rp::kC, 1, 1) __launch_bounds__(rp::kThreads, 4)
     verify_rows_kernel(const VerifyProbParams p) {
     extern __shared__ __align__(16) unsigned char dyn[];
     __shared__ rp::Smem sm;
@@ -222,7 +223,7 @@ __global__ void __cluster_dims__(rp::kC, 1, 1) __launch_bounds__(rp::kThreads)
 }
 
 template <int kDtype>
-__global__ void __cluster_dims__(rp::kC, 1, 1) __launch_bounds__(rp::kThreads)
+__global__ void __cluster_dims__(rp::kC, 1, 1) __launch_bounds__(rp::kThreads, 4)
     markov_step_kernel(const MarkovStepParams p) {
     extern __shared__ __align__(16) unsigned char dyn[];
     __shared__ rp::Smem sm;
@@ -398,7 +399,8 @@ int policy_slice(int V) { return ((V + kC - 1) / kC + 7) / 8 * 8; }
 int policy_smem_bytes(int V, int store_bf16) {
     (void)V;
     (void)store_bf16;
-    return rp::kCap * static_cast<int>(sizeof(unsigned long long));
+    return rp::kCap * static_cast<int>(sizeof(unsigned long long)) +
+           rp::kWarps * rp::kBins * static_cast<int>(sizeof(uint32_t));
 }
 
 cudaError_t launch_verify_prob(const VerifyProbParams& p, cudaStream_t stream) {

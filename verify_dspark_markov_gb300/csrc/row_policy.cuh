@@ -3,8 +3,7 @@
 // exact inverse-CDF draw over the policy's weights.  The slices stay in
 // global memory: the first pass over a row streams it from HBM (or from L2
 // when the row was just written, like the Markov logits), later passes find
-// it in L2.  With no row held in shared memory a cluster needs ~24 KB, so one
-// row per SM is in flight (4 CTAs of 256 threads).
+// it in L2.  With no row held in shared memory a CTA needs ~37 KB.
 //
 // The policy [FT Exact decoding semantics > Probabilistic] as this library
 // reads it: greedy = one-hot at the lowest-index argmax; otherwise temperature,
@@ -18,13 +17,13 @@
 // integers w = round(2^40 exp((z - zmax)/T)), so every sum, every top-p
 // comparison and every inverse-CDF boundary is an exact, order-independent
 // integer decision.  To find the cut, one pass builds a histogram of
-// s = (zmax - z)/T in bins of 1/8 (counts, and fixed-point masses when top-p
-// applies to the whole row), reduced once over the cluster; the bin where the
-// cumulative count reaches k (or the mass reaches p of the total) bounds a
-// small candidate set, which is compacted into rank 0, sorted by (logit
-// descending, index ascending) and cut there by exact prefix sums.  Rows whose
-// candidates would not fit (very flat rows) fall back to radix selection on
-// order-preserving 32-bit keys over the slices.
+// s = (zmax - z)/T in bins of 1/8 with exact counts and exact fixed-point
+// masses, reduced once over the cluster; its prefix sums bound the cuts to a
+// window of bins (usually one), whose elements are compacted into rank 0,
+// sorted by (logit descending, index ascending) and cut there by exact
+// prefix sums continued from the exact mass above the window.  A window too
+// large for the buffer (very flat rows) is resolved by radix selection on
+// order-preserving 32-bit keys inside its key range.
 #pragma once
 
 #include <cooperative_groups.h>
@@ -42,9 +41,9 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kBins = 256;      // 8-bit radix digits
 constexpr int kWin = 8;         // candidate window widths
 constexpr int kCap = 2048;      // candidate buffer of rank 0 (composite keys)
-constexpr int kSample = 8;      // 1 in kSample elements feeds the window estimate
 constexpr double kFix = 1099511627776.0;  // 2^40: fixed-point scale of the weights
-static_assert(kWarps * kBins <= kCap, "the per-warp histograms live in the candidate buffer");
+static_assert(kWarps * kBins <= kCap, "the per-warp histogram masses live in the candidate buffer");
+static_assert(kBins == kThreads, "one histogram bin per thread");
 constexpr float kLog2e = 1.4426950408889634f;
 
 __device__ __forceinline__ float ex2(float x) {
@@ -350,79 +349,86 @@ __device__ __forceinline__ void for_run(const Slice& sl, int a, int e, F fn) {
     }
 }
 
-// Warp-aggregated histogram update for the radix digits, where a flat row
-// sends nearly every element to one or two bins: the active lanes with the
-// same bin (bin < 0: none) add their counts and values with one atomic by
-// the group's first lane.  Values are split into two parts of 20 bits so that
-// a 32-lane sum fits 32-bit reductions.  (Where bins are spread, plain
-// atomics are cheaper than the grouping.)
-__device__ __forceinline__ void hist_add(uint32_t* cnt, unsigned long long* mass, int bin, unsigned long long w) {
-    const unsigned act = __activemask();
-    const unsigned peers = __match_any_sync(act, bin);
-    if (bin < 0) return;
-    const int lane = threadIdx.x & 31;
-    const int leader = __ffs(peers) - 1;
-    unsigned long long sum = 0;
-    if (mass) {
-        const unsigned hi = __reduce_add_sync(peers, static_cast<unsigned>(w >> 20));
-        const unsigned lo = __reduce_add_sync(peers, static_cast<unsigned>(w & 0xFFFFFull));
-        sum = (static_cast<unsigned long long>(hi) << 20) + lo;
-    }
-    if (lane == leader) {
-        if (cnt) atomicAdd(&cnt[bin], static_cast<unsigned>(__popc(peers)));
-        if (mass) atomicAdd(&mass[bin], sum);
-    }
-}
-
-// Radix selection on keys: among elements matching `pred` with key in the
-// range sharing the common prefix of [klo, khi], find the key tau at which the
-// descending cumulative measure (count, or fixed-point mass when kMass)
-// reaches `target`.  Returns tau, the measure strictly above tau and the
-// count / mass of elements equal to tau (all within pred).
+// Radix selection on keys inside the window [klo, khi]: among the elements
+// with a key in the window matching `pred`, find the key tau at which the
+// descending cumulative measure (count, or fixed-point mass when kMass),
+// started at above0 (the measure of everything above the window), reaches
+// `target`.  Returns tau, the measure strictly above tau (above0 included)
+// and the count / mass of the elements equal to tau (within pred); false when
+// the window does not reach target.  Digits of 8 bits below the window's
+// common prefix; in bf16 slices the low 16 bits of every key follow from its
+// sign bit, so the digits stop at bit 16.  Each warp counts into a private
+// copy (wbuf: kWarps x kBins masses, then kWarps x kBins counts), summed per
+// CTA and then over the cluster.
 template <bool kMass, typename Pred>
-__device__ bool radix_select(Smem& sm, cg::cluster_group& cl, const Slice& sl, uint32_t klo, uint32_t khi,
-                             unsigned long long target, float zmax, float inv_t, Pred pred, uint32_t& tau,
-                             unsigned long long& above, unsigned long long& eq_cnt,
-                             unsigned long long& eq_mass) {
+__device__ bool radix_select(Smem& sm, cg::cluster_group& cl, const Slice& sl, unsigned long long* wbuf,
+                             uint32_t klo, uint32_t khi, unsigned long long above0, unsigned long long target,
+                             float zmax, float inv_t, Pred pred, uint32_t& tau, unsigned long long& above,
+                             unsigned long long& eq_cnt, unsigned long long& eq_mass) {
     const int tid = threadIdx.x;
+    const int min_bit = sl.bf16 ? 16 : 0;
     int hi_bit = klo == khi ? 0 : 32 - __clz(static_cast<int>(klo ^ khi));  // bits still open
+    if (hi_bit < min_bit) hi_bit = min_bit;
     uint32_t prefix = hi_bit >= 32 ? 0u : (khi >> hi_bit);
-    above = 0;
+    auto full_key = [min_bit](uint32_t pre) -> uint32_t {
+        return min_bit ? ((pre << 16) | ((pre & 0x8000u) ? 0u : 0xFFFFu)) : pre;
+    };
+    above = above0;
     eq_cnt = 0;
     eq_mass = 0;
-    if (hi_bit == 0) {  // a single key in the window: count it
+    if (hi_bit == min_bit) {  // a single key in the window: count it
+        const uint32_t k1 = full_key(prefix);
         unsigned long long v[2] = {0, 0};
-        for_each_elem(sl, [&](float z, int32_t idx) {
-            const uint32_t key = ordered_key(z);
-            if (key == khi && pred(key, idx)) {
-                v[0] += 1;
-                if (kMass) v[1] += to_fixed(weight_f(z, zmax, inv_t));
-            }
-        });
+        if (k1 >= klo && k1 <= khi) {
+            for_each_elem(sl, [&](float z, int32_t idx) {
+                const uint32_t key = ordered_key(z);
+                if (key == k1 && pred(key, idx)) {
+                    v[0] += 1;
+                    if (kMass) v[1] += to_fixed(weight_f(z, zmax, inv_t));
+                }
+            });
+        }
         unsigned long long o[2];
         cluster_sum_u64<2>(sm, cl, v, o);
-        tau = khi;
+        tau = k1;
         eq_cnt = o[0];
         eq_mass = o[1];
-        return (kMass ? o[1] : o[0]) >= target;
+        return above0 + (kMass ? o[1] : o[0]) >= target;
     }
+    const int warp = tid >> 5;
+    uint32_t* wcnt = reinterpret_cast<uint32_t*>(wbuf + kWarps * kBins);
+    unsigned long long* wm = wbuf + warp * kBins;
+    uint32_t* wc = wcnt + warp * kBins;
     bool found = true;
-    while (hi_bit > 0) {
-        const int nb = hi_bit >= 8 ? 8 : hi_bit;
+    while (hi_bit > min_bit) {
+        const int nb = min(8, hi_bit - min_bit);
         const int lo_bit = hi_bit - nb;
         const int buf = sm.hparity;
-        for (int b = tid; b < kBins; b += kThreads) {
-            sm.hcnt[buf][b] = 0;
-            if (kMass) sm.hmass[buf][b] = 0;
+        for (int i = tid; i < kWarps * kBins; i += kThreads) {
+            wcnt[i] = 0u;
+            if (kMass) wbuf[i] = 0ull;
         }
         __syncthreads();
+        const uint32_t pre = prefix;
+        const int hb = hi_bit;
         for_each_elem(sl, [&](float z, int32_t idx) {
             const uint32_t key = ordered_key(z);
-            const bool match = (hi_bit >= 32 ? true : (key >> hi_bit) == prefix) && pred(key, idx);
-            const int d = match ? static_cast<int>((key >> lo_bit) & ((1u << nb) - 1u)) : -1;
-            hist_add(sm.hcnt[buf], kMass ? sm.hmass[buf] : nullptr, d,
-                     kMass && match ? static_cast<unsigned long long>(to_fixed(weight_f(z, zmax, inv_t))) : 0ull);
+            if (key < klo || key > khi || (hb < 32 && (key >> hb) != pre) || !pred(key, idx)) return;
+            const int d = static_cast<int>((key >> lo_bit) & ((1u << nb) - 1u));
+            atomicAdd(&wc[d], 1u);
+            if (kMass) atomicAdd(&wm[d], static_cast<unsigned long long>(to_fixed(weight_f(z, zmax, inv_t))));
         });
+        __syncthreads();
+        {  // the CTA's histogram: bin tid over the warps' copies
+            uint32_t c = 0;
+            unsigned long long m = 0;
+            for (int w = 0; w < kWarps; ++w) {
+                c += wcnt[w * kBins + tid];
+                if (kMass) m += wbuf[w * kBins + tid];
+            }
+            sm.hcnt[buf][tid] = c;
+            if (kMass) sm.hmass[buf][tid] = m;
+        }
         cl.sync();
         // thread t takes bin (nbins - 1 - t): descending key order
         const int nbins = 1 << nb;
@@ -456,7 +462,7 @@ __device__ bool radix_select(Smem& sm, cg::cluster_group& cl, const Slice& sl, u
         if (tid == 0) sm.hparity ^= 1;
         __syncthreads();
     }
-    tau = prefix;
+    tau = full_key(prefix);
     return found;
 }
 
@@ -518,7 +524,7 @@ __device__ int32_t tie_index(Smem& sm, cg::cluster_group& cl, const Slice& sl, u
 // candidate set of row_policy would not fit).  z slice already loaded; max
 // key, argmax and the bad flag already reduced.
 __device__ void row_policy_radix(Smem& sm, cg::cluster_group& cl, const Slice& sl, int V, const Policy& pol,
-                                 RowResult& res) {
+                                 RowResult& res, unsigned long long* wbuf) {
     const float zmax = res.zmax;
     const uint32_t kmax = ordered_key(zmax);
     // greedy: the argmax alone
@@ -550,10 +556,10 @@ __device__ void row_policy_radix(Smem& sm, cg::cluster_group& cl, const Slice& s
         const uint32_t klo = zlo == -__int_as_float(0x7F800000) ? 0u : ordered_key(zlo);
         unsigned long long above, eqc, eqm;
         auto all = [](uint32_t, int32_t) { return true; };
-        if (!radix_select<false>(sm, cl, sl, klo, kmax, static_cast<unsigned long long>(pol.top_k), zmax, inv_t,
-                                 all, tau_k, above, eqc, eqm))
-            radix_select<false>(sm, cl, sl, 0u, kmax, static_cast<unsigned long long>(pol.top_k), zmax, inv_t,
-                                all, tau_k, above, eqc, eqm);
+        if (!radix_select<false>(sm, cl, sl, wbuf, klo, kmax, 0ull, static_cast<unsigned long long>(pol.top_k),
+                                 zmax, inv_t, all, tau_k, above, eqc, eqm))
+            radix_select<false>(sm, cl, sl, wbuf, 0u, kmax, 0ull, static_cast<unsigned long long>(pol.top_k), zmax,
+                                inv_t, all, tau_k, above, eqc, eqm);
         const unsigned long long need = static_cast<unsigned long long>(pol.top_k) - above;
         cut_k = tie_index(sm, cl, sl, tau_k, need, [](uint32_t, int32_t) { return true; });
     }
@@ -592,8 +598,8 @@ __device__ void row_policy_radix(Smem& sm, cg::cluster_group& cl, const Slice& s
     if (use_k && klo < tau_k) klo = tau_k;  // the cut lies inside the top-k set
     uint32_t tau_p;
     unsigned long long above, eqc, eqm;
-    if (!radix_select<true>(sm, cl, sl, klo, kmax, theta, zmax, inv_t, in_k, tau_p, above, eqc, eqm))
-        radix_select<true>(sm, cl, sl, 0u, kmax, theta, zmax, inv_t, in_k, tau_p, above, eqc, eqm);
+    if (!radix_select<true>(sm, cl, sl, wbuf, klo, kmax, 0ull, theta, zmax, inv_t, in_k, tau_p, above, eqc, eqm))
+        radix_select<true>(sm, cl, sl, wbuf, 0u, kmax, 0ull, theta, zmax, inv_t, in_k, tau_p, above, eqc, eqm);
     // tied elements share one weight; take just enough of them in index order
     const unsigned long long wt = eqc ? eqm / eqc : 0ull;
     unsigned long long t = wt ? (theta - above + wt - 1) / wt : eqc;
@@ -889,20 +895,96 @@ __device__ int find_crossing(Smem& sm, int n, unsigned long long th, bool strict
     return pos;
 }
 
-// Window widths: top-k in logit units, top-p in units of (zmax - z) / T.
-__device__ __forceinline__ float k_width(int w) { return 0.25f * static_cast<float>(1 << w); }
-__device__ __forceinline__ float p_width(int w) { return 0.5f * static_cast<float>(1 << w); }
 
-// The policy of the row held by the cluster.  One pass builds the histogram
-// of s = (zmax - z)/T in bins of 1/8 below s = 32 (beyond, the weight is 0 in
-// fixed point): counts, plus fixed-point masses when top-k is off.  Its
-// cluster sum gives the bin where the cumulative count reaches k (top-k) or
-// the cumulative mass reaches p of the total (top-p alone); every element of
-// the support lies at or below that bin.  Those candidates are compacted into
-// rank 0's buffer, sorted by (logit descending, index ascending), and the
-// cuts are taken there by exact fixed-point prefix sums.  cbuf = this CTA's
-// candidate buffer (only rank 0's is used).  Falls back to row_policy_radix
-// when the candidates would not fit kCap.
+// ceil(p * kept) clamped to [1, kept] (kept = 0 gives 0): the fixed-point
+// mass a top-p prefix must reach.
+__device__ __forceinline__ unsigned long long p_threshold(float p, unsigned long long kept) {
+    const double th = ceil(static_cast<double>(p) * static_cast<double>(kept));
+    const unsigned long long t = th < 1.0 ? 1ull : static_cast<unsigned long long>(th);
+    return t > kept ? kept : t;
+}
+
+// The first bin whose inclusive prefix reaches x (the prefix reaches x at the
+// last bin).
+template <typename T>
+__device__ __forceinline__ int first_at_least(const T* prefix, unsigned long long x) {
+    int lo = 0, hi = kBins - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (static_cast<unsigned long long>(prefix[mid]) >= x) hi = mid;
+        else lo = mid + 1;
+    }
+    return lo;
+}
+
+// s = (zmax - z)/T falls in a bin <= b (monotone in z: false below some
+// value, true from there up).
+struct BinAtMost {
+    float zmax, inv_t;
+    int b;
+    __device__ __forceinline__ bool operator()(float z) const {
+        const float sc = (zmax - z) * inv_t;
+        return sc < 32.0f && min(kBins - 1, static_cast<int>(sc * 8.0f)) <= b;
+    }
+};
+
+// One pass over the slice for the histogram of s = (zmax - z)/T in bins of
+// 1/8 below s = 32: kMode 0 sums the fixed-point weights alone (returned),
+// 1 counts into this warp's bins, 2 counts and adds the weights.  One
+// instantiation per mode keeps the weight off the count-only path.
+template <int kMode>
+__device__ __forceinline__ unsigned long long hist_pass(const Slice& sl, float zmax, float inv_t, uint32_t* whc,
+                                                        unsigned long long* whp) {
+    unsigned long long tmass = 0;
+    const int vp = sl.vper(), nv = sl.nvec();
+    for (int j0 = threadIdx.x; j0 < nv; j0 += kThreads * kBatch) {
+        uint4 vb[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            const int j = j0 + u * kThreads;
+            vb[u] = j < nv ? sl.vec(j) : make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u);
+        }
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            const uint4 v = vb[u];
+            if (j0 + u * kThreads >= nv) break;
+            if ((zmax - vec_max(v, sl.bf16)) * inv_t >= 32.0f) continue;  // the whole vector is out of range
+#pragma unroll
+            for (int l = 0; l < 8; ++l) {
+                if (l >= vp) break;
+                const float z = vec_elem(v, l, sl.bf16);
+                const float sc = (zmax - z) * inv_t;
+                if (sc < 32.0f) {
+                    if (kMode == 0) {
+                        tmass += to_fixed(weight_f(z, zmax, inv_t));
+                    } else {
+                        const int bin = min(kBins - 1, static_cast<int>(sc * 8.0f));
+                        if (kMode == 2) atomicAdd(&whp[bin], to_fixed(weight_f(z, zmax, inv_t)));
+                        atomicAdd(&whc[bin], 1u);
+                    }
+                }
+            }
+        }
+    }
+    return tmass;
+}
+
+// The policy of the row held by the cluster.  One pass builds a histogram of
+// s = (zmax - z)/T in bins of 1/8 below s = 32 (beyond, the weight is 0 in
+// fixed point): exact counts and exact fixed-point masses per bin, each warp
+// into a private copy, summed per CTA and over the cluster.  Its prefix sums
+// give the bin where the cumulative count reaches k (top-k), bounds on the
+// kept mass, and from them the first bin where the cumulative mass can reach
+// p of it (top-p): both cuts lie in the window of bins between.  The window's
+// elements are compacted into rank 0's buffer, sorted by (logit descending,
+// index ascending) and cut there by exact prefix sums continued from the
+// exact mass above the window.  A support of at most kThreads tokens is
+// compacted whole, so that rank 0 holds it for the draw.  A window too large
+// for the buffer (a flat row: thousands of tokens in one bin, bf16 ties) is
+// resolved for top-p alone by radix selection inside the window's key range;
+// other such rows fall back to row_policy_radix.  cbuf = this CTA's
+// candidate buffer (kCap composite keys; only rank 0's receives candidates)
+// followed by kWarps x kBins 32-bit counts.
 __device__ void row_policy(Smem& sm, cg::cluster_group& cl, const Slice& sl, int V, const Policy& pol,
                            RowResult& res, unsigned long long* cbuf) {
     const float zmax = res.zmax;
@@ -918,75 +1000,45 @@ __device__ void row_policy(Smem& sm, cg::cluster_group& cl, const Slice& sl, int
     const float inv_t = pol.inv_t;
     const bool use_k = pol.top_k > 0;
     const bool use_p = pol.top_p < 1.0f;
-    const bool with_mass = !use_k;  // the kept set is the whole row: its mass, and the top-p crossing
+    const bool trunc = use_k || use_p;
+    // Exact masses narrow the window; a top-k set of at most kThreads tokens
+    // is compacted whole, so its rows count alone.
+    const bool with_mass = !use_k || pol.top_k > kThreads;
 
-    // ---- histogram (buffer 1 of the radix histograms, zeroed at kernel start).
-    // Count-only rows add 1 to a 32-bit bin.  When top-k is off, one 64-bit
-    // atomic adds (1 << 40) + floor(w * 2^16) per element: the count in the
-    // high bits and a lower bound of the fixed-point mass (floor(w 2^16) 2^24
-    // <= round(w 2^40)) in the low 40 bits (at most 16160 * 2^16 < 2^40: no
-    // carry).  The exact total mass is summed in registers.
+    // ---- histogram (rows without truncation need the total mass alone)
+    const int warp_id = tid >> 5;
+    uint32_t* wcnt = reinterpret_cast<uint32_t*>(cbuf + kWarps * kBins);
+    unsigned long long* whp = cbuf + warp_id * kBins;
+    uint32_t* whc = wcnt + warp_id * kBins;
+    unsigned long long tmass = 0;
+    if (trunc) {
+        for (int i = tid; i < kWarps * kBins; i += kThreads) {
+            if (with_mass) cbuf[i] = 0ull;
+            wcnt[i] = 0u;
+        }
+        __syncthreads();
+    }
+    if (!trunc) tmass = hist_pass<0>(sl, zmax, inv_t, whc, whp);
+    else if (with_mass) hist_pass<2>(sl, zmax, inv_t, whc, whp);
+    else hist_pass<1>(sl, zmax, inv_t, whc, whp);
+    __syncthreads();
     uint32_t* hc = sm.hcnt[1];
     unsigned long long* hp = sm.hmass[1];
-    unsigned long long tmass = 0;
-    const bool hist = use_k || use_p;
-    // Each warp counts into a private copy (in the candidate buffer, unused
-    // until the compaction): no contention between warps on busy bins.
-    const int warp_id = tid >> 5;
-    uint32_t* whc = reinterpret_cast<uint32_t*>(cbuf) + warp_id * kBins;
-    unsigned long long* whp = cbuf + warp_id * kBins;
-    for (int i = tid; i < kWarps * kBins; i += kThreads) cbuf[i] = 0ull;  // kWarps * kBins == kCap
-    __syncthreads();
-    {
-        const int vp = sl.vper(), nv = sl.nvec();
-        for (int j0 = tid; j0 < nv; j0 += kThreads * kBatch) {
-          uint4 vb[kBatch];
-#pragma unroll
-          for (int u = 0; u < kBatch; ++u) {
-              const int j = j0 + u * kThreads;
-              vb[u] = j < nv ? sl.vec(j) : make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u);
-          }
-#pragma unroll
-          for (int u = 0; u < kBatch; ++u) {
-            const uint4 v = vb[u];
-            if (j0 + u * kThreads >= nv) break;
-            if ((zmax - vec_max(v, sl.bf16)) * inv_t >= 32.0f) continue;  // the whole vector is out of range
-#pragma unroll
-            for (int l = 0; l < 8; ++l) {
-                if (l >= vp) break;
-                const float z = vec_elem(v, l, sl.bf16);
-                const float sc = (zmax - z) * inv_t;
-                if (sc < 32.0f) {
-                    const int bin = min(kBins - 1, static_cast<int>(sc * 8.0f));
-                    if (with_mass) {
-                        const float w = weight_f(z, zmax, inv_t);
-                        tmass += to_fixed(w);
-                        if (hist) atomicAdd(&whp[bin], (1ull << 40) + __float2uint_rd(w * 65536.0f));
-                    } else {
-                        atomicAdd(&whc[bin], 1u);
-                    }
-                }
-            }
-          }
-        }
-    }
-    __syncthreads();
-    {  // the CTA's histogram: bin tid over the warps' copies
+    __shared__ unsigned long long s_ctot;  // this CTA's total mass (no truncation)
+    if (trunc) {  // the CTA's histogram: bin tid over the warps' copies
         unsigned long long t = 0;
-        if (with_mass) {
-            for (int w = 0; w < kWarps; ++w) t += cbuf[w * kBins + tid];
-            hp[tid] = t;
-        } else {
-            for (int w = 0; w < kWarps; ++w) t += reinterpret_cast<const uint32_t*>(cbuf)[w * kBins + tid];
-            hc[tid] = static_cast<uint32_t>(t);
+        uint32_t cn = 0;
+        for (int w = 0; w < kWarps; ++w) {
+            if (with_mass) t += cbuf[w * kBins + tid];
+            cn += wcnt[w * kBins + tid];
         }
-    }
-    __shared__ unsigned long long s_ctot;  // this CTA's exact mass (top-k off)
-    if (with_mass) {
-        const int lane = tid & 31, warp = tid >> 5;
+        hp[tid] = t;
+        hc[tid] = cn;
+    } else {
+        const int lane = tid & 31;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) tmass += __shfl_xor_sync(0xFFFFFFFFu, tmass, o);
-        if (lane == 0) sm.wu[warp][0] = tmass;
+        if (lane == 0) sm.wu[warp_id][0] = tmass;
         __syncthreads();
         if (tid == 0) {
             unsigned long long t = 0;
@@ -995,111 +1047,133 @@ __device__ void row_policy(Smem& sm, cg::cluster_group& cl, const Slice& sl, int
         }
     }
     cl.sync();
-    unsigned long long c = 0, m = 0, total_mass = 0;  // bin tid of the cluster's histogram
-    if (with_mass) {
+    if (!trunc) {  // the whole vocabulary
+        unsigned long long total = 0;
 #pragma unroll
-        for (int r = 0; r < kC; ++r) {
-            const unsigned long long pk = cl.map_shared_rank(hp, r)[tid];
-            c += pk >> 40;
-            m += pk & ((1ull << 40) - 1ull);
-            total_mass += *cl.map_shared_rank(&s_ctot, r);
-        }
-        m <<= 24;  // lower bound of the bin's fixed-point mass
-    } else {
-#pragma unroll
-        for (int r = 0; r < kC; ++r) c += cl.map_shared_rank(hc, r)[tid];
-    }
-    const unsigned long long cc = block_scan_u64(sm, c);
-    const unsigned long long cm = with_mass ? block_scan_u64(sm, m) : 0ull;
-    __shared__ unsigned long long s_count;
-    __shared__ int s_bin;
-    if (tid == 0) s_bin = -1;
-    __syncthreads();
-    if (!use_k && !use_p) {  // no truncation: the whole vocabulary
+        for (int r = 0; r < kC; ++r) total += *cl.map_shared_rank(&s_ctot, r);
         res.tau = 0u;
         res.cut = -1;
-        res.mass = total_mass;
+        res.mass = total;
         res.count = V;
         return;
     }
-    unsigned long long theta = 0;
-    if (!use_k) {
-        const double th = ceil(static_cast<double>(pol.top_p) * static_cast<double>(total_mass));
-        theta = th < 1.0 ? 1ull : static_cast<unsigned long long>(th);
-        if (theta > total_mass) theta = total_mass;
+    unsigned long long c = 0, m = 0;  // bin tid of the cluster's histogram
+#pragma unroll
+    for (int r = 0; r < kC; ++r) {
+        c += cl.map_shared_rank(hc, r)[tid];
+        if (with_mass) m += cl.map_shared_rank(hp, r)[tid];
     }
-    // Top-p alone: the first bin whose cumulative lower-bound mass reaches
-    // theta; the exact cumulative mass there is at least as large, so the
-    // support lies at or below it.
-    const unsigned long long need = use_k ? static_cast<unsigned long long>(pol.top_k) : theta;
-    const unsigned long long incl = use_k ? cc : cm, here = use_k ? c : m;
-    if (incl >= need && incl - here < need) {  // the crossing bin (unique)
-        s_bin = tid;
-        s_count = cc;
+    __shared__ uint32_t s_cc[kBins];            // inclusive prefix counts
+    __shared__ unsigned long long s_cm[kBins];  // inclusive prefix masses
+    const unsigned long long cc = block_scan_u64(sm, c);
+    const unsigned long long cm = with_mass ? block_scan_u64(sm, m) : 0ull;
+    s_cc[tid] = static_cast<uint32_t>(cc);
+    s_cm[tid] = cm;
+    __syncthreads();
+    const unsigned long long n_in = s_cc[kBins - 1], total_mass = s_cm[kBins - 1];
+    // top-k past s = 32 takes every token in range: the others weigh 0
+    const unsigned long long k_eff = use_k ? min(static_cast<unsigned long long>(pol.top_k), n_in) : 0ull;
+
+    // ---- the window of bins [wlo, whi] holding the cuts
+    __shared__ int s_win[2];
+    __shared__ unsigned long long s_pl[4];  // above count, above mass, window count, theta (top-p alone)
+    if (tid == 0) {
+        int whi = use_k ? first_at_least(s_cc, k_eff) : kBins - 1;
+        int wlo = 0;
+        unsigned long long theta = 0;
+        if (with_mass) {
+            // lower bound of the kept mass (exact when top-k is off)
+            const unsigned long long mk_lo = use_k ? (whi ? s_cm[whi - 1] : 0ull) : total_mass;
+            wlo = whi;
+            if (use_p) {
+                theta = p_threshold(pol.top_p, mk_lo);
+                wlo = first_at_least(s_cm, theta);
+                if (!use_k) whi = wlo;
+            }
+            if (s_cc[whi] <= static_cast<uint32_t>(kThreads)) wlo = 0;  // small support: all of it
+        }
+        const unsigned long long ac = wlo ? s_cc[wlo - 1] : 0ull;
+        s_win[0] = wlo;
+        s_win[1] = whi;
+        s_pl[0] = ac;
+        s_pl[1] = wlo ? s_cm[wlo - 1] : 0ull;
+        s_pl[2] = s_cc[whi] - ac;
+        s_pl[3] = theta;
     }
     __syncthreads();
-    // No crossing: top-k reaches past s = 32 or the lower bounds of top-p's
-    // mass fall short.  Tokens past s = 32 have weight 0 in fixed point: they
-    // are never drawn and carry no mass, so every token of the support that
-    // matters is in range - take them all as candidates.
-    if (s_bin < 0 && tid == kThreads - 1) {
-        s_bin = kBins - 1;
-        s_count = cc;
-    }
+    const int wlo = s_win[0], whi = s_win[1];
+    const unsigned long long above_cnt = s_pl[0], above_mass = s_pl[1], wcount = s_pl[2], theta_p = s_pl[3];
     __syncthreads();
-    const int bstar = s_bin;
-    const unsigned long long count = bstar >= 0 ? s_count : 0ull;
-    __syncthreads();
-    if (bstar < 0 || count > static_cast<unsigned long long>(kCap)) {  // flat row: radix selection
-        row_policy_radix(sm, cl, sl, V, pol, res);
+    // keys of the window: [klo, kab - 1] (kab: the lowest key above it)
+    const uint32_t klo = lowest_true_key(kmax, BinAtMost{zmax, inv_t, whi});
+    const uint32_t kab = wlo > 0 ? lowest_true_key(kmax, BinAtMost{zmax, inv_t, wlo - 1}) : 0u;
+
+    if (wcount > static_cast<unsigned long long>(kCap)) {
+        if (!use_k) {  // top-p alone: radix selection inside the window
+            const uint32_t khi = wlo > 0 ? kab - 1u : kmax;
+            auto all = [](uint32_t, int32_t) { return true; };
+            uint32_t tau;
+            unsigned long long above, eqc, eqm;
+            if (radix_select<true>(sm, cl, sl, cbuf, klo, khi, above_mass, theta_p, zmax, inv_t, all, tau, above,
+                                   eqc, eqm) &&
+                eqc > 0) {
+                // tied elements share one weight; take just enough of them in index order
+                const unsigned long long wt = eqm / eqc;
+                unsigned long long t = wt ? (theta_p - above + wt - 1) / wt : eqc;
+                if (t < 1) t = 1;
+                if (t > eqc) t = eqc;
+                res.cut = tie_index(sm, cl, sl, tau, t, all);
+                res.tau = tau;
+                res.mass = above + t * wt;
+                res.count = 0x7FFFFFFF;
+                return;
+            }
+        }
+        row_policy_radix(sm, cl, sl, V, pol, res, cbuf);
         res.count = 0x7FFFFFFF;
         return;
     }
 
-    // ---- compact the candidates (bins <= bstar) into rank 0's buffer
-    // the candidate test is monotone in z: one threshold value, found by bisection
-    const float zb = key_to_float(lowest_true_key(kmax, [&](float z) {
-        const float sc = (zmax - z) * inv_t;
-        return sc < 32.0f && min(kBins - 1, static_cast<int>(sc * 8.0f)) <= bstar;
-    }));
-    compact_candidates(sm, cl, sl, cbuf, zb, [zb](float z, int32_t) { return z >= zb; });
+    // ---- compact the window's elements into rank 0's buffer
+    {
+        const float zlo = key_to_float(klo);
+        const float zab = wlo > 0 ? key_to_float(kab) : __int_as_float(0x7F800000);
+        compact_candidates(sm, cl, sl, cbuf, zlo, [zlo, zab](float z, int32_t) { return z >= zlo && z < zab; });
+    }
 
-    // ---- rank 0: sort, take the cuts
+    // ---- rank 0: sort, take the cuts (prefix sums continue from the mass above the window)
     const int buf = sm.parity;
     if (rank == 0) {
-        const int n = static_cast<int>(min(static_cast<unsigned long long>(sm.ccount), count));
+        const int n = static_cast<int>(min(static_cast<unsigned long long>(sm.ccount), wcount));
         sort_candidates(cbuf, n);
-        const int K = use_k ? min(pol.top_k, n) : n;
+        const int K = use_k ? static_cast<int>(min(k_eff - above_cnt, static_cast<unsigned long long>(n))) : n;
         auto wt = [&](int i) -> unsigned long long {
             return i < K ? to_fixed(weight_f(key_to_float(vo_key(cbuf[i])), zmax, inv_t)) : 0ull;
         };
-        unsigned long long kept = 0;
-        int mm = K;
+        unsigned long long kept = total_mass;
         if (use_k) {
-            find_crossing(sm, K, 0ull, true, wt, kept);  // the kept mass
-        } else {
-            kept = total_mass;
+            unsigned long long part;
+            find_crossing(sm, K, 0ull, true, wt, part);
+            kept = above_mass + part;
         }
+        int mm = K;
         unsigned long long mass = kept;
         if (use_p) {
-            if (use_k) {
-                const double th = ceil(static_cast<double>(pol.top_p) * static_cast<double>(kept));
-                theta = th < 1.0 ? 1ull : static_cast<unsigned long long>(th);
-                if (theta > kept) theta = kept;
-            }
+            const unsigned long long theta = p_threshold(pol.top_p, kept);
             unsigned long long tot;
-            const int pos = find_crossing(sm, K, theta, false, wt, tot);
+            const int pos = find_crossing(sm, K, theta - above_mass, false, wt, tot);
             mm = min(pos + 1, K);
             unsigned long long pm;
             find_crossing(sm, mm, 0ull, true, wt, pm);  // mass of the first mm
-            mass = pm;
+            mass = above_mass + pm;
         }
+        mm = max(mm, 1);
         if (tid == 0) {
             const unsigned long long last = cbuf[mm - 1];
             sm.xu[buf][0] = vo_key(last);
             sm.xu[buf][1] = static_cast<unsigned long long>(static_cast<uint32_t>(vo_idx(last)));
             sm.xu[buf][2] = mass;
-            sm.xu[buf][3] = static_cast<unsigned long long>(mm);
+            sm.xu[buf][3] = above_cnt + static_cast<unsigned long long>(mm);
         }
     }
     cl.sync();
@@ -1108,8 +1182,8 @@ __device__ void row_policy(Smem& sm, cg::cluster_group& cl, const Slice& sl, int
     res.tau = static_cast<uint32_t>(sm.tot[0]);
     res.cut = static_cast<int32_t>(static_cast<uint32_t>(sm.tot[1]));
     res.mass = sm.tot[2];
-    res.count = static_cast<int32_t>(sm.tot[3]);
-    res.in_buf = 1;
+    res.count = static_cast<int32_t>(min(sm.tot[3], 0x7FFFFFFFull));
+    res.in_buf = above_cnt == 0;
     __syncthreads();
     if (tid == 0) sm.parity ^= 1;
     __syncthreads();
