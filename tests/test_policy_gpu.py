@@ -200,6 +200,17 @@ def test_draft_sampled_policies(ds, oracle, maker, kw):
     _check_draft(ref, got, w.V)
 
 
+def test_draft_sampled_mixed_full_vocab(ds, oracle):
+    """Mixed policies at V = 129,280: rows with top-k 1,000 and top-p cut
+    inside the top-k set leave a gap of whole bins between the two cuts."""
+    w = synth.mixed_serving(V=129_280, B=32, r=0, H=0, device="cuda")
+    ref = _draft_oracle(oracle, w)
+    got = ds.markov_sample(w.backbone, w.anchor, policy=w.policy.packed(), **_keys_dev(w.keys))
+    torch.cuda.synchronize()
+    n = _check_draft(ref, got, w.V, max_indet_frac=0.35)
+    print(f"indeterminate positions: {n} of {w.B * w.gamma}")
+
+
 @pytest.mark.parametrize("dtype", [synth.BF16, synth.F32])
 def test_draft_sampled_flat_rows(ds, oracle, dtype):
     """Drafting on flat rows, bf16 and fp32 (fp32 rows take the same row

@@ -917,6 +917,16 @@ __device__ __forceinline__ int first_at_least(const T* prefix, unsigned long lon
     return lo;
 }
 
+// The bin of s = (zmax - z)/T in steps of 1/8 below s = 32 (kBins beyond):
+// non-increasing in z.
+struct BinOf {
+    float zmax, inv_t;
+    __device__ __forceinline__ int operator()(float z) const {
+        const float sc = (zmax - z) * inv_t;
+        return sc < 32.0f ? min(kBins - 1, static_cast<int>(sc * 8.0f)) : kBins;
+    }
+};
+
 // s = (zmax - z)/T falls in a bin <= b (monotone in z: false below some
 // value, true from there up).
 struct BinAtMost {
@@ -1074,13 +1084,18 @@ __device__ void row_policy(Smem& sm, cg::cluster_group& cl, const Slice& sl, int
     // top-k past s = 32 takes every token in range: the others weigh 0
     const unsigned long long k_eff = use_k ? min(static_cast<unsigned long long>(pol.top_k), n_in) : 0ull;
 
-    // ---- the window of bins [wlo, whi] holding the cuts
-    __shared__ int s_win[2];
-    __shared__ unsigned long long s_pl[4];  // above count, above mass, window count, theta (top-p alone)
+    // ---- the window of bins [wlo, whi] holding the cuts.  With top-k and
+    // top-p together the window runs from the top-p crossing down to the top-k
+    // bin; only its first bins (those where the top-p crossing can lie, up to
+    // phi) and the top-k bin need their tokens: the bins between (the gap)
+    // enter the cuts as their exact count and mass.
+    __shared__ int s_win[3];
+    __shared__ unsigned long long s_pl[6];  // above count / mass, window count, theta (top-p alone), gap count / mass
     if (tid == 0) {
         int whi = use_k ? first_at_least(s_cc, k_eff) : kBins - 1;
         int wlo = 0;
         unsigned long long theta = 0;
+        const bool small = s_cc[whi] <= static_cast<uint32_t>(kThreads);
         if (with_mass) {
             // lower bound of the kept mass (exact when top-k is off)
             const unsigned long long mk_lo = use_k ? (whi ? s_cm[whi - 1] : 0ull) : total_mass;
@@ -1090,27 +1105,37 @@ __device__ void row_policy(Smem& sm, cg::cluster_group& cl, const Slice& sl, int
                 wlo = first_at_least(s_cm, theta);
                 if (!use_k) whi = wlo;
             }
-            if (s_cc[whi] <= static_cast<uint32_t>(kThreads)) wlo = 0;  // small support: all of it
+            if (small || s_cc[whi] <= static_cast<uint32_t>(kThreads)) wlo = 0;  // small support: all of it
+        }
+        int phi = whi;
+        if (with_mass && use_k && use_p && !small) {
+            // the kept mass is at most the mass through the top-k bin
+            const int p_hi = first_at_least(s_cm, p_threshold(pol.top_p, s_cm[whi]));
+            if (p_hi + 1 < whi) phi = p_hi;
         }
         const unsigned long long ac = wlo ? s_cc[wlo - 1] : 0ull;
+        const unsigned long long gc = phi < whi ? s_cc[whi - 1] - s_cc[phi] : 0ull;
         s_win[0] = wlo;
         s_win[1] = whi;
+        s_win[2] = phi;
         s_pl[0] = ac;
         s_pl[1] = wlo ? s_cm[wlo - 1] : 0ull;
-        s_pl[2] = s_cc[whi] - ac;
+        s_pl[2] = s_cc[whi] - ac - gc;
         s_pl[3] = theta;
+        s_pl[4] = gc;
+        s_pl[5] = phi < whi ? s_cm[whi - 1] - s_cm[phi] : 0ull;
     }
     __syncthreads();
-    const int wlo = s_win[0], whi = s_win[1];
+    const int wlo = s_win[0], whi = s_win[1], phi = s_win[2];
     const unsigned long long above_cnt = s_pl[0], above_mass = s_pl[1], wcount = s_pl[2], theta_p = s_pl[3];
+    const unsigned long long gap_cnt = s_pl[4], gap_mass = s_pl[5];
     __syncthreads();
-    // keys of the window: [klo, kab - 1] (kab: the lowest key above it)
+    // the lowest key of the window
     const uint32_t klo = lowest_true_key(kmax, BinAtMost{zmax, inv_t, whi});
-    const uint32_t kab = wlo > 0 ? lowest_true_key(kmax, BinAtMost{zmax, inv_t, wlo - 1}) : 0u;
 
     if (wcount > static_cast<unsigned long long>(kCap)) {
         if (!use_k) {  // top-p alone: radix selection inside the window
-            const uint32_t khi = wlo > 0 ? kab - 1u : kmax;
+            const uint32_t khi = wlo > 0 ? lowest_true_key(kmax, BinAtMost{zmax, inv_t, wlo - 1}) - 1u : kmax;
             auto all = [](uint32_t, int32_t) { return true; };
             uint32_t tau;
             unsigned long long above, eqc, eqm;
@@ -1134,11 +1159,13 @@ __device__ void row_policy(Smem& sm, cg::cluster_group& cl, const Slice& sl, int
         return;
     }
 
-    // ---- compact the window's elements into rank 0's buffer
+    // ---- compact the window's elements (but the gap's) into rank 0's buffer
     {
-        const float zlo = key_to_float(klo);
-        const float zab = wlo > 0 ? key_to_float(kab) : __int_as_float(0x7F800000);
-        compact_candidates(sm, cl, sl, cbuf, zlo, [zlo, zab](float z, int32_t) { return z >= zlo && z < zab; });
+        const BinOf bin_of{zmax, inv_t};
+        compact_candidates(sm, cl, sl, cbuf, key_to_float(klo), [=](float z, int32_t) {
+            const int b = bin_of(z);
+            return b >= wlo && b <= whi && (b <= phi || b == whi);
+        });
     }
 
     // ---- rank 0: sort, take the cuts (prefix sums continue from the mass above the window)
@@ -1146,7 +1173,9 @@ __device__ void row_policy(Smem& sm, cg::cluster_group& cl, const Slice& sl, int
     if (rank == 0) {
         const int n = static_cast<int>(min(static_cast<unsigned long long>(sm.ccount), wcount));
         sort_candidates(cbuf, n);
-        const int K = use_k ? static_cast<int>(min(k_eff - above_cnt, static_cast<unsigned long long>(n))) : n;
+        // buffer positions inside the top-k set (the gap's tokens are all in it)
+        const int K = use_k ? static_cast<int>(min(k_eff - above_cnt - gap_cnt, static_cast<unsigned long long>(n)))
+                            : n;
         auto wt = [&](int i) -> unsigned long long {
             return i < K ? to_fixed(weight_f(key_to_float(vo_key(cbuf[i])), zmax, inv_t)) : 0ull;
         };
@@ -1154,7 +1183,7 @@ __device__ void row_policy(Smem& sm, cg::cluster_group& cl, const Slice& sl, int
         if (use_k) {
             unsigned long long part;
             find_crossing(sm, K, 0ull, true, wt, part);
-            kept = above_mass + part;
+            kept = above_mass + gap_mass + part;
         }
         int mm = K;
         unsigned long long mass = kept;
