@@ -139,7 +139,7 @@ int dspark_verify(const void* target, int dtype, const int32_t* proposals, const
         vp.B = B;
         vp.gamma = gamma;
         vp.V = V;
-        vp.slice = policy_slice(V);
+        vp.slice = verify_slice(V);
         vp.out_tokens = out_tokens;
         vp.num_accepted = num_accepted;
         vp.status = status;
@@ -220,7 +220,7 @@ int dspark_markov_sample(const void* backbone, int dtype, const int32_t* anchor,
         mp.B = B;
         mp.gamma = gamma;
         mp.V = V;
-        mp.slice = policy_slice(V);
+        mp.slice = step_slice(V);
         mp.error_flag = r > 0 ? error_flag : nullptr;
         for (int k = 1; k <= gamma; ++k) {
             if (r > 0) {

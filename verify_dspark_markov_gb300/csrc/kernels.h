@@ -126,8 +126,9 @@ struct MarkovGemmPlan {
 // outside what the kernel supports.
 bool prepare_markov_bias(MarkovGemmParams& p, MarkovGemmPlan& plan);
 cudaError_t launch_markov_bias(const MarkovGemmParams& p, const MarkovGemmPlan& plan, cudaStream_t stream);
-int policy_cluster_size();
-int policy_slice(int V);
+// Elements of a row each CTA of the verify / drafting step owns.
+int verify_slice(int V);
+int step_slice(int V);
 int policy_smem_bytes(int V, int store_bf16);
 cudaError_t launch_verify_prob(const VerifyProbParams& p, cudaStream_t stream);
 cudaError_t launch_markov_step(const MarkovStepParams& p, cudaStream_t stream);

@@ -1,5 +1,7 @@
-// Sampled paths built on the row engine (row_policy.cuh): one cluster of
-// rp::kC CTAs per vocabulary row, reading the row in place.
+// Sampled paths built on the row engine (row_policy.cuh): one cluster of CTAs
+// per vocabulary row, reading the row in place - 4 per target row in the
+// verify (384 rows and more fill the GPU), 8 per row in the drafting step,
+// whose batch of rows is smaller.
 //
 //  * verify_rows_kernel - exact verify of a block under per-request policies
 //    [FT Exact decoding semantics > Probabilistic]: each cluster forms the
@@ -23,8 +25,10 @@ namespace dspark {
 namespace {
 
 namespace cg = cooperative_groups;
-using rp::kC;
 using rp::kThreads;
+constexpr int kVerifyC = 4;  // CTAs per target row in the verify
+constexpr int kStepC = 8;    // CTAs per row in the drafting step
+static_assert(kVerifyC <= rp::kMaxC && kStepC <= rp::kMaxC, "cluster sizes the row engine holds");
 
 __device__ __forceinline__ float inv_mass(uint64_t mass) {
     return static_cast<float>(rp::kFix / static_cast<double>(mass));
@@ -35,7 +39,7 @@ __device__ __forceinline__ float inv_mass(uint64_t mass) {
 // global memory.
 
 template <int kDtype>
-__global__ void __cluster_dims__(rp::kC, 1, 1) __launch_bounds__(rp::kThreads, 4)
+__global__ void __cluster_dims__(kVerifyC, 1, 1) __launch_bounds__(rp::kThreads, 4)
     verify_rows_kernel(const VerifyProbParams p) {
     extern __shared__ __align__(16) unsigned char dyn[];
     __shared__ rp::Smem sm;
@@ -58,7 +62,7 @@ __global__ void __cluster_dims__(rp::kC, 1, 1) __launch_bounds__(rp::kThreads, 4
     __syncthreads();
 
     const int rows = p.gamma + 1;
-    const int64_t row = blockIdx.x / kC;
+    const int64_t row = blockIdx.x / kVerifyC;
     const int b = static_cast<int>(row / rows), i = static_cast<int>(row % rows);
     const int lo = rank * p.slice;
     const int n = max(0, min(p.slice, p.V - lo));
@@ -223,7 +227,7 @@ __global__ void __cluster_dims__(rp::kC, 1, 1) __launch_bounds__(rp::kThreads, 4
 }
 
 template <int kDtype>
-__global__ void __cluster_dims__(rp::kC, 1, 1) __launch_bounds__(rp::kThreads, 4)
+__global__ void __cluster_dims__(kStepC, 1, 1) __launch_bounds__(rp::kThreads, 4)
     markov_step_kernel(const MarkovStepParams p) {
     extern __shared__ __align__(16) unsigned char dyn[];
     __shared__ rp::Smem sm;
@@ -239,7 +243,7 @@ __global__ void __cluster_dims__(rp::kC, 1, 1) __launch_bounds__(rp::kThreads, 4
     }
     __syncthreads();
 
-    const int b = blockIdx.x / kC;
+    const int b = blockIdx.x / kStepC;
     const int k = p.k;  // 1-based position
     const int64_t pidx = static_cast<int64_t>(b) * p.gamma + (k - 1);
     const int32_t x_prev = k == 1 ? p.anchor[b] : p.proposals[pidx - 1];
@@ -374,7 +378,7 @@ __global__ void __cluster_dims__(rp::kC, 1, 1) __launch_bounds__(rp::kThreads, 4
         // the owner of x for a draw over every slice
         int src = 0;
         if (!pol.greedy && !(res.in_buf && res.count <= rp::kThreads)) {
-            for (int r = 0; r < kC; ++r)
+            for (int r = 0; r < kStepC; ++r)
                 if (*cl.map_shared_rank(&s_x, r) >= 0) { src = r; break; }
         }
         const int32_t xk = *cl.map_shared_rank(&s_x, src);
@@ -392,9 +396,9 @@ cudaError_t set_smem(K kernel, int bytes) {
 
 }  // namespace
 
-int policy_cluster_size() { return kC; }
+int verify_slice(int V) { return ((V + kVerifyC - 1) / kVerifyC + 7) / 8 * 8; }
 
-int policy_slice(int V) { return ((V + kC - 1) / kC + 7) / 8 * 8; }
+int step_slice(int V) { return ((V + kStepC - 1) / kStepC + 7) / 8 * 8; }
 
 int policy_smem_bytes(int V, int store_bf16) {
     (void)V;
@@ -405,7 +409,7 @@ int policy_smem_bytes(int V, int store_bf16) {
 
 cudaError_t launch_verify_prob(const VerifyProbParams& p, cudaStream_t stream) {
     const int smem = policy_smem_bytes(p.V, p.dtype == kBF16);
-    const dim3 grid(static_cast<unsigned>(static_cast<int64_t>(p.B) * (p.gamma + 1) * kC));
+    const dim3 grid(static_cast<unsigned>(static_cast<int64_t>(p.B) * (p.gamma + 1) * kVerifyC));
     cudaError_t e;
     if (p.dtype == kBF16) {
         if ((e = set_smem(verify_rows_kernel<kBF16>, smem)) != cudaSuccess) return e;
@@ -419,7 +423,7 @@ cudaError_t launch_verify_prob(const VerifyProbParams& p, cudaStream_t stream) {
 
 cudaError_t launch_markov_step(const MarkovStepParams& p, cudaStream_t stream) {
     const int smem = policy_smem_bytes(p.V, !p.zbuf && p.dtype == kBF16);
-    const dim3 grid(static_cast<unsigned>(p.B * kC));
+    const dim3 grid(static_cast<unsigned>(p.B * kStepC));
     cudaError_t e;
     if (p.dtype == kBF16) {
         if ((e = set_smem(markov_step_kernel<kBF16>, smem)) != cudaSuccess) return e;

@@ -1,6 +1,7 @@
 // Row engine: the sampling policy of one vocabulary row, computed by a
-// cluster of kC CTAs that each own a contiguous slice of the row, plus the
-// exact inverse-CDF draw over the policy's weights.  The slices stay in
+// cluster of CTAs (up to kMaxC; the kernel fixes the size) that each own a
+// contiguous slice of the row, plus the exact inverse-CDF draw over the
+// policy's weights.  The slices stay in
 // global memory: the first pass over a row streams it from HBM (or from L2
 // when the row was just written, like the Markov logits), later passes find
 // it in L2.  With no row held in shared memory a CTA needs ~37 KB.
@@ -35,7 +36,7 @@ namespace rp {
 
 namespace cg = cooperative_groups;
 
-constexpr int kC = 4;           // CTAs per row
+constexpr int kMaxC = 8;        // CTAs per row, at most (the cluster's size, read at run time)
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kBins = 256;      // 8-bit radix digits
@@ -88,7 +89,7 @@ struct Smem {
     uint32_t hcnt[2][kBins];
     unsigned long long hmass[2][kBins];
     unsigned long long wu[kWarps][kWin + 2];  // per-warp partials
-    unsigned long long gat[kC][kWin + 2];     // slots gathered from the cluster's ranks
+    unsigned long long gat[kMaxC][kWin + 2];  // slots gathered from the cluster's ranks
     unsigned long long tot[kWin + 2];         // their combination, for every thread
     unsigned long long scan_u[kWarps];
     int32_t pick[4];
@@ -127,6 +128,7 @@ __device__ __forceinline__ float support_floor(uint32_t tau) {
 template <int kN>
 __device__ __forceinline__ void cluster_sum_u64(Smem& sm, cg::cluster_group& cl, unsigned long long (&v)[kN],
                                                 unsigned long long (&out)[kN]) {
+    const int nc = static_cast<int>(cl.num_blocks());  // CTAs in the cluster
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
     for (int i = 0; i < kN; ++i) {
@@ -144,14 +146,14 @@ __device__ __forceinline__ void cluster_sum_u64(Smem& sm, cg::cluster_group& cl,
     }
     cl.sync();
     // one remote load per (rank, value) pair, then one combination per value
-    if (threadIdx.x < kC * kN) {
+    if (threadIdx.x < nc * kN) {
         const int r = threadIdx.x / kN, i = threadIdx.x % kN;
         sm.gat[r][i] = cl.map_shared_rank(&sm.xu[buf][0], r)[i];
     }
     __syncthreads();
     if (threadIdx.x < kN) {
         unsigned long long t = 0;
-        for (int r = 0; r < kC; ++r) t += sm.gat[r][threadIdx.x];
+        for (int r = 0; r < nc; ++r) t += sm.gat[r][threadIdx.x];
         sm.tot[threadIdx.x] = t;
     }
     __syncthreads();
@@ -166,6 +168,7 @@ __device__ __forceinline__ void cluster_sum_u64(Smem& sm, cg::cluster_group& cl,
 __device__ __forceinline__ void cluster_max_u64(Smem& sm, cg::cluster_group& cl, unsigned long long v,
                                                 unsigned long long flags, unsigned long long& out_max,
                                                 unsigned long long& out_flags) {
+    const int nc = static_cast<int>(cl.num_blocks());  // CTAs in the cluster
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -189,14 +192,14 @@ __device__ __forceinline__ void cluster_max_u64(Smem& sm, cg::cluster_group& cl,
         sm.xu[buf][1] = f;
     }
     cl.sync();
-    if (threadIdx.x < 2 * kC) {
+    if (threadIdx.x < 2 * nc) {
         const int r = threadIdx.x >> 1, i = threadIdx.x & 1;
         sm.gat[r][i] = cl.map_shared_rank(&sm.xu[buf][0], r)[i];
     }
     __syncthreads();
     if (threadIdx.x == 0) {
         unsigned long long m = 0, f = 0;
-        for (int r = 0; r < kC; ++r) {
+        for (int r = 0; r < nc; ++r) {
             m = sm.gat[r][0] > m ? sm.gat[r][0] : m;
             f |= sm.gat[r][1];
         }
@@ -211,18 +214,15 @@ __device__ __forceinline__ void cluster_max_u64(Smem& sm, cg::cluster_group& cl,
     __syncthreads();
 }
 
-// Exclusive prefix over the CTAs of the cluster of one uint64 per CTA (value
-// given by thread 0); returns (prefix of this CTA's rank for every rank via
-// totals[]).  totals[r] = value of rank r.
-__device__ __forceinline__ void cluster_gather_u64(Smem& sm, cg::cluster_group& cl, unsigned long long mine,
-                                                   unsigned long long (&totals)[kC]) {
+// Gather one uint64 per CTA (thread 0's `mine`) from every CTA of the
+// cluster: afterwards sm.gat[r][0] holds rank r's value, for every thread,
+// until the next exchange.
+__device__ __forceinline__ void cluster_gather_u64(Smem& sm, cg::cluster_group& cl, unsigned long long mine) {
+    const int nc = static_cast<int>(cl.num_blocks());  // CTAs in the cluster
     const int buf = sm.parity;
     if (threadIdx.x == 0) sm.xu[buf][0] = mine;
     cl.sync();
-    if (threadIdx.x < kC) sm.gat[threadIdx.x][0] = cl.map_shared_rank(&sm.xu[buf][0], threadIdx.x)[0];
-    __syncthreads();
-#pragma unroll
-    for (int r = 0; r < kC; ++r) totals[r] = sm.gat[r][0];
+    if (threadIdx.x < nc) sm.gat[threadIdx.x][0] = cl.map_shared_rank(&sm.xu[buf][0], threadIdx.x)[0];
     __syncthreads();
     if (threadIdx.x == 0) sm.parity ^= 1;
     __syncthreads();
@@ -365,6 +365,7 @@ __device__ bool radix_select(Smem& sm, cg::cluster_group& cl, const Slice& sl, u
                              uint32_t klo, uint32_t khi, unsigned long long above0, unsigned long long target,
                              float zmax, float inv_t, Pred pred, uint32_t& tau, unsigned long long& above,
                              unsigned long long& eq_cnt, unsigned long long& eq_mass) {
+    const int nc = static_cast<int>(cl.num_blocks());  // CTAs in the cluster
     const int tid = threadIdx.x;
     const int min_bit = sl.bf16 ? 16 : 0;
     int hi_bit = klo == khi ? 0 : 32 - __clz(static_cast<int>(klo ^ khi));  // bits still open
@@ -435,7 +436,7 @@ __device__ bool radix_select(Smem& sm, cg::cluster_group& cl, const Slice& sl, u
         const int b = nbins - 1 - tid;
         unsigned long long c = 0, m = 0;
         if (b >= 0) {
-            for (int r = 0; r < kC; ++r) {
+            for (int r = 0; r < nc; ++r) {
                 c += cl.map_shared_rank(&sm.hcnt[buf][0], r)[b];
                 if (kMass) m += cl.map_shared_rank(&sm.hmass[buf][0], r)[b];
             }
@@ -471,6 +472,7 @@ __device__ bool radix_select(Smem& sm, cg::cluster_group& cl, const Slice& sl, u
 template <typename Pred>
 __device__ int32_t tie_index(Smem& sm, cg::cluster_group& cl, const Slice& sl, uint32_t tau,
                              unsigned long long t, Pred pred) {
+    const int nc = static_cast<int>(cl.num_blocks());  // CTAs in the cluster
     const int tid = threadIdx.x;
     const int rank = static_cast<int>(cl.block_rank());
     // ordered ownership: each thread a contiguous run of the slice's vectors
@@ -485,13 +487,13 @@ __device__ int32_t tie_index(Smem& sm, cg::cluster_group& cl, const Slice& sl, u
     __shared__ unsigned long long s_total;
     if (tid == kThreads - 1) s_total = incl;
     __syncthreads();
-    unsigned long long totals[kC];
-    cluster_gather_u64(sm, cl, s_total, totals);
+    cluster_gather_u64(sm, cl, s_total);
+    const auto totals = [&sm](int r) { return sm.gat[r][0]; };  // per rank
     unsigned long long before = 0;
-    int owner = kC - 1;
-    for (int r = 0; r < kC; ++r) {
-        if (before + totals[r] >= t) { owner = r; break; }
-        before += totals[r];
+    int owner = nc - 1;
+    for (int r = 0; r < nc; ++r) {
+        if (before + totals(r) >= t) { owner = r; break; }
+        before += totals(r);
     }
     const int buf = sm.parity;
     if (rank == owner && tid == 0) sm.xu[buf][0] = static_cast<unsigned long long>(sl.lo + max(sl.n - 1, 0));
@@ -620,6 +622,7 @@ __device__ void row_policy_radix(Smem& sm, cg::cluster_group& cl, const Slice& s
 template <typename Wz>
 __device__ int32_t sample_fixed(Smem& sm, cg::cluster_group& cl, const Slice& sl, uint32_t m24, Wz wz,
                                 unsigned long long& total_out) {
+    const int nc = static_cast<int>(cl.num_blocks());  // CTAs in the cluster
     const int tid = threadIdx.x;
     const int rank = static_cast<int>(cl.block_rank());
     const int vp = sl.vper(), nv = sl.nvec();
@@ -645,19 +648,19 @@ __device__ int32_t sample_fixed(Smem& sm, cg::cluster_group& cl, const Slice& sl
     __shared__ unsigned long long s_total;
     if (tid == kThreads - 1) s_total = incl;
     __syncthreads();
-    unsigned long long totals[kC];
-    cluster_gather_u64(sm, cl, s_total, totals);
+    cluster_gather_u64(sm, cl, s_total);
+    const auto totals = [&sm](int r) { return sm.gat[r][0]; };  // per rank
     unsigned long long total = 0;
-    for (int r = 0; r < kC; ++r) total += totals[r];
+    for (int r = 0; r < nc; ++r) total += totals(r);
     total_out = total;
     if (total == 0) return -1;
     const unsigned long long target =
         static_cast<unsigned long long>((static_cast<unsigned __int128>(m24) * total) >> 24);
     unsigned long long before = 0;
-    int owner = kC - 1;
-    for (int r = 0; r < kC; ++r) {
-        if (before + totals[r] > target) { owner = r; break; }
-        before += totals[r];
+    int owner = nc - 1;
+    for (int r = 0; r < nc; ++r) {
+        if (before + totals(r) > target) { owner = r; break; }
+        before += totals(r);
     }
     const int buf = sm.parity;
     if (rank == owner && tid == 0) sm.xu[buf][0] = static_cast<unsigned long long>(sl.lo + max(sl.n - 1, 0));
@@ -997,6 +1000,7 @@ __device__ __forceinline__ unsigned long long hist_pass(const Slice& sl, float z
 // followed by kWarps x kBins 32-bit counts.
 __device__ void row_policy(Smem& sm, cg::cluster_group& cl, const Slice& sl, int V, const Policy& pol,
                            RowResult& res, unsigned long long* cbuf) {
+    const int nc = static_cast<int>(cl.num_blocks());  // CTAs in the cluster
     const float zmax = res.zmax;
     const uint32_t kmax = ordered_key(zmax);
     const int tid = threadIdx.x;
@@ -1060,7 +1064,7 @@ __device__ void row_policy(Smem& sm, cg::cluster_group& cl, const Slice& sl, int
     if (!trunc) {  // the whole vocabulary
         unsigned long long total = 0;
 #pragma unroll
-        for (int r = 0; r < kC; ++r) total += *cl.map_shared_rank(&s_ctot, r);
+        for (int r = 0; r < nc; ++r) total += *cl.map_shared_rank(&s_ctot, r);
         res.tau = 0u;
         res.cut = -1;
         res.mass = total;
@@ -1069,7 +1073,7 @@ __device__ void row_policy(Smem& sm, cg::cluster_group& cl, const Slice& sl, int
     }
     unsigned long long c = 0, m = 0;  // bin tid of the cluster's histogram
 #pragma unroll
-    for (int r = 0; r < kC; ++r) {
+    for (int r = 0; r < nc; ++r) {
         c += cl.map_shared_rank(hc, r)[tid];
         if (with_mass) m += cl.map_shared_rank(hp, r)[tid];
     }
