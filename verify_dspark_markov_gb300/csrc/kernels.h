@@ -115,6 +115,7 @@ struct MarkovGemmParams {
     int nt;                    // vocabulary rows per tile (MMA N)
     int stages;                // W tiles in flight per CTA
     int rpq;                   // requests per 32-row TMEM lane quadrant of an M tile
+    int nbb;                   // backbone blocks in flight per epilogue warp (1 or 2)
     int grid;
 };
 // Opaque per-call state of the bias GEMM (the W tensor map).

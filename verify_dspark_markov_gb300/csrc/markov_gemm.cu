@@ -15,13 +15,14 @@
 // lands directly in the canonical core-matrix layout), 4 to 6 tiles ahead.
 // Warp roles: one thread of warp 0 issues the TMA loads and the MMAs (after
 // the MMAs of tile i it refills the stage of tile i - 1), warps 1..8 drain
-// the accumulators, one 32 x 32 block of each tile per warp.  Accumulators
-// are double-buffered in tensor memory so that the epilogue of one
-// vocabulary tile overlaps the MMAs of the next.  The W stream starts before the gather,
-// which runs as asynchronous 16-byte copies.  Requests are spread over the
-// four 32-lane TMEM quadrants so that every epilogue warp has rows; each warp
+// the accumulators, one 32 x 32 block of each tile per warp.  Four
+// accumulator buffers in tensor memory let the MMAs run up to three tiles
+// ahead of the epilogue.  The W stream starts before the gather, which runs as
+// asynchronous 16-byte copies.  Requests are spread over the four
+// 32-lane TMEM quadrants so that every epilogue warp has rows; each warp
 // transposes its 32 x 32 accumulator blocks through a swizzled shared-memory
-// tile, so the backbone loads and z stores run along rows (coalesced).
+// tile, so the backbone loads and z stores run along rows (coalesced); its
+// backbone blocks arrive two tiles ahead where shared memory allows.
 // Persistent CTAs, one per SM, walk the vocabulary tiles.
 
 #include <cuda.h>
@@ -40,21 +41,24 @@ namespace {
 constexpr int kThreads = 288;  // a control warp (TMA + MMA issue) and 8 epilogue warps
 constexpr int kEpiWarps = 8;
 constexpr int kMaxStages = 8;
-constexpr uint32_t kTmemCols = 128;  // two accumulator buffers of mtiles * nt = 64 columns
+constexpr int kAcc = 4;              // accumulator buffers in tensor memory
+constexpr uint32_t kTmemCols = 256;  // kAcc buffers of mtiles * nt = 64 columns
 // Per epilogue warp, for its rpq requests (<= 32): an rpq x 32 fp32 transpose
 // tile, element (row, col) at row * 32 + (col ^ row) (conflict-free both ways
-// without padding), and the backbone of its block of the next tile (rpq x 32,
-// copied asynchronously).
-__host__ __device__ constexpr int epi_warp_bytes(int esz, int rpq) { return rpq * 32 * (4 + esz); }
-__host__ __device__ constexpr int epi_bytes(int esz, int rpq) { return kEpiWarps * epi_warp_bytes(esz, rpq); }
+// without padding), and nbb buffers for the backbone of its block of the next
+// tiles (rpq x 32 each, copied asynchronously).
+__host__ __device__ constexpr int epi_warp_bytes(int esz, int rpq, int nbb) { return rpq * 32 * (4 + nbb * esz); }
+__host__ __device__ constexpr int epi_bytes(int esz, int rpq, int nbb) {
+    return kEpiWarps * epi_warp_bytes(esz, rpq, nbb);
+}
 // Shared memory per CTA (227 KB opt-in) less an allowance for the static part.
 constexpr int kSmemMax = 232448 - 1280;
 
 struct GemmSmem {
     uint64_t full[kMaxStages];   // W stage landed (TMA transaction bytes)
     uint64_t empty[kMaxStages];  // W stage consumed (MMA commit)
-    uint64_t acc_full[2];        // accumulator ready (MMA commit)
-    uint64_t acc_empty[2];       // accumulator drained (one arrival per epilogue warp)
+    uint64_t acc_full[kAcc];     // accumulator ready (MMA commit)
+    uint64_t acc_empty[kAcc];    // accumulator drained (one arrival per epilogue warp)
     uint32_t tmem_base;
     int timeout;
     int32_t x[256];  // x_{k-1} of every request (-1: none)
@@ -201,7 +205,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&sm.full[s], 1);
             mbar_init(&sm.empty[s], 1);
         }
-        for (int a = 0; a < 2; ++a) {
+        for (int a = 0; a < kAcc; ++a) {
             mbar_init(&sm.acc_full[a], 1);
             mbar_init(&sm.acc_empty[a], kEpiWarps);
         }
@@ -234,6 +238,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         else
             *reinterpret_cast<uint4*>(d) = make_uint4(0u, 0u, 0u, 0u);
     }
+    // The W stream starts once the gather's few latency-bound reads are on
+    // their way (issued first, they do not queue behind S stages of W).
     cp_async_wait_all();
     fence_proxy_async_smem();  // generic and async-copy stores -> visible to the tensor cores
     tc_fence_before();
@@ -248,9 +254,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t abase = smem_u32(sA), wbase = smem_u32(sW);
             int i = 0, issued = pre;
             for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++i) {
-                const int s = i % S, a = i & 1;
+                const int s = i % S, a = i % kAcc;
                 if (!mbar_wait(&sm.full[s], (i / S) & 1, kWaitLimitNs) ||
-                    (i >= 2 && !mbar_wait(&sm.acc_empty[a], ((i >> 1) - 1) & 1, kWaitLimitNs))) {
+                    (i >= kAcc && !mbar_wait(&sm.acc_empty[a], ((i / kAcc) - 1) & 1, kWaitLimitNs))) {
                     set_timeout(sm, p);
                     break;
                 }
@@ -279,7 +285,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             // Nothing may still be in flight when the tensor memory is released
             // and the CTA exits: the last MMAs, and (after a timeout) copies.
-            if (i > 0 && !mbar_wait(&sm.acc_full[(i - 1) & 1], ((i - 1) >> 1) & 1, kWaitLimitNs)) set_timeout(sm, p);
+            if (i > 0 && !mbar_wait(&sm.acc_full[(i - 1) % kAcc], ((i - 1) / kAcc) & 1, kWaitLimitNs))
+                set_timeout(sm, p);
             if (timed_out(sm))
                 for (int k = max(0, issued - S); k < issued; ++k) mbar_wait(&sm.full[k % S], (k / S) & 1, kWaitLimitNs);
         }
@@ -297,15 +304,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int m = f0 / NT, c0 = f0 % NT;
         const int b0 = m * 128 + quad * rpq;             // first request of the block
         const int nrows = max(0, min(rpq, p.B - b0));   // its valid requests
-        uint8_t* wbase_epi = stage_epi + e * epi_warp_bytes(kEsz, rpq);
+        const int nbb = p.nbb;
+        uint8_t* wbase_epi = stage_epi + e * epi_warp_bytes(kEsz, rpq, nbb);
         float* T = reinterpret_cast<float*>(wbase_epi);
-        uint8_t* bbuf = wbase_epi + rpq * 32 * 4;  // [row][32 columns] of the backbone
+        // [nbb][row][32 columns] of the backbone: tile i's block in buffer i % nbb
+        uint8_t* bbuf0 = wbase_epi + rpq * 32 * 4;
         const size_t esz = kEsz;
         const char* bb = static_cast<const char*>(p.backbone) + static_cast<size_t>(p.k - 1) * p.V * esz;
         const size_t bb_stride = static_cast<size_t>(p.gamma) * p.V * esz;  // one request
         // Asynchronous copy of the block's backbone of tile t into bbuf, in
-        // 16-byte pieces (4 or 8 lanes per row).
-        auto fetch_bb = [&](int t) {
+        // 16-byte pieces (4 or 8 lanes per row); one commit group per tile.
+        auto fetch_bb = [&](int t, uint8_t* bbuf) {
             constexpr int kLanesPerRow = 32 * kEsz / 16;
             constexpr int kRowsPerStep = 32 / kLanesPerRow;
             const int piece = lane % kLanesPerRow;
@@ -320,10 +329,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             asm volatile("cp.async.commit_group;" ::: "memory");
         };
         int i = 0;
-        if (nrows > 0 && blockIdx.x < ntiles) fetch_bb(blockIdx.x);
+        if (nrows > 0) {
+            for (int q = 0; q < nbb; ++q) {
+                const int tq = blockIdx.x + q * static_cast<int>(gridDim.x);
+                if (tq < ntiles) fetch_bb(tq, bbuf0 + q * rpq * 32 * kEsz);
+                else asm volatile("cp.async.commit_group;" ::: "memory");  // keep one group per tile
+            }
+        }
         for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++i) {
-            const int a = i & 1;
-            if (!mbar_wait(&sm.acc_full[a], (i >> 1) & 1, kWaitLimitNs)) {
+            const int a = i % kAcc;
+            uint8_t* bbuf = bbuf0 + (i % nbb) * rpq * 32 * kEsz;
+            if (!mbar_wait(&sm.acc_full[a], (i / kAcc) & 1, kWaitLimitNs)) {
                 set_timeout(sm, p);
                 asm volatile("cp.async.wait_group 0;" ::: "memory");
                 break;
@@ -339,7 +355,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                               static_cast<uint32_t>(a * mt * NT + m * NT + c0),
                           acc);
                 tmem_wait_ld();
-                asm volatile("cp.async.wait_group 0;" ::: "memory");  // this tile's backbone is in bbuf
+                // this tile's backbone is in bbuf (the next tile's may still be in flight)
+                if (nbb == 2) asm volatile("cp.async.wait_group 1;" ::: "memory");
+                else asm volatile("cp.async.wait_group 0;" ::: "memory");
                 if (lane < rpq) {  // lanes past rpq hold no request
 #pragma unroll
                     for (int j = 0; j < 32; ++j) T[lane * 32 + (j ^ lane)] = __uint_as_float(acc[j]);
@@ -360,8 +378,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 __syncwarp();
-                // the next tile's backbone streams in while its accumulator is computed
-                if (t + static_cast<int>(gridDim.x) < ntiles) fetch_bb(t + gridDim.x);
+                // the backbone nbb tiles ahead streams in while the accumulators are computed
+                const int tn = t + nbb * static_cast<int>(gridDim.x);
+                if (tn < ntiles) fetch_bb(tn, bbuf);
+                else asm volatile("cp.async.commit_group;" ::: "memory");
             }
             tc_fence_before();
             __syncwarp();
@@ -390,8 +410,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 int smem_bytes(const MarkovGemmParams& p) {
-    return p.mtiles * 128 * p.r * 2 + p.stages * p.nt * p.r * 2 + epi_bytes(p.dtype == kBF16 ? 2 : 4, p.rpq) +
-           1024;  // + alignment slack
+    return p.mtiles * 128 * p.r * 2 + p.stages * p.nt * p.r * 2 +
+           epi_bytes(p.dtype == kBF16 ? 2 : 4, p.rpq, p.nbb) + 1024;  // + alignment slack
 }
 
 template <int kDtype, bool kSw128>
@@ -412,9 +432,14 @@ bool prepare_markov_bias(MarkovGemmParams& p, MarkovGemmPlan& plan) {
     p.nt = 64 / p.mtiles;
     const int a = p.mtiles * 128 * p.r * 2, w = p.nt * p.r * 2;
     p.rpq = p.mtiles == 1 ? (p.B + 3) / 4 : 32;
-    const int budget = kSmemMax - epi_bytes(p.dtype == kBF16 ? 2 : 4, p.rpq) - 1024;  // A + W stages
-    p.stages = std::min(kMaxStages, (budget - a) / w);
-    if (p.stages < 2) return false;
+    // two backbone buffers per epilogue warp where they leave three W stages, else one
+    const int esz = p.dtype == kBF16 ? 2 : 4;
+    for (p.nbb = 2; p.nbb >= 1; --p.nbb) {
+        const int budget = kSmemMax - epi_bytes(esz, p.rpq, p.nbb) - 1024;  // A + W stages
+        p.stages = std::min(kMaxStages, (budget - a) / w);
+        if (p.stages >= 3 || (p.nbb == 1 && p.stages >= 2)) break;
+    }
+    if (p.nbb < 1 || p.stages < 2) return false;
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
