@@ -899,6 +899,46 @@ __device__ int find_crossing(Smem& sm, int n, unsigned long long th, bool strict
 }
 
 
+// One block scan over rank 0's first K candidates (weights wt(i), contiguous
+// ranges per thread): total = their weight sum; th = thresh(total); when th
+// is nonzero, pos = the first position whose inclusive prefix reaches th
+// (K if none) and prefix = the prefix there.  All threads of one CTA.
+template <typename Wf, typename Th>
+__device__ void cut_scan(Smem& sm, int K, Wf wt, Th thresh, unsigned long long& total, int& pos,
+                         unsigned long long& prefix) {
+    const int per = (K + kThreads - 1) / kThreads;
+    const int a = min(static_cast<int>(threadIdx.x) * per, K), e = min(a + per, K);
+    unsigned long long mine = 0;
+    for (int i = a; i < e; ++i) mine += wt(i);
+    const unsigned long long incl = block_scan_u64(sm, mine);
+    __shared__ unsigned long long s_tot, s_pm;
+    __shared__ int s_pos;
+    if (threadIdx.x == kThreads - 1) s_tot = incl;
+    if (threadIdx.x == 0) {
+        s_pos = K;
+        s_pm = 0ull;
+    }
+    __syncthreads();
+    total = s_tot;
+    const unsigned long long th = thresh(total);
+    const unsigned long long before = incl - mine;
+    if (th > 0 && mine > 0 && incl >= th && before < th) {
+        unsigned long long c = before;
+        for (int i = a; i < e; ++i) {
+            c += wt(i);
+            if (c >= th) {
+                s_pos = i;
+                s_pm = c;
+                break;
+            }
+        }
+    }
+    __syncthreads();
+    pos = s_pos;
+    prefix = s_pm;
+    __syncthreads();
+}
+
 // ceil(p * kept) clamped to [1, kept] (kept = 0 gives 0): the fixed-point
 // mass a top-p prefix must reach.
 __device__ __forceinline__ unsigned long long p_threshold(float p, unsigned long long kept) {
@@ -1181,24 +1221,25 @@ __device__ void row_policy(Smem& sm, cg::cluster_group& cl, const Slice& sl, int
         const int K = use_k ? static_cast<int>(min(k_eff - above_cnt - gap_cnt, static_cast<unsigned long long>(n)))
                             : n;
         auto wt = [&](int i) -> unsigned long long {
-            return i < K ? to_fixed(weight_f(key_to_float(vo_key(cbuf[i])), zmax, inv_t)) : 0ull;
+            return to_fixed(weight_f(key_to_float(vo_key(cbuf[i])), zmax, inv_t));
         };
-        unsigned long long kept = total_mass;
-        if (use_k) {
-            unsigned long long part;
-            find_crossing(sm, K, 0ull, true, wt, part);
-            kept = above_mass + gap_mass + part;
-        }
+        // one scan: the mass of the K kept candidates, then the top-p crossing
+        // (theta relative to the mass above the window) and the prefix there
+        unsigned long long part, pm;
+        int pos;
+        cut_scan(sm, K, wt,
+                 [&](unsigned long long k_part) -> unsigned long long {
+                     if (!use_p) return 0ull;
+                     const unsigned long long kept = use_k ? above_mass + gap_mass + k_part : total_mass;
+                     return p_threshold(pol.top_p, kept) - above_mass;
+                 },
+                 part, pos, pm);
+        const unsigned long long kept = use_k ? above_mass + gap_mass + part : total_mass;
         int mm = K;
         unsigned long long mass = kept;
         if (use_p) {
-            const unsigned long long theta = p_threshold(pol.top_p, kept);
-            unsigned long long tot;
-            const int pos = find_crossing(sm, K, theta - above_mass, false, wt, tot);
-            mm = min(pos + 1, K);
-            unsigned long long pm;
-            find_crossing(sm, mm, 0ull, true, wt, pm);  // mass of the first mm
-            mass = above_mass + pm;
+            mm = pos < K ? pos + 1 : K;
+            mass = above_mass + (pos < K ? pm : part);
         }
         mm = max(mm, 1);
         if (tid == 0) {
