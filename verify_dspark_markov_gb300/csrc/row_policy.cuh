@@ -1174,10 +1174,9 @@ __device__ void row_policy(Smem& sm, cg::cluster_group& cl, const Slice& sl, int
     const unsigned long long above_cnt = s_pl[0], above_mass = s_pl[1], wcount = s_pl[2], theta_p = s_pl[3];
     const unsigned long long gap_cnt = s_pl[4], gap_mass = s_pl[5];
     __syncthreads();
-    // the lowest key of the window
-    const uint32_t klo = lowest_true_key(kmax, BinAtMost{zmax, inv_t, whi});
 
     if (wcount > static_cast<unsigned long long>(kCap)) {
+        const uint32_t klo = lowest_true_key(kmax, BinAtMost{zmax, inv_t, whi});  // the window's lowest key
         if (!use_k) {  // top-p alone: radix selection inside the window
             const uint32_t khi = wlo > 0 ? lowest_true_key(kmax, BinAtMost{zmax, inv_t, wlo - 1}) - 1u : kmax;
             auto all = [](uint32_t, int32_t) { return true; };
@@ -1203,10 +1202,15 @@ __device__ void row_policy(Smem& sm, cg::cluster_group& cl, const Slice& sl, int
         return;
     }
 
-    // ---- compact the window's elements (but the gap's) into rank 0's buffer
+    // ---- compact the window's elements (but the gap's) into rank 0's buffer.
+    // The pick tests the exact bin; the floor only lets whole vectors be
+    // skipped, so it is taken below the window's lowest value with margins
+    // well past the rounding of s = (zmax - z)/T and of the subtraction.
     {
         const BinOf bin_of{zmax, inv_t};
-        compact_candidates(sm, cl, sl, cbuf, key_to_float(klo), [=](float z, int32_t) {
+        float zf = zmax - (static_cast<float>(whi + 1) * 0.125f / inv_t) * 1.0001f;
+        zf -= fabsf(zf) * 1e-6f + 1e-30f;
+        compact_candidates(sm, cl, sl, cbuf, zf, [=](float z, int32_t) {
             const int b = bin_of(z);
             return b >= wlo && b <= whi && (b <= phi || b == whi);
         });
