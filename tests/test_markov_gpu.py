@@ -92,6 +92,20 @@ def test_markov_mixed_policies_rank256(ds, oracle):
     _check(ref, got)
 
 
+def test_markov_nonfinite_rows_rank64(ds, oracle):
+    """Rows the bias kernel's maxima must flag: NaN at step 1, +inf at step 3,
+    every logit -inf at step 2 (no maximum) - each in its own request."""
+    w = synth.decode_verify_tile(V=4096, B=8, r=64, H=0)
+    bb = w.backbone.float()
+    bb[1, 0, 17] = float("nan")
+    bb[2, 2, 5] = float("inf")
+    bb[3, 1, :] = float("-inf")
+    w.backbone = bb.to(w.backbone.dtype).contiguous()
+    ref, got = _both(ds, oracle, w, with_h=False)
+    assert ref["status"].tolist()[1:4] == [1, 1, 2], ref["status"]
+    _check(ref, got, with_h=False, max_indet_frac=0.25)
+
+
 def test_markov_greedy_no_policy(ds, oracle):
     w = synth.decode_verify_tile(V=4096, B=24, r=256, H=0)
     ref, got = _both(ds, oracle, w, with_policy=False, with_h=False)
