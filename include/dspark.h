@@ -48,9 +48,12 @@
  *   Workspace  dspark_workspace_size() gives the bytes an operation needs.
  *              The workspace must be zero-filled once after allocation
  *              (e.g. cudaMemsetAsync(ws, 0, bytes, stream)); every call that
- *              completes leaves it zero-filled again, so it can be reused by
- *              the next call of the same operation on the same stream without
- *              clearing.  Calls that share one workspace must not overlap in
+ *              completes returns the words a call reads before writing them
+ *              (tickets, records, the error flag) to zero, so it can be
+ *              reused by the next call of the same operation on the same
+ *              stream without clearing.  The other regions (the Markov
+ *              logits, per-CTA partial sums) keep what the call wrote; every
+ *              call overwrites them before reading them.  Calls that share one workspace must not overlap in
  *              time, and a workspace serves one operation (clear it before
  *              handing it to another).  The greedy paths keep all their state
  *              on chip and ignore the workspace (it may be NULL): dspark_verify
