@@ -238,7 +238,7 @@ class Serving:
         bb, tg = synth.host(w.backbone), synth.host(w.target)
         anchor = w.anchor.cpu().numpy()
         keys = w.keys.numpy()
-        pol = (synth.uniform_policy(w.B, greedy=True) if self.pol is None else w.policy).numpy()
+        pol = (synth.uniform_policy(w.B, greedy=True) if self.greedy_only else w.policy).numpy()
         U = synth.host(w.weights.U) if w.weights.r else None
         Wm = synth.host(w.weights.W) if w.weights.r else None
         hh = synth.host(w.h) if w.h is not None else None
