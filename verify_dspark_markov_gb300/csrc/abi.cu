@@ -49,7 +49,9 @@ MarkovLayout markov_layout(int B, int gamma, int V, int r) {
     (void)gamma;
     l.error_flag = 0;  // zero between calls; set only after a device wait gave up
     l.zbuf = align_up(sizeof(int));
-    const size_t zbytes = r > 0 ? static_cast<size_t>(B) * V * sizeof(float) : 0;
+    // two z buffers: step k + 1's bias kernel writes one while step k's
+    // policy kernel still reads the other
+    const size_t zbytes = r > 0 ? 2 * static_cast<size_t>(B) * V * sizeof(float) : 0;
     l.total = align_up(l.zbuf + zbytes);
     return l;
 }
@@ -224,8 +226,11 @@ int dspark_markov_sample(const void* backbone, int dtype, const int32_t* anchor,
         mp.error_flag = r > 0 ? error_flag : nullptr;
         for (int k = 1; k <= gamma; ++k) {
             if (r > 0) {
+                float* zk = zbuf + static_cast<size_t>(k & 1) * B * V;
                 gp.k = k;
-                if (launch_markov_bias(gp, plan, s) != cudaSuccess) return DSPARK_ECUDA;
+                gp.zbuf = zk;
+                mp.zbuf = zk;
+                if (launch_markov_bias(gp, plan, k > 1, s) != cudaSuccess) return DSPARK_ECUDA;
             }
             mp.k = k;
             if (launch_markov_step(mp, s) != cudaSuccess) return DSPARK_ECUDA;

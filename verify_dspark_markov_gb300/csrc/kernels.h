@@ -126,7 +126,10 @@ struct MarkovGemmPlan {
 // Fill the launch shape of `p` and the tensor map of W; false if B or r are
 // outside what the kernel supports.
 bool prepare_markov_bias(MarkovGemmParams& p, MarkovGemmPlan& plan);
-cudaError_t launch_markov_bias(const MarkovGemmParams& p, const MarkovGemmPlan& plan, cudaStream_t stream);
+// overlap: a programmatic launch behind the previous step's policy kernel
+// (its z buffer must differ from the one that kernel reads).
+cudaError_t launch_markov_bias(const MarkovGemmParams& p, const MarkovGemmPlan& plan, bool overlap,
+                               cudaStream_t stream);
 // Elements of a row each CTA of the verify / drafting step owns.
 int verify_slice(int V);
 int step_slice(int V);

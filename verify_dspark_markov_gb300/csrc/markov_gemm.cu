@@ -213,6 +213,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_mbar_init();
         for (int t = blockIdx.x; t < ntiles && pre < S; t += gridDim.x, ++pre) issue_w(t, pre);
     }
+    // With a programmatic launch behind the previous step's policy kernel, the
+    // code above (TMEM, barriers, the first W stages) overlapped its tail;
+    // x_{k-1} is read only once that kernel has completed.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     // A operand: the gathered rows U[x_{k-1}(b)]; row i of lane quadrant q of
     // M tile m holds request m * 128 + q * rpq + i (i < rpq).  Zero rows past
     // the batch and for failed requests (their rows are ignored downstream).
@@ -415,13 +419,25 @@ int smem_bytes(const MarkovGemmParams& p) {
 }
 
 template <int kDtype, bool kSw128>
-cudaError_t launch_one(const MarkovGemmParams& p, const CUtensorMap& map, cudaStream_t stream) {
+cudaError_t launch_one(const MarkovGemmParams& p, const CUtensorMap& map, bool overlap, cudaStream_t stream) {
     const int smem = smem_bytes(p);
-    const cudaError_t e =
+    cudaError_t e =
         cudaFuncSetAttribute(markov_bias_kernel<kDtype, kSw128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    markov_bias_kernel<kDtype, kSw128><<<p.grid, kThreads, smem, stream>>>(map, p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(p.grid));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    if (overlap) {  // may start while the preceding kernel finishes (it waits before reading its outputs)
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    e = cudaLaunchKernelEx(&cfg, markov_bias_kernel<kDtype, kSw128>, map, p);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace
@@ -471,11 +487,14 @@ bool prepare_markov_bias(MarkovGemmParams& p, MarkovGemmPlan& plan) {
     return res == CUDA_SUCCESS;
 }
 
-cudaError_t launch_markov_bias(const MarkovGemmParams& p, const MarkovGemmPlan& plan, cudaStream_t stream) {
+cudaError_t launch_markov_bias(const MarkovGemmParams& p, const MarkovGemmPlan& plan, bool overlap,
+                               cudaStream_t stream) {
     const CUtensorMap& map = *reinterpret_cast<const CUtensorMap*>(plan.tmap);
     if (p.dtype == kBF16)
-        return plan.sw128 ? launch_one<kBF16, true>(p, map, stream) : launch_one<kBF16, false>(p, map, stream);
-    return plan.sw128 ? launch_one<kF32, true>(p, map, stream) : launch_one<kF32, false>(p, map, stream);
+        return plan.sw128 ? launch_one<kBF16, true>(p, map, overlap, stream)
+                          : launch_one<kBF16, false>(p, map, overlap, stream);
+    return plan.sw128 ? launch_one<kF32, true>(p, map, overlap, stream)
+                      : launch_one<kF32, false>(p, map, overlap, stream);
 }
 
 }  // namespace dspark

@@ -236,6 +236,9 @@ __global__ void __cluster_dims__(kStepC, 1, 1) __launch_bounds__(rp::kThreads, 4
     cg::cluster_group cl = cg::this_cluster();
     const int rank = static_cast<int>(cl.block_rank());
     const int tid = threadIdx.x;
+    // the next step's bias kernel may start on SMs this grid leaves free (it
+    // waits for this grid's completion before it reads the proposals)
+    asm volatile("griddepcontrol.launch_dependents;");
     rp::init_smem(sm);
     if (tid == 0) {
         s_qx = 0.0f;
