@@ -1,10 +1,10 @@
 // Row engine: the sampling policy of one vocabulary row, computed by a
 // cluster of CTAs (up to kMaxC; the kernel fixes the size) that each own a
 // contiguous slice of the row, plus the exact inverse-CDF draw over the
-// policy's weights.  The slices stay in
-// global memory: the first pass over a row streams it from HBM (or from L2
-// when the row was just written, like the Markov logits), later passes find
-// it in L2.  With no row held in shared memory a CTA needs ~37 KB.
+// policy's weights.  The slices stay in global memory: the first pass over a
+// row streams it from HBM (or from L2 when the row was just written, like the
+// Markov logits), later passes find it in L2.  With no row held in shared
+// memory a CTA needs ~37 KB.
 //
 // The policy [FT Exact decoding semantics > Probabilistic] as this library
 // reads it: greedy = one-hot at the lowest-index argmax; otherwise temperature,
@@ -17,14 +17,14 @@
 // (support = {key > tau} + {key == tau, index <= cut}); masses are fixed-point
 // integers w = round(2^40 exp((z - zmax)/T)), so every sum, every top-p
 // comparison and every inverse-CDF boundary is an exact, order-independent
-// integer decision.  To find the cut, one pass builds a histogram of
-// s = (zmax - z)/T in bins of 1/8 with exact counts and exact fixed-point
-// masses, reduced once over the cluster; its prefix sums bound the cuts to a
-// window of bins (usually one), whose elements are compacted into rank 0,
-// sorted by (logit descending, index ascending) and cut there by exact
-// prefix sums continued from the exact mass above the window.  A window too
-// large for the buffer (very flat rows) is resolved by radix selection on
-// order-preserving 32-bit keys inside its key range.
+// integer decision.  To find the cuts, one pass builds a histogram of
+// s = (zmax - z)/T in bins of 1/8 (exact counts, and exact fixed-point masses
+// unless the top-k set is small), reduced once over the cluster; its prefix
+// sums bound the cuts to a window of bins (usually one), whose elements are
+// compacted into rank 0, sorted by (logit descending, index ascending) and cut
+// there by exact prefix sums continued from the exact mass above the window.
+// A window too large for the buffer (very flat rows) is resolved by radix
+// selection on order-preserving 32-bit keys inside its key range.
 #pragma once
 
 #include <cooperative_groups.h>
@@ -1024,20 +1024,25 @@ __device__ __forceinline__ unsigned long long hist_pass(const Slice& sl, float z
 
 // The policy of the row held by the cluster.  One pass builds a histogram of
 // s = (zmax - z)/T in bins of 1/8 below s = 32 (beyond, the weight is 0 in
-// fixed point): exact counts and exact fixed-point masses per bin, each warp
-// into a private copy, summed per CTA and over the cluster.  Its prefix sums
-// give the bin where the cumulative count reaches k (top-k), bounds on the
-// kept mass, and from them the first bin where the cumulative mass can reach
-// p of it (top-p): both cuts lie in the window of bins between.  The window's
-// elements are compacted into rank 0's buffer, sorted by (logit descending,
-// index ascending) and cut there by exact prefix sums continued from the
-// exact mass above the window.  A support of at most kThreads tokens is
-// compacted whole, so that rank 0 holds it for the draw.  A window too large
-// for the buffer (a flat row: thousands of tokens in one bin, bf16 ties) is
-// resolved for top-p alone by radix selection inside the window's key range;
-// other such rows fall back to row_policy_radix.  cbuf = this CTA's
-// candidate buffer (kCap composite keys; only rank 0's receives candidates)
-// followed by kWarps x kBins 32-bit counts.
+// fixed point), each warp into a private copy, summed per CTA and over the
+// cluster: counts alone when top-k keeps at most kThreads tokens (that set is
+// compacted whole), otherwise exact counts and exact fixed-point masses.  Its
+// prefix sums give the bin where the cumulative count reaches k (top-k),
+// bounds on the kept mass, and from them the bins where the cumulative mass
+// can reach p of it (top-p): both cuts lie in the window of bins between.
+// With top-k and top-p together only the bins where the top-p cut can lie and
+// the top-k bin need their tokens; the bins between (the gap) enter as their
+// exact count and mass.  The window's elements (but the gap's) are compacted
+// into rank 0's buffer, whole vectors below a closed-form floor skipped;
+// rank 0 sorts them by (logit descending, index ascending) and takes both cuts
+// in one block scan of exact prefix sums continued from the exact mass above
+// the window.  A support of at most kThreads tokens is compacted whole, so
+// that rank 0 holds it for the draw.  A window too large for the buffer (a
+// flat row: thousands of tokens in one bin, bf16 ties) is resolved for top-p
+// alone by radix selection inside the window's key range; other such rows
+// fall back to row_policy_radix.  cbuf = this CTA's candidate buffer (kCap
+// composite keys; only rank 0's receives candidates) followed by
+// kWarps x kBins 32-bit counts.
 __device__ void row_policy(Smem& sm, cg::cluster_group& cl, const Slice& sl, int V, const Policy& pol,
                            RowResult& res, unsigned long long* cbuf) {
     const int nc = static_cast<int>(cl.num_blocks());  // CTAs in the cluster
