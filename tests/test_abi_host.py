@@ -47,6 +47,9 @@ def test_workspace_sizes(lib):
     assert ds.workspace_size(ds.OP_VERIFY, 64, 0, 129280) == 0      # invalid gamma
     assert ds.workspace_size(ds.OP_VERIFY, 64, 7, 129281) == 0      # V not a multiple of 8
     assert ds.workspace_size(99, 64, 7, 129280) == 0
+    # drafting with the Markov bias alternates two fp32 z buffers [B, V]
+    assert ds.workspace_size(ds.OP_MARKOV_SAMPLE, 64, 5, 129280, 256) >= 2 * 64 * 129280 * 4
+    assert ds.workspace_size(ds.OP_MARKOV_SAMPLE, 64, 5, 129280, 0) < 64 * 129280 * 4
 
 
 FAKE = ctypes.c_void_p(0x7F0000000000)       # aligned, never dereferenced
