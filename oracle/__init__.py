@@ -66,6 +66,8 @@ def _load():
             lib.orc_verify.restype = None
             lib.orc_accept_stats.argtypes = [P, P, i32, P, P, P, i32, i32, i32] + [P] * 7
             lib.orc_accept_stats.restype = None
+            lib.orc_accept_stats_backward.argtypes = [P, P, i32, P, P, P, i32, i32, i32, f64, P, P]
+            lib.orc_accept_stats_backward.restype = None
             _lib = lib
     return _lib
 
@@ -213,3 +215,23 @@ def accept_stats(draft, target, labels, conf_logits, mask=None):
                              _ptr(report), _ptr(ntok), _ptr(status))
     return dict(l1=l1, accept=acc, tau=tau, loss_num=loss, report=report,
                 num_tokens=int(ntok[0]), status=status)
+
+
+def accept_stats_backward(draft, target, labels, conf_logits, mask=None, scale=1.0):
+    """Gradient of 0.1 CE + 0.9 L1 + 1.0 BCE (weighted, masked numerators)
+    with respect to the draft logits and the confidence logits, the target
+    and the BCE label held fixed, times scale.  Returns (grad_draft float32
+    [N,gamma,V], grad_conf float32 [N,gamma])."""
+    draft = np.ascontiguousarray(draft)
+    target = np.ascontiguousarray(target)
+    if draft.shape != target.shape or draft.dtype != target.dtype:
+        raise ValueError("draft and target must match in shape and dtype")
+    N, gamma, V = draft.shape
+    y = _c(labels, np.int32)
+    zc = _c(conf_logits, np.float32)
+    m = None if mask is None else _c(mask, np.uint8)
+    gd = np.zeros((N, gamma, V), np.float32)
+    gc = np.zeros((N, gamma), np.float32)
+    _load().orc_accept_stats_backward(_ptr(draft), _ptr(target), _dtype_code(draft), _ptr(y), _ptr(zc),
+                                      _ptr(m), N, gamma, V, float(scale), _ptr(gd), _ptr(gc))
+    return gd, gc

@@ -518,3 +518,72 @@ extern "C" void orc_accept_stats(const void* draft, const void* target,
     report[1] = tau_sum;
     *num_tokens = count;
 }
+
+// Gradient of the loss numerator's total J = sum m w_k (0.1 CE + 0.9 L1 +
+// 1.0 BCE) [MB Training objective; Acceptance and confidence; Memory contract
+// for the full-vocabulary terms], the target the frozen teacher and the BCE
+// label accept detached, times scale:
+//   dJ/dd_u = m w_k (0.1 (p_d,u - [u = y]) + 0.9 p_d,u (s_u - sum_v s_v p_d,v)),
+//   s_v = sign(p_d,v - p_t,v) (0 at equality),
+//   dJ/dz_c = m w_k (sigmoid(z_c) - accept).
+// Masked positions get 0; a position with a NaN / +inf logit or a label
+// outside [0, V) (and mask 1) gets NaN in its whole draft gradient row.
+extern "C" void orc_accept_stats_backward(const void* draft, const void* target,
+                                          int32_t dtype, const int32_t* labels,
+                                          const float* conf_logits, const uint8_t* mask,
+                                          int32_t N, int32_t gamma, int32_t V, double scale,
+                                          float* grad_draft, float* grad_conf) {
+    std::vector<double> d(V), t(V), pd(V), pt(V);
+    const double nan = std::numeric_limits<double>::quiet_NaN();
+    for (int n = 0; n < N; ++n) {
+        for (int k = 1; k <= gamma; ++k) {
+            const size_t idx = static_cast<size_t>(n) * gamma + (k - 1);
+            float* g = grad_draft + idx * V;
+            const bool m = mask ? mask[idx] != 0 : true;
+            if (!m) {
+                for (int v = 0; v < V; ++v) g[v] = 0.0f;
+                grad_conf[idx] = 0.0f;
+                continue;
+            }
+            bool bad = false;
+            double dmax = -std::numeric_limits<double>::infinity(), tmax = dmax;
+            for (int v = 0; v < V; ++v) {
+                d[v] = load_value(draft, dtype, idx * V + v);
+                t[v] = load_value(target, dtype, idx * V + v);
+                if (is_bad_logit(d[v]) || is_bad_logit(t[v])) bad = true;
+                dmax = std::max(dmax, d[v]);
+                tmax = std::max(tmax, t[v]);
+            }
+            const int y = labels[idx];
+            if (y < 0 || y >= V) bad = true;
+            const double zc = conf_logits[idx];
+            const double c = scale * std::exp(-static_cast<double>(k) / gamma);
+            if (bad) {
+                for (int v = 0; v < V; ++v) g[v] = static_cast<float>(nan);
+                grad_conf[idx] = static_cast<float>(nan);
+                continue;
+            }
+            double dsum = 0.0, tsum = 0.0;
+            for (int v = 0; v < V; ++v) {
+                dsum += std::exp(d[v] - dmax);
+                tsum += std::exp(t[v] - tmax);
+            }
+            double dist = 0.0, S = 0.0;
+            for (int v = 0; v < V; ++v) {
+                pd[v] = std::exp(d[v] - dmax) / dsum;
+                pt[v] = std::exp(t[v] - tmax) / tsum;
+                const double diff = pd[v] - pt[v];
+                dist += std::fabs(diff);
+                S += (diff > 0.0 ? 1.0 : (diff < 0.0 ? -1.0 : 0.0)) * pd[v];
+            }
+            const double acc = std::min(1.0, std::max(0.0, 1.0 - 0.5 * dist));
+            for (int v = 0; v < V; ++v) {
+                const double diff = pd[v] - pt[v];
+                const double sv = diff > 0.0 ? 1.0 : (diff < 0.0 ? -1.0 : 0.0);
+                const double gce = pd[v] - (v == y ? 1.0 : 0.0);
+                g[v] = static_cast<float>(c * (0.1 * gce + 0.9 * pd[v] * (sv - S)));
+            }
+            grad_conf[idx] = static_cast<float>(c * (1.0 / (1.0 + std::exp(-zc)) - acc));
+        }
+    }
+}

@@ -110,6 +110,16 @@ void orc_accept_stats(const void* draft, const void* target, int32_t dtype,
                       float* l1, float* accept, float* tau, double* loss_num,
                       double* report, int64_t* num_tokens, int32_t* status);
 
+/* (c') Gradient of the loss numerators' total 0.1 CE + 0.9 L1 + 1.0 BCE
+ * (weighted, masked) with respect to the draft logits [N,gamma,V] and the
+ * confidence logits [N,gamma], the target and the BCE label (accept) held
+ * fixed, times scale.  Masked positions: 0; a non-finite logit or a label
+ * outside [0, V): NaN. */
+void orc_accept_stats_backward(const void* draft, const void* target, int32_t dtype,
+                               const int32_t* labels, const float* conf_logits,
+                               const uint8_t* mask, int32_t N, int32_t gamma, int32_t V,
+                               double scale, float* grad_draft, float* grad_conf);
+
 #ifdef __cplusplus
 }
 #endif
