@@ -16,6 +16,8 @@
  *   dspark_accept_stats   the analytical training-side statistics: L1
  *                         distance, acceptance rate, tau and the weighted
  *                         CE / L1 / confidence-BCE numerators.
+ *   dspark_accept_stats_grad  their loss's gradient with respect to the
+ *                         draft logits and the confidence logits.
  *
  * Sources, by page title and section:
  *   [FT] FreeToken PR #69 "[2/3] feat(dsv4): implement exact DSpark
@@ -250,6 +252,33 @@ int dspark_accept_stats(const void* draft, const void* target, int dtype,
                         float* l1, float* accept, float* tau, double* loss_num,
                         double* report, int64_t* num_tokens, int32_t* status,
                         void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * dspark_accept_stats_grad - the backward of dspark_accept_stats' loss: the
+ * gradient of J = 0.1 CE + 0.9 L1 + 1.0 BCE (the weighted, masked numerators'
+ * total, loss_num[3]) with respect to the draft logits and the confidence
+ * logits, times `scale` (e.g. the caller's 1 / num_tokens).  The target is
+ * the frozen teacher and the BCE label accept_rate is detached, so
+ *   d J / d draft[n,k,v] = scale m w_k (0.1 (p_d,v - [v = label])
+ *                                       + 0.9 p_d,v (s_v - sum_u s_u p_d,u)),
+ *   s_v = sign(p_d,v - p_t,v) (0 at equality),
+ *   d J / d conf_logits[n,k] = scale m w_k (sigmoid(z) - accept_rate).
+ * [MB Training objective; Memory contract for the full-vocabulary terms]:
+ * the softmax statistics are recomputed per row; nothing full-vocabulary is
+ * kept between the passes.
+ *
+ *   draft, target, labels, conf_logits, mask   as for dspark_accept_stats.
+ *   scale          the factor applied to both gradients.
+ *   grad_draft     fp32 [N, gamma, V] out (16-byte aligned).
+ *   grad_conf      fp32 [N, gamma] out.
+ * Masked positions get zeros; a position with a NaN / +inf logit or a label
+ * outside [0, V) gets NaN (its whole draft gradient row).  No workspace.
+ */
+int dspark_accept_stats_grad(const void* draft, const void* target, int dtype,
+                             const int32_t* labels, const float* conf_logits,
+                             const uint8_t* mask, int N, int gamma, int V,
+                             double scale, float* grad_draft, float* grad_conf,
+                             void* stream);
 
 /*
  * dspark_verify_greedy_noalloc - the greedy verify of dspark_verify (policy

@@ -101,6 +101,20 @@ def test_accept_stats_rejects_invalid_arguments(lib):
     assert f(FAKE, FAKE, 3, FAKE, FAKE, None, 4, 5, 1024, *([FAKE] * 7), FAKE, 1 << 20, None) == binding.EINVAL
 
 
+def test_accept_stats_grad_rejects_invalid_arguments(lib):
+    f = lib.dspark_accept_stats_grad
+    args = lambda **kw: dict(dict(d=FAKE, dt=0, N=4, g=5, V=1024, scale=1.0, gd=FAKE), **kw)
+    call = lambda a: f(a["d"], FAKE, a["dt"], FAKE, FAKE, None, a["N"], a["g"], a["V"], a["scale"], a["gd"], FAKE,
+                       None)
+    assert call(args(N=0)) == binding.OK                    # empty batch: no-op
+    assert call(args(g=0)) == binding.EINVAL
+    assert call(args(V=1001)) == binding.EINVAL
+    assert call(args(dt=7)) == binding.EINVAL
+    assert call(args(d=None)) == binding.EINVAL
+    assert call(args(gd=FAKE_ODD)) == binding.EINVAL        # the gradient rows take 16-byte stores
+    assert call(args(scale=float("nan"))) == binding.EINVAL
+
+
 def test_binding_fails_loudly_without_library(tmp_path):
     with pytest.raises((RuntimeError, OSError)):
         binding._lib = None

@@ -21,7 +21,7 @@ OP_MARKOV_SAMPLE, OP_VERIFY, OP_ACCEPT_STATS = 0, 1, 2
 REQ_OK, REQ_NONFINITE, REQ_EMPTY, REQ_TIMEOUT, REQ_BAD_POLICY, REQ_BAD_TOKEN = range(6)
 
 EXPORTED = ("dspark_workspace_size", "dspark_markov_sample", "dspark_verify",
-            "dspark_accept_stats", "dspark_status_string", "dspark_version",
+            "dspark_accept_stats", "dspark_accept_stats_grad", "dspark_status_string", "dspark_version",
             "dspark_verify_greedy_noalloc")
 
 _lock = threading.Lock()
@@ -59,6 +59,9 @@ def load(path: str | None = None):
             lib.dspark_accept_stats.argtypes = ([P, P, i32, P, P, P] + [i32] * 3 + [P] * 8
                                                 + [sz, P])
             lib.dspark_accept_stats.restype = i32
+            lib.dspark_accept_stats_grad.argtypes = ([P, P, i32, P, P, P] + [i32] * 3
+                                                     + [ctypes.c_double, P, P, P])
+            lib.dspark_accept_stats_grad.restype = i32
             lib.dspark_status_string.argtypes = [i32]
             lib.dspark_status_string.restype = ctypes.c_char_p
             lib.dspark_version.argtypes = []
@@ -240,4 +243,28 @@ def accept_stats(draft, target, labels, conf_logits, mask=None, workspace: Works
         _ptr(out["report"]), _ptr(out["num_tokens"]), _ptr(out["status"]), _ptr(ws), ws_n,
         _stream(stream))
     _check(code, "dspark_accept_stats")
+    return out
+
+
+def accept_stats_grad(draft, target, labels, conf_logits, mask=None, scale=1.0, stream=None, out=None):
+    """Gradient of the statistics' loss 0.1 CE + 0.9 L1 + 1.0 BCE (weighted,
+    masked numerators; target and the BCE label held fixed) with respect to
+    the draft logits and the confidence logits, times scale.  Returns
+    (grad_draft fp32 [N, gamma, V], grad_conf fp32 [N, gamma])."""
+    _dev(draft, "draft")
+    _dev(target, "target")
+    if draft.shape != target.shape or draft.dtype != target.dtype:
+        raise ValueError("draft and target must match in shape and dtype")
+    N, gamma, V = draft.shape
+    dev = draft.device
+    _dev(labels, "labels", torch.int32)
+    _dev(conf_logits, "conf_logits", torch.float32)
+    _dev(mask, "mask", torch.uint8)
+    if out is None:
+        out = (torch.empty((N, gamma, V), dtype=torch.float32, device=dev),
+               torch.empty((N, gamma), dtype=torch.float32, device=dev))
+    code = load().dspark_accept_stats_grad(
+        _ptr(draft), _ptr(target), _dtype_code(draft), _ptr(labels), _ptr(conf_logits), _ptr(mask),
+        N, gamma, V, float(scale), _ptr(out[0]), _ptr(out[1]), _stream(stream))
+    _check(code, "dspark_accept_stats_grad")
     return out

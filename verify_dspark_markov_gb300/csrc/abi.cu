@@ -306,4 +306,32 @@ int dspark_accept_stats(const void* draft, const void* target, int dtype, const 
     return launch_accept_stats(p, s) == cudaSuccess ? DSPARK_OK : DSPARK_ECUDA;
 }
 
+int dspark_accept_stats_grad(const void* draft, const void* target, int dtype, const int32_t* labels,
+                             const float* conf_logits, const uint8_t* mask, int N, int gamma, int V,
+                             double scale, float* grad_draft, float* grad_conf, void* stream) {
+    if (!valid_common(N, gamma, V, dtype)) return DSPARK_EINVAL;
+    if (static_cast<int64_t>(N) * gamma * stats_cluster_size() > 0x7FFFFFFFll) return DSPARK_EINVAL;
+    if (N == 0) return DSPARK_OK;
+    if (!draft || !target || !labels || !conf_logits || !grad_draft || !grad_conf) return DSPARK_EINVAL;
+    if (!aligned16(draft) || !aligned16(target) || !aligned16(grad_draft)) return DSPARK_EINVAL;
+    if (!(scale == scale)) return DSPARK_EINVAL;
+    StatsGradParams p{};
+    p.draft = draft;
+    p.target = target;
+    p.dtype = dtype;
+    p.labels = labels;
+    p.conf_logits = conf_logits;
+    p.mask = mask;
+    p.N = N;
+    p.gamma = gamma;
+    p.V = V;
+    const int C = stats_cluster_size();
+    p.slice = ((V + C - 1) / C + 7) / 8 * 8;
+    p.scale = scale;
+    p.grad_draft = grad_draft;
+    p.grad_conf = grad_conf;
+    return launch_accept_stats_grad(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? DSPARK_OK
+                                                                                           : DSPARK_ECUDA;
+}
+
 }  // extern "C"

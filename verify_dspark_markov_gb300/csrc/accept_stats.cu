@@ -15,6 +15,16 @@
 // Kernels 2 and 3: tau and the status per block (one thread each) with the
 // weighted sums reduced by fixed binary trees, then the CTA partials in a
 // fixed order, so repeated calls give identical bits.
+// Kernel 4 (one cluster per row pair, the backward [MB Training objective;
+// Memory contract for the full-vocabulary terms: the softmax statistics are
+// recomputed, nothing full-vocabulary is kept]): the gradient of the loss
+// numerators' total J = sum m w_k (0.1 CE + 0.9 L1 + 1.0 BCE), the target the
+// frozen teacher and the BCE label accept held fixed, times a scale:
+//   dJ/dd_v = m w_k (0.1 (p_d,v - [v = label]) + 0.9 p_d,v (s_v - S)),
+//   s_v = sign(p_d,v - p_t,v), S = sum_v s_v p_d,v,
+//   dJ/dz   = m w_k (sigmoid(z) - accept).
+// Pass 1 as in kernel 1; pass 2 sums the L1 terms and S; pass 3 re-reads the
+// slice (L2) and writes its gradient row.
 
 #include <cooperative_groups.h>
 
@@ -217,6 +227,200 @@ __global__ void __cluster_dims__(kC, 1, 1) __launch_bounds__(kThreads)
     cluster.sync();  // no CTA leaves while rank 0 reads its shared memory
 }
 
+// Kernel 4: see the file comment.  Masked positions write zeros; a position
+// with a NaN / +inf logit or a label outside [0, V) writes NaN.
+template <int kDtype>
+__global__ void __cluster_dims__(kC, 1, 1) __launch_bounds__(kThreads)
+    stats_grad_kernel(const StatsGradParams p) {
+    constexpr int kPer = kDtype == kBF16 ? 8 : 4;
+    constexpr int64_t kEsize = kDtype == kBF16 ? 2 : 4;
+    __shared__ float s_warp[4][kThreads / 32];
+    __shared__ float s_stats[4];   // this CTA's (md, sd, mt, st)
+    __shared__ double s_sums[2];   // this CTA's (L1, S) partials
+
+    cg::cluster_group cluster = cg::this_cluster();
+    const int rank = static_cast<int>(cluster.block_rank());
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int64_t pair = blockIdx.x / kC;
+    const int k = static_cast<int>(pair % p.gamma) + 1;  // 1-based position in the block
+    const int64_t lo = static_cast<int64_t>(rank) * p.slice;
+    const int64_t hi = min(lo + p.slice, static_cast<int64_t>(p.V));
+    const int nvec = hi > lo ? static_cast<int>((hi - lo) / kPer) : 0;
+    const char* drow = static_cast<const char*>(p.draft) + (pair * p.V + lo) * kEsize;
+    const char* trow = static_cast<const char*>(p.target) + (pair * p.V + lo) * kEsize;
+    float* grow = p.grad_draft + pair * p.V + lo;  // kPer floats per vector, 16-byte aligned
+
+    if (p.mask && p.mask[pair] == 0) {  // the same branch in every CTA of the cluster
+        const float4 z4 = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        for (int j = tid; j < nvec; j += kThreads) {
+            float4* g4 = reinterpret_cast<float4*>(grow + static_cast<int64_t>(j) * kPer);
+            g4[0] = z4;
+            if (kPer == 8) g4[1] = z4;
+        }
+        if (rank == 0 && tid == 0) p.grad_conf[pair] = 0.0f;
+        return;
+    }
+
+    // ---- pass 1: online max / sum of exp over the slice, both rows
+    Online od, ot;
+    od.init();
+    ot.init();
+    for (int j0 = tid; j0 < nvec; j0 += kBatch * kThreads) {
+        uint4 vd[kBatch], vt[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            const int j = j0 + u * kThreads;
+            if (j < nvec) {
+                vd[u] = ld_stream_v4(drow + static_cast<int64_t>(j) * 16);
+                vt[u] = ld_stream_v4(trow + static_cast<int64_t>(j) * 16);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            if (j0 + u * kThreads < nvec) {
+                float x[kPer];
+                unpack<kDtype>(vd[u], x);
+                od.add(x);
+                unpack<kDtype>(vt[u], x);
+                ot.add(x);
+            }
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        od.merge(__shfl_xor_sync(0xFFFFFFFFu, od.m, o), __shfl_xor_sync(0xFFFFFFFFu, od.s, o));
+        ot.merge(__shfl_xor_sync(0xFFFFFFFFu, ot.m, o), __shfl_xor_sync(0xFFFFFFFFu, ot.s, o));
+    }
+    if (lane == 0) {
+        s_warp[0][warp] = od.m; s_warp[1][warp] = od.s;
+        s_warp[2][warp] = ot.m; s_warp[3][warp] = ot.s;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        Online a, b;
+        a.init();
+        b.init();
+        for (int w = 0; w < kThreads / 32; ++w) {
+            a.merge(s_warp[0][w], s_warp[1][w]);
+            b.merge(s_warp[2][w], s_warp[3][w]);
+        }
+        s_stats[0] = a.m; s_stats[1] = a.s; s_stats[2] = b.m; s_stats[3] = b.s;
+    }
+    cluster.sync();
+    // every CTA combines the kC slices in rank order: identical results
+    Online gd, gt;
+    gd.init();
+    gt.init();
+    for (int r = 0; r < kC; ++r) {
+        const float* st = cluster.map_shared_rank(s_stats, r);
+        gd.merge(st[0], st[1]);
+        gt.merge(st[2], st[3]);
+    }
+    const float inv_sd = 1.0f / gd.s, inv_st = 1.0f / gt.s;
+    const int32_t y = p.labels[pair];
+    const bool bad = gd.s != gd.s || gt.s != gt.s || y < 0 || y >= p.V;
+
+    // ---- pass 2: the L1 terms and S = sum of sign(p_d - p_t) p_d (re-read, served by L2)
+    float l1 = 0.0f, sg = 0.0f;
+    for (int j0 = tid; j0 < nvec; j0 += kBatch * kThreads) {
+        uint4 vd[kBatch], vt[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            const int j = j0 + u * kThreads;
+            if (j < nvec) {
+                vd[u] = ld_stream_v4(drow + static_cast<int64_t>(j) * 16);
+                vt[u] = ld_stream_v4(trow + static_cast<int64_t>(j) * 16);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            if (j0 + u * kThreads < nvec) {
+                float xd[kPer], xt[kPer];
+                unpack<kDtype>(vd[u], xd);
+                unpack<kDtype>(vt[u], xt);
+#pragma unroll
+                for (int i = 0; i < kPer; ++i) {
+                    // both probabilities rounded before the difference (no
+                    // contraction): equal rows give sign 0 exactly
+                    const float pd = __fmul_rn(ex2((xd[i] - gd.m) * kLog2e), inv_sd);
+                    const float diff = __fsub_rn(pd, __fmul_rn(ex2((xt[i] - gt.m) * kLog2e), inv_st));
+                    l1 += fabsf(diff);
+                    sg += diff > 0.0f ? pd : (diff < 0.0f ? -pd : 0.0f);
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        l1 += __shfl_xor_sync(0xFFFFFFFFu, l1, o);
+        sg += __shfl_xor_sync(0xFFFFFFFFu, sg, o);
+    }
+    if (lane == 0) {
+        s_warp[0][warp] = l1;
+        s_warp[1][warp] = sg;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        double a = 0.0, b = 0.0;
+        for (int w = 0; w < kThreads / 32; ++w) {
+            a += s_warp[0][w];
+            b += s_warp[1][w];
+        }
+        s_sums[0] = a;
+        s_sums[1] = b;
+    }
+    cluster.sync();
+    double dist = 0.0, S = 0.0;
+    for (int r = 0; r < kC; ++r) {
+        const double* sr = cluster.map_shared_rank(s_sums, r);
+        dist += sr[0];
+        S += sr[1];
+    }
+    const float c = static_cast<float>(p.scale * exp(-static_cast<double>(k) / p.gamma));
+    const float Sf = static_cast<float>(S);
+    const float nanf = __int_as_float(0x7FC00000);
+
+    // ---- pass 3: the slice's gradient row (re-read, served by L2)
+    for (int j0 = tid; j0 < nvec; j0 += kBatch * kThreads) {
+        uint4 vd[kBatch], vt[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            const int j = j0 + u * kThreads;
+            if (j < nvec) {
+                vd[u] = ld_stream_v4(drow + static_cast<int64_t>(j) * 16);
+                vt[u] = ld_stream_v4(trow + static_cast<int64_t>(j) * 16);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            const int j = j0 + u * kThreads;
+            if (j < nvec) {
+                float xd[kPer], xt[kPer], g[kPer];
+                unpack<kDtype>(vd[u], xd);
+                unpack<kDtype>(vt[u], xt);
+#pragma unroll
+                for (int i = 0; i < kPer; ++i) {
+                    const float pd = __fmul_rn(ex2((xd[i] - gd.m) * kLog2e), inv_sd);
+                    const float diff = __fsub_rn(pd, __fmul_rn(ex2((xt[i] - gt.m) * kLog2e), inv_st));
+                    const float sv = diff > 0.0f ? 1.0f : (diff < 0.0f ? -1.0f : 0.0f);
+                    const int64_t v = lo + static_cast<int64_t>(j) * kPer + i;
+                    const float gce = pd - (v == y ? 1.0f : 0.0f);
+                    g[i] = bad ? nanf : c * (0.1f * gce + 0.9f * pd * (sv - Sf));
+                }
+                float4* g4 = reinterpret_cast<float4*>(grow + static_cast<int64_t>(j) * kPer);
+                g4[0] = make_float4(g[0], g[1], g[2], g[3]);
+                if constexpr (kPer == 8) g4[1] = make_float4(g[4], g[5], g[6], g[7]);
+            }
+        }
+    }
+    if (rank == 0 && tid == 0) {
+        const float acc = fminf(1.0f, fmaxf(0.0f, 1.0f - 0.5f * static_cast<float>(dist)));
+        const float zc = p.conf_logits[pair];
+        p.grad_conf[pair] = bad ? nanf : c * (1.0f / (1.0f + expf(-zc)) - acc);
+    }
+    cluster.sync();  // no CTA leaves while others read its shared memory
+}
+
 constexpr int kFinalThreads = 256;
 constexpr int kSums = 6;  // weighted CE, L1, BCE; sum of accept; sum of tau; token count
 
@@ -298,6 +502,16 @@ __global__ void __launch_bounds__(kFinalThreads) stats_total_kernel(const StatsP
 int stats_cluster_size() { return kC; }
 
 int stats_partials(int N) { return (N + kFinalThreads - 1) / kFinalThreads; }
+
+cudaError_t launch_accept_stats_grad(const StatsGradParams& p, cudaStream_t stream) {
+    const int64_t pairs = static_cast<int64_t>(p.N) * p.gamma;
+    const dim3 grid(static_cast<unsigned>(pairs * kC));
+    if (p.dtype == kBF16)
+        stats_grad_kernel<kBF16><<<grid, kThreads, 0, stream>>>(p);
+    else
+        stats_grad_kernel<kF32><<<grid, kThreads, 0, stream>>>(p);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_accept_stats(const StatsParams& p, cudaStream_t stream) {
     const int64_t pairs = static_cast<int64_t>(p.N) * p.gamma;

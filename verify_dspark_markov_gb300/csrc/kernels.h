@@ -166,4 +166,20 @@ int stats_cluster_size();
 int stats_partials(int N);
 cudaError_t launch_accept_stats(const StatsParams& p, cudaStream_t stream);
 
+// Gradient of the loss numerators' total (accept_stats.cu).
+struct StatsGradParams {
+    const void* draft;
+    const void* target;
+    int dtype;
+    const int32_t* labels;
+    const float* conf_logits;
+    const uint8_t* mask;      // or null
+    int N, gamma, V;
+    int slice;                // elements per CTA slice, a multiple of 8
+    double scale;
+    float* grad_draft;        // [N, gamma, V]
+    float* grad_conf;         // [N, gamma]
+};
+cudaError_t launch_accept_stats_grad(const StatsGradParams& p, cudaStream_t stream);
+
 }  // namespace dspark
