@@ -16,6 +16,9 @@ in HBM when the timed region starts.  Workloads (``--workload``):
                      greedy, 10 % adversarial drafts, rank 256.
   training_stats     4096 blocks x gamma = 7 fp32 row pairs: L1, accept rate,
                      tau and the weighted loss numerators.
+  training_stats_grad  the same row pairs: the gradient of the loss numerators'
+                     total with respect to the draft and confidence logits
+                     (gradient rows written in full).
 
 The step's inputs exceed L2 (135.5 MB on GB300) in every workload; in addition
 a 2 x L2-sized read of another buffer before every timed step, outside the
@@ -340,6 +343,65 @@ class Stats:
                           f"recipe in {el:.1f} s, single-threaded C++ oracle"}
 
 
+class StatsGrad(Stats):
+    """The gradient of the statistics' loss numerators for one batch of row
+    pairs: the draft-logit gradient rows written in full (they stay on the
+    device for the optimizer; the end-to-end leg reads back the confidence
+    gradients)."""
+
+    def __init__(self, w, blocks=None):
+        super().__init__(w, blocks)
+        self.name = "training_stats_grad"
+
+    def setup(self, ds, dev):
+        w = self.w
+        self.ds = ds
+        N, g, V = w.N, w.gamma, w.V
+        self.grads = (torch.empty((N, g, V), dtype=torch.float32, device=dev),
+                      torch.empty((N, g), dtype=torch.float32, device=dev))
+        self.inputs = [w.draft, w.target, w.labels, w.conf_logits]
+
+    def stats(self, stream, draft=None, target=None, labels=None, conf=None):
+        w = self.w
+        self.ds.accept_stats_grad(draft if draft is not None else w.draft,
+                                  target if target is not None else w.target,
+                                  labels if labels is not None else w.labels,
+                                  conf if conf is not None else w.conf_logits,
+                                  scale=1.0, out=self.grads, stream=stream)
+
+    def parts(self):
+        return [("stats_grad", self.stats)]
+
+    def bytes(self):
+        w = self.w
+        return {"stats_grad": 3 * w.N * w.gamma * w.V * 4 + w.N * w.gamma * 12}
+
+    def outputs(self):
+        return [self.grads[1]]
+
+    def check(self):
+        assert bool(torch.isfinite(self.grads[1]).all())
+
+    def cpu_sample(self, budget_s, max_requests=None):
+        import oracle
+        oracle.build()
+        w = self.w
+        done, n, t0 = 0, 0, time.perf_counter()
+        while True:
+            sl = slice(n, n + 1)
+            oracle.accept_stats_backward(synth.host(w.draft[sl]), synth.host(w.target[sl]),
+                                         w.labels[sl].cpu().numpy(), w.conf_logits[sl].cpu().numpy())
+            done += 1
+            n = (n + 1) % w.N
+            el = time.perf_counter() - t0
+            if el >= budget_s or (max_requests and done >= max_requests):
+                break
+        pos = done * w.gamma
+        return {"value": pos / el, "unit": UNIT, "cores": 1, "kind": "oracle",
+                "sample": f"{done} whole blocks ({pos} row pairs) of a {w.N}-block draw of the workload's "
+                          f"recipe in {el:.1f} s, single-threaded C++ oracle (gradient)"}
+
+
 def make_workload(name, device, stats_blocks=4096):
     if name == "full_decode_tile":
         return Serving(name, synth.full_decode_tile(device=device), 2)
@@ -349,10 +411,12 @@ def make_workload(name, device, stats_blocks=4096):
         return Serving(name, synth.mixed_serving(device=device), 2)
     if name == "training_stats":
         return Stats(synth.training_stats(device=device, N=stats_blocks))
+    if name == "training_stats_grad":
+        return StatsGrad(synth.training_stats(device=device, N=stats_blocks))
     raise ValueError(name)
 
 
-WORKLOADS = ("full_decode_tile", "decode_verify_tile", "mixed_serving", "training_stats")
+WORKLOADS = ("full_decode_tile", "decode_verify_tile", "mixed_serving", "training_stats", "training_stats_grad")
 
 
 # ------------------------------------------------------------------ GPU arm
@@ -446,7 +510,8 @@ def run_gpu(args):
     dom = max(part_ms, key=part_ms.get)
     achieved = nbytes[dom] / (part_ms[dom] * 1e-3) / 1e9
     kernel = {"full_decode_tile": "argmax_rows_kernel<bf16> (draft + verify launches)",
-              "training_stats": "stats_pairs_kernel<f32> (+ stats_blocks_kernel, stats_total_kernel)"}.get(
+              "training_stats": "stats_pairs_kernel<f32> (+ stats_blocks_kernel, stats_total_kernel)",
+              "training_stats_grad": "stats_grad_kernel<f32>"}.get(
                   wl.name, {"draft": "markov_sample (markov_bias_kernel + markov_step_kernel per position)",
                             "verify": "verify_rows_kernel<bf16>"}.get(dom, dom))
     if wl.name == "full_decode_tile":  # the same kernel serves both parts: average over both launches
@@ -462,7 +527,7 @@ def run_gpu(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16" if wl.name != "training_stats" else "f32",
+        "dtype": "f32" if isinstance(wl, Stats) else "bf16",
         "data": "synthetic",
         "config": dict(wl.config(), l2="inputs larger than L2, plus a 2 x L2 read of another buffer "
                                        "before every step",
@@ -488,8 +553,8 @@ def run_gpu(args):
             launches = 2
         else:
             launches = (2 * g if wl.w.weights.r else g) + (1 if wl.w.h is not None else 0) + 1
-    else:
-        launches = 2
+    else:  # the statistics: pairs + per-block + total kernels; the gradient: one kernel
+        launches = 1 if isinstance(wl, StatsGrad) else 3
     result["gpu_launches"] = launches * steps
     traffic = os.path.join(ROOT, "profiles", "traffic.json")
     if os.path.exists(traffic):
@@ -511,6 +576,8 @@ def make_workload_small(name):
     (the training statistics for 64 of its 4096 blocks)."""
     if name == "training_stats":
         return Stats(synth.training_stats(device="cpu", N=64), blocks=4096)
+    if name == "training_stats_grad":
+        return StatsGrad(synth.training_stats(device="cpu", N=64), blocks=4096)
     return make_workload(name, "cpu")
 
 
