@@ -230,7 +230,7 @@ __global__ void __cluster_dims__(kC, 1, 1) __launch_bounds__(kThreads)
 // Kernel 4: see the file comment.  Masked positions write zeros; a position
 // with a NaN / +inf logit or a label outside [0, V) writes NaN.
 template <int kDtype>
-__global__ void __cluster_dims__(kC, 1, 1) __launch_bounds__(kThreads)
+__global__ void __cluster_dims__(kC, 1, 1) __launch_bounds__(kThreads, 4)
     stats_grad_kernel(const StatsGradParams p) {
     constexpr int kPer = kDtype == kBF16 ? 8 : 4;
     constexpr int64_t kEsize = kDtype == kBF16 ? 2 : 4;
