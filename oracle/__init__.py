@@ -64,6 +64,8 @@ def _load():
             lib.orc_markov_sample.restype = None
             lib.orc_verify.argtypes = [P, i32, P, P, P] + [P] * 7 + [i32, i32, i32] + [P] * 4
             lib.orc_verify.restype = None
+            lib.orc_verify_width.argtypes = [P, i32, P, P, P] + [P] * 7 + [i32, i32, i32] + [P] * 5
+            lib.orc_verify_width.restype = None
             lib.orc_accept_stats.argtypes = [P, P, i32, P, P, P, i32, i32, i32] + [P] * 7
             lib.orc_accept_stats.restype = None
             lib.orc_accept_stats_backward.argtypes = [P, P, i32, P, P, P, i32, i32, i32, f64, P, P]
@@ -164,10 +166,12 @@ def markov_sample(backbone, anchor, U, W, h, E, w_conf, policy, seed, request_id
                 indet=indet.astype(bool))
 
 
-def verify(target, proposals, q, q_at_x, policy, seed, request_id, pos0):
+def verify(target, proposals, q, q_at_x, policy, seed, request_id, pos0, width=None):
     """target [B,gamma+1,V] (uint16 bf16 bits or float32); proposals int32
     [B,gamma]; q float32 [B,gamma,V] or None (all-greedy batch); q_at_x float32
-    [B,gamma] or None.  Returns dict(out_tokens, num_accepted, status, indet)."""
+    [B,gamma] or None; width int32 [B] (proposals each request verifies,
+    0..gamma) or None (all gamma).  Returns dict(out_tokens, num_accepted,
+    status, indet)."""
     target = np.ascontiguousarray(target)
     B, rows, V = target.shape
     gamma = rows - 1
@@ -186,9 +190,15 @@ def verify(target, proposals, q, q_at_x, policy, seed, request_id, pos0):
     nacc = np.zeros(B, np.int32)
     status = np.zeros(B, np.int32)
     indet = np.zeros(B, np.uint8)
-    _load().orc_verify(_ptr(target), _dtype_code(target), _ptr(x), _ptr(qc), _ptr(qx),
-                       _ptr(T), _ptr(K), _ptr(P), _ptr(G), _ptr(seed), _ptr(rid), _ptr(p0),
-                       B, gamma, V, _ptr(out), _ptr(nacc), _ptr(status), _ptr(indet))
+    if width is None:
+        _load().orc_verify(_ptr(target), _dtype_code(target), _ptr(x), _ptr(qc), _ptr(qx),
+                           _ptr(T), _ptr(K), _ptr(P), _ptr(G), _ptr(seed), _ptr(rid), _ptr(p0),
+                           B, gamma, V, _ptr(out), _ptr(nacc), _ptr(status), _ptr(indet))
+    else:
+        wd = _c(width, np.int32)
+        _load().orc_verify_width(_ptr(target), _dtype_code(target), _ptr(x), _ptr(qc), _ptr(qx),
+                                 _ptr(T), _ptr(K), _ptr(P), _ptr(G), _ptr(seed), _ptr(rid), _ptr(p0),
+                                 B, gamma, V, _ptr(wd), _ptr(out), _ptr(nacc), _ptr(status), _ptr(indet))
     return dict(out_tokens=out, num_accepted=nacc, status=status, indet=indet.astype(bool))
 
 

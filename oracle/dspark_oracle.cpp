@@ -338,15 +338,20 @@ extern "C" void orc_markov_sample(
 // and resample from p; a chi-square test of the emitted-token law against
 // target-only sampling on agreeing, disagreeing and nearly disjoint rows.
 // ---------------------------------------------------------------------------
-extern "C" void orc_verify(const void* target, int32_t dtype,
-                           const int32_t* proposals, const float* q,
-                           const float* q_at_x, const float* temperature,
-                           const int32_t* top_k, const float* top_p,
-                           const int32_t* greedy, const uint64_t* seed,
-                           const uint64_t* request_id, const int64_t* pos0,
-                           int32_t B, int32_t gamma, int32_t V,
-                           int32_t* out_tokens, int32_t* num_accepted,
-                           int32_t* status, uint8_t* indet) {
+// The verify of each request over its first width[b] proposals (width NULL:
+// all gamma).  A request checks proposals 1..g and reads target rows 0..g
+// (g = its width); every later row and proposal is ignored.  The bonus comes
+// from row g, drawn at position pos0 + g + 1; g = 0 is one target-only draw
+// from row 0.  A width outside [0, gamma] is reported as a bad token.
+extern "C" void orc_verify_width(const void* target, int32_t dtype,
+                                 const int32_t* proposals, const float* q,
+                                 const float* q_at_x, const float* temperature,
+                                 const int32_t* top_k, const float* top_p,
+                                 const int32_t* greedy, const uint64_t* seed,
+                                 const uint64_t* request_id, const int64_t* pos0,
+                                 int32_t B, int32_t gamma, int32_t V,
+                                 const int32_t* width, int32_t* out_tokens,
+                                 int32_t* num_accepted, int32_t* status, uint8_t* indet) {
     const int rows = gamma + 1;
     std::vector<double> z(V), w(V);
     std::vector<std::vector<double>> p(rows, std::vector<double>(V));
@@ -359,12 +364,17 @@ extern "C" void orc_verify(const void* target, int32_t dtype,
         num_accepted[b] = -1;
         status[b] = ORC_OK;
         indet[b] = 0;
+        const int g = width ? width[b] : gamma;  // proposals this request verifies
+        if (g < 0 || g > gamma) {
+            status[b] = ORC_BAD_TOKEN;
+            continue;
+        }
 
-        for (int k = 0; k < gamma; ++k)
+        for (int k = 0; k < g; ++k)
             if (x[k] < 0 || x[k] >= V) status[b] = ORC_BAD_TOKEN;
         if (status[b] != ORC_OK) continue;
 
-        for (int i = 0; i < rows; ++i) {
+        for (int i = 0; i <= g; ++i) {
             const size_t row = static_cast<size_t>(b) * rows + i;
             for (int v = 0; v < V; ++v) z[v] = load_value(target, dtype, row * V + v);
             int32_t support = 0;
@@ -377,7 +387,7 @@ extern "C" void orc_verify(const void* target, int32_t dtype,
 
         if (greedy[b]) {
             int n = 0;
-            while (n < gamma && x[n] == am[n]) ++n;
+            while (n < g && x[n] == am[n]) ++n;
             for (int i = 0; i < n; ++i) out[i] = x[i];
             out[n] = am[n];
             num_accepted[b] = n;
@@ -385,7 +395,7 @@ extern "C" void orc_verify(const void* target, int32_t dtype,
         }
 
         int rejected_at = 0;  // 1-based k of the first rejection, 0 = none
-        for (int k = 1; k <= gamma; ++k) {
+        for (int k = 1; k <= g; ++k) {
             const double pk = p[k - 1][x[k - 1]];
             const double qk = q_at_x[static_cast<size_t>(b) * gamma + (k - 1)];
             double ratio;
@@ -415,16 +425,28 @@ extern "C" void orc_verify(const void* target, int32_t dtype,
             out[j - 1] = token;
             num_accepted[b] = j - 1;
         } else {
-            if (row_indet[gamma]) indet[b] = 1;
-            const double u =
-                orc_uniform(seed[b], request_id[b], pos0[b] + gamma + 1, 2);
-            token = orc_sample_index(p[gamma].data(), V, u, &margin);
-            for (int i = 0; i < gamma; ++i) out[i] = x[i];
-            out[gamma] = token;
-            num_accepted[b] = gamma;
+            if (row_indet[g]) indet[b] = 1;
+            const double u = orc_uniform(seed[b], request_id[b], pos0[b] + g + 1, 2);
+            token = orc_sample_index(p[g].data(), V, u, &margin);
+            for (int i = 0; i < g; ++i) out[i] = x[i];
+            out[g] = token;
+            num_accepted[b] = g;
         }
         if (margin < kTol) indet[b] = 1;
     }
+}
+
+extern "C" void orc_verify(const void* target, int32_t dtype,
+                           const int32_t* proposals, const float* q,
+                           const float* q_at_x, const float* temperature,
+                           const int32_t* top_k, const float* top_p,
+                           const int32_t* greedy, const uint64_t* seed,
+                           const uint64_t* request_id, const int64_t* pos0,
+                           int32_t B, int32_t gamma, int32_t V,
+                           int32_t* out_tokens, int32_t* num_accepted,
+                           int32_t* status, uint8_t* indet) {
+    orc_verify_width(target, dtype, proposals, q, q_at_x, temperature, top_k, top_p, greedy, seed,
+                     request_id, pos0, B, gamma, V, nullptr, out_tokens, num_accepted, status, indet);
 }
 
 // ---------------------------------------------------------------------------

@@ -97,6 +97,17 @@ void orc_verify(const void* target, int32_t dtype, const int32_t* proposals,
                 const int64_t* pos0, int32_t B, int32_t gamma, int32_t V,
                 int32_t* out_tokens, int32_t* num_accepted, int32_t* status,
                 uint8_t* indet);
+/* (b') The same verify over a per-request width: request b checks its first
+ * width[b] proposals (0..gamma) against target rows 0..width[b] and draws the
+ * bonus from row width[b]; width NULL = gamma for every request.  A width
+ * outside [0, gamma] is reported as a bad token. */
+void orc_verify_width(const void* target, int32_t dtype, const int32_t* proposals,
+                      const float* q, const float* q_at_x, const float* temperature,
+                      const int32_t* top_k, const float* top_p, const int32_t* greedy,
+                      const uint64_t* seed, const uint64_t* request_id,
+                      const int64_t* pos0, int32_t B, int32_t gamma, int32_t V,
+                      const int32_t* width, int32_t* out_tokens, int32_t* num_accepted,
+                      int32_t* status, uint8_t* indet);
 
 /* (c) Analytical acceptance statistics [MB Training objective; Acceptance
  * and confidence; Loss return contract].  draft/target [N,gamma,V] at T=1
