@@ -13,6 +13,8 @@
  *                         target's logits: greedy contiguous-prefix argmax
  *                         acceptance, or accept-with-min(1, p/q), residual
  *                         resampling and a bonus token.
+ *   dspark_verify_width   the same over a per-request number of proposals
+ *                         to check (0..gamma).
  *   dspark_accept_stats   the analytical training-side statistics: L1
  *                         distance, acceptance rate, tau and the weighted
  *                         CE / L1 / confidence-BCE numerators.
@@ -23,7 +25,8 @@
  *   [FT] FreeToken PR #69 "[2/3] feat(dsv4): implement exact DSpark
  *        speculative decoding": "End-to-end speculative cycle",
  *        "Checkpoint-faithful DSpark architecture", "Exact decoding
- *        semantics" (Greedy; Probabilistic).
+ *        semantics" (Greedy; Probabilistic), "Scope and limitations" and
+ *        the review thread below it.
  *   [MB] NeMo Megatron-Bridge "DSpark Speculative Decoding (Draft Training)
  *        Design": "Semi-autoregressive draft", "Training objective",
  *        "Acceptance and confidence", "Loss return contract", "Memory
@@ -219,6 +222,33 @@ int dspark_verify(const void* target, int dtype, const int32_t* proposals,
                   int gamma, int V, int32_t* out_tokens, int32_t* num_accepted,
                   int32_t* status, void* workspace, size_t workspace_bytes,
                   void* stream);
+
+/*
+ * dspark_verify_width - dspark_verify over a per-request verify width.
+ *
+ * [FT Scope and limitations, and the review thread]: a serving scheduler
+ * may verify fewer than gamma proposals of a request (0..gamma), choosing the
+ * width from measured draft and verify costs (the pages give no formula, so
+ * the width is an input); [FT Exact decoding semantics] holds at any width.  With width w the request checks x_1..x_w against
+ * target rows 0..w-1 exactly as dspark_verify does, and when all w survive
+ * the bonus token comes from row w at pos0+w+1 (draw 2).  Rows past w are
+ * not read and proposals past x_w are ignored (both may hold anything);
+ * emitted tokens are 1..w+1, and out_tokens is -1 after them.
+ *   width      int32 [B] device, each in [0, gamma]; NULL = gamma for every
+ *              request (exactly dspark_verify).  A width outside [0, gamma]
+ *              fails that request with DSPARK_REQ_BAD_TOKEN (num_accepted -1).
+ * Every other argument, the layouts (still [B, gamma+1, V] and [B, gamma])
+ * and the workspace are those of dspark_verify.  Rows past the width cost a
+ * CTA launch each but move no logit bytes.
+ */
+int dspark_verify_width(const void* target, int dtype, const int32_t* proposals,
+                        const float* q, const float* q_at_x,
+                        const dspark_policy* policy, const uint64_t* seed,
+                        const uint64_t* request_id, const int64_t* pos0,
+                        const int32_t* width, int B, int gamma, int V,
+                        int32_t* out_tokens, int32_t* num_accepted,
+                        int32_t* status, void* workspace,
+                        size_t workspace_bytes, void* stream);
 
 /*
  * dspark_accept_stats - analytical acceptance statistics of a draft against

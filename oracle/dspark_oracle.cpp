@@ -338,6 +338,10 @@ extern "C" void orc_markov_sample(
 // and resample from p; a chi-square test of the emitted-token law against
 // target-only sampling on agreeing, disagreeing and nearly disjoint rows.
 // ---------------------------------------------------------------------------
+// [FT Scope and limitations, and the review thread]: a later change lets the
+// scheduler verify 0..gamma proposals per request, chosen from measured
+// draft and verify costs; the choice has no formula on the pages, so the
+// width is an input here.
 // The verify of each request over its first width[b] proposals (width NULL:
 // all gamma).  A request checks proposals 1..g and reads target rows 0..g
 // (g = its width); every later row and proposal is ignored.  The bonus comes

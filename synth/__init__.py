@@ -282,6 +282,18 @@ def mixed_serving(V=VOCAB, B=256, gamma=5, r=256, H=4096, device="cpu", seed=100
                     extra=dict(adversarial=adv))
 
 
+def verify_widths(B, gamma, seed=1007, invalid=0, device="cpu") -> torch.Tensor:
+    """Per-request verify widths, int32 [B]: uniform over 0..gamma (a
+    scheduler's choice of how many proposals to check; the pages pick it from
+    measured costs, so every width is equally exercised here), with `invalid`
+    requests (chosen by seed) at -1 or gamma + 1."""
+    g = _gen(seed, "cpu")
+    w = torch.randint(0, gamma + 1, (B,), generator=g, dtype=torch.int32)
+    bad = torch.randperm(B, generator=g)[:invalid]
+    w[bad] = torch.where(torch.arange(len(bad)) % 2 == 0, -1, gamma + 1).to(torch.int32)
+    return w.to(device)
+
+
 FLAT_POLICIES = ((1.0, 0, 0.9), (1.0, 5000, 1.0), (1.0, 5000, 0.9), (1.3, 0, 0.5),
                  (0.8, 0, 0.95), (1.0, 0, 1.0), (2.0, 300, 0.9), (1.0, 20000, 0.99))
 

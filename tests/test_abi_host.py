@@ -76,6 +76,22 @@ def test_verify_rejects_invalid_arguments(lib):
     assert _verify(lib, ws_bytes=16, policy=FAKE) == binding.ENOSPC   # sampled path needs workspace
 
 
+def test_verify_width_rejects_invalid_arguments(lib):
+    """dspark_verify_width checks what dspark_verify checks; the widths
+    themselves are data (a bad one fails its request, not the call)."""
+    def call(B=4, gamma=5, V=1024, target=FAKE, props=FAKE, policy=None, ws_bytes=1 << 20, width=FAKE):
+        return lib.dspark_verify_width(target, 0, props, FAKE, FAKE, policy, FAKE, FAKE, FAKE, width, B, gamma,
+                                       V, FAKE, FAKE, FAKE, FAKE, ws_bytes, None)
+    assert call(B=0) == binding.OK
+    assert call(gamma=0) == binding.EINVAL
+    assert call(gamma=17) == binding.EINVAL
+    assert call(V=1001) == binding.EINVAL
+    assert call(target=None) == binding.EINVAL
+    assert call(props=None) == binding.EINVAL
+    assert call(target=FAKE_ODD) == binding.EINVAL
+    assert call(ws_bytes=16, policy=FAKE) == binding.ENOSPC
+
+
 def _markov(lib, B=4, gamma=5, V=1024, r=0, U=None, W=None, policy=None, q=None, h=None, H=0,
             ws_bytes=1 << 20):
     return lib.dspark_markov_sample(FAKE, 0, FAKE, U, W, r, h, 0, FAKE, FAKE, H, policy, FAKE, FAKE,

@@ -20,7 +20,7 @@ BF16, F32 = 0, 1
 OP_MARKOV_SAMPLE, OP_VERIFY, OP_ACCEPT_STATS = 0, 1, 2
 REQ_OK, REQ_NONFINITE, REQ_EMPTY, REQ_TIMEOUT, REQ_BAD_POLICY, REQ_BAD_TOKEN = range(6)
 
-EXPORTED = ("dspark_workspace_size", "dspark_markov_sample", "dspark_verify",
+EXPORTED = ("dspark_workspace_size", "dspark_markov_sample", "dspark_verify", "dspark_verify_width",
             "dspark_accept_stats", "dspark_accept_stats_grad", "dspark_status_string", "dspark_version",
             "dspark_verify_greedy_noalloc")
 
@@ -56,6 +56,9 @@ def load(path: str | None = None):
             lib.dspark_markov_sample.restype = i32
             lib.dspark_verify.argtypes = [P, i32, P, P, P, P, P, P, P] + [i32] * 3 + [P] * 4 + [sz, P]
             lib.dspark_verify.restype = i32
+            lib.dspark_verify_width.argtypes = ([P, i32, P, P, P, P, P, P, P, P] + [i32] * 3 + [P] * 4
+                                                + [sz, P])
+            lib.dspark_verify_width.restype = i32
             lib.dspark_accept_stats.argtypes = ([P, P, i32, P, P, P] + [i32] * 3 + [P] * 8
                                                 + [sz, P])
             lib.dspark_accept_stats.restype = i32
@@ -147,13 +150,19 @@ def _policy_ptr(policy):
 
 # ------------------------------------------------------------------ entry points
 def verify(target, proposals, q=None, q_at_x=None, policy=None, seed=None, request_id=None,
-           pos0=None, out=None, workspace: Workspace | None = None, stream=None):
+           pos0=None, out=None, workspace: Workspace | None = None, stream=None, width=None):
     """Exact verify of [B, gamma+1, V] target logits against [B, gamma]
-    proposals.  Returns (out_tokens [B, gamma+1], num_accepted [B], status [B])."""
+    proposals.  Returns (out_tokens [B, gamma+1], num_accepted [B], status [B]).
+    width: None, or an int32 [B] CUDA tensor of per-request verify widths
+    (0..gamma proposals checked; dspark_verify_width)."""
     _dev(target, "target")
     B, rows, V = target.shape
     gamma = rows - 1
     _dev(proposals, "proposals", torch.int32)
+    if width is not None:
+        _dev(width, "width", torch.int32)
+        if width.shape != (B,):
+            raise ValueError(f"width must have shape ({B},), got {tuple(width.shape)}")
     dev = target.device
     if out is None:
         out = (torch.empty((B, rows), dtype=torch.int32, device=dev),
@@ -162,13 +171,16 @@ def verify(target, proposals, q=None, q_at_x=None, policy=None, seed=None, reque
     # greedy calls (policy None) keep their state on chip and take no workspace
     ws_n = workspace_size(OP_VERIFY, B, gamma, V) if policy is not None else 0
     ws = (workspace or _default_ws).get(OP_VERIFY, ws_n, dev)
-    code = load().dspark_verify(
-        _ptr(target), _dtype_code(target), _ptr(proposals), _ptr(_dev(q, "q", torch.float32)),
-        _ptr(_dev(q_at_x, "q_at_x", torch.float32)), _policy_ptr(policy),
-        _ptr(_dev(seed, "seed", torch.int64)), _ptr(_dev(request_id, "request_id", torch.int64)),
-        _ptr(_dev(pos0, "pos0", torch.int64)), B, gamma, V,
-        _ptr(out[0]), _ptr(out[1]), _ptr(out[2]), _ptr(ws), ws_n, _stream(stream))
-    _check(code, "dspark_verify")
+    args = [_ptr(target), _dtype_code(target), _ptr(proposals), _ptr(_dev(q, "q", torch.float32)),
+            _ptr(_dev(q_at_x, "q_at_x", torch.float32)), _policy_ptr(policy),
+            _ptr(_dev(seed, "seed", torch.int64)), _ptr(_dev(request_id, "request_id", torch.int64)),
+            _ptr(_dev(pos0, "pos0", torch.int64))]
+    tail = [B, gamma, V, _ptr(out[0]), _ptr(out[1]), _ptr(out[2]), _ptr(ws), ws_n, _stream(stream)]
+    if width is None:
+        code, what = load().dspark_verify(*args, *tail), "dspark_verify"
+    else:
+        code, what = load().dspark_verify_width(*args, _ptr(width), *tail), "dspark_verify_width"
+    _check(code, what)
     return out
 
 

@@ -111,11 +111,11 @@ size_t dspark_workspace_size(int op, int B, int gamma, int V, int r, int H) {
     }
 }
 
-int dspark_verify(const void* target, int dtype, const int32_t* proposals, const float* q,
-                  const float* q_at_x, const dspark_policy* policy, const uint64_t* seed,
-                  const uint64_t* request_id, const int64_t* pos0, int B, int gamma, int V,
-                  int32_t* out_tokens, int32_t* num_accepted, int32_t* status, void* workspace,
-                  size_t workspace_bytes, void* stream) {
+int dspark_verify_width(const void* target, int dtype, const int32_t* proposals, const float* q,
+                        const float* q_at_x, const dspark_policy* policy, const uint64_t* seed,
+                        const uint64_t* request_id, const int64_t* pos0, const int32_t* width, int B,
+                        int gamma, int V, int32_t* out_tokens, int32_t* num_accepted, int32_t* status,
+                        void* workspace, size_t workspace_bytes, void* stream) {
     if (!valid_common(B, gamma, V, dtype)) return DSPARK_EINVAL;
     if (B == 0) return DSPARK_OK;
     if (!target || !proposals || !out_tokens || !num_accepted || !status) return DSPARK_EINVAL;
@@ -147,7 +147,7 @@ int dspark_verify(const void* target, int dtype, const int32_t* proposals, const
         vp.status = status;
         vp.records = at<RowRecord>(workspace, lay.records);
         vp.ticket = at<unsigned int>(workspace, lay.ticket);
-        return launch_verify_prob(vp, s) == cudaSuccess ? DSPARK_OK : DSPARK_ECUDA;
+        return launch_verify_prob(vp, s, width) == cudaSuccess ? DSPARK_OK : DSPARK_ECUDA;
     }
 
     ArgmaxParams p{};
@@ -161,7 +161,16 @@ int dspark_verify(const void* target, int dtype, const int32_t* proposals, const
     p.out_tokens = out_tokens;
     p.num_accepted = num_accepted;
     p.status = status;
-    return launch_argmax_rows(p, B, s) == cudaSuccess ? DSPARK_OK : DSPARK_ECUDA;
+    return launch_argmax_rows(p, B, s, width) == cudaSuccess ? DSPARK_OK : DSPARK_ECUDA;
+}
+
+int dspark_verify(const void* target, int dtype, const int32_t* proposals, const float* q,
+                  const float* q_at_x, const dspark_policy* policy, const uint64_t* seed,
+                  const uint64_t* request_id, const int64_t* pos0, int B, int gamma, int V,
+                  int32_t* out_tokens, int32_t* num_accepted, int32_t* status, void* workspace,
+                  size_t workspace_bytes, void* stream) {
+    return dspark_verify_width(target, dtype, proposals, q, q_at_x, policy, seed, request_id, pos0, nullptr, B,
+                               gamma, V, out_tokens, num_accepted, status, workspace, workspace_bytes, stream);
 }
 
 int dspark_markov_sample(const void* backbone, int dtype, const int32_t* anchor, const uint16_t* U,

@@ -4,7 +4,9 @@
 //  * Greedy verify [FT Exact decoding semantics > Greedy; PT Speculative
 //    decoding (K=7) > Acceptance]: a_i = argmax of target row i (lowest index
 //    on ties); n = length of the prefix with x_k == a_{k-1}; emit x_1..x_n
-//    then a_n.
+//    then a_n.  The width variant (kWidth) checks x_1..x_w of each request
+//    (w = its width, 0..gamma): only rows 0..w are streamed and the prefix
+//    stops at w.
 //  * Greedy drafting without a Markov bias (r = 0): x_k = argmax of backbone
 //    row k.
 //
@@ -25,6 +27,8 @@
 // CTA makes the request's decision with one lane per row.  Nothing goes
 // through global memory but the logits and the outputs, so the kernel needs
 // no workspace.
+
+#include <type_traits>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -131,19 +135,29 @@ __device__ __forceinline__ void cluster_wait_acquire() {
 // ------------------------------------------------------- the decision
 // All 32 lanes of one warp; lane i < G holds row i's merged key k and flags
 // f; for verify lane k < gamma holds the proposal x_{k+1}, for drafting every
-// lane holds the anchor.
-__device__ void decide(const ArgmaxParams& p, int64_t g, uint64_t k, uint32_t f, int32_t x, int lane) {
+// lane holds the anchor.  kWidth: the request checks x_1..x_w (rows 0..w were
+// read); a width outside [0, gamma] fails it as a bad token.
+template <bool kWidth>
+__device__ void decide(const ArgmaxParams& p, int64_t g, int w, uint64_t k, uint32_t f, int32_t x, int lane) {
     const int G = p.rows_per_group;
     const int gamma = p.gamma;
-    const int32_t st = lane < G ? row_status(k, f) : kReqOk;
+    bool w_ok = true;
+    int live = G;  // rows whose status counts
+    if constexpr (kWidth) {
+        w_ok = w >= 0 && w <= gamma;
+        live = w_ok ? w + 1 : 0;
+    } else {
+        w = gamma;
+    }
+    const int32_t st = lane < live ? row_status(k, f) : kReqOk;
     const int32_t a = key_index(k);
-    const unsigned badrow = __ballot_sync(0xFFFFFFFFu, lane < G && st != kReqOk);
+    const unsigned badrow = __ballot_sync(0xFFFFFFFFu, lane < live && st != kReqOk);
 
     if (p.mode == kArgmaxVerify) {
         int32_t* out = p.out_tokens + g * (gamma + 1);
-        const unsigned badtok = __ballot_sync(0xFFFFFFFFu, lane < gamma && (x < 0 || x >= p.V));
+        const unsigned badtok = __ballot_sync(0xFFFFFFFFu, lane < w && (x < 0 || x >= p.V));
         int32_t status = kReqOk;
-        if (badtok) status = kReqBadToken;
+        if (!w_ok || badtok) status = kReqBadToken;
         else if (badrow) status = __shfl_sync(0xFFFFFFFFu, st, __ffs(badrow) - 1);
         if (status != kReqOk) {
             if (lane <= gamma) out[lane] = -1;
@@ -154,8 +168,8 @@ __device__ void decide(const ArgmaxParams& p, int64_t g, uint64_t k, uint32_t f,
             return;
         }
         // accepted prefix: the first k with x_k != a_{k-1} ends it
-        const unsigned mismatch = __ballot_sync(0xFFFFFFFFu, lane < gamma && x != a);
-        const int n = mismatch ? __ffs(mismatch) - 1 : gamma;
+        const unsigned mismatch = __ballot_sync(0xFFFFFFFFu, lane < w && x != a);
+        const int n = mismatch ? __ffs(mismatch) - 1 : w;
         const int32_t an = __shfl_sync(0xFFFFFFFFu, a, n);
         if (lane <= gamma) out[lane] = lane < n ? x : (lane == n ? an : -1);
         if (lane == 0) {
@@ -315,8 +329,11 @@ struct StageWalk {
     }
 };
 
-template <int kDtype>
-__global__ void __launch_bounds__(kThreads, kCtasPerSm) argmax_rows_kernel(const ArgmaxParams p) {
+template <bool kWidth>
+using ArgmaxArgs = std::conditional_t<kWidth, ArgmaxWidthParams, ArgmaxParams>;
+
+template <int kDtype, bool kWidth>
+__global__ void __launch_bounds__(kThreads, kCtasPerSm) argmax_rows_kernel(const ArgmaxArgs<kWidth> p) {
     extern __shared__ __align__(128) uint8_t ring[];
     __shared__ ArgmaxSmem sm;
     constexpr int kPer = kDtype == kBF16 ? 8 : 4;
@@ -326,8 +343,16 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) argmax_rows_kernel(const
     const int G = p.rows_per_group;
     const int64_t V = p.V;
     const int64_t glen = static_cast<int64_t>(G) * V;
-    const int64_t lo = min(glen, static_cast<int64_t>(q) * p.per);  // request-relative element range
-    const int64_t hi = min(glen, lo + p.per);
+    // elements of the request that are read: every row, or rows 0..w of the
+    // width variant (none for an invalid width)
+    int w = 0;
+    int64_t gread = glen;
+    if constexpr (kWidth) {
+        w = p.width[g];
+        gread = w >= 0 && w <= p.gamma ? static_cast<int64_t>(w + 1) * V : 0;
+    }
+    const int64_t lo = min(gread, static_cast<int64_t>(q) * p.per);  // request-relative element range
+    const int64_t hi = min(gread, lo + p.per);
     const int64_t vpr = V / kPer;    // vectors per row (V is a multiple of 8)
     const int64_t v_lo = lo / kPer;  // request-relative vector index of the range start
     const int64_t v_hi = hi / kPer;
@@ -481,26 +506,27 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) argmax_rows_kernel(const
                 }
             }
             const int32_t x = p.mode == kArgmaxVerify ? (lane < p.gamma ? sm.x[lane] : 0) : sm.x[0];
-            decide(p, g, k, f, x, lane);
+            decide<kWidth>(p, g, w, k, f, x, lane);
         }
     }
 }
 
-template <int kDtype>
+template <int kDtype, bool kWidth = false>
 const void* kernel_ptr() {
-    return reinterpret_cast<const void*>(&argmax_rows_kernel<kDtype>);
+    return reinterpret_cast<const void*>(&argmax_rows_kernel<kDtype, kWidth>);
 }
 
 // Opt the kernels into the ring's dynamic shared memory (once per device).
-cudaError_t prepare_argmax(int dtype) {
+cudaError_t prepare_argmax(int dtype, bool width = false) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    static bool ready[64][2] = {};
-    if (dev < 64 && ready[dev][dtype]) return cudaSuccess;
-    const void* f = dtype == kBF16 ? kernel_ptr<kBF16>() : kernel_ptr<kF32>();
+    static bool ready[64][2][2] = {};
+    if (dev < 64 && ready[dev][dtype][width]) return cudaSuccess;
+    const void* f = width ? (dtype == kBF16 ? kernel_ptr<kBF16, true>() : kernel_ptr<kF32, true>())
+                          : (dtype == kBF16 ? kernel_ptr<kBF16>() : kernel_ptr<kF32>());
     e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kRingBytes);
-    if (e == cudaSuccess && dev < 64) ready[dev][dtype] = true;
+    if (e == cudaSuccess && dev < 64) ready[dev][dtype][width] = true;
     return e;
 }
 
@@ -548,21 +574,32 @@ int argmax_cluster_size(int dtype, int groups) {
     return c;
 }
 
-cudaError_t launch_argmax_rows(ArgmaxParams p, int groups, cudaStream_t stream) {
+cudaError_t launch_argmax_rows(ArgmaxParams p, int groups, cudaStream_t stream, const int32_t* width) {
     if (groups <= 0) return cudaSuccess;
     if (p.rows_per_group < 1 || p.rows_per_group > kMaxRows || p.gamma < 1 || p.gamma > kMaxRows - 2)
         return cudaErrorInvalidValue;
+    if (width && p.mode != kArgmaxVerify) return cudaErrorInvalidValue;
     cudaError_t e = prepare_argmax(p.dtype);
+    if (e == cudaSuccess && width) e = prepare_argmax(p.dtype, true);
     if (e != cudaSuccess) return e;
     const int c = argmax_cluster_size(p.dtype, groups);
     const int64_t glen = static_cast<int64_t>(p.rows_per_group) * p.V;
     p.per = ((glen + c - 1) / c + 7) / 8 * 8;  // elements per CTA: ranges start on 16-byte boundaries
     cudaLaunchAttribute attr[1];
     const cudaLaunchConfig_t cfg = launch_config(groups, c, stream, attr);
-    if (p.dtype == kBF16)
-        e = cudaLaunchKernelEx(&cfg, argmax_rows_kernel<kBF16>, p);
-    else
-        e = cudaLaunchKernelEx(&cfg, argmax_rows_kernel<kF32>, p);
+    if (width) {
+        ArgmaxWidthParams pw;
+        static_cast<ArgmaxParams&>(pw) = p;
+        pw.width = width;
+        if (p.dtype == kBF16)
+            e = cudaLaunchKernelEx(&cfg, argmax_rows_kernel<kBF16, true>, pw);
+        else
+            e = cudaLaunchKernelEx(&cfg, argmax_rows_kernel<kF32, true>, pw);
+    } else if (p.dtype == kBF16) {
+        e = cudaLaunchKernelEx(&cfg, argmax_rows_kernel<kBF16, false>, p);
+    } else {
+        e = cudaLaunchKernelEx(&cfg, argmax_rows_kernel<kF32, false>, p);
+    }
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 

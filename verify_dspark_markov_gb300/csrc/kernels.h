@@ -29,7 +29,14 @@ struct ArgmaxParams {
     float* q_at_x;
     int32_t* status;
 };
-cudaError_t launch_argmax_rows(ArgmaxParams p, int groups, cudaStream_t stream);
+// Greedy verify over a per-request width: the same block plus the widths, a
+// type of its own so that the fixed-width kernel keeps its parameter block.
+struct ArgmaxWidthParams : ArgmaxParams {
+    const int32_t* width;     // [groups] proposals each request checks (0..gamma)
+};
+// width null: the fixed-width kernel; otherwise (verify mode) its width variant
+cudaError_t launch_argmax_rows(ArgmaxParams p, int groups, cudaStream_t stream,
+                               const int32_t* width = nullptr);
 int argmax_cluster_size(int dtype, int groups);
 
 // Confidence head c_k = sigmoid(w[:H] . h_k + w[H:] . E[x_{k-1}]) (confidence.cu).
@@ -134,7 +141,12 @@ cudaError_t launch_markov_bias(const MarkovGemmParams& p, const MarkovGemmPlan& 
 int verify_slice(int V);
 int step_slice(int V);
 int policy_smem_bytes(int V, int store_bf16);
-cudaError_t launch_verify_prob(const VerifyProbParams& p, cudaStream_t stream);
+struct VerifyWidthParams : VerifyProbParams {
+    const int32_t* width;      // [B] proposals each request checks (0..gamma)
+};
+// width null: the fixed-width kernel; otherwise its width variant
+cudaError_t launch_verify_prob(const VerifyProbParams& p, cudaStream_t stream,
+                               const int32_t* width = nullptr);
 cudaError_t launch_markov_step(const MarkovStepParams& p, cudaStream_t stream);
 
 // Acceptance statistics (accept_stats.cu).

@@ -11,11 +11,16 @@
 //    token from normalised max(p - q, 0) at the first rejection, or the bonus
 //    token from the last target row, by an exact inverse CDF in token order.
 //    Greedy requests in the batch take the contiguous-prefix argmax rule.
+//    The width variant (kWidth) checks x_1..x_w of each request (w = its
+//    width, 0..gamma): rows past w take their ticket without reading logits,
+//    and the bonus comes from row w.
 //  * markov_step_kernel - one left-to-right step of the draft's sequential
 //    head [FT Checkpoint-faithful DSpark architecture]: q_k = policy(z_k),
 //    written in full, and x_k drawn from it (greedy: the argmax).
 
 #include <cooperative_groups.h>
+
+#include <type_traits>
 
 #include "kernels.h"
 #include "row_policy.cuh"
@@ -38,15 +43,19 @@ __device__ __forceinline__ float inv_mass(uint64_t mass) {
 // the per-warp histogram counts.  The row slices are read in place from
 // global memory.
 
-template <int kDtype>
+template <bool kWidth>
+using VerifyArgs = std::conditional_t<kWidth, VerifyWidthParams, VerifyProbParams>;
+
+template <int kDtype, bool kWidth>
 __global__ void __cluster_dims__(kVerifyC, 1, 1) __launch_bounds__(rp::kThreads, 4)
-    verify_rows_kernel(const VerifyProbParams p) {
+    verify_rows_kernel(const VerifyArgs<kWidth> p) {
     extern __shared__ __align__(16) unsigned char dyn[];
     __shared__ rp::Smem sm;
     __shared__ float s_px;          // p(x) of this row's proposal, in its owner CTA
     __shared__ int32_t s_last;      // rank 0: this cluster decides the request
     __shared__ int32_t s_plan[4];   // rank 0: (row to draw from, rejected position, token, -)
     __shared__ int32_t s_bcast[4];
+    __shared__ int32_t s_w;         // kWidth: the request's width
     cg::cluster_group cl = cg::this_cluster();
     const int rank = static_cast<int>(cl.block_rank());
     const int tid = threadIdx.x;
@@ -58,14 +67,20 @@ __global__ void __cluster_dims__(kVerifyC, 1, 1) __launch_bounds__(rp::kThreads,
         s_last = 0;
         s_plan[0] = -1;
         s_plan[1] = 0;
+        if constexpr (kWidth) s_w = p.width[blockIdx.x / kVerifyC / (p.gamma + 1)];
     }
     __syncthreads();
 
     const int rows = p.gamma + 1;
     const int64_t row = blockIdx.x / kVerifyC;
     const int b = static_cast<int>(row / rows), i = static_cast<int>(row % rows);
+    // kWidth: rows 0..w-1 score x_1..x_w and row w gives the bonus; a row
+    // past w (every row, for an invalid width) gets an empty slice, reads
+    // nothing, reports "empty", and the decision never looks at its record
+    bool live = true;
+    if constexpr (kWidth) live = s_w >= 0 && s_w <= p.gamma && i <= s_w;
     const int lo = rank * p.slice;
-    const int n = max(0, min(p.slice, p.V - lo));
+    const int n = live ? max(0, min(p.slice, p.V - lo)) : 0;
     const int esize = kDtype == kBF16 ? 2 : 4;
     const char* tgt = static_cast<const char*>(p.target);
     rp::Slice sl{tgt + (row * p.V + lo) * esize, lo, n, (n + kThreads - 1) / kThreads, kStoreBf16};
@@ -80,9 +95,13 @@ __global__ void __cluster_dims__(kVerifyC, 1, 1) __launch_bounds__(rp::kThreads,
     res.in_buf = 0;
     if (res.status == kReqOk) rp::row_policy(sm, cl, sl, p.V, pol, res, cbuf);
 
-    // p(x) of the proposal scored by this row (rows 0..gamma-1), in its owner CTA
+    // p(x) of the proposal scored by this row (rows 0..gamma-1, or 0..w-1), in its owner CTA
     int32_t x = -1;
-    if (i < p.gamma) x = p.proposals[b * p.gamma + i];
+    if constexpr (kWidth) {
+        if (live && i < s_w) x = p.proposals[b * p.gamma + i];
+    } else {
+        if (i < p.gamma) x = p.proposals[b * p.gamma + i];
+    }
     const bool x_ok = x >= 0 && x < p.V;
     const int owner = x_ok ? x / p.slice : 0;
     if (res.status == kReqOk && !pol.greedy && x_ok && rank == owner && tid == 0) {
@@ -122,11 +141,19 @@ __global__ void __cluster_dims__(kVerifyC, 1, 1) __launch_bounds__(rp::kThreads,
         p.ticket[b] = 0u;  // leave the workspace zero-filled
         const RowRecord* rec = p.records + static_cast<int64_t>(b) * rows;
         const int32_t* xs = p.proposals + b * p.gamma;
-        int32_t status = kReqOk;
-        for (int k = 0; k < p.gamma; ++k)
+        // proposals checked: gamma, or the width (0 with a failed status
+        // when it lies outside [0, gamma])
+        int wd = p.gamma;
+        bool w_ok = true;
+        if constexpr (kWidth) {
+            w_ok = s_w >= 0 && s_w <= p.gamma;
+            wd = w_ok ? s_w : 0;
+        }
+        int32_t status = w_ok ? kReqOk : kReqBadToken;
+        for (int k = 0; k < wd; ++k)
             if (xs[k] < 0 || xs[k] >= p.V) status = kReqBadToken;
         if (status == kReqOk)
-            for (int r = 0; r < rows; ++r)
+            for (int r = 0; r < wd + 1; ++r)
                 if (rec[r].status != kReqOk) { status = rec[r].status; break; }
         if (status != kReqOk) {
             for (int r = 0; r < rows; ++r) out[r] = -1;
@@ -134,13 +161,13 @@ __global__ void __cluster_dims__(kVerifyC, 1, 1) __launch_bounds__(rp::kThreads,
             p.status[b] = status;
         } else if (pol.greedy) {
             int nacc = 0;
-            while (nacc < p.gamma && xs[nacc] == rec[nacc].argmax) ++nacc;
+            while (nacc < wd && xs[nacc] == rec[nacc].argmax) ++nacc;
             for (int r = 0; r < rows; ++r) out[r] = r < nacc ? xs[r] : (r == nacc ? rec[nacc].argmax : -1);
             p.num_accepted[b] = nacc;
             p.status[b] = kReqOk;
         } else {
             int j = 0;  // first rejected position (1-based), 0 = none
-            for (int k = 1; k <= p.gamma; ++k) {
+            for (int k = 1; k <= wd; ++k) {
                 const float pk = rec[k - 1].p_x;
                 const float qk = p.q_at_x[b * p.gamma + (k - 1)];
                 const float ratio = qk > 0.0f ? pk / qk : (pk > 0.0f ? __int_as_float(0x7F800000) : 0.0f);
@@ -148,8 +175,8 @@ __global__ void __cluster_dims__(kVerifyC, 1, 1) __launch_bounds__(rp::kThreads,
                 if (!(pk > 0.0f && u < ratio)) { j = k; break; }
             }
             for (int r = 0; r < rows; ++r) out[r] = -1;
-            for (int r = 0; r < (j ? j - 1 : p.gamma); ++r) out[r] = xs[r];
-            s_plan[0] = j ? j - 1 : p.gamma;  // target row to draw from
+            for (int r = 0; r < (j ? j - 1 : wd); ++r) out[r] = xs[r];
+            s_plan[0] = j ? j - 1 : wd;  // target row to draw from
             s_plan[1] = j;                    // residual against q_j when j > 0
         }
     }
@@ -162,10 +189,13 @@ __global__ void __cluster_dims__(kVerifyC, 1, 1) __launch_bounds__(rp::kThreads,
         // draw the residual / bonus token from target row R of request b
         const RowRecord rr = p.records[static_cast<int64_t>(b) * rows + R];
         const int64_t trow = static_cast<int64_t>(b) * rows + R;
-        const rp::Slice sr{tgt + (trow * p.V + lo) * esize, lo, n, (n + kThreads - 1) / kThreads, kStoreBf16};
+        // (the deciding cluster may have had a row past the width: its own
+        // slice was empty, row R's is not)
+        const int nr = kWidth ? max(0, min(p.slice, p.V - lo)) : n;
+        const rp::Slice sr{tgt + (trow * p.V + lo) * esize, lo, nr, (nr + kThreads - 1) / kThreads, kStoreBf16};
         const float invS = inv_mass(rr.mass);
         const float* qrow = j ? p.q + (static_cast<int64_t>(b) * p.gamma + (j - 1)) * p.V : nullptr;
-        const int64_t pos = p.pos0[b] + (j ? j : p.gamma + 1);
+        const int64_t pos = p.pos0[b] + (j ? j : (kWidth ? s_w : p.gamma) + 1);
         const uint32_t m24 = uniform_bits24(p.seed[b], p.request_id[b], pos, 2);
         // p of a support element, its fixed-point weight and residual weight
         auto pw = [&](uint32_t key) { return rp::to_fixed(rp::weight_f(key_to_float(key), rr.zmax, rr.inv_t)); };
@@ -410,18 +440,26 @@ int policy_smem_bytes(int V, int store_bf16) {
            rp::kWarps * rp::kBins * static_cast<int>(sizeof(uint32_t));
 }
 
-cudaError_t launch_verify_prob(const VerifyProbParams& p, cudaStream_t stream) {
+template <int kDtype, bool kWidth>
+cudaError_t launch_verify_rows(const VerifyArgs<kWidth>& p, int smem, dim3 grid, cudaStream_t stream) {
+    const cudaError_t e = set_smem(verify_rows_kernel<kDtype, kWidth>, smem);
+    if (e != cudaSuccess) return e;
+    verify_rows_kernel<kDtype, kWidth><<<grid, kThreads, smem, stream>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_verify_prob(const VerifyProbParams& p, cudaStream_t stream, const int32_t* width) {
     const int smem = policy_smem_bytes(p.V, p.dtype == kBF16);
     const dim3 grid(static_cast<unsigned>(static_cast<int64_t>(p.B) * (p.gamma + 1) * kVerifyC));
-    cudaError_t e;
-    if (p.dtype == kBF16) {
-        if ((e = set_smem(verify_rows_kernel<kBF16>, smem)) != cudaSuccess) return e;
-        verify_rows_kernel<kBF16><<<grid, kThreads, smem, stream>>>(p);
-    } else {
-        if ((e = set_smem(verify_rows_kernel<kF32>, smem)) != cudaSuccess) return e;
-        verify_rows_kernel<kF32><<<grid, kThreads, smem, stream>>>(p);
+    if (width) {
+        VerifyWidthParams pw;
+        static_cast<VerifyProbParams&>(pw) = p;
+        pw.width = width;
+        return p.dtype == kBF16 ? launch_verify_rows<kBF16, true>(pw, smem, grid, stream)
+                                : launch_verify_rows<kF32, true>(pw, smem, grid, stream);
     }
-    return cudaGetLastError();
+    return p.dtype == kBF16 ? launch_verify_rows<kBF16, false>(p, smem, grid, stream)
+                            : launch_verify_rows<kF32, false>(p, smem, grid, stream);
 }
 
 cudaError_t launch_markov_step(const MarkovStepParams& p, cudaStream_t stream) {
