@@ -120,3 +120,31 @@ def test_width_ignores_rows_past_it(oracle):
                         width=np.array([2, 3, gamma + 1, -1], np.int32))
     assert res["status"].tolist() == [0, 0, 5, 5]
     assert res["num_accepted"].tolist()[:2] == [2, 3]
+
+
+@pytest.mark.parametrize("policy", ["sampled", "greedy"])
+def test_width_is_the_truncated_block(oracle, policy):
+    """Verifying at width w is the fixed-width verify of the block cut to
+    x_1..x_w and target rows 0..w, under the same keys: the accept tests, the
+    residual and the bonus draw at the same positions.  The tail past w is -1."""
+    V, gamma, B = 64, 4, 96
+    rng = np.random.default_rng(27)
+    t = rng.normal(0, 2.0, (B, gamma + 1, V)).astype(np.float32)
+    d_logits = t[:, :gamma] + rng.normal(0, 1.0, (B, gamma, V))
+    q = np.exp(d_logits - d_logits.max(-1, keepdims=True))
+    q = (q / q.sum(-1, keepdims=True)).astype(np.float32)
+    x = np.array([[rng.choice(V, p=q[b, k] / q[b, k].sum()) for k in range(gamma)] for b in range(B)], np.int32)
+    qx = np.take_along_axis(q, x[..., None], 2)[..., 0]
+    pol = synth.uniform_policy(B, greedy=policy == "greedy").numpy()
+    keys = synth.make_keys(B, seed=9, pos0=1000).numpy()
+    for w in range(1, gamma + 1):
+        res = oracle.verify(t, x, q, qx, pol, **keys, width=np.full(B, w, np.int32))
+        cut = oracle.verify(np.ascontiguousarray(t[:, :w + 1]), np.ascontiguousarray(x[:, :w]),
+                            np.ascontiguousarray(q[:, :w]), np.ascontiguousarray(qx[:, :w]), pol, **keys)
+        np.testing.assert_array_equal(res["status"], cut["status"])
+        np.testing.assert_array_equal(res["num_accepted"], cut["num_accepted"])
+        np.testing.assert_array_equal(res["out_tokens"][:, :w + 1], cut["out_tokens"])
+        assert np.all(res["out_tokens"][:, w + 1:] == -1)
+        # the accept tests are live: some requests stop early, some run to w
+        if policy == "sampled":
+            assert (res["num_accepted"] < w).any() and (res["num_accepted"] == w).any()
