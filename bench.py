@@ -14,6 +14,10 @@ in HBM when the timed region starts.  Workloads (``--workload``):
                      confidences) then the sampled verify.
   mixed_serving      256 requests, gamma = 5, per-request policies, 25 %
                      greedy, 10 % adversarial drafts, rank 256.
+  decode_verify_tile_width  the decode verify tile with a per-request verify
+                     width uniform over 0..gamma (seeded): the draft of gamma
+                     positions, then the verify of x_1..x_w and the bonus from
+                     row w; positions = the sum of (w + 1).
   training_stats     4096 blocks x gamma = 7 fp32 row pairs: L1, accept rate,
                      tau and the weighted loss numerators.
   training_stats_grad  the same row pairs: the gradient of the loss numerators'
@@ -145,9 +149,10 @@ class Clocks:
 class Serving:
     """Draft sampling then exact verify of one batch."""
 
-    def __init__(self, name, w, esize):
+    def __init__(self, name, w, esize, width=None):
         self.name, self.w, self.esize = name, w, esize
-        self.positions = w.B * (w.gamma + 1)
+        self.width = width  # int32 [B] verify widths, or None (gamma for every request)
+        self.positions = w.B * (w.gamma + 1) if width is None else int((width.cpu().long() + 1).sum())
         self.greedy_only = bool(w.policy.greedy.all()) and w.weights.r == 0
 
     def config(self):
@@ -155,7 +160,11 @@ class Serving:
         return {"workload": self.name, "requests": w.B, "gamma": w.gamma, "vocab": w.V,
                 "target_rows": w.B * (w.gamma + 1), "draft_rows": w.B * w.gamma,
                 "policy": "greedy" if self.greedy_only else "per-request temperature / top-k / top-p",
-                "markov_rank": w.weights.r, "draft_hidden": w.weights.H}
+                "markov_rank": w.weights.r, "draft_hidden": w.weights.H,
+                **({} if self.width is None else {
+                    "verify_width": f"per request, uniform over 0..{w.gamma} (seeded; mean "
+                                    f"{float(self.width.float().mean()):.2f} proposals checked)",
+                    "verified_rows": self.positions})}
 
     def setup(self, ds, dev):
         w = self.w
@@ -173,7 +182,16 @@ class Serving:
         self.ver_out = (torch.empty((B, g + 1), dtype=torch.int32, device=dev),
                         torch.empty((B,), dtype=torch.int32, device=dev),
                         torch.empty((B,), dtype=torch.int32, device=dev))
-        self.inputs = [w.backbone, w.target, w.anchor] + ([w.h] if w.h is not None else [])
+        self.width_dev = None if self.width is None else self.width.to(dev)
+        # the step's inputs, in the order e2e_step unpacks them
+        self.inputs = [w.backbone, w.target, w.anchor]
+        self.h_at = self.width_at = None
+        if w.h is not None:
+            self.h_at = len(self.inputs)
+            self.inputs.append(w.h)
+        if self.width_dev is not None:
+            self.width_at = len(self.inputs)
+            self.inputs.append(self.width_dev)
 
     def draft(self, stream, backbone=None, anchor=None, h=None):
         w = self.w
@@ -183,11 +201,12 @@ class Serving:
                               h=h if h is not None else w.h, policy=self.pol, workspace=self.ws, out=d,
                               stream=stream, **self.wts, **(self.keys if self.pol is not None else {}))
 
-    def verify(self, stream, target=None):
+    def verify(self, stream, target=None, width=None):
         d = self.draft_out
         self.ds.verify(target if target is not None else self.w.target, d["proposals"], q=d["q"],
                        q_at_x=d["q_at_x"] if self.pol is not None else None, policy=self.pol,
                        workspace=self.ws, out=self.ver_out, stream=stream,
+                       width=width if width is not None else self.width_dev,
                        **(self.keys if self.pol is not None else {}))
 
     def parts(self):
@@ -204,11 +223,16 @@ class Serving:
                  + B * g * (H * 2 * 2 if w.h is not None else 0)  # h and E rows for c_k
                  + B * 4 + B * g * 12)              # anchors, proposals, q(x), c_k
         rejecting = 0
+        checked = g if self.width is None else self.width.cpu()
         if self.pol is not None:
             nacc = self.ver_out[1].cpu()
             greedy = self.w.policy.greedy.cpu() != 0
-            rejecting = int(((nacc < g) & (nacc >= 0) & ~greedy).sum())
-        verify = (B * (g + 1) * V * e + rejecting * V * 4 + B * g * 8 + B * (g + 1) * 4 + B * 8)
+            rejecting = int(((nacc < checked) & (nacc >= 0) & ~greedy).sum())
+        # target rows 0..w of every request, the residual's q row at a
+        # rejection, proposals and q(x), outputs, keys (and the widths)
+        rows = self.positions
+        verify = (rows * V * e + rejecting * V * 4 + B * g * 8 + B * (g + 1) * 4 + B * 8
+                  + (0 if self.width is None else B * 4))
         return {"draft": draft, "verify": verify}
 
     def flops(self):
@@ -219,9 +243,10 @@ class Serving:
         for d, h in zip(dev_inputs, host_inputs):
             d.copy_(h, non_blocking=True)
         backbone, target, anchor = dev_inputs[:3]
-        h = dev_inputs[3] if len(dev_inputs) > 3 else None
+        h = dev_inputs[self.h_at] if self.h_at is not None else None
+        width = dev_inputs[self.width_at] if self.width_at is not None else None
         self.draft(stream, backbone=backbone, anchor=anchor, h=h)
-        self.verify(stream, target=target)
+        self.verify(stream, target=target, width=width)
         for h, d in zip(host_outputs, self.ver_out):
             h.copy_(d, non_blocking=True)
 
@@ -247,22 +272,25 @@ class Serving:
         hh = synth.host(w.h) if w.h is not None else None
         E = synth.host(w.weights.E) if w.h is not None else None
         wc = w.weights.w_conf.cpu().numpy() if w.h is not None else None
-        done, b, t0 = 0, 0, time.perf_counter()
+        wd = None if self.width is None else self.width.cpu().numpy().astype(np.int32)
+        done, pos, b, t0 = 0, 0, 0, time.perf_counter()
         while True:
             sl = slice(b, b + 1)
             k = {n: v[sl] for n, v in keys.items()}
             p = {n: v[sl] for n, v in pol.items()}
             d = oracle.markov_sample(bb[sl], anchor[sl], U, Wm, None if hh is None else hh[sl], E, wc, p, **k)
-            oracle.verify(tg[sl], d["proposals"], d["q"], d["q_at_x"], p, **k)
+            oracle.verify(tg[sl], d["proposals"], d["q"], d["q_at_x"], p, **k,
+                          width=None if wd is None else wd[sl])
             done += 1
+            pos += w.gamma + 1 if wd is None else int(wd[b]) + 1
             b = (b + 1) % w.B
             el = time.perf_counter() - t0
             if el >= budget_s or (max_requests and done >= max_requests):
                 break
-        pos = done * (w.gamma + 1)
+        rows = f"{w.gamma + 1} rows each" if wd is None else "w + 1 rows each at the request's width w"
         return {"value": pos / el, "unit": UNIT, "cores": 1, "kind": "oracle",
                 "sample": f"{done} whole requests of the workload (draft of {w.gamma} rows + verify of "
-                          f"{w.gamma + 1} rows each; {pos} verified positions) in {el:.1f} s, "
+                          f"{rows}; {pos} verified positions) in {el:.1f} s, "
                           f"single-threaded C++ oracle"}
 
 
@@ -409,6 +437,9 @@ def make_workload(name, device, stats_blocks=4096):
         return Serving(name, synth.decode_verify_tile(device=device), 2)
     if name == "mixed_serving":
         return Serving(name, synth.mixed_serving(device=device), 2)
+    if name == "decode_verify_tile_width":
+        w = synth.decode_verify_tile(device=device)
+        return Serving(name, w, 2, width=synth.verify_widths(w.B, w.gamma))
     if name == "training_stats":
         return Stats(synth.training_stats(device=device, N=stats_blocks))
     if name == "training_stats_grad":
@@ -416,7 +447,8 @@ def make_workload(name, device, stats_blocks=4096):
     raise ValueError(name)
 
 
-WORKLOADS = ("full_decode_tile", "decode_verify_tile", "mixed_serving", "training_stats", "training_stats_grad")
+WORKLOADS = ("full_decode_tile", "decode_verify_tile", "mixed_serving", "decode_verify_tile_width",
+             "training_stats", "training_stats_grad")
 
 
 # ------------------------------------------------------------------ GPU arm
@@ -513,7 +545,8 @@ def run_gpu(args):
               "training_stats": "stats_pairs_kernel<f32> (+ stats_blocks_kernel, stats_total_kernel)",
               "training_stats_grad": "stats_grad_kernel<f32>"}.get(
                   wl.name, {"draft": "markov_sample (markov_bias_kernel + markov_step_kernel per position)",
-                            "verify": "verify_rows_kernel<bf16>"}.get(dom, dom))
+                            "verify": "verify_rows_kernel<bf16>" if getattr(wl, "width", None) is None
+                            else "verify_rows_kernel<bf16, width>"}.get(dom, dom))
     if wl.name == "full_decode_tile":  # the same kernel serves both parts: average over both launches
         achieved = sum(nbytes.values()) / (sum(part_ms.values()) * 1e-3) / 1e9
     result = {
