@@ -62,6 +62,9 @@ def _load():
             lib.orc_markov_sample.argtypes = ([P, i32, P, P, P, i32, P, i32, P, P, i32]
                                               + [P] * 7 + [i32, i32, i32] + [P] * 6)
             lib.orc_markov_sample.restype = None
+            lib.orc_rnn_sample.argtypes = ([P, i32, P, P, P, i32, P, P, P, P, P, i32, P, P, i32]
+                                           + [P] * 7 + [i32] * 3 + [P] * 7)
+            lib.orc_rnn_sample.restype = None
             lib.orc_verify.argtypes = [P, i32, P, P, P] + [P] * 7 + [i32, i32, i32] + [P] * 4
             lib.orc_verify.restype = None
             lib.orc_verify_width.argtypes = [P, i32, P, P, P] + [P] * 7 + [i32, i32, i32] + [P] * 5
@@ -164,6 +167,47 @@ def markov_sample(backbone, anchor, U, W, h, E, w_conf, policy, seed, request_id
                               _ptr(conf), _ptr(status), _ptr(indet))
     return dict(proposals=proposals, q=q, q_at_x=q_at_x, conf=conf, status=status,
                 indet=indet.astype(bool))
+
+
+def rnn_sample(backbone, anchor, U, W, Wi, Wh, bi, bh, h, E, w_conf, policy, seed, request_id, pos0):
+    """The RNN-head sampler: as markov_sample, plus the GRU weights Wi, Wh
+    uint16 [3r, r] (bf16 bits; gate order r, z, n) and bi, bh float32 [3r].
+    Returns markov_sample's dict plus states float64 [B, gamma, r]."""
+    backbone = np.ascontiguousarray(backbone)
+    B, gamma, V = backbone.shape
+    anchor = _c(anchor, np.int32)
+    r = U.shape[1]
+    Uc, Wc = _c(U, np.uint16), _c(W, np.uint16)
+    Wic, Whc = _c(Wi, np.uint16), _c(Wh, np.uint16)
+    bic, bhc = _c(bi, np.float32), _c(bh, np.float32)
+    assert Wic.shape == (3 * r, r) and Whc.shape == (3 * r, r) and bic.shape == (3 * r,) and bhc.shape == (3 * r,)
+    T, K, P, G = _policy_arrays(policy)
+    H = 0
+    hc = Ec = wc = None
+    h_dtype = 1
+    if h is not None:
+        hc = np.ascontiguousarray(h)
+        h_dtype = _dtype_code(hc)
+        H = hc.shape[2]
+        Ec = _c(E, np.uint16)
+        wc = _c(w_conf, np.float32)
+    seed = _c(seed, np.uint64)
+    rid = _c(request_id, np.uint64)
+    p0 = _c(pos0, np.int64)
+    proposals = np.full((B, gamma), -7, np.int32)
+    q = np.zeros((B, gamma, V), np.float32)
+    q_at_x = np.zeros((B, gamma), np.float32)
+    conf = np.zeros((B, gamma), np.float32) if h is not None else None
+    status = np.zeros(B, np.int32)
+    indet = np.zeros((B, gamma), np.uint8)
+    states = np.zeros((B, gamma, r), np.float64)
+    _load().orc_rnn_sample(_ptr(backbone), _dtype_code(backbone), _ptr(anchor), _ptr(Uc), _ptr(Wc), r,
+                           _ptr(Wic), _ptr(Whc), _ptr(bic), _ptr(bhc), _ptr(hc), h_dtype, _ptr(Ec), _ptr(wc), H,
+                           _ptr(T), _ptr(K), _ptr(P), _ptr(G), _ptr(seed), _ptr(rid), _ptr(p0), B, gamma, V,
+                           _ptr(proposals), _ptr(q), _ptr(q_at_x), _ptr(conf), _ptr(status), _ptr(indet),
+                           _ptr(states))
+    return dict(proposals=proposals, q=q, q_at_x=q_at_x, conf=conf, status=status,
+                indet=indet.astype(bool), states=states)
 
 
 def verify(target, proposals, q, q_at_x, policy, seed, request_id, pos0, width=None):

@@ -321,6 +321,131 @@ extern "C" void orc_markov_sample(
 }
 
 // ---------------------------------------------------------------------------
+// (a') RNN-head draft sampling.
+// [MB Semi-autoregressive draft]: besides the Markov head, DSpark offers an
+// RNN head, a GRU-like recurrence that carries prefix state across the block
+// and, like the Markov head, adds intra-block dependency on top of the
+// parallel backbone logits; at inference it runs serially.  The pages give
+// no equations, so every step below is a reading (parity of this function is
+// pinned to the GRU's textbook definition and to the Markov / backbone-only
+// sampler, not to the pages):
+//   * the recurrence is a standard GRU cell (Cho et al., 2014) in the gate
+//     layout r, z, n:  r = sigma(Wi_r e + bi_r + Wh_r s + bh_r),
+//     z = sigma(Wi_z e + bi_z + Wh_z s + bh_z),
+//     n = tanh(Wi_n e + bi_n + r * (Wh_n s + bh_n)),  s' = (1 - z) n + z s;
+//   * its input is the rank-r embedding of the previous token, e_k =
+//     U[x_{k-1}] (the Markov head's table), x_0 the anchor; its state starts
+//     at s_0 = 0 for every block;
+//   * its output is a logit bias of the same low-rank form as the Markov
+//     head's, bias_k[v] = sum_j s_k[j] * Wm[j, v] with Wm stored as W[v, j],
+//     added to the backbone logits; the state is not rounded (the sum is
+//     rounded to fp32 once, as in the Markov sampler);
+//   * the policy, the draw, q, q_at_x and the confidence are the Markov
+//     sampler's.
+// Pinned by: the states equal a float64 library GRU cell iterated over the
+// proposals; log q against the bias of those states; an update gate held at
+// one (the state stays 0) reproduces the backbone-only sampler; a state
+// that carries nothing (update gate at zero, no hidden weights) makes the
+// bias a function of x_{k-1} alone.
+// ---------------------------------------------------------------------------
+extern "C" void orc_rnn_sample(
+    const void* backbone, int32_t dtype, const int32_t* anchor,
+    const uint16_t* U, const uint16_t* W, int32_t r, const uint16_t* Wi,
+    const uint16_t* Wh, const float* bi, const float* bh, const void* h,
+    int32_t h_dtype, const uint16_t* E, const float* w_conf, int32_t H,
+    const float* temperature, const int32_t* top_k, const float* top_p,
+    const int32_t* greedy, const uint64_t* seed, const uint64_t* request_id,
+    const int64_t* pos0, int32_t B, int32_t gamma, int32_t V,
+    int32_t* proposals, float* q, float* q_at_x, float* conf, int32_t* status,
+    uint8_t* indet, double* states) {
+    std::vector<double> z(V), p(V), s(r), s_next(r), e(r), gi(3 * r), gh(3 * r);
+    auto sigmoid = [](double a) { return 1.0 / (1.0 + std::exp(-a)); };
+    for (int b = 0; b < B; ++b) {
+        status[b] = ORC_OK;
+        int x_prev = anchor[b];
+        if (x_prev < 0 || x_prev >= V) status[b] = ORC_BAD_TOKEN;
+        std::fill(s.begin(), s.end(), 0.0);
+
+        for (int k = 1; k <= gamma; ++k) {
+            const size_t idx = static_cast<size_t>(b) * gamma + (k - 1);
+            indet[idx] = 0;
+            if (status[b] != ORC_OK) {
+                proposals[idx] = -1;
+                q_at_x[idx] = 0.0f;
+                if (conf) conf[idx] = 0.0f;
+                if (states)
+                    for (int j = 0; j < r; ++j) states[idx * r + j] = 0.0;
+                continue;
+            }
+
+            // the GRU step on e_k = U[x_{k-1}]
+            for (int j = 0; j < r; ++j) e[j] = bf16_to_double(U[static_cast<size_t>(x_prev) * r + j]);
+            for (int g = 0; g < 3 * r; ++g) {
+                double ai = bi[g], ah = bh[g];
+                for (int j = 0; j < r; ++j) {
+                    ai += bf16_to_double(Wi[static_cast<size_t>(g) * r + j]) * e[j];
+                    ah += bf16_to_double(Wh[static_cast<size_t>(g) * r + j]) * s[j];
+                }
+                gi[g] = ai;
+                gh[g] = ah;
+            }
+            for (int j = 0; j < r; ++j) {
+                const double rg = sigmoid(gi[j] + gh[j]);
+                const double ug = sigmoid(gi[r + j] + gh[r + j]);
+                const double n = std::tanh(gi[2 * r + j] + rg * gh[2 * r + j]);
+                s_next[j] = (1.0 - ug) * n + ug * s[j];
+            }
+            s.swap(s_next);
+            if (states)
+                for (int j = 0; j < r; ++j) states[idx * r + j] = s[j];
+
+            for (int v = 0; v < V; ++v) {
+                double bias = 0.0;
+                for (int j = 0; j < r; ++j)
+                    bias += s[j] * bf16_to_double(W[static_cast<size_t>(v) * r + j]);
+                double sum = load_value(backbone, dtype, idx * V + v) + bias;
+                z[v] = static_cast<double>(static_cast<float>(sum));
+            }
+
+            if (h && conf) {
+                double a = 0.0;
+                for (int i = 0; i < H; ++i)
+                    a += static_cast<double>(w_conf[i]) * load_value(h, h_dtype, idx * H + i);
+                for (int i = 0; i < H; ++i)
+                    a += static_cast<double>(w_conf[H + i]) *
+                         bf16_to_double(E[static_cast<size_t>(x_prev) * H + i]);
+                conf[idx] = static_cast<float>(sigmoid(a));
+            }
+
+            int32_t am = -1, support = 0, pind = 0;
+            int st = orc_policy_row(z.data(), V, temperature[b], top_k[b], top_p[b], greedy[b],
+                                    r == 0 ? 1 : 0, p.data(), &am, &support, &pind);
+            if (st != ORC_OK) {
+                status[b] = st;
+                proposals[idx] = -1;
+                q_at_x[idx] = 0.0f;
+                continue;
+            }
+            int x;
+            if (greedy[b]) {
+                x = am;
+                q_at_x[idx] = 1.0f;
+            } else {
+                double u = orc_uniform(seed[b], request_id[b], pos0[b] + k, 0);
+                double margin = 0.0;
+                x = orc_sample_index(p.data(), V, u, &margin);
+                if (margin < kTol) pind = 1;
+                for (int v = 0; v < V; ++v) q[idx * V + v] = static_cast<float>(p[v]);
+                q_at_x[idx] = static_cast<float>(p[x]);
+            }
+            indet[idx] = static_cast<uint8_t>(pind);
+            proposals[idx] = x;
+            x_prev = x;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
 // (b) Exact verify.
 // [FT Exact decoding semantics > Greedy]: accept the contiguous prefix of
 // proposals equal to the target argmax; at the first disagreement emit the

@@ -87,6 +87,21 @@ void orc_markov_sample(const void* backbone, int32_t dtype,
                        float* q, float* q_at_x, float* conf, int32_t* status,
                        uint8_t* indet);
 
+// RNN-head draft sampling: the Markov sampler with the bias taken from a GRU
+// state carried across the block (Wi, Wh bf16 [3r, r] in gate order r, z, n;
+// bi, bh fp32 [3r]); states (may be NULL) receives s_k, [B, gamma, r].
+void orc_rnn_sample(const void* backbone, int32_t dtype, const int32_t* anchor,
+                    const uint16_t* U, const uint16_t* W, int32_t r,
+                    const uint16_t* Wi, const uint16_t* Wh, const float* bi,
+                    const float* bh, const void* h, int32_t h_dtype,
+                    const uint16_t* E, const float* w_conf, int32_t H,
+                    const float* temperature, const int32_t* top_k,
+                    const float* top_p, const int32_t* greedy,
+                    const uint64_t* seed, const uint64_t* request_id,
+                    const int64_t* pos0, int32_t B, int32_t gamma, int32_t V,
+                    int32_t* proposals, float* q, float* q_at_x, float* conf,
+                    int32_t* status, uint8_t* indet, double* states);
+
 /* (b) Exact verify [FT Exact decoding semantics; PT Acceptance].
  * out_tokens [B, gamma+1] (-1 after the emitted tokens), num_accepted [B]
  * (-1 for a failed request), status [B], indet [B]. */
