@@ -65,6 +65,8 @@ def _load():
             lib.orc_rnn_sample.argtypes = ([P, i32, P, P, P, i32, P, P, P, P, P, i32, P, P, i32]
                                            + [P] * 7 + [i32] * 3 + [P] * 7)
             lib.orc_rnn_sample.restype = None
+            lib.orc_sts_fit.argtypes = [P, P, P, i32, i32, P, P]
+            lib.orc_sts_fit.restype = None
             lib.orc_verify.argtypes = [P, i32, P, P, P] + [P] * 7 + [i32, i32, i32] + [P] * 4
             lib.orc_verify.restype = None
             lib.orc_verify_width.argtypes = [P, i32, P, P, P] + [P] * 7 + [i32, i32, i32] + [P] * 5
@@ -289,3 +291,17 @@ def accept_stats_backward(draft, target, labels, conf_logits, mask=None, scale=1
     _load().orc_accept_stats_backward(_ptr(draft), _ptr(target), _dtype_code(draft), _ptr(y), _ptr(zc),
                                       _ptr(m), N, gamma, V, float(scale), _ptr(gd), _ptr(gc))
     return gd, gc
+
+
+def sts_fit(conf_logits, labels, mask=None):
+    """Sequential Temperature Scaling: conf_logits, labels float32 [N, gamma];
+    mask uint8 [N, gamma] or None.  Returns dict(beta float64 [gamma],
+    status int32 [gamma])."""
+    z = _c(conf_logits, np.float32)
+    a = _c(labels, np.float32)
+    N, gamma = z.shape
+    m = None if mask is None else _c(mask, np.uint8)
+    beta = np.zeros(gamma, np.float64)
+    status = np.zeros(gamma, np.int32)
+    _load().orc_sts_fit(_ptr(z), _ptr(a), _ptr(m), N, gamma, _ptr(beta), _ptr(status))
+    return dict(beta=beta, status=status)

@@ -738,3 +738,84 @@ extern "C" void orc_accept_stats_backward(const void* draft, const void* target,
         }
     }
 }
+
+// ---------------------------------------------------------------------------
+// (d) Sequential Temperature Scaling of the confidence.
+// [MB Acceptance and confidence]: the confidence head regresses to the
+// accept rate, and a post-hoc Sequential Temperature Scaling calibrates it
+// for serving.  The pages give no formula; the reading: temperature scaling
+// (Guo et al., 2017) with one inverse temperature per block position k,
+// beta_k >= 0, the calibrated confidence being sigmoid(beta_k * z); beta_k
+// minimises the masked BCE of sigmoid(beta * z) against the accept labels
+// a in [0, 1] over the logged pairs (z, a) of position k.  The objective is
+// convex in beta, its derivative sum z (sigmoid(beta z) - a) non-decreasing,
+// so the minimiser is its root, found here by plain bisection to the
+// resolution of a double.  As beta grows the derivative tends to
+// sum_{z>0} z (1 - a) + sum_{z<0} (-z) a >= 0, which is 0 exactly when every
+// label agrees with the sign of its z (a = 1 for z > 0, a = 0 for z < 0):
+// then no finite minimiser exists.  Per-position status: 0 fitted; 1 no
+// information (no pair, or every z = 0): beta = 1; 2 labels separated by the
+// sign of z, or a root beyond beta = 2^20: beta = 2^20.  A derivative >= 0 at
+// beta = 0 gives beta = 0 (a constant confidence of 1/2).
+// Pinned by: soft labels a = sigmoid(z / T) give back beta = 1 / T; a
+// library scalar minimiser of the library BCE agrees; scaling every z by c
+// divides beta by c; masked pairs do not count.
+// ---------------------------------------------------------------------------
+extern "C" void orc_sts_fit(const float* conf_logits, const float* labels, const uint8_t* mask,
+                            int32_t N, int32_t gamma, double* beta, int32_t* status) {
+    const double kBetaMax = 1048576.0;
+    for (int k = 0; k < gamma; ++k) {
+        // the derivative of the position's BCE in beta
+        auto slope = [&](double bt) {
+            double d = 0.0;
+            for (int n = 0; n < N; ++n) {
+                const size_t idx = static_cast<size_t>(n) * gamma + k;
+                if (mask && !mask[idx]) continue;
+                const double z = conf_logits[idx];
+                d += z * (1.0 / (1.0 + std::exp(-bt * z)) - static_cast<double>(labels[idx]));
+            }
+            return d;
+        };
+        bool informative = false, separated = true;
+        for (int n = 0; n < N; ++n) {
+            const size_t idx = static_cast<size_t>(n) * gamma + k;
+            if (mask && !mask[idx]) continue;
+            const float z = conf_logits[idx], a = labels[idx];
+            if (z != 0.0f) informative = true;
+            if ((z > 0.0f && a < 1.0f) || (z < 0.0f && a > 0.0f)) separated = false;
+        }
+        if (!informative) {
+            beta[k] = 1.0;
+            status[k] = 1;
+            continue;
+        }
+        if (separated) {
+            beta[k] = kBetaMax;
+            status[k] = 2;
+            continue;
+        }
+        status[k] = 0;
+        if (slope(0.0) >= 0.0) {
+            beta[k] = 0.0;
+            continue;
+        }
+        double lo = 0.0, hi = 1.0;
+        while (slope(hi) < 0.0 && hi < kBetaMax) {
+            lo = hi;
+            hi *= 2.0;
+        }
+        if (slope(hi) < 0.0) {
+            beta[k] = kBetaMax;
+            status[k] = 2;
+            continue;
+        }
+        // slope(lo) < 0 <= slope(hi): halve the bracket until it stops shrinking
+        for (int it = 0; it < 2000; ++it) {
+            const double mid = 0.5 * (lo + hi);
+            if (mid <= lo || mid >= hi) break;
+            if (slope(mid) < 0.0) lo = mid;
+            else hi = mid;
+        }
+        beta[k] = 0.5 * (lo + hi);
+    }
+}

@@ -146,6 +146,13 @@ void orc_accept_stats_backward(const void* draft, const void* target, int32_t dt
                                const uint8_t* mask, int32_t N, int32_t gamma, int32_t V,
                                double scale, float* grad_draft, float* grad_conf);
 
+// Sequential Temperature Scaling: per block position k the inverse
+// temperature beta[k] >= 0 minimising the masked BCE of sigmoid(beta z)
+// against the accept labels (conf_logits, labels fp32 [N, gamma]); status[k]:
+// 0 fitted, 1 no information (beta 1), 2 separated labels (beta 2^20).
+void orc_sts_fit(const float* conf_logits, const float* labels, const uint8_t* mask,
+                 int32_t N, int32_t gamma, double* beta, int32_t* status);
+
 #ifdef __cplusplus
 }
 #endif
