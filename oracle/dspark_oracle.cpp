@@ -755,8 +755,9 @@ extern "C" void orc_accept_stats_backward(const void* draft, const void* target,
 // label agrees with the sign of its z (a = 1 for z > 0, a = 0 for z < 0):
 // then no finite minimiser exists.  Per-position status: 0 fitted; 1 no
 // information (no pair, or every z = 0): beta = 1; 2 labels separated by the
-// sign of z, or a root beyond beta = 2^20: beta = 2^20.  A derivative >= 0 at
-// beta = 0 gives beta = 0 (a constant confidence of 1/2).
+// sign of z, or a root beyond beta = 2^20: beta = 2^20; 3 a non-finite logit
+// or a label outside [0, 1] in a counted pair: beta = NaN.  A derivative >= 0
+// at beta = 0 gives beta = 0 (a constant confidence of 1/2).
 // Pinned by: soft labels a = sigmoid(z / T) give back beta = 1 / T; a
 // library scalar minimiser of the library BCE agrees; scaling every z by c
 // divides beta by c; masked pairs do not count.
@@ -776,13 +777,19 @@ extern "C" void orc_sts_fit(const float* conf_logits, const float* labels, const
             }
             return d;
         };
-        bool informative = false, separated = true;
+        bool informative = false, separated = true, invalid = false;
         for (int n = 0; n < N; ++n) {
             const size_t idx = static_cast<size_t>(n) * gamma + k;
             if (mask && !mask[idx]) continue;
             const float z = conf_logits[idx], a = labels[idx];
+            if (!std::isfinite(z) || !(a >= 0.0f && a <= 1.0f)) invalid = true;
             if (z != 0.0f) informative = true;
             if ((z > 0.0f && a < 1.0f) || (z < 0.0f && a > 0.0f)) separated = false;
+        }
+        if (invalid) {
+            beta[k] = std::numeric_limits<double>::quiet_NaN();
+            status[k] = 3;
+            continue;
         }
         if (!informative) {
             beta[k] = 1.0;

@@ -149,7 +149,8 @@ void orc_accept_stats_backward(const void* draft, const void* target, int32_t dt
 // Sequential Temperature Scaling: per block position k the inverse
 // temperature beta[k] >= 0 minimising the masked BCE of sigmoid(beta z)
 // against the accept labels (conf_logits, labels fp32 [N, gamma]); status[k]:
-// 0 fitted, 1 no information (beta 1), 2 separated labels (beta 2^20).
+// 0 fitted, 1 no information (beta 1), 2 separated labels (beta 2^20),
+// 3 a non-finite logit or a label outside [0, 1] (beta NaN).
 void orc_sts_fit(const float* conf_logits, const float* labels, const uint8_t* mask,
                  int32_t N, int32_t gamma, double* beta, int32_t* status);
 

@@ -101,3 +101,21 @@ def test_sts_nearly_separated_labels_have_a_finite_fit(oracle):
     f = lambda b: float(torch.nn.functional.binary_cross_entropy_with_logits(b * zk, ak, reduction="sum"))
     m = minimize_scalar(f, bounds=(0.0, 50.0), method="bounded", options=dict(xatol=1e-10))
     np.testing.assert_allclose(res["beta"][0], m.x, rtol=1e-6)
+
+
+def test_sts_invalid_pairs(oracle):
+    """A non-finite logit or a label outside [0, 1] in a counted pair fails
+    its position (status 3, beta NaN); the same pair masked out does not."""
+    z = _logits(7)
+    a = (1.0 / (1.0 + np.exp(-z))).astype(np.float32)
+    z[10, 0] = np.nan
+    z[11, 1] = np.inf
+    a[12, 2] = 1.5
+    a[13, 3] = np.nan
+    res = oracle.sts_fit(z, a)
+    assert res["status"].tolist() == [3, 3, 3, 3, 0] and np.all(np.isnan(res["beta"][:4]))
+    mask = np.ones((N, GAMMA), np.uint8)
+    mask[10:14] = 0
+    res = oracle.sts_fit(z, a, mask)
+    assert np.all(res["status"] == 0)
+    np.testing.assert_allclose(res["beta"], 1.0, rtol=1e-5)
