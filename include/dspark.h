@@ -20,6 +20,8 @@
  *                         CE / L1 / confidence-BCE numerators.
  *   dspark_accept_stats_grad  their loss's gradient with respect to the
  *                         draft logits and the confidence logits.
+ *   dspark_sts_fit        Sequential Temperature Scaling: the confidence
+ *                         head's per-position inverse temperatures.
  *
  * Sources, by page title and section:
  *   [FT] FreeToken PR #69 "[2/3] feat(dsv4): implement exact DSpark
@@ -129,12 +131,13 @@ typedef enum {
 enum {
     DSPARK_OP_MARKOV_SAMPLE = 0,
     DSPARK_OP_VERIFY = 1,
-    DSPARK_OP_ACCEPT_STATS = 2
+    DSPARK_OP_ACCEPT_STATS = 2,
+    DSPARK_OP_STS_FIT = 3
 };
 
 /* Workspace bytes `op` needs for these sizes (r and H matter only for
- * DSPARK_OP_MARKOV_SAMPLE; pass B = N for DSPARK_OP_ACCEPT_STATS).  Returns 0
- * for invalid sizes. */
+ * DSPARK_OP_MARKOV_SAMPLE; pass B = N for DSPARK_OP_ACCEPT_STATS and
+ * DSPARK_OP_STS_FIT, whose V is not used).  Returns 0 for invalid sizes. */
 size_t dspark_workspace_size(int op, int B, int gamma, int V, int r, int H);
 
 /*
@@ -335,6 +338,40 @@ const char* dspark_status_string(int code);
 
 /* Library version, major * 10000 + minor * 100 + patch. */
 int dspark_version(void);
+
+/*
+ * dspark_sts_fit - Sequential Temperature Scaling of the confidence head.
+ *
+ * [MB Acceptance and confidence]: the confidence head regresses to the
+ * accept rate, and a post-hoc Sequential Temperature Scaling calibrates it
+ * for serving.  The pages give no formula; the reading: temperature scaling
+ * with one inverse temperature per block position k, beta_k >= 0, the
+ * calibrated confidence being sigmoid(beta_k z); beta_k minimises the masked
+ * BCE of sigmoid(beta_k z) against the accept labels over N logged blocks.
+ *   conf_logits  fp32 [N, gamma]: the confidence head's logits z.
+ *   labels       fp32 [N, gamma]: the accept labels a in [0, 1] (e.g. the
+ *                accept rates dspark_accept_stats reports, or observed 0/1
+ *                acceptances).
+ *   mask         uint8 [N, gamma] (nonzero = counted) or NULL (all).
+ *   beta         fp64 [gamma] out.
+ *   status       int32 [gamma] out, per position: 0 fitted; 1 no counted
+ *                pair with z != 0 (beta = 1); 2 every label agrees with the
+ *                sign of its z (a = 1 for z > 0, a = 0 for z < 0), or the
+ *                root lies beyond 2^20: no finite fit (beta = 2^20); 3 a
+ *                counted pair with a non-finite z or a label outside [0, 1]
+ *                (beta = NaN).  A BCE slope >= 0 at beta = 0 gives beta = 0
+ *                (status 0).
+ *   workspace    dspark_workspace_size(DSPARK_OP_STS_FIT, N, gamma, 0, 0, 0)
+ *                bytes; every region is written before it is read.
+ * N = 0 is valid (every position reports status 1).  The fit is a root
+ * search on the device (Newton steps inside a bracket, a fixed number of
+ * rounds enqueued); beta is accurate to about 1e-6 relative (its sums are
+ * fp32 per thread, fp64 across threads).
+ */
+int dspark_sts_fit(const float* conf_logits, const float* labels,
+                   const uint8_t* mask, int N, int gamma, double* beta,
+                   int32_t* status, void* workspace, size_t workspace_bytes,
+                   void* stream);
 
 #ifdef __cplusplus
 }

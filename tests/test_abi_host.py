@@ -92,6 +92,22 @@ def test_verify_width_rejects_invalid_arguments(lib):
     assert call(ws_bytes=16, policy=FAKE) == binding.ENOSPC
 
 
+def test_sts_fit_rejects_invalid_arguments(lib):
+    f = lib.dspark_sts_fit
+    ws = ds.workspace_size(ds.OP_STS_FIT, 100, 5, 0)
+    assert 0 < ws <= 4096
+    assert ds.workspace_size(ds.OP_STS_FIT, 100, 0, 0) == 0 and ds.workspace_size(ds.OP_STS_FIT, -1, 5, 0) == 0
+    call = lambda N=100, g=5, z=FAKE, a=FAKE, beta=FAKE, st=FAKE, wsb=ws: f(z, a, None, N, g, beta, st, FAKE, wsb, None)
+    assert call(g=0) == binding.EINVAL
+    assert call(g=17) == binding.EINVAL
+    assert call(N=-1) == binding.EINVAL
+    assert call(z=None) == binding.EINVAL
+    assert call(beta=None) == binding.EINVAL
+    assert call(beta=FAKE_ODD) == binding.EINVAL                   # fp64 output, 8-byte aligned
+    assert call(z=ctypes.c_void_p(0x7F0000000002)) == binding.EINVAL
+    assert call(wsb=8) == binding.ENOSPC
+
+
 def _markov(lib, B=4, gamma=5, V=1024, r=0, U=None, W=None, policy=None, q=None, h=None, H=0,
             ws_bytes=1 << 20):
     return lib.dspark_markov_sample(FAKE, 0, FAKE, U, W, r, h, 0, FAKE, FAKE, H, policy, FAKE, FAKE,

@@ -17,12 +17,12 @@ from . import build as _build
 
 OK, EINVAL, ENOSPC, ECUDA, ENOTSUP = 0, -1, -2, -3, -4
 BF16, F32 = 0, 1
-OP_MARKOV_SAMPLE, OP_VERIFY, OP_ACCEPT_STATS = 0, 1, 2
+OP_MARKOV_SAMPLE, OP_VERIFY, OP_ACCEPT_STATS, OP_STS_FIT = 0, 1, 2, 3
 REQ_OK, REQ_NONFINITE, REQ_EMPTY, REQ_TIMEOUT, REQ_BAD_POLICY, REQ_BAD_TOKEN = range(6)
 
 EXPORTED = ("dspark_workspace_size", "dspark_markov_sample", "dspark_verify", "dspark_verify_width",
             "dspark_accept_stats", "dspark_accept_stats_grad", "dspark_status_string", "dspark_version",
-            "dspark_verify_greedy_noalloc")
+            "dspark_verify_greedy_noalloc", "dspark_sts_fit")
 
 _lock = threading.Lock()
 _lib = None
@@ -65,6 +65,8 @@ def load(path: str | None = None):
             lib.dspark_accept_stats_grad.argtypes = ([P, P, i32, P, P, P] + [i32] * 3
                                                      + [ctypes.c_double, P, P, P])
             lib.dspark_accept_stats_grad.restype = i32
+            lib.dspark_sts_fit.argtypes = [P, P, P, i32, i32, P, P, P, sz, P]
+            lib.dspark_sts_fit.restype = i32
             lib.dspark_status_string.argtypes = [i32]
             lib.dspark_status_string.restype = ctypes.c_char_p
             lib.dspark_version.argtypes = []
@@ -279,4 +281,30 @@ def accept_stats_grad(draft, target, labels, conf_logits, mask=None, scale=1.0, 
         _ptr(draft), _ptr(target), _dtype_code(draft), _ptr(labels), _ptr(conf_logits), _ptr(mask),
         N, gamma, V, float(scale), _ptr(out[0]), _ptr(out[1]), _stream(stream))
     _check(code, "dspark_accept_stats_grad")
+    return out
+
+
+def sts_fit(conf_logits, labels, mask=None, workspace: Workspace | None = None, stream=None, out=None):
+    """Sequential Temperature Scaling: per block position the inverse
+    temperature beta >= 0 of the confidence head, from fp32 [N, gamma]
+    confidence logits and accept labels (mask: uint8 [N, gamma] or None).
+    Returns (beta float64 [gamma], status int32 [gamma])."""
+    _dev(conf_logits, "conf_logits", torch.float32)
+    _dev(labels, "labels", torch.float32)
+    if conf_logits.dim() != 2 or labels.shape != conf_logits.shape:
+        raise ValueError("conf_logits and labels must be [N, gamma] tensors of one shape")
+    N, gamma = conf_logits.shape
+    if mask is not None:
+        _dev(mask, "mask", torch.uint8)
+        if mask.shape != conf_logits.shape:
+            raise ValueError("mask must have the shape of conf_logits")
+    dev = conf_logits.device
+    if out is None:
+        out = (torch.empty((gamma,), dtype=torch.float64, device=dev),
+               torch.empty((gamma,), dtype=torch.int32, device=dev))
+    ws_n = workspace_size(OP_STS_FIT, N, gamma, 8)
+    ws = (workspace or _default_ws).get(OP_STS_FIT, ws_n, dev)
+    code = load().dspark_sts_fit(_ptr(conf_logits), _ptr(labels), _ptr(mask), N, gamma, _ptr(out[0]),
+                                 _ptr(out[1]), _ptr(ws), ws_n, _stream(stream))
+    _check(code, "dspark_sts_fit")
     return out

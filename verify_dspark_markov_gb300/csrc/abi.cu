@@ -64,6 +64,11 @@ size_t stats_workspace(int N, int gamma) {
     return align_up(stats_partials_offset(N, gamma) + static_cast<size_t>(stats_partials(N)) * 6 * sizeof(double));
 }
 
+// Sequential Temperature Scaling: the per-position search states, then the
+// count of positions still searching.
+size_t sts_active_offset() { return align_up(static_cast<size_t>(DSPARK_MAX_GAMMA) * sizeof(StsState)); }
+size_t sts_workspace() { return align_up(sts_active_offset() + sizeof(int)); }
+
 template <typename T>
 T* at(void* ws, size_t off) {
     return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
@@ -102,6 +107,7 @@ const char* dspark_status_string(int code) {
 }
 
 size_t dspark_workspace_size(int op, int B, int gamma, int V, int r, int H) {
+    if (op == DSPARK_OP_STS_FIT) return B >= 0 && gamma >= 1 && gamma <= DSPARK_MAX_GAMMA ? sts_workspace() : 0;
     if (!valid_common(B, gamma, V, DSPARK_BF16) || r < 0 || H < 0) return 0;
     switch (op) {
         case DSPARK_OP_MARKOV_SAMPLE: return markov_layout(B, gamma, V, r).total;
@@ -341,6 +347,29 @@ int dspark_accept_stats_grad(const void* draft, const void* target, int dtype, c
     p.grad_conf = grad_conf;
     return launch_accept_stats_grad(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? DSPARK_OK
                                                                                            : DSPARK_ECUDA;
+}
+
+
+int dspark_sts_fit(const float* conf_logits, const float* labels, const uint8_t* mask, int N, int gamma,
+                   double* beta, int32_t* status, void* workspace, size_t workspace_bytes, void* stream) {
+    if (N < 0 || gamma < 1 || gamma > DSPARK_MAX_GAMMA) return DSPARK_EINVAL;
+    if (!beta || !status) return DSPARK_EINVAL;
+    if (N > 0 && (!conf_logits || !labels)) return DSPARK_EINVAL;
+    if ((reinterpret_cast<uintptr_t>(conf_logits) & 3u) || (reinterpret_cast<uintptr_t>(labels) & 3u) ||
+        (reinterpret_cast<uintptr_t>(beta) & 7u) || (reinterpret_cast<uintptr_t>(status) & 3u))
+        return DSPARK_EINVAL;
+    if (!workspace || workspace_bytes < sts_workspace()) return DSPARK_ENOSPC;
+    StsParams p{};
+    p.conf_logits = conf_logits;
+    p.labels = labels;
+    p.mask = mask;
+    p.N = N;
+    p.gamma = gamma;
+    p.beta = beta;
+    p.status = status;
+    p.state = at<StsState>(workspace, 0);
+    p.active = at<int>(workspace, sts_active_offset());
+    return launch_sts_fit(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? DSPARK_OK : DSPARK_ECUDA;
 }
 
 }  // extern "C"

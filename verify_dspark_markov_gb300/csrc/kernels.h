@@ -194,4 +194,28 @@ struct StatsGradParams {
 };
 cudaError_t launch_accept_stats_grad(const StatsGradParams& p, cudaStream_t stream);
 
+// Sequential Temperature Scaling fit (sts.cu): per block position the state
+// of its root search, kept in the caller's workspace.
+struct StsState {
+    double beta;          // the current iterate (the answer once phase == 2)
+    double lo, hi;        // bracket of the root (hi = +inf until a slope >= 0 is seen)
+    double s1, s2;        // this round's slope and curvature sums
+    unsigned int flags;   // bit 0 a counted z != 0, bit 1 a label against the sign of z, bit 2 an invalid pair
+    int phase;            // 0 first round (beta = 0), 1 searching, 2 done
+    int status;           // 0 fitted, 1 no information, 2 no finite root below the cap, 3 invalid input
+    int pad;
+};
+struct StsParams {
+    const float* conf_logits;  // [N, gamma]
+    const float* labels;       // [N, gamma]
+    const uint8_t* mask;       // [N, gamma] or null
+    int64_t N;
+    int gamma;
+    double* beta;              // [gamma] out
+    int32_t* status;           // [gamma] out
+    StsState* state;           // [DSPARK_MAX_GAMMA] workspace
+    int* active;               // workspace: positions still searching
+};
+cudaError_t launch_sts_fit(const StsParams& p, cudaStream_t stream);
+
 }  // namespace dspark

@@ -1,0 +1,214 @@
+// Sequential Temperature Scaling of the confidence head [MB Acceptance and
+// confidence]: for each block position k, the inverse temperature
+// beta_k >= 0 whose calibrated confidence sigmoid(beta_k z) minimises the
+// masked BCE against the accept labels a over logged pairs (z, a).  The BCE
+// is convex in beta and its slope sum z (sigmoid(beta z) - a) does not
+// decrease, so the fit is the slope's root.
+//
+// The fit runs on the device in rounds; the host only enqueues them:
+//  * sts_pass_kernel - one streaming pass over the pairs at the current
+//    beta_k of every position: the slope and the curvature
+//    sum z^2 sigmoid (1 - sigmoid) per position, and exact flags (a counted
+//    z != 0; a label against the sign of its z; an invalid pair).  A thread
+//    takes whole rows n (gamma contiguous pairs) with per-position sums in
+//    registers; warps reduce by shuffles, CTAs through shared memory, and
+//    one double atomic per position and CTA lands in the position's state.
+//  * sts_update_kernel - one warp, lane k: the degenerate cases on the first
+//    round (taken at beta = 0), then a Newton step kept inside the bracket
+//    [lo, hi] of the root, bisection (or doubling while hi is open) when the
+//    step leaves it; the sums are cleared for the next round.
+// Once every position has converged the remaining passes return at once.
+// HBM-bound: 9 bytes a pair a round (8 without a mask).
+
+#include <algorithm>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace dspark {
+
+namespace {
+
+constexpr int kStsThreads = 256;
+constexpr int kStsWarps = kStsThreads / 32;
+constexpr int kG = DSPARK_MAX_GAMMA;
+constexpr double kBetaMax = 1048576.0;  // 2^20
+constexpr unsigned kInformative = 1u, kViolated = 2u, kInvalid = 4u;
+// Rounds enqueued per fit: enough for beta to double from 1 to the cap (20)
+// and then halve a bracket to below 1e-7 of its width (24), with margin;
+// Newton usually converges in a handful and the later passes return at once.
+constexpr int kStsRounds = 64;
+
+__global__ void sts_init_kernel(StsState* st, int* active, int gamma) {
+    const int k = threadIdx.x;
+    if (k < kG) {
+        StsState s{};
+        s.beta = 0.0;
+        s.lo = 0.0;
+        s.hi = __longlong_as_double(0x7FF0000000000000ll);  // +inf: no upper bound yet
+        s.phase = k < gamma ? 0 : 2;
+        st[k] = s;
+    }
+    if (k == 0) *active = gamma;
+}
+
+__global__ void __launch_bounds__(kStsThreads) sts_pass_kernel(const float* __restrict__ z,
+                                                               const float* __restrict__ a,
+                                                               const uint8_t* __restrict__ mask, int64_t N,
+                                                               int gamma, StsState* st, const int* active) {
+    if (*active == 0) return;
+    __shared__ float s_beta[kG];
+    __shared__ float s_red[kStsWarps][kG][2];
+    __shared__ unsigned s_flag[3];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid < kG) s_beta[tid] = tid < gamma ? static_cast<float>(st[tid].beta) : 0.0f;
+    if (tid < 3) s_flag[tid] = 0u;
+    __syncthreads();
+
+    float bt[kG], g1[kG], g2[kG];
+#pragma unroll
+    for (int k = 0; k < kG; ++k) {
+        bt[k] = s_beta[k];
+        g1[k] = 0.0f;
+        g2[k] = 0.0f;
+    }
+    unsigned inf = 0u, viol = 0u, bad = 0u;  // bit k: position k
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kStsThreads;
+    for (int64_t n = static_cast<int64_t>(blockIdx.x) * kStsThreads + tid; n < N; n += stride) {
+        const int64_t base = n * gamma;
+#pragma unroll
+        for (int k = 0; k < kG; ++k) {
+            if (k < gamma && (!mask || mask[base + k])) {
+                const float zv = z[base + k], av = a[base + k];
+                if (!isfinite(zv) || !(av >= 0.0f && av <= 1.0f)) bad |= 1u << k;
+                if (zv != 0.0f) inf |= 1u << k;
+                if ((zv > 0.0f && av < 1.0f) || (zv < 0.0f && av > 0.0f)) viol |= 1u << k;
+                const float sg = 1.0f / (1.0f + expf(-bt[k] * zv));
+                g1[k] += zv * (sg - av);
+                g2[k] += zv * zv * (sg * (1.0f - sg));
+            }
+        }
+    }
+
+#pragma unroll
+    for (int k = 0; k < kG; ++k) {
+        if (k < gamma) {
+            float x = g1[k], y = g2[k];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                x += __shfl_xor_sync(0xFFFFFFFFu, x, o);
+                y += __shfl_xor_sync(0xFFFFFFFFu, y, o);
+            }
+            if (lane == 0) {
+                s_red[warp][k][0] = x;
+                s_red[warp][k][1] = y;
+            }
+        }
+    }
+    inf = __reduce_or_sync(0xFFFFFFFFu, inf);
+    viol = __reduce_or_sync(0xFFFFFFFFu, viol);
+    bad = __reduce_or_sync(0xFFFFFFFFu, bad);
+    if (lane == 0) {
+        if (inf) atomicOr(&s_flag[0], inf);
+        if (viol) atomicOr(&s_flag[1], viol);
+        if (bad) atomicOr(&s_flag[2], bad);
+    }
+    __syncthreads();
+    if (tid < gamma) {
+        double x = 0.0, y = 0.0;
+        for (int w = 0; w < kStsWarps; ++w) {
+            x += static_cast<double>(s_red[w][tid][0]);
+            y += static_cast<double>(s_red[w][tid][1]);
+        }
+        atomicAdd(&st[tid].s1, x);
+        atomicAdd(&st[tid].s2, y);
+        const unsigned f = (((s_flag[0] >> tid) & 1u) ? kInformative : 0u) |
+                           (((s_flag[1] >> tid) & 1u) ? kViolated : 0u) |
+                           (((s_flag[2] >> tid) & 1u) ? kInvalid : 0u);
+        if (f) atomicOr(&st[tid].flags, f);
+    }
+}
+
+__global__ void sts_update_kernel(StsState* st, int* active, int gamma, double* beta_out, int32_t* status_out) {
+    const int k = threadIdx.x;
+    bool finished = false;
+    if (k < gamma) {
+        StsState s = st[k];
+        const double inf = __longlong_as_double(0x7FF0000000000000ll);
+        if (s.phase == 0) {  // the sums were taken at beta = 0
+            s.phase = 2;
+            if (s.flags & kInvalid) {
+                s.beta = __longlong_as_double(0x7FF8000000000000ll);
+                s.status = 3;
+            } else if (!(s.flags & kInformative)) {
+                s.beta = 1.0;
+                s.status = 1;
+            } else if (!(s.flags & kViolated)) {  // labels agree with the sign of z: no finite root
+                s.beta = kBetaMax;
+                s.status = 2;
+            } else if (s.s1 >= 0.0) {
+                s.beta = 0.0;
+                s.status = 0;
+            } else {
+                s.lo = 0.0;
+                s.hi = inf;
+                s.beta = 1.0;
+                s.status = 0;
+                s.phase = 1;
+            }
+            finished = s.phase == 2;
+        } else if (s.phase == 1) {
+            const double g = s.s1, h = s.s2, b = s.beta;
+            if (g < 0.0) s.lo = b;
+            else s.hi = b;
+            if (g < 0.0 && b >= kBetaMax) {  // the root lies beyond the cap
+                s.beta = kBetaMax;
+                s.status = 2;
+                s.phase = 2;
+            } else if (g == 0.0) {
+                s.phase = 2;
+            } else {
+                const double step = h > 0.0 ? b - g / h : b;
+                double next;
+                if (s.hi == inf) next = (step > b && step < inf) ? step : 2.0 * b;
+                else next = (step > s.lo && step < s.hi) ? step : 0.5 * (s.lo + s.hi);
+                next = fmin(next, kBetaMax);
+                // stop at the accuracy the fp32 pair terms allow: nearer
+                // the root their rounding decides the slope's sign
+                const bool converged = fabs(next - b) <= 1e-7 * b ||
+                                       (s.hi != inf && s.hi - s.lo <= 1e-7 * s.hi);
+                s.beta = next;
+                if (converged) s.phase = 2;
+            }
+            finished = s.phase == 2;
+        }
+        s.s1 = 0.0;
+        s.s2 = 0.0;
+        st[k] = s;
+        beta_out[k] = s.beta;
+        status_out[k] = s.status;
+    }
+    const unsigned fin = __ballot_sync(0xFFFFFFFFu, finished);
+    if (k == 0 && fin) atomicSub(active, __popc(fin));
+}
+
+}  // namespace
+
+cudaError_t launch_sts_fit(const StsParams& p, cudaStream_t stream) {
+    if (p.gamma < 1 || p.gamma > kG || p.N < 0) return cudaErrorInvalidValue;
+    sts_init_kernel<<<1, 32, 0, stream>>>(p.state, p.active, p.gamma);
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    const int64_t want = (p.N + kStsThreads - 1) / kStsThreads;
+    const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(want, static_cast<int64_t>(sms) * 8)));
+    for (int r = 0; r < kStsRounds; ++r) {
+        sts_pass_kernel<<<grid, kStsThreads, 0, stream>>>(p.conf_logits, p.labels, p.mask, p.N, p.gamma, p.state,
+                                                          p.active);
+        sts_update_kernel<<<1, 32, 0, stream>>>(p.state, p.active, p.gamma, p.beta, p.status);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace dspark
