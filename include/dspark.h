@@ -9,6 +9,8 @@
  *                         proposal per position left to right, the full
  *                         proposal distribution q and a confidence per
  *                         position.
+ *   dspark_rnn_sample     the same draft with the RNN head: a GRU state
+ *                         carried across the block gives the low-rank bias.
  *   dspark_verify         exact verification of a proposal block against the
  *                         target's logits: greedy contiguous-prefix argmax
  *                         acceptance, or accept-with-min(1, p/q), residual
@@ -132,11 +134,12 @@ enum {
     DSPARK_OP_MARKOV_SAMPLE = 0,
     DSPARK_OP_VERIFY = 1,
     DSPARK_OP_ACCEPT_STATS = 2,
-    DSPARK_OP_STS_FIT = 3
+    DSPARK_OP_STS_FIT = 3,
+    DSPARK_OP_RNN_SAMPLE = 4
 };
 
-/* Workspace bytes `op` needs for these sizes (r and H matter only for
- * DSPARK_OP_MARKOV_SAMPLE; pass B = N for DSPARK_OP_ACCEPT_STATS and
+/* Workspace bytes `op` needs for these sizes (r matters only for
+ * DSPARK_OP_MARKOV_SAMPLE and DSPARK_OP_RNN_SAMPLE; pass B = N for DSPARK_OP_ACCEPT_STATS and
  * DSPARK_OP_STS_FIT, whose V is not used).  Returns 0 for invalid sizes. */
 size_t dspark_workspace_size(int op, int B, int gamma, int V, int r, int H);
 
@@ -189,6 +192,42 @@ int dspark_markov_sample(const void* backbone, int dtype, const int32_t* anchor,
                          int32_t* proposals, float* q, float* q_at_x,
                          float* conf, int32_t* status, void* workspace,
                          size_t workspace_bytes, void* stream);
+
+/*
+ * dspark_rnn_sample - the draft's sequential head in its RNN form.
+ *
+ * [MB Semi-autoregressive draft]: besides the Markov head DSpark offers an
+ * RNN head, a GRU-like recurrence carrying prefix state across the block,
+ * run serially at inference.  The pages give no equations; the reading: a
+ * standard GRU cell (gate order r, z, n) whose input is the rank-r embedding
+ * of the previous token, e_k = U[x_{k-1}] (x_0 = the anchor), from the state
+ * s_0 = 0 of every block:
+ *   r = sigmoid(Wi_r e + bi_r + Wh_r s + bh_r)
+ *   z = sigmoid(Wi_z e + bi_z + Wh_z s + bh_z)
+ *   n = tanh(Wi_n e + bi_n + r * (Wh_n s + bh_n)),   s_k = (1 - z) n + z s
+ * and its state gives a bias of the Markov head's form, added to the backbone
+ * logits: z_k[v] = backbone_k[v] + sum_j s_k[j] W[v, j].  Everything else
+ * (policy, proposals, q, q_at_x, confidence, statuses, random draws) is
+ * dspark_markov_sample's.
+ *   U, W       bf16 [V, r], r a multiple of 16 in 16..DSPARK_MAX_RANK.
+ *   Wi, Wh     bf16 [3r, r] (rows r, z, n); 16-byte aligned.
+ *   bi, bh     fp32 [3r].
+ *   Sizes      B <= DSPARK_MAX_BATCH and B <= V.
+ *   workspace  dspark_workspace_size(DSPARK_OP_RNN_SAMPLE, B, gamma, V, r, 0).
+ * The bias reaches the logits through the tensor cores in bf16: s_k is passed
+ * as hi = bf16(s_k) plus lo = bf16(s_k - hi), two products summed in fp32, so
+ * the logits carry s_k to about 2^-16 of its size.
+ */
+int dspark_rnn_sample(const void* backbone, int dtype, const int32_t* anchor,
+                      const uint16_t* U, const uint16_t* W, int r,
+                      const uint16_t* Wi, const uint16_t* Wh, const float* bi,
+                      const float* bh, const void* h, int h_dtype,
+                      const uint16_t* E, const float* w_conf, int H,
+                      const dspark_policy* policy, const uint64_t* seed,
+                      const uint64_t* request_id, const int64_t* pos0, int B,
+                      int gamma, int V, int32_t* proposals, float* q,
+                      float* q_at_x, float* conf, int32_t* status,
+                      void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * dspark_verify - exact verification of one proposal block per request.

@@ -282,6 +282,24 @@ def mixed_serving(V=VOCAB, B=256, gamma=5, r=256, H=4096, device="cpu", seed=100
                     extra=dict(adversarial=adv))
 
 
+@dataclass
+class GruWeights:
+    Wi: torch.Tensor  # bf16 [3r, r], gate rows r, z, n
+    Wh: torch.Tensor  # bf16 [3r, r]
+    bi: torch.Tensor  # fp32 [3r]
+    bh: torch.Tensor  # fp32 [3r]
+
+
+def gru_weights(r, g, device, scale=None) -> GruWeights:
+    """The RNN head's GRU cell at rank r: weights N(0, 1/r) (the usual
+    1/sqrt(fan-in) scale), biases N(0, 0.1^2)."""
+    sc = scale if scale is not None else 1.0 / r ** 0.5
+    return GruWeights(_normal((3 * r, r), sc, g, device, torch.bfloat16).contiguous(),
+                      _normal((3 * r, r), sc, g, device, torch.bfloat16).contiguous(),
+                      _normal((3 * r,), 0.1, g, device).contiguous(),
+                      _normal((3 * r,), 0.1, g, device).contiguous())
+
+
 def verify_widths(B, gamma, seed=1007, invalid=0, device="cpu") -> torch.Tensor:
     """Per-request verify widths, int32 [B]: uniform over 0..gamma (a
     scheduler's choice of how many proposals to check; the pages pick it from

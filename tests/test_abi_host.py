@@ -108,6 +108,25 @@ def test_sts_fit_rejects_invalid_arguments(lib):
     assert call(wsb=8) == binding.ENOSPC
 
 
+def test_rnn_rejects_invalid_arguments(lib):
+    f = lib.dspark_rnn_sample
+    ws = ds.workspace_size(ds.OP_RNN_SAMPLE, 4, 5, 1024, 64)
+    assert ws >= 2 * 4 * 1024 * 4 and ds.workspace_size(ds.OP_RNN_SAMPLE, 4, 5, 1024, 0) == 0
+
+    def call(B=4, gamma=5, V=1024, r=64, Wi=FAKE, U=FAKE, wsb=ws, policy=None, q=None):
+        return f(FAKE, 0, FAKE, U, FAKE, r, Wi, FAKE, FAKE, FAKE, None, 0, None, None, 0, policy, FAKE, FAKE, FAKE,
+                 B, gamma, V, FAKE, q, FAKE, None, FAKE, FAKE, wsb, None)
+    assert call(B=0) == binding.OK
+    assert call(r=0) == binding.EINVAL                      # the RNN head needs a rank
+    assert call(r=24) == binding.EINVAL
+    assert call(B=300) == binding.EINVAL
+    assert call(B=16, V=8) == binding.EINVAL                # the bias gather needs B <= V
+    assert call(Wi=None) == binding.EINVAL
+    assert call(Wi=FAKE_ODD) == binding.EINVAL
+    assert call(policy=FAKE, q=None) == binding.EINVAL
+    assert call(wsb=16) == binding.ENOSPC
+
+
 def _markov(lib, B=4, gamma=5, V=1024, r=0, U=None, W=None, policy=None, q=None, h=None, H=0,
             ws_bytes=1 << 20):
     return lib.dspark_markov_sample(FAKE, 0, FAKE, U, W, r, h, 0, FAKE, FAKE, H, policy, FAKE, FAKE,

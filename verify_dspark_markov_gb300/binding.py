@@ -17,12 +17,12 @@ from . import build as _build
 
 OK, EINVAL, ENOSPC, ECUDA, ENOTSUP = 0, -1, -2, -3, -4
 BF16, F32 = 0, 1
-OP_MARKOV_SAMPLE, OP_VERIFY, OP_ACCEPT_STATS, OP_STS_FIT = 0, 1, 2, 3
+OP_MARKOV_SAMPLE, OP_VERIFY, OP_ACCEPT_STATS, OP_STS_FIT, OP_RNN_SAMPLE = 0, 1, 2, 3, 4
 REQ_OK, REQ_NONFINITE, REQ_EMPTY, REQ_TIMEOUT, REQ_BAD_POLICY, REQ_BAD_TOKEN = range(6)
 
 EXPORTED = ("dspark_workspace_size", "dspark_markov_sample", "dspark_verify", "dspark_verify_width",
             "dspark_accept_stats", "dspark_accept_stats_grad", "dspark_status_string", "dspark_version",
-            "dspark_verify_greedy_noalloc", "dspark_sts_fit")
+            "dspark_verify_greedy_noalloc", "dspark_sts_fit", "dspark_rnn_sample")
 
 _lock = threading.Lock()
 _lib = None
@@ -65,6 +65,9 @@ def load(path: str | None = None):
             lib.dspark_accept_stats_grad.argtypes = ([P, P, i32, P, P, P] + [i32] * 3
                                                      + [ctypes.c_double, P, P, P])
             lib.dspark_accept_stats_grad.restype = i32
+            lib.dspark_rnn_sample.argtypes = ([P, i32, P, P, P, i32, P, P, P, P, P, i32, P, P, i32]
+                                              + [P] * 4 + [i32] * 3 + [P] * 6 + [sz, P])
+            lib.dspark_rnn_sample.restype = i32
             lib.dspark_sts_fit.argtypes = [P, P, P, i32, i32, P, P, P, sz, P]
             lib.dspark_sts_fit.restype = i32
             lib.dspark_status_string.argtypes = [i32]
@@ -151,6 +154,50 @@ def _policy_ptr(policy):
 
 
 # ------------------------------------------------------------------ entry points
+def rnn_sample(backbone, anchor, U, W, Wi, Wh, bi, bh, h=None, E=None, w_conf=None, policy=None,
+               seed=None, request_id=None, pos0=None, workspace: Workspace | None = None, stream=None, out=None):
+    """The draft's sequential head in its RNN form over [B, gamma, V] backbone
+    logits: U, W bf16 [V, r]; Wi, Wh bf16 [3r, r] (gate rows r, z, n); bi, bh
+    fp32 [3r].  Returns dict(proposals, q, q_at_x, conf, status) as
+    markov_sample does."""
+    _dev(backbone, "backbone")
+    B, gamma, V = backbone.shape
+    dev = backbone.device
+    _dev(anchor, "anchor", torch.int32)
+    for t, name in ((U, "U"), (W, "W"), (Wi, "Wi"), (Wh, "Wh")):
+        _dev(t, name, torch.bfloat16)
+    _dev(bi, "bi", torch.float32)
+    _dev(bh, "bh", torch.float32)
+    r = U.shape[1]
+    if Wi.shape != (3 * r, r) or Wh.shape != (3 * r, r) or bi.shape != (3 * r,) or bh.shape != (3 * r,):
+        raise ValueError("Wi, Wh must be [3r, r] and bi, bh [3r]")
+    H, h_code = 0, F32
+    if h is not None:
+        _dev(h, "h")
+        h_code = _dtype_code(h)
+        H = h.shape[2]
+        _dev(E, "E", torch.bfloat16)
+        _dev(w_conf, "w_conf", torch.float32)
+    if out is None:
+        out = dict(proposals=torch.empty((B, gamma), dtype=torch.int32, device=dev),
+                   q=(torch.empty((B, gamma, V), dtype=torch.float32, device=dev)
+                      if policy is not None else None),
+                   q_at_x=torch.empty((B, gamma), dtype=torch.float32, device=dev),
+                   conf=(torch.empty((B, gamma), dtype=torch.float32, device=dev)
+                         if h is not None else None),
+                   status=torch.empty((B,), dtype=torch.int32, device=dev))
+    ws_n = workspace_size(OP_RNN_SAMPLE, B, gamma, V, r, H)
+    ws = (workspace or _default_ws).get(OP_RNN_SAMPLE, ws_n, dev)
+    code = load().dspark_rnn_sample(
+        _ptr(backbone), _dtype_code(backbone), _ptr(anchor), _ptr(U), _ptr(W), r, _ptr(Wi), _ptr(Wh), _ptr(bi),
+        _ptr(bh), _ptr(h), h_code, _ptr(E), _ptr(w_conf), H, _policy_ptr(policy),
+        _ptr(_dev(seed, "seed", torch.int64)), _ptr(_dev(request_id, "request_id", torch.int64)),
+        _ptr(_dev(pos0, "pos0", torch.int64)), B, gamma, V, _ptr(out["proposals"]), _ptr(out["q"]),
+        _ptr(out["q_at_x"]), _ptr(out["conf"]), _ptr(out["status"]), _ptr(ws), ws_n, _stream(stream))
+    _check(code, "dspark_rnn_sample")
+    return out
+
+
 def verify(target, proposals, q=None, q_at_x=None, policy=None, seed=None, request_id=None,
            pos0=None, out=None, workspace: Workspace | None = None, stream=None, width=None):
     """Exact verify of [B, gamma+1, V] target logits against [B, gamma]

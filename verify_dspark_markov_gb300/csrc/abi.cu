@@ -56,6 +56,24 @@ MarkovLayout markov_layout(int B, int gamma, int V, int r) {
     return l;
 }
 
+// RNN head: the error flag and two z buffers as for the Markov head (z after
+// the hi product, z after the lo product), then the fp32 state, its bf16 hi
+// and lo rows and the gather index.
+struct RnnLayout {
+    size_t error_flag, zbuf, state, hi, lo, index, total;
+};
+RnnLayout rnn_layout(int B, int V, int r) {
+    RnnLayout l;
+    l.error_flag = 0;
+    l.zbuf = align_up(sizeof(int));
+    l.state = align_up(l.zbuf + 2 * static_cast<size_t>(B) * V * sizeof(float));
+    l.hi = align_up(l.state + static_cast<size_t>(B) * r * sizeof(float));
+    l.lo = align_up(l.hi + static_cast<size_t>(B) * r * sizeof(uint16_t));
+    l.index = align_up(l.lo + static_cast<size_t>(B) * r * sizeof(uint16_t));
+    l.total = align_up(l.index + static_cast<size_t>(B) * sizeof(int32_t));
+    return l;
+}
+
 // Statistics: per-position records, then the per-CTA partial sums.
 size_t stats_partials_offset(int N, int gamma) {
     return align_up(static_cast<size_t>(N) * gamma * sizeof(StatsRecord));
@@ -113,6 +131,7 @@ size_t dspark_workspace_size(int op, int B, int gamma, int V, int r, int H) {
         case DSPARK_OP_MARKOV_SAMPLE: return markov_layout(B, gamma, V, r).total;
         case DSPARK_OP_VERIFY: return verify_layout(B, gamma).total;
         case DSPARK_OP_ACCEPT_STATS: return stats_workspace(B, gamma);
+        case DSPARK_OP_RNN_SAMPLE: return r >= 16 ? rnn_layout(B, V, r).total : 0;
         default: return 0;
     }
 }
@@ -270,6 +289,110 @@ int dspark_markov_sample(const void* backbone, int dtype, const int32_t* anchor,
     p.q_at_x = q_at_x;
     p.status = status;
     if (launch_argmax_rows(p, B, s) != cudaSuccess) return DSPARK_ECUDA;
+    if (h) {
+        ConfParams c{h, h_dtype, E, w_conf, H, B, gamma, V, anchor, proposals, 1, gamma, conf};
+        if (launch_confidence(c, s) != cudaSuccess) return DSPARK_ECUDA;
+    }
+    return DSPARK_OK;
+}
+
+int dspark_rnn_sample(const void* backbone, int dtype, const int32_t* anchor, const uint16_t* U,
+                      const uint16_t* W, int r, const uint16_t* Wi, const uint16_t* Wh, const float* bi,
+                      const float* bh, const void* h, int h_dtype, const uint16_t* E, const float* w_conf,
+                      int H, const dspark_policy* policy, const uint64_t* seed, const uint64_t* request_id,
+                      const int64_t* pos0, int B, int gamma, int V, int32_t* proposals, float* q,
+                      float* q_at_x, float* conf, int32_t* status, void* workspace, size_t workspace_bytes,
+                      void* stream) {
+    if (!valid_common(B, gamma, V, dtype)) return DSPARK_EINVAL;
+    if (B > DSPARK_MAX_BATCH || B > V) return DSPARK_EINVAL;
+    if (r < 16 || r > DSPARK_MAX_RANK || r % 16 != 0) return DSPARK_EINVAL;
+    if (B == 0) return DSPARK_OK;
+    if (!backbone || !anchor || !proposals || !q_at_x || !status) return DSPARK_EINVAL;
+    if (!U || !W || !Wi || !Wh || !bi || !bh) return DSPARK_EINVAL;
+    if (!aligned16(backbone) || !aligned16(U) || !aligned16(W) || !aligned16(Wi) || !aligned16(Wh))
+        return DSPARK_EINVAL;
+    if (h && (H <= 0 || !E || !w_conf || !conf || (h_dtype != DSPARK_BF16 && h_dtype != DSPARK_F32)))
+        return DSPARK_EINVAL;
+    if (policy && (!q || !seed || !request_id || !pos0 || !aligned16(q))) return DSPARK_EINVAL;
+    const RnnLayout lay = rnn_layout(B, V, r);
+    if (workspace_bytes < lay.total || !workspace) return DSPARK_ENOSPC;
+    if (!policy_vocab_ok(V)) return DSPARK_ENOTSUP;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int* error_flag = at<int>(workspace, lay.error_flag);
+    float* zA = at<float>(workspace, lay.zbuf);
+    float* zB = zA + static_cast<size_t>(B) * V;
+
+    GruParams gru{};
+    gru.U = U;
+    gru.Wi = Wi;
+    gru.Wh = Wh;
+    gru.bi = bi;
+    gru.bh = bh;
+    gru.anchor = anchor;
+    gru.proposals = proposals;
+    gru.B = B;
+    gru.gamma = gamma;
+    gru.V = V;
+    gru.r = r;
+    gru.state = at<float>(workspace, lay.state);
+    gru.hi = at<uint16_t>(workspace, lay.hi);
+    gru.lo = at<uint16_t>(workspace, lay.lo);
+    gru.index = at<int32_t>(workspace, lay.index);
+
+    // the bias in two products on the tensor cores: zA = backbone_k + hi W^T,
+    // then zB = zA + lo W^T; the gather reads row index[b] (= b) of hi / lo
+    MarkovGemmParams g1{}, g2{};
+    MarkovGemmPlan plan1{}, plan2{};
+    g1.backbone = backbone;
+    g1.dtype = dtype;
+    g1.U = gru.hi;
+    g1.W = W;
+    g1.anchor = gru.index;
+    g1.proposals = proposals;
+    g1.B = B;
+    g1.gamma = gamma;
+    g1.V = V;
+    g1.r = r;
+    g1.k = 1;
+    g1.zbuf = zA;
+    g1.error_flag = error_flag;
+    g2 = g1;
+    g2.backbone = zA;
+    g2.dtype = DSPARK_F32;
+    g2.U = gru.lo;
+    g2.gamma = 1;
+    g2.zbuf = zB;
+    if (!prepare_markov_bias(g1, plan1) || !prepare_markov_bias(g2, plan2)) return DSPARK_ENOTSUP;
+
+    MarkovStepParams mp{};
+    mp.backbone = backbone;
+    mp.dtype = dtype;
+    mp.zbuf = zB;
+    mp.anchor = anchor;
+    mp.proposals = proposals;
+    mp.q = q;
+    mp.q_at_x = q_at_x;
+    mp.status = status;
+    mp.policy = policy;
+    mp.seed = seed;
+    mp.request_id = request_id;
+    mp.pos0 = pos0;
+    mp.B = B;
+    mp.gamma = gamma;
+    mp.V = V;
+    mp.slice = step_slice(V);
+    mp.error_flag = error_flag;
+    const size_t esz = dtype == DSPARK_BF16 ? 2 : 4;
+    for (int k = 1; k <= gamma; ++k) {
+        gru.k = k;
+        if (launch_gru_step(gru, s) != cudaSuccess) return DSPARK_ECUDA;
+        // step k's backbone rows, read as the first rows of a [B, gamma, V] array
+        g1.backbone = static_cast<const char*>(backbone) + static_cast<size_t>(k - 1) * V * esz;
+        if (launch_markov_bias(g1, plan1, false, s) != cudaSuccess) return DSPARK_ECUDA;
+        if (launch_markov_bias(g2, plan2, false, s) != cudaSuccess) return DSPARK_ECUDA;
+        mp.k = k;
+        if (launch_markov_step(mp, s) != cudaSuccess) return DSPARK_ECUDA;
+    }
     if (h) {
         ConfParams c{h, h_dtype, E, w_conf, H, B, gamma, V, anchor, proposals, 1, gamma, conf};
         if (launch_confidence(c, s) != cudaSuccess) return DSPARK_ECUDA;

@@ -218,4 +218,22 @@ struct StsParams {
 };
 cudaError_t launch_sts_fit(const StsParams& p, cudaStream_t stream);
 
+// One step of the RNN head's GRU (rnn.cu): s_k from s_{k-1} and U[x_{k-1}],
+// written as fp32 and as the bf16 pair (hi, lo) the bias GEMM reads.
+struct GruParams {
+    const uint16_t* U;          // bf16 [V, r]
+    const uint16_t* Wi;         // bf16 [3r, r], gate order r, z, n
+    const uint16_t* Wh;         // bf16 [3r, r]
+    const float* bi;            // [3r]
+    const float* bh;            // [3r]
+    const int32_t* anchor;      // [B]
+    const int32_t* proposals;   // [B, gamma]
+    int B, gamma, V, r, k;      // k: 1-based step
+    float* state;               // [B, r] fp32 workspace: s_{k-1} in, s_k out
+    uint16_t* hi;               // [B, r] bf16(s_k)
+    uint16_t* lo;               // [B, r] bf16(s_k - hi)
+    int32_t* index;             // [B]: b, or -1 when x_{k-1} is not a token (a failed request)
+};
+cudaError_t launch_gru_step(const GruParams& p, cudaStream_t stream);
+
 }  // namespace dspark
