@@ -400,6 +400,9 @@ int dspark_version(void);
  *                counted pair with a non-finite z or a label outside [0, 1]
  *                (beta = NaN).  A BCE slope >= 0 at beta = 0 gives beta = 0
  *                (status 0).
+ *   rounds       int32 [gamma] out, or NULL: the passes over the pairs each
+ *                position's search used (every pass reads all positions
+ *                until the last one stops).
  *   workspace    dspark_workspace_size(DSPARK_OP_STS_FIT, N, gamma, 0, 0, 0)
  *                bytes; every region is written before it is read.
  * N = 0 is valid (every position reports status 1).  The fit is a root
@@ -409,8 +412,8 @@ int dspark_version(void);
  */
 int dspark_sts_fit(const float* conf_logits, const float* labels,
                    const uint8_t* mask, int N, int gamma, double* beta,
-                   int32_t* status, void* workspace, size_t workspace_bytes,
-                   void* stream);
+                   int32_t* status, int32_t* rounds, void* workspace,
+                   size_t workspace_bytes, void* stream);
 
 #ifdef __cplusplus
 }

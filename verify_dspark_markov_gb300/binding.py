@@ -68,7 +68,7 @@ def load(path: str | None = None):
             lib.dspark_rnn_sample.argtypes = ([P, i32, P, P, P, i32, P, P, P, P, P, i32, P, P, i32]
                                               + [P] * 4 + [i32] * 3 + [P] * 6 + [sz, P])
             lib.dspark_rnn_sample.restype = i32
-            lib.dspark_sts_fit.argtypes = [P, P, P, i32, i32, P, P, P, sz, P]
+            lib.dspark_sts_fit.argtypes = [P, P, P, i32, i32, P, P, P, P, sz, P]
             lib.dspark_sts_fit.restype = i32
             lib.dspark_status_string.argtypes = [i32]
             lib.dspark_status_string.restype = ctypes.c_char_p
@@ -335,7 +335,8 @@ def sts_fit(conf_logits, labels, mask=None, workspace: Workspace | None = None, 
     """Sequential Temperature Scaling: per block position the inverse
     temperature beta >= 0 of the confidence head, from fp32 [N, gamma]
     confidence logits and accept labels (mask: uint8 [N, gamma] or None).
-    Returns (beta float64 [gamma], status int32 [gamma])."""
+    Returns (beta float64 [gamma], status int32 [gamma], rounds int32
+    [gamma]: the passes each position's search used)."""
     _dev(conf_logits, "conf_logits", torch.float32)
     _dev(labels, "labels", torch.float32)
     if conf_logits.dim() != 2 or labels.shape != conf_logits.shape:
@@ -348,10 +349,11 @@ def sts_fit(conf_logits, labels, mask=None, workspace: Workspace | None = None, 
     dev = conf_logits.device
     if out is None:
         out = (torch.empty((gamma,), dtype=torch.float64, device=dev),
+               torch.empty((gamma,), dtype=torch.int32, device=dev),
                torch.empty((gamma,), dtype=torch.int32, device=dev))
     ws_n = workspace_size(OP_STS_FIT, N, gamma, 8)
     ws = (workspace or _default_ws).get(OP_STS_FIT, ws_n, dev)
     code = load().dspark_sts_fit(_ptr(conf_logits), _ptr(labels), _ptr(mask), N, gamma, _ptr(out[0]),
-                                 _ptr(out[1]), _ptr(ws), ws_n, _stream(stream))
+                                 _ptr(out[1]), _ptr(out[2]), _ptr(ws), ws_n, _stream(stream))
     _check(code, "dspark_sts_fit")
     return out

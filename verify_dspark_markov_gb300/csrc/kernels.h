@@ -203,7 +203,7 @@ struct StsState {
     unsigned int flags;   // bit 0 a counted z != 0, bit 1 a label against the sign of z, bit 2 an invalid pair
     int phase;            // 0 first round (beta = 0), 1 searching, 2 done
     int status;           // 0 fitted, 1 no information, 2 no finite root below the cap, 3 invalid input
-    int pad;
+    int rounds;           // passes whose sums the position used
 };
 struct StsParams {
     const float* conf_logits;  // [N, gamma]
@@ -213,6 +213,7 @@ struct StsParams {
     int gamma;
     double* beta;              // [gamma] out
     int32_t* status;           // [gamma] out
+    int32_t* rounds;           // [gamma] out, or null
     StsState* state;           // [DSPARK_MAX_GAMMA] workspace
     int* active;               // workspace: positions still searching
 };

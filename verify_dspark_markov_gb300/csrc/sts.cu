@@ -129,12 +129,14 @@ __global__ void __launch_bounds__(kStsThreads) sts_pass_kernel(const float* __re
     }
 }
 
-__global__ void sts_update_kernel(StsState* st, int* active, int gamma, double* beta_out, int32_t* status_out) {
+__global__ void sts_update_kernel(StsState* st, int* active, int gamma, double* beta_out, int32_t* status_out,
+                                  int32_t* rounds_out) {
     const int k = threadIdx.x;
     bool finished = false;
     if (k < gamma) {
         StsState s = st[k];
         const double inf = __longlong_as_double(0x7FF0000000000000ll);
+        if (s.phase != 2) ++s.rounds;  // this round's sums are the position's
         if (s.phase == 0) {  // the sums were taken at beta = 0
             s.phase = 2;
             if (s.flags & kInvalid) {
@@ -187,6 +189,7 @@ __global__ void sts_update_kernel(StsState* st, int* active, int gamma, double* 
         st[k] = s;
         beta_out[k] = s.beta;
         status_out[k] = s.status;
+        if (rounds_out) rounds_out[k] = s.rounds;
     }
     const unsigned fin = __ballot_sync(0xFFFFFFFFu, finished);
     if (k == 0 && fin) atomicSub(active, __popc(fin));
@@ -206,7 +209,7 @@ cudaError_t launch_sts_fit(const StsParams& p, cudaStream_t stream) {
     for (int r = 0; r < kStsRounds; ++r) {
         sts_pass_kernel<<<grid, kStsThreads, 0, stream>>>(p.conf_logits, p.labels, p.mask, p.N, p.gamma, p.state,
                                                           p.active);
-        sts_update_kernel<<<1, 32, 0, stream>>>(p.state, p.active, p.gamma, p.beta, p.status);
+        sts_update_kernel<<<1, 32, 0, stream>>>(p.state, p.active, p.gamma, p.beta, p.status, p.rounds);
     }
     return cudaGetLastError();
 }
