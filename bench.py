@@ -18,6 +18,12 @@ in HBM when the timed region starts.  Workloads (``--workload``):
                      width uniform over 0..gamma (seeded): the draft of gamma
                      positions, then the verify of x_1..x_w and the bonus from
                      row w; positions = the sum of (w + 1).
+  rnn_decode_tile    the decode verify tile drafted by the RNN head instead
+                     of the Markov head (a GRU state at rank 256 carried
+                     across the block gives the bias), then the sampled verify.
+  sts_fit            Sequential Temperature Scaling of a serving log:
+                     4,194,304 blocks x gamma = 7 (confidence logit, 0 / 1
+                     acceptance, mask) pairs; one whole fit per step.
   training_stats     4096 blocks x gamma = 7 fp32 row pairs: L1, accept rate,
                      tau and the weighted loss numerators.
   training_stats_grad  the same row pairs: the gradient of the loss numerators'
@@ -149,9 +155,10 @@ class Clocks:
 class Serving:
     """Draft sampling then exact verify of one batch."""
 
-    def __init__(self, name, w, esize, width=None):
+    def __init__(self, name, w, esize, width=None, gru=None):
         self.name, self.w, self.esize = name, w, esize
         self.width = width  # int32 [B] verify widths, or None (gamma for every request)
+        self.gru = gru      # GRU weights: the RNN head drafts instead of the Markov head
         self.positions = w.B * (w.gamma + 1) if width is None else int((width.cpu().long() + 1).sum())
         self.greedy_only = bool(w.policy.greedy.all()) and w.weights.r == 0
 
@@ -161,6 +168,7 @@ class Serving:
                 "target_rows": w.B * (w.gamma + 1), "draft_rows": w.B * w.gamma,
                 "policy": "greedy" if self.greedy_only else "per-request temperature / top-k / top-p",
                 "markov_rank": w.weights.r, "draft_hidden": w.weights.H,
+                **({} if self.gru is None else {"sequential_head": f"RNN (GRU, rank {w.weights.r})"}),
                 **({} if self.width is None else {
                     "verify_width": f"per request, uniform over 0..{w.gamma} (seeded; mean "
                                     f"{float(self.width.float().mean()):.2f} proposals checked)",
@@ -174,6 +182,9 @@ class Serving:
         self.pol = None if self.greedy_only else w.policy.packed().to(dev)
         self.keys = dict(seed=w.keys.seed.to(dev), request_id=w.keys.request_id.to(dev), pos0=w.keys.pos0.to(dev))
         self.wts = dict(U=w.weights.U, W=w.weights.W, E=w.weights.E, w_conf=w.weights.w_conf)
+        if self.gru is not None:
+            self.gru_dev = dict(Wi=self.gru.Wi.to(dev), Wh=self.gru.Wh.to(dev), bi=self.gru.bi.to(dev),
+                                bh=self.gru.bh.to(dev))
         self.draft_out = dict(proposals=torch.empty((B, g), dtype=torch.int32, device=dev),
                               q=None if self.pol is None else torch.empty((B, g, V), dtype=torch.float32, device=dev),
                               q_at_x=torch.empty((B, g), dtype=torch.float32, device=dev),
@@ -196,10 +207,17 @@ class Serving:
     def draft(self, stream, backbone=None, anchor=None, h=None):
         w = self.w
         d = self.draft_out
-        self.ds.markov_sample(backbone if backbone is not None else w.backbone,
-                              anchor if anchor is not None else w.anchor,
-                              h=h if h is not None else w.h, policy=self.pol, workspace=self.ws, out=d,
-                              stream=stream, **self.wts, **(self.keys if self.pol is not None else {}))
+        bb = backbone if backbone is not None else w.backbone
+        an = anchor if anchor is not None else w.anchor
+        hh = h if h is not None else w.h
+        keys = self.keys if self.pol is not None else {}
+        if self.gru is not None:
+            self.ds.rnn_sample(bb, an, self.wts["U"], self.wts["W"], **self.gru_dev, h=hh, E=self.wts["E"],
+                               w_conf=self.wts["w_conf"], policy=self.pol, workspace=self.ws, out=d, stream=stream,
+                               **keys)
+        else:
+            self.ds.markov_sample(bb, an, h=hh, policy=self.pol, workspace=self.ws, out=d, stream=stream,
+                                  **self.wts, **keys)
 
     def verify(self, stream, target=None, width=None):
         d = self.draft_out
@@ -217,8 +235,10 @@ class Serving:
         w, e = self.w, self.esize
         B, g, V, r, H = w.B, w.gamma, w.V, w.weights.r, w.weights.H
         sampled = int((self.w.policy.greedy == 0).sum()) if self.pol is not None else 0
+        passes = 1 if self.gru is None else 2     # the RNN head's bias: a hi and a lo product
         draft = (B * g * V * e                      # backbone rows
-                 + g * (V * r * 2 + B * r * 2)      # the rank-r matrix per step, gathered U rows
+                 + passes * g * (V * r * 2 + B * r * 2)  # the rank-r matrix per product, gathered rows
+                 + (0 if self.gru is None else g * (2 * 3 * r * r * 2 + B * V * 4 * 2))  # GRU weights; z_A out, in
                  + sampled * g * V * 4              # q rows of sampled requests
                  + B * g * (H * 2 * 2 if w.h is not None else 0)  # h and E rows for c_k
                  + B * 4 + B * g * 12)              # anchors, proposals, q(x), c_k
@@ -237,7 +257,8 @@ class Serving:
 
     def flops(self):
         w = self.w
-        return {"draft": 2 * w.B * w.weights.r * w.V * w.gamma}
+        passes = 1 if self.gru is None else 2
+        return {"draft": passes * 2 * w.B * w.weights.r * w.V * w.gamma}
 
     def e2e_step(self, stream, dev_inputs, host_inputs, host_outputs):
         for d, h in zip(dev_inputs, host_inputs):
@@ -278,7 +299,13 @@ class Serving:
             sl = slice(b, b + 1)
             k = {n: v[sl] for n, v in keys.items()}
             p = {n: v[sl] for n, v in pol.items()}
-            d = oracle.markov_sample(bb[sl], anchor[sl], U, Wm, None if hh is None else hh[sl], E, wc, p, **k)
+            if self.gru is not None:
+                gw = self.gru
+                d = oracle.rnn_sample(bb[sl], anchor[sl], U, Wm, synth.host(gw.Wi), synth.host(gw.Wh),
+                                      gw.bi.cpu().numpy(), gw.bh.cpu().numpy(), None if hh is None else hh[sl], E,
+                                      wc, p, **k)
+            else:
+                d = oracle.markov_sample(bb[sl], anchor[sl], U, Wm, None if hh is None else hh[sl], E, wc, p, **k)
             oracle.verify(tg[sl], d["proposals"], d["q"], d["q_at_x"], p, **k,
                           width=None if wd is None else wd[sl])
             done += 1
@@ -430,6 +457,83 @@ class StatsGrad(Stats):
                           f"recipe in {el:.1f} s, single-threaded C++ oracle (gradient)"}
 
 
+class StsFit:
+    """Sequential Temperature Scaling of one serving log: a whole fit (every
+    round the device search takes) per step."""
+
+    def __init__(self, log, blocks=None):
+        self.log = log
+        self.name = "sts_fit"
+        self.positions = log.N * log.gamma  # pairs
+        self.blocks = blocks or log.N
+
+    def config(self):
+        lg = self.log
+        return {"workload": self.name, "blocks": self.blocks, "gamma": lg.gamma, "pairs": self.blocks * lg.gamma,
+                "labels": "0/1 acceptances drawn from a miscalibrated confidence (T 0.6..3 over positions)",
+                "mask": "90 % of the pairs counted"}
+
+    def setup(self, ds, dev):
+        lg = self.log
+        self.ds = ds
+        self.ws = ds.Workspace()
+        self.out = (torch.empty((lg.gamma,), dtype=torch.float64, device=dev),
+                    torch.empty((lg.gamma,), dtype=torch.int32, device=dev),
+                    torch.empty((lg.gamma,), dtype=torch.int32, device=dev))
+        self.inputs = [lg.conf_logits, lg.labels, lg.mask]
+
+    def fit(self, stream, z=None, a=None, m=None):
+        lg = self.log
+        self.ds.sts_fit(z if z is not None else lg.conf_logits, a if a is not None else lg.labels,
+                        m if m is not None else lg.mask, workspace=self.ws, out=self.out, stream=stream)
+
+    def parts(self):
+        return [("sts_fit", self.fit)]
+
+    def bytes(self):
+        """Every pass reads each pair once (z, a: 4 B each; the mask byte)
+        until the last position stops: the largest rounds count."""
+        return {"sts_fit": int(self.out[2].max()) * self.positions * 9 + 64}
+
+    def flops(self):
+        return {}
+
+    def e2e_step(self, stream, dev_inputs, host_inputs, host_outputs):
+        for d, h in zip(dev_inputs, host_inputs):
+            d.copy_(h, non_blocking=True)
+        self.fit(stream, *dev_inputs)
+        for h, d in zip(host_outputs, self.outputs()):
+            h.copy_(d, non_blocking=True)
+
+    def outputs(self):
+        return [self.out[0], self.out[1]]
+
+    def check(self):
+        assert int((self.out[1] != 0).sum()) == 0, "a position of the benchmark log did not fit"
+
+    def cpu_sample(self, budget_s, max_requests=None):
+        """The oracle's fit on chunks of 4096 blocks of the log, one after the
+        other, single-threaded."""
+        import oracle
+        oracle.build()
+        lg = self.log
+        chunk = min(4096, lg.N)
+        z, a, m = (lg.conf_logits.cpu().numpy(), lg.labels.cpu().numpy(), lg.mask.cpu().numpy())
+        done, n0, t0 = 0, 0, time.perf_counter()
+        while True:
+            sl = slice(n0, n0 + chunk)
+            oracle.sts_fit(z[sl], a[sl], m[sl])
+            done += 1
+            n0 = (n0 + chunk) % max(1, lg.N - chunk + 1)
+            el = time.perf_counter() - t0
+            if el >= budget_s or (max_requests and done >= max_requests):
+                break
+        pairs = done * chunk * lg.gamma
+        return {"value": pairs / el, "unit": UNIT, "cores": 1, "kind": "oracle",
+                "sample": f"{done} fits of {chunk} blocks x {lg.gamma} pairs ({pairs} pairs) in {el:.1f} s, "
+                          f"single-threaded C++ oracle (bisection)"}
+
+
 def make_workload(name, device, stats_blocks=4096):
     if name == "full_decode_tile":
         return Serving(name, synth.full_decode_tile(device=device), 2)
@@ -437,6 +541,11 @@ def make_workload(name, device, stats_blocks=4096):
         return Serving(name, synth.decode_verify_tile(device=device), 2)
     if name == "mixed_serving":
         return Serving(name, synth.mixed_serving(device=device), 2)
+    if name == "rnn_decode_tile":
+        w = synth.decode_verify_tile(device=device)
+        return Serving(name, w, 2, gru=synth.gru_weights(w.weights.r, synth._gen(1009, "cpu"), device))
+    if name == "sts_fit":
+        return StsFit(synth.sts_log(device=device))
     if name == "decode_verify_tile_width":
         w = synth.decode_verify_tile(device=device)
         return Serving(name, w, 2, width=synth.verify_widths(w.B, w.gamma))
@@ -448,7 +557,7 @@ def make_workload(name, device, stats_blocks=4096):
 
 
 WORKLOADS = ("full_decode_tile", "decode_verify_tile", "mixed_serving", "decode_verify_tile_width",
-             "training_stats", "training_stats_grad")
+             "rnn_decode_tile", "training_stats", "training_stats_grad", "sts_fit")
 
 
 # ------------------------------------------------------------------ GPU arm
@@ -543,7 +652,8 @@ def run_gpu(args):
     achieved = nbytes[dom] / (part_ms[dom] * 1e-3) / 1e9
     kernel = {"full_decode_tile": "argmax_rows_kernel<bf16> (draft + verify launches)",
               "training_stats": "stats_pairs_kernel<f32> (+ stats_blocks_kernel, stats_total_kernel)",
-              "training_stats_grad": "stats_grad_kernel<f32>"}.get(
+              "training_stats_grad": "stats_grad_kernel<f32>",
+              "sts_fit": "sts_pass_kernel (+ sts_update_kernel per round)"}.get(
                   wl.name, {"draft": "markov_sample (markov_bias_kernel + markov_step_kernel per position)",
                             "verify": "verify_rows_kernel<bf16>" if getattr(wl, "width", None) is None
                             else "verify_rows_kernel<bf16, width>"}.get(dom, dom))
@@ -560,7 +670,7 @@ def run_gpu(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "f32" if isinstance(wl, Stats) else "bf16",
+        "dtype": "f32" if isinstance(wl, (Stats, StsFit)) else "bf16",
         "data": "synthetic",
         "config": dict(wl.config(), l2="inputs larger than L2, plus a 2 x L2 read of another buffer "
                                        "before every step",
@@ -584,8 +694,12 @@ def run_gpu(args):
         g = wl.w.gamma
         if wl.name == "full_decode_tile":
             launches = 2
+        elif wl.gru is not None:  # GRU step, the hi and lo products, the policy step; confidence; verify
+            launches = 4 * g + (1 if wl.w.h is not None else 0) + 1
         else:
             launches = (2 * g if wl.w.weights.r else g) + (1 if wl.w.h is not None else 0) + 1
+    elif isinstance(wl, StsFit):  # init, then 64 rounds of a pass and an update (late passes return at once)
+        launches = 1 + 2 * 64
     else:  # the statistics: pairs + per-block + total kernels; the gradient: one kernel
         launches = 1 if isinstance(wl, StatsGrad) else 3
     result["gpu_launches"] = launches * steps
@@ -611,6 +725,8 @@ def make_workload_small(name):
         return Stats(synth.training_stats(device="cpu", N=64), blocks=4096)
     if name == "training_stats_grad":
         return StatsGrad(synth.training_stats(device="cpu", N=64), blocks=4096)
+    if name == "sts_fit":
+        return StsFit(synth.sts_log(device="cpu", N=65_536), blocks=4_194_304)
     return make_workload(name, "cpu")
 
 

@@ -300,6 +300,29 @@ def gru_weights(r, g, device, scale=None) -> GruWeights:
                       _normal((3 * r,), 0.1, g, device).contiguous())
 
 
+@dataclass
+class StsLog:
+    N: int
+    gamma: int
+    conf_logits: torch.Tensor  # fp32 [N, gamma]
+    labels: torch.Tensor       # fp32 [N, gamma], 0 / 1 acceptances
+    mask: torch.Tensor         # uint8 [N, gamma]
+    temperature: torch.Tensor  # fp32 [gamma]: the miscalibration the labels were drawn with
+
+
+def sts_log(N=4_194_304, gamma=7, device="cpu", seed=1008, counted=0.9) -> StsLog:
+    """A serving log for Sequential Temperature Scaling: confidence logits
+    N(0, 2^2) per block position, observed 0 / 1 acceptances drawn as
+    Bernoulli(sigmoid(z / T_k)) with T_k spread over 0.6..3 (an over- to
+    under-confident head), and a mask counting `counted` of the pairs."""
+    g = _gen(seed, device)
+    z = _normal((N, gamma), 2.0, g, device)
+    T = torch.linspace(0.6, 3.0, gamma, device=device)
+    a = (torch.rand((N, gamma), generator=g, device=device) < torch.sigmoid(z / T)).to(torch.float32)
+    m = (torch.rand((N, gamma), generator=g, device=device) < counted).to(torch.uint8)
+    return StsLog(N, gamma, z.contiguous(), a.contiguous(), m.contiguous(), T)
+
+
 def verify_widths(B, gamma, seed=1007, invalid=0, device="cpu") -> torch.Tensor:
     """Per-request verify widths, int32 [B]: uniform over 0..gamma (a
     scheduler's choice of how many proposals to check; the pages pick it from

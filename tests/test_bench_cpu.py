@@ -32,3 +32,19 @@ def test_reference_arm_width_workload():
     assert line["config"]["workload"] == "decode_verify_tile_width"
     assert "verify_width" in line["config"] and line["config"]["verified_rows"] < 64 * 6
     assert line["value"] > 0 and "w + 1 rows" in line["cpu_baseline"]["sample"]
+
+
+def _reference_line(workload):
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
+                          "--warmup", "3", "--workload", workload, "--cpu-seconds", "2"],
+                         capture_output=True, text=True, timeout=900, cwd=ROOT)
+    assert out.returncode == 0, out.stderr[-2000:]
+    return json.loads(out.stdout.strip().splitlines()[-1])
+
+
+def test_reference_arm_rnn_and_sts_workloads():
+    line = _reference_line("rnn_decode_tile")
+    assert line["config"]["sequential_head"].startswith("RNN") and line["value"] > 0
+    line = _reference_line("sts_fit")
+    assert line["config"]["workload"] == "sts_fit" and line["config"]["pairs"] == 4_194_304 * 7
+    assert line["value"] > 0 and "bisection" in line["cpu_baseline"]["sample"]
