@@ -535,7 +535,6 @@ __device__ void row_policy_radix(Smem& sm, cg::cluster_group& cl, const Slice& s
     res.mass = static_cast<unsigned long long>(kFix);
     if (pol.greedy) return;
     const float inv_t = pol.inv_t;
-    const int tid = threadIdx.x;
 
     // ---- top-k: exactly k tokens
     uint32_t tau_k = 0;      // key > 0 holds for every non-NaN value: "all"
