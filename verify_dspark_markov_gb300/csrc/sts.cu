@@ -13,10 +13,11 @@
 //    takes whole rows n (gamma contiguous pairs) with per-position sums in
 //    registers; warps reduce by shuffles, CTAs through shared memory, and
 //    one double atomic per position and CTA lands in the position's state.
-//  * sts_update_kernel - one warp, lane k: the degenerate cases on the first
-//    round (taken at beta = 0), then a Newton step kept inside the bracket
-//    [lo, hi] of the root, bisection (or doubling while hi is open) when the
-//    step leaves it; the sums are cleared for the next round.
+//  * sts_update_kernel - one warp, lane k: sts_search_step (sts_search.cuh)
+//    on position k - the degenerate cases on the first round (taken at
+//    beta = 0), then a Newton step kept inside the bracket [lo, hi] of the
+//    root, bisection (or doubling while hi is open) when the step leaves it;
+//    the sums are cleared for the next round.
 // Once every position has converged the remaining passes return at once.
 // HBM-bound: 9 bytes a pair a round (8 without a mask).
 
@@ -24,6 +25,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "sts_search.cuh"
 
 namespace dspark {
 
@@ -32,8 +34,7 @@ namespace {
 constexpr int kStsThreads = 256;
 constexpr int kStsWarps = kStsThreads / 32;
 constexpr int kG = DSPARK_MAX_GAMMA;
-constexpr double kBetaMax = 1048576.0;  // 2^20
-constexpr unsigned kInformative = 1u, kViolated = 2u, kInvalid = 4u;
+constexpr unsigned kInformative = kStsInformative, kViolated = kStsViolated, kInvalid = kStsInvalid;
 // Rounds enqueued per fit: enough for beta to double from 1 to the cap (20)
 // and then halve a bracket to below 1e-7 of its width (24), with margin;
 // Newton usually converges in a handful and the later passes return at once.
@@ -135,57 +136,7 @@ __global__ void sts_update_kernel(StsState* st, int* active, int gamma, double* 
     bool finished = false;
     if (k < gamma) {
         StsState s = st[k];
-        const double inf = __longlong_as_double(0x7FF0000000000000ll);
-        if (s.phase != 2) ++s.rounds;  // this round's sums are the position's
-        if (s.phase == 0) {  // the sums were taken at beta = 0
-            s.phase = 2;
-            if (s.flags & kInvalid) {
-                s.beta = __longlong_as_double(0x7FF8000000000000ll);
-                s.status = 3;
-            } else if (!(s.flags & kInformative)) {
-                s.beta = 1.0;
-                s.status = 1;
-            } else if (!(s.flags & kViolated)) {  // labels agree with the sign of z: no finite root
-                s.beta = kBetaMax;
-                s.status = 2;
-            } else if (s.s1 >= 0.0) {
-                s.beta = 0.0;
-                s.status = 0;
-            } else {
-                s.lo = 0.0;
-                s.hi = inf;
-                s.beta = 1.0;
-                s.status = 0;
-                s.phase = 1;
-            }
-            finished = s.phase == 2;
-        } else if (s.phase == 1) {
-            const double g = s.s1, h = s.s2, b = s.beta;
-            if (g < 0.0) s.lo = b;
-            else s.hi = b;
-            if (g < 0.0 && b >= kBetaMax) {  // the root lies beyond the cap
-                s.beta = kBetaMax;
-                s.status = 2;
-                s.phase = 2;
-            } else if (g == 0.0) {
-                s.phase = 2;
-            } else {
-                const double step = h > 0.0 ? b - g / h : b;
-                double next;
-                if (s.hi == inf) next = (step > b && step < inf) ? step : 2.0 * b;
-                else next = (step > s.lo && step < s.hi) ? step : 0.5 * (s.lo + s.hi);
-                next = fmin(next, kBetaMax);
-                // stop at the accuracy the fp32 pair terms allow: nearer
-                // the root their rounding decides the slope's sign
-                const bool converged = fabs(next - b) <= 1e-7 * b ||
-                                       (s.hi != inf && s.hi - s.lo <= 1e-7 * s.hi);
-                s.beta = next;
-                if (converged) s.phase = 2;
-            }
-            finished = s.phase == 2;
-        }
-        s.s1 = 0.0;
-        s.s2 = 0.0;
+        finished = sts_search_step(s);
         st[k] = s;
         beta_out[k] = s.beta;
         status_out[k] = s.status;
