@@ -43,6 +43,7 @@ import json
 import os
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -96,10 +97,11 @@ class Clocks:
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, device_index: int):
+    def __init__(self, device_index: int, path: str | None = None):
         self.dev = device_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+        # the raw samples: a temporary file unless --clocks-csv names one to keep
+        self.path = path or os.path.join(tempfile.gettempdir(), f"dspark_clocks_{os.getpid()}.csv")
 
     def __enter__(self):
         try:
@@ -459,7 +461,7 @@ class StatsGrad(Stats):
 
 class StsFit:
     """Sequential Temperature Scaling of one serving log: a whole fit (every
-    round the device search takes) per step."""
+    pass the device search takes) per step."""
 
     def __init__(self, log, blocks=None):
         self.log = log
@@ -492,7 +494,7 @@ class StsFit:
 
     def bytes(self):
         """Every pass reads each pair once (z, a: 4 B each; the mask byte)
-        until the last position stops: the largest rounds count."""
+        until the last position stops: the largest passes count."""
         return {"sts_fit": int(self.out[2].max()) * self.positions * 9 + 64}
 
     def flops(self):
@@ -608,7 +610,7 @@ def run_gpu(args):
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    with Clocks(local) as clk:
+    with Clocks(local, args.clocks_csv) as clk:
         time.sleep(0.3)  # let the sampler start
         t0 = time.perf_counter()
         w0 = time.time()
@@ -653,7 +655,7 @@ def run_gpu(args):
     kernel = {"full_decode_tile": "argmax_rows_kernel<bf16> (draft + verify launches)",
               "training_stats": "stats_pairs_kernel<f32> (+ stats_blocks_kernel, stats_total_kernel)",
               "training_stats_grad": "stats_grad_kernel<f32>",
-              "sts_fit": "sts_pass_kernel (+ sts_update_kernel per round)"}.get(
+              "sts_fit": "sts_pass_kernel (+ sts_update_kernel per pass)"}.get(
                   wl.name, {"draft": "markov_sample (markov_bias_kernel + markov_step_kernel per position)",
                             "verify": "verify_rows_kernel<bf16>" if getattr(wl, "width", None) is None
                             else "verify_rows_kernel<bf16, width>"}.get(dom, dom))
@@ -698,7 +700,7 @@ def run_gpu(args):
             launches = 4 * g + (1 if wl.w.h is not None else 0) + 1
         else:
             launches = (2 * g if wl.w.weights.r else g) + (1 if wl.w.h is not None else 0) + 1
-    elif isinstance(wl, StsFit):  # init, then 64 rounds of a pass and an update (late passes return at once)
+    elif isinstance(wl, StsFit):  # init, then 64 passes and their updates (late passes return at once)
         launches = 1 + 2 * 64
     else:  # the statistics: pairs + per-block + total kernels; the gradient: one kernel
         launches = 1 if isinstance(wl, StatsGrad) else 3
@@ -765,6 +767,8 @@ def main():
                     help="cap on the timed region's GPU time (fewer steps for slow workloads)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--clocks-csv", default=None,
+                    help="keep the nvidia-smi samples of the timed region in this file")
     ap.add_argument("--stats-blocks", type=int, default=4096,
                     help="training_stats only: blocks of the workload (smaller sizes for profiling captures)")
     args = ap.parse_args()

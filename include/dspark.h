@@ -400,19 +400,19 @@ int dspark_version(void);
  *                counted pair with a non-finite z or a label outside [0, 1]
  *                (beta = NaN).  A BCE slope >= 0 at beta = 0 gives beta = 0
  *                (status 0).
- *   rounds       int32 [gamma] out, or NULL: the passes over the pairs each
+ *   passes       int32 [gamma] out, or NULL: the passes over the pairs each
  *                position's search used (every pass reads all positions
  *                until the last one stops).
  *   workspace    dspark_workspace_size(DSPARK_OP_STS_FIT, N, gamma, 0, 0, 0)
  *                bytes; every region is written before it is read.
  * N = 0 is valid (every position reports status 1).  The fit is a root
  * search on the device (Newton steps inside a bracket, a fixed number of
- * rounds enqueued); beta is accurate to about 1e-6 relative (its sums are
+ * passes enqueued); beta is accurate to about 1e-6 relative (its sums are
  * fp32 per thread, fp64 across threads).
  */
 int dspark_sts_fit(const float* conf_logits, const float* labels,
                    const uint8_t* mask, int N, int gamma, double* beta,
-                   int32_t* status, int32_t* rounds, void* workspace,
+                   int32_t* status, int32_t* passes, void* workspace,
                    size_t workspace_bytes, void* stream);
 
 #ifdef __cplusplus

@@ -97,8 +97,8 @@ def test_sts_fit_rejects_invalid_arguments(lib):
     ws = ds.workspace_size(ds.OP_STS_FIT, 100, 5, 0)
     assert 0 < ws <= 4096
     assert ds.workspace_size(ds.OP_STS_FIT, 100, 0, 0) == 0 and ds.workspace_size(ds.OP_STS_FIT, -1, 5, 0) == 0
-    call = lambda N=100, g=5, z=FAKE, a=FAKE, beta=FAKE, st=FAKE, rounds=None, wsb=ws: f(z, a, None, N, g, beta, st,
-                                                                                       rounds, FAKE, wsb, None)
+    call = lambda N=100, g=5, z=FAKE, a=FAKE, beta=FAKE, st=FAKE, passes=None, wsb=ws: f(z, a, None, N, g, beta, st,
+                                                                                       passes, FAKE, wsb, None)
     assert call(g=0) == binding.EINVAL
     assert call(g=17) == binding.EINVAL
     assert call(N=-1) == binding.EINVAL
@@ -106,7 +106,7 @@ def test_sts_fit_rejects_invalid_arguments(lib):
     assert call(beta=None) == binding.EINVAL
     assert call(beta=FAKE_ODD) == binding.EINVAL                   # fp64 output, 8-byte aligned
     assert call(z=ctypes.c_void_p(0x7F0000000002)) == binding.EINVAL
-    assert call(rounds=ctypes.c_void_p(0x7F0000000002)) == binding.EINVAL   # int32 output, 4-byte aligned
+    assert call(passes=ctypes.c_void_p(0x7F0000000002)) == binding.EINVAL   # int32 output, 4-byte aligned
     assert call(wsb=8) == binding.ENOSPC
 
 

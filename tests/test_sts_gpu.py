@@ -27,11 +27,11 @@ def ds():
 def _both(ds, oracle, z, a, mask=None):
     ref = oracle.sts_fit(z, a, mask)
     dev = torch.device("cuda")
-    beta, status, rounds = ds.sts_fit(torch.from_numpy(z).to(dev), torch.from_numpy(a).to(dev),
+    beta, status, passes = ds.sts_fit(torch.from_numpy(z).to(dev), torch.from_numpy(a).to(dev),
                                       None if mask is None else torch.from_numpy(mask).to(dev))
     torch.cuda.synchronize()
-    # every position stops well inside the enqueued rounds
-    assert int(rounds.max()) < 64
+    # every position stops well inside the enqueued passes
+    assert int(passes.max()) < 64
     return ref, beta.cpu().numpy(), status.cpu().numpy()
 
 

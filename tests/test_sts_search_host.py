@@ -18,7 +18,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 class StsState(ctypes.Structure):
     _fields_ = [("beta", ctypes.c_double), ("lo", ctypes.c_double), ("hi", ctypes.c_double),
                 ("s1", ctypes.c_double), ("s2", ctypes.c_double), ("flags", ctypes.c_uint32),
-                ("phase", ctypes.c_int32), ("status", ctypes.c_int32), ("rounds", ctypes.c_int32)]
+                ("phase", ctypes.c_int32), ("status", ctypes.c_int32), ("passes", ctypes.c_int32)]
 
 
 @pytest.fixture(scope="module")
@@ -39,7 +39,7 @@ def search(tmp_path_factory):
     return lib
 
 
-def _fit(lib, z, a, mask=None, rounds=64):
+def _fit(lib, z, a, mask=None, passes=64):
     """Whole fits of every position with the library's search; the pass sums
     formed as the device forms them."""
     N, G = z.shape
@@ -55,7 +55,7 @@ def _fit(lib, z, a, mask=None, rounds=64):
             flags |= 1
         if np.any(((zk > 0) & (ak < 1)) | ((zk < 0) & (ak > 0))):
             flags |= 2
-        for _ in range(rounds):
+        for _ in range(passes):
             b = np.float32(st.beta)
             with np.errstate(over="ignore", invalid="ignore"):
                 sg = (np.float32(1) / (np.float32(1) + np.exp(-b * zk))).astype(np.float32)
@@ -64,7 +64,7 @@ def _fit(lib, z, a, mask=None, rounds=64):
             st.s1, st.s2, st.flags = float(t1.astype(np.float64).sum()), float(t2.astype(np.float64).sum()), flags
             if lib.sts_search_step_host(ctypes.byref(st)):
                 break
-        beta[k], status[k], used[k] = st.beta, st.status, st.rounds
+        beta[k], status[k], used[k] = st.beta, st.status, st.passes
     return beta, status, used
 
 

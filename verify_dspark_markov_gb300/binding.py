@@ -335,7 +335,7 @@ def sts_fit(conf_logits, labels, mask=None, workspace: Workspace | None = None, 
     """Sequential Temperature Scaling: per block position the inverse
     temperature beta >= 0 of the confidence head, from fp32 [N, gamma]
     confidence logits and accept labels (mask: uint8 [N, gamma] or None).
-    Returns (beta float64 [gamma], status int32 [gamma], rounds int32
+    Returns (beta float64 [gamma], status int32 [gamma], passes int32
     [gamma]: the passes each position's search used)."""
     _dev(conf_logits, "conf_logits", torch.float32)
     _dev(labels, "labels", torch.float32)

@@ -467,14 +467,14 @@ int dspark_accept_stats_grad(const void* draft, const void* target, int dtype, c
 
 
 int dspark_sts_fit(const float* conf_logits, const float* labels, const uint8_t* mask, int N, int gamma,
-                   double* beta, int32_t* status, int32_t* rounds, void* workspace, size_t workspace_bytes,
+                   double* beta, int32_t* status, int32_t* passes, void* workspace, size_t workspace_bytes,
                    void* stream) {
     if (N < 0 || gamma < 1 || gamma > DSPARK_MAX_GAMMA) return DSPARK_EINVAL;
     if (!beta || !status) return DSPARK_EINVAL;
     if (N > 0 && (!conf_logits || !labels)) return DSPARK_EINVAL;
     if ((reinterpret_cast<uintptr_t>(conf_logits) & 3u) || (reinterpret_cast<uintptr_t>(labels) & 3u) ||
         (reinterpret_cast<uintptr_t>(beta) & 7u) || (reinterpret_cast<uintptr_t>(status) & 3u) ||
-        (reinterpret_cast<uintptr_t>(rounds) & 3u))
+        (reinterpret_cast<uintptr_t>(passes) & 3u))
         return DSPARK_EINVAL;
     if (!workspace || workspace_bytes < sts_workspace()) return DSPARK_ENOSPC;
     StsParams p{};
@@ -485,7 +485,7 @@ int dspark_sts_fit(const float* conf_logits, const float* labels, const uint8_t*
     p.gamma = gamma;
     p.beta = beta;
     p.status = status;
-    p.rounds = rounds;
+    p.passes = passes;
     p.state = at<StsState>(workspace, 0);
     p.active = at<int>(workspace, sts_active_offset());
     return launch_sts_fit(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? DSPARK_OK : DSPARK_ECUDA;

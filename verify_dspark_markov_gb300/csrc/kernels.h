@@ -199,11 +199,11 @@ cudaError_t launch_accept_stats_grad(const StatsGradParams& p, cudaStream_t stre
 struct StsState {
     double beta;          // the current iterate (the answer once phase == 2)
     double lo, hi;        // bracket of the root (hi = +inf until a slope >= 0 is seen)
-    double s1, s2;        // this round's slope and curvature sums
+    double s1, s2;        // this pass's slope and curvature sums
     unsigned int flags;   // bit 0 a counted z != 0, bit 1 a label against the sign of z, bit 2 an invalid pair
-    int phase;            // 0 first round (beta = 0), 1 searching, 2 done
+    int phase;            // 0 first pass (beta = 0), 1 searching, 2 done
     int status;           // 0 fitted, 1 no information, 2 no finite root below the cap, 3 invalid input
-    int rounds;           // passes whose sums the position used
+    int passes;           // passes whose sums the position used
 };
 struct StsParams {
     const float* conf_logits;  // [N, gamma]
@@ -213,7 +213,7 @@ struct StsParams {
     int gamma;
     double* beta;              // [gamma] out
     int32_t* status;           // [gamma] out
-    int32_t* rounds;           // [gamma] out, or null
+    int32_t* passes;           // [gamma] out, or null
     StsState* state;           // [DSPARK_MAX_GAMMA] workspace
     int* active;               // workspace: positions still searching
 };

@@ -5,7 +5,7 @@
 // is convex in beta and its slope sum z (sigmoid(beta z) - a) does not
 // decrease, so the fit is the slope's root.
 //
-// The fit runs on the device in rounds; the host only enqueues them:
+// The fit runs on the device in passes; the host only enqueues them:
 //  * sts_pass_kernel - one streaming pass over the pairs at the current
 //    beta_k of every position: the slope and the curvature
 //    sum z^2 sigmoid (1 - sigmoid) per position, and exact flags (a counted
@@ -14,12 +14,12 @@
 //    registers; warps reduce by shuffles, CTAs through shared memory, and
 //    one double atomic per position and CTA lands in the position's state.
 //  * sts_update_kernel - one warp, lane k: sts_search_step (sts_search.cuh)
-//    on position k - the degenerate cases on the first round (taken at
+//    on position k - the degenerate cases on the first pass (taken at
 //    beta = 0), then a Newton step kept inside the bracket [lo, hi] of the
 //    root, bisection (or doubling while hi is open) when the step leaves it;
-//    the sums are cleared for the next round.
+//    the sums are cleared for the next pass.
 // Once every position has converged the remaining passes return at once.
-// HBM-bound: 9 bytes a pair a round (8 without a mask).
+// HBM-bound: 9 bytes a pair a pass (8 without a mask).
 
 #include <algorithm>
 
@@ -38,7 +38,7 @@ constexpr unsigned kInformative = kStsInformative, kViolated = kStsViolated, kIn
 // Rounds enqueued per fit: enough for beta to double from 1 to the cap (20)
 // and then halve a bracket to below 1e-7 of its width (24), with margin;
 // Newton usually converges in a handful and the later passes return at once.
-constexpr int kStsRounds = 64;
+constexpr int kStsPasses = 64;
 
 __global__ void sts_init_kernel(StsState* st, int* active, int gamma) {
     const int k = threadIdx.x;
@@ -131,7 +131,7 @@ __global__ void __launch_bounds__(kStsThreads) sts_pass_kernel(const float* __re
 }
 
 __global__ void sts_update_kernel(StsState* st, int* active, int gamma, double* beta_out, int32_t* status_out,
-                                  int32_t* rounds_out) {
+                                  int32_t* passes_out) {
     const int k = threadIdx.x;
     bool finished = false;
     if (k < gamma) {
@@ -140,7 +140,7 @@ __global__ void sts_update_kernel(StsState* st, int* active, int gamma, double* 
         st[k] = s;
         beta_out[k] = s.beta;
         status_out[k] = s.status;
-        if (rounds_out) rounds_out[k] = s.rounds;
+        if (passes_out) passes_out[k] = s.passes;
     }
     const unsigned fin = __ballot_sync(0xFFFFFFFFu, finished);
     if (k == 0 && fin) atomicSub(active, __popc(fin));
@@ -157,10 +157,10 @@ cudaError_t launch_sts_fit(const StsParams& p, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     const int64_t want = (p.N + kStsThreads - 1) / kStsThreads;
     const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(want, static_cast<int64_t>(sms) * 8)));
-    for (int r = 0; r < kStsRounds; ++r) {
+    for (int r = 0; r < kStsPasses; ++r) {
         sts_pass_kernel<<<grid, kStsThreads, 0, stream>>>(p.conf_logits, p.labels, p.mask, p.N, p.gamma, p.state,
                                                           p.active);
-        sts_update_kernel<<<1, 32, 0, stream>>>(p.state, p.active, p.gamma, p.beta, p.status, p.rounds);
+        sts_update_kernel<<<1, 32, 0, stream>>>(p.state, p.active, p.gamma, p.beta, p.status, p.passes);
     }
     return cudaGetLastError();
 }

@@ -20,7 +20,7 @@ namespace dspark {
 constexpr double kStsBetaMax = 1048576.0;  // 2^20
 constexpr unsigned kStsInformative = 1u, kStsViolated = 2u, kStsInvalid = 4u;
 
-// Advance `s` by the sums of one pass; true when its search ends this round.
+// Advance `s` by the sums of one pass; true when its search ends with this pass.
 // Phase 0 (the pass at beta = 0) decides the degenerate cases: an invalid
 // pair (status 3, beta NaN), no counted z != 0 (status 1, beta 1), every
 // label agreeing with the sign of its z (no finite root: status 2, beta
@@ -28,7 +28,7 @@ constexpr unsigned kStsInformative = 1u, kStsViolated = 2u, kStsInvalid = 4u;
 __host__ __device__ inline bool sts_search_step(StsState& s) {
     const double inf = std::numeric_limits<double>::infinity();
     if (s.phase == 2) return false;
-    ++s.rounds;  // this round's sums are the position's
+    ++s.passes;  // this pass's sums are the position's
     if (s.phase == 0) {
         s.phase = 2;
         if (s.flags & kStsInvalid) {
