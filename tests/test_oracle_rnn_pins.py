@@ -119,3 +119,29 @@ def test_rnn_bad_anchor(oracle):
                             None, None, None, synth.uniform_policy(B).numpy(), **synth.make_keys(B).numpy())
     assert res["status"][3] == 5 and np.all(res["proposals"][3] == -1)
     assert np.all(np.delete(res["status"], 3) == 0)
+
+
+def test_rnn_confidence_is_the_markov_heads(oracle):
+    """The confidence c_k = sigmoid(w^T [h_k ; E[x_{k-1}]]) is the sampler's,
+    not the head's: with the update gate at one (no bias) the RNN sampler's
+    proposals and confidences equal the backbone-only sampler's."""
+    wts = _weights(46)
+    wts["bi"][R:2 * R] = 60.0
+    rng = np.random.default_rng(10)
+    H = 8
+    backbone = rng.normal(0, 2.0, (B, GAMMA, V)).astype(np.float32)
+    anchor = rng.integers(0, V, B).astype(np.int32)
+    h = rng.normal(0, 1.0, (B, GAMMA, H)).astype(np.float32)
+    E = _bf16(rng.normal(0, 1.0, (V, H)))
+    w_conf = rng.normal(0, 0.5, 2 * H).astype(np.float32)
+    pol = synth.uniform_policy(B).numpy()
+    keys = synth.make_keys(B, seed=11).numpy()
+    res = oracle.rnn_sample(backbone, anchor, wts["U"], wts["W"], wts["Wi"], wts["Wh"], wts["bi"], wts["bh"],
+                            h, E, w_conf, pol, **keys)
+    ref = oracle.markov_sample(backbone, anchor, None, None, h, E, w_conf, pol, **keys)
+    np.testing.assert_array_equal(res["proposals"], ref["proposals"])
+    np.testing.assert_array_equal(res["conf"], ref["conf"])
+    # and it uses x_{k-1}: the first position's confidence reads the anchor's E row
+    e0 = _f64(E)[anchor]
+    want = 1.0 / (1.0 + np.exp(-(h[:, 0].astype(np.float64) @ w_conf[:H] + e0 @ w_conf[H:])))
+    np.testing.assert_allclose(res["conf"][:, 0], want, rtol=1e-6)
