@@ -67,9 +67,9 @@ def _load():
             lib.orc_rnn_sample.restype = None
             lib.orc_sts_fit.argtypes = [P, P, P, i32, i32, P, P]
             lib.orc_sts_fit.restype = None
-            lib.orc_verify.argtypes = [P, i32, P, P, P] + [P] * 7 + [i32, i32, i32] + [P] * 4
+            lib.orc_verify.argtypes = [P, i32, P, P, P] + [P] * 7 + [i32, i32, i32] + [P] * 6
             lib.orc_verify.restype = None
-            lib.orc_verify_width.argtypes = [P, i32, P, P, P] + [P] * 7 + [i32, i32, i32] + [P] * 5
+            lib.orc_verify_width.argtypes = [P, i32, P, P, P] + [P] * 7 + [i32, i32, i32] + [P] * 7
             lib.orc_verify_width.restype = None
             lib.orc_accept_stats.argtypes = [P, P, i32, P, P, P, i32, i32, i32] + [P] * 7
             lib.orc_accept_stats.restype = None
@@ -217,7 +217,9 @@ def verify(target, proposals, q, q_at_x, policy, seed, request_id, pos0, width=N
     [B,gamma]; q float32 [B,gamma,V] or None (all-greedy batch); q_at_x float32
     [B,gamma] or None; width int32 [B] (proposals each request verifies,
     0..gamma) or None (all gamma).  Returns dict(out_tokens, num_accepted,
-    status, indet)."""
+    status, indet, det_tokens, det_nacc): det_tokens [B] leading out_tokens
+    entries decided before the request's first indeterminate decision,
+    det_nacc [B] whether num_accepted was (all of it when indet is False)."""
     target = np.ascontiguousarray(target)
     B, rows, V = target.shape
     gamma = rows - 1
@@ -236,16 +238,21 @@ def verify(target, proposals, q, q_at_x, policy, seed, request_id, pos0, width=N
     nacc = np.zeros(B, np.int32)
     status = np.zeros(B, np.int32)
     indet = np.zeros(B, np.uint8)
+    det_tokens = np.zeros(B, np.int32)
+    det_nacc = np.zeros(B, np.uint8)
     if width is None:
         _load().orc_verify(_ptr(target), _dtype_code(target), _ptr(x), _ptr(qc), _ptr(qx),
                            _ptr(T), _ptr(K), _ptr(P), _ptr(G), _ptr(seed), _ptr(rid), _ptr(p0),
-                           B, gamma, V, _ptr(out), _ptr(nacc), _ptr(status), _ptr(indet))
+                           B, gamma, V, _ptr(out), _ptr(nacc), _ptr(status), _ptr(indet),
+                           _ptr(det_tokens), _ptr(det_nacc))
     else:
         wd = _c(width, np.int32)
         _load().orc_verify_width(_ptr(target), _dtype_code(target), _ptr(x), _ptr(qc), _ptr(qx),
                                  _ptr(T), _ptr(K), _ptr(P), _ptr(G), _ptr(seed), _ptr(rid), _ptr(p0),
-                                 B, gamma, V, _ptr(wd), _ptr(out), _ptr(nacc), _ptr(status), _ptr(indet))
-    return dict(out_tokens=out, num_accepted=nacc, status=status, indet=indet.astype(bool))
+                                 B, gamma, V, _ptr(wd), _ptr(out), _ptr(nacc), _ptr(status), _ptr(indet),
+                                 _ptr(det_tokens), _ptr(det_nacc))
+    return dict(out_tokens=out, num_accepted=nacc, status=status, indet=indet.astype(bool),
+                det_tokens=det_tokens, det_nacc=det_nacc.astype(bool))
 
 
 def accept_stats(draft, target, labels, conf_logits, mask=None):

@@ -480,7 +480,8 @@ extern "C" void orc_verify_width(const void* target, int32_t dtype,
                                  const uint64_t* request_id, const int64_t* pos0,
                                  int32_t B, int32_t gamma, int32_t V,
                                  const int32_t* width, int32_t* out_tokens,
-                                 int32_t* num_accepted, int32_t* status, uint8_t* indet) {
+                                 int32_t* num_accepted, int32_t* status, uint8_t* indet,
+                                 int32_t* det_tokens, uint8_t* det_nacc) {
     const int rows = gamma + 1;
     std::vector<double> z(V), w(V);
     std::vector<std::vector<double>> p(rows, std::vector<double>(V));
@@ -493,6 +494,17 @@ extern "C" void orc_verify_width(const void* target, int32_t dtype,
         num_accepted[b] = -1;
         status[b] = ORC_OK;
         indet[b] = 0;
+        // How much of the request stays exactly comparable: the leading
+        // tokens emitted before its first indeterminate decision, and whether
+        // num_accepted is decided before it (every output while indet is 0).
+        if (det_tokens) det_tokens[b] = rows;
+        if (det_nacc) det_nacc[b] = 1;
+        auto first_indet = [&](int tokens, bool nacc) {
+            if (indet[b]) return;  // only the first one counts
+            indet[b] = 1;
+            if (det_tokens) det_tokens[b] = tokens;
+            if (det_nacc) det_nacc[b] = nacc ? 1 : 0;
+        };
         const int g = width ? width[b] : gamma;  // proposals this request verifies
         if (g < 0 || g > gamma) {
             status[b] = ORC_BAD_TOKEN;
@@ -531,8 +543,9 @@ extern "C" void orc_verify_width(const void* target, int32_t dtype,
             if (qk > 0.0) ratio = pk / qk;
             else ratio = pk > 0.0 ? std::numeric_limits<double>::infinity() : 0.0;
             const double u = orc_uniform(seed[b], request_id[b], pos0[b] + k, 1);
-            if (row_indet[k - 1]) indet[b] = 1;
-            if (std::isfinite(ratio) && std::fabs(u - ratio) < kTol) indet[b] = 1;
+            // decision k is indeterminate: x_1..x_{k-1} stay comparable
+            if (row_indet[k - 1]) first_indet(k - 1, false);
+            if (std::isfinite(ratio) && std::fabs(u - ratio) < kTol) first_indet(k - 1, false);
             const bool accept = pk > 0.0 && u < ratio;
             if (!accept) { rejected_at = k; break; }
         }
@@ -553,15 +566,16 @@ extern "C" void orc_verify_width(const void* target, int32_t dtype,
             for (int i = 0; i < j - 1; ++i) out[i] = x[i];
             out[j - 1] = token;
             num_accepted[b] = j - 1;
+            if (margin < kTol) first_indet(j - 1, true);  // only the drawn token
         } else {
-            if (row_indet[g]) indet[b] = 1;
+            if (row_indet[g]) first_indet(g, true);
             const double u = orc_uniform(seed[b], request_id[b], pos0[b] + g + 1, 2);
             token = orc_sample_index(p[g].data(), V, u, &margin);
             for (int i = 0; i < g; ++i) out[i] = x[i];
             out[g] = token;
             num_accepted[b] = g;
+            if (margin < kTol) first_indet(g, true);
         }
-        if (margin < kTol) indet[b] = 1;
     }
 }
 
@@ -573,9 +587,10 @@ extern "C" void orc_verify(const void* target, int32_t dtype,
                            const uint64_t* request_id, const int64_t* pos0,
                            int32_t B, int32_t gamma, int32_t V,
                            int32_t* out_tokens, int32_t* num_accepted,
-                           int32_t* status, uint8_t* indet) {
+                           int32_t* status, uint8_t* indet, int32_t* det_tokens, uint8_t* det_nacc) {
     orc_verify_width(target, dtype, proposals, q, q_at_x, temperature, top_k, top_p, greedy, seed,
-                     request_id, pos0, B, gamma, V, nullptr, out_tokens, num_accepted, status, indet);
+                     request_id, pos0, B, gamma, V, nullptr, out_tokens, num_accepted, status, indet,
+                     det_tokens, det_nacc);
 }
 
 // ---------------------------------------------------------------------------

@@ -104,14 +104,17 @@ void orc_rnn_sample(const void* backbone, int32_t dtype, const int32_t* anchor,
 
 /* (b) Exact verify [FT Exact decoding semantics; PT Acceptance].
  * out_tokens [B, gamma+1] (-1 after the emitted tokens), num_accepted [B]
- * (-1 for a failed request), status [B], indet [B]. */
+ * (-1 for a failed request), status [B], indet [B].  det_tokens [B] and
+ * det_nacc [B] (each may be NULL): the leading out_tokens entries decided
+ * before the request's first indeterminate decision, and 1 if num_accepted
+ * was decided before it (gamma + 1 and 1 when indet is 0). */
 void orc_verify(const void* target, int32_t dtype, const int32_t* proposals,
                 const float* q, const float* q_at_x, const float* temperature,
                 const int32_t* top_k, const float* top_p, const int32_t* greedy,
                 const uint64_t* seed, const uint64_t* request_id,
                 const int64_t* pos0, int32_t B, int32_t gamma, int32_t V,
                 int32_t* out_tokens, int32_t* num_accepted, int32_t* status,
-                uint8_t* indet);
+                uint8_t* indet, int32_t* det_tokens, uint8_t* det_nacc);
 /* (b') The same verify over a per-request width: request b checks its first
  * width[b] proposals (0..gamma) against target rows 0..width[b] and draws the
  * bonus from row width[b]; width NULL = gamma for every request.  A width
@@ -122,7 +125,7 @@ void orc_verify_width(const void* target, int32_t dtype, const int32_t* proposal
                       const uint64_t* seed, const uint64_t* request_id,
                       const int64_t* pos0, int32_t B, int32_t gamma, int32_t V,
                       const int32_t* width, int32_t* out_tokens, int32_t* num_accepted,
-                      int32_t* status, uint8_t* indet);
+                      int32_t* status, uint8_t* indet, int32_t* det_tokens, uint8_t* det_nacc);
 
 /* (c) Analytical acceptance statistics [MB Training objective; Acceptance
  * and confidence; Loss return contract].  draft/target [N,gamma,V] at T=1

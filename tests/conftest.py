@@ -7,11 +7,6 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-# tests/pending/ holds GPU parity tests written for kernels that have not yet
-# run on a GB300 (the RNN-head draft; the bias GEMM's fp32-backbone epilogue).
-# They join the suite, moved into tests/, once they have run and passed there.
-collect_ignore = ["pending"]
-
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built CUDA library")

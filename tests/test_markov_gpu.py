@@ -119,3 +119,14 @@ def test_markov_full_vocab_rank256(ds, oracle):
     ref, got = _both(ds, oracle, w)
     _check(ref, got)
 
+
+
+@pytest.mark.parametrize("B,V,r", [(5, 4096, 256), (33, 2056, 128), (160, 2056, 64)])
+def test_markov_fp32_backbone(ds, oracle, B, V, r):
+    """The bias GEMM's fp32-backbone epilogue, which no bf16 case reaches (the
+    RNN-head draft's second product runs on it): fp32 backbone rows at three
+    ranks and ragged batches."""
+    w = synth.decode_verify_tile(V=V, B=B, r=r, H=0, seed=3001 + B)
+    w.backbone = w.backbone.float().contiguous()
+    ref, got = _both(ds, oracle, w, with_h=False)
+    _check(ref, got, with_h=False)

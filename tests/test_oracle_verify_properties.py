@@ -45,3 +45,38 @@ def test_verify_output_structure(oracle, seed, V, gamma, B, with_width):
         # a bad width, a proposal checked and out of range, or a NaN in a row
         # the request reads would have failed it
         assert np.all((x[b, :w] >= 0) & (x[b, :w] < V)) and not bad[b, :w + 1].any()
+        # the determinate prefix: everything when the request is determinate;
+        # otherwise a prefix of the emitted tokens, all of the accepted ones
+        # when only the final draw was indeterminate
+        dt, dn = int(res["det_tokens"][b]), bool(res["det_nacc"][b])
+        if not res["indet"][b]:
+            assert dt == gamma + 1 and dn
+        elif dn:
+            assert dt == n
+        else:
+            assert 0 <= dt <= n
+
+
+def test_verify_determinate_prefix_at_a_planted_tie(oracle):
+    """Decision 2 planted on its accept threshold (q(x_2) = p_1(x_2) / u_2,
+    so u = p/q exactly) after a sure accept of x_1: the oracle marks the
+    request indeterminate with x_1 alone still comparable and num_accepted
+    undecided."""
+    V, gamma, B = 16, 3, 1
+    rng = np.random.default_rng(5)
+    t = rng.normal(0, 1.0, (B, gamma + 1, V)).astype(np.float32)
+    x = np.array([[3, 7, 1]], np.int32)
+    q = np.full((B, gamma, V), 1.0 / V, np.float32)
+    keys = synth.make_keys(B, seed=4, pos0=10).numpy()
+    p1 = torch.softmax(torch.tensor(t[0, 1], dtype=torch.float64), 0).numpy()
+    u2 = oracle.uniform(4, 0, 12, 1)
+    qx = np.array([[1e-6, np.float32(p1[7] / u2), 0.5]], np.float32)
+    pol = synth.uniform_policy(B, temperature=1.0).numpy()
+    res = oracle.verify(t, x, q, qx, pol, **keys)
+    assert res["indet"][0] and res["det_tokens"][0] == 1 and not res["det_nacc"][0]
+    assert res["out_tokens"][0, 0] == 3
+    # the same request with decision 2 far from its threshold is determinate
+    qx[0, 1] = 1e-6
+    res = oracle.verify(t, x, q, qx, pol, **keys)
+    if not res["indet"][0]:
+        assert res["det_tokens"][0] == gamma + 1 and res["det_nacc"][0]

@@ -52,12 +52,26 @@ def _verify_both(ds, oracle, w, draft):
 
 
 def _check_verify(ref, got, max_indet_frac=0.05):
+    """Status of every request; every output of a determinate request; of an
+    indeterminate one, the tokens emitted before its first indeterminate
+    decision (and num_accepted when it was decided before it).  Returns the
+    number of indeterminate requests."""
     out, nacc, st = got
     np.testing.assert_array_equal(st, ref["status"])
     det = ~ref["indet"]
     assert det.mean() >= 1 - max_indet_frac, f"{(~det).sum()} indeterminate of {det.size}"
     np.testing.assert_array_equal(nacc[det], ref["num_accepted"][det])
     np.testing.assert_array_equal(out[det], ref["out_tokens"][det])
+    partial = 0
+    for b in np.flatnonzero(~det):
+        n = int(ref["det_tokens"][b])
+        np.testing.assert_array_equal(out[b, :n], ref["out_tokens"][b, :n], err_msg=f"request {b}")
+        partial += n
+        if ref["det_nacc"][b]:
+            assert nacc[b] == ref["num_accepted"][b], b
+    if (~det).any():
+        print(f"indeterminate requests: {(~det).sum()} of {det.size}; "
+              f"{partial} tokens of theirs compared before the first indeterminate decision")
     return int((~det).sum())
 
 

@@ -61,6 +61,13 @@ def _determinate(ref, got, max_indet_frac):
     assert det.mean() >= 1 - max_indet_frac, f"{(~det).sum()} indeterminate of {det.size}"
     np.testing.assert_array_equal(nacc[det], ref["num_accepted"][det])
     np.testing.assert_array_equal(out[det], ref["out_tokens"][det])
+    # an indeterminate request: the tokens emitted before its first
+    # indeterminate decision, and num_accepted when decided before it
+    for b in np.flatnonzero(~det):
+        n = int(ref["det_tokens"][b])
+        np.testing.assert_array_equal(out[b, :n], ref["out_tokens"][b, :n], err_msg=f"request {b}")
+        if ref["det_nacc"][b]:
+            assert nacc[b] == ref["num_accepted"][b], b
 
 
 @pytest.mark.parametrize("B,gamma,V,dtype", [

@@ -55,7 +55,8 @@ def test_noalloc_matches_verify_twice_in_a_row(lib):
         torch.cuda.synchronize()
         for a, b in zip(ref, got):
             assert torch.equal(a, b)
-    # a different batch right after: the shared scratch starts clean again
+    # a call of another shape right after, on the same stream: it must match
+    # dspark_verify too
     w2 = synth.full_decode_tile(V=40_008, B=9, gamma=3, device="cuda", seed=77)
     x2 = w2.backbone.float().argmax(dim=2).to(torch.int32)
     x2[0, 1] = 5
@@ -90,3 +91,26 @@ def test_noalloc_large_batch_and_no_workspace(lib):
         assert torch.equal(a, b)
         assert torch.equal(a, c)
     assert int((ref[1] < rows - 1).sum()) > 0      # some requests stop early
+
+
+def test_noalloc_overlapping_streams(lib):
+    """Two calls with different batches enqueued on two streams with no
+    synchronisation between them (they may run at the same time on the GPU):
+    each matches dspark_verify on its own batch."""
+    import verify_dspark_markov_gb300 as ds
+    cases = []
+    for seed, (V, B, gamma) in ((11, (40_008, 33, 5)), (12, (8192, 70, 7))):
+        w = synth.full_decode_tile(V=V, B=B, gamma=gamma, device="cuda", seed=seed)
+        x = w.backbone.float().argmax(dim=2).to(torch.int32)
+        x[::5, 0] = 1
+        cases.append((w.target, x, ds.verify(w.target, x)))
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    got = []
+    for (t, x, _), s in zip(cases, streams):
+        with torch.cuda.stream(s):
+            got.append(_noalloc(lib, t, x))
+    torch.cuda.synchronize()
+    for (_, _, ref), g in zip(cases, got):
+        for a, b in zip(ref, g):
+            assert torch.equal(a, b)

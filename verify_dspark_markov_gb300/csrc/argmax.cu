@@ -22,12 +22,13 @@
 // look up the lowest index holding it in the registers they already have.
 // Per-thread results are 64-bit keys (ordered value << 32 | ~index) merged
 // with atomicMax (max value, then lowest index) into the CTA's row slots;
-// each CTA then merges its slots into those of the cluster's first CTA over
-// distributed shared memory and arrives on that CTA's mbarrier, and the first
+// each CTA then writes its slots into those of the cluster's first CTA over
+// distributed shared memory, a cluster barrier publishes them, and the first
 // CTA makes the request's decision with one lane per row.  Nothing goes
 // through global memory but the logits and the outputs, so the kernel needs
 // no workspace.
 
+#include <atomic>
 #include <type_traits>
 
 #include "common.cuh"
@@ -52,7 +53,6 @@ constexpr int kMaxCluster = 8;
 struct ArgmaxSmem {
     uint64_t full[kStages];
     uint64_t empty[kStages];
-    uint64_t done;  // first CTA of the cluster: one arrival per lane of every CTA's warp 0
     unsigned long long key[kMaxRows];
     unsigned int bad[kMaxRows];  // bit 0: NaN / +inf seen; bit 1: a device wait gave up
     unsigned int timed_out;
@@ -102,28 +102,6 @@ __device__ __forceinline__ void st_cluster_u64(uint32_t addr, uint64_t v) {
 }
 __device__ __forceinline__ void st_cluster_u32(uint32_t addr, uint32_t v) {
     asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t addr) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(addr) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
-    if (mbar_try_wait_cluster(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
-    while (!mbar_try_wait_cluster(bar, parity)) {
-        if (globaltimer_ns() - t0 > limit_ns) return false;
-    }
-    return true;
 }
 __device__ __forceinline__ void cluster_arrive_release() {
     asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
@@ -367,7 +345,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) argmax_rows_kernel(const
             mbar_init(&sm.full[s], 1);
             mbar_init(&sm.empty[s], kConsumerWarps);
         }
-        mbar_init(&sm.done, C * 32);
         sm.timed_out = 0u;
         fence_mbar_init();
     }
@@ -485,29 +462,31 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) argmax_rows_kernel(const
     cluster_wait_acquire();
 
     // Hand this CTA's row slots to the first CTA of the cluster (distributed
-    // shared memory; every lane's arrival releases its own stores), which
-    // then merges them and decides.
+    // shared memory), then one cluster barrier: its release orders the remote
+    // stores before the first CTA's reads, and no CTA exits while another may
+    // still write into its shared memory.  Every wait before the barrier is
+    // bounded, so every thread of the cluster reaches it.
     if (warp == 0) {
         const unsigned tflag = sm.timed_out ? 2u : 0u;
         if (lane < G) {
             st_cluster_u64(map_rank(&sm.rkey[q][lane], 0), sm.key[lane]);
             st_cluster_u32(map_rank(&sm.rbad[q][lane], 0), sm.bad[lane] | tflag);
         }
-        mbar_arrive_remote(map_rank(&sm.done, 0));
-        if (q == 0) {
-            const bool ok = mbar_wait_cluster(&sm.done, 0, kWaitLimitNs);
-            uint64_t k = 0;
-            uint32_t f = ok ? 0u : 2u;
-            if (lane < G && ok) {
-                for (uint32_t r = 0; r < C; ++r) {
-                    const uint64_t kr = sm.rkey[r][lane];
-                    k = kr > k ? kr : k;
-                    f |= sm.rbad[r][lane];
-                }
+    }
+    cluster_arrive_release();
+    cluster_wait_acquire();
+    if (warp == 0 && q == 0) {
+        uint64_t k = 0;
+        uint32_t f = 0u;
+        if (lane < G) {
+            for (uint32_t r = 0; r < C; ++r) {
+                const uint64_t kr = sm.rkey[r][lane];
+                k = kr > k ? kr : k;
+                f |= sm.rbad[r][lane];
             }
-            const int32_t x = p.mode == kArgmaxVerify ? (lane < p.gamma ? sm.x[lane] : 0) : sm.x[0];
-            decide<kWidth>(p, g, w, k, f, x, lane);
         }
+        const int32_t x = p.mode == kArgmaxVerify ? (lane < p.gamma ? sm.x[lane] : 0) : sm.x[0];
+        decide<kWidth>(p, g, w, k, f, x, lane);
     }
 }
 
@@ -521,12 +500,14 @@ cudaError_t prepare_argmax(int dtype, bool width = false) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    static bool ready[64][2][2] = {};
-    if (dev < 64 && ready[dev][dtype][width]) return cudaSuccess;
+    // per device, dtype and variant; host threads may race here, so the flags
+    // are atomic (setting the attribute twice is harmless)
+    static std::atomic<bool> ready[64][2][2] = {};
+    if (dev < 64 && ready[dev][dtype][width].load(std::memory_order_acquire)) return cudaSuccess;
     const void* f = width ? (dtype == kBF16 ? kernel_ptr<kBF16, true>() : kernel_ptr<kF32, true>())
                           : (dtype == kBF16 ? kernel_ptr<kBF16>() : kernel_ptr<kF32>());
     e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kRingBytes);
-    if (e == cudaSuccess && dev < 64) ready[dev][dtype][width] = true;
+    if (e == cudaSuccess && dev < 64) ready[dev][dtype][width].store(true, std::memory_order_release);
     return e;
 }
 
@@ -549,16 +530,19 @@ cudaLaunchConfig_t launch_config(int clusters, int c, cudaStream_t stream, cudaL
 int resident_clusters(int dtype, int c) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-    static int cache[64][2][4] = {};
+    static std::atomic<int> cache[64][2][4] = {};  // 0: not yet queried (atomic: host threads may race)
     const int ci = c == 1 ? 0 : c == 2 ? 1 : c == 4 ? 2 : 3;
-    if (dev < 64 && cache[dev][dtype][ci]) return cache[dev][dtype][ci];
+    if (dev < 64) {
+        const int n = cache[dev][dtype][ci].load(std::memory_order_acquire);
+        if (n) return n;
+    }
     if (prepare_argmax(dtype) != cudaSuccess) return 0;
     cudaLaunchAttribute attr[1];
     const cudaLaunchConfig_t cfg = launch_config(64, c, nullptr, attr);
     int n = 0;
     const void* f = dtype == kBF16 ? kernel_ptr<kBF16>() : kernel_ptr<kF32>();
     if (cudaOccupancyMaxActiveClusters(&n, f, &cfg) != cudaSuccess) return 0;
-    if (dev < 64) cache[dev][dtype][ci] = n;
+    if (dev < 64) cache[dev][dtype][ci].store(n, std::memory_order_release);
     return n;
 }
 
