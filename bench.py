@@ -39,6 +39,7 @@ CPU oracle on a bounded sample of the same workload instead.
 from __future__ import annotations
 
 import argparse
+import atexit
 import json
 import os
 import subprocess
@@ -110,17 +111,19 @@ class Clocks:
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.dev}", f"--query-gpu={self.QUERY}",
                                           "--format=csv,noheader,nounits", "-lms", "20"],
                                          stdout=self.f, stderr=subprocess.DEVNULL)
+            atexit.register(self.__exit__, None, None, None)  # the sampler never outlives the bench
         except (OSError, FileNotFoundError):
             self.proc = None
         return self
 
     def __exit__(self, *a):
-        if self.proc is not None:
+        if self.proc is not None and self.proc.poll() is None:
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
+        if self.proc is not None and not self.f.closed:
             self.f.close()
 
     def summary(self, t_start=None, t_end=None):
@@ -590,6 +593,11 @@ def run_gpu(args):
     def flush_l2():
         torch.sum(flush_r, dim=0, out=flush_sink)  # evict L2 by reading another 2 x L2 buffer
 
+    # clock samples cover the warm-up, the timed steps and the end-to-end
+    # steps (a short timed region alone may fall between two samples)
+    clk = Clocks(local, args.clocks_csv).__enter__()
+    time.sleep(0.3)  # let the sampler start
+    w0 = time.time()
     for _ in range(args.warmup):
         flush_l2()
         for _, fn in parts:
@@ -610,20 +618,15 @@ def run_gpu(args):
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    with Clocks(local, args.clocks_csv) as clk:
-        time.sleep(0.3)  # let the sampler start
-        t0 = time.perf_counter()
-        w0 = time.time()
-        for i in range(steps):
-            flush_l2()
-            ev[i][0].record(stream)
-            for j, (_, fn) in enumerate(parts):
-                fn(stream)
-                ev[i][j + 1].record(stream)
-        torch.cuda.synchronize()
-        wall = time.perf_counter() - t0
-        w1 = time.time()
-        time.sleep(0.1)
+    t0 = time.perf_counter()
+    for i in range(steps):
+        flush_l2()
+        ev[i][0].record(stream)
+        for j, (_, fn) in enumerate(parts):
+            fn(stream)
+            ev[i][j + 1].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
     step_ms = [ev[i][0].elapsed_time(ev[i][-1]) for i in range(steps)]
     part_ms = {name: float(np.mean([ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(steps)]))
                for j, (name, _) in enumerate(parts)}
@@ -644,6 +647,9 @@ def run_gpu(args):
         b.record(stream)
         b.synchronize()
         e2e_ms.append(a.elapsed_time(b))
+    w1 = time.time()
+    time.sleep(0.1)
+    clk.__exit__(None, None, None)
     h2d = sum(t.numel() * t.element_size() for t in host_in)
     d2h = sum(t.numel() * t.element_size() for t in host_out)
 
@@ -684,7 +690,7 @@ def run_gpu(args):
         "parts_GBps": {k: nbytes[k] / (part_ms[k] * 1e-3) / 1e9 for k in part_ms},
         "e2e": {"value": wl.positions * world / (float(np.mean(e2e_ms)) * 1e-3), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": float(np.mean(e2e_ms))},
-        "clocks": clk.summary(w0, w1),
+        "clocks": dict(clk.summary(w0, w1), window="warm-up, timed and end-to-end steps"),
         "wall_s_timed_region": wall,
     }
     if flops.get("draft"):

@@ -90,6 +90,7 @@ extern "C" {
 #define DSPARK_MAX_VOCAB (1 << 20)
 #define DSPARK_MAX_RANK 256
 #define DSPARK_MAX_BATCH 256  /* requests per dspark_markov_sample call */
+#define DSPARK_STS_MAX_PASSES 4096  /* largest pass budget of dspark_sts_fit */
 
 /* Sampling policy of one request [FT Exact decoding semantics > Probabilistic:
  * p and q are formed after the request's temperature, top-p and top-k].
@@ -398,21 +399,28 @@ int dspark_version(void);
  *                sign of its z (a = 1 for z > 0, a = 0 for z < 0), or the
  *                root lies beyond 2^20: no finite fit (beta = 2^20); 3 a
  *                counted pair with a non-finite z or a label outside [0, 1]
- *                (beta = NaN).  A BCE slope >= 0 at beta = 0 gives beta = 0
- *                (status 0).
+ *                (beta = NaN); 4 the pass budget ran out with the search
+ *                still open (beta = its last iterate, not the fit).  A BCE
+ *                slope >= 0 at beta = 0 gives beta = 0 (status 0).
  *   passes       int32 [gamma] out, or NULL: the passes over the pairs each
  *                position's search used (every pass reads all positions
  *                until the last one stops).
+ *   max_passes   passes enqueued, 1..DSPARK_STS_MAX_PASSES, or 0 for 64
+ *                (enough for beta to double from 1 to the 2^20 cap and then
+ *                halve its bracket below 1e-7; Newton usually ends in ten
+ *                or fewer).  Passes after the last position stops return at
+ *                once.
  *   workspace    dspark_workspace_size(DSPARK_OP_STS_FIT, N, gamma, 0, 0, 0)
  *                bytes; every region is written before it is read.
  * N = 0 is valid (every position reports status 1).  The fit is a root
  * search on the device (Newton steps inside a bracket, a fixed number of
  * passes enqueued); beta is accurate to about 1e-6 relative (its sums are
- * fp32 per thread, fp64 across threads).
+ * fp32 per thread, fp64 across threads) and bit-identical across calls on
+ * the same inputs (the CTAs' sums are combined in a fixed order).
  */
 int dspark_sts_fit(const float* conf_logits, const float* labels,
                    const uint8_t* mask, int N, int gamma, double* beta,
-                   int32_t* status, int32_t* passes, void* workspace,
+                   int32_t* status, int32_t* passes, int max_passes, void* workspace,
                    size_t workspace_bytes, void* stream);
 
 #ifdef __cplusplus

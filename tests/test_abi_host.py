@@ -95,10 +95,10 @@ def test_verify_width_rejects_invalid_arguments(lib):
 def test_sts_fit_rejects_invalid_arguments(lib):
     f = lib.dspark_sts_fit
     ws = ds.workspace_size(ds.OP_STS_FIT, 100, 5, 0)
-    assert 0 < ws <= 4096
+    assert 0 < ws <= 1 << 19
     assert ds.workspace_size(ds.OP_STS_FIT, 100, 0, 0) == 0 and ds.workspace_size(ds.OP_STS_FIT, -1, 5, 0) == 0
-    call = lambda N=100, g=5, z=FAKE, a=FAKE, beta=FAKE, st=FAKE, passes=None, wsb=ws: f(z, a, None, N, g, beta, st,
-                                                                                       passes, FAKE, wsb, None)
+    call = lambda N=100, g=5, z=FAKE, a=FAKE, beta=FAKE, st=FAKE, passes=None, mp=0, wsb=ws: f(
+        z, a, None, N, g, beta, st, passes, mp, FAKE, wsb, None)
     assert call(g=0) == binding.EINVAL
     assert call(g=17) == binding.EINVAL
     assert call(N=-1) == binding.EINVAL
@@ -108,6 +108,8 @@ def test_sts_fit_rejects_invalid_arguments(lib):
     assert call(z=ctypes.c_void_p(0x7F0000000002)) == binding.EINVAL
     assert call(passes=ctypes.c_void_p(0x7F0000000002)) == binding.EINVAL   # int32 output, 4-byte aligned
     assert call(wsb=8) == binding.ENOSPC
+    assert call(mp=-1) == binding.EINVAL                           # pass budget 0 (default) .. 4096
+    assert call(mp=4097) == binding.EINVAL
 
 
 def test_rnn_rejects_invalid_arguments(lib):

@@ -97,3 +97,37 @@ def test_sts_large_beta_and_empty(ds, oracle):
     ref, beta, status = _both(ds, oracle, np.zeros((0, 4), np.float32), np.zeros((0, 4), np.float32))
     assert status.tolist() == [1, 1, 1, 1] and beta.tolist() == [1.0] * 4
     _check(ref, beta, status)
+
+
+def test_sts_repeat_is_bitwise_identical(ds):
+    """The CTAs' sums are combined in a fixed order: two fits of the same
+    log give the same bits."""
+    rng = np.random.default_rng(15)
+    z = torch.from_numpy(rng.normal(0, 2.0, (3_000_000, 7)).astype(np.float32)).cuda()
+    a = (torch.rand(z.shape, device="cuda") < torch.sigmoid(z / 1.7)).float()
+    b1, s1, p1 = ds.sts_fit(z, a)
+    b2, s2, p2 = ds.sts_fit(z, a)
+    torch.cuda.synchronize()
+    assert torch.equal(b1.view(torch.int64), b2.view(torch.int64))
+    assert torch.equal(s1, s2) and torch.equal(p1, p2)
+    assert torch.all(s1 == 0)
+
+
+def test_sts_pass_budget_exhausted(ds, oracle):
+    """Two passes leave every informative position searching (the first pass
+    is taken at beta = 0, the second starts Newton at beta = 1): they report
+    status 4 with their last iterate, which the default budget carries on to
+    the oracle's fit."""
+    rng = np.random.default_rng(16)
+    z = rng.normal(0, 2.0, (200_000, 5)).astype(np.float32)
+    T = np.array([0.25, 0.5, 3.0, 2.0, 7.0])
+    a = (1.0 / (1.0 + np.exp(-z.astype(np.float64) / T))).astype(np.float32)
+    zd, ad = torch.from_numpy(z).cuda(), torch.from_numpy(a).cuda()
+    beta, status, passes = ds.sts_fit(zd, ad, max_passes=2)
+    torch.cuda.synchronize()
+    assert status.tolist() == [4] * 5 and passes.tolist() == [2] * 5
+    assert np.all(np.isfinite(beta.cpu().numpy()))
+    ref = oracle.sts_fit(z, a)
+    beta, status, passes = ds.sts_fit(zd, ad)
+    torch.cuda.synchronize()
+    _check(ref, beta.cpu().numpy(), status.cpu().numpy())

@@ -68,7 +68,7 @@ def load(path: str | None = None):
             lib.dspark_rnn_sample.argtypes = ([P, i32, P, P, P, i32, P, P, P, P, P, i32, P, P, i32]
                                               + [P] * 4 + [i32] * 3 + [P] * 6 + [sz, P])
             lib.dspark_rnn_sample.restype = i32
-            lib.dspark_sts_fit.argtypes = [P, P, P, i32, i32, P, P, P, P, sz, P]
+            lib.dspark_sts_fit.argtypes = [P, P, P, i32, i32, P, P, P, i32, P, sz, P]
             lib.dspark_sts_fit.restype = i32
             lib.dspark_status_string.argtypes = [i32]
             lib.dspark_status_string.restype = ctypes.c_char_p
@@ -331,10 +331,12 @@ def accept_stats_grad(draft, target, labels, conf_logits, mask=None, scale=1.0, 
     return out
 
 
-def sts_fit(conf_logits, labels, mask=None, workspace: Workspace | None = None, stream=None, out=None):
+def sts_fit(conf_logits, labels, mask=None, max_passes=0, workspace: Workspace | None = None, stream=None,
+            out=None):
     """Sequential Temperature Scaling: per block position the inverse
     temperature beta >= 0 of the confidence head, from fp32 [N, gamma]
-    confidence logits and accept labels (mask: uint8 [N, gamma] or None).
+    confidence logits and accept labels (mask: uint8 [N, gamma] or None);
+    max_passes bounds the passes enqueued (0: the library's default).
     Returns (beta float64 [gamma], status int32 [gamma], passes int32
     [gamma]: the passes each position's search used)."""
     _dev(conf_logits, "conf_logits", torch.float32)
@@ -354,6 +356,6 @@ def sts_fit(conf_logits, labels, mask=None, workspace: Workspace | None = None, 
     ws_n = workspace_size(OP_STS_FIT, N, gamma, 8)
     ws = (workspace or _default_ws).get(OP_STS_FIT, ws_n, dev)
     code = load().dspark_sts_fit(_ptr(conf_logits), _ptr(labels), _ptr(mask), N, gamma, _ptr(out[0]),
-                                 _ptr(out[1]), _ptr(out[2]), _ptr(ws), ws_n, _stream(stream))
+                                 _ptr(out[1]), _ptr(out[2]), int(max_passes), _ptr(ws), ws_n, _stream(stream))
     _check(code, "dspark_sts_fit")
     return out

@@ -82,10 +82,13 @@ size_t stats_workspace(int N, int gamma) {
     return align_up(stats_partials_offset(N, gamma) + static_cast<size_t>(stats_partials(N)) * 6 * sizeof(double));
 }
 
-// Sequential Temperature Scaling: the per-position search states, then the
-// count of positions still searching.
+// Sequential Temperature Scaling: the per-position search states, the count
+// of positions still searching, then the per-CTA sums of a pass.
 size_t sts_active_offset() { return align_up(static_cast<size_t>(DSPARK_MAX_GAMMA) * sizeof(StsState)); }
-size_t sts_workspace() { return align_up(sts_active_offset() + sizeof(int)); }
+size_t sts_partial_offset() { return align_up(sts_active_offset() + sizeof(int)); }
+size_t sts_workspace() {
+    return align_up(sts_partial_offset() + static_cast<size_t>(kStsMaxGrid) * DSPARK_MAX_GAMMA * 2 * sizeof(double));
+}
 
 template <typename T>
 T* at(void* ws, size_t off) {
@@ -467,9 +470,10 @@ int dspark_accept_stats_grad(const void* draft, const void* target, int dtype, c
 
 
 int dspark_sts_fit(const float* conf_logits, const float* labels, const uint8_t* mask, int N, int gamma,
-                   double* beta, int32_t* status, int32_t* passes, void* workspace, size_t workspace_bytes,
-                   void* stream) {
+                   double* beta, int32_t* status, int32_t* passes, int max_passes, void* workspace,
+                   size_t workspace_bytes, void* stream) {
     if (N < 0 || gamma < 1 || gamma > DSPARK_MAX_GAMMA) return DSPARK_EINVAL;
+    if (max_passes < 0 || max_passes > DSPARK_STS_MAX_PASSES) return DSPARK_EINVAL;
     if (!beta || !status) return DSPARK_EINVAL;
     if (N > 0 && (!conf_logits || !labels)) return DSPARK_EINVAL;
     if ((reinterpret_cast<uintptr_t>(conf_logits) & 3u) || (reinterpret_cast<uintptr_t>(labels) & 3u) ||
@@ -488,6 +492,8 @@ int dspark_sts_fit(const float* conf_logits, const float* labels, const uint8_t*
     p.passes = passes;
     p.state = at<StsState>(workspace, 0);
     p.active = at<int>(workspace, sts_active_offset());
+    p.partial = at<double>(workspace, sts_partial_offset());
+    p.max_passes = max_passes ? max_passes : kStsDefaultPasses;
     return launch_sts_fit(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? DSPARK_OK : DSPARK_ECUDA;
 }
 

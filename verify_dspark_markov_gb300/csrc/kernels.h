@@ -216,7 +216,11 @@ struct StsParams {
     int32_t* passes;           // [gamma] out, or null
     StsState* state;           // [DSPARK_MAX_GAMMA] workspace
     int* active;               // workspace: positions still searching
+    double* partial;           // [kStsMaxGrid][DSPARK_MAX_GAMMA][2] workspace: per-CTA slope and curvature sums
+    int max_passes;            // passes enqueued (the search budget)
 };
+constexpr int kStsMaxGrid = 1024;   // CTAs of one pass over the pairs, at most
+constexpr int kStsDefaultPasses = 64;
 cudaError_t launch_sts_fit(const StsParams& p, cudaStream_t stream);
 
 // One step of the RNN head's GRU (rnn.cu): s_k from s_{k-1} and U[x_{k-1}],

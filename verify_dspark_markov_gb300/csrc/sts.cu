@@ -12,12 +12,15 @@
 //    z != 0; a label against the sign of its z; an invalid pair).  A thread
 //    takes whole rows n (gamma contiguous pairs) with per-position sums in
 //    registers; warps reduce by shuffles, CTAs through shared memory, and
-//    one double atomic per position and CTA lands in the position's state.
-//  * sts_update_kernel - one warp, lane k: sts_search_step (sts_search.cuh)
-//    on position k - the degenerate cases on the first pass (taken at
-//    beta = 0), then a Newton step kept inside the bracket [lo, hi] of the
-//    root, bisection (or doubling while hi is open) when the step leaves it;
-//    the sums are cleared for the next pass.
+//    each CTA writes its per-position sums (fp64) to its own slot.
+//  * sts_update_kernel - sums the CTAs' slots per position in a fixed order
+//    (a strided sum per thread, then a fixed tree), so beta's bits do not
+//    depend on the order the CTAs ran in; then lane k runs sts_search_step
+//    (sts_search.cuh) on position k - the degenerate cases on the first pass
+//    (taken at beta = 0), then a Newton step kept inside the bracket [lo, hi]
+//    of the root, bisection (or doubling while hi is open) when the step
+//    leaves it.  A position still searching after the last enqueued pass
+//    reports status 4 with its last iterate.
 // Once every position has converged the remaining passes return at once.
 // HBM-bound: 9 bytes a pair a pass (8 without a mask).
 
@@ -35,10 +38,8 @@ constexpr int kStsThreads = 256;
 constexpr int kStsWarps = kStsThreads / 32;
 constexpr int kG = DSPARK_MAX_GAMMA;
 constexpr unsigned kInformative = kStsInformative, kViolated = kStsViolated, kInvalid = kStsInvalid;
-// Rounds enqueued per fit: enough for beta to double from 1 to the cap (20)
-// and then halve a bracket to below 1e-7 of its width (24), with margin;
-// Newton usually converges in a handful and the later passes return at once.
-constexpr int kStsPasses = 64;
+constexpr int kUpdThreads = 256;
+constexpr int32_t kStsNotConverged = 4;
 
 __global__ void sts_init_kernel(StsState* st, int* active, int gamma) {
     const int k = threadIdx.x;
@@ -56,7 +57,8 @@ __global__ void sts_init_kernel(StsState* st, int* active, int gamma) {
 __global__ void __launch_bounds__(kStsThreads) sts_pass_kernel(const float* __restrict__ z,
                                                                const float* __restrict__ a,
                                                                const uint8_t* __restrict__ mask, int64_t N,
-                                                               int gamma, StsState* st, const int* active) {
+                                                               int gamma, StsState* st, const int* active,
+                                                               double* partial) {
     if (*active == 0) return;
     __shared__ float s_beta[kG];
     __shared__ float s_red[kStsWarps][kG][2];
@@ -121,8 +123,9 @@ __global__ void __launch_bounds__(kStsThreads) sts_pass_kernel(const float* __re
             x += static_cast<double>(s_red[w][tid][0]);
             y += static_cast<double>(s_red[w][tid][1]);
         }
-        atomicAdd(&st[tid].s1, x);
-        atomicAdd(&st[tid].s2, y);
+        double* slot = partial + (static_cast<size_t>(blockIdx.x) * kG + tid) * 2;
+        slot[0] = x;
+        slot[1] = y;
         const unsigned f = (((s_flag[0] >> tid) & 1u) ? kInformative : 0u) |
                            (((s_flag[1] >> tid) & 1u) ? kViolated : 0u) |
                            (((s_flag[2] >> tid) & 1u) ? kInvalid : 0u);
@@ -130,16 +133,47 @@ __global__ void __launch_bounds__(kStsThreads) sts_pass_kernel(const float* __re
     }
 }
 
-__global__ void sts_update_kernel(StsState* st, int* active, int gamma, double* beta_out, int32_t* status_out,
-                                  int32_t* passes_out) {
-    const int k = threadIdx.x;
+__global__ void __launch_bounds__(kUpdThreads) sts_update_kernel(StsState* st, int* active, int gamma,
+                                                                 const double* partial, int grid, bool last,
+                                                                 double* beta_out, int32_t* status_out,
+                                                                 int32_t* passes_out) {
+    __shared__ double s_sum[kUpdThreads][2];
+    const int tid = threadIdx.x;
+    if (*active == 0) return;  // the pass kernel wrote no slots (uniform over the CTA)
+    // the pass's sums, per position: thread t adds slots t, t + 256, ... in
+    // order, then a fixed binary tree over the threads
+    for (int k = 0; k < gamma; ++k) {
+        double x = 0.0, y = 0.0;
+        for (int c = tid; c < grid; c += kUpdThreads) {
+            x += partial[(static_cast<size_t>(c) * kG + k) * 2];
+            y += partial[(static_cast<size_t>(c) * kG + k) * 2 + 1];
+        }
+        s_sum[tid][0] = x;
+        s_sum[tid][1] = y;
+        __syncthreads();
+        for (int h = kUpdThreads / 2; h > 0; h >>= 1) {
+            if (tid < h) {
+                s_sum[tid][0] += s_sum[tid + h][0];
+                s_sum[tid][1] += s_sum[tid + h][1];
+            }
+            __syncthreads();
+        }
+        if (tid == 0 && st[k].phase != 2) {
+            st[k].s1 = s_sum[0][0];
+            st[k].s2 = s_sum[0][1];
+        }
+        __syncthreads();
+    }
+    if (tid >= 32) return;
+    const int k = tid;
     bool finished = false;
     if (k < gamma) {
         StsState s = st[k];
         finished = sts_search_step(s);
         st[k] = s;
         beta_out[k] = s.beta;
-        status_out[k] = s.status;
+        // the budget ran out with the search still open: its last iterate
+        status_out[k] = (last && s.phase != 2) ? kStsNotConverged : s.status;
         if (passes_out) passes_out[k] = s.passes;
     }
     const unsigned fin = __ballot_sync(0xFFFFFFFFu, finished);
@@ -149,18 +183,20 @@ __global__ void sts_update_kernel(StsState* st, int* active, int gamma, double* 
 }  // namespace
 
 cudaError_t launch_sts_fit(const StsParams& p, cudaStream_t stream) {
-    if (p.gamma < 1 || p.gamma > kG || p.N < 0) return cudaErrorInvalidValue;
+    if (p.gamma < 1 || p.gamma > kG || p.N < 0 || p.max_passes < 1) return cudaErrorInvalidValue;
     sts_init_kernel<<<1, 32, 0, stream>>>(p.state, p.active, p.gamma);
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
     const int64_t want = (p.N + kStsThreads - 1) / kStsThreads;
-    const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(want, static_cast<int64_t>(sms) * 8)));
-    for (int r = 0; r < kStsPasses; ++r) {
+    const int grid = static_cast<int>(std::max<int64_t>(
+        1, std::min<int64_t>(std::min<int64_t>(want, static_cast<int64_t>(sms) * 8), kStsMaxGrid)));
+    for (int r = 0; r < p.max_passes; ++r) {
         sts_pass_kernel<<<grid, kStsThreads, 0, stream>>>(p.conf_logits, p.labels, p.mask, p.N, p.gamma, p.state,
-                                                          p.active);
-        sts_update_kernel<<<1, 32, 0, stream>>>(p.state, p.active, p.gamma, p.beta, p.status, p.passes);
+                                                          p.active, p.partial);
+        sts_update_kernel<<<1, kUpdThreads, 0, stream>>>(p.state, p.active, p.gamma, p.partial, grid,
+                                                         r == p.max_passes - 1, p.beta, p.status, p.passes);
     }
     return cudaGetLastError();
 }
