@@ -548,7 +548,8 @@ def make_workload(name, device, stats_blocks=4096):
         return Serving(name, synth.mixed_serving(device=device), 2)
     if name == "rnn_decode_tile":
         w = synth.decode_verify_tile(device=device)
-        return Serving(name, w, 2, gru=synth.gru_weights(w.weights.r, synth._gen(1009, "cpu"), device))
+        gw = synth.gru_weights(w.weights.r, synth._gen(1009, "cpu"), "cpu")  # small: drawn on the host
+        return Serving(name, w, 2, gru=synth.GruWeights(*(t.to(device) for t in (gw.Wi, gw.Wh, gw.bi, gw.bh))))
     if name == "sts_fit":
         return StsFit(synth.sts_log(device=device))
     if name == "decode_verify_tile_width":
