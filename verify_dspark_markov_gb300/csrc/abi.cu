@@ -124,7 +124,10 @@ size_t dspark_workspace_size(int op, int B, int gamma, int V, int r, int H) {
     if (op == DSPARK_OP_STS_FIT) return B >= 0 && gamma >= 1 && gamma <= DSPARK_MAX_GAMMA ? sts_workspace() : 0;
     if (!valid_common(B, gamma, V, DSPARK_BF16) || r < 0 || H < 0) return 0;
     switch (op) {
-        case DSPARK_OP_MARKOV_SAMPLE: return markov_layout(B, gamma, V, r).total;
+        case DSPARK_OP_MARKOV_SAMPLE:
+            // the larger of the two paths' needs (which one runs depends on the device)
+            return std::max(markov_layout(B, gamma, V, r).total,
+                            r >= 64 && r % 64 == 0 ? markov_fused_workspace(B, gamma, V) : size_t(0));
         case DSPARK_OP_VERIFY: return verify_layout(B, gamma).total;
         case DSPARK_OP_ACCEPT_STATS: return stats_workspace(B, gamma);
         case DSPARK_OP_RNN_SAMPLE: return r >= 16 ? rnn_layout(B, V, r).total : 0;
@@ -212,6 +215,34 @@ int dspark_markov_sample(const void* backbone, int dtype, const int32_t* anchor,
         return DSPARK_EINVAL;
     if (policy && (!q || !seed || !request_id || !pos0 || !aligned16(q))) return DSPARK_EINVAL;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+    if (r > 0 && r % 64 == 0 && markov_fused_supported(dtype, B, V, r)) {
+        // the whole draft in one persistent launch, z kept in tensor memory
+        if (!workspace || workspace_bytes < markov_fused_workspace(B, gamma, V)) return DSPARK_ENOSPC;
+        MarkovFusedArgs a{};
+        a.backbone = static_cast<const uint16_t*>(backbone);
+        a.U = U;
+        a.W = W;
+        a.anchor = anchor;
+        a.policy = policy;
+        a.seed = seed;
+        a.request_id = request_id;
+        a.pos0 = pos0;
+        a.B = B;
+        a.gamma = gamma;
+        a.V = V;
+        a.r = r;
+        a.proposals = proposals;
+        a.q = q;
+        a.q_at_x = q_at_x;
+        a.status = status;
+        if (launch_markov_fused(a, workspace, workspace_bytes, s) != cudaSuccess) return DSPARK_ECUDA;
+        if (h) {
+            ConfParams c{h, h_dtype, E, w_conf, H, B, gamma, V, anchor, proposals, 1, gamma, conf};
+            if (launch_confidence(c, s) != cudaSuccess) return DSPARK_ECUDA;
+        }
+        return DSPARK_OK;
+    }
 
     if (policy || r > 0) {  // the row engine, one launch per step (after the bias GEMM when r > 0)
         const MarkovLayout lay = markov_layout(B, gamma, V, r);

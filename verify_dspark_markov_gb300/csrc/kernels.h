@@ -137,6 +137,31 @@ bool prepare_markov_bias(MarkovGemmParams& p, MarkovGemmPlan& plan);
 // (its z buffer must differ from the one that kernel reads).
 cudaError_t launch_markov_bias(const MarkovGemmParams& p, const MarkovGemmPlan& plan, bool overlap,
                                cudaStream_t stream);
+// The whole draft (every step's bias GEMM, policy and draw) in one persistent
+// launch with the biased logits in tensor memory (markov_fused.cu): bf16
+// backbone, r a multiple of 64 up to 256, a vocabulary of at most 8 tiles of
+// 128 per SM.
+struct MarkovFusedArgs {
+    const uint16_t* backbone;  // bf16 [B, gamma, V]
+    const uint16_t* U;         // bf16 [V, r]
+    const uint16_t* W;         // bf16 [V, r]
+    const int32_t* anchor;
+    const dspark_policy* policy;
+    const uint64_t* seed;
+    const uint64_t* request_id;
+    const int64_t* pos0;
+    int B, gamma, V, r;
+    int32_t* proposals;
+    float* q;
+    float* q_at_x;
+    int32_t* status;
+};
+bool markov_fused_supported(int dtype, int B, int V, int r);
+// Workspace bytes from the start of the Markov workspace (its first 256 bytes
+// belong to the per-step path's error word).
+size_t markov_fused_workspace(int B, int gamma, int V);
+cudaError_t launch_markov_fused(const MarkovFusedArgs& a, void* ws, size_t ws_bytes, cudaStream_t stream);
+
 // Elements of a row each CTA of the verify / drafting step owns.
 int verify_slice(int V);
 int step_slice(int V);

@@ -1,0 +1,1058 @@
+// The draft's sequential head in one persistent launch: every step's Markov
+// bias GEMM, sampling policy and draw, with the biased logits z kept in tensor
+// memory [MB Semi-autoregressive draft; FT Checkpoint-faithful DSpark
+// architecture; FT Exact decoding semantics > Probabilistic].
+//
+// Per step k (left to right) and request b:
+//   z_k[b, v] = backbone[b, k-1, v] + sum_j U[x_{k-1}(b), j] * W[v, j]
+//   q_k = policy(z_k) (temperature, top-k, top-p), written in full;
+//   x_k = inverse-CDF draw from q_k in token order (greedy: the argmax).
+//
+// Layout.  Requests go in groups of up to 64 (the MMA's N); the vocabulary
+// goes to the CTAs in contiguous ranges of 128-row tiles (the MMA's M), so a
+// CTA's tokens precede the next CTA's in token order.  Tile j of a CTA lives
+// in tensor-memory columns [64 j, 64 j + 64): lane = vocabulary row of the
+// tile, column = request.  z never leaves the SM: the GEMM writes it there,
+// every later phase of the step reads it there, and only q goes to HBM.
+//
+// Phases of a step, separated by grid barriers (all CTAs resident: a
+// cooperative launch, one CTA per SM):
+//   A  gather U[x_{k-1}] (B operand), stream W and backbone tiles by TMA,
+//      tcgen05.mma into tensor memory; epilogue warps add the backbone, store
+//      z back, and reduce each request's maximum and non-finite flag into
+//      global words.                                              | barrier
+//   B  greedy rows: the lowest index holding the maximum.  Sampled rows: a
+//      16-bin histogram of s = (zmax - z)/T (bins of 2 below s = 32; exact
+//      counts and exact fixed-point masses, the weights of the row engine),
+//      reduced into global words.                                 | barrier
+//   C  (every CTA, for every request) the window of bins holding the top-k
+//      and top-p cuts, from the histogram's prefix sums (the row engine's
+//      rule); D compaction of the window's tokens into the request's
+//      candidate list in global memory.  A window larger than the list
+//      makes the row "hard": every CTA writes its z there instead.  | barrier
+//   E  the request's owner CTA sorts its candidates and takes the cuts by
+//      exact prefix sums; with the whole support in the list it draws x_k at
+//      once.  A hard row is done whole by its owner with the row engine
+//      (row_policy.cuh) as one CTA.                              | barrier
+//   F  every CTA writes its share of q (from tensor memory) and, for rows
+//      whose support is not in a list, the support mass of its range.
+//                                                      | barrier (if any)
+//   G  the CTA whose range holds the draw finds x_k.    | barrier (if any)
+// Every sum that decides a token is an integer (fixed-point weights,
+// 2^-40), so decisions do not depend on the order of the reductions.
+//
+// Waits are bounded (kWaitLimitNs); a wait that gives up sets the call's
+// error word, every CTA then skips the remaining work, and the requests
+// report DSPARK_REQ_TIMEOUT.
+
+#include <cooperative_groups.h>
+
+#include <algorithm>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "row_policy.cuh"
+#include "tc_common.cuh"
+
+namespace dspark {
+
+namespace {
+
+using namespace tc;
+namespace cg = cooperative_groups;
+
+constexpr int kFT = 256;             // threads: the row engine's block size
+constexpr int kNG = 64;              // requests per group (MMA N)
+constexpr int kMaxLT = 8;            // vocabulary tiles per CTA (8 x 64 columns = all of tensor memory)
+constexpr int kTileV = 128;          // vocabulary rows per tile (MMA M)
+constexpr int kHB = 16;              // histogram bins: s in [2i, 2i + 2), s < 32
+constexpr int kCand = rp::kCap;      // candidates a list holds (the owner sorts them in shared memory)
+constexpr int kWhole = rp::kThreads; // a support this small is compacted whole (drawn by its owner)
+constexpr uint32_t kTmemCols = 512;
+
+// request modes after the histogram
+enum : int { kModeNone = 0, kModeGreedy = 1, kModeWin = 2, kModeAll = 3, kModeHard = 4 };
+// descriptor flags
+enum : uint32_t { kDescDrawn = 1u, kDescPrefix = 2u, kDescDone = 4u };
+
+// Per (group, step) words in the workspace, cleared by the host before the launch.
+struct StepWords {
+    uint32_t maxkey[kNG];     // ordered key of the row maximum (0: none yet)
+    uint32_t bad[kNG];        // a NaN or +inf logit
+    uint32_t amax[kNG];       // greedy: 0xFFFFFFFF - (lowest index holding the maximum), max-reduced
+    uint32_t ccount[kNG];     // candidates claimed
+    uint32_t hcnt[kNG][kHB];
+    unsigned long long hmass[kNG][kHB];
+};
+// The owner's result for a request of the current step.
+struct Desc {
+    uint32_t tau;
+    int32_t cut;
+    unsigned long long mass;   // fixed-point support mass
+    unsigned long long target; // prefix draw: the first token whose inclusive prefix exceeds this
+    uint32_t flags;
+    int32_t pad;
+};
+// Window of one request (every CTA computes the same).
+struct Win {
+    int mode;
+    int wlo, whi, phi;
+    unsigned long long above_cnt, above_mass, wcount, gap_cnt, gap_mass, k_eff, total;
+};
+
+struct FusedParams {
+    const uint16_t* backbone;   // bf16 [B, gamma, V]
+    const uint16_t* U;          // bf16 [V, r]
+    const int32_t* anchor;
+    const dspark_policy* policy;  // null: all greedy
+    const uint64_t* seed;
+    const uint64_t* request_id;
+    const int64_t* pos0;
+    int B, gamma, V, r;
+    int32_t* proposals;
+    float* q;
+    float* q_at_x;
+    int32_t* status;
+    // layout
+    int ntiles, tpc, grid, groups, stages;
+    // workspace
+    unsigned int* bar;         // barrier arrivals (cleared before the launch)
+    int* error;                // set when a wait gave up
+    StepWords* words;          // [groups * gamma]
+    unsigned long long* cand;  // [kNG][kCand] value-order keys
+    Desc* desc;                // [kNG]
+    unsigned long long* part;  // [kNG][grid] support mass of each CTA's range
+    float* zhard;              // [kNG][V] z of hard rows
+};
+
+struct FusedSmem {
+    uint64_t wfull[4], wempty[4], bfull[4], bempty[4];
+    uint64_t accfull[kMaxLT];
+    uint32_t tmem_base;
+    int abort;
+    unsigned int bar_gen;
+    int any_prefix;
+    int32_t x[kNG];
+    uint32_t cmax[4][kNG];
+    uint32_t cbad[4][kNG];
+    // per request of the group, for the policy phases
+    float zmax[kNG];
+    float inv_t[kNG];
+    int mode[kNG];
+    int32_t code[kNG];   // the row's status when it fails at this step
+    Win win[kNG];
+    Desc d[kNG];
+    unsigned long long wpart[4][kNG];   // per quadrant: support mass of the CTA's rows
+    unsigned long long qsum[4];         // the draw's scan: per quadrant sums of one tile
+    unsigned long long ex;              // the draw's scan: mass of the CTAs before this one
+    int32_t pick[4];
+};
+
+// ------------------------------------------------------------- helpers
+__device__ __forceinline__ uint32_t ld_cg_u32(const uint32_t* p) { return __ldcg(p); }
+__device__ __forceinline__ unsigned long long ld_cg_u64(const unsigned long long* p) { return __ldcg(p); }
+
+__device__ __forceinline__ void red_max_u32(uint32_t* p, uint32_t v) {
+    asm volatile("red.relaxed.gpu.global.max.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ void red_or_u32(uint32_t* p, uint32_t v) {
+    asm volatile("red.relaxed.gpu.global.or.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ void red_add_u32(uint32_t* p, uint32_t v) {
+    asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ void red_add_u64(unsigned long long* p, unsigned long long v) {
+    asm volatile("red.relaxed.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+// Grid barrier: arrivals counted on bar[0] for the whole launch (generation
+// g waits for g * nctas arrivals); bounded, and a wait that gives up (or an
+// error set elsewhere) makes the CTA abort.
+__device__ void grid_sync(const FusedParams& p, FusedSmem& sm) {
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const unsigned gen = ++sm.bar_gen;
+        const unsigned target = gen * static_cast<unsigned>(gridDim.x);
+        __threadfence();
+        atomicAdd(p.bar, 1u);
+        const uint64_t t0 = globaltimer_ns();
+        for (;;) {
+            if (ld_relaxed_u32(p.bar) >= target) break;
+            if (*reinterpret_cast<volatile int*>(p.error)) { sm.abort = 1; break; }
+            if (globaltimer_ns() - t0 > kWaitLimitNs) {
+                atomicExch(p.error, 1);
+                sm.abort = 1;
+                break;
+            }
+        }
+        __threadfence();
+    }
+    __syncthreads();
+}
+
+// Bin of s = (zmax - z) * inv_t in steps of 2 below s = 32; kHB beyond.
+__device__ __forceinline__ int sbin(float z, float zmax, float inv_t) {
+    const float s = (zmax - z) * inv_t;
+    return s < 32.0f ? min(kHB - 1, static_cast<int>(s * 0.5f)) : kHB;
+}
+
+__device__ __forceinline__ float inv_mass(unsigned long long mass) {
+    return static_cast<float>(rp::kFix / static_cast<double>(mass));
+}
+
+// The window of bins holding a row's cuts from its 16-bin histogram (the
+// row engine's rule with 16 bins; cc / cm are inclusive prefix sums).
+__device__ Win make_window(const rp::Policy& pol, const unsigned long long* cc, const unsigned long long* cm) {
+    Win w{};
+    const bool use_k = pol.top_k > 0, use_p = pol.top_p < 1.0f;
+    w.total = cm[kHB - 1];
+    if (!use_k && !use_p) {
+        w.mode = kModeAll;
+        return w;
+    }
+    const bool with_mass = !use_k || pol.top_k > kWhole;
+    const unsigned long long n_in = cc[kHB - 1];
+    w.k_eff = use_k ? min(static_cast<unsigned long long>(pol.top_k), n_in) : 0ull;
+    auto first_at_least = [](const unsigned long long* pre, unsigned long long x) {
+        int i = 0;
+        while (i < kHB - 1 && pre[i] < x) ++i;
+        return i;
+    };
+    int whi = use_k ? first_at_least(cc, w.k_eff) : kHB - 1;
+    int wlo = 0;
+    const bool small = cc[whi] <= static_cast<unsigned long long>(kWhole);
+    if (with_mass) {
+        const unsigned long long mk_lo = use_k ? (whi ? cm[whi - 1] : 0ull) : w.total;
+        wlo = whi;
+        if (use_p) {
+            wlo = first_at_least(cm, rp::p_threshold(pol.top_p, mk_lo));
+            if (!use_k) whi = wlo;
+        }
+        if (small || cc[whi] <= static_cast<unsigned long long>(kWhole)) wlo = 0;
+    }
+    int phi = whi;
+    if (with_mass && use_k && use_p && !small) {
+        const int p_hi = first_at_least(cm, rp::p_threshold(pol.top_p, cm[whi]));
+        if (p_hi + 1 < whi) phi = p_hi;
+    }
+    const unsigned long long ac = wlo ? cc[wlo - 1] : 0ull;
+    const unsigned long long gc = phi < whi ? cc[whi - 1] - cc[phi] : 0ull;
+    w.wlo = wlo;
+    w.whi = whi;
+    w.phi = phi;
+    w.above_cnt = ac;
+    w.above_mass = wlo ? cm[wlo - 1] : 0ull;
+    w.wcount = cc[whi] - ac - gc;
+    w.gap_cnt = gc;
+    w.gap_mass = phi < whi ? cm[whi - 1] - cm[phi] : 0ull;
+    w.mode = w.wcount > static_cast<unsigned long long>(kCand) ? kModeHard : kModeWin;
+    return w;
+}
+
+template <typename F>
+__device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    return v;
+}
+
+// ------------------------------------------------------------------ kernel
+__global__ void __launch_bounds__(kFT, 1)
+    markov_fused_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap bmap,
+                        const FusedParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ FusedSmem sm;
+    __shared__ rp::Smem rsm;
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int r = p.r, S = p.stages, V = p.V;
+    const uint32_t w_bytes = static_cast<uint32_t>(kTileV * r * 2);  // one W stage
+    const uint32_t b_bytes = static_cast<uint32_t>(kNG * kTileV * 2);  // one backbone stage
+    uint8_t* sW = smem;
+    uint8_t* sB = sW + S * w_bytes;
+    uint8_t* sU = sB + S * b_bytes;  // also the owner's candidate buffer (and the row engine's scratch)
+    unsigned long long* cbuf = reinterpret_cast<unsigned long long*>(sU);
+    // phase B's histogram lives there too (the step's MMAs have read U by then)
+    unsigned long long (*hmass)[kHB] = reinterpret_cast<unsigned long long (*)[kHB]>(sU);
+    uint32_t (*hcnt)[kHB] = reinterpret_cast<uint32_t (*)[kHB]>(sU + kNG * kHB * 8);
+
+    const int t0 = blockIdx.x * p.tpc;                        // first tile of this CTA
+    const int ntl = max(0, min(p.tpc, p.ntiles - t0));        // its tiles
+    const int vend = min(V, (t0 + ntl) * kTileV);             // one past its last token
+
+    if (warp == 0) tmem_alloc(&sm.tmem_base, kTmemCols);
+    if (tid == 0) {
+        for (int s = 0; s < 4; ++s) {
+            mbar_init(&sm.wfull[s], 1);
+            mbar_init(&sm.wempty[s], 1);
+            mbar_init(&sm.bfull[s], 1);
+            mbar_init(&sm.bempty[s], 4);
+        }
+        for (int j = 0; j < kMaxLT; ++j) mbar_init(&sm.accfull[j], 1);
+        sm.abort = 0;
+        sm.bar_gen = 0;
+        fence_mbar_init();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sm.tmem_base;
+
+    // producer state (thread 0): W / backbone tiles issued and consumed, in order
+    int w_issued = 0, b_issued = 0, mma_done = 0;
+    const int steps_total = p.groups * p.gamma;
+    auto tile_of = [&](int n) { return n % max(ntl, 1); };         // n-th tile of the whole launch
+    auto step_of = [&](int n) { return n / max(ntl, 1); };         // its (group, step) index
+    auto issue_w = [&](int n) {
+        const int s = n % S;
+        mbar_arrive_expect_tx(&sm.wfull[s], w_bytes);
+        uint8_t* dst = sW + s * w_bytes;
+        const int t = t0 + tile_of(n);
+        for (int kb = 0; kb < r / 64; ++kb) tma_load_2d(dst + kb * kTileV * 128, &wmap, kb * 64, t * kTileV, &sm.wfull[s]);
+    };
+    auto issue_b = [&](int n) {
+        const int s = n % S;
+        const int gs = step_of(n), g = gs / p.gamma, k = gs % p.gamma;  // k 0-based
+        mbar_arrive_expect_tx(&sm.bfull[s], b_bytes);
+        const int t = t0 + tile_of(n);
+        tma_load_3d(sB + s * b_bytes, &bmap, t * kTileV, k, g * kNG, &sm.bfull[s]);
+    };
+    const int total_tiles = steps_total * ntl;
+    if (tid == 0) {
+        for (; w_issued < min(S, total_tiles); ++w_issued) issue_w(w_issued);
+        for (; b_issued < min(S, total_tiles); ++b_issued) issue_b(b_issued);
+    }
+
+    for (int gs = 0; gs < steps_total; ++gs) {
+        const int g = gs / p.gamma, k = gs % p.gamma + 1;  // k 1-based
+        const int nb = min(kNG, p.B - g * kNG);           // requests of the group
+        StepWords& sw = p.words[gs];
+        const bool aborted = sm.abort != 0;
+
+        // ------------------------------------------------ A: gather, GEMM, epilogue
+        if (tid < kNG) {
+            int32_t x = -1;
+            if (tid < nb) {
+                const int b = g * kNG + tid;
+                x = k == 1 ? p.anchor[b] : __ldcg(p.proposals + static_cast<int64_t>(b) * p.gamma + (k - 2));
+                if (x < 0 || x >= V) x = -1;
+            }
+            sm.x[tid] = x;
+        }
+        __syncthreads();
+        {
+            const int kchunks = r / 8;
+            for (int c = tid; c < kNG * kchunks; c += kFT) {
+                const int row = c / kchunks, kc = c % kchunks;
+                const int32_t x = sm.x[row];
+                uint8_t* d = sU + chunk_off<true>(row, kc, kNG);
+                if (x >= 0) cp_async16(d, p.U + static_cast<int64_t>(x) * r + kc * 8);
+                else *reinterpret_cast<uint4*>(d) = make_uint4(0u, 0u, 0u, 0u);
+            }
+            cp_async_wait_all();
+            fence_proxy_async_smem();
+        }
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        const uint32_t par = static_cast<uint32_t>(gs & 1);  // accumulator barriers complete once per step
+
+        if (warp == 0) {
+            if (lane == 0 && !aborted) {
+                const uint32_t idesc = instr_desc(128, kNG);
+                const uint32_t ubase = smem_u32(sU), wbase = smem_u32(sW);
+                for (int j = 0; j < ntl; ++j) {
+                    const int n = gs * ntl + j, s = n % S;
+                    if (!mbar_wait(&sm.wfull[s], (n / S) & 1, kWaitLimitNs)) {
+                        atomicExch(p.error, 1);
+                        sm.abort = 1;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t d = tmem + static_cast<uint32_t>(j * kNG);
+                    for (int ks = 0; ks < r / 16; ++ks)
+                        mma_bf16(d, op_desc<true>(wbase + s * w_bytes, ks, kTileV), op_desc<true>(ubase, ks, kNG), idesc,
+                                 ks > 0 ? 1u : 0u);
+                    mma_commit(&sm.wempty[s]);
+                    mma_commit(&sm.accfull[j]);
+                    ++mma_done;
+                    // refill the W stage of the previous tile (its MMAs were issued one tile ago)
+                    if (n >= 1 && w_issued < total_tiles && w_issued <= n - 1 + S) {
+                        const int m = n - 1;
+                        if (!mbar_wait(&sm.wempty[m % S], (m / S) & 1, kWaitLimitNs)) {
+                            atomicExch(p.error, 1);
+                            sm.abort = 1;
+                            break;
+                        }
+                        issue_w(w_issued++);
+                    }
+                    // and the backbone stage of the previous tile, once the
+                    // epilogue has read it (that needs only MMAs already issued)
+                    if (n >= 1 && b_issued < total_tiles && b_issued <= n - 1 + S) {
+                        const int m = n - 1;
+                        if (!mbar_wait(&sm.bempty[m % S], (m / S) & 1, kWaitLimitNs)) {
+                            atomicExch(p.error, 1);
+                            sm.abort = 1;
+                            break;
+                        }
+                        issue_b(b_issued++);
+                    }
+                }
+            }
+        } else if (warp >= 4) {
+            // epilogue: quadrant q = lanes 32q..32q+31 of every tile, all 64 columns
+            const int q = warp - 4;
+            uint32_t kmax[kNG];
+            uint32_t badm0 = 0u, badm1 = 0u;
+#pragma unroll
+            for (int c = 0; c < kNG; ++c) kmax[c] = 0u;
+            for (int j = 0; j < ntl && !aborted; ++j) {
+                const int n = gs * ntl + j, s = n % S;
+                if (!mbar_wait(&sm.accfull[j], par, kWaitLimitNs) || !mbar_wait(&sm.bfull[s], (n / S) & 1, kWaitLimitNs)) {
+                    atomicExch(p.error, 1);
+                    sm.abort = 1;
+                    break;
+                }
+                tc_fence_after();
+                uint32_t acc[64];
+                const uint32_t ta = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(j * kNG);
+                tmem_ld64(ta, acc);
+                tmem_wait_ld();
+                const int vl = q * 32 + lane;                 // row of the tile
+                const int v = (t0 + j) * kTileV + vl;
+                const uint16_t* bb = reinterpret_cast<const uint16_t*>(sB + s * b_bytes);
+                const bool valid = v < V;
+#pragma unroll
+                for (int c = 0; c < kNG; ++c) {
+                    const float z = __uint_as_float(acc[c]) +
+                                    __uint_as_float(static_cast<uint32_t>(bb[c * kTileV + vl]) << 16);
+                    acc[c] = __float_as_uint(valid ? z : -__int_as_float(0x7F800000));
+                    if (valid) {
+                        if (bad_logit(z)) {
+                            if (c < 32) badm0 |= 1u << c;
+                            else badm1 |= 1u << (c - 32);
+                        } else {
+                            const uint32_t kz = ordered_key(z);
+                            kmax[c] = kz > kmax[c] ? kz : kmax[c];
+                        }
+                    }
+                }
+                tmem_st64(ta, acc);
+                tmem_wait_st();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sm.bempty[s]);
+            }
+            // column maxima over the warp's lanes, then over the four quadrants
+#pragma unroll
+            for (int c = 0; c < kNG; ++c) {
+                const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, kmax[c]);
+                if (lane == 0) sm.cmax[q][c] = m;
+            }
+            badm0 = __reduce_or_sync(0xFFFFFFFFu, badm0);
+            badm1 = __reduce_or_sync(0xFFFFFFFFu, badm1);
+            if (lane == 0) {
+                for (int c = 0; c < kNG; ++c) sm.cbad[q][c] = ((c < 32 ? badm0 >> c : badm1 >> (c - 32)) & 1u);
+            }
+        }
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        if (tid < nb && !sm.abort) {
+            const uint32_t m = max(max(sm.cmax[0][tid], sm.cmax[1][tid]), max(sm.cmax[2][tid], sm.cmax[3][tid]));
+            const uint32_t bd = sm.cbad[0][tid] | sm.cbad[1][tid] | sm.cbad[2][tid] | sm.cbad[3][tid];
+            if (m) red_max_u32(&sw.maxkey[tid], m);
+            if (bd) red_or_u32(&sw.bad[tid], 1u);
+        }
+        grid_sync(p, sm);  // ---------------------------------------- barrier 1
+
+        // ------------------------------------------------ B: greedy argmax, histograms
+        if (tid < kNG) {
+            int mode = kModeNone;
+            int32_t code = kReqOk;
+            float zm = 0.0f, it = 1.0f;
+            if (tid < nb && sm.x[tid] >= 0 && !sm.abort) {
+                const int b = g * kNG + tid;
+                const uint32_t mk = ld_cg_u32(&sw.maxkey[tid]);
+                const bool bad = ld_cg_u32(&sw.bad[tid]) != 0;
+                rp::Policy pol;
+                const bool pol_ok = p.policy ? rp::make_policy(p.policy[b], V, pol)
+                                             : (pol = rp::Policy{1.0f, 0, 1.0f, 1}, true);
+                zm = mk ? key_to_float(mk) : -__int_as_float(0x7F800000);
+                const bool empty = mk == 0 || zm == -__int_as_float(0x7F800000);
+                it = pol.inv_t;
+                // the row engine's order: non-finite, then empty, then an invalid policy
+                code = bad ? kReqNonfinite : (empty ? kReqEmpty : (pol_ok ? kReqOk : kReqBadPolicy));
+                if (code == kReqOk) mode = pol.greedy ? kModeGreedy : kModeWin;  // Win refined in C
+            }
+            sm.mode[tid] = mode;
+            sm.code[tid] = code;
+            sm.zmax[tid] = zm;
+            sm.inv_t[tid] = it;
+        }
+        for (int i = tid; i < kNG * kHB; i += kFT) {
+            (&hcnt[0][0])[i] = 0u;
+            (&hmass[0][0])[i] = 0ull;
+        }
+        // next step's first W stages (the W ring is free: this step's MMAs are done)
+        if (tid == 0 && !sm.abort) {
+            while (w_issued < total_tiles && w_issued < (gs + 1) * ntl + S && w_issued < mma_done + S) {
+                const int m = w_issued - S;
+                if (m >= 0 && !mbar_wait(&sm.wempty[m % S], (m / S) & 1, kWaitLimitNs)) {
+                    atomicExch(p.error, 1);
+                    sm.abort = 1;
+                    break;
+                }
+                issue_w(w_issued++);
+            }
+        }
+        __syncthreads();
+        const int q = warp & 3, h = warp >> 2;  // TMEM lane quadrant; column half
+        if (!sm.abort) {
+            for (int j = 0; j < ntl; ++j) {
+                uint32_t zr[32];
+                tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(j * kNG + h * 32), zr);
+                tmem_wait_ld();
+                const int v = (t0 + j) * kTileV + q * 32 + lane;
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const int c = h * 32 + i;
+                    const int mode = sm.mode[c];
+                    if (mode == kModeNone) continue;
+                    const float z = __uint_as_float(zr[i]);
+                    if (mode == kModeGreedy) {
+                        const bool hit = v < V && ordered_key(z) == ordered_key(sm.zmax[c]);
+                        const uint32_t key = hit ? 0xFFFFFFFFu - static_cast<uint32_t>(v) : 0u;
+                        const uint32_t best = __reduce_max_sync(0xFFFFFFFFu, key);
+                        if (lane == 0 && best) red_max_u32(&sw.amax[c], best);
+                    } else if (v < V) {
+                        const float zm = sm.zmax[c], it = sm.inv_t[c];
+                        const int bin = sbin(z, zm, it);
+                        if (bin < kHB) {
+                            atomicAdd(&hcnt[c][bin], 1u);
+                            atomicAdd(&hmass[c][bin], static_cast<unsigned long long>(rp::to_fixed(rp::weight_f(z, zm, it))));
+                        }
+                    }
+                }
+            }
+        }
+        __syncthreads();
+        for (int i = tid; i < kNG * kHB; i += kFT) {
+            const int c = i / kHB;
+            if (sm.mode[c] != kModeWin) continue;
+            const uint32_t cn = (&hcnt[0][0])[i];
+            if (cn) {
+                red_add_u32(&sw.hcnt[0][0] + i, cn);
+                red_add_u64(&sw.hmass[0][0] + i, (&hmass[0][0])[i]);
+            }
+        }
+        grid_sync(p, sm);  // ---------------------------------------- barrier 2
+
+        // ------------------------------------------------ C: windows (every CTA)
+        for (int c = warp; c < kNG; c += kFT / 32) {
+            if (sm.mode[c] != kModeWin) {
+                if (lane == 0) sm.win[c].mode = sm.mode[c];
+                continue;
+            }
+            unsigned long long cn = 0, ms = 0;
+            if (lane < kHB) {
+                cn = ld_cg_u32(&sw.hcnt[c][lane]);
+                ms = ld_cg_u64(&sw.hmass[c][lane]);
+            }
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {  // inclusive prefix sums over the bins
+                const unsigned long long a = __shfl_up_sync(0xFFFFFFFFu, cn, o);
+                const unsigned long long bm = __shfl_up_sync(0xFFFFFFFFu, ms, o);
+                if (lane >= o) {
+                    cn += a;
+                    ms += bm;
+                }
+            }
+            unsigned long long cc[kHB], cm[kHB];
+#pragma unroll
+            for (int i = 0; i < kHB; ++i) {
+                cc[i] = __shfl_sync(0xFFFFFFFFu, cn, i);
+                cm[i] = __shfl_sync(0xFFFFFFFFu, ms, i);
+            }
+            if (lane == 0) {
+                rp::Policy pol;
+                rp::make_policy(p.policy[g * kNG + c], V, pol);
+                sm.win[c] = make_window(pol, cc, cm);
+            }
+        }
+        __syncthreads();
+        // ------------------------------------------------ D: compaction (and hard rows' z)
+        if (!sm.abort) {
+            for (int j = 0; j < ntl; ++j) {
+                uint32_t zr[32];
+                tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(j * kNG + h * 32), zr);
+                tmem_wait_ld();
+                const int v = (t0 + j) * kTileV + q * 32 + lane;
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const int c = h * 32 + i;
+                    const int mode = sm.win[c].mode;
+                    const float z = __uint_as_float(zr[i]);
+                    if (mode == kModeHard) {
+                        if (v < V) p.zhard[static_cast<size_t>(c) * V + v] = z;
+                    } else if (mode == kModeWin) {
+                        const Win& w = sm.win[c];
+                        const int bin = v < V ? sbin(z, sm.zmax[c], sm.inv_t[c]) : kHB;
+                        const bool pick = bin >= w.wlo && bin <= w.whi && (bin <= w.phi || bin == w.whi);
+                        const unsigned mask = __ballot_sync(0xFFFFFFFFu, pick);
+                        if (mask) {
+                            uint32_t base = 0;
+                            if (lane == 0) base = atomicAdd(&sw.ccount[c], static_cast<uint32_t>(__popc(mask)));
+                            base = __shfl_sync(0xFFFFFFFFu, base, 0) + __popc(mask & ((1u << lane) - 1u));
+                            if (pick && base < static_cast<uint32_t>(kCand))
+                                p.cand[static_cast<size_t>(c) * kCand + base] = rp::value_order(ordered_key(z), v);
+                        }
+                    }
+                }
+            }
+        }
+        grid_sync(p, sm);  // ---------------------------------------- barrier 3
+
+        // ------------------------------------------------ E: owners (cuts, draws, hard rows)
+        for (int c = blockIdx.x; c < nb; c += gridDim.x) {
+            if (sm.abort) break;
+            const int b = g * kNG + c;
+            const int64_t pidx = static_cast<int64_t>(b) * p.gamma + (k - 1);
+            const int mode = sm.win[c].mode;
+            Desc d{};
+            if (mode == kModeNone) {
+                if (tid == 0) {
+                    // a failed request, or this step's row failed
+                    p.proposals[pidx] = -1;
+                    p.q_at_x[pidx] = 0.0f;
+                    if (sm.x[c] < 0) {
+                        if (k == 1) p.status[b] = kReqBadToken;
+                    } else {
+                        p.status[b] = sm.code[c];
+                    }
+                    p.desc[c].flags = kDescDone;
+                }
+                continue;
+            }
+            if (mode == kModeGreedy) {
+                if (tid == 0) {
+                    const uint32_t a = ld_cg_u32(&sw.amax[c]);
+                    p.proposals[pidx] = static_cast<int32_t>(0xFFFFFFFFu - a);
+                    p.q_at_x[pidx] = 1.0f;
+                    if (k == 1) p.status[b] = kReqOk;
+                    p.desc[c].flags = kDescDone;
+                }
+                continue;
+            }
+            rp::Policy pol;
+            rp::make_policy(p.policy[b], V, pol);
+            const float zmax = sm.zmax[c], inv_t = pol.inv_t;
+            const uint32_t m24 = uniform_bits24(p.seed[b], p.request_id[b], p.pos0[b] + k, 0);
+            if (mode == kModeAll) {
+                if (tid == 0) {
+                    d.tau = 0u;
+                    d.cut = -1;
+                    d.mass = sm.win[c].total;
+                    d.target = static_cast<unsigned long long>((static_cast<unsigned __int128>(m24) * d.mass) >> 24);
+                    d.flags = kDescPrefix;
+                    p.desc[c] = d;
+                    p.proposals[pidx] = -1;  // until the CTA holding the draw writes it
+                    if (k == 1) p.status[b] = kReqOk;
+                }
+                continue;
+            }
+            if (mode == kModeHard) {
+                // the row engine on the whole row, this CTA as a cluster of one
+                cg::cluster_group cl = cg::this_cluster();
+                rp::init_smem(rsm);
+                __syncthreads();
+                const float* zrow = p.zhard + static_cast<size_t>(c) * V;
+                rp::Slice sl{zrow, 0, V, (V + kFT - 1) / kFT, 0, 1};  // written by this launch: coherent loads
+                rp::RowResult res;
+                bool bad;
+                rp::slice_max(rsm, cl, sl, res, bad);
+                res.status = kReqOk;
+                res.count = 1;
+                res.in_buf = 0;
+                rp::row_policy(rsm, cl, sl, V, pol, res, cbuf);
+                const float invS = inv_mass(res.mass);
+                float* qrow = p.q + pidx * V;
+                for (int v = tid; v < V; v += kFT) {
+                    const float z = __ldcg(zrow + v);
+                    qrow[v] = rp::in_set(ordered_key(z), v, res.tau, res.cut) ? rp::weight_f(z, res.zmax, pol.inv_t) * invS
+                                                                              : 0.0f;
+                }
+                unsigned long long total = 0;
+                const int32_t xk = rp::sample_fixed(
+                    rsm, cl, sl, m24,
+                    [&](float z, int32_t idx) {
+                        return rp::in_set(ordered_key(z), idx, res.tau, res.cut)
+                                   ? rp::to_fixed(rp::weight_f(z, res.zmax, pol.inv_t))
+                                   : 0ull;
+                    },
+                    total);
+                if (tid == 0) {
+                    p.proposals[pidx] = xk;
+                    p.q_at_x[pidx] = xk >= 0 ? rp::weight_f(__ldcg(zrow + xk), res.zmax, pol.inv_t) * invS : 0.0f;
+                    if (k == 1) p.status[b] = kReqOk;
+                    d.flags = kDescDone;
+                    p.desc[c] = d;
+                }
+                __syncthreads();
+                continue;
+            }
+            // kModeWin: the candidates, sorted; the cuts by exact prefix sums
+            const Win w = sm.win[c];
+            const int n = static_cast<int>(min(static_cast<unsigned long long>(ld_cg_u32(&sw.ccount[c])), w.wcount));
+            for (int i = tid; i < n; i += kFT) cbuf[i] = __ldcg(p.cand + static_cast<size_t>(c) * kCand + i);
+            __syncthreads();
+            rp::sort_candidates(cbuf, n);
+            const bool use_k = pol.top_k > 0, use_p = pol.top_p < 1.0f;
+            const int K = use_k ? static_cast<int>(min(w.k_eff - w.above_cnt - w.gap_cnt, static_cast<unsigned long long>(n)))
+                                : n;
+            auto wt = [&](int i) -> unsigned long long {
+                return rp::to_fixed(rp::weight_f(key_to_float(rp::vo_key(cbuf[i])), zmax, inv_t));
+            };
+            unsigned long long part, pm;
+            int pos;
+            rp::cut_scan(rsm, K, wt,
+                         [&](unsigned long long k_part) -> unsigned long long {
+                             if (!use_p) return 0ull;
+                             const unsigned long long kept = use_k ? w.above_mass + w.gap_mass + k_part : w.total;
+                             return rp::p_threshold(pol.top_p, kept) - w.above_mass;
+                         },
+                         part, pos, pm);
+            const unsigned long long kept = use_k ? w.above_mass + w.gap_mass + part : w.total;
+            int mm = K;
+            unsigned long long mass = kept;
+            if (use_p) {
+                mm = pos < K ? pos + 1 : K;
+                mass = w.above_mass + (pos < K ? pm : part);
+            }
+            mm = max(mm, 1);
+            const unsigned long long last = cbuf[mm - 1];
+            d.tau = rp::vo_key(last);
+            d.cut = rp::vo_idx(last);
+            d.mass = mass;
+            if (w.above_cnt == 0 && mm <= kWhole) {
+                // the support is the first mm candidates: draw here
+                unsigned long long total = 0;
+                const int32_t xk = rp::draw_small_support(
+                    rsm, cbuf, mm, m24,
+                    [&](uint32_t key, int32_t) { return rp::to_fixed(rp::weight_f(key_to_float(key), zmax, inv_t)); },
+                    total);
+                if (tid == 0) sm.pick[0] = xk;
+                __syncthreads();
+                for (int i = tid; i < mm; i += kFT)
+                    if (rp::vo_idx(cbuf[i]) == sm.pick[0])
+                        p.q_at_x[pidx] = rp::weight_f(key_to_float(rp::vo_key(cbuf[i])), zmax, inv_t) * inv_mass(mass);
+                if (tid == 0) {
+                    p.proposals[pidx] = sm.pick[0];
+                    d.flags = kDescDrawn;
+                }
+            } else {
+                d.target = static_cast<unsigned long long>((static_cast<unsigned __int128>(m24) * mass) >> 24);
+                d.flags = kDescPrefix;
+                if (tid == 0) p.proposals[pidx] = -1;  // until the CTA holding the draw writes it
+            }
+            if (tid == 0) {
+                p.desc[c] = d;
+                if (k == 1) p.status[b] = kReqOk;
+            }
+            __syncthreads();
+        }
+        grid_sync(p, sm);  // ---------------------------------------- barrier 4
+
+        // ------------------------------------------------ F: q, support mass of this range
+        if (tid < kNG) {
+            Desc d{};
+            if (tid < nb && (sm.win[tid].mode == kModeWin || sm.win[tid].mode == kModeAll)) {
+                const Desc* gd = p.desc + tid;
+                d.tau = __ldcg(&gd->tau);
+                d.cut = __ldcg(&gd->cut);
+                d.mass = __ldcg(&gd->mass);
+                d.target = __ldcg(&gd->target);
+                d.flags = __ldcg(&gd->flags);
+            }
+            sm.d[tid] = d;
+        }
+        __syncthreads();
+        if (tid == 0) {
+            int any = 0;
+            for (int c = 0; c < nb; ++c) any |= (sm.d[c].flags & kDescPrefix) ? 1 : 0;
+            sm.any_prefix = any;
+        }
+        __syncthreads();
+        if (!sm.abort) {
+            unsigned long long mine[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) mine[i] = 0ull;
+            for (int j = 0; j < ntl; ++j) {
+                uint32_t zr[32];
+                tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(j * kNG + h * 32), zr);
+                tmem_wait_ld();
+                const int v = (t0 + j) * kTileV + q * 32 + lane;
+                if (v >= V) continue;
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const int c = h * 32 + i;
+                    const Desc& d = sm.d[c];
+                    if (!(d.flags & (kDescDrawn | kDescPrefix))) continue;
+                    const float z = __uint_as_float(zr[i]);
+                    const bool in = rp::in_set(ordered_key(z), v, d.tau, d.cut);
+                    const float wv = in ? rp::weight_f(z, sm.zmax[c], sm.inv_t[c]) : 0.0f;
+                    const int b = g * kNG + c;
+                    __stcs(p.q + (static_cast<int64_t>(b) * p.gamma + (k - 1)) * V + v, wv * inv_mass(d.mass));
+                    if (d.flags & kDescPrefix) mine[i] += in ? rp::to_fixed(wv) : 0ull;
+                }
+            }
+            if (sm.any_prefix) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    unsigned long long s = mine[i];
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, o);
+                    if (lane == 0) sm.wpart[q][h * 32 + i] = s;
+                }
+            }
+        }
+        __syncthreads();
+        if (sm.any_prefix) {
+            if (tid < nb && (sm.d[tid].flags & kDescPrefix))
+                p.part[static_cast<size_t>(tid) * gridDim.x + blockIdx.x] =
+                    sm.wpart[0][tid] + sm.wpart[1][tid] + sm.wpart[2][tid] + sm.wpart[3][tid];
+            grid_sync(p, sm);  // ------------------------------------ barrier 5
+            // ------------------------------------------------ G: the CTA holding the draw finds it
+            for (int c = 0; c < nb; ++c) {
+                if (!(sm.d[c].flags & kDescPrefix) || sm.abort) continue;
+                // exclusive prefix of this CTA's range (CTAs in token order)
+                if (warp == 0) {
+                    unsigned long long ex = 0;
+                    for (int o = lane; o < static_cast<int>(blockIdx.x); o += 32)
+                        ex += __ldcg(p.part + static_cast<size_t>(c) * gridDim.x + o);
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) ex += __shfl_xor_sync(0xFFFFFFFFu, ex, o);
+                    if (lane == 0) {
+                        const unsigned long long mine = __ldcg(p.part + static_cast<size_t>(c) * gridDim.x + blockIdx.x);
+                        const unsigned long long tg = sm.d[c].target;
+                        sm.pick[1] = (ex <= tg && tg < ex + mine) ? 1 : 0;
+                        sm.ex = ex;
+                    }
+                }
+                __syncthreads();
+                if (!sm.pick[1]) continue;
+                // scan this range in token order: tiles in order, 128 rows each
+                // (warps 0..3 = quadrants 0..3 hold rows 32q..32q+31)
+                unsigned long long before = sm.ex;
+                const unsigned long long tg = sm.d[c].target;
+                const Desc d = sm.d[c];
+                int found = -1;
+                float fz = 0.0f;
+                for (int j = 0; j < ntl && found < 0; ++j) {
+                    unsigned long long wq = 0;
+                    float z = 0.0f;
+                    const int v = (t0 + j) * kTileV + (warp & 3) * 32 + lane;
+                    if (warp < 4) {
+                        z = __uint_as_float(tmem_ld1(tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) +
+                                                     static_cast<uint32_t>(j * kNG + c)));
+                        tmem_wait_ld();
+                        if (v < V && rp::in_set(ordered_key(z), v, d.tau, d.cut))
+                            wq = rp::to_fixed(rp::weight_f(z, sm.zmax[c], sm.inv_t[c]));
+                    }
+                    // inclusive scan over the 128 rows: warp scans, then the quadrant offsets
+                    unsigned long long incl = wq;
+#pragma unroll
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const unsigned long long y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+                        if (lane >= o) incl += y;
+                    }
+                    if (warp < 4 && lane == 31) sm.qsum[warp] = incl;
+                    __syncthreads();
+                    unsigned long long off = before;
+                    for (int w2 = 0; w2 < (warp & 3) && warp < 4; ++w2) off += sm.qsum[w2];
+                    if (warp < 4 && wq > 0 && off + incl > tg && off + incl - wq <= tg) {
+                        sm.pick[2] = v;
+                        reinterpret_cast<float*>(&sm.pick[3])[0] = z;
+                    }
+                    const unsigned long long tile_sum = sm.qsum[0] + sm.qsum[1] + sm.qsum[2] + sm.qsum[3];
+                    __syncthreads();
+                    if (before + tile_sum > tg) {
+                        found = sm.pick[2];
+                        fz = reinterpret_cast<float*>(&sm.pick[3])[0];
+                    }
+                    before += tile_sum;
+                    __syncthreads();
+                }
+                if (tid == 0) {
+                    const int b = g * kNG + c;
+                    const int64_t pidx = static_cast<int64_t>(b) * p.gamma + (k - 1);
+                    p.proposals[pidx] = found;
+                    p.q_at_x[pidx] = found >= 0 ? rp::weight_f(fz, sm.zmax[c], sm.inv_t[c]) * inv_mass(d.mass) : 0.0f;
+                }
+                __syncthreads();
+            }
+            grid_sync(p, sm);  // ------------------------------------ barrier 6
+        }
+    }
+
+    // ------------------------------------------------ exit
+    // On an abort, no copy or MMA may still be landing: wait (bounded) for
+    // what was issued.
+    if (tid == 0 && sm.abort) {
+        for (int n = max(0, w_issued - S); n < w_issued; ++n) mbar_wait(&sm.wfull[n % S], (n / S) & 1, kWaitLimitNs);
+        for (int n = max(0, b_issued - S); n < b_issued; ++n) mbar_wait(&sm.bfull[n % S], (n / S) & 1, kWaitLimitNs);
+        if (mma_done > 0) mbar_wait(&sm.wempty[(mma_done - 1) % S], ((mma_done - 1) / S) & 1, kWaitLimitNs);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+    // a wait gave up somewhere: no request's outputs can be trusted
+    if (blockIdx.x == 0 && *reinterpret_cast<volatile int*>(p.error))
+        for (int b = tid; b < p.B; b += kFT) p.status[b] = kReqTimeout;
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------ host
+namespace {
+
+constexpr int kSmemLimit = 232448;   // opt-in shared memory per CTA
+constexpr int kStaticAllowance = 24 * 1024;  // FusedSmem + the row engine's static shared memory
+constexpr int kEngineScratch = rp::kCap * 8 + rp::kWarps * rp::kBins * 4;  // the row engine's cbuf
+
+int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return 0;
+    return n;
+}
+
+struct FusedShape {
+    int ntiles, tpc, grid, groups, stages, smem;
+};
+
+bool fused_shape(int B, int V, int r, FusedShape& f) {
+    const int sms = sm_count();
+    if (sms <= 0 || B < 1 || r < 64 || r > 256 || r % 64 != 0 || V < kTileV) return false;
+    f.ntiles = (V + kTileV - 1) / kTileV;
+    f.tpc = (f.ntiles + sms - 1) / sms;
+    if (f.tpc > kMaxLT) return false;
+    f.grid = (f.ntiles + f.tpc - 1) / f.tpc;
+    f.groups = (B + kNG - 1) / kNG;
+    const int w = kTileV * r * 2, b = kNG * kTileV * 2, u = std::max(kNG * r * 2, kEngineScratch);
+    const int budget = kSmemLimit - kStaticAllowance - 1024;
+    f.stages = std::min(4, (budget - u) / (w + b));
+    if (f.stages < 2) return false;
+    // at least half the SM's shared memory, so that no two CTAs (each taking
+    // all of tensor memory) share an SM
+    f.smem = std::max(f.stages * (w + b) + u + 1024, 120 * 1024);
+    return true;
+}
+
+struct FusedLayout {
+    size_t bar, words, clear_end, desc, cand, part, zhard, total;
+};
+// Offsets from `base` (past the slower path's error word, which must stay
+// zero between calls); the words up to clear_end are cleared per call.
+FusedLayout fused_layout(int B, int gamma, int V) {
+    auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+    FusedLayout l;
+    const int groups = (B + kNG - 1) / kNG, rows = std::min(B, kNG);
+    l.bar = 256;
+    l.words = up(l.bar + 16);
+    l.clear_end = up(l.words + static_cast<size_t>(groups) * gamma * sizeof(StepWords));
+    l.desc = l.clear_end;
+    l.cand = up(l.desc + kNG * sizeof(Desc));
+    l.part = up(l.cand + static_cast<size_t>(kNG) * kCand * 8);
+    l.zhard = up(l.part + static_cast<size_t>(kNG) * 1024 * 8);
+    l.total = up(l.zhard + static_cast<size_t>(rows) * V * 4);
+    return l;
+}
+
+}  // namespace
+
+bool markov_fused_supported(int dtype, int B, int V, int r) {
+    FusedShape f;
+    return dtype == kBF16 && fused_shape(B, V, r, f) && f.grid <= 1024;
+}
+
+size_t markov_fused_workspace(int B, int gamma, int V) { return fused_layout(B, gamma, V).total; }
+
+cudaError_t launch_markov_fused(const MarkovFusedArgs& a, void* ws, size_t ws_bytes, cudaStream_t stream) {
+    FusedShape f;
+    if (!fused_shape(a.B, a.V, a.r, f)) return cudaErrorInvalidValue;
+    const FusedLayout lay = fused_layout(a.B, a.gamma, a.V);
+    if (ws_bytes < lay.total) return cudaErrorInvalidValue;
+    char* base = static_cast<char*>(ws);
+    FusedParams p{};
+    p.backbone = a.backbone;
+    p.U = a.U;
+    p.anchor = a.anchor;
+    p.policy = a.policy;
+    p.seed = a.seed;
+    p.request_id = a.request_id;
+    p.pos0 = a.pos0;
+    p.B = a.B;
+    p.gamma = a.gamma;
+    p.V = a.V;
+    p.r = a.r;
+    p.proposals = a.proposals;
+    p.q = a.q;
+    p.q_at_x = a.q_at_x;
+    p.status = a.status;
+    p.ntiles = f.ntiles;
+    p.tpc = f.tpc;
+    p.grid = f.grid;
+    p.groups = f.groups;
+    p.stages = f.stages;
+    p.bar = reinterpret_cast<unsigned int*>(base + lay.bar);
+    p.error = reinterpret_cast<int*>(base + lay.bar + 8);
+    p.words = reinterpret_cast<StepWords*>(base + lay.words);
+    p.desc = reinterpret_cast<Desc*>(base + lay.desc);
+    p.cand = reinterpret_cast<unsigned long long*>(base + lay.cand);
+    p.part = reinterpret_cast<unsigned long long*>(base + lay.part);
+    p.zhard = reinterpret_cast<float*>(base + lay.zhard);
+
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+    if (!enc) return cudaErrorNotSupported;
+    CUtensorMap wmap, bmap;
+    const cuuint32_t estr[3] = {1, 1, 1};
+    {   // W [V, r]: boxes of 64 columns (128 B) x 128 rows, 128-byte swizzle (the MMA's A operand)
+        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(a.r), static_cast<cuuint64_t>(a.V)};
+        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(a.r) * 2};
+        const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kTileV)};
+        if (enc(&wmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(a.W), dims, strides, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    {   // backbone [B, gamma, V]: boxes of 128 tokens x 1 step x 64 requests
+        const cuuint64_t dims[3] = {static_cast<cuuint64_t>(a.V), static_cast<cuuint64_t>(a.gamma),
+                                    static_cast<cuuint64_t>(a.B)};
+        const cuuint64_t strides[2] = {static_cast<cuuint64_t>(a.V) * 2, static_cast<cuuint64_t>(a.gamma) * a.V * 2};
+        const cuuint32_t box[3] = {static_cast<cuuint32_t>(kTileV), 1, static_cast<cuuint32_t>(kNG)};
+        if (enc(&bmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t*>(a.backbone), dims, strides, box,
+                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    cudaError_t e = cudaMemsetAsync(base + lay.bar, 0, lay.clear_end - lay.bar, stream);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(markov_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, f.smem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(f.grid));
+    cfg.blockDim = dim3(kFT);
+    cfg.dynamicSmemBytes = static_cast<size_t>(f.smem);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;  // every CTA resident: the grid barriers need it
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, markov_fused_kernel, wmap, bmap, p);
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+}  // namespace dspark
+

@@ -252,14 +252,18 @@ struct Slice {
     int lo, n;
     int per;   // contiguous elements per thread for ordered scans
     int bf16;  // storage format
+    int coherent = 0;  // 1: the row was written earlier in the same launch (read through L2, not the read-only path)
     __device__ __forceinline__ float val(int i) const {
+        if (coherent) return __ldcg(static_cast<const float*>(z) + i);
         return bf16 ? __uint_as_float(static_cast<uint32_t>(__ldg(static_cast<const unsigned short*>(z) + i)) << 16)
                     : __ldg(static_cast<const float*>(z) + i);
     }
     // 16-byte vectors: 8 (bf16) or 4 (fp32) elements each; n is a multiple of 8
     __device__ __forceinline__ int vper() const { return bf16 ? 8 : 4; }
     __device__ __forceinline__ int nvec() const { return n / vper(); }
-    __device__ __forceinline__ uint4 vec(int j) const { return __ldg(static_cast<const uint4*>(z) + j); }
+    __device__ __forceinline__ uint4 vec(int j) const {
+        return coherent ? __ldcg(static_cast<const uint4*>(z) + j) : __ldg(static_cast<const uint4*>(z) + j);
+    }
 };
 
 __device__ __forceinline__ uint32_t bf16x2_max(uint32_t a, uint32_t b) {
@@ -525,7 +529,7 @@ __device__ int32_t tie_index(Smem& sm, cg::cluster_group& cl, const Slice& sl, u
 // The policy by radix selection over the whole slice (the fallback when the
 // candidate set of row_policy would not fit).  z slice already loaded; max
 // key, argmax and the bad flag already reduced.
-__device__ void row_policy_radix(Smem& sm, cg::cluster_group& cl, const Slice& sl, int V, const Policy& pol,
+static __device__ void row_policy_radix(Smem& sm, cg::cluster_group& cl, const Slice& sl, int V, const Policy& pol,
                                  RowResult& res, unsigned long long* wbuf) {
     const float zmax = res.zmax;
     const uint32_t kmax = ordered_key(zmax);
@@ -697,7 +701,7 @@ __device__ int32_t sample_fixed(Smem& sm, cg::cluster_group& cl, const Slice& sl
 // flight): the row's max key / lowest argmax / non-finite flag, reduced over
 // the cluster.  Each thread keeps a packed maximum and looks for the index
 // only when a vector beats it.
-__device__ void slice_max(Smem& sm, cg::cluster_group& cl, const Slice& sl, RowResult& res, bool& bad) {
+static __device__ void slice_max(Smem& sm, cg::cluster_group& cl, const Slice& sl, RowResult& res, bool& bad) {
     const int vp = sl.vper(), nv = sl.nvec();
     float nanacc = -__int_as_float(0x7F800000);
     float bval = -__int_as_float(0x7F800000);  // this thread's maximum (vectors in index order)
@@ -761,7 +765,7 @@ __device__ __forceinline__ int32_t io_idx(unsigned long long c) {
 // Bitonic sort of buf[0, n) in descending order (n <= kCap), padding with 0
 // (below every real composite key) up to a power of two.  Each iteration
 // handles one compare-exchange pair.  All threads of the CTA.
-__device__ void sort_desc(unsigned long long* buf, int n) {
+static __device__ void sort_desc(unsigned long long* buf, int n) {
     int P = 1;
     while (P < n) P <<= 1;
     for (int i = n + threadIdx.x; i < P; i += kThreads) buf[i] = 0ull;
@@ -787,7 +791,7 @@ __device__ void sort_desc(unsigned long long* buf, int n) {
 // places one key at its rank (the number of larger keys), one pass over the
 // keys in shared memory; larger sets: the bitonic network.  All threads of
 // the CTA.
-__device__ void sort_candidates(unsigned long long* buf, int n) {
+static __device__ void sort_candidates(unsigned long long* buf, int n) {
     if (n > kThreads) {
         sort_desc(buf, n);
         return;
@@ -1042,7 +1046,7 @@ __device__ __forceinline__ unsigned long long hist_pass(const Slice& sl, float z
 // fall back to row_policy_radix.  cbuf = this CTA's candidate buffer (kCap
 // composite keys; only rank 0's receives candidates) followed by
 // kWarps x kBins 32-bit counts.
-__device__ void row_policy(Smem& sm, cg::cluster_group& cl, const Slice& sl, int V, const Policy& pol,
+static __device__ void row_policy(Smem& sm, cg::cluster_group& cl, const Slice& sl, int V, const Policy& pol,
                            RowResult& res, unsigned long long* cbuf) {
     const int nc = static_cast<int>(cl.num_blocks());  // CTAs in the cluster
     const float zmax = res.zmax;
