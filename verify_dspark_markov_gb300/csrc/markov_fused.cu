@@ -23,13 +23,17 @@
 //      global words.                                              | barrier
 //   B  greedy rows: the lowest index holding the maximum.  Sampled rows: a
 //      16-bin histogram of s = (zmax - z)/T (bins of 2 below s = 32; exact
-//      counts and exact fixed-point masses, the weights of the row engine),
-//      reduced into global words.                                 | barrier
+//      counts and, where top-p or a large top-k needs them, exact fixed-point
+//      masses with the row engine's weights), reduced into global words.
+//                                                                 | barrier
 //   C  (every CTA, for every request) the window of bins holding the top-k
 //      and top-p cuts, from the histogram's prefix sums (the row engine's
-//      rule); D compaction of the window's tokens into the request's
-//      candidate list in global memory.  A window larger than the list
-//      makes the row "hard": every CTA writes its z there instead.  | barrier
+//      rule).  A one-bin window with more tokens than a candidate list holds
+//      is refined once: a 16-bin histogram inside that bin (bins of 1/8),
+//      a barrier, the window again over the finer bins.
+//   D  compaction of the window's tokens into the request's candidate list
+//      in global memory.  A window still too large makes the row "hard":
+//      every CTA writes its z there instead.                      | barrier
 //   E  the request's owner CTA sorts its candidates and takes the cuts by
 //      exact prefix sums; with the whole support in the list it draws x_k at
 //      once.  A hard row is done whole by its owner with the row engine
@@ -51,6 +55,11 @@
 
 #include "common.cuh"
 #include "kernels.h"
+// The row engine (hard rows, the owners' sorts and draws) runs on the first
+// 256 threads of this kernel's 512, as a cluster of one CTA: its barriers are
+// a named barrier of those threads.
+#define RP_SYNC() asm volatile("bar.sync 1, 256;" ::: "memory")
+#define RP_CL_SYNC(cl) RP_SYNC()
 #include "row_policy.cuh"
 #include "tc_common.cuh"
 
@@ -61,17 +70,20 @@ namespace {
 using namespace tc;
 namespace cg = cooperative_groups;
 
-constexpr int kFT = 256;             // threads: the row engine's block size
+constexpr int kFT = 512;             // threads (16 warps)
+constexpr int kEng = rp::kThreads;   // the first kEng threads run the row engine
 constexpr int kNG = 64;              // requests per group (MMA N)
 constexpr int kMaxLT = 8;            // vocabulary tiles per CTA (8 x 64 columns = all of tensor memory)
 constexpr int kTileV = 128;          // vocabulary rows per tile (MMA M)
-constexpr int kHB = 16;              // histogram bins: s in [2i, 2i + 2), s < 32
+constexpr int kHB = 16;              // histogram bins: s in [2i, 2i + 2), s < 32; inside one: 16 of 1/8
 constexpr int kCand = rp::kCap;      // candidates a list holds (the owner sorts them in shared memory)
 constexpr int kWhole = rp::kThreads; // a support this small is compacted whole (drawn by its owner)
 constexpr uint32_t kTmemCols = 512;
 
-// request modes after the histogram
-enum : int { kModeNone = 0, kModeGreedy = 1, kModeWin = 2, kModeAll = 3, kModeHard = 4 };
+// request modes
+enum : int { kModeNone = 0, kModeGreedy = 1, kModeWin = 2, kModeAll = 3, kModeHard = 4, kModeRefine = 5 };
+// histogram work of a request in phase B: none, greedy argmax, counts, counts and masses
+enum : int { kHistNone = 0, kHistGreedy = 1, kHistCount = 2, kHistMass = 3 };
 // descriptor flags
 enum : uint32_t { kDescDrawn = 1u, kDescPrefix = 2u, kDescDone = 4u };
 
@@ -83,6 +95,8 @@ struct StepWords {
     uint32_t ccount[kNG];     // candidates claimed
     uint32_t hcnt[kNG][kHB];
     unsigned long long hmass[kNG][kHB];
+    uint32_t hcnt2[kNG][kHB];            // the refinement inside one bin
+    unsigned long long hmass2[kNG][kHB];
 };
 // The owner's result for a request of the current step.
 struct Desc {
@@ -93,9 +107,14 @@ struct Desc {
     uint32_t flags;
     int32_t pad;
 };
-// Window of one request (every CTA computes the same).
+// Window of one request (every CTA computes the same).  lvl 1: bins
+// [wlo, whi] but (phi, whi) of the 16 coarse bins; lvl 2: those of the 16
+// fine bins that split the coarse bins [rlo, rhi] evenly (fscale fine bins
+// per unit of s), and (keep_above) every coarse bin before rlo.
 struct Win {
     int mode;
+    int lvl, rlo, rhi, keep_above;
+    float fscale;
     int wlo, whi, phi;
     unsigned long long above_cnt, above_mass, wcount, gap_cnt, gap_mass, k_eff, total;
 };
@@ -132,13 +151,18 @@ struct FusedSmem {
     int abort;
     unsigned int bar_gen;
     int any_prefix;
+    int any_refine;
     int32_t x[kNG];
-    uint32_t cmax[4][kNG];
+    uint32_t smax[kMaxLT][kNG];  // per tile and request: the largest ordered key of its 128 rows (0: none)
     uint32_t cbad[4][kNG];
+    uint32_t floor_key[kNG];     // a pass's threshold: slabs whose maximum is below it hold no work
     // per request of the group, for the policy phases
     float zmax[kNG];
     float inv_t[kNG];
+    float inv_s[kNG];    // 1 / support mass (phase F)
+    float ba[kNG], bb[kNG];  // bin coefficients (bin_val)
     int mode[kNG];
+    int hist[kNG];
     int32_t code[kNG];   // the row's status when it fails at this step
     Win win[kNG];
     Desc d[kNG];
@@ -190,70 +214,126 @@ __device__ void grid_sync(const FusedParams& p, FusedSmem& sm) {
     __syncthreads();
 }
 
-// Bin of s = (zmax - z) * inv_t in steps of 2 below s = 32; kHB beyond.
-__device__ __forceinline__ int sbin(float z, float zmax, float inv_t) {
-    const float s = (zmax - z) * inv_t;
-    return s < 32.0f ? min(kHB - 1, static_cast<int>(s * 0.5f)) : kHB;
+// Bins of s = (zmax - z) / T in half units, bf = s / 2, taken as one fma
+// -z * ba + bb with ba = inv_t / 2, bb = zmax * ba (monotone in z; every
+// phase bins a token the same way): coarse bin floor(bf) below bf = 16 (kHB
+// beyond), fine bins splitting the coarse bins [rlo, rhi] in 16 even steps.
+__device__ __forceinline__ float bin_val(float z, float ba, float bb) { return fmaf(-z, ba, bb); }
+__device__ __forceinline__ int coarse_bin(float bf) { return bf < 16.0f ? min(kHB - 1, static_cast<int>(bf)) : kHB; }
+__device__ __forceinline__ int fine_bin(float bf, int rlo, float fscale) {
+    return min(kHB - 1, max(0, static_cast<int>((bf - static_cast<float>(rlo)) * fscale)));
+}
+
+// An ordered key below which every token has s = (zmax - z) * inv_t >= S
+// (margins far past the rounding of s): a slab whose maximum is below it
+// has no token with s < S.
+__device__ __forceinline__ uint32_t floor_key_s(float zmax, float inv_t, float S) {
+    float zf = zmax - (S / inv_t) * 1.0001f;
+    zf -= fabsf(zf) * 1e-6f + 1e-30f;
+    return ordered_key(zf);
+}
+// Is any of the 8 slabs (tile j, requests c0..c0+7) at or above its request's floor?
+__device__ __forceinline__ bool any_active8(const uint32_t* smax_j, const uint32_t* floor_key, int c0) {
+    bool a = false;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) a |= smax_j[c0 + i] >= floor_key[c0 + i];
+    return a;
 }
 
 __device__ __forceinline__ float inv_mass(unsigned long long mass) {
     return static_cast<float>(rp::kFix / static_cast<double>(mass));
 }
 
-// The window of bins holding a row's cuts from its 16-bin histogram (the
-// row engine's rule with 16 bins; cc / cm are inclusive prefix sums).
+// The window of bins holding a row's cuts from NB bins' inclusive prefix
+// sums cc (counts) and cm (masses): the row engine's rule (a support of at
+// most kWhole tokens is compacted whole, so that its owner can draw).
+template <int NB>
 __device__ Win make_window(const rp::Policy& pol, const unsigned long long* cc, const unsigned long long* cm) {
     Win w{};
     const bool use_k = pol.top_k > 0, use_p = pol.top_p < 1.0f;
-    w.total = cm[kHB - 1];
+    w.total = cm[NB - 1];
+    w.lvl = 1;
     if (!use_k && !use_p) {
         w.mode = kModeAll;
         return w;
     }
     const bool with_mass = !use_k || pol.top_k > kWhole;
-    const unsigned long long n_in = cc[kHB - 1];
+    const unsigned long long n_in = cc[NB - 1];
     w.k_eff = use_k ? min(static_cast<unsigned long long>(pol.top_k), n_in) : 0ull;
+    // (unrolled scans and selects: the prefix sums stay in registers)
     auto first_at_least = [](const unsigned long long* pre, unsigned long long x) {
-        int i = 0;
-        while (i < kHB - 1 && pre[i] < x) ++i;
+        int i = NB - 1;
+#pragma unroll
+        for (int b = NB - 2; b >= 0; --b)
+            if (pre[b] >= x) i = b;
         return i;
     };
-    int whi = use_k ? first_at_least(cc, w.k_eff) : kHB - 1;
+    auto at = [](const unsigned long long* pre, int idx) {
+        unsigned long long v = 0;
+#pragma unroll
+        for (int b = 0; b < NB; ++b)
+            if (b == idx) v = pre[b];
+        return v;
+    };
+    int whi = use_k ? first_at_least(cc, w.k_eff) : NB - 1;
     int wlo = 0;
-    const bool small = cc[whi] <= static_cast<unsigned long long>(kWhole);
+    const bool small = at(cc, whi) <= static_cast<unsigned long long>(kWhole);
     if (with_mass) {
-        const unsigned long long mk_lo = use_k ? (whi ? cm[whi - 1] : 0ull) : w.total;
+        const unsigned long long mk_lo = use_k ? (whi ? at(cm, whi - 1) : 0ull) : w.total;
         wlo = whi;
         if (use_p) {
             wlo = first_at_least(cm, rp::p_threshold(pol.top_p, mk_lo));
             if (!use_k) whi = wlo;
         }
-        if (small || cc[whi] <= static_cast<unsigned long long>(kWhole)) wlo = 0;
+        if (small || at(cc, whi) <= static_cast<unsigned long long>(kWhole)) wlo = 0;
     }
     int phi = whi;
     if (with_mass && use_k && use_p && !small) {
-        const int p_hi = first_at_least(cm, rp::p_threshold(pol.top_p, cm[whi]));
+        const int p_hi = first_at_least(cm, rp::p_threshold(pol.top_p, at(cm, whi)));
         if (p_hi + 1 < whi) phi = p_hi;
     }
-    const unsigned long long ac = wlo ? cc[wlo - 1] : 0ull;
-    const unsigned long long gc = phi < whi ? cc[whi - 1] - cc[phi] : 0ull;
+    const unsigned long long ac = wlo ? at(cc, wlo - 1) : 0ull;
+    const unsigned long long gc = phi < whi ? at(cc, whi - 1) - at(cc, phi) : 0ull;
     w.wlo = wlo;
     w.whi = whi;
     w.phi = phi;
     w.above_cnt = ac;
-    w.above_mass = wlo ? cm[wlo - 1] : 0ull;
-    w.wcount = cc[whi] - ac - gc;
+    w.above_mass = wlo ? at(cm, wlo - 1) : 0ull;
+    w.wcount = at(cc, whi) - ac - gc;
     w.gap_cnt = gc;
-    w.gap_mass = phi < whi ? cm[whi - 1] - cm[phi] : 0ull;
-    w.mode = w.wcount > static_cast<unsigned long long>(kCand) ? kModeHard : kModeWin;
+    w.gap_mass = phi < whi ? at(cm, whi - 1) - at(cm, phi) : 0ull;
+    if (NB == kHB && !with_mass && cc[kHB / 2 - 1] < static_cast<unsigned long long>(pol.top_k)) {
+        // counts only: the top-k crossing lies past s = 16, where tokens were
+        // not counted: refine s in [16, 32), keep the bins before
+        w.mode = kModeRefine;
+        w.rlo = kHB / 2;
+        w.rhi = kHB - 1;
+        w.fscale = 16.0f / static_cast<float>(w.rhi - w.rlo + 1);
+        return w;
+    } else if (w.wcount <= static_cast<unsigned long long>(kCand)) {
+        w.mode = kModeWin;
+    } else {
+        // too many tokens: refine the window's coarse bins into 16 finer ones
+        // (counts-only rows keep exact counts below s = 16 only: a top-k
+        // crossing past that goes to the row engine).
+        // Counts only (top-k <= kWhole): the bins before the top-k bin hold
+        // fewer than k tokens; refine the top-k bin and keep them whole.
+        w.mode = kModeRefine;
+        w.rlo = with_mass ? wlo : whi;
+        w.rhi = whi;
+        w.fscale = 16.0f / static_cast<float>(w.rhi - w.rlo + 1);
+    }
     return w;
 }
 
-template <typename F>
-__device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
-    return v;
+// Is a token of coarse bin b1 (and fine bin b2, level 2) in the window?
+__device__ __forceinline__ bool in_window(const Win& w, int b1, int b2) {
+    if (w.lvl == 2) {
+        if (b1 < w.rlo) return w.keep_above != 0;
+        if (b1 > w.rhi) return false;
+        b1 = b2;
+    }
+    return b1 >= w.wlo && b1 <= w.whi && (b1 <= w.phi || b1 == w.whi);
 }
 
 // ------------------------------------------------------------------ kernel
@@ -272,13 +352,12 @@ __global__ void __launch_bounds__(kFT, 1)
     uint8_t* sB = sW + S * w_bytes;
     uint8_t* sU = sB + S * b_bytes;  // also the owner's candidate buffer (and the row engine's scratch)
     unsigned long long* cbuf = reinterpret_cast<unsigned long long*>(sU);
-    // phase B's histogram lives there too (the step's MMAs have read U by then)
+    // the histograms of phases B and C live there too (the step's MMAs have read U by then)
     unsigned long long (*hmass)[kHB] = reinterpret_cast<unsigned long long (*)[kHB]>(sU);
     uint32_t (*hcnt)[kHB] = reinterpret_cast<uint32_t (*)[kHB]>(sU + kNG * kHB * 8);
 
     const int t0 = blockIdx.x * p.tpc;                        // first tile of this CTA
     const int ntl = max(0, min(p.tpc, p.ntiles - t0));        // its tiles
-    const int vend = min(V, (t0 + ntl) * kTileV);             // one past its last token
 
     if (warp == 0) tmem_alloc(&sm.tmem_base, kTmemCols);
     if (tid == 0) {
@@ -286,7 +365,7 @@ __global__ void __launch_bounds__(kFT, 1)
             mbar_init(&sm.wfull[s], 1);
             mbar_init(&sm.wempty[s], 1);
             mbar_init(&sm.bfull[s], 1);
-            mbar_init(&sm.bempty[s], 4);
+            mbar_init(&sm.bempty[s], 8);
         }
         for (int j = 0; j < kMaxLT; ++j) mbar_init(&sm.accfull[j], 1);
         sm.abort = 0;
@@ -297,8 +376,12 @@ __global__ void __launch_bounds__(kFT, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = sm.tmem_base;
+    // policy phases: warp w reads TMEM lane quadrant w % 4 and the 16 columns
+    // [16 (w / 4), 16 (w / 4) + 16)
+    const int q = warp & 3, cq = (warp >> 2) * 16;
+    const uint32_t tq = tmem + (static_cast<uint32_t>(q * 32) << 16);
 
-    // producer state (thread 0): W / backbone tiles issued and consumed, in order
+    // producers: thread 0 the W tiles and the MMAs, thread 32 the backbone tiles
     int w_issued = 0, b_issued = 0, mma_done = 0;
     const int steps_total = p.groups * p.gamma;
     auto tile_of = [&](int n) { return n % max(ntl, 1); };         // n-th tile of the whole launch
@@ -318,10 +401,10 @@ __global__ void __launch_bounds__(kFT, 1)
         tma_load_3d(sB + s * b_bytes, &bmap, t * kTileV, k, g * kNG, &sm.bfull[s]);
     };
     const int total_tiles = steps_total * ntl;
-    if (tid == 0) {
+    if (tid == 0)
         for (; w_issued < min(S, total_tiles); ++w_issued) issue_w(w_issued);
+    if (tid == 32)
         for (; b_issued < min(S, total_tiles); ++b_issued) issue_b(b_issued);
-    }
 
     for (int gs = 0; gs < steps_total; ++gs) {
         const int g = gs / p.gamma, k = gs % p.gamma + 1;  // k 1-based
@@ -339,6 +422,8 @@ __global__ void __launch_bounds__(kFT, 1)
             }
             sm.x[tid] = x;
         }
+        for (int i = tid; i < kMaxLT * kNG; i += kFT) (&sm.smax[0][0])[i] = 0u;
+        for (int i = tid; i < 4 * kNG; i += kFT) (&sm.cbad[0][0])[i] = 0u;
         __syncthreads();
         {
             const int kchunks = r / 8;
@@ -376,36 +461,45 @@ __global__ void __launch_bounds__(kFT, 1)
                     mma_commit(&sm.wempty[s]);
                     mma_commit(&sm.accfull[j]);
                     ++mma_done;
-                    // refill the W stage of the previous tile (its MMAs were issued one tile ago)
-                    if (n >= 1 && w_issued < total_tiles && w_issued <= n - 1 + S) {
-                        const int m = n - 1;
-                        if (!mbar_wait(&sm.wempty[m % S], (m / S) & 1, kWaitLimitNs)) {
+                    // refill this stage S tiles ahead once its MMAs have read it
+                    // (a short wait: S tiles stay in flight)
+                    if (w_issued < total_tiles && w_issued <= n + S) {
+                        if (!mbar_wait(&sm.wempty[s], (n / S) & 1, kWaitLimitNs)) {
                             atomicExch(p.error, 1);
                             sm.abort = 1;
                             break;
                         }
                         issue_w(w_issued++);
                     }
-                    // and the backbone stage of the previous tile, once the
-                    // epilogue has read it (that needs only MMAs already issued)
-                    if (n >= 1 && b_issued < total_tiles && b_issued <= n - 1 + S) {
-                        const int m = n - 1;
-                        if (!mbar_wait(&sm.bempty[m % S], (m / S) & 1, kWaitLimitNs)) {
+                }
+            }
+        } else if (warp == 1) {
+            // the backbone stream: S tiles ahead of the epilogue, each stage
+            // refilled once the epilogue has read it (the epilogue needs only
+            // MMAs that thread 0 issues without waiting for this thread)
+            if (lane == 0 && !aborted) {
+                for (int j = 0; j < ntl; ++j) {
+                    const int n = gs * ntl + j;
+                    bool ok = true;
+                    while (b_issued < total_tiles && b_issued <= n + S - 1) {
+                        const int m = b_issued - S;
+                        if (m >= 0 && !mbar_wait(&sm.bempty[m % S], (m / S) & 1, kWaitLimitNs)) {
                             atomicExch(p.error, 1);
                             sm.abort = 1;
+                            ok = false;
                             break;
                         }
                         issue_b(b_issued++);
                     }
+                    if (!ok) break;
                 }
             }
-        } else if (warp >= 4) {
-            // epilogue: quadrant q = lanes 32q..32q+31 of every tile, all 64 columns
-            const int q = warp - 4;
-            uint32_t kmax[kNG];
-            uint32_t badm0 = 0u, badm1 = 0u;
-#pragma unroll
-            for (int c = 0; c < kNG; ++c) kmax[c] = 0u;
+        } else if (warp >= 8) {
+            // epilogue: warp w takes TMEM lane quadrant w % 4 of every tile and
+            // the 32 columns [32 eh, 32 eh + 32), in chunks of 16
+            const int eq = warp & 3, eh = (warp - 8) >> 2;
+            const uint32_t te = tmem + (static_cast<uint32_t>(eq * 32) << 16) + static_cast<uint32_t>(eh * 32);
+            const float ninf = -__int_as_float(0x7F800000);
             for (int j = 0; j < ntl && !aborted; ++j) {
                 const int n = gs * ntl + j, s = n % S;
                 if (!mbar_wait(&sm.accfull[j], par, kWaitLimitNs) || !mbar_wait(&sm.bfull[s], (n / S) & 1, kWaitLimitNs)) {
@@ -414,51 +508,54 @@ __global__ void __launch_bounds__(kFT, 1)
                     break;
                 }
                 tc_fence_after();
-                uint32_t acc[64];
-                const uint32_t ta = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(j * kNG);
-                tmem_ld64(ta, acc);
-                tmem_wait_ld();
-                const int vl = q * 32 + lane;                 // row of the tile
-                const int v = (t0 + j) * kTileV + vl;
-                const uint16_t* bb = reinterpret_cast<const uint16_t*>(sB + s * b_bytes);
-                const bool valid = v < V;
+                const int vl = eq * 32 + lane;                // row of the tile
+                const bool valid = (t0 + j) * kTileV + vl < V;
+                const uint16_t* bb = reinterpret_cast<const uint16_t*>(sB + s * b_bytes) + eh * 32 * kTileV + vl;
+                float mx[32];  // this row's logit per request, NaN-propagating (rows past V: -inf)
 #pragma unroll
-                for (int c = 0; c < kNG; ++c) {
-                    const float z = __uint_as_float(acc[c]) +
-                                    __uint_as_float(static_cast<uint32_t>(bb[c * kTileV + vl]) << 16);
-                    acc[c] = __float_as_uint(valid ? z : -__int_as_float(0x7F800000));
-                    if (valid) {
-                        if (bad_logit(z)) {
-                            if (c < 32) badm0 |= 1u << c;
-                            else badm1 |= 1u << (c - 32);
-                        } else {
-                            const uint32_t kz = ordered_key(z);
-                            kmax[c] = kz > kmax[c] ? kz : kmax[c];
-                        }
+                for (int h16 = 0; h16 < 2; ++h16) {
+                    uint32_t acc[16];
+                    const uint32_t ta = te + static_cast<uint32_t>(j * kNG + h16 * 16);
+                    tmem_ld16(ta, acc);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const float z = valid ? __uint_as_float(acc[i]) +
+                                                    __uint_as_float(static_cast<uint32_t>(bb[(h16 * 16 + i) * kTileV]) << 16)
+                                              : ninf;
+                        acc[i] = __float_as_uint(z);
+                        mx[h16 * 16 + i] = z;
+                    }
+                    tmem_st16(ta, acc);
+                }
+                // slab maxima (this tile, 32 requests) over the warp's 32 rows
+                // with a NaN-propagating max (a NaN or +inf maximum marks the
+                // row non-finite): a transposing butterfly leaves request
+                // eh * 32 + lane's in this lane
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {
+                    const bool upper = (lane & o) != 0;
+#pragma unroll
+                    for (int i = 0; i < o; ++i) {
+                        const float keep = upper ? mx[i + o] : mx[i];
+                        const float give = upper ? mx[i] : mx[i + o];
+                        mx[i] = fmax_nan(keep, __shfl_xor_sync(0xFFFFFFFFu, give, o));
                     }
                 }
-                tmem_st64(ta, acc);
+                const float m = mx[0];
+                if (bad_logit(m)) sm.cbad[eq][eh * 32 + lane] = 1u;
+                else if (m != ninf) atomicMax(&sm.smax[j][eh * 32 + lane], ordered_key(m));
                 tmem_wait_st();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&sm.bempty[s]);
-            }
-            // column maxima over the warp's lanes, then over the four quadrants
-#pragma unroll
-            for (int c = 0; c < kNG; ++c) {
-                const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, kmax[c]);
-                if (lane == 0) sm.cmax[q][c] = m;
-            }
-            badm0 = __reduce_or_sync(0xFFFFFFFFu, badm0);
-            badm1 = __reduce_or_sync(0xFFFFFFFFu, badm1);
-            if (lane == 0) {
-                for (int c = 0; c < kNG; ++c) sm.cbad[q][c] = ((c < 32 ? badm0 >> c : badm1 >> (c - 32)) & 1u);
             }
         }
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
         if (tid < nb && !sm.abort) {
-            const uint32_t m = max(max(sm.cmax[0][tid], sm.cmax[1][tid]), max(sm.cmax[2][tid], sm.cmax[3][tid]));
+            uint32_t m = 0u;
+            for (int j = 0; j < ntl; ++j) m = max(m, sm.smax[j][tid]);
             const uint32_t bd = sm.cbad[0][tid] | sm.cbad[1][tid] | sm.cbad[2][tid] | sm.cbad[3][tid];
             if (m) red_max_u32(&sw.maxkey[tid], m);
             if (bd) red_or_u32(&sw.bad[tid], 1u);
@@ -467,7 +564,7 @@ __global__ void __launch_bounds__(kFT, 1)
 
         // ------------------------------------------------ B: greedy argmax, histograms
         if (tid < kNG) {
-            int mode = kModeNone;
+            int mode = kModeNone, hist = kHistNone;
             int32_t code = kReqOk;
             float zm = 0.0f, it = 1.0f;
             if (tid < nb && sm.x[tid] >= 0 && !sm.abort) {
@@ -482,12 +579,24 @@ __global__ void __launch_bounds__(kFT, 1)
                 it = pol.inv_t;
                 // the row engine's order: non-finite, then empty, then an invalid policy
                 code = bad ? kReqNonfinite : (empty ? kReqEmpty : (pol_ok ? kReqOk : kReqBadPolicy));
-                if (code == kReqOk) mode = pol.greedy ? kModeGreedy : kModeWin;  // Win refined in C
+                if (code == kReqOk) {
+                    mode = pol.greedy ? kModeGreedy : kModeWin;  // Win refined in C
+                    hist = pol.greedy ? kHistGreedy
+                                      : ((pol.top_k > 0 && pol.top_k <= kWhole) ? kHistCount : kHistMass);
+                }
             }
             sm.mode[tid] = mode;
+            sm.hist[tid] = hist;
             sm.code[tid] = code;
             sm.zmax[tid] = zm;
             sm.inv_t[tid] = it;
+            sm.ba[tid] = 0.5f * it;
+            sm.bb[tid] = zm * (0.5f * it);
+            // slabs that can hold work: greedy rows the maximum, counts-only
+            // rows s < 16, other sampled rows s < 32
+            sm.floor_key[tid] = hist == kHistNone ? 0xFFFFFFFFu
+                              : hist == kHistGreedy ? ordered_key(zm)
+                              : floor_key_s(zm, it, hist == kHistCount ? 16.0f : 32.0f);
         }
         for (int i = tid; i < kNG * kHB; i += kFT) {
             (&hcnt[0][0])[i] = 0u;
@@ -506,31 +615,60 @@ __global__ void __launch_bounds__(kFT, 1)
             }
         }
         __syncthreads();
-        const int q = warp & 3, h = warp >> 2;  // TMEM lane quadrant; column half
         if (!sm.abort) {
-            for (int j = 0; j < ntl; ++j) {
-                uint32_t zr[32];
-                tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(j * kNG + h * 32), zr);
-                tmem_wait_ld();
-                const int v = (t0 + j) * kTileV + q * 32 + lane;
+            for (int c0 = cq; c0 < cq + 16; c0 += 8) {
+                // counts-only rows count s < 16 only (a top-k crossing past it
+                // is refined over [16, 32) in phase C)
+                int hmr[8];
+                float zmr[8], bar_[8], bbr[8], itr[8];
+                uint32_t flr[8];
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int c = h * 32 + i;
-                    const int mode = sm.mode[c];
-                    if (mode == kModeNone) continue;
-                    const float z = __uint_as_float(zr[i]);
-                    if (mode == kModeGreedy) {
-                        const bool hit = v < V && ordered_key(z) == ordered_key(sm.zmax[c]);
-                        const uint32_t key = hit ? 0xFFFFFFFFu - static_cast<uint32_t>(v) : 0u;
-                        const uint32_t best = __reduce_max_sync(0xFFFFFFFFu, key);
+                for (int i = 0; i < 8; ++i) {
+                    hmr[i] = sm.hist[c0 + i];
+                    zmr[i] = sm.zmax[c0 + i];
+                    itr[i] = sm.inv_t[c0 + i];
+                    bar_[i] = sm.ba[c0 + i];
+                    bbr[i] = sm.bb[c0 + i];
+                    flr[i] = sm.floor_key[c0 + i];
+                }
+                for (int j = 0; j < ntl; ++j) {
+                    uint32_t act = 0u;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) act |= (sm.smax[j][c0 + i] >= flr[i] ? 1u : 0u) << i;
+                    if (!act) continue;
+                    uint32_t zr[8];
+                    tmem_ld8(tq + static_cast<uint32_t>(j * kNG + c0), zr);
+                    tmem_wait_ld();
+                    const int v = (t0 + j) * kTileV + q * 32 + lane;
+                    if (v >= V) continue;  // (greedy rows' warp reduction below needs every lane: handled there)
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int hm = hmr[i];
+                        if (hm <= kHistGreedy || !((act >> i) & 1u)) continue;
+                        const float z = __uint_as_float(zr[i]);
+                        const float bf = bin_val(z, bar_[i], bbr[i]);
+                        if (bf >= (hm == kHistCount ? 8.0f : 16.0f)) continue;
+                        const int bin = min(kHB - 1, static_cast<int>(bf));
+                        atomicAdd(&hcnt[c0 + i][bin], 1u);
+                        if (hm == kHistMass)
+                            atomicAdd(&hmass[c0 + i][bin],
+                                      static_cast<unsigned long long>(rp::to_fixed(rp::weight_f(z, zmr[i], itr[i]))));
+                    }
+                }
+                // greedy rows: the lowest index holding the maximum
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    if (hmr[i] != kHistGreedy) continue;
+                    const int c = c0 + i;
+                    const uint32_t mk = ordered_key(zmr[i]);
+                    for (int j = 0; j < ntl; ++j) {
+                        if (sm.smax[j][c] < mk) continue;
+                        const uint32_t z = tmem_ld1(tq + static_cast<uint32_t>(j * kNG + c));
+                        tmem_wait_ld();
+                        const int v = (t0 + j) * kTileV + q * 32 + lane;
+                        const bool hit = v < V && ordered_key(__uint_as_float(z)) == mk;
+                        const uint32_t best = __reduce_max_sync(0xFFFFFFFFu, hit ? 0xFFFFFFFFu - static_cast<uint32_t>(v) : 0u);
                         if (lane == 0 && best) red_max_u32(&sw.amax[c], best);
-                    } else if (v < V) {
-                        const float zm = sm.zmax[c], it = sm.inv_t[c];
-                        const int bin = sbin(z, zm, it);
-                        if (bin < kHB) {
-                            atomicAdd(&hcnt[c][bin], 1u);
-                            atomicAdd(&hmass[c][bin], static_cast<unsigned long long>(rp::to_fixed(rp::weight_f(z, zm, it))));
-                        }
                     }
                 }
             }
@@ -538,73 +676,188 @@ __global__ void __launch_bounds__(kFT, 1)
         __syncthreads();
         for (int i = tid; i < kNG * kHB; i += kFT) {
             const int c = i / kHB;
-            if (sm.mode[c] != kModeWin) continue;
+            if (sm.hist[c] < kHistCount) continue;
             const uint32_t cn = (&hcnt[0][0])[i];
             if (cn) {
                 red_add_u32(&sw.hcnt[0][0] + i, cn);
-                red_add_u64(&sw.hmass[0][0] + i, (&hmass[0][0])[i]);
+                if (sm.hist[c] == kHistMass) red_add_u64(&sw.hmass[0][0] + i, (&hmass[0][0])[i]);
             }
         }
         grid_sync(p, sm);  // ---------------------------------------- barrier 2
 
         // ------------------------------------------------ C: windows (every CTA)
-        for (int c = warp; c < kNG; c += kFT / 32) {
+        for (int i = tid; i < kNG * kHB; i += kFT) {  // the histograms, all loads in flight at once
+            const int c = i / kHB;
+            if (sm.mode[c] != kModeWin) continue;
+            (&hcnt[0][0])[i] = ld_cg_u32(&sw.hcnt[0][0] + i);
+            (&hmass[0][0])[i] = sm.hist[c] == kHistMass ? ld_cg_u64(&sw.hmass[0][0] + i) : 0ull;
+        }
+        __syncthreads();
+        if (tid < kNG) {
+            const int c = tid;
             if (sm.mode[c] != kModeWin) {
-                if (lane == 0) sm.win[c].mode = sm.mode[c];
-                continue;
-            }
-            unsigned long long cn = 0, ms = 0;
-            if (lane < kHB) {
-                cn = ld_cg_u32(&sw.hcnt[c][lane]);
-                ms = ld_cg_u64(&sw.hmass[c][lane]);
-            }
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {  // inclusive prefix sums over the bins
-                const unsigned long long a = __shfl_up_sync(0xFFFFFFFFu, cn, o);
-                const unsigned long long bm = __shfl_up_sync(0xFFFFFFFFu, ms, o);
-                if (lane >= o) {
-                    cn += a;
-                    ms += bm;
+                sm.win[c].mode = sm.mode[c];
+            } else {
+                unsigned long long cc[kHB], cm[kHB], a = 0, m = 0;
+                for (int i = 0; i < kHB; ++i) {
+                    a += hcnt[c][i];
+                    m += hmass[c][i];
+                    cc[i] = a;
+                    cm[i] = m;
                 }
-            }
-            unsigned long long cc[kHB], cm[kHB];
-#pragma unroll
-            for (int i = 0; i < kHB; ++i) {
-                cc[i] = __shfl_sync(0xFFFFFFFFu, cn, i);
-                cm[i] = __shfl_sync(0xFFFFFFFFu, ms, i);
-            }
-            if (lane == 0) {
                 rp::Policy pol;
                 rp::make_policy(p.policy[g * kNG + c], V, pol);
-                sm.win[c] = make_window(pol, cc, cm);
+                sm.win[c] = make_window<kHB>(pol, cc, cm);
             }
         }
         __syncthreads();
-        // ------------------------------------------------ D: compaction (and hard rows' z)
-        if (!sm.abort) {
-            for (int j = 0; j < ntl; ++j) {
-                uint32_t zr[32];
-                tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(j * kNG + h * 32), zr);
-                tmem_wait_ld();
-                const int v = (t0 + j) * kTileV + q * 32 + lane;
+        if (tid == 0) {
+            int any = 0;
+            for (int c = 0; c < nb; ++c) any |= sm.win[c].mode == kModeRefine;
+            sm.any_refine = any;
+        }
+        __syncthreads();
+        if (sm.any_refine) {
+            // ---- C2: a 16-bin histogram of 1/8 steps inside each refined row's bin
+            for (int i = tid; i < kNG * kHB; i += kFT) {
+                (&hcnt[0][0])[i] = 0u;
+                (&hmass[0][0])[i] = 0ull;
+            }
+            __syncthreads();
+            if (!sm.abort) {
+                for (int c0 = cq; c0 < cq + 16; c0 += 8) {
+                    for (int j = 0; j < ntl; ++j) {
+                        uint32_t zr[8];
+                        tmem_ld8(tq + static_cast<uint32_t>(j * kNG + c0), zr);
+                        tmem_wait_ld();
+                        const int v = (t0 + j) * kTileV + q * 32 + lane;
+                        if (v >= V) continue;
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int c = h * 32 + i;
-                    const int mode = sm.win[c].mode;
-                    const float z = __uint_as_float(zr[i]);
-                    if (mode == kModeHard) {
-                        if (v < V) p.zhard[static_cast<size_t>(c) * V + v] = z;
-                    } else if (mode == kModeWin) {
-                        const Win& w = sm.win[c];
-                        const int bin = v < V ? sbin(z, sm.zmax[c], sm.inv_t[c]) : kHB;
-                        const bool pick = bin >= w.wlo && bin <= w.whi && (bin <= w.phi || bin == w.whi);
-                        const unsigned mask = __ballot_sync(0xFFFFFFFFu, pick);
-                        if (mask) {
-                            uint32_t base = 0;
-                            if (lane == 0) base = atomicAdd(&sw.ccount[c], static_cast<uint32_t>(__popc(mask)));
-                            base = __shfl_sync(0xFFFFFFFFu, base, 0) + __popc(mask & ((1u << lane) - 1u));
-                            if (pick && base < static_cast<uint32_t>(kCand))
-                                p.cand[static_cast<size_t>(c) * kCand + base] = rp::value_order(ordered_key(z), v);
+                        for (int i = 0; i < 8; ++i) {
+                            const int c = c0 + i;
+                            if (sm.win[c].mode != kModeRefine) continue;
+                            const float z = __uint_as_float(zr[i]);
+                            const float zm = sm.zmax[c], it = sm.inv_t[c];
+                            const float bf = bin_val(z, sm.ba[c], sm.bb[c]);
+                            const int b1 = coarse_bin(bf);
+                            if (b1 < sm.win[c].rlo || b1 > sm.win[c].rhi) continue;
+                            const int fb = fine_bin(bf, sm.win[c].rlo, sm.win[c].fscale);
+                            atomicAdd(&hcnt[c][fb], 1u);
+                            atomicAdd(&hmass[c][fb], static_cast<unsigned long long>(rp::to_fixed(rp::weight_f(z, zm, it))));
+                        }
+                    }
+                }
+            }
+            __syncthreads();
+            for (int i = tid; i < kNG * kHB; i += kFT) {
+                const int c = i / kHB;
+                if (sm.win[c].mode != kModeRefine) continue;
+                const uint32_t cn = (&hcnt[0][0])[i];
+                if (cn) {
+                    red_add_u32(&sw.hcnt2[0][0] + i, cn);
+                    red_add_u64(&sw.hmass2[0][0] + i, (&hmass[0][0])[i]);
+                }
+            }
+            grid_sync(p, sm);  // ------------------------------------ barrier 2b
+            for (int i = tid; i < kNG * kHB; i += kFT) {
+                const int c = i / kHB;
+                if (sm.win[c].mode != kModeRefine) continue;
+                (&hcnt[0][0])[i] = ld_cg_u32(&sw.hcnt2[0][0] + i);
+                (&hmass[0][0])[i] = ld_cg_u64(&sw.hmass2[0][0] + i);
+            }
+            __syncthreads();
+            if (tid < kNG && sm.win[tid].mode == kModeRefine) {
+                // bins: everything above the refined range, its 16 fine bins,
+                // everything below it (inside s < 32)
+                const int c = tid;
+                const int rlo = sm.win[c].rlo, rhi = sm.win[c].rhi;
+                const float fscale = sm.win[c].fscale;
+                unsigned long long cc[kHB + 2], cm[kHB + 2];
+                unsigned long long a = 0, m = 0, a1 = 0, m1 = 0, b1 = 0, bm = 0;
+#pragma unroll
+                for (int i = 0; i < kHB; ++i) {
+                    const unsigned long long ci = ld_cg_u32(&sw.hcnt[c][i]), mi = ld_cg_u64(&sw.hmass[c][i]);
+                    if (i < rlo) {
+                        a1 += ci;
+                        m1 += mi;
+                    }
+                    if (i > rhi) {
+                        b1 += ci;
+                        bm += mi;
+                    }
+                }
+                cc[0] = a = a1;
+                cm[0] = m = m1;
+#pragma unroll
+                for (int i = 0; i < kHB; ++i) {
+                    a += hcnt[c][i];
+                    m += hmass[c][i];
+                    cc[1 + i] = a;
+                    cm[1 + i] = m;
+                }
+                cc[kHB + 1] = a + b1;
+                cm[kHB + 1] = m + bm;
+                rp::Policy pol;
+                rp::make_policy(p.policy[g * kNG + c], V, pol);
+                Win w = make_window<kHB + 2>(pol, cc, cm);
+                // the window must end inside the refined bin (fine bins 1..16);
+                // starting at bin 0 keeps every coarse bin before it
+                if (w.mode == kModeWin && w.whi >= 1 && w.whi <= kHB && w.phi >= 1 && w.phi <= kHB) {
+                    w.lvl = 2;
+                    w.rlo = rlo;
+                    w.rhi = rhi;
+                    w.fscale = fscale;
+                    w.keep_above = w.wlo == 0;
+                    w.wlo = max(w.wlo, 1) - 1;
+                    w.whi -= 1;
+                    w.phi -= 1;
+                } else {
+                    w.mode = kModeHard;
+                }
+                sm.win[c] = w;
+            }
+            __syncthreads();
+        }
+        // ------------------------------------------------ D: compaction (and hard rows' z)
+        if (tid < kNG) {
+            const Win& w = sm.win[tid];
+            sm.floor_key[tid] = w.mode == kModeHard ? 0u
+                              : w.mode == kModeWin ? floor_key_s(sm.zmax[tid], sm.inv_t[tid],
+                                                                 2.0f * static_cast<float>((w.lvl == 1 ? w.whi : w.rhi) + 1))
+                                                   : 0xFFFFFFFFu;
+        }
+        __syncthreads();
+        if (!sm.abort) {
+            for (int c0 = cq; c0 < cq + 16; c0 += 8) {
+                for (int j = 0; j < ntl; ++j) {
+                    if (!any_active8(sm.smax[j], sm.floor_key, c0)) continue;
+                    uint32_t zr[8];
+                    tmem_ld8(tq + static_cast<uint32_t>(j * kNG + c0), zr);
+                    tmem_wait_ld();
+                    const int v = (t0 + j) * kTileV + q * 32 + lane;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int c = c0 + i;
+                        const int mode = sm.win[c].mode;
+                        if (sm.smax[j][c] < sm.floor_key[c]) continue;
+                        const float z = __uint_as_float(zr[i]);
+                        if (mode == kModeHard) {
+                            if (v < V) p.zhard[static_cast<size_t>(c) * V + v] = z;
+                        } else if (mode == kModeWin) {
+                            const float bf = bin_val(z, sm.ba[c], sm.bb[c]);
+                            const int b1 = v < V ? coarse_bin(bf) : kHB;
+                            const Win& w = sm.win[c];
+                            const bool pick =
+                                b1 < kHB &&
+                                in_window(w, b1, (w.lvl == 2 && b1 >= w.rlo && b1 <= w.rhi) ? fine_bin(bf, w.rlo, w.fscale) : 0);
+                            const unsigned mask = __ballot_sync(0xFFFFFFFFu, pick);
+                            if (mask) {
+                                uint32_t base = 0;
+                                if (lane == 0) base = atomicAdd(&sw.ccount[c], static_cast<uint32_t>(__popc(mask)));
+                                base = __shfl_sync(0xFFFFFFFFu, base, 0) + __popc(mask & ((1u << lane) - 1u));
+                                if (pick && base < static_cast<uint32_t>(kCand))
+                                    p.cand[static_cast<size_t>(c) * kCand + base] = rp::value_order(ordered_key(z), v);
+                            }
                         }
                     }
                 }
@@ -613,7 +866,8 @@ __global__ void __launch_bounds__(kFT, 1)
         grid_sync(p, sm);  // ---------------------------------------- barrier 3
 
         // ------------------------------------------------ E: owners (cuts, draws, hard rows)
-        for (int c = blockIdx.x; c < nb; c += gridDim.x) {
+        // on the row engine's threads (the first kEng); the others wait at the barrier
+        for (int c = blockIdx.x; c < nb && tid < kEng; c += gridDim.x) {
             if (sm.abort) break;
             const int b = g * kNG + c;
             const int64_t pidx = static_cast<int64_t>(b) * p.gamma + (k - 1);
@@ -664,9 +918,9 @@ __global__ void __launch_bounds__(kFT, 1)
                 // the row engine on the whole row, this CTA as a cluster of one
                 cg::cluster_group cl = cg::this_cluster();
                 rp::init_smem(rsm);
-                __syncthreads();
+                RP_SYNC();
                 const float* zrow = p.zhard + static_cast<size_t>(c) * V;
-                rp::Slice sl{zrow, 0, V, (V + kFT - 1) / kFT, 0, 1};  // written by this launch: coherent loads
+                rp::Slice sl{zrow, 0, V, (V + kEng - 1) / kEng, 0, 1};  // written by this launch: coherent loads
                 rp::RowResult res;
                 bool bad;
                 rp::slice_max(rsm, cl, sl, res, bad);
@@ -676,7 +930,7 @@ __global__ void __launch_bounds__(kFT, 1)
                 rp::row_policy(rsm, cl, sl, V, pol, res, cbuf);
                 const float invS = inv_mass(res.mass);
                 float* qrow = p.q + pidx * V;
-                for (int v = tid; v < V; v += kFT) {
+                for (int v = tid; v < V; v += kEng) {
                     const float z = __ldcg(zrow + v);
                     qrow[v] = rp::in_set(ordered_key(z), v, res.tau, res.cut) ? rp::weight_f(z, res.zmax, pol.inv_t) * invS
                                                                               : 0.0f;
@@ -697,14 +951,14 @@ __global__ void __launch_bounds__(kFT, 1)
                     d.flags = kDescDone;
                     p.desc[c] = d;
                 }
-                __syncthreads();
+                RP_SYNC();
                 continue;
             }
             // kModeWin: the candidates, sorted; the cuts by exact prefix sums
             const Win w = sm.win[c];
             const int n = static_cast<int>(min(static_cast<unsigned long long>(ld_cg_u32(&sw.ccount[c])), w.wcount));
-            for (int i = tid; i < n; i += kFT) cbuf[i] = __ldcg(p.cand + static_cast<size_t>(c) * kCand + i);
-            __syncthreads();
+            for (int i = tid; i < n; i += kEng) cbuf[i] = __ldcg(p.cand + static_cast<size_t>(c) * kCand + i);
+            RP_SYNC();
             rp::sort_candidates(cbuf, n);
             const bool use_k = pol.top_k > 0, use_p = pol.top_p < 1.0f;
             const int K = use_k ? static_cast<int>(min(w.k_eff - w.above_cnt - w.gap_cnt, static_cast<unsigned long long>(n)))
@@ -741,8 +995,8 @@ __global__ void __launch_bounds__(kFT, 1)
                     [&](uint32_t key, int32_t) { return rp::to_fixed(rp::weight_f(key_to_float(key), zmax, inv_t)); },
                     total);
                 if (tid == 0) sm.pick[0] = xk;
-                __syncthreads();
-                for (int i = tid; i < mm; i += kFT)
+                RP_SYNC();
+                for (int i = tid; i < mm; i += kEng)
                     if (rp::vo_idx(cbuf[i]) == sm.pick[0])
                         p.q_at_x[pidx] = rp::weight_f(key_to_float(rp::vo_key(cbuf[i])), zmax, inv_t) * inv_mass(mass);
                 if (tid == 0) {
@@ -758,13 +1012,14 @@ __global__ void __launch_bounds__(kFT, 1)
                 p.desc[c] = d;
                 if (k == 1) p.status[b] = kReqOk;
             }
-            __syncthreads();
+            RP_SYNC();
         }
         grid_sync(p, sm);  // ---------------------------------------- barrier 4
 
         // ------------------------------------------------ F: q, support mass of this range
         if (tid < kNG) {
             Desc d{};
+            float is = 0.0f;
             if (tid < nb && (sm.win[tid].mode == kModeWin || sm.win[tid].mode == kModeAll)) {
                 const Desc* gd = p.desc + tid;
                 d.tau = __ldcg(&gd->tau);
@@ -772,8 +1027,10 @@ __global__ void __launch_bounds__(kFT, 1)
                 d.mass = __ldcg(&gd->mass);
                 d.target = __ldcg(&gd->target);
                 d.flags = __ldcg(&gd->flags);
+                is = d.mass ? inv_mass(d.mass) : 0.0f;
             }
             sm.d[tid] = d;
+            sm.inv_s[tid] = is;
         }
         __syncthreads();
         if (tid == 0) {
@@ -782,36 +1039,56 @@ __global__ void __launch_bounds__(kFT, 1)
             sm.any_prefix = any;
         }
         __syncthreads();
+        // slabs with a support token (key >= tau) are written from tensor
+        // memory; the others of the rows with q get zeros, 16 bytes a lane
+        if (tid < kNG) {
+            const uint32_t fl = sm.d[tid].flags;
+            sm.floor_key[tid] = (fl & (kDescDrawn | kDescPrefix)) ? sm.d[tid].tau : 0xFFFFFFFFu;
+        }
+        __syncthreads();
         if (!sm.abort) {
-            unsigned long long mine[32];
+            for (int c0 = cq; c0 < cq + 16; c0 += 8) {
+                unsigned long long mine[8];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) mine[i] = 0ull;
-            for (int j = 0; j < ntl; ++j) {
-                uint32_t zr[32];
-                tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(j * kNG + h * 32), zr);
-                tmem_wait_ld();
-                const int v = (t0 + j) * kTileV + q * 32 + lane;
-                if (v >= V) continue;
+                for (int i = 0; i < 8; ++i) mine[i] = 0ull;
+                for (int j = 0; j < ntl; ++j) {
+                    const int vt = (t0 + j) * kTileV;        // first token of the tile
+                    // zeros: lane l takes rows 32q + 4 (l % 8) .. + 3 of requests c0 + l / 8 and c0 + 4 + l / 8
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int c = h * 32 + i;
-                    const Desc& d = sm.d[c];
-                    if (!(d.flags & (kDescDrawn | kDescPrefix))) continue;
-                    const float z = __uint_as_float(zr[i]);
-                    const bool in = rp::in_set(ordered_key(z), v, d.tau, d.cut);
-                    const float wv = in ? rp::weight_f(z, sm.zmax[c], sm.inv_t[c]) : 0.0f;
-                    const int b = g * kNG + c;
-                    __stcs(p.q + (static_cast<int64_t>(b) * p.gamma + (k - 1)) * V + v, wv * inv_mass(d.mass));
-                    if (d.flags & kDescPrefix) mine[i] += in ? rp::to_fixed(wv) : 0ull;
+                    for (int half = 0; half < 2; ++half) {
+                        const int c = c0 + half * 4 + (lane >> 3);
+                        const int v4 = vt + q * 32 + 4 * (lane & 7);
+                        const uint32_t fl = sm.d[c].flags;
+                        if ((fl & (kDescDrawn | kDescPrefix)) && sm.smax[j][c] < sm.floor_key[c] && v4 < V)
+                            __stcs(reinterpret_cast<float4*>(p.q + (static_cast<int64_t>(g * kNG + c) * p.gamma + (k - 1)) * V + v4),
+                                   make_float4(0.0f, 0.0f, 0.0f, 0.0f));
+                    }
+                    if (!any_active8(sm.smax[j], sm.floor_key, c0)) continue;
+                    uint32_t zr[8];
+                    tmem_ld8(tq + static_cast<uint32_t>(j * kNG + c0), zr);
+                    tmem_wait_ld();
+                    const int v = vt + q * 32 + lane;
+                    if (v >= V) continue;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int c = c0 + i;
+                        if (sm.smax[j][c] < sm.floor_key[c]) continue;
+                        const uint32_t fl = sm.d[c].flags;
+                        const float z = __uint_as_float(zr[i]);
+                        const bool in = rp::in_set(ordered_key(z), v, sm.d[c].tau, sm.d[c].cut);
+                        const float wv = in ? rp::weight_f(z, sm.zmax[c], sm.inv_t[c]) : 0.0f;
+                        __stcs(p.q + (static_cast<int64_t>(g * kNG + c) * p.gamma + (k - 1)) * V + v, wv * sm.inv_s[c]);
+                        if (fl & kDescPrefix) mine[i] += in ? rp::to_fixed(wv) : 0ull;
+                    }
                 }
-            }
-            if (sm.any_prefix) {
+                if (sm.any_prefix) {
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    unsigned long long s = mine[i];
+                    for (int i = 0; i < 8; ++i) {
+                        unsigned long long s = mine[i];
 #pragma unroll
-                    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, o);
-                    if (lane == 0) sm.wpart[q][h * 32 + i] = s;
+                        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, o);
+                        if (lane == 0) sm.wpart[q][c0 + i] = s;
+                    }
                 }
             }
         }
@@ -899,9 +1176,10 @@ __global__ void __launch_bounds__(kFT, 1)
     // what was issued.
     if (tid == 0 && sm.abort) {
         for (int n = max(0, w_issued - S); n < w_issued; ++n) mbar_wait(&sm.wfull[n % S], (n / S) & 1, kWaitLimitNs);
-        for (int n = max(0, b_issued - S); n < b_issued; ++n) mbar_wait(&sm.bfull[n % S], (n / S) & 1, kWaitLimitNs);
         if (mma_done > 0) mbar_wait(&sm.wempty[(mma_done - 1) % S], ((mma_done - 1) / S) & 1, kWaitLimitNs);
     }
+    if (tid == 32 && sm.abort)
+        for (int n = max(0, b_issued - S); n < b_issued; ++n) mbar_wait(&sm.bfull[n % S], (n / S) & 1, kWaitLimitNs);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();

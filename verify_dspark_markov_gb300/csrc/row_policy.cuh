@@ -31,6 +31,16 @@
 
 #include "common.cuh"
 
+// Barriers of the engine: the CTA's threads and the cluster.  A kernel that
+// runs the engine on part of a larger CTA (as a cluster of one) defines both
+// as a named barrier of kThreads threads before including this header.
+#ifndef RP_SYNC
+#define RP_SYNC() __syncthreads()
+#endif
+#ifndef RP_CL_SYNC
+#define RP_CL_SYNC(cl) (cl).sync()
+#endif
+
 namespace dspark {
 namespace rp {
 
@@ -137,31 +147,31 @@ __device__ __forceinline__ void cluster_sum_u64(Smem& sm, cg::cluster_group& cl,
         for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xFFFFFFFFu, x, o);
         if (lane == 0) sm.wu[warp][i] = x;
     }
-    __syncthreads();
+    RP_SYNC();
     const int buf = sm.parity;
     if (threadIdx.x < kN) {
         unsigned long long t = 0;
         for (int w = 0; w < kWarps; ++w) t += sm.wu[w][threadIdx.x];
         sm.xu[buf][threadIdx.x] = t;
     }
-    cl.sync();
+    RP_CL_SYNC(cl);
     // one remote load per (rank, value) pair, then one combination per value
     if (threadIdx.x < nc * kN) {
         const int r = threadIdx.x / kN, i = threadIdx.x % kN;
         sm.gat[r][i] = cl.map_shared_rank(&sm.xu[buf][0], r)[i];
     }
-    __syncthreads();
+    RP_SYNC();
     if (threadIdx.x < kN) {
         unsigned long long t = 0;
         for (int r = 0; r < nc; ++r) t += sm.gat[r][threadIdx.x];
         sm.tot[threadIdx.x] = t;
     }
-    __syncthreads();
+    RP_SYNC();
 #pragma unroll
     for (int i = 0; i < kN; ++i) out[i] = sm.tot[i];
-    __syncthreads();
+    RP_SYNC();
     if (threadIdx.x == 0) sm.parity ^= 1;
-    __syncthreads();
+    RP_SYNC();
 }
 
 // Block-max then cluster-max of one uint64 (and OR of a flag word).
@@ -180,7 +190,7 @@ __device__ __forceinline__ void cluster_max_u64(Smem& sm, cg::cluster_group& cl,
         sm.wu[warp][0] = v;
         sm.wu[warp][1] = flags;
     }
-    __syncthreads();
+    RP_SYNC();
     const int buf = sm.parity;
     if (threadIdx.x == 0) {
         unsigned long long m = 0, f = 0;
@@ -191,12 +201,12 @@ __device__ __forceinline__ void cluster_max_u64(Smem& sm, cg::cluster_group& cl,
         sm.xu[buf][0] = m;
         sm.xu[buf][1] = f;
     }
-    cl.sync();
+    RP_CL_SYNC(cl);
     if (threadIdx.x < 2 * nc) {
         const int r = threadIdx.x >> 1, i = threadIdx.x & 1;
         sm.gat[r][i] = cl.map_shared_rank(&sm.xu[buf][0], r)[i];
     }
-    __syncthreads();
+    RP_SYNC();
     if (threadIdx.x == 0) {
         unsigned long long m = 0, f = 0;
         for (int r = 0; r < nc; ++r) {
@@ -206,12 +216,12 @@ __device__ __forceinline__ void cluster_max_u64(Smem& sm, cg::cluster_group& cl,
         sm.tot[0] = m;
         sm.tot[1] = f;
     }
-    __syncthreads();
+    RP_SYNC();
     out_max = sm.tot[0];
     out_flags = sm.tot[1];
-    __syncthreads();
+    RP_SYNC();
     if (threadIdx.x == 0) sm.parity ^= 1;
-    __syncthreads();
+    RP_SYNC();
 }
 
 // Gather one uint64 per CTA (thread 0's `mine`) from every CTA of the
@@ -221,11 +231,11 @@ __device__ __forceinline__ void cluster_gather_u64(Smem& sm, cg::cluster_group& 
     const int nc = static_cast<int>(cl.num_blocks());  // CTAs in the cluster
     const int buf = sm.parity;
     if (threadIdx.x == 0) sm.xu[buf][0] = mine;
-    cl.sync();
+    RP_CL_SYNC(cl);
     if (threadIdx.x < nc) sm.gat[threadIdx.x][0] = cl.map_shared_rank(&sm.xu[buf][0], threadIdx.x)[0];
-    __syncthreads();
+    RP_SYNC();
     if (threadIdx.x == 0) sm.parity ^= 1;
-    __syncthreads();
+    RP_SYNC();
 }
 
 // Inclusive block scan of one uint64 per thread.
@@ -237,10 +247,10 @@ __device__ __forceinline__ unsigned long long block_scan_u64(Smem& sm, unsigned 
         if (lane >= o) x += y;
     }
     if (lane == 31) sm.scan_u[warp] = x;
-    __syncthreads();
+    RP_SYNC();
     unsigned long long base = 0;
     for (int w = 0; w < warp; ++w) base += sm.scan_u[w];
-    __syncthreads();
+    RP_SYNC();
     return x + base;
 }
 
@@ -413,7 +423,7 @@ __device__ bool radix_select(Smem& sm, cg::cluster_group& cl, const Slice& sl, u
             wcnt[i] = 0u;
             if (kMass) wbuf[i] = 0ull;
         }
-        __syncthreads();
+        RP_SYNC();
         const uint32_t pre = prefix;
         const int hb = hi_bit;
         for_each_elem(sl, [&](float z, int32_t idx) {
@@ -423,7 +433,7 @@ __device__ bool radix_select(Smem& sm, cg::cluster_group& cl, const Slice& sl, u
             atomicAdd(&wc[d], 1u);
             if (kMass) atomicAdd(&wm[d], static_cast<unsigned long long>(to_fixed(weight_f(z, zmax, inv_t))));
         });
-        __syncthreads();
+        RP_SYNC();
         {  // the CTA's histogram: bin tid over the warps' copies
             uint32_t c = 0;
             unsigned long long m = 0;
@@ -434,7 +444,7 @@ __device__ bool radix_select(Smem& sm, cg::cluster_group& cl, const Slice& sl, u
             sm.hcnt[buf][tid] = c;
             if (kMass) sm.hmass[buf][tid] = m;
         }
-        cl.sync();
+        RP_CL_SYNC(cl);
         // thread t takes bin (nbins - 1 - t): descending key order
         const int nbins = 1 << nb;
         const int b = nbins - 1 - tid;
@@ -455,7 +465,7 @@ __device__ bool radix_select(Smem& sm, cg::cluster_group& cl, const Slice& sl, u
             reinterpret_cast<unsigned long long*>(&sm.wu[0][0])[0] = c;
             reinterpret_cast<unsigned long long*>(&sm.wu[0][1])[0] = m;
         }
-        __syncthreads();
+        RP_SYNC();
         if (!sm.pick[1]) found = false;
         const int pb = sm.pick[1] ? sm.pick[0] : 0;
         above += sm.pick[1] ? sm.scan_u[0] : 0ull;
@@ -463,9 +473,9 @@ __device__ bool radix_select(Smem& sm, cg::cluster_group& cl, const Slice& sl, u
         eq_mass = sm.wu[0][1];
         prefix = (prefix << nb) | static_cast<uint32_t>(pb);
         hi_bit = lo_bit;
-        __syncthreads();
+        RP_SYNC();
         if (tid == 0) sm.hparity ^= 1;
-        __syncthreads();
+        RP_SYNC();
     }
     tau = full_key(prefix);
     return found;
@@ -490,7 +500,7 @@ __device__ int32_t tie_index(Smem& sm, cg::cluster_group& cl, const Slice& sl, u
     const unsigned long long incl = block_scan_u64(sm, mine);
     __shared__ unsigned long long s_total;
     if (tid == kThreads - 1) s_total = incl;
-    __syncthreads();
+    RP_SYNC();
     cluster_gather_u64(sm, cl, s_total);
     const auto totals = [&sm](int r) { return sm.gat[r][0]; };  // per rank
     unsigned long long before = 0;
@@ -501,7 +511,7 @@ __device__ int32_t tie_index(Smem& sm, cg::cluster_group& cl, const Slice& sl, u
     }
     const int buf = sm.parity;
     if (rank == owner && tid == 0) sm.xu[buf][0] = static_cast<unsigned long long>(sl.lo + max(sl.n - 1, 0));
-    __syncthreads();
+    RP_SYNC();
     if (rank == owner) {
         const unsigned long long want = t - before;
         if (incl >= want && incl - mine < want) {
@@ -516,13 +526,13 @@ __device__ int32_t tie_index(Smem& sm, cg::cluster_group& cl, const Slice& sl, u
             });
         }
     }
-    cl.sync();
+    RP_CL_SYNC(cl);
     if (tid == 0) sm.tot[0] = cl.map_shared_rank(&sm.xu[buf][0], owner)[0];
-    __syncthreads();
+    RP_SYNC();
     const int32_t idx = static_cast<int32_t>(sm.tot[0]);
-    __syncthreads();
+    RP_SYNC();
     if (tid == 0) sm.parity ^= 1;
-    __syncthreads();
+    RP_SYNC();
     return idx;
 }
 
@@ -650,7 +660,7 @@ __device__ int32_t sample_fixed(Smem& sm, cg::cluster_group& cl, const Slice& sl
     const unsigned long long incl = block_scan_u64(sm, mine);
     __shared__ unsigned long long s_total;
     if (tid == kThreads - 1) s_total = incl;
-    __syncthreads();
+    RP_SYNC();
     cluster_gather_u64(sm, cl, s_total);
     const auto totals = [&sm](int r) { return sm.gat[r][0]; };  // per rank
     unsigned long long total = 0;
@@ -667,7 +677,7 @@ __device__ int32_t sample_fixed(Smem& sm, cg::cluster_group& cl, const Slice& sl
     }
     const int buf = sm.parity;
     if (rank == owner && tid == 0) sm.xu[buf][0] = static_cast<unsigned long long>(sl.lo + max(sl.n - 1, 0));
-    __syncthreads();
+    RP_SYNC();
     if (rank == owner) {
         const unsigned long long tl = target - before;  // within this CTA: first prefix > tl
         if (incl > tl && incl - mine <= tl) {
@@ -687,13 +697,13 @@ __device__ int32_t sample_fixed(Smem& sm, cg::cluster_group& cl, const Slice& sl
             }
         }
     }
-    cl.sync();
+    RP_CL_SYNC(cl);
     if (tid == 0) sm.tot[0] = cl.map_shared_rank(&sm.xu[buf][0], owner)[0];
-    __syncthreads();
+    RP_SYNC();
     const int32_t idx = static_cast<int32_t>(sm.tot[0]);
-    __syncthreads();
+    RP_SYNC();
     if (tid == 0) sm.parity ^= 1;
-    __syncthreads();
+    RP_SYNC();
     return idx;
 }
 
@@ -769,7 +779,7 @@ static __device__ void sort_desc(unsigned long long* buf, int n) {
     int P = 1;
     while (P < n) P <<= 1;
     for (int i = n + threadIdx.x; i < P; i += kThreads) buf[i] = 0ull;
-    __syncthreads();
+    RP_SYNC();
     const int half = P >> 1;
     for (int k = 2; k <= P; k <<= 1) {
         for (int j = k >> 1; j > 0; j >>= 1) {
@@ -782,7 +792,7 @@ static __device__ void sort_desc(unsigned long long* buf, int n) {
                     buf[ixj] = a;
                 }
             }
-            __syncthreads();
+            RP_SYNC();
         }
     }
 }
@@ -803,9 +813,9 @@ static __device__ void sort_candidates(unsigned long long* buf, int n) {
         c = buf[t];
         for (int j = 0; j < n; ++j) r += buf[j] > c ? 1 : 0;
     }
-    __syncthreads();
+    RP_SYNC();
     if (t < n) buf[r] = c;
-    __syncthreads();
+    RP_SYNC();
 }
 
 // Compact the elements of the slice for which pick(z, index) holds into rank
@@ -862,7 +872,7 @@ __device__ void compact_candidates(Smem& sm, cg::cluster_group& cl, const Slice&
         }
       }
     }
-    cl.sync();
+    RP_CL_SYNC(cl);
 }
 
 // First position i in [0, n) whose inclusive prefix of w(i) satisfies
@@ -881,7 +891,7 @@ __device__ int find_crossing(Smem& sm, int n, unsigned long long th, bool strict
     __shared__ int s_pos;
     if (threadIdx.x == kThreads - 1) s_tot = incl;
     if (threadIdx.x == 0) s_pos = n;
-    __syncthreads();
+    RP_SYNC();
     const unsigned long long before = incl - mine;
     const bool here = strict ? (incl > th && before <= th) : (incl >= th && before < th);
     if (here && mine > 0) {
@@ -894,10 +904,10 @@ __device__ int find_crossing(Smem& sm, int n, unsigned long long th, bool strict
             }
         }
     }
-    __syncthreads();
+    RP_SYNC();
     total = s_tot;
     const int pos = s_pos;
-    __syncthreads();
+    RP_SYNC();
     return pos;
 }
 
@@ -921,7 +931,7 @@ __device__ void cut_scan(Smem& sm, int K, Wf wt, Th thresh, unsigned long long& 
         s_pos = K;
         s_pm = 0ull;
     }
-    __syncthreads();
+    RP_SYNC();
     total = s_tot;
     const unsigned long long th = thresh(total);
     const unsigned long long before = incl - mine;
@@ -936,10 +946,10 @@ __device__ void cut_scan(Smem& sm, int K, Wf wt, Th thresh, unsigned long long& 
             }
         }
     }
-    __syncthreads();
+    RP_SYNC();
     pos = s_pos;
     prefix = s_pm;
-    __syncthreads();
+    RP_SYNC();
 }
 
 // ceil(p * kept) clamped to [1, kept] (kept = 0 gives 0): the fixed-point
@@ -1078,12 +1088,12 @@ static __device__ void row_policy(Smem& sm, cg::cluster_group& cl, const Slice& 
             if (with_mass) cbuf[i] = 0ull;
             wcnt[i] = 0u;
         }
-        __syncthreads();
+        RP_SYNC();
     }
     if (!trunc) tmass = hist_pass<0>(sl, zmax, inv_t, whc, whp);
     else if (with_mass) hist_pass<2>(sl, zmax, inv_t, whc, whp);
     else hist_pass<1>(sl, zmax, inv_t, whc, whp);
-    __syncthreads();
+    RP_SYNC();
     uint32_t* hc = sm.hcnt[1];
     unsigned long long* hp = sm.hmass[1];
     __shared__ unsigned long long s_ctot;  // this CTA's total mass (no truncation)
@@ -1101,14 +1111,14 @@ static __device__ void row_policy(Smem& sm, cg::cluster_group& cl, const Slice& 
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) tmass += __shfl_xor_sync(0xFFFFFFFFu, tmass, o);
         if (lane == 0) sm.wu[warp_id][0] = tmass;
-        __syncthreads();
+        RP_SYNC();
         if (tid == 0) {
             unsigned long long t = 0;
             for (int w = 0; w < kWarps; ++w) t += sm.wu[w][0];
             s_ctot = t;
         }
     }
-    cl.sync();
+    RP_CL_SYNC(cl);
     if (!trunc) {  // the whole vocabulary
         unsigned long long total = 0;
 #pragma unroll
@@ -1131,7 +1141,7 @@ static __device__ void row_policy(Smem& sm, cg::cluster_group& cl, const Slice& 
     const unsigned long long cm = with_mass ? block_scan_u64(sm, m) : 0ull;
     s_cc[tid] = static_cast<uint32_t>(cc);
     s_cm[tid] = cm;
-    __syncthreads();
+    RP_SYNC();
     const unsigned long long n_in = s_cc[kBins - 1], total_mass = s_cm[kBins - 1];
     // top-k past s = 32 takes every token in range: the others weigh 0
     const unsigned long long k_eff = use_k ? min(static_cast<unsigned long long>(pol.top_k), n_in) : 0ull;
@@ -1177,11 +1187,11 @@ static __device__ void row_policy(Smem& sm, cg::cluster_group& cl, const Slice& 
         s_pl[4] = gc;
         s_pl[5] = phi < whi ? s_cm[whi - 1] - s_cm[phi] : 0ull;
     }
-    __syncthreads();
+    RP_SYNC();
     const int wlo = s_win[0], whi = s_win[1], phi = s_win[2];
     const unsigned long long above_cnt = s_pl[0], above_mass = s_pl[1], wcount = s_pl[2], theta_p = s_pl[3];
     const unsigned long long gap_cnt = s_pl[4], gap_mass = s_pl[5];
-    __syncthreads();
+    RP_SYNC();
 
     if (wcount > static_cast<unsigned long long>(kCap)) {
         const uint32_t klo = lowest_true_key(kmax, BinAtMost{zmax, inv_t, whi});  // the window's lowest key
@@ -1262,17 +1272,17 @@ static __device__ void row_policy(Smem& sm, cg::cluster_group& cl, const Slice& 
             sm.xu[buf][3] = above_cnt + static_cast<unsigned long long>(mm);
         }
     }
-    cl.sync();
+    RP_CL_SYNC(cl);
     if (tid < 4) sm.tot[tid] = cl.map_shared_rank(&sm.xu[buf][0], 0)[tid];
-    __syncthreads();
+    RP_SYNC();
     res.tau = static_cast<uint32_t>(sm.tot[0]);
     res.cut = static_cast<int32_t>(static_cast<uint32_t>(sm.tot[1]));
     res.mass = sm.tot[2];
     res.count = static_cast<int32_t>(min(sm.tot[3], 0x7FFFFFFFull));
     res.in_buf = above_cnt == 0;
-    __syncthreads();
+    RP_SYNC();
     if (tid == 0) sm.parity ^= 1;
-    __syncthreads();
+    RP_SYNC();
 }
 
 // Inverse-CDF draw over a support held in rank 0's candidate buffer (its
@@ -1303,7 +1313,7 @@ __device__ int32_t draw_small_support(Smem& sm, unsigned long long* cbuf, int n,
         __shared__ int32_t s_pick;
         if (t == kThreads - 1) s_tot = incl;
         if (t == 0) s_pick = -1;
-        __syncthreads();
+        RP_SYNC();
         total = s_tot;
         if (total == 0) return -1;
         const unsigned long long target =
@@ -1313,16 +1323,16 @@ __device__ int32_t draw_small_support(Smem& sm, unsigned long long* cbuf, int n,
             for (int j = 0; j < n; ++j) before += ibuf[j] < idx ? wbuf[j] : 0ull;
             if (before <= target && target < before + wt) s_pick = idx;
         }
-        __syncthreads();
+        RP_SYNC();
         const int32_t pick = s_pick;
-        __syncthreads();
+        RP_SYNC();
         return pick;
     }
     for (int i = threadIdx.x; i < n; i += kThreads) {
         const unsigned long long c = cbuf[i];
         cbuf[i] = index_order(vo_key(c), vo_idx(c));
     }
-    __syncthreads();
+    RP_SYNC();
     sort_desc(cbuf, n);
     auto wi = [&](int i) -> unsigned long long { return w(io_key(cbuf[i]), io_idx(cbuf[i])); };
     unsigned long long tot;
@@ -1334,12 +1344,12 @@ __device__ int32_t draw_small_support(Smem& sm, unsigned long long* cbuf, int n,
     unsigned long long t2;
     const int pos = find_crossing(sm, n, target, true, wi, t2);
     const int32_t pick = pos < n ? io_idx(cbuf[pos]) : io_idx(cbuf[n - 1]);
-    __syncthreads();
+    RP_SYNC();
     for (int i = threadIdx.x; i < n; i += kThreads) {  // back to value order keys
         const unsigned long long c = cbuf[i];
         cbuf[i] = value_order(io_key(c), io_idx(c));
     }
-    __syncthreads();
+    RP_SYNC();
     return pick;
 }
 
