@@ -79,6 +79,7 @@ constexpr int kHB = 16;              // histogram bins: s in [2i, 2i + 2), s < 3
 constexpr int kCand = rp::kCap;      // candidates a list holds (the owner sorts them in shared memory)
 constexpr int kWhole = rp::kThreads; // a support this small is compacted whole (drawn by its owner)
 constexpr uint32_t kTmemCols = 512;
+constexpr int kCountBins = 8;        // counts-only rows count the first 8 coarse bins (s < 16)
 
 // request modes
 enum : int { kModeNone = 0, kModeGreedy = 1, kModeWin = 2, kModeAll = 3, kModeHard = 4, kModeRefine = 5 };
@@ -302,11 +303,11 @@ __device__ Win make_window(const rp::Policy& pol, const unsigned long long* cc, 
     w.wcount = at(cc, whi) - ac - gc;
     w.gap_cnt = gc;
     w.gap_mass = phi < whi ? at(cm, whi - 1) - at(cm, phi) : 0ull;
-    if (NB == kHB && !with_mass && cc[kHB / 2 - 1] < static_cast<unsigned long long>(pol.top_k)) {
-        // counts only: the top-k crossing lies past s = 16, where tokens were
-        // not counted: refine s in [16, 32), keep the bins before
+    if (NB == kHB && !with_mass && cc[kCountBins - 1] < static_cast<unsigned long long>(pol.top_k)) {
+        // counts only: the top-k crossing lies past the counted bins: refine
+        // the rest of s < 32, keep the bins before
         w.mode = kModeRefine;
-        w.rlo = kHB / 2;
+        w.rlo = kCountBins;
         w.rhi = kHB - 1;
         w.fscale = 16.0f / static_cast<float>(w.rhi - w.rlo + 1);
         return w;
@@ -314,8 +315,6 @@ __device__ Win make_window(const rp::Policy& pol, const unsigned long long* cc, 
         w.mode = kModeWin;
     } else {
         // too many tokens: refine the window's coarse bins into 16 finer ones
-        // (counts-only rows keep exact counts below s = 16 only: a top-k
-        // crossing past that goes to the row engine).
         // Counts only (top-k <= kWhole): the bins before the top-k bin hold
         // fewer than k tokens; refine the top-k bin and keep them whole.
         w.mode = kModeRefine;
@@ -386,19 +385,22 @@ __global__ void __launch_bounds__(kFT, 1)
     const int steps_total = p.groups * p.gamma;
     auto tile_of = [&](int n) { return n % max(ntl, 1); };         // n-th tile of the whole launch
     auto step_of = [&](int n) { return n / max(ntl, 1); };         // its (group, step) index
+    // W is read again every step: keep it in L2; the backbone streams through
+    const uint64_t pol_keep = l2_policy_evict_last(), pol_stream = l2_policy_evict_first();
     auto issue_w = [&](int n) {
         const int s = n % S;
         mbar_arrive_expect_tx(&sm.wfull[s], w_bytes);
         uint8_t* dst = sW + s * w_bytes;
         const int t = t0 + tile_of(n);
-        for (int kb = 0; kb < r / 64; ++kb) tma_load_2d(dst + kb * kTileV * 128, &wmap, kb * 64, t * kTileV, &sm.wfull[s]);
+        for (int kb = 0; kb < r / 64; ++kb)
+            tma_load_2d_hint(dst + kb * kTileV * 128, &wmap, kb * 64, t * kTileV, &sm.wfull[s], pol_keep);
     };
     auto issue_b = [&](int n) {
         const int s = n % S;
         const int gs = step_of(n), g = gs / p.gamma, k = gs % p.gamma;  // k 0-based
         mbar_arrive_expect_tx(&sm.bfull[s], b_bytes);
         const int t = t0 + tile_of(n);
-        tma_load_3d(sB + s * b_bytes, &bmap, t * kTileV, k, g * kNG, &sm.bfull[s]);
+        tma_load_3d_hint(sB + s * b_bytes, &bmap, t * kTileV, k, g * kNG, &sm.bfull[s], pol_stream);
     };
     const int total_tiles = steps_total * ntl;
     if (tid == 0)
@@ -596,7 +598,7 @@ __global__ void __launch_bounds__(kFT, 1)
             // rows s < 16, other sampled rows s < 32
             sm.floor_key[tid] = hist == kHistNone ? 0xFFFFFFFFu
                               : hist == kHistGreedy ? ordered_key(zm)
-                              : floor_key_s(zm, it, hist == kHistCount ? 16.0f : 32.0f);
+                              : floor_key_s(zm, it, hist == kHistCount ? 2.0f * kCountBins : 32.0f);
         }
         for (int i = tid; i < kNG * kHB; i += kFT) {
             (&hcnt[0][0])[i] = 0u;
@@ -617,8 +619,8 @@ __global__ void __launch_bounds__(kFT, 1)
         __syncthreads();
         if (!sm.abort) {
             for (int c0 = cq; c0 < cq + 16; c0 += 8) {
-                // counts-only rows count s < 16 only (a top-k crossing past it
-                // is refined over [16, 32) in phase C)
+                // counts-only rows count s < 2 kCountBins only (a top-k
+                // crossing past it is refined over the rest in phase C)
                 int hmr[8];
                 float zmr[8], bar_[8], bbr[8], itr[8];
                 uint32_t flr[8];
@@ -640,19 +642,20 @@ __global__ void __launch_bounds__(kFT, 1)
                     tmem_ld8(tq + static_cast<uint32_t>(j * kNG + c0), zr);
                     tmem_wait_ld();
                     const int v = (t0 + j) * kTileV + q * 32 + lane;
-                    if (v >= V) continue;  // (greedy rows' warp reduction below needs every lane: handled there)
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
                         const int hm = hmr[i];
                         if (hm <= kHistGreedy || !((act >> i) & 1u)) continue;
                         const float z = __uint_as_float(zr[i]);
-                        const float bf = bin_val(z, bar_[i], bbr[i]);
-                        if (bf >= (hm == kHistCount ? 8.0f : 16.0f)) continue;
-                        const int bin = min(kHB - 1, static_cast<int>(bf));
-                        atomicAdd(&hcnt[c0 + i][bin], 1u);
-                        if (hm == kHistMass)
+                        const float bf = v < V ? bin_val(z, bar_[i], bbr[i]) : 16.0f;
+                        if (hm == kHistCount) {
+                            if (bf < static_cast<float>(kCountBins)) atomicAdd(&hcnt[c0 + i][static_cast<int>(bf)], 1u);
+                        } else if (bf < 16.0f) {
+                            const int bin = min(kHB - 1, static_cast<int>(bf));
+                            atomicAdd(&hcnt[c0 + i][bin], 1u);
                             atomicAdd(&hmass[c0 + i][bin],
                                       static_cast<unsigned long long>(rp::to_fixed(rp::weight_f(z, zmr[i], itr[i]))));
+                        }
                     }
                 }
                 // greedy rows: the lowest index holding the maximum
@@ -718,15 +721,20 @@ __global__ void __launch_bounds__(kFT, 1)
         }
         __syncthreads();
         if (sm.any_refine) {
-            // ---- C2: a 16-bin histogram of 1/8 steps inside each refined row's bin
+            // ---- C2: a 16-bin histogram inside each refined row's coarse bins
             for (int i = tid; i < kNG * kHB; i += kFT) {
                 (&hcnt[0][0])[i] = 0u;
                 (&hmass[0][0])[i] = 0ull;
             }
+            if (tid < kNG)
+                sm.floor_key[tid] = sm.win[tid].mode == kModeRefine
+                                        ? floor_key_s(sm.zmax[tid], sm.inv_t[tid], 2.0f * static_cast<float>(sm.win[tid].rhi + 1))
+                                        : 0xFFFFFFFFu;
             __syncthreads();
             if (!sm.abort) {
                 for (int c0 = cq; c0 < cq + 16; c0 += 8) {
                     for (int j = 0; j < ntl; ++j) {
+                        if (!any_active8(sm.smax[j], sm.floor_key, c0)) continue;
                         uint32_t zr[8];
                         tmem_ld8(tq + static_cast<uint32_t>(j * kNG + c0), zr);
                         tmem_wait_ld();
@@ -735,7 +743,7 @@ __global__ void __launch_bounds__(kFT, 1)
 #pragma unroll
                         for (int i = 0; i < 8; ++i) {
                             const int c = c0 + i;
-                            if (sm.win[c].mode != kModeRefine) continue;
+                            if (sm.win[c].mode != kModeRefine || sm.smax[j][c] < sm.floor_key[c]) continue;
                             const float z = __uint_as_float(zr[i]);
                             const float zm = sm.zmax[c], it = sm.inv_t[c];
                             const float bf = bin_val(z, sm.ba[c], sm.bb[c]);
@@ -821,9 +829,11 @@ __global__ void __launch_bounds__(kFT, 1)
         // ------------------------------------------------ D: compaction (and hard rows' z)
         if (tid < kNG) {
             const Win& w = sm.win[tid];
+            // picked tokens have bf = s / 2 below the window's last bin's end
+            const float bf_end = w.lvl == 1 ? static_cast<float>(w.whi + 1)
+                                            : static_cast<float>(w.rlo) + static_cast<float>(w.whi + 1) / w.fscale;
             sm.floor_key[tid] = w.mode == kModeHard ? 0u
-                              : w.mode == kModeWin ? floor_key_s(sm.zmax[tid], sm.inv_t[tid],
-                                                                 2.0f * static_cast<float>((w.lvl == 1 ? w.whi : w.rhi) + 1))
+                              : w.mode == kModeWin ? floor_key_s(sm.zmax[tid], sm.inv_t[tid], 2.0f * bf_end)
                                                    : 0xFFFFFFFFu;
         }
         __syncthreads();
