@@ -127,7 +127,8 @@ size_t dspark_workspace_size(int op, int B, int gamma, int V, int r, int H) {
         case DSPARK_OP_MARKOV_SAMPLE:
             // the larger of the two paths' needs (which one runs depends on the device)
             return std::max(markov_layout(B, gamma, V, r).total,
-                            r >= 64 && r % 64 == 0 ? markov_fused_workspace(B, gamma, V) : size_t(0));
+                            r >= 64 && r % 64 == 0 && B <= kFusedMaxBatch ? markov_fused_workspace(B, gamma, V)
+                                                                           : size_t(0));
         case DSPARK_OP_VERIFY: return verify_layout(B, gamma).total;
         case DSPARK_OP_ACCEPT_STATS: return stats_workspace(B, gamma);
         case DSPARK_OP_RNN_SAMPLE: return r >= 16 ? rnn_layout(B, V, r).total : 0;

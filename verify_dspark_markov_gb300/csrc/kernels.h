@@ -140,7 +140,10 @@ cudaError_t launch_markov_bias(const MarkovGemmParams& p, const MarkovGemmPlan& 
 // The whole draft (every step's bias GEMM, policy and draw) in one persistent
 // launch with the biased logits in tensor memory (markov_fused.cu): bf16
 // backbone, r a multiple of 64 up to 256, a vocabulary of at most 8 tiles of
-// 128 per SM.
+// 128 per SM, and one group of at most kFusedMaxBatch requests (the kernel
+// runs larger batches as groups one after another, which the per-step path
+// beats: 3.1 against 1.2 ms at 256 requests, 129,280 tokens, r = 256).
+constexpr int kFusedMaxBatch = 64;
 struct MarkovFusedArgs {
     const uint16_t* backbone;  // bf16 [B, gamma, V]
     const uint16_t* U;         // bf16 [V, r]

@@ -1261,7 +1261,7 @@ FusedLayout fused_layout(int B, int gamma, int V) {
 
 bool markov_fused_supported(int dtype, int B, int V, int r) {
     FusedShape f;
-    return dtype == kBF16 && fused_shape(B, V, r, f) && f.grid <= 1024;
+    return dtype == kBF16 && B <= kFusedMaxBatch && fused_shape(B, V, r, f) && f.grid <= 1024;
 }
 
 size_t markov_fused_workspace(int B, int gamma, int V) { return fused_layout(B, gamma, V).total; }
