@@ -659,11 +659,22 @@ def run_gpu(args):
     flops = wl.flops()
     dom = max(part_ms, key=part_ms.get)
     achieved = nbytes[dom] / (part_ms[dom] * 1e-3) / 1e9
+    fused = False
+    if isinstance(wl, Serving) and wl.gru is None:
+        w = wl.w
+        n_draft = ds.markov_launches(ds.BF16, w.B, w.gamma, w.V, w.weights.r, policy=not wl.greedy_only,
+                                     conf=w.h is not None)
+        fused = w.weights.r > 0 and n_draft == 1 + (1 if w.h is not None else 0)
+    draft_kernel = ("markov_fused_kernel (bias GEMM, policy and draw of every position in one launch) + "
+                    "confidence_kernel" if fused else
+                    "rnn_sample (gru_step_kernel, the hi and lo markov_bias_kernel products and "
+                    "markov_step_kernel per position)" if isinstance(wl, Serving) and wl.gru is not None else
+                    "markov_sample (markov_bias_kernel + markov_step_kernel per position)")
     kernel = {"full_decode_tile": "argmax_rows_kernel<bf16> (draft + verify launches)",
               "training_stats": "stats_pairs_kernel<f32> (+ stats_blocks_kernel, stats_total_kernel)",
               "training_stats_grad": "stats_grad_kernel<f32>",
               "sts_fit": "sts_pass_kernel (+ sts_update_kernel per pass)"}.get(
-                  wl.name, {"draft": "markov_sample (markov_bias_kernel + markov_step_kernel per position)",
+                  wl.name, {"draft": draft_kernel,
                             "verify": "verify_rows_kernel<bf16>" if getattr(wl, "width", None) is None
                             else "verify_rows_kernel<bf16, width>"}.get(dom, dom))
     if wl.name == "full_decode_tile":  # the same kernel serves both parts: average over both launches
@@ -696,7 +707,8 @@ def run_gpu(args):
     }
     if flops.get("draft"):
         t = flops["draft"] / (part_ms["draft"] * 1e-3) / 1e12
-        result["tensor"] = {"part": "draft (markov_bias_kernel, tcgen05)", "achieved": t,
+        result["tensor"] = {"part": "draft (markov_fused_kernel, tcgen05)" if fused else
+                            "draft (markov_bias_kernel, tcgen05)", "achieved": t,
                             "peak": tflops_peak, "unit": "TFLOP/s", "frac": t / tflops_peak,
                             "note": "FLOPs of the bias GEMM over the whole draft part's time"}
     if isinstance(wl, Serving):
@@ -705,8 +717,8 @@ def run_gpu(args):
             launches = 2
         elif wl.gru is not None:  # GRU step, the hi and lo products, the policy step; confidence; verify
             launches = 4 * g + (1 if wl.w.h is not None else 0) + 1
-        else:
-            launches = (2 * g if wl.w.weights.r else g) + (1 if wl.w.h is not None else 0) + 1
+        else:  # the library's own count for the draft, then the verify
+            launches = n_draft + 1
     elif isinstance(wl, StsFit):  # init, then 64 passes and their updates (late passes return at once)
         launches = 1 + 2 * 64
     else:  # the statistics: pairs + per-block + total kernels; the gradient: one kernel

@@ -181,8 +181,12 @@ size_t dspark_workspace_size(int op, int B, int gamma, int V, int r, int H);
  *   conf      fp32 [B, gamma] out (when h != NULL): c_k.
  *   status    int32 [B] out: dspark_request_status.
  *
- * B <= DSPARK_MAX_BATCH.  The gamma steps are sequential; each enqueues at
- * most two kernels.
+ * B <= DSPARK_MAX_BATCH.  The gamma steps are sequential.  With a bf16
+ * backbone, r a multiple of 64 (64..256), at most 64 requests and a
+ * vocabulary the device's SMs hold in eight 128-token tiles each, all steps
+ * run in one persistent launch that keeps the biased logits on chip;
+ * otherwise each step enqueues at most two kernels (the bias GEMM, then the
+ * policy and draw).  dspark_markov_launches() says which.
  */
 int dspark_markov_sample(const void* backbone, int dtype, const int32_t* anchor,
                          const uint16_t* U, const uint16_t* W, int r,
@@ -193,6 +197,12 @@ int dspark_markov_sample(const void* backbone, int dtype, const int32_t* anchor,
                          int32_t* proposals, float* q, float* q_at_x,
                          float* conf, int32_t* status, void* workspace,
                          size_t workspace_bytes, void* stream);
+
+/* Kernels one dspark_markov_sample call with these sizes enqueues on the
+ * current device (the confidence kernel included when with_conf is nonzero),
+ * or -1 when the sizes are invalid.  The path depends on the device's SM
+ * count, so this asks the CUDA runtime for the current device's properties. */
+int dspark_markov_launches(int dtype, int B, int gamma, int V, int r, int with_policy, int with_conf);
 
 /*
  * dspark_rnn_sample - the draft's sequential head in its RNN form.

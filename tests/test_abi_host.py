@@ -150,6 +150,20 @@ def test_markov_rejects_invalid_arguments(lib):
     assert _markov(lib, ws_bytes=0, r=16, U=FAKE, W=FAKE) == binding.ENOSPC
 
 
+def test_markov_launch_counts(lib):
+    f = lib.dspark_markov_launches
+    f.argtypes = [ctypes.c_int] * 7
+    f.restype = ctypes.c_int
+    assert f(0, 4, 5, 1004, 0, 1, 0) == -1        # V not a multiple of 8
+    assert f(0, 257, 5, 1024, 0, 1, 0) == -1      # above DSPARK_MAX_BATCH
+    assert f(0, 4, 5, 1024, 8, 1, 0) == -1        # rank not a multiple of 16
+    assert f(0, 0, 5, 1024, 0, 1, 1) == 0
+    assert f(0, 4, 5, 1024, 0, 0, 0) == 1         # greedy, no bias: one arg-max launch
+    assert f(0, 4, 5, 1024, 0, 0, 1) == 2         # ... and the confidence kernel
+    assert f(0, 4, 5, 1024, 0, 1, 0) == 5         # sampled, no bias: the policy step per position
+    assert f(0, 4, 5, 1024, 16, 1, 1) == 11       # r = 16 (never fused): GEMM + step per position, conf
+
+
 def test_accept_stats_rejects_invalid_arguments(lib):
     f = lib.dspark_accept_stats
     assert f(FAKE, FAKE, 0, FAKE, FAKE, None, 4, 0, 1024, *([FAKE] * 7), FAKE, 1 << 20, None) == binding.EINVAL

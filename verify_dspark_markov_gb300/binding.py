@@ -22,7 +22,7 @@ REQ_OK, REQ_NONFINITE, REQ_EMPTY, REQ_TIMEOUT, REQ_BAD_POLICY, REQ_BAD_TOKEN = r
 
 EXPORTED = ("dspark_workspace_size", "dspark_markov_sample", "dspark_verify", "dspark_verify_width",
             "dspark_accept_stats", "dspark_accept_stats_grad", "dspark_status_string", "dspark_version",
-            "dspark_verify_greedy_noalloc", "dspark_sts_fit", "dspark_rnn_sample")
+            "dspark_verify_greedy_noalloc", "dspark_sts_fit", "dspark_rnn_sample", "dspark_markov_launches")
 
 _lock = threading.Lock()
 _lib = None
@@ -72,6 +72,8 @@ def load(path: str | None = None):
             lib.dspark_sts_fit.restype = i32
             lib.dspark_status_string.argtypes = [i32]
             lib.dspark_status_string.restype = ctypes.c_char_p
+            lib.dspark_markov_launches.argtypes = [i32] * 7
+            lib.dspark_markov_launches.restype = i32
             lib.dspark_version.argtypes = []
             lib.dspark_version.restype = i32
             _lib = lib
@@ -84,6 +86,15 @@ def status_string(code: int) -> str:
 
 def workspace_size(op: int, B: int, gamma: int, V: int, r: int = 0, H: int = 0) -> int:
     return int(load().dspark_workspace_size(op, B, gamma, V, r, H))
+
+
+def markov_launches(dtype: int, B: int, gamma: int, V: int, r: int = 0, policy: bool = True,
+                    conf: bool = False) -> int:
+    """Kernels one markov_sample call with these sizes enqueues on the current device."""
+    n = int(load().dspark_markov_launches(dtype, B, gamma, V, r, int(bool(policy)), int(bool(conf))))
+    if n < 0:
+        raise ValueError("invalid sizes")
+    return n
 
 
 # ------------------------------------------------------------------ helpers

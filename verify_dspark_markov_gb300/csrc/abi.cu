@@ -324,6 +324,16 @@ int dspark_markov_sample(const void* backbone, int dtype, const int32_t* anchor,
     return DSPARK_OK;
 }
 
+int dspark_markov_launches(int dtype, int B, int gamma, int V, int r, int with_policy, int with_conf) {
+    if (!valid_common(B, gamma, V, dtype) || B > DSPARK_MAX_BATCH) return -1;
+    if (r < 0 || r > DSPARK_MAX_RANK || r % 16 != 0) return -1;
+    if (B == 0) return 0;
+    const int conf = with_conf ? 1 : 0;
+    if (r > 0 && r % 64 == 0 && markov_fused_supported(dtype, B, V, r)) return 1 + conf;
+    if (with_policy || r > 0) return gamma * (r > 0 ? 2 : 1) + conf;
+    return 1 + conf;
+}
+
 int dspark_rnn_sample(const void* backbone, int dtype, const int32_t* anchor, const uint16_t* U,
                       const uint16_t* W, int r, const uint16_t* Wi, const uint16_t* Wh, const float* bi,
                       const float* bh, const void* h, int h_dtype, const uint16_t* E, const float* w_conf,
