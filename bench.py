@@ -673,7 +673,7 @@ def run_gpu(args):
     kernel = {"full_decode_tile": "argmax_rows_kernel<bf16> (draft + verify launches)",
               "training_stats": "stats_pairs_kernel<f32> (+ stats_blocks_kernel, stats_total_kernel)",
               "training_stats_grad": "stats_grad_kernel<f32>",
-              "sts_fit": "sts_pass_kernel (+ sts_update_kernel per pass)"}.get(
+              "sts_fit": "sts_fit_kernel (every pass and update in one cooperative launch)"}.get(
                   wl.name, {"draft": draft_kernel,
                             "verify": "verify_rows_kernel<bf16>" if getattr(wl, "width", None) is None
                             else "verify_rows_kernel<bf16, width>"}.get(dom, dom))
@@ -719,8 +719,8 @@ def run_gpu(args):
             launches = 4 * g + (1 if wl.w.h is not None else 0) + 1
         else:  # the library's own count for the draft, then the verify
             launches = n_draft + 1
-    elif isinstance(wl, StsFit):  # init, then 64 passes and their updates (late passes return at once)
-        launches = 1 + 2 * 64
+    elif isinstance(wl, StsFit):  # init, the fit, the status check
+        launches = 3
     else:  # the statistics: pairs + per-block + total kernels; the gradient: one kernel
         launches = 1 if isinstance(wl, StatsGrad) else 3
     result["gpu_launches"] = launches * steps

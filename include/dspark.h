@@ -410,23 +410,26 @@ int dspark_version(void);
  *                root lies beyond 2^20: no finite fit (beta = 2^20); 3 a
  *                counted pair with a non-finite z or a label outside [0, 1]
  *                (beta = NaN); 4 the pass budget ran out with the search
- *                still open (beta = its last iterate, not the fit).  A BCE
- *                slope >= 0 at beta = 0 gives beta = 0 (status 0).
+ *                still open (beta = its last iterate, not the fit); 5 a
+ *                wait between the fit's thread blocks ran past its time
+ *                limit (about 2 s), so beta is not a fit.  A BCE slope >= 0
+ *                at beta = 0 gives beta = 0 (status 0).
  *   passes       int32 [gamma] out, or NULL: the passes over the pairs each
  *                position's search used (every pass reads all positions
  *                until the last one stops).
- *   max_passes   passes enqueued, 1..DSPARK_STS_MAX_PASSES, or 0 for 64
+ *   max_passes   the pass budget, 1..DSPARK_STS_MAX_PASSES, or 0 for 64
  *                (enough for beta to double from 1 to the 2^20 cap and then
  *                halve its bracket below 1e-7; Newton usually ends in ten
- *                or fewer).  Passes after the last position stops return at
- *                once.
+ *                or fewer).  The fit stops after the pass in which the last
+ *                position stopped.
  *   workspace    dspark_workspace_size(DSPARK_OP_STS_FIT, N, gamma, 0, 0, 0)
  *                bytes; every region is written before it is read.
  * N = 0 is valid (every position reports status 1).  The fit is a root
- * search on the device (Newton steps inside a bracket, a fixed number of
- * passes enqueued); beta is accurate to about 1e-6 relative (its sums are
- * fp32 per thread, fp64 across threads) and bit-identical across calls on
- * the same inputs (the CTAs' sums are combined in a fixed order).
+ * search on the device (Newton steps inside a bracket) in one persistent
+ * cooperative launch, with three kernels enqueued in all; beta is accurate
+ * to about 1e-6 relative (its sums are fp32 per thread, fp64 across
+ * threads) and bit-identical across calls on the same inputs and device
+ * (the CTAs' sums are combined in a fixed order).
  */
 int dspark_sts_fit(const float* conf_logits, const float* labels,
                    const uint8_t* mask, int N, int gamma, double* beta,

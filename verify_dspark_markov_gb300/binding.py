@@ -347,7 +347,7 @@ def sts_fit(conf_logits, labels, mask=None, max_passes=0, workspace: Workspace |
     """Sequential Temperature Scaling: per block position the inverse
     temperature beta >= 0 of the confidence head, from fp32 [N, gamma]
     confidence logits and accept labels (mask: uint8 [N, gamma] or None);
-    max_passes bounds the passes enqueued (0: the library's default).
+    max_passes is the pass budget (0: the library's default).
     Returns (beta float64 [gamma], status int32 [gamma], passes int32
     [gamma]: the passes each position's search used)."""
     _dev(conf_logits, "conf_logits", torch.float32)

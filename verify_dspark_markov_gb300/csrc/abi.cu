@@ -85,7 +85,8 @@ size_t stats_workspace(int N, int gamma) {
 // Sequential Temperature Scaling: the per-position search states, the count
 // of positions still searching, then the per-CTA sums of a pass.
 size_t sts_active_offset() { return align_up(static_cast<size_t>(DSPARK_MAX_GAMMA) * sizeof(StsState)); }
-size_t sts_partial_offset() { return align_up(sts_active_offset() + sizeof(int)); }
+// the active count, the barrier count and the error word share one aligned block
+size_t sts_partial_offset() { return align_up(sts_active_offset() + 3 * sizeof(int)); }
 size_t sts_workspace() {
     return align_up(sts_partial_offset() + static_cast<size_t>(kStsMaxGrid) * DSPARK_MAX_GAMMA * 2 * sizeof(double));
 }
@@ -534,6 +535,8 @@ int dspark_sts_fit(const float* conf_logits, const float* labels, const uint8_t*
     p.passes = passes;
     p.state = at<StsState>(workspace, 0);
     p.active = at<int>(workspace, sts_active_offset());
+    p.bar = at<unsigned>(workspace, sts_active_offset() + sizeof(int));
+    p.error = at<int>(workspace, sts_active_offset() + 2 * sizeof(int));
     p.partial = at<double>(workspace, sts_partial_offset());
     p.max_passes = max_passes ? max_passes : kStsDefaultPasses;
     return launch_sts_fit(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? DSPARK_OK : DSPARK_ECUDA;

@@ -245,7 +245,9 @@ struct StsParams {
     StsState* state;           // [DSPARK_MAX_GAMMA] workspace
     int* active;               // workspace: positions still searching
     double* partial;           // [kStsMaxGrid][DSPARK_MAX_GAMMA][2] workspace: per-CTA slope and curvature sums
-    int max_passes;            // passes enqueued (the search budget)
+    unsigned* bar;             // workspace: the grid barrier's arrival count
+    int* error;                // workspace: set when a barrier wait gave up
+    int max_passes;            // the pass budget
 };
 constexpr int kStsMaxGrid = 1024;   // CTAs of one pass over the pairs, at most
 constexpr int kStsDefaultPasses = 64;
