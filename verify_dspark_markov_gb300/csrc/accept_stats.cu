@@ -10,8 +10,11 @@
 // slice of both rows once from HBM, keeping an online (max, sum of exp) per
 // thread; the cluster combines the slices' statistics through distributed
 // shared memory; each CTA then re-reads its slice (a ~129 KB working set per
-// CTA, so the re-read is served by L2) to form the L1 terms.  NaN / +inf poison
-// the running sums, which is how non-finite rows are detected at no cost.
+// CTA, so the re-read is served by L2) to form the L1 terms.  The first
+// read marks its L2 lines evict_last and the last read evict_first, so that
+// the slices of the CTAs in flight (4 per SM) stay in L2 for their re-reads
+// while the stream passes through.  NaN / +inf poison the running sums,
+// which is how non-finite rows are detected at no cost.
 // Kernels 2 and 3: tau and the status per block (one thread each) with the
 // weighted sums reduced by fixed binary trees, then the CTA partials in a
 // fixed order, so repeated calls give identical bits.
@@ -24,7 +27,8 @@
 //   s_v = sign(p_d,v - p_t,v), S = sum_v s_v p_d,v,
 //   dJ/dz   = m w_k (sigmoid(z) - accept).
 // Pass 1 as in kernel 1; pass 2 sums the L1 terms and S; pass 3 re-reads the
-// slice (L2) and writes its gradient row.
+// slice (L2, its last read: evict_first) and writes its gradient row with
+// streaming stores (kept out of the way of the slices still to be re-read).
 
 #include <cooperative_groups.h>
 
@@ -39,7 +43,8 @@ namespace {
 
 constexpr int kC = 8;          // CTAs per row pair (cluster size)
 constexpr int kThreads = 256;
-constexpr int kBatch = 6;      // 16-byte vectors per row per thread in flight
+constexpr int kBatch = 5;      // 16-byte vectors per row per thread in flight (64 registers, no spills)
+constexpr int kBatchGrad = 4;  // the same in the backward (more would spill at 4 CTAs per SM)
 constexpr float kLog2e = 1.4426950408889634f;
 
 __device__ __forceinline__ float ex2(float x) {
@@ -84,7 +89,7 @@ __device__ __forceinline__ void unpack(const uint4& v, float (&x)[kDtype == kBF1
 }
 
 template <int kDtype>
-__global__ void __cluster_dims__(kC, 1, 1) __launch_bounds__(kThreads)
+__global__ void __cluster_dims__(kC, 1, 1) __launch_bounds__(kThreads, 4)
     stats_pairs_kernel(const StatsParams p) {
     constexpr int kPer = kDtype == kBF16 ? 8 : 4;
     constexpr int64_t kEsize = kDtype == kBF16 ? 2 : 4;
@@ -103,6 +108,7 @@ __global__ void __cluster_dims__(kC, 1, 1) __launch_bounds__(kThreads)
     const char* trow = static_cast<const char*>(p.target) + (pair * p.V + lo) * kEsize;
 
     // ---- pass 1: online max / sum of exp over the slice, both rows
+    const uint64_t keep = l2_policy_evict_last(), drop = l2_policy_evict_first();
     Online od, ot;
     od.init();
     ot.init();
@@ -112,8 +118,8 @@ __global__ void __cluster_dims__(kC, 1, 1) __launch_bounds__(kThreads)
         for (int u = 0; u < kBatch; ++u) {
             const int j = j0 + u * kThreads;
             if (j < nvec) {
-                vd[u] = ld_stream_v4(drow + static_cast<int64_t>(j) * 16);
-                vt[u] = ld_stream_v4(trow + static_cast<int64_t>(j) * 16);
+                vd[u] = ld_stream_v4(drow + static_cast<int64_t>(j) * 16, keep);
+                vt[u] = ld_stream_v4(trow + static_cast<int64_t>(j) * 16, keep);
             }
         }
 #pragma unroll
@@ -159,7 +165,7 @@ __global__ void __cluster_dims__(kC, 1, 1) __launch_bounds__(kThreads)
     }
     const float inv_sd = 1.0f / gd.s, inv_st = 1.0f / gt.s;
 
-    // ---- pass 2: sum of |p_d - p_t| over the slice (re-read, served by L2)
+    // ---- pass 2: sum of |p_d - p_t| over the slice (re-read, served by L2; its last read)
     float l1 = 0.0f;
     for (int j0 = tid; j0 < nvec; j0 += kBatch * kThreads) {
         uint4 vd[kBatch], vt[kBatch];
@@ -167,8 +173,8 @@ __global__ void __cluster_dims__(kC, 1, 1) __launch_bounds__(kThreads)
         for (int u = 0; u < kBatch; ++u) {
             const int j = j0 + u * kThreads;
             if (j < nvec) {
-                vd[u] = ld_stream_v4(drow + static_cast<int64_t>(j) * 16);
-                vt[u] = ld_stream_v4(trow + static_cast<int64_t>(j) * 16);
+                vd[u] = ld_stream_v4(drow + static_cast<int64_t>(j) * 16, drop);
+                vt[u] = ld_stream_v4(trow + static_cast<int64_t>(j) * 16, drop);
             }
         }
 #pragma unroll
@@ -262,21 +268,22 @@ __global__ void __cluster_dims__(kC, 1, 1) __launch_bounds__(kThreads, 4)
     }
 
     // ---- pass 1: online max / sum of exp over the slice, both rows
+    const uint64_t keep = l2_policy_evict_last(), drop = l2_policy_evict_first();
     Online od, ot;
     od.init();
     ot.init();
-    for (int j0 = tid; j0 < nvec; j0 += kBatch * kThreads) {
-        uint4 vd[kBatch], vt[kBatch];
+    for (int j0 = tid; j0 < nvec; j0 += kBatchGrad * kThreads) {
+        uint4 vd[kBatchGrad], vt[kBatchGrad];
 #pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
+        for (int u = 0; u < kBatchGrad; ++u) {
             const int j = j0 + u * kThreads;
             if (j < nvec) {
-                vd[u] = ld_stream_v4(drow + static_cast<int64_t>(j) * 16);
-                vt[u] = ld_stream_v4(trow + static_cast<int64_t>(j) * 16);
+                vd[u] = ld_stream_v4(drow + static_cast<int64_t>(j) * 16, keep);
+                vt[u] = ld_stream_v4(trow + static_cast<int64_t>(j) * 16, keep);
             }
         }
 #pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
+        for (int u = 0; u < kBatchGrad; ++u) {
             if (j0 + u * kThreads < nvec) {
                 float x[kPer];
                 unpack<kDtype>(vd[u], x);
@@ -322,18 +329,18 @@ __global__ void __cluster_dims__(kC, 1, 1) __launch_bounds__(kThreads, 4)
 
     // ---- pass 2: the L1 terms and S = sum of sign(p_d - p_t) p_d (re-read, served by L2)
     float l1 = 0.0f, sg = 0.0f;
-    for (int j0 = tid; j0 < nvec; j0 += kBatch * kThreads) {
-        uint4 vd[kBatch], vt[kBatch];
+    for (int j0 = tid; j0 < nvec; j0 += kBatchGrad * kThreads) {
+        uint4 vd[kBatchGrad], vt[kBatchGrad];
 #pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
+        for (int u = 0; u < kBatchGrad; ++u) {
             const int j = j0 + u * kThreads;
             if (j < nvec) {
-                vd[u] = ld_stream_v4(drow + static_cast<int64_t>(j) * 16);
-                vt[u] = ld_stream_v4(trow + static_cast<int64_t>(j) * 16);
+                vd[u] = ld_stream_v4(drow + static_cast<int64_t>(j) * 16, keep);
+                vt[u] = ld_stream_v4(trow + static_cast<int64_t>(j) * 16, keep);
             }
         }
 #pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
+        for (int u = 0; u < kBatchGrad; ++u) {
             if (j0 + u * kThreads < nvec) {
                 float xd[kPer], xt[kPer];
                 unpack<kDtype>(vd[u], xd);
@@ -381,18 +388,18 @@ __global__ void __cluster_dims__(kC, 1, 1) __launch_bounds__(kThreads, 4)
     const float nanf = __int_as_float(0x7FC00000);
 
     // ---- pass 3: the slice's gradient row (re-read, served by L2)
-    for (int j0 = tid; j0 < nvec; j0 += kBatch * kThreads) {
-        uint4 vd[kBatch], vt[kBatch];
+    for (int j0 = tid; j0 < nvec; j0 += kBatchGrad * kThreads) {
+        uint4 vd[kBatchGrad], vt[kBatchGrad];
 #pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
+        for (int u = 0; u < kBatchGrad; ++u) {
             const int j = j0 + u * kThreads;
             if (j < nvec) {
-                vd[u] = ld_stream_v4(drow + static_cast<int64_t>(j) * 16);
-                vt[u] = ld_stream_v4(trow + static_cast<int64_t>(j) * 16);
+                vd[u] = ld_stream_v4(drow + static_cast<int64_t>(j) * 16, drop);
+                vt[u] = ld_stream_v4(trow + static_cast<int64_t>(j) * 16, drop);
             }
         }
 #pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
+        for (int u = 0; u < kBatchGrad; ++u) {
             const int j = j0 + u * kThreads;
             if (j < nvec) {
                 float xd[kPer], xt[kPer], g[kPer];
@@ -408,8 +415,8 @@ __global__ void __cluster_dims__(kC, 1, 1) __launch_bounds__(kThreads, 4)
                     g[i] = bad ? nanf : c * (0.1f * gce + 0.9f * pd * (sv - Sf));
                 }
                 float4* g4 = reinterpret_cast<float4*>(grow + static_cast<int64_t>(j) * kPer);
-                g4[0] = make_float4(g[0], g[1], g[2], g[3]);
-                if constexpr (kPer == 8) g4[1] = make_float4(g[4], g[5], g[6], g[7]);
+                __stcs(g4, make_float4(g[0], g[1], g[2], g[3]));
+                if constexpr (kPer == 8) __stcs(g4 + 1, make_float4(g[4], g[5], g[6], g[7]));
             }
         }
     }

@@ -111,6 +111,27 @@ __device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
     return v;
 }
 
+// L2 eviction policies for loads that carry a cache hint: lines to be read
+// again soon (evict_last) and lines read for the last time (evict_first).
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+// ld_stream_v4 with an L2 eviction policy.
+__device__ __forceinline__ uint4 ld_stream_v4(const void* p, uint64_t policy) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p), "l"(policy));
+    return v;
+}
+
 // ------------------------------------------------ TMA bulk copies, mbarriers
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));

@@ -163,16 +163,6 @@ __device__ __forceinline__ void tma_load_3d_hint(void* dst, const CUtensorMap* m
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar)), "l"(policy)
         : "memory");
 }
-__device__ __forceinline__ uint64_t l2_policy_evict_last() {
-    uint64_t p;
-    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
-    return p;
-}
-__device__ __forceinline__ uint64_t l2_policy_evict_first() {
-    uint64_t p;
-    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
-    return p;
-}
 
 // 16-byte asynchronous copy global -> shared (no register staging).
 __device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc) {
