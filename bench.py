@@ -240,10 +240,11 @@ class Serving:
         w, e = self.w, self.esize
         B, g, V, r, H = w.B, w.gamma, w.V, w.weights.r, w.weights.H
         sampled = int((self.w.policy.greedy == 0).sum()) if self.pol is not None else 0
-        passes = 1 if self.gru is None else 2     # the RNN head's bias: a hi and a lo product
+        # the method reads the rank-r matrix once a step (the RNN head's two
+        # products, hi and lo, and the z between them are this library's cost)
         draft = (B * g * V * e                      # backbone rows
-                 + passes * g * (V * r * 2 + B * r * 2)  # the rank-r matrix per product, gathered rows
-                 + (0 if self.gru is None else g * (2 * 3 * r * r * 2 + B * V * 4 * 2))  # GRU weights; z_A out, in
+                 + g * (V * r * 2 + B * r * 2)      # the rank-r matrix, gathered rows / states
+                 + (0 if self.gru is None else g * 2 * 3 * r * r * 2)  # GRU weights
                  + sampled * g * V * 4              # q rows of sampled requests
                  + B * g * (H * 2 * 2 if w.h is not None else 0)  # h and E rows for c_k
                  + B * 4 + B * g * 12)              # anchors, proposals, q(x), c_k

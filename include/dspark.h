@@ -390,6 +390,29 @@ const char* dspark_status_string(int code);
 int dspark_version(void);
 
 /*
+ * dspark_wait_selftest - diagnostic of the library's bounded device waits.
+ *
+ * The persistent kernels (the fused Markov draft, the temperature-scaling
+ * fit) meet at grid barriers whose waits end after about 2 s of global time
+ * at most, so that a block that never arrives turns into a status instead of
+ * a hung GPU.  This call launches `blocks` thread blocks (1..64, all
+ * resident) that meet at one such barrier told to expect blocks + missing
+ * arrivals: with missing > 0 the wait can end only by its limit.  Nothing else
+ * is in flight meanwhile (no copy, MMA or tensor memory).
+ *   limit_us   the wait's limit, 1..2,000,000 microseconds.
+ *   status     int32 [blocks] out: DSPARK_REQ_OK when the barrier completed,
+ *              DSPARK_REQ_TIMEOUT when the block gave up waiting (a block
+ *              that sees another give up stops waiting too).
+ *   waited_ns  uint64 [blocks] out: the global time each block waited.
+ *   workspace  at least 256 bytes of device memory, 16-byte aligned (the
+ *              barrier's count and error word, set by the call).
+ * The device stays usable afterwards; any later call may follow on the
+ * stream.
+ */
+int dspark_wait_selftest(int blocks, int missing, int limit_us, int32_t* status, uint64_t* waited_ns,
+                         void* workspace, void* stream);
+
+/*
  * dspark_sts_fit - Sequential Temperature Scaling of the confidence head.
  *
  * [MB Acceptance and confidence]: the confidence head regresses to the

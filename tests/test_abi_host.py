@@ -164,6 +164,19 @@ def test_markov_launch_counts(lib):
     assert f(0, 4, 5, 1024, 16, 1, 1) == 11       # r = 16 (never fused): GEMM + step per position, conf
 
 
+def test_wait_selftest_rejects_invalid_arguments(lib):
+    f = lib.dspark_wait_selftest
+    f.argtypes = [ctypes.c_int] * 3 + [ctypes.c_void_p] * 4
+    f.restype = ctypes.c_int
+    assert f(0, 0, 1000, FAKE, FAKE, FAKE, None) == binding.EINVAL       # no blocks
+    assert f(65, 0, 1000, FAKE, FAKE, FAKE, None) == binding.EINVAL      # more than 64
+    assert f(2, -1, 1000, FAKE, FAKE, FAKE, None) == binding.EINVAL      # negative missing arrivals
+    assert f(2, 1, 0, FAKE, FAKE, FAKE, None) == binding.EINVAL          # no time limit
+    assert f(2, 1, 2_000_001, FAKE, FAKE, FAKE, None) == binding.EINVAL  # above 2 s
+    assert f(2, 1, 1000, None, FAKE, FAKE, None) == binding.EINVAL
+    assert f(2, 1, 1000, FAKE, FAKE, FAKE_ODD, None) == binding.EINVAL   # workspace not 16-byte aligned
+
+
 def test_accept_stats_rejects_invalid_arguments(lib):
     f = lib.dspark_accept_stats
     assert f(FAKE, FAKE, 0, FAKE, FAKE, None, 4, 0, 1024, *([FAKE] * 7), FAKE, 1 << 20, None) == binding.EINVAL

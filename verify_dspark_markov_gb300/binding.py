@@ -22,7 +22,8 @@ REQ_OK, REQ_NONFINITE, REQ_EMPTY, REQ_TIMEOUT, REQ_BAD_POLICY, REQ_BAD_TOKEN = r
 
 EXPORTED = ("dspark_workspace_size", "dspark_markov_sample", "dspark_verify", "dspark_verify_width",
             "dspark_accept_stats", "dspark_accept_stats_grad", "dspark_status_string", "dspark_version",
-            "dspark_verify_greedy_noalloc", "dspark_sts_fit", "dspark_rnn_sample", "dspark_markov_launches")
+            "dspark_verify_greedy_noalloc", "dspark_sts_fit", "dspark_rnn_sample", "dspark_markov_launches",
+            "dspark_wait_selftest")
 
 _lock = threading.Lock()
 _lib = None
@@ -72,6 +73,8 @@ def load(path: str | None = None):
             lib.dspark_sts_fit.restype = i32
             lib.dspark_status_string.argtypes = [i32]
             lib.dspark_status_string.restype = ctypes.c_char_p
+            lib.dspark_wait_selftest.argtypes = [i32, i32, i32, P, P, P, P]
+            lib.dspark_wait_selftest.restype = i32
             lib.dspark_markov_launches.argtypes = [i32] * 7
             lib.dspark_markov_launches.restype = i32
             lib.dspark_version.argtypes = []
@@ -86,6 +89,19 @@ def status_string(code: int) -> str:
 
 def workspace_size(op: int, B: int, gamma: int, V: int, r: int = 0, H: int = 0) -> int:
     return int(load().dspark_workspace_size(op, B, gamma, V, r, H))
+
+
+def wait_selftest(blocks: int, missing: int, limit_us: int, device=None, stream=None):
+    """Blocks meeting at the library's bounded grid barrier, told to expect
+    `missing` more arrivals than they make.  Returns (status int32 [blocks],
+    waited_ns int64 [blocks]) on the device."""
+    dev = torch.device("cuda") if device is None else torch.device(device)
+    status = torch.empty((blocks,), dtype=torch.int32, device=dev)
+    waited = torch.empty((blocks,), dtype=torch.int64, device=dev)
+    ws = torch.empty((256,), dtype=torch.uint8, device=dev)
+    _check(load().dspark_wait_selftest(blocks, missing, limit_us, _ptr(status), _ptr(waited), _ptr(ws),
+                                       _stream(stream)), "dspark_wait_selftest")
+    return status, waited
 
 
 def markov_launches(dtype: int, B: int, gamma: int, V: int, r: int = 0, policy: bool = True,

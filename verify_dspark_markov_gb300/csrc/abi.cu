@@ -325,6 +325,22 @@ int dspark_markov_sample(const void* backbone, int dtype, const int32_t* anchor,
     return DSPARK_OK;
 }
 
+int dspark_wait_selftest(int blocks, int missing, int limit_us, int32_t* status, uint64_t* waited_ns,
+                         void* workspace, void* stream) {
+    if (blocks < 1 || blocks > 64 || missing < 0 || missing > 64 || limit_us < 1 || limit_us > 2000000)
+        return DSPARK_EINVAL;
+    if (!status || !waited_ns || !workspace || !aligned16(workspace) ||
+        (reinterpret_cast<uintptr_t>(status) & 3u) || (reinterpret_cast<uintptr_t>(waited_ns) & 7u))
+        return DSPARK_EINVAL;
+    unsigned* bar = static_cast<unsigned*>(workspace);
+    int* error = reinterpret_cast<int*>(static_cast<char*>(workspace) + 8);
+    return launch_wait_selftest(blocks, missing, static_cast<uint64_t>(limit_us) * 1000u, bar, error, status,
+                                reinterpret_cast<unsigned long long*>(waited_ns),
+                                static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? DSPARK_OK
+               : DSPARK_ECUDA;
+}
+
 int dspark_markov_launches(int dtype, int B, int gamma, int V, int r, int with_policy, int with_conf) {
     if (!valid_common(B, gamma, V, dtype) || B > DSPARK_MAX_BATCH) return -1;
     if (r < 0 || r > DSPARK_MAX_RANK || r % 16 != 0) return -1;

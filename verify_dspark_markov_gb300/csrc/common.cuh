@@ -196,6 +196,35 @@ __device__ __forceinline__ uint4 ld_shared_v4(const void* p) {
 // microseconds); the affected requests then report DSPARK_REQ_TIMEOUT.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
+// Grid barrier of a persistent launch whose CTAs are all resident (a
+// cooperative launch): thread 0 of each CTA adds one arrival to *bar and
+// waits until it reaches `target` (gen * gridDim.x for the gen-th barrier).
+// The wait ends after limit_ns of global time, or as soon as another CTA has
+// given up (*error set): it then sets *error and returns false in every
+// thread of the CTA.  No copy, MMA or other wait of the caller may be in
+// flight across the call.
+__device__ __forceinline__ bool grid_barrier_bounded(unsigned* bar, int* error, unsigned target, uint64_t limit_ns,
+                                                     int* s_ok) {
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int ok = 1;
+        __threadfence();
+        atomicAdd(bar, 1u);
+        const uint64_t t0 = globaltimer_ns();
+        while (ld_relaxed_u32(bar) < target) {
+            if (*reinterpret_cast<volatile int*>(error) || globaltimer_ns() - t0 > limit_ns) {
+                atomicExch(error, 1);
+                ok = 0;
+                break;
+            }
+        }
+        __threadfence();
+        *s_ok = ok;
+    }
+    __syncthreads();
+    return *s_ok != 0;
+}
+
 // ----------------------------------------------------------- reductions
 __device__ __forceinline__ uint64_t warp_max_u64(uint64_t v) {
 #pragma unroll

@@ -271,4 +271,9 @@ struct GruParams {
 };
 cudaError_t launch_gru_step(const GruParams& p, cudaStream_t stream);
 
+// Diagnostic of the bounded grid barrier (selftest.cu): `blocks` blocks wait
+// for blocks + missing arrivals, at most limit_ns each.
+cudaError_t launch_wait_selftest(int blocks, int missing, uint64_t limit_ns, unsigned* bar, int* error,
+                                 int32_t* status, unsigned long long* waited_ns, cudaStream_t stream);
+
 }  // namespace dspark

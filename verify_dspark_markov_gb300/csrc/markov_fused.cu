@@ -8,7 +8,9 @@
 //   q_k = policy(z_k) (temperature, top-k, top-p), written in full;
 //   x_k = inverse-CDF draw from q_k in token order (greedy: the argmax).
 //
-// Layout.  Requests go in groups of up to 64 (the MMA's N); the vocabulary
+// Layout.  Requests go in groups of up to 64 (the MMA's N; the library
+// launches the kernel for one group, since groups run one after another and
+// the per-step path beats that for larger batches); the vocabulary
 // goes to the CTAs in contiguous ranges of 128-row tiles (the MMA's M), so a
 // CTA's tokens precede the next CTA's in token order.  Tile j of a CTA lives
 // in tensor-memory columns [64 j, 64 j + 64): lane = vocabulary row of the
@@ -150,7 +152,7 @@ struct FusedSmem {
     uint64_t accfull[kMaxLT];
     uint32_t tmem_base;
     int abort;
-    unsigned int bar_gen;
+    int barrier_ok;
     int any_prefix;
     int any_refine;
     int32_t x[kNG];
@@ -193,26 +195,9 @@ __device__ __forceinline__ void red_add_u64(unsigned long long* p, unsigned long
 // Grid barrier: arrivals counted on bar[0] for the whole launch (generation
 // g waits for g * nctas arrivals); bounded, and a wait that gives up (or an
 // error set elsewhere) makes the CTA abort.
-__device__ void grid_sync(const FusedParams& p, FusedSmem& sm) {
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        const unsigned gen = ++sm.bar_gen;
-        const unsigned target = gen * static_cast<unsigned>(gridDim.x);
-        __threadfence();
-        atomicAdd(p.bar, 1u);
-        const uint64_t t0 = globaltimer_ns();
-        for (;;) {
-            if (ld_relaxed_u32(p.bar) >= target) break;
-            if (*reinterpret_cast<volatile int*>(p.error)) { sm.abort = 1; break; }
-            if (globaltimer_ns() - t0 > kWaitLimitNs) {
-                atomicExch(p.error, 1);
-                sm.abort = 1;
-                break;
-            }
-        }
-        __threadfence();
-    }
-    __syncthreads();
+// gen: this thread's count of the barriers passed (the same in every thread)
+__device__ void grid_sync(const FusedParams& p, FusedSmem& sm, unsigned& gen) {
+    if (!grid_barrier_bounded(p.bar, p.error, ++gen * gridDim.x, kWaitLimitNs, &sm.barrier_ok)) sm.abort = 1;
 }
 
 // Bins of s = (zmax - z) / T in half units, bf = s / 2, taken as one fma
@@ -368,13 +353,13 @@ __global__ void __launch_bounds__(kFT, 1)
         }
         for (int j = 0; j < kMaxLT; ++j) mbar_init(&sm.accfull[j], 1);
         sm.abort = 0;
-        sm.bar_gen = 0;
         fence_mbar_init();
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = sm.tmem_base;
+    unsigned bar_gen = 0;  // grid barriers passed
     // policy phases: warp w reads TMEM lane quadrant w % 4 and the 16 columns
     // [16 (w / 4), 16 (w / 4) + 16)
     const int q = warp & 3, cq = (warp >> 2) * 16;
@@ -562,7 +547,7 @@ __global__ void __launch_bounds__(kFT, 1)
             if (m) red_max_u32(&sw.maxkey[tid], m);
             if (bd) red_or_u32(&sw.bad[tid], 1u);
         }
-        grid_sync(p, sm);  // ---------------------------------------- barrier 1
+        grid_sync(p, sm, bar_gen);  // ---------------------------------------- barrier 1
 
         // ------------------------------------------------ B: greedy argmax, histograms
         if (tid < kNG) {
@@ -686,7 +671,7 @@ __global__ void __launch_bounds__(kFT, 1)
                 if (sm.hist[c] == kHistMass) red_add_u64(&sw.hmass[0][0] + i, (&hmass[0][0])[i]);
             }
         }
-        grid_sync(p, sm);  // ---------------------------------------- barrier 2
+        grid_sync(p, sm, bar_gen);  // ---------------------------------------- barrier 2
 
         // ------------------------------------------------ C: windows (every CTA)
         for (int i = tid; i < kNG * kHB; i += kFT) {  // the histograms, all loads in flight at once
@@ -766,7 +751,7 @@ __global__ void __launch_bounds__(kFT, 1)
                     red_add_u64(&sw.hmass2[0][0] + i, (&hmass[0][0])[i]);
                 }
             }
-            grid_sync(p, sm);  // ------------------------------------ barrier 2b
+            grid_sync(p, sm, bar_gen);  // ------------------------------------ barrier 2b
             for (int i = tid; i < kNG * kHB; i += kFT) {
                 const int c = i / kHB;
                 if (sm.win[c].mode != kModeRefine) continue;
@@ -873,7 +858,7 @@ __global__ void __launch_bounds__(kFT, 1)
                 }
             }
         }
-        grid_sync(p, sm);  // ---------------------------------------- barrier 3
+        grid_sync(p, sm, bar_gen);  // ---------------------------------------- barrier 3
 
         // ------------------------------------------------ E: owners (cuts, draws, hard rows)
         // on the row engine's threads (the first kEng); the others wait at the barrier
@@ -1024,7 +1009,7 @@ __global__ void __launch_bounds__(kFT, 1)
             }
             RP_SYNC();
         }
-        grid_sync(p, sm);  // ---------------------------------------- barrier 4
+        grid_sync(p, sm, bar_gen);  // ---------------------------------------- barrier 4
 
         // ------------------------------------------------ F: q, support mass of this range
         if (tid < kNG) {
@@ -1107,7 +1092,7 @@ __global__ void __launch_bounds__(kFT, 1)
             if (tid < nb && (sm.d[tid].flags & kDescPrefix))
                 p.part[static_cast<size_t>(tid) * gridDim.x + blockIdx.x] =
                     sm.wpart[0][tid] + sm.wpart[1][tid] + sm.wpart[2][tid] + sm.wpart[3][tid];
-            grid_sync(p, sm);  // ------------------------------------ barrier 5
+            grid_sync(p, sm, bar_gen);  // ------------------------------------ barrier 5
             // ------------------------------------------------ G: the CTA holding the draw finds it
             for (int c = 0; c < nb; ++c) {
                 if (!(sm.d[c].flags & kDescPrefix) || sm.abort) continue;
@@ -1177,7 +1162,7 @@ __global__ void __launch_bounds__(kFT, 1)
                 }
                 __syncthreads();
             }
-            grid_sync(p, sm);  // ------------------------------------ barrier 6
+            grid_sync(p, sm, bar_gen);  // ------------------------------------ barrier 6
         }
     }
 

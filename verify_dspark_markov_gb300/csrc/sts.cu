@@ -79,30 +79,6 @@ __device__ __forceinline__ StsState load_state(const StsState* p) {
     return s;
 }
 
-// Grid barrier number `gen` (1, 2, ...): false when this CTA gave up waiting
-// (or saw another CTA give up); the caller then leaves the kernel.
-__device__ bool sts_barrier(unsigned* bar, int* error, unsigned gen, int* s_ok) {
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        const unsigned target = gen * gridDim.x;
-        int ok = 1;
-        __threadfence();
-        atomicAdd(bar, 1u);
-        const uint64_t t0 = globaltimer_ns();
-        while (ld_relaxed_u32(bar) < target) {
-            if (*reinterpret_cast<volatile int*>(error) || globaltimer_ns() - t0 > kWaitLimitNs) {
-                atomicExch(error, 1);
-                ok = 0;
-                break;
-            }
-        }
-        __threadfence();
-        *s_ok = ok;
-    }
-    __syncthreads();
-    return *s_ok != 0;
-}
-
 // One pair's terms at inverse temperature b into the position's sums and flags.
 __device__ __forceinline__ void add_pair(float zv, float av, float b, float& g1, float& g2, unsigned& inf,
                                          unsigned& viol, unsigned& bad, unsigned bit) {
@@ -213,7 +189,7 @@ __global__ void __launch_bounds__(kStsThreads) sts_fit_kernel(const StsParams p,
                                (((s_flag[2] >> tid) & 1u) ? kInvalid : 0u);
             if (f) atomicOr(&p.state[tid].flags, f);
         }
-        if (!sts_barrier(p.bar, p.error, ++gen, &s_ok)) return;
+        if (!grid_barrier_bounded(p.bar, p.error, ++gen * gridDim.x, kWaitLimitNs, &s_ok)) return;
 
         if (blockIdx.x == 0) {
             // the pass's sums per position, in a fixed order: lane l adds
@@ -255,7 +231,7 @@ __global__ void __launch_bounds__(kStsThreads) sts_fit_kernel(const StsParams p,
                 if (k == 0 && fin) atomicSub(p.active, __popc(fin));
             }
         }
-        if (!sts_barrier(p.bar, p.error, ++gen, &s_ok)) return;
+        if (!grid_barrier_bounded(p.bar, p.error, ++gen * gridDim.x, kWaitLimitNs, &s_ok)) return;
     }
 }
 
