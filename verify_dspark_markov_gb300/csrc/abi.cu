@@ -60,14 +60,14 @@ MarkovLayout markov_layout(int B, int gamma, int V, int r) {
 // the hi product, z after the lo product), then the fp32 state, its bf16 hi
 // and lo rows and the gather index.
 struct RnnLayout {
-    size_t error_flag, zbuf, state, hi, lo, index, total;
+    size_t error_flag, zbuf, state, hi, lo, index, total;  // state: two [B, r] buffers (steps alternate)
 };
 RnnLayout rnn_layout(int B, int V, int r) {
     RnnLayout l;
     l.error_flag = 0;
     l.zbuf = align_up(sizeof(int));
     l.state = align_up(l.zbuf + 2 * static_cast<size_t>(B) * V * sizeof(float));
-    l.hi = align_up(l.state + static_cast<size_t>(B) * r * sizeof(float));
+    l.hi = align_up(l.state + 2 * static_cast<size_t>(B) * r * sizeof(float));
     l.lo = align_up(l.hi + static_cast<size_t>(B) * r * sizeof(uint16_t));
     l.index = align_up(l.lo + static_cast<size_t>(B) * r * sizeof(uint16_t));
     l.total = align_up(l.index + static_cast<size_t>(B) * sizeof(int32_t));
@@ -389,7 +389,8 @@ int dspark_rnn_sample(const void* backbone, int dtype, const int32_t* anchor, co
     gru.gamma = gamma;
     gru.V = V;
     gru.r = r;
-    gru.state = at<float>(workspace, lay.state);
+    float* state0 = at<float>(workspace, lay.state);
+    float* state1 = state0 + static_cast<size_t>(B) * r;
     gru.hi = at<uint16_t>(workspace, lay.hi);
     gru.lo = at<uint16_t>(workspace, lay.lo);
     gru.index = at<int32_t>(workspace, lay.index);
@@ -440,6 +441,8 @@ int dspark_rnn_sample(const void* backbone, int dtype, const int32_t* anchor, co
     const size_t esz = dtype == DSPARK_BF16 ? 2 : 4;
     for (int k = 1; k <= gamma; ++k) {
         gru.k = k;
+        gru.state_in = (k & 1) ? state1 : state0;   // s_{k-1}
+        gru.state_out = (k & 1) ? state0 : state1;  // s_k
         if (launch_gru_step(gru, s) != cudaSuccess) return DSPARK_ECUDA;
         // step k's backbone rows, read as the first rows of a [B, gamma, V] array
         g1.backbone = static_cast<const char*>(backbone) + static_cast<size_t>(k - 1) * V * esz;

@@ -264,7 +264,8 @@ struct GruParams {
     const int32_t* anchor;      // [B]
     const int32_t* proposals;   // [B, gamma]
     int B, gamma, V, r, k;      // k: 1-based step
-    float* state;               // [B, r] fp32 workspace: s_{k-1} in, s_k out
+    const float* state_in;      // [B, r] fp32 workspace: s_{k-1} (unread at k = 1)
+    float* state_out;           // [B, r] fp32 workspace: s_k (another buffer than state_in)
     uint16_t* hi;               // [B, r] bf16(s_k)
     uint16_t* lo;               // [B, r] bf16(s_k - hi)
     int32_t* index;             // [B]: b, or -1 when x_{k-1} is not a token (a failed request)
