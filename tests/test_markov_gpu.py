@@ -75,12 +75,16 @@ def test_markov_tiny_rank16(ds, oracle, greedy):
 
 
 @pytest.mark.parametrize("B,V,r", [(5, 4096, 256), (16, 4096, 64), (33, 2056, 128), (160, 2056, 256),
-                                   (200, 1032, 48), (129, 1000, 16)])
+                                   (200, 1032, 48), (129, 1000, 16), (1, 50000, 192), (48, 50000, 64),
+                                   (8, 150000, 128)])
 def test_markov_ragged_batches(ds, oracle, B, V, r):
     """Batches that do not fill the 128-request M tile (padding rows) or need
     two of them (B > 128), vocabularies that are not a multiple of the
     vocabulary tile, and ranks that are not a multiple of 64 (the W tiles then
-    arrive without swizzle)."""
+    arrive without swizzle).  Up to 64 requests with r a multiple of 64 run
+    the fused draft: V = 50,000 gives each CTA three vocabulary tiles and a
+    ragged last tile, V = 150,000 eight tiles (all of tensor memory) and a
+    ragged last tile."""
     w = synth.decode_verify_tile(V=V, B=B, r=r, H=32)
     ref, got = _both(ds, oracle, w)
     _check(ref, got)
