@@ -11,8 +11,7 @@
 //
 // gru_step_kernel: one CTA per 8 requests and 8 state units (one per warp).
 // The CTA stages e and s_{k-1} of its requests in shared memory (fp32); a
-// warp takes one unit at a time, its lanes splitting the K dimension 8
-// elements each, so that each of the unit's six weight rows (Wi and Wh at j,
+// warp takes one unit, its lanes splitting the K dimension 8 elements each, so that each of the unit's six weight rows (Wi and Wh at j,
 // r + j, 2r + j) is one coalesced 512-byte read of the warp; the lanes' partial
 // dot products for the 8 requests are summed by a butterfly, and lane m
 // applies the gates for request m.  s_{k-1} is read from one state buffer and
@@ -37,13 +36,13 @@ __device__ __forceinline__ float sigmoidf_(float a) { return 1.0f / (1.0f + expf
 __global__ void __launch_bounds__(kGruThreads) gru_step_kernel(const GruParams p) {
     __shared__ __align__(16) float s_e[kGruReq][256];
     __shared__ __align__(16) float s_s[kGruReq][256];
+    __shared__ int32_t s_x[kGruReq];
     const int r = p.r, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int b0 = blockIdx.x * kGruReq;
     const int nreq = min(kGruReq, p.B - b0);
 
     // the CTA's tokens x_{k-1} first, then e = U[x_{k-1}] and s_{k-1} (all r
     // units) of its requests, every thread's loads independent of each other
-    __shared__ int32_t s_x[kGruReq];
     if (tid < kGruReq) {
         int32_t x = -1;
         if (tid < nreq) {

@@ -27,7 +27,7 @@
 //    the last pass of the budget reports status 4 with its last iterate.
 //  * barrier; the next pass starts unless every position has stopped.
 // A barrier wait that runs past its limit sets an error word and ends the
-// CTA; a one-thread kernel after the fit then reports status 5 at every
+// CTA; a one-warp kernel after the fit then reports status 5 at every
 // position.  HBM-bound: 9 bytes a pair a pass (8 without a mask).
 
 #include <algorithm>
