@@ -689,8 +689,15 @@ def run_gpu(args):
         n_draft = ds.markov_launches(ds.BF16, w.B, w.gamma, w.V, w.weights.r, policy=not wl.greedy_only,
                                      conf=w.h is not None)
         fused = w.weights.r > 0 and n_draft == 1 + (1 if w.h is not None else 0)
+    rnn_fused = False
+    if isinstance(wl, Serving) and wl.gru is not None:
+        w = wl.w
+        rnn_fused = ds.rnn_launches(ds.BF16, w.B, w.gamma, w.V, w.weights.r, conf=w.h is not None) == \
+            1 + (1 if w.h is not None else 0)
     draft_kernel = ("markov_fused_kernel (bias GEMM, policy and draw of every position in one launch) + "
                     "confidence_kernel" if fused else
+                    "markov_fused_kernel, RNN head (GRU cell, bias GEMM, policy and draw of every position in one "
+                    "launch) + confidence_kernel" if rnn_fused else
                     "rnn_sample (gru_step_kernel, the hi and lo markov_bias_kernel products and "
                     "markov_step_kernel per position)" if isinstance(wl, Serving) and wl.gru is not None else
                     "markov_sample (markov_bias_kernel + markov_step_kernel per position)")
@@ -743,8 +750,8 @@ def run_gpu(args):
         g = wl.w.gamma
         if wl.name == "full_decode_tile":
             launches = 2
-        elif wl.gru is not None:  # GRU step, the hi and lo products, the policy step; confidence; verify
-            launches = 4 * g + (1 if wl.w.h is not None else 0) + 1
+        elif wl.gru is not None:  # the library's own count for the RNN draft, then the verify
+            launches = ds.rnn_launches(ds.BF16, wl.w.B, g, wl.w.V, wl.w.weights.r, conf=wl.w.h is not None) + 1
         else:  # the library's own count for the draft, then the verify
             launches = n_draft + 1
     elif isinstance(wl, StsFit):  # init, the fit, the status check

@@ -204,6 +204,9 @@ int dspark_markov_sample(const void* backbone, int dtype, const int32_t* anchor,
  * count, so this asks the CUDA runtime for the current device's properties. */
 int dspark_markov_launches(int dtype, int B, int gamma, int V, int r, int with_policy, int with_conf);
 
+/* The same for dspark_rnn_sample (r >= 16). */
+int dspark_rnn_launches(int dtype, int B, int gamma, int V, int r, int with_conf);
+
 /*
  * dspark_rnn_sample - the draft's sequential head in its RNN form.
  *
@@ -227,7 +230,11 @@ int dspark_markov_launches(int dtype, int B, int gamma, int V, int r, int with_p
  *   workspace  dspark_workspace_size(DSPARK_OP_RNN_SAMPLE, B, gamma, V, r, 0).
  * The bias reaches the logits through the tensor cores in bf16: s_k is passed
  * as hi = bf16(s_k) plus lo = bf16(s_k - hi), two products summed in fp32, so
- * the logits carry s_k to about 2^-16 of its size.
+ * the logits carry s_k to about 2^-16 of its size.  Under the same conditions
+ * as dspark_markov_sample's one-launch path (bf16 backbone, r a multiple of
+ * 64, at most 64 requests) the whole draft, GRU cell included, runs in one
+ * persistent launch; otherwise each step enqueues four kernels.
+ * dspark_rnn_launches() says which.
  */
 int dspark_rnn_sample(const void* backbone, int dtype, const int32_t* anchor,
                       const uint16_t* U, const uint16_t* W, int r,

@@ -164,6 +164,17 @@ def test_markov_launch_counts(lib):
     assert f(0, 4, 5, 1024, 16, 1, 1) == 11       # r = 16 (never fused): GEMM + step per position, conf
 
 
+def test_rnn_launch_counts(lib):
+    f = lib.dspark_rnn_launches
+    f.argtypes = [ctypes.c_int] * 6
+    f.restype = ctypes.c_int
+    assert f(0, 4, 5, 1024, 8, 0) == -1           # rank below 16
+    assert f(0, 2000, 5, 1024, 16, 0) == -1       # more requests than tokens (and above the maximum)
+    assert f(0, 0, 5, 1024, 16, 1) == 0
+    assert f(0, 4, 5, 1024, 16, 0) == 20          # r = 16 (never fused): four kernels a step
+    assert f(0, 4, 5, 1024, 16, 1) == 21
+
+
 def test_wait_selftest_rejects_invalid_arguments(lib):
     f = lib.dspark_wait_selftest
     f.argtypes = [ctypes.c_int] * 3 + [ctypes.c_void_p] * 4

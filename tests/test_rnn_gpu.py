@@ -73,8 +73,13 @@ def _check(ref, got, max_indet_frac=0.05):
     return indet
 
 
-@pytest.mark.parametrize("V,B,r,H", [(4096, 16, 64, 64), (2056, 33, 128, 0), (4096, 200, 256, 0)])
+@pytest.mark.parametrize("V,B,r,H", [(4096, 16, 64, 64), (2056, 33, 128, 0), (4096, 200, 256, 0),
+                                     (1032, 12, 48, 0), (50000, 40, 192, 0), (4096, 20, 256, 32)])
 def test_rnn_sampled(ds, oracle, V, B, r, H):
+    """Up to 64 requests with r a multiple of 64 run the whole draft in one
+    launch (GRU cell included); 200 requests, or r = 48, take the per-step
+    kernels.  V = 50,000 gives the one-launch path three vocabulary tiles per
+    CTA and a ragged last tile; r = 256 takes a single W stage."""
     w, gw = _case(V, B, r, H, seed=2001 + B)
     _check(*_both(ds, oracle, w, gw))
 

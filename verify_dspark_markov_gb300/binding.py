@@ -23,7 +23,7 @@ REQ_OK, REQ_NONFINITE, REQ_EMPTY, REQ_TIMEOUT, REQ_BAD_POLICY, REQ_BAD_TOKEN = r
 EXPORTED = ("dspark_workspace_size", "dspark_markov_sample", "dspark_verify", "dspark_verify_width",
             "dspark_accept_stats", "dspark_accept_stats_grad", "dspark_status_string", "dspark_version",
             "dspark_verify_greedy_noalloc", "dspark_sts_fit", "dspark_rnn_sample", "dspark_markov_launches",
-            "dspark_wait_selftest")
+            "dspark_wait_selftest", "dspark_rnn_launches")
 
 _lock = threading.Lock()
 _lib = None
@@ -75,6 +75,8 @@ def load(path: str | None = None):
             lib.dspark_status_string.restype = ctypes.c_char_p
             lib.dspark_wait_selftest.argtypes = [i32, i32, i32, P, P, P, P]
             lib.dspark_wait_selftest.restype = i32
+            lib.dspark_rnn_launches.argtypes = [i32] * 6
+            lib.dspark_rnn_launches.restype = i32
             lib.dspark_markov_launches.argtypes = [i32] * 7
             lib.dspark_markov_launches.restype = i32
             lib.dspark_version.argtypes = []
@@ -102,6 +104,14 @@ def wait_selftest(blocks: int, missing: int, limit_us: int, device=None, stream=
     _check(load().dspark_wait_selftest(blocks, missing, limit_us, _ptr(status), _ptr(waited), _ptr(ws),
                                        _stream(stream)), "dspark_wait_selftest")
     return status, waited
+
+
+def rnn_launches(dtype: int, B: int, gamma: int, V: int, r: int, conf: bool = False) -> int:
+    """Kernels one rnn_sample call with these sizes enqueues on the current device."""
+    n = int(load().dspark_rnn_launches(dtype, B, gamma, V, r, int(bool(conf))))
+    if n < 0:
+        raise ValueError("invalid sizes")
+    return n
 
 
 def markov_launches(dtype: int, B: int, gamma: int, V: int, r: int = 0, policy: bool = True,

@@ -132,7 +132,13 @@ size_t dspark_workspace_size(int op, int B, int gamma, int V, int r, int H) {
                                                                            : size_t(0));
         case DSPARK_OP_VERIFY: return verify_layout(B, gamma).total;
         case DSPARK_OP_ACCEPT_STATS: return stats_workspace(B, gamma);
-        case DSPARK_OP_RNN_SAMPLE: return r >= 16 ? rnn_layout(B, V, r).total : 0;
+        case DSPARK_OP_RNN_SAMPLE:
+            // the larger of the two paths' needs (which one runs depends on the device)
+            return r >= 16 ? std::max(rnn_layout(B, V, r).total,
+                                      r >= 64 && r % 64 == 0 && B <= kFusedMaxBatch
+                                          ? markov_fused_workspace(B, gamma, V, r, true)
+                                          : size_t(0))
+                           : 0;
         default: return 0;
     }
 }
@@ -325,6 +331,15 @@ int dspark_markov_sample(const void* backbone, int dtype, const int32_t* anchor,
     return DSPARK_OK;
 }
 
+int dspark_rnn_launches(int dtype, int B, int gamma, int V, int r, int with_conf) {
+    if (!valid_common(B, gamma, V, dtype) || B > DSPARK_MAX_BATCH || B > V) return -1;
+    if (r < 16 || r > DSPARK_MAX_RANK || r % 16 != 0) return -1;
+    if (B == 0) return 0;
+    const int conf = with_conf ? 1 : 0;
+    if (r % 64 == 0 && markov_fused_supported(dtype, B, V, r, true)) return 1 + conf;
+    return 4 * gamma + conf;  // per step: the GRU cell, the hi and lo products, the policy step
+}
+
 int dspark_wait_selftest(int blocks, int missing, int limit_us, int32_t* status, uint64_t* waited_ns,
                          void* workspace, void* stream) {
     if (blocks < 1 || blocks > 64 || missing < 0 || missing > 64 || limit_us < 1 || limit_us > 2000000)
@@ -369,10 +384,44 @@ int dspark_rnn_sample(const void* backbone, int dtype, const int32_t* anchor, co
     if (h && (H <= 0 || !E || !w_conf || !conf || (h_dtype != DSPARK_BF16 && h_dtype != DSPARK_F32)))
         return DSPARK_EINVAL;
     if (policy && (!q || !seed || !request_id || !pos0 || !aligned16(q))) return DSPARK_EINVAL;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+    if (r % 64 == 0 && markov_fused_supported(dtype, B, V, r, true)) {
+        // the whole draft in one persistent launch: the GRU cell, the bias
+        // and the policy of every step, z kept in tensor memory
+        if (!workspace || workspace_bytes < markov_fused_workspace(B, gamma, V, r, true)) return DSPARK_ENOSPC;
+        MarkovFusedArgs a{};
+        a.backbone = static_cast<const uint16_t*>(backbone);
+        a.U = U;
+        a.W = W;
+        a.anchor = anchor;
+        a.policy = policy;
+        a.seed = seed;
+        a.request_id = request_id;
+        a.pos0 = pos0;
+        a.B = B;
+        a.gamma = gamma;
+        a.V = V;
+        a.r = r;
+        a.proposals = proposals;
+        a.q = q;
+        a.q_at_x = q_at_x;
+        a.status = status;
+        a.Wi = Wi;
+        a.Wh = Wh;
+        a.bi = bi;
+        a.bh = bh;
+        if (launch_markov_fused(a, workspace, workspace_bytes, s) != cudaSuccess) return DSPARK_ECUDA;
+        if (h) {
+            ConfParams c{h, h_dtype, E, w_conf, H, B, gamma, V, anchor, proposals, 1, gamma, conf};
+            if (launch_confidence(c, s) != cudaSuccess) return DSPARK_ECUDA;
+        }
+        return DSPARK_OK;
+    }
+
     const RnnLayout lay = rnn_layout(B, V, r);
     if (workspace_bytes < lay.total || !workspace) return DSPARK_ENOSPC;
     if (!policy_vocab_ok(V)) return DSPARK_ENOTSUP;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
     int* error_flag = at<int>(workspace, lay.error_flag);
     float* zA = at<float>(workspace, lay.zbuf);
     float* zB = zA + static_cast<size_t>(B) * V;

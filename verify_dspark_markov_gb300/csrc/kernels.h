@@ -158,11 +158,18 @@ struct MarkovFusedArgs {
     float* q;
     float* q_at_x;
     int32_t* status;
+    // the RNN head instead of the Markov head (all four set, or all null):
+    // the GRU cell's weights; the bias is then W s_k with s_k the GRU state
+    const uint16_t* Wi = nullptr;  // bf16 [3r, r], gate order r, z, n
+    const uint16_t* Wh = nullptr;  // bf16 [3r, r]
+    const float* bi = nullptr;     // [3r]
+    const float* bh = nullptr;     // [3r]
 };
-bool markov_fused_supported(int dtype, int B, int V, int r);
+// rnn: the RNN head's form (one shared-memory operand more, one W stage fewer)
+bool markov_fused_supported(int dtype, int B, int V, int r, bool rnn = false);
 // Workspace bytes from the start of the Markov workspace (its first 256 bytes
-// belong to the per-step path's error word).
-size_t markov_fused_workspace(int B, int gamma, int V);
+// belong to the per-step path's error word); rnn adds the GRU state buffers.
+size_t markov_fused_workspace(int B, int gamma, int V, int r = 0, bool rnn = false);
 cudaError_t launch_markov_fused(const MarkovFusedArgs& a, void* ws, size_t ws_bytes, cudaStream_t stream);
 
 // Elements of a row each CTA of the verify / drafting step owns.

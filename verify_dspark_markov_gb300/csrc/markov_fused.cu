@@ -136,7 +136,7 @@ struct FusedParams {
     float* q_at_x;
     int32_t* status;
     // layout
-    int ntiles, tpc, grid, groups, stages;
+    int ntiles, tpc, grid, groups, stages, bstages;
     // workspace
     unsigned int* bar;         // barrier arrivals (cleared before the launch)
     int* error;                // set when a wait gave up
@@ -145,6 +145,14 @@ struct FusedParams {
     Desc* desc;                // [kNG]
     unsigned long long* part;  // [kNG][grid] support mass of each CTA's range
     float* zhard;              // [kNG][V] z of hard rows
+    // the RNN head (rnn = 1): the GRU cell's weights and its state s_k,
+    // fp32 [2][kNG][r] (step k writes buffer k & 1)
+    int rnn;
+    const uint16_t* Wi;
+    const uint16_t* Wh;
+    const float* bi;
+    const float* bh;
+    float* state;
 };
 
 struct FusedSmem {
@@ -320,7 +328,99 @@ __device__ __forceinline__ bool in_window(const Win& w, int b1, int b2) {
     return b1 >= w.wlo && b1 <= w.whi && (b1 <= w.phi || b1 == w.whi);
 }
 
+// RNN head, phase A0 of step k: the GRU cell s_k = GRU(s_{k-1}, U[x_{k-1}])
+// (gate order r, z, n; s_0 = 0) for the group's nb requests.  Work items
+// (state unit u, 4 requests) go to every warp of the grid; a warp's lanes
+// split K eight elements each, so each of the unit's six weight rows (Wi and
+// Wh at u, r + u, 2r + u) is one coalesced read; the lanes' partial dot
+// products are summed by a butterfly and lane m applies the gates for
+// request m0 + m.  s_{k-1} is read through L2 (other CTAs wrote it); s_k goes
+// to the other state buffer, which the gather reads after a grid barrier.
+__device__ __forceinline__ void gru_phase(const FusedParams& p, const int32_t* xsm, int k, int g, int nb, int warp,
+                                          int lane) {
+    const int r = p.r;
+    const float* sprev = p.state + static_cast<size_t>((k - 1) & 1) * kNG * r;
+    float* scur = p.state + static_cast<size_t>(k & 1) * kNG * r;
+    constexpr int kM = 4;  // requests per work item
+    const int items = ((nb + kM - 1) / kM) * r;
+    const int k0 = lane * 8;  // this lane's 8 elements of K
+    for (int it = blockIdx.x * (kFT / 32) + warp; it < items; it += gridDim.x * (kFT / 32)) {
+        const int u = it % r, m0 = (it / r) * kM;
+        const float bir = p.bi[u], biz = p.bi[r + u], bin = p.bi[2 * r + u];
+        const float bhr = p.bh[u], bhz = p.bh[r + u], bhn = p.bh[2 * r + u];
+        // lane m's s_{k-1} at unit u, for the gate update (loaded with the rest)
+        const float sp = (k > 1 && lane < kM && m0 + lane < nb) ? __ldcg(sprev + (m0 + lane) * r + u) : 0.0f;
+        float acc[6][kM];
+#pragma unroll
+        for (int q6 = 0; q6 < 6; ++q6)
+#pragma unroll
+            for (int m = 0; m < kM; ++m) acc[q6][m] = 0.0f;
+        if (k0 < r) {
+            // every load of the item first (tokens, then embedding and state
+            // rows, then weights), so that they overlap
+            int32_t xs[kM];  // x_{k-1} of the item's requests (-1: none or invalid)
+#pragma unroll
+            for (int m = 0; m < kM; ++m) xs[m] = m0 + m < nb ? xsm[m0 + m] : -1;
+            uint4 ev[kM];
+            float4 s0[kM], s1[kM];
+#pragma unroll
+            for (int m = 0; m < kM; ++m) {
+                const int c = m0 + m;
+                ev[m] = xs[m] >= 0 ? __ldg(reinterpret_cast<const uint4*>(p.U + static_cast<int64_t>(xs[m]) * r + k0))
+                                   : make_uint4(0u, 0u, 0u, 0u);
+                const bool has_s = k > 1 && c < nb;
+                s0[m] = has_s ? __ldcg(reinterpret_cast<const float4*>(sprev + c * r + k0)) : make_float4(0.f, 0.f, 0.f, 0.f);
+                s1[m] = has_s ? __ldcg(reinterpret_cast<const float4*>(sprev + c * r + k0 + 4))
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+            uint4 wv[6];
+#pragma unroll
+            for (int q6 = 0; q6 < 6; ++q6)
+                wv[q6] = __ldg(reinterpret_cast<const uint4*>((q6 < 3 ? p.Wi : p.Wh) +
+                                                              static_cast<int64_t>((q6 % 3) * r + u) * r + k0));
+#pragma unroll
+            for (int q6 = 0; q6 < 6; ++q6) {
+                const float wf[8] = {bf16_lo(wv[q6].x), bf16_hi(wv[q6].x), bf16_lo(wv[q6].y), bf16_hi(wv[q6].y),
+                                     bf16_lo(wv[q6].z), bf16_hi(wv[q6].z), bf16_lo(wv[q6].w), bf16_hi(wv[q6].w)};
+#pragma unroll
+                for (int m = 0; m < kM; ++m) {
+                    float v[8];
+                    if (q6 < 3) {
+                        v[0] = bf16_lo(ev[m].x); v[1] = bf16_hi(ev[m].x); v[2] = bf16_lo(ev[m].y); v[3] = bf16_hi(ev[m].y);
+                        v[4] = bf16_lo(ev[m].z); v[5] = bf16_hi(ev[m].z); v[6] = bf16_lo(ev[m].w); v[7] = bf16_hi(ev[m].w);
+                    } else {
+                        v[0] = s0[m].x; v[1] = s0[m].y; v[2] = s0[m].z; v[3] = s0[m].w;
+                        v[4] = s1[m].x; v[5] = s1[m].y; v[6] = s1[m].z; v[7] = s1[m].w;
+                    }
+                    float t = acc[q6][m];
+#pragma unroll
+                    for (int l = 0; l < 8; ++l) t = fmaf(wf[l], v[l], t);
+                    acc[q6][m] = t;
+                }
+            }
+        }
+#pragma unroll
+        for (int q6 = 0; q6 < 6; ++q6)
+#pragma unroll
+            for (int m = 0; m < kM; ++m)
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) acc[q6][m] += __shfl_xor_sync(0xFFFFFFFFu, acc[q6][m], o);
+#pragma unroll
+        for (int m = 0; m < kM; ++m) {
+            const int c = m0 + m;
+            if (lane != m || c >= nb) continue;
+            const float rg = 1.0f / (1.0f + expf(-((acc[0][m] + bir) + (acc[3][m] + bhr))));
+            const float zg = 1.0f / (1.0f + expf(-((acc[1][m] + biz) + (acc[4][m] + bhz))));
+            const float n = tanhf((acc[2][m] + bin) + rg * (acc[5][m] + bhn));
+            scur[c * r + u] = (1.0f - zg) * n + zg * sp;
+        }
+    }
+}
+
 // ------------------------------------------------------------------ kernel
+// kRnn: the RNN head (p.rnn set), a kernel of its own so that the Markov
+// head's registers are not shared with the GRU phase
+template <bool kRnn>
 __global__ void __launch_bounds__(kFT, 1)
     markov_fused_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap bmap,
                         const FusedParams p) {
@@ -329,12 +429,13 @@ __global__ void __launch_bounds__(kFT, 1)
     __shared__ rp::Smem rsm;
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int r = p.r, S = p.stages, V = p.V;
+    const int r = p.r, S = p.stages, SB = p.bstages, V = p.V;  // W and backbone stages
     const uint32_t w_bytes = static_cast<uint32_t>(kTileV * r * 2);  // one W stage
     const uint32_t b_bytes = static_cast<uint32_t>(kNG * kTileV * 2);  // one backbone stage
     uint8_t* sW = smem;
     uint8_t* sB = sW + S * w_bytes;
-    uint8_t* sU = sB + S * b_bytes;  // also the owner's candidate buffer (and the row engine's scratch)
+    uint8_t* sU = sB + SB * b_bytes;  // also the owner's candidate buffer (and the row engine's scratch)
+    uint8_t* sU2 = sU + kNG * r * 2;  // RNN head: the state's lo rows (sU holds its hi rows)
     unsigned long long* cbuf = reinterpret_cast<unsigned long long*>(sU);
     // the histograms of phases B and C live there too (the step's MMAs have read U by then)
     unsigned long long (*hmass)[kHB] = reinterpret_cast<unsigned long long (*)[kHB]>(sU);
@@ -381,7 +482,7 @@ __global__ void __launch_bounds__(kFT, 1)
             tma_load_2d_hint(dst + kb * kTileV * 128, &wmap, kb * 64, t * kTileV, &sm.wfull[s], pol_keep);
     };
     auto issue_b = [&](int n) {
-        const int s = n % S;
+        const int s = n % SB;
         const int gs = step_of(n), g = gs / p.gamma, k = gs % p.gamma;  // k 0-based
         mbar_arrive_expect_tx(&sm.bfull[s], b_bytes);
         const int t = t0 + tile_of(n);
@@ -391,13 +492,29 @@ __global__ void __launch_bounds__(kFT, 1)
     if (tid == 0)
         for (; w_issued < min(S, total_tiles); ++w_issued) issue_w(w_issued);
     if (tid == 32)
-        for (; b_issued < min(S, total_tiles); ++b_issued) issue_b(b_issued);
+        for (; b_issued < min(SB, total_tiles); ++b_issued) issue_b(b_issued);
 
     for (int gs = 0; gs < steps_total; ++gs) {
         const int g = gs / p.gamma, k = gs % p.gamma + 1;  // k 1-based
         const int nb = min(kNG, p.B - g * kNG);           // requests of the group
         StepWords& sw = p.words[gs];
         const bool aborted = sm.abort != 0;
+
+        // ------------------------------------------------ A0 (RNN head): the GRU cell
+        if constexpr (kRnn) {
+            if (tid < kNG) {
+                int32_t x = -1;
+                if (tid < nb) {
+                    const int b = g * kNG + tid;
+                    x = k == 1 ? p.anchor[b] : __ldcg(p.proposals + static_cast<int64_t>(b) * p.gamma + (k - 2));
+                    if (x < 0 || x >= V) x = -1;
+                }
+                sm.x[tid] = x;
+            }
+            __syncthreads();
+            if (!sm.abort) gru_phase(p, sm.x, k, g, nb, warp, lane);
+            grid_sync(p, sm, bar_gen);  // ---------------------------------- barrier 0
+        }
 
         // ------------------------------------------------ A: gather, GEMM, epilogue
         if (tid < kNG) {
@@ -414,14 +531,45 @@ __global__ void __launch_bounds__(kFT, 1)
         __syncthreads();
         {
             const int kchunks = r / 8;
-            for (int c = tid; c < kNG * kchunks; c += kFT) {
-                const int row = c / kchunks, kc = c % kchunks;
-                const int32_t x = sm.x[row];
-                uint8_t* d = sU + chunk_off<true>(row, kc, kNG);
-                if (x >= 0) cp_async16(d, p.U + static_cast<int64_t>(x) * r + kc * 8);
-                else *reinterpret_cast<uint4*>(d) = make_uint4(0u, 0u, 0u, 0u);
+            if constexpr (!kRnn) {
+                for (int c = tid; c < kNG * kchunks; c += kFT) {
+                    const int row = c / kchunks, kc = c % kchunks;
+                    const int32_t x = sm.x[row];
+                    uint8_t* d = sU + chunk_off<true>(row, kc, kNG);
+                    if (x >= 0) cp_async16(d, p.U + static_cast<int64_t>(x) * r + kc * 8);
+                    else *reinterpret_cast<uint4*>(d) = make_uint4(0u, 0u, 0u, 0u);
+                }
+                cp_async_wait_all();
+            } else {
+                // the state s_k as two bf16 operands, hi = bf16(s) and lo =
+                // bf16(s - hi) (s to about 2^-16): the bias is hi W^T + lo W^T
+                const float* sk = p.state + static_cast<size_t>(k & 1) * kNG * r;
+                for (int c = tid; c < kNG * kchunks; c += kFT) {
+                    const int row = c / kchunks, kc = c % kchunks;
+                    uint4 hv = make_uint4(0u, 0u, 0u, 0u), lv = make_uint4(0u, 0u, 0u, 0u);
+                    if (sm.x[row] >= 0) {
+                        const float4 a0 = __ldcg(reinterpret_cast<const float4*>(sk + row * r + kc * 8));
+                        const float4 a1 = __ldcg(reinterpret_cast<const float4*>(sk + row * r + kc * 8 + 4));
+                        const float v[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+                        uint32_t hw[4], lw[4];
+#pragma unroll
+                        for (int l = 0; l < 4; ++l) {
+                            const __nv_bfloat16 h0 = __float2bfloat16_rn(v[2 * l]), h1 = __float2bfloat16_rn(v[2 * l + 1]);
+                            const __nv_bfloat16 l0 = __float2bfloat16_rn(v[2 * l] - __bfloat162float(h0));
+                            const __nv_bfloat16 l1 = __float2bfloat16_rn(v[2 * l + 1] - __bfloat162float(h1));
+                            hw[l] = static_cast<uint32_t>(__bfloat16_as_ushort(h0)) |
+                                    (static_cast<uint32_t>(__bfloat16_as_ushort(h1)) << 16);
+                            lw[l] = static_cast<uint32_t>(__bfloat16_as_ushort(l0)) |
+                                    (static_cast<uint32_t>(__bfloat16_as_ushort(l1)) << 16);
+                        }
+                        hv = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                        lv = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                    }
+                    const uint32_t off = chunk_off<true>(row, kc, kNG);
+                    *reinterpret_cast<uint4*>(sU + off) = hv;
+                    *reinterpret_cast<uint4*>(sU2 + off) = lv;
+                }
             }
-            cp_async_wait_all();
             fence_proxy_async_smem();
         }
         tc_fence_before();
@@ -432,7 +580,7 @@ __global__ void __launch_bounds__(kFT, 1)
         if (warp == 0) {
             if (lane == 0 && !aborted) {
                 const uint32_t idesc = instr_desc(128, kNG);
-                const uint32_t ubase = smem_u32(sU), wbase = smem_u32(sW);
+                const uint32_t ubase = smem_u32(sU), ubase2 = smem_u32(sU2), wbase = smem_u32(sW);
                 for (int j = 0; j < ntl; ++j) {
                     const int n = gs * ntl + j, s = n % S;
                     if (!mbar_wait(&sm.wfull[s], (n / S) & 1, kWaitLimitNs)) {
@@ -445,6 +593,10 @@ __global__ void __launch_bounds__(kFT, 1)
                     for (int ks = 0; ks < r / 16; ++ks)
                         mma_bf16(d, op_desc<true>(wbase + s * w_bytes, ks, kTileV), op_desc<true>(ubase, ks, kNG), idesc,
                                  ks > 0 ? 1u : 0u);
+                    if constexpr (kRnn)  // the lo product into the same accumulator
+                        for (int ks = 0; ks < r / 16; ++ks)
+                            mma_bf16(d, op_desc<true>(wbase + s * w_bytes, ks, kTileV), op_desc<true>(ubase2, ks, kNG),
+                                     idesc, 1u);
                     mma_commit(&sm.wempty[s]);
                     mma_commit(&sm.accfull[j]);
                     ++mma_done;
@@ -468,9 +620,9 @@ __global__ void __launch_bounds__(kFT, 1)
                 for (int j = 0; j < ntl; ++j) {
                     const int n = gs * ntl + j;
                     bool ok = true;
-                    while (b_issued < total_tiles && b_issued <= n + S - 1) {
-                        const int m = b_issued - S;
-                        if (m >= 0 && !mbar_wait(&sm.bempty[m % S], (m / S) & 1, kWaitLimitNs)) {
+                    while (b_issued < total_tiles && b_issued <= n + SB - 1) {
+                        const int m = b_issued - SB;
+                        if (m >= 0 && !mbar_wait(&sm.bempty[m % SB], (m / SB) & 1, kWaitLimitNs)) {
                             atomicExch(p.error, 1);
                             sm.abort = 1;
                             ok = false;
@@ -488,8 +640,8 @@ __global__ void __launch_bounds__(kFT, 1)
             const uint32_t te = tmem + (static_cast<uint32_t>(eq * 32) << 16) + static_cast<uint32_t>(eh * 32);
             const float ninf = -__int_as_float(0x7F800000);
             for (int j = 0; j < ntl && !aborted; ++j) {
-                const int n = gs * ntl + j, s = n % S;
-                if (!mbar_wait(&sm.accfull[j], par, kWaitLimitNs) || !mbar_wait(&sm.bfull[s], (n / S) & 1, kWaitLimitNs)) {
+                const int n = gs * ntl + j, s = n % SB;  // the backbone stage
+                if (!mbar_wait(&sm.accfull[j], par, kWaitLimitNs) || !mbar_wait(&sm.bfull[s], (n / SB) & 1, kWaitLimitNs)) {
                     atomicExch(p.error, 1);
                     sm.abort = 1;
                     break;
@@ -1174,7 +1326,7 @@ __global__ void __launch_bounds__(kFT, 1)
         if (mma_done > 0) mbar_wait(&sm.wempty[(mma_done - 1) % S], ((mma_done - 1) / S) & 1, kWaitLimitNs);
     }
     if (tid == 32 && sm.abort)
-        for (int n = max(0, b_issued - S); n < b_issued; ++n) mbar_wait(&sm.bfull[n % S], (n / S) & 1, kWaitLimitNs);
+        for (int n = max(0, b_issued - SB); n < b_issued; ++n) mbar_wait(&sm.bfull[n % SB], (n / SB) & 1, kWaitLimitNs);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -1201,10 +1353,10 @@ int sm_count() {
 }
 
 struct FusedShape {
-    int ntiles, tpc, grid, groups, stages, smem;
+    int ntiles, tpc, grid, groups, stages, bstages, smem;  // stages: W tiles in flight; bstages: backbone tiles
 };
 
-bool fused_shape(int B, int V, int r, FusedShape& f) {
+bool fused_shape(int B, int V, int r, bool rnn, FusedShape& f) {
     const int sms = sm_count();
     if (sms <= 0 || B < 1 || r < 64 || r > 256 || r % 64 != 0 || V < kTileV) return false;
     f.ntiles = (V + kTileV - 1) / kTileV;
@@ -1212,22 +1364,33 @@ bool fused_shape(int B, int V, int r, FusedShape& f) {
     if (f.tpc > kMaxLT) return false;
     f.grid = (f.ntiles + f.tpc - 1) / f.tpc;
     f.groups = (B + kNG - 1) / kNG;
-    const int w = kTileV * r * 2, b = kNG * kTileV * 2, u = std::max(kNG * r * 2, kEngineScratch);
+    // B operands: the gathered U rows, or (RNN head) the state's bf16 hi and lo rows
+    const int ops = rnn ? 2 : 1;
+    const int w = kTileV * r * 2, b = kNG * kTileV * 2, u = std::max(ops * kNG * r * 2, kEngineScratch);
     const int budget = kSmemLimit - kStaticAllowance - 1024;
-    f.stages = std::min(4, (budget - u) / (w + b));
-    if (f.stages < 2) return false;
+    if (!rnn) {
+        f.stages = f.bstages = std::min(4, (budget - u) / (w + b));
+        if (f.stages < 2) return false;
+    } else {
+        // the RNN head may take a single W stage (at r = 256 two do not fit
+        // beside its second operand; phase A's cadence is set by its epilogue,
+        // which overlaps the next tile's W load), keeping two backbone stages
+        f.bstages = 2;
+        f.stages = std::min(4, (budget - u - f.bstages * b) / w);
+        if (f.stages < 1) return false;
+    }
     // at least half the SM's shared memory, so that no two CTAs (each taking
     // all of tensor memory) share an SM
-    f.smem = std::max(f.stages * (w + b) + u + 1024, 120 * 1024);
+    f.smem = std::max(f.stages * w + f.bstages * b + u + 1024, 120 * 1024);
     return true;
 }
 
 struct FusedLayout {
-    size_t bar, words, clear_end, desc, cand, part, zhard, total;
+    size_t bar, words, clear_end, desc, cand, part, zhard, state, total;
 };
 // Offsets from `base` (past the slower path's error word, which must stay
 // zero between calls); the words up to clear_end are cleared per call.
-FusedLayout fused_layout(int B, int gamma, int V) {
+FusedLayout fused_layout(int B, int gamma, int V, int r_state) {
     auto up = [](size_t x) { return (x + 255) / 256 * 256; };
     FusedLayout l;
     const int groups = (B + kNG - 1) / kNG, rows = std::min(B, kNG);
@@ -1238,23 +1401,29 @@ FusedLayout fused_layout(int B, int gamma, int V) {
     l.cand = up(l.desc + kNG * sizeof(Desc));
     l.part = up(l.cand + static_cast<size_t>(kNG) * kCand * 8);
     l.zhard = up(l.part + static_cast<size_t>(kNG) * 1024 * 8);
-    l.total = up(l.zhard + static_cast<size_t>(rows) * V * 4);
+    l.state = up(l.zhard + static_cast<size_t>(rows) * V * 4);
+    l.total = up(l.state + 2 * static_cast<size_t>(kNG) * r_state * 4);  // the GRU state, two buffers
     return l;
 }
 
 }  // namespace
 
-bool markov_fused_supported(int dtype, int B, int V, int r) {
+bool markov_fused_supported(int dtype, int B, int V, int r, bool rnn) {
     FusedShape f;
-    return dtype == kBF16 && B <= kFusedMaxBatch && fused_shape(B, V, r, f) && f.grid <= 1024;
+    return dtype == kBF16 && B <= kFusedMaxBatch && fused_shape(B, V, r, rnn, f) && f.grid <= 1024;
 }
 
-size_t markov_fused_workspace(int B, int gamma, int V) { return fused_layout(B, gamma, V).total; }
+size_t markov_fused_workspace(int B, int gamma, int V, int r, bool rnn) {
+    return fused_layout(B, gamma, V, rnn ? r : 0).total;
+}
 
 cudaError_t launch_markov_fused(const MarkovFusedArgs& a, void* ws, size_t ws_bytes, cudaStream_t stream) {
+    const bool rnn = a.Wi != nullptr;
+    if (rnn && (!a.Wh || !a.bi || !a.bh)) return cudaErrorInvalidValue;
     FusedShape f;
-    if (!fused_shape(a.B, a.V, a.r, f)) return cudaErrorInvalidValue;
-    const FusedLayout lay = fused_layout(a.B, a.gamma, a.V);
+    if (!fused_shape(a.B, a.V, a.r, rnn, f)) return cudaErrorInvalidValue;
+    if (rnn && f.groups != 1) return cudaErrorInvalidValue;  // the state buffers hold one group
+    const FusedLayout lay = fused_layout(a.B, a.gamma, a.V, rnn ? a.r : 0);
     if (ws_bytes < lay.total) return cudaErrorInvalidValue;
     char* base = static_cast<char*>(ws);
     FusedParams p{};
@@ -1278,6 +1447,7 @@ cudaError_t launch_markov_fused(const MarkovFusedArgs& a, void* ws, size_t ws_by
     p.grid = f.grid;
     p.groups = f.groups;
     p.stages = f.stages;
+    p.bstages = f.bstages;
     p.bar = reinterpret_cast<unsigned int*>(base + lay.bar);
     p.error = reinterpret_cast<int*>(base + lay.bar + 8);
     p.words = reinterpret_cast<StepWords*>(base + lay.words);
@@ -1285,6 +1455,12 @@ cudaError_t launch_markov_fused(const MarkovFusedArgs& a, void* ws, size_t ws_by
     p.cand = reinterpret_cast<unsigned long long*>(base + lay.cand);
     p.part = reinterpret_cast<unsigned long long*>(base + lay.part);
     p.zhard = reinterpret_cast<float*>(base + lay.zhard);
+    p.rnn = rnn ? 1 : 0;
+    p.Wi = a.Wi;
+    p.Wh = a.Wh;
+    p.bi = a.bi;
+    p.bh = a.bh;
+    p.state = rnn ? reinterpret_cast<float*>(base + lay.state) : nullptr;
 
     PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
     if (!enc) return cudaErrorNotSupported;
@@ -1311,7 +1487,8 @@ cudaError_t launch_markov_fused(const MarkovFusedArgs& a, void* ws, size_t ws_by
     }
     cudaError_t e = cudaMemsetAsync(base + lay.bar, 0, lay.clear_end - lay.bar, stream);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(markov_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, f.smem);
+    auto kernel = rnn ? markov_fused_kernel<true> : markov_fused_kernel<false>;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, f.smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(f.grid));
@@ -1323,7 +1500,7 @@ cudaError_t launch_markov_fused(const MarkovFusedArgs& a, void* ws, size_t ws_by
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, markov_fused_kernel, wmap, bmap, p);
+    e = cudaLaunchKernelEx(&cfg, kernel, wmap, bmap, p);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
