@@ -47,6 +47,14 @@
 // Every sum that decides a token is an integer (fixed-point weights,
 // 2^-40), so decisions do not depend on the order of the reductions.
 //
+// The RNN head (the kernel's second instantiation) differs in two places:
+//   A0 before A: the GRU cell s_k = GRU(s_{k-1}, U[x_{k-1}]) for the group's
+//      requests, spread over every warp of the grid, into a state buffer in
+//      the workspace.                                             | barrier
+//   A: the B operand is s_k as two bf16 rows, hi = bf16(s) and lo =
+//      bf16(s - hi), and every tile takes two MMAs into one accumulator,
+//      z = backbone + hi W^T + lo W^T (s_k to about 2^-16 of its size).
+//
 // Waits are bounded (kWaitLimitNs); a wait that gives up sets the call's
 // error word, every CTA then skips the remaining work, and the requests
 // report DSPARK_REQ_TIMEOUT.
