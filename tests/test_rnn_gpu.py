@@ -101,3 +101,18 @@ def test_rnn_bad_anchor(ds, oracle):
     ref, got = _both(ds, oracle, w, gw)
     assert ref["status"][3] == 5
     _check(ref, got)
+
+
+def test_rnn_nonfinite_rows(ds, oracle):
+    """Rows the one-launch path must flag (8 requests, r = 64): NaN at step 1,
+    +inf at step 3, every logit -inf at step 2 (no maximum) - each in its own
+    request; the others draft on."""
+    w, gw = _case(4096, 8, 64, 0, seed=2005)
+    bb = w.backbone.float()
+    bb[1, 0, 17] = float("nan")
+    bb[2, 2, 5] = float("inf")
+    bb[3, 1, :] = float("-inf")
+    w.backbone = bb.to(w.backbone.dtype).contiguous()
+    ref, got = _both(ds, oracle, w, gw)
+    assert ref["status"].tolist()[1:4] == [1, 1, 2], ref["status"]
+    _check(ref, got, max_indet_frac=0.25)

@@ -131,3 +131,37 @@ def test_sts_pass_budget_exhausted(ds, oracle):
     beta, status, passes = ds.sts_fit(zd, ad)
     torch.cuda.synchronize()
     _check(ref, beta.cpu().numpy(), status.cpu().numpy())
+
+
+def test_sts_ragged_rows_and_misaligned_inputs(ds, oracle):
+    """Row counts that leave one to three rows after the four-row chunks the
+    kernel reads as vectors, and inputs that start off a 16-byte boundary
+    (read a row at a time): the same fit as the oracle's."""
+    rng = np.random.default_rng(17)
+    for N, G in ((10_007, 7), (50_001, 3), (3, 5)):
+        z = rng.normal(0, 2.0, (N, G)).astype(np.float32)
+        a = (rng.random((N, G)) < 1.0 / (1.0 + np.exp(-z / 1.3))).astype(np.float32)
+        mask = (rng.random((N, G)) < 0.8).astype(np.uint8)
+        if N == 3:  # three rows cannot pin a fit down: soft labels keep it finite
+            a = (1.0 / (1.0 + np.exp(-z / 1.3))).astype(np.float32)
+            mask[:] = 1
+        _check(*_both(ds, oracle, z, a, mask))
+    # views one element into larger buffers: 4-byte aligned, not 16
+    N, G = 40_000, 4
+    z = rng.normal(0, 2.0, (N, G)).astype(np.float32)
+    a = (1.0 / (1.0 + np.exp(-z.astype(np.float64) / np.array([0.5, 1.0, 2.0, 4.0])))).astype(np.float32)
+    mask = (rng.random((N, G)) < 0.9).astype(np.uint8)
+    ref = oracle.sts_fit(z, a, mask)
+    dev = torch.device("cuda")
+    zb = torch.zeros(N * G + 1, dtype=torch.float32, device=dev)
+    ab = torch.zeros(N * G + 1, dtype=torch.float32, device=dev)
+    mb = torch.zeros(N * G + 1, dtype=torch.uint8, device=dev)
+    zb[1:] = torch.from_numpy(z.reshape(-1)).to(dev)
+    ab[1:] = torch.from_numpy(a.reshape(-1)).to(dev)
+    mb[1:] = torch.from_numpy(mask.reshape(-1)).to(dev)
+    zv, av, mv = zb[1:].view(N, G), ab[1:].view(N, G), mb[1:].view(N, G)
+    assert zv.data_ptr() % 16 != 0 and mv.data_ptr() % 4 != 0
+    beta, status, passes = ds.sts_fit(zv, av, mv)
+    torch.cuda.synchronize()
+    _check(ref, beta.cpu().numpy(), status.cpu().numpy())
+    np.testing.assert_allclose(beta.cpu().numpy(), [2.0, 1.0, 0.5, 0.25], rtol=1e-3)
