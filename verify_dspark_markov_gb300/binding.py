@@ -100,9 +100,11 @@ def wait_selftest(blocks: int, missing: int, limit_us: int, device=None, stream=
     dev = torch.device("cuda") if device is None else torch.device(device)
     status = torch.empty((blocks,), dtype=torch.int32, device=dev)
     waited = torch.empty((blocks,), dtype=torch.int64, device=dev)
-    ws = torch.empty((256,), dtype=torch.uint8, device=dev)
+    ws = torch.empty((256,), dtype=torch.uint8, device=dev)  # set by the call itself
     _check(load().dspark_wait_selftest(blocks, missing, limit_us, _ptr(status), _ptr(waited), _ptr(ws),
                                        _stream(stream)), "dspark_wait_selftest")
+    if stream is not None:  # the buffer is in use on that stream until the kernels finish
+        ws.record_stream(stream)
     return status, waited
 
 
