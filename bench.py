@@ -742,10 +742,11 @@ def run_gpu(args):
     }
     if flops.get("draft"):
         t = flops["draft"] / (part_ms["draft"] * 1e-3) / 1e12
-        result["tensor"] = {"part": "draft (markov_fused_kernel, tcgen05)" if fused else
+        result["tensor"] = {"part": "draft (markov_fused_kernel, tcgen05)" if fused or rnn_fused else
                             "draft (markov_bias_kernel, tcgen05)", "achieved": t,
                             "peak": tflops_peak, "unit": "TFLOP/s", "frac": t / tflops_peak,
-                            "note": "FLOPs of the bias GEMM over the whole draft part's time"}
+                            "note": "FLOPs of the bias GEMM (the RNN head: its hi and lo products) over the "
+                                    "whole draft part's time"}
     if isinstance(wl, Serving):
         g = wl.w.gamma
         if wl.name == "full_decode_tile":
