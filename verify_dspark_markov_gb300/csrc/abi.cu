@@ -39,6 +39,42 @@ VerifyLayout verify_layout(int B, int gamma) {
 // Largest vocabulary the row engine holds in one cluster's shared memory.
 bool policy_vocab_ok(int V) { return policy_smem_bytes(V, 0) <= 200 * 1024; }
 
+// The one-launch draft's arguments (the Markov head; the RNN head adds its
+// GRU weights) and its launch followed by the confidence kernel.
+MarkovFusedArgs fused_args(const void* backbone, const uint16_t* U, const uint16_t* W, const int32_t* anchor,
+                           const dspark_policy* policy, const uint64_t* seed, const uint64_t* request_id,
+                           const int64_t* pos0, int B, int gamma, int V, int r, int32_t* proposals, float* q,
+                           float* q_at_x, int32_t* status) {
+    MarkovFusedArgs a{};
+    a.backbone = static_cast<const uint16_t*>(backbone);
+    a.U = U;
+    a.W = W;
+    a.anchor = anchor;
+    a.policy = policy;
+    a.seed = seed;
+    a.request_id = request_id;
+    a.pos0 = pos0;
+    a.B = B;
+    a.gamma = gamma;
+    a.V = V;
+    a.r = r;
+    a.proposals = proposals;
+    a.q = q;
+    a.q_at_x = q_at_x;
+    a.status = status;
+    return a;
+}
+
+int fused_draft(const MarkovFusedArgs& a, const void* h, int h_dtype, const uint16_t* E, const float* w_conf, int H,
+                float* conf, void* workspace, size_t workspace_bytes, cudaStream_t s) {
+    if (launch_markov_fused(a, workspace, workspace_bytes, s) != cudaSuccess) return DSPARK_ECUDA;
+    if (h) {
+        ConfParams c{h, h_dtype, E, w_conf, H, a.B, a.gamma, a.V, a.anchor, a.proposals, 1, a.gamma, conf};
+        if (launch_confidence(c, s) != cudaSuccess) return DSPARK_ECUDA;
+    }
+    return DSPARK_OK;
+}
+
 struct MarkovLayout {
     size_t error_flag, zbuf, total;
 };
@@ -227,29 +263,9 @@ int dspark_markov_sample(const void* backbone, int dtype, const int32_t* anchor,
     if (r > 0 && r % 64 == 0 && markov_fused_supported(dtype, B, V, r)) {
         // the whole draft in one persistent launch, z kept in tensor memory
         if (!workspace || workspace_bytes < markov_fused_workspace(B, gamma, V)) return DSPARK_ENOSPC;
-        MarkovFusedArgs a{};
-        a.backbone = static_cast<const uint16_t*>(backbone);
-        a.U = U;
-        a.W = W;
-        a.anchor = anchor;
-        a.policy = policy;
-        a.seed = seed;
-        a.request_id = request_id;
-        a.pos0 = pos0;
-        a.B = B;
-        a.gamma = gamma;
-        a.V = V;
-        a.r = r;
-        a.proposals = proposals;
-        a.q = q;
-        a.q_at_x = q_at_x;
-        a.status = status;
-        if (launch_markov_fused(a, workspace, workspace_bytes, s) != cudaSuccess) return DSPARK_ECUDA;
-        if (h) {
-            ConfParams c{h, h_dtype, E, w_conf, H, B, gamma, V, anchor, proposals, 1, gamma, conf};
-            if (launch_confidence(c, s) != cudaSuccess) return DSPARK_ECUDA;
-        }
-        return DSPARK_OK;
+        const MarkovFusedArgs a = fused_args(backbone, U, W, anchor, policy, seed, request_id, pos0, B, gamma, V, r,
+                                             proposals, q, q_at_x, status);
+        return fused_draft(a, h, h_dtype, E, w_conf, H, conf, workspace, workspace_bytes, s);
     }
 
     if (policy || r > 0) {  // the row engine, one launch per step (after the bias GEMM when r > 0)
@@ -390,33 +406,13 @@ int dspark_rnn_sample(const void* backbone, int dtype, const int32_t* anchor, co
         // the whole draft in one persistent launch: the GRU cell, the bias
         // and the policy of every step, z kept in tensor memory
         if (!workspace || workspace_bytes < markov_fused_workspace(B, gamma, V, r, true)) return DSPARK_ENOSPC;
-        MarkovFusedArgs a{};
-        a.backbone = static_cast<const uint16_t*>(backbone);
-        a.U = U;
-        a.W = W;
-        a.anchor = anchor;
-        a.policy = policy;
-        a.seed = seed;
-        a.request_id = request_id;
-        a.pos0 = pos0;
-        a.B = B;
-        a.gamma = gamma;
-        a.V = V;
-        a.r = r;
-        a.proposals = proposals;
-        a.q = q;
-        a.q_at_x = q_at_x;
-        a.status = status;
+        MarkovFusedArgs a = fused_args(backbone, U, W, anchor, policy, seed, request_id, pos0, B, gamma, V, r,
+                                       proposals, q, q_at_x, status);
         a.Wi = Wi;
         a.Wh = Wh;
         a.bi = bi;
         a.bh = bh;
-        if (launch_markov_fused(a, workspace, workspace_bytes, s) != cudaSuccess) return DSPARK_ECUDA;
-        if (h) {
-            ConfParams c{h, h_dtype, E, w_conf, H, B, gamma, V, anchor, proposals, 1, gamma, conf};
-            if (launch_confidence(c, s) != cudaSuccess) return DSPARK_ECUDA;
-        }
-        return DSPARK_OK;
+        return fused_draft(a, h, h_dtype, E, w_conf, H, conf, workspace, workspace_bytes, s);
     }
 
     const RnnLayout lay = rnn_layout(B, V, r);
