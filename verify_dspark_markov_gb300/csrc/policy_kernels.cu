@@ -46,8 +46,10 @@ __device__ __forceinline__ float inv_mass(uint64_t mass) {
 template <bool kWidth>
 using VerifyArgs = std::conditional_t<kWidth, VerifyWidthParams, VerifyProbParams>;
 
+// Six CTAs per SM (40 registers, a few spilled): more rows in flight hides
+// more of the passes' latency (measured against four and five CTAs per SM).
 template <int kDtype, bool kWidth>
-__global__ void __cluster_dims__(kVerifyC, 1, 1) __launch_bounds__(rp::kThreads, 4)
+__global__ void __cluster_dims__(kVerifyC, 1, 1) __launch_bounds__(rp::kThreads, 6)
     verify_rows_kernel(const VerifyArgs<kWidth> p) {
     extern __shared__ __align__(16) unsigned char dyn[];
     __shared__ rp::Smem sm;
